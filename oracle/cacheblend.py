@@ -1,0 +1,467 @@
+"""Plain, slow, fp64 CPU oracle of non-prefix KV-cache fusion for RAG prefill.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and ``bench.py``'s CPU-baseline leg, never by the CUDA product path.  It shares
+no code with the CUDA path (no kernels, headers, tables or helpers); the two
+meet only at the seeded inputs of ``workload.py``.
+
+Everything here is float64 numpy.  Library primitives used as single steps:
+``@`` (matmul), ``np.exp``, ``np.cos``/``np.sin``, ``np.argsort``/``sorted``.
+No blocking, fusion or reordering beyond the definitions cited per function.
+
+Sources ("pages"):
+* QCFuse: Query-Aware Cache Fusion via Compressed View for Efficient RAG
+  Serving (arxiv 2606.05875) -- Tables 1-2, Eqs. 1-7 and 8-20.
+* CacheBlend: Reusing KV Caches When Your Text Isn't a Prefix (blog) --
+  "Quantifying the Damage", "Selective Recompute Without Skipping", "The
+  Chicken-and-Egg Problem", "Hiding Recompute Behind I/O".
+* Request Order Matters: Cache-History Sensitivity in Selective KV-Cache
+  Reuse for Rolling Agents -- §2.2 Eqs. 1-2, §2.3 Eq. 3, §4.4.
+
+Readings taken where the pages are silent (each is pinned by a test in
+``tests/test_oracle_*.py``):
+* decoder block: pre-norm Llama-style (RMSNorm, GQA attention with
+  rotate-half RoPE, SwiGLU), no biases, LM head tied to the embedding;
+* selection layer s = 1 (0-based) by default; layers < s run in full;
+* k = floor(N * r_bp / 10000), at least 1 when r_bp > 0, 0 when r_bp == 0;
+* top-k ties: larger deviation first, then lower index; output ascending;
+* deviation: squared L2 of post-RoPE keys over all kv heads (Eq. 1 of the
+  rolling-agent page); at the selection layer the fused cache follows Eq. 7;
+* uncached segments (the query, a new document) are recomputed at every
+  layer and are not counted in N.
+
+Parity unpinned: none of the functions below -- every one has a pin in
+``tests/test_oracle_pins.py`` or ``tests/test_oracle_blend.py``.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+
+__all__ = [
+    "Model", "model_from_weights", "rope_inv_freq", "rope_rotate",
+    "reposition_keys", "stitch", "rms_norm", "silu", "causal_attention",
+    "decoder_layer", "full_prefill", "chunk_prefill", "kv_deviation",
+    "select_count", "token_topk", "doc_aligned_select", "blend_prefill",
+    "first_token", "kv_bytes_per_layer", "BlendResult", "PrefillResult",
+]
+
+
+# --------------------------------------------------------------------------
+# model container
+# --------------------------------------------------------------------------
+@dataclass
+class Model:
+    n_layers: int
+    d_model: int
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    d_ffn: int
+    vocab: int
+    rope_base: float
+    norm_eps: float
+    embed: np.ndarray          # [V, d]
+    final_norm: np.ndarray     # [d]
+    layers: list               # list of dicts of float64 arrays
+
+
+def model_from_weights(shape, weights) -> Model:
+    """Wrap generator output (float32 arrays) as float64 arrays."""
+    f = lambda a: np.asarray(a, dtype=np.float64)
+    layers = [{k: f(v) for k, v in lw.items()} for lw in weights["layers"]]
+    return Model(shape.n_layers, shape.d_model, shape.n_q_heads,
+                 shape.n_kv_heads, shape.head_dim, shape.d_ffn, shape.vocab,
+                 float(shape.rope_base), float(shape.norm_eps),
+                 f(weights["embed"]), f(weights["final_norm"]), layers)
+
+
+# --------------------------------------------------------------------------
+# rotary position embedding and re-positioning
+# --------------------------------------------------------------------------
+def rope_inv_freq(head_dim: int, base: float) -> np.ndarray:
+    """theta_e = base^(-2e/hd), e = 0 .. hd/2-1 (rotary embedding of Su et
+    al., the position-encoding scheme the QCFuse page's Eq. 4 remaps)."""
+    e = np.arange(head_dim // 2, dtype=np.float64)
+    return base ** (-2.0 * e / head_dim)
+
+
+def rope_rotate(x: np.ndarray, pos, base: float) -> np.ndarray:
+    """Rotate-half RoPE of x [n, H, hd] at positions pos [n] (or a scalar).
+
+    Pair (x_e, x_{e+hd/2}) is rotated by the angle pos * theta_e:
+        out_e        = x_e cos - x_{e+hd/2} sin
+        out_{e+hd/2} = x_{e+hd/2} cos + x_e sin
+    """
+    hd = x.shape[-1]
+    half = hd // 2
+    ang = np.multiply.outer(np.asarray(pos, dtype=np.float64),
+                            rope_inv_freq(hd, base))           # [n, hd/2]
+    c = np.cos(ang)[..., None, :]
+    s = np.sin(ang)[..., None, :]
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+def reposition_keys(k_local: np.ndarray, delta: int, n_kv_heads: int,
+                    head_dim: int, base: float) -> np.ndarray:
+    """Pi_i of QCFuse Eq. 4 for keys: a chunk prefilled standalone holds keys
+    rotated to chunk-local positions t; moving it to request offset
+    o = delta applies one more rotation by delta (RoPE rotations compose,
+    CacheBlend blog "Why You Can't Just Concatenate").  k_local [n, Hkv*hd]."""
+    n = k_local.shape[0]
+    k = k_local.reshape(n, n_kv_heads, head_dim)
+    return rope_rotate(k, delta, base).reshape(n, n_kv_heads * head_dim)
+
+
+def stitch(store, lens, n_kv_heads, head_dim, base):
+    """KV^PIC(C) = [Pi_1(KV_1); ...; Pi_m(KV_m)] (QCFuse Eq. 4).
+
+    store: list over chunks of (K, V), each [n_layers][len][Hkv*hd];
+    returns (K, V) each [n_layers][N][Hkv*hd] with chunk i at offset
+    o_i = sum_{j<i} |c_j|; values are stitched in token order unchanged."""
+    n_layers = store[0][0].shape[0]
+    Ks, Vs = [], []
+    for l in range(n_layers):
+        off = 0
+        kl, vl = [], []
+        for (kc, vc), ln in zip(store, lens):
+            kl.append(reposition_keys(kc[l], off, n_kv_heads, head_dim, base))
+            vl.append(vc[l].copy())
+            off += ln
+        Ks.append(np.concatenate(kl, 0))
+        Vs.append(np.concatenate(vl, 0))
+    return np.stack(Ks), np.stack(Vs)
+
+
+# --------------------------------------------------------------------------
+# decoder block pieces
+# --------------------------------------------------------------------------
+def rms_norm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
+    """x / sqrt(mean(x^2) + eps) * g, per row."""
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * g
+
+
+def silu(x: np.ndarray) -> np.ndarray:
+    return x / (1.0 + np.exp(-x))
+
+
+def causal_attention(q, q_pos, K, V, n_q_heads, n_kv_heads):
+    """softmax(q K^T / sqrt(hd) + causal mask) V for selected query rows.
+
+    q [n, Hq, hd] at positions q_pos [n]; K, V [T, Hkv, hd] hold the cache at
+    positions 0..T-1.  A query at position p sees keys 0..p only (QCFuse
+    §2.1.3: recomputation stays causal over the partially fused prefix); q head h
+    uses kv head floor(h / (Hq/Hkv)) (grouped-query attention).  Attention
+    cost is n x T, not T x T (CacheBlend blog, step 4 of blend_layer)."""
+    n, Hq, hd = q.shape
+    T = K.shape[0]
+    group = n_q_heads // n_kv_heads
+    q_pos = np.asarray(q_pos)
+    mask = np.arange(T)[None, :] > q_pos[:, None]                   # [n, T]
+    out = np.empty_like(q)
+    for h in range(Hq):
+        kh = h // group
+        s = (q[:, h, :] @ K[:, kh, :].T) / math.sqrt(hd)            # [n, T]
+        s = np.where(mask, -np.inf, s)
+        s = s - s.max(axis=1, keepdims=True)
+        p = np.exp(s)
+        p = p / p.sum(axis=1, keepdims=True)
+        out[:, h, :] = p @ V[:, kh, :]
+    return out
+
+
+def decoder_layer(m: Model, l: int, h_rows, pos_rows, K_cache, V_cache,
+                  cache_rows, write_kv=True):
+    """One pre-norm decoder layer for the rows ``h_rows`` [n, d] at request
+    positions ``pos_rows``; their fresh K/V are written into the layer's
+    cache at ``cache_rows`` (Eq. 7: selected entries replace the reused
+    ones) and the rows then attend causally over the whole cache.  Returns
+    the new hidden rows and the fresh (post-RoPE) K and V rows.
+
+        x  = RMSNorm(h; norm1)
+        q, k, v = x W_q^T, x W_k^T, x W_v^T ; q, k rotated at their positions
+        h1 = h + Attn(q, K_fused, V_fused) W_o^T
+        h2 = h1 + (silu(x2 W_gate^T) * (x2 W_up^T)) W_down^T, x2 = RMSNorm(h1)
+    """
+    L = m.layers[l]
+    n = h_rows.shape[0]
+    Hq, Hkv, hd = m.n_q_heads, m.n_kv_heads, m.head_dim
+    x = rms_norm(h_rows, L["norm1"], m.norm_eps)
+    qkv = x @ L["w_qkv"].T
+    q = qkv[:, :Hq * hd].reshape(n, Hq, hd)
+    k = qkv[:, Hq * hd:(Hq + Hkv) * hd].reshape(n, Hkv, hd)
+    v = qkv[:, (Hq + Hkv) * hd:].reshape(n, Hkv, hd)
+    q = rope_rotate(q, pos_rows, m.rope_base)
+    k = rope_rotate(k, pos_rows, m.rope_base)
+    k_new = k.reshape(n, Hkv * hd)
+    v_new = v.reshape(n, Hkv * hd)
+    if write_kv:
+        K_cache[cache_rows] = k_new
+        V_cache[cache_rows] = v_new
+    T = K_cache.shape[0]
+    o = causal_attention(q, pos_rows, K_cache.reshape(T, Hkv, hd),
+                         V_cache.reshape(T, Hkv, hd), Hq, Hkv)
+    h1 = h_rows + o.reshape(n, Hq * hd) @ L["w_o"].T
+    x2 = rms_norm(h1, L["norm2"], m.norm_eps)
+    g = silu(x2 @ L["w_gate"].T) * (x2 @ L["w_up"].T)
+    h2 = h1 + g @ L["w_down"].T
+    return h2, k_new, v_new
+
+
+def first_token(m: Model, h_last: np.ndarray) -> int:
+    """argmax over the vocabulary of RMSNorm(h_last) E^T (LM head tied to
+    the embedding); the first generated token that ends TTFT (QCFuse
+    §4.1.5).  Ties resolve to the lowest id."""
+    logits = rms_norm(h_last[None, :], m.final_norm, m.norm_eps)[0] @ m.embed.T
+    return int(np.argmax(logits))
+
+
+# --------------------------------------------------------------------------
+# full prefill and standalone chunk prefill
+# --------------------------------------------------------------------------
+@dataclass
+class PrefillResult:
+    K: np.ndarray          # [n_layers][T][Hkv*hd]
+    V: np.ndarray
+    hidden: np.ndarray     # [T][d] final hidden states (before final norm)
+    token: int             # argmax of the last row's logits
+
+
+def full_prefill(m: Model, tokens) -> PrefillResult:
+    """KV^Full(C) (QCFuse Eq. 2): every token computed under the full
+    request at positions 0..T-1, causal attention."""
+    tokens = np.asarray(tokens)
+    T = len(tokens)
+    kvw = m.n_kv_heads * m.head_dim
+    K = np.zeros((m.n_layers, T, kvw))
+    V = np.zeros((m.n_layers, T, kvw))
+    h = m.embed[tokens].copy()
+    rows = np.arange(T)
+    for l in range(m.n_layers):
+        h, _, _ = decoder_layer(m, l, h, rows, K[l], V[l], rows)
+    return PrefillResult(K, V, h, first_token(m, h[-1]))
+
+
+def chunk_prefill(m: Model, chunk_tokens):
+    """KV_c^PIC <- LLM(c) (QCFuse Eq. 3): the chunk alone at chunk-local
+    positions 0..|c|-1.  Returns (K, V) [n_layers][|c|][Hkv*hd]."""
+    r = full_prefill(m, chunk_tokens)
+    return r.K, r.V
+
+
+# --------------------------------------------------------------------------
+# deviation and selection
+# --------------------------------------------------------------------------
+def kv_deviation(k_current: np.ndarray, k_cached: np.ndarray) -> np.ndarray:
+    """d_i = || K_i^current - K_i^cached ||_2^2 over all kv heads and head
+    dims ("Request Order Matters" §2.2 Eq. 1).  Rows are tokens."""
+    diff = k_current - k_cached
+    return np.sum(diff * diff, axis=-1)
+
+
+def select_count(n_ctx: int, ratio_bp: int) -> int:
+    """k = max(1, floor(r N)) ("Request Order Matters" §2.2 Eq. 2; QCFuse Eq.
+    8 writes floor(rho N)).  r is given in integer basis points so that the
+    floor is exact; r = 0 selects nothing (the direct-reuse endpoint)."""
+    if ratio_bp <= 0 or n_ctx <= 0:
+        return 0
+    return max(1, (n_ctx * ratio_bp) // 10000)
+
+
+def token_topk(d: np.ndarray, k: int) -> np.ndarray:
+    """The k tokens with the largest deviation (LMCache's token top-k,
+    "Request Order Matters" §2.2; CacheBlend blog select_hkvd).  Ties go to
+    the lower index; the result is sorted ascending by position."""
+    order = sorted(range(len(d)), key=lambda i: (-d[i], i))
+    return np.array(sorted(order[:k]), dtype=np.int64)
+
+
+def doc_aligned_select(d: np.ndarray, span_offsets, k: int) -> np.ndarray:
+    """Document-aligned recomputation ("Request Order Matters" §2.3).
+
+    Spans S_j = [span_offsets[j], span_offsets[j+1]).  rho_j is the mean
+    deviation over S_j (Eq. 3).  Spans are visited by rho_j descending (ties:
+    lower j); whole spans are taken while they fit in the remaining budget;
+    at the first span that does not fit, the contiguous window of the
+    remaining length with the largest total deviation inside that span is
+    taken (ties: leftmost) and selection stops.  Exactly k tokens.  Empty
+    spans are skipped.  Sums are float64."""
+    offs = list(span_offsets)
+    spans = [(offs[j], offs[j + 1]) for j in range(len(offs) - 1)
+             if offs[j + 1] > offs[j]]
+    idx = [j for j in range(len(spans))]
+    rho = [float(np.sum(d[a:b], dtype=np.float64)) / (b - a) for a, b in spans]
+    idx.sort(key=lambda j: (-rho[j], j))
+    rem = k
+    chosen = []
+    for j in idx:
+        if rem == 0:
+            break
+        a, b = spans[j]
+        if b - a <= rem:
+            chosen.extend(range(a, b))
+            rem -= b - a
+            continue
+        best, best_s = None, -math.inf
+        for s in range(a, b - rem + 1):
+            tot = float(np.sum(d[s:s + rem], dtype=np.float64))
+            if tot > best_s:
+                best, best_s = s, tot
+        chosen.extend(range(best, best + rem))
+        rem = 0
+        break
+    return np.array(sorted(chosen), dtype=np.int64)
+
+
+# --------------------------------------------------------------------------
+# blended prefill
+# --------------------------------------------------------------------------
+@dataclass
+class BlendResult:
+    K: np.ndarray              # fused cache [n_layers][T][Hkv*hd]
+    V: np.ndarray
+    selected: np.ndarray       # P: selected context positions, ascending
+    deviation: np.ndarray      # d over the N context tokens at layer s
+    rows: np.ndarray           # rows computed after layer s (P + always-rows)
+    hidden: np.ndarray         # final hidden states of ``rows`` [R][d]
+    token: int
+    selected_per_layer: dict   # layer -> P used at that layer
+
+
+def blend_prefill(m: Model, segments, store, ratio_bp: int,
+                  policy: str = "token_topk", sel_layer: int = 1,
+                  forced=None, schedule=None) -> BlendResult:
+    """Selective KV recomputation over a partially reused cache (QCFuse
+    §2.1.3 Eqs. 6-7; CacheBlend blog ``blend_layer``; LMCache flow of
+    "Request Order Matters" §2.2).
+
+    segments: list of (tokens, cached) in request order; cached segments form
+      the reusable context C (N tokens), uncached ones (the query U, a new
+      document) are recomputed at every layer and are not counted in N.
+    store:    list, one entry per cached segment, of (K, V) PIC caches
+      [n_layers][len][Hkv*hd] computed standalone at position 0 (Eq. 3).
+    forced:   if given, the selected context positions P (ascending) are
+      taken from it instead of being ranked (the "forced" mode used for bf16
+      parity, where ranking near the k-th deviation is precision dependent).
+    schedule: optional gradual filtering (CacheBlend blog select_hkvd):
+      list of (layer, keep_count) with layer > sel_layer; at that layer the
+      current P is re-ranked by the deviation of its fresh keys and only
+      keep_count rows are kept from then on.
+
+    Steps:
+      1. positions 0..T-1; context positions of cached segments are the
+         context token indices 0..N-1 in order (uncached rows interleave at
+         their own positions but are not in C).
+      2. KV^PIC(C): stitch the store with Pi_i (Eq. 4).
+      3. layers < s: full layer on every row (fused = fresh).
+      4. layer s: keys of every row are projected fresh; d over context
+         tokens (Eq. 1); P = top-k (Eq. 2) or document-aligned spans (Eq. 3).
+      5. layers >= s: only P and the uncached rows are computed; their fresh
+         K/V replace the PIC entries (Eq. 7) and they attend causally over the
+         fused cache; all other rows keep KV^PIC.
+      6. first token from the last row.
+    """
+    Hkv, hd = m.n_kv_heads, m.head_dim
+    kvw = Hkv * hd
+    toks = np.concatenate([np.asarray(t) for t, _ in segments])
+    T = len(toks)
+    cached_rows, uncached_rows, lens = [], [], []
+    off = 0
+    for t, c in segments:
+        r = np.arange(off, off + len(t))
+        (cached_rows if c else uncached_rows).append(r)
+        if c:
+            lens.append(len(t))
+        off += len(t)
+    ctx_rows = np.concatenate(cached_rows) if cached_rows else np.zeros(0, int)
+    always = np.concatenate(uncached_rows) if uncached_rows else np.zeros(0, int)
+    N = len(ctx_rows)
+
+    # 2. stitched reused cache, placed at the request rows of each chunk.
+    # Each chunk is re-rotated by its own request offset.
+    K = np.zeros((m.n_layers, T, kvw))
+    V = np.zeros((m.n_layers, T, kvw))
+    off = 0
+    si = 0
+    for t, c in segments:
+        if c:
+            kc, vc = store[si]
+            si += 1
+            for l in range(m.n_layers):
+                K[l, off:off + len(t)] = reposition_keys(kc[l], off, Hkv, hd,
+                                                         m.rope_base)
+                V[l, off:off + len(t)] = vc[l]
+        off += len(t)
+
+    pos_all = np.arange(T)
+    h = m.embed[toks].copy()
+    # 3. full layers before the selection layer
+    for l in range(min(sel_layer, m.n_layers)):
+        h, _, _ = decoder_layer(m, l, h, pos_all, K[l], V[l], pos_all)
+
+    k = select_count(N, ratio_bp)
+    d = np.zeros(N)
+    per_layer = {}
+    if sel_layer >= m.n_layers:
+        P = np.arange(N)
+        active = pos_all
+    else:
+        # 4. fresh keys of all rows at layer s, deviation over context rows
+        L = m.layers[sel_layer]
+        x = rms_norm(h, L["norm1"], m.norm_eps)
+        qd = m.n_q_heads * hd
+        k_all = (x @ L["w_qkv"][qd:qd + kvw].T).reshape(T, Hkv, hd)
+        k_all = rope_rotate(k_all, pos_all, m.rope_base).reshape(T, kvw)
+        d = kv_deviation(k_all[ctx_rows], K[sel_layer][ctx_rows])
+        if forced is not None:
+            P = np.asarray(forced, dtype=np.int64)
+        elif policy == "token_topk":
+            P = token_topk(d, k)
+        elif policy == "doc_aligned":
+            offs = np.concatenate([[0], np.cumsum(lens)])
+            P = doc_aligned_select(d, offs, k)
+        else:
+            raise ValueError(policy)
+        sched = dict(schedule or [])
+        h_act = None
+        active = None
+        for l in range(sel_layer, m.n_layers):
+            if l in sched and l > sel_layer:
+                # gradual filtering: re-rank the current P by its fresh keys
+                Lw = m.layers[l]
+                rows_p = ctx_rows[P]
+                sub = np.searchsorted(active, rows_p)
+                xp = rms_norm(h_act[sub], Lw["norm1"], m.norm_eps)
+                kp = (xp @ Lw["w_qkv"][qd:qd + kvw].T).reshape(-1, Hkv, hd)
+                kp = rope_rotate(kp, rows_p, m.rope_base).reshape(-1, kvw)
+                dp = kv_deviation(kp, K[l][rows_p])
+                keep = token_topk(dp, min(sched[l], len(P)))
+                P = P[keep]
+            new_active = np.union1d(ctx_rows[P], always).astype(np.int64)
+            if active is None:
+                h_act = h[new_active]
+            else:
+                h_act = h_act[np.searchsorted(active, new_active)]
+            active = new_active
+            per_layer[l] = P.copy()
+            # 5. Eq. 7 write of fresh K/V, then attention over the fused cache
+            h_act, _, _ = decoder_layer(m, l, h_act, active, K[l], V[l], active)
+        h_final_rows = active
+        tok = first_token(m, h_act[-1])
+        return BlendResult(K, V, P, d, h_final_rows, h_act, tok, per_layer)
+    tok = first_token(m, h[-1])
+    return BlendResult(K, V, P, d, active, h, tok, per_layer)
+
+
+# --------------------------------------------------------------------------
+# byte model
+# --------------------------------------------------------------------------
+def kv_bytes_per_layer(context_len: int, kv_heads: int, head_dim: int,
+                       bytes_per_elem: int = 2) -> int:
+    """K plus V bytes of one layer's cache: 2 * L * kv_heads * hd * 2 for
+    fp16 (CacheBlend blog, "Hiding Recompute Behind I/O")."""
+    return 2 * context_len * kv_heads * head_dim * bytes_per_elem

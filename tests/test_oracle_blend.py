@@ -1,0 +1,193 @@
+"""Pins of the oracle's prefill and blend paths against what the pages fix:
+the rho = 1 and rho = 0 endpoints (QCFuse §4.1.5), exact reuse of a chunk at
+position 0 and the context independence of layer 0 (QCFuse Eqs. 3-5),
+causality, and the Eq. 7 fusion rule.  No GPU."""
+import numpy as np
+import pytest
+
+import oracle as O
+import workload as W
+
+
+def _model(n_layers=3, d=48, Hq=4, Hkv=2, hd=12, F_=40, V=97, seed=0):
+    shape = W.ModelShape("t", n_layers, d, Hq, Hkv, hd, F_, V, dtype="f32")
+    w = W.make_weights(shape, seed, std=0.15, embed_std=1.0)
+    return O.model_from_weights(shape, w)
+
+
+def _request(m, seed=1, lens=(7, 9, 5), n_query=4):
+    rng = np.random.default_rng(seed)
+    chunks = [rng.integers(0, m.vocab, size=n) for n in lens]
+    query = rng.integers(0, m.vocab, size=n_query)
+    segs = [(c, True) for c in chunks] + [(query, False)]
+    store = [O.chunk_prefill(m, c) for c in chunks]
+    return chunks, query, segs, store
+
+
+def _close(a, b, tol=1e-10):
+    scale = max(1.0, float(np.max(np.abs(b))))
+    assert float(np.max(np.abs(a - b))) <= tol * scale
+
+
+def test_full_prefill_is_causal():
+    m = _model()
+    toks = np.random.default_rng(2).integers(0, m.vocab, size=20)
+    a = O.full_prefill(m, toks)
+    b = O.full_prefill(m, toks[:13])
+    _close(a.K[:, :13], b.K)
+    _close(a.V[:, :13], b.V)
+    _close(a.hidden[:13], b.hidden)
+
+
+def test_chunk_at_position_zero_reuses_exactly():
+    m = _model()
+    chunks, query, segs, store = _request(m)
+    full = O.full_prefill(m, np.concatenate(chunks + [query]))
+    n0 = len(chunks[0])
+    _close(full.K[:, :n0], store[0][0], 1e-12)
+    _close(full.V[:, :n0], store[0][1], 1e-12)
+
+
+def test_layer0_kv_is_context_independent():
+    # the layer-0 input is the embedding alone, so fresh layer-0 K equals the
+    # re-positioned PIC key and fresh V the stored V, for every chunk
+    m = _model()
+    chunks, query, segs, store = _request(m)
+    full = O.full_prefill(m, np.concatenate(chunks + [query]))
+    K, V = O.stitch(store, [len(c) for c in chunks], m.n_kv_heads, m.head_dim,
+                    m.rope_base)
+    N = sum(len(c) for c in chunks)
+    _close(full.K[0, :N], K[0])
+    _close(full.V[0, :N], V[0])
+    # ... but not at layer 1, where cross-chunk attention has acted (Eq. 5)
+    assert np.max(np.abs(full.K[1, len(chunks[0]):N] -
+                         K[1, len(chunks[0]):])) > 1e-3
+
+
+def test_full_recompute_equals_full_prefill():
+    m = _model()
+    chunks, query, segs, store = _request(m)
+    full = O.full_prefill(m, np.concatenate(chunks + [query]))
+    r = O.blend_prefill(m, segs, store, ratio_bp=10000)
+    N = sum(len(c) for c in chunks)
+    assert list(r.selected) == list(range(N))
+    _close(r.K, full.K)
+    _close(r.V, full.V)
+    _close(r.hidden, full.hidden)
+    assert r.token == full.token
+
+
+def test_zero_recompute_is_direct_reuse():
+    # rho = 0: every context entry at layers >= s is the stitched PIC entry
+    # and the query is prefilled over KV^PIC(C) (layer 0 is recomputed in
+    # full, which reproduces the PIC entries up to rounding)
+    m = _model()
+    chunks, query, segs, store = _request(m)
+    r = O.blend_prefill(m, segs, store, ratio_bp=0)
+    assert len(r.selected) == 0
+    lens = [len(c) for c in chunks]
+    N = sum(lens)
+    K, V = O.stitch(store, lens, m.n_kv_heads, m.head_dim, m.rope_base)
+    for l in range(1, m.n_layers):
+        assert np.array_equal(r.K[l, :N], K[l])
+        assert np.array_equal(r.V[l, :N], V[l])
+    # independent composition: query rows prefilled over the stitched cache
+    T = N + len(query)
+    Kc = np.concatenate([K, np.zeros((m.n_layers, len(query), K.shape[2]))], 1)
+    Vc = np.concatenate([V, np.zeros_like(Kc[:, N:])], 1)
+    qrows = np.arange(N, T)
+    h = m.embed[query].copy()
+    for l in range(m.n_layers):
+        h, _, _ = O.decoder_layer(m, l, h, qrows, Kc[l], Vc[l], qrows)
+    _close(r.hidden, h, 1e-9)
+    for l in range(m.n_layers):
+        _close(r.K[l, N:], Kc[l, N:], 1e-9)
+    assert r.token == O.first_token(m, h[-1])
+
+
+def test_first_chunk_has_zero_deviation():
+    # chunk 1's causal prefix is the same standalone and in the request
+    m = _model()
+    chunks, query, segs, store = _request(m)
+    r = O.blend_prefill(m, segs, store, ratio_bp=2000)
+    n0 = len(chunks[0])
+    assert np.all(r.deviation >= 0)
+    assert np.max(r.deviation[:n0]) < 1e-18 * max(1.0, np.max(r.deviation))
+    assert np.min(r.deviation[n0:]) > 0
+
+
+def test_selection_at_layer0_sees_no_deviation():
+    # at layer 0 the fresh keys equal the re-positioned PIC keys for every
+    # chunk, which pins the per-chunk offsets used by the blend's stitching
+    m = _model()
+    chunks, query, segs, store = _request(m)
+    r = O.blend_prefill(m, segs, store, ratio_bp=1500, sel_layer=0)
+    assert np.max(r.deviation) < 1e-18
+
+
+def test_fusion_rule_eq7():
+    m = _model()
+    chunks, query, segs, store = _request(m)
+    r = O.blend_prefill(m, segs, store, ratio_bp=3000)
+    lens = [len(c) for c in chunks]
+    N = sum(lens)
+    k = O.select_count(N, 3000)
+    assert len(r.selected) == k
+    assert np.all(np.diff(r.selected) > 0)
+    assert list(r.selected) == list(O.token_topk(r.deviation, k))
+    K, V = O.stitch(store, lens, m.n_kv_heads, m.head_dim, m.rope_base)
+    unsel = np.setdiff1d(np.arange(N), r.selected)
+    for l in range(1, m.n_layers):
+        assert np.array_equal(r.K[l, unsel], K[l, unsel])      # PIC kept
+        assert np.array_equal(r.V[l, unsel], V[l, unsel])
+        assert np.all(np.abs(r.K[l, r.selected] - K[l, r.selected]).max(1) > 0)
+    assert list(r.rows) == list(r.selected) + list(range(N, N + len(query)))
+
+
+def test_forced_selection_reproduces_free_selection():
+    m = _model()
+    chunks, query, segs, store = _request(m)
+    a = O.blend_prefill(m, segs, store, ratio_bp=2500)
+    b = O.blend_prefill(m, segs, store, ratio_bp=2500, forced=a.selected)
+    assert np.array_equal(a.K, b.K) and np.array_equal(a.hidden, b.hidden)
+
+
+def test_gradual_filtering_only_shrinks():
+    m = _model(n_layers=4)
+    chunks, query, segs, store = _request(m)
+    N = sum(len(c) for c in chunks)
+    r = O.blend_prefill(m, segs, store, ratio_bp=2000,
+                        schedule=[(2, 3), (3, 2)])
+    p1, p2, p3 = (set(r.selected_per_layer[l]) for l in (1, 2, 3))
+    assert len(p1) == O.select_count(N, 2000) and len(p2) == 3 and len(p3) == 2
+    assert p3 <= p2 <= p1
+
+
+def test_selection_past_last_layer_is_full_prefill():
+    m = _model()
+    chunks, query, segs, store = _request(m)
+    full = O.full_prefill(m, np.concatenate(chunks + [query]))
+    r = O.blend_prefill(m, segs, store, ratio_bp=1500, sel_layer=m.n_layers)
+    _close(r.K, full.K)
+    assert r.token == full.token
+
+
+def test_doc_aligned_policy_in_blend():
+    m = _model()
+    chunks, query, segs, store = _request(m, lens=(6, 6, 6))
+    r = O.blend_prefill(m, segs, store, ratio_bp=3400, policy="doc_aligned")
+    k = O.select_count(18, 3400)          # 6
+    assert len(r.selected) == k
+    ref = O.doc_aligned_select(r.deviation, [0, 6, 12, 18], k)
+    assert list(r.selected) == list(ref)
+
+
+@pytest.mark.slow
+def test_tiny_workload_runs():
+    wl = W.tiny_blend()
+    m = O.model_from_weights(wl.model, W.make_weights(wl.model, wl.seed))
+    req = wl.requests[0]
+    store = [O.chunk_prefill(m, s.tokens) for s in req.segments if s.cached]
+    segs = [(s.tokens, s.cached) for s in req.segments]
+    r = O.blend_prefill(m, segs, store, wl.ratio_bp)
+    assert len(r.selected) == 57 and r.hidden.shape == (89, 256)
