@@ -1,0 +1,398 @@
+#!/usr/bin/env python3
+"""Blended-prefill benchmark on GB300.
+
+Workload: Llama-3-8B-shaped stack (32 layers, d=4096, 32 q / 8 kv heads,
+head_dim 128, SwiGLU 14336, vocab 128256, bf16, random-init N(0, 0.02)),
+one request of 6 retrieved chunks x 512 tokens + 64 query tokens, 15% token
+top-k at selection layer 1.  The per-chunk caches are prefilled standalone
+before timing (offline preparation, outside TTFT).  One timed step is one
+``cb_blend_prefill`` call: re-position + stitch, layer 0 on every row, key
+deviation + top-k at layer 1, the 31 compact layers, final norm + LM head +
+argmax.
+
+Prints one JSON line.  Under torchrun (N > 1) every rank runs an independent
+replica on its own GPU (no data-path collective); rank 0 prints the line.
+``--impl reference`` times the CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workload as W  # noqa: E402
+
+METRIC = "blended-prefill context tokens/s and TTFT at r=15% on 1 GB300; % of roofline"
+UNIT = "tokens/s"
+RATIO_BP = 1500
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                  "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- clocks --
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------ GPU setup --
+def device_weights(shape, seed, device):
+    """Random-init weights generated on the device (seeded): projections
+    N(0, 0.02), embeddings N(0, 1), bf16; RMSNorm gains 1."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    dt = torch.bfloat16
+
+    def rnd(*s, std=0.02):
+        return (torch.randn(*s, generator=g, device=device, dtype=torch.float32) * std).to(dt)
+    d, F = shape.d_model, shape.d_ffn
+    qd = shape.n_q_heads * shape.head_dim
+    w = {"embed": rnd(shape.vocab, d, std=1.0),
+         "final_norm": torch.ones(d, device=device), "layers": []}
+    for _ in range(shape.n_layers):
+        w["layers"].append({
+            "w_qkv": rnd(shape.qkv_rows, d), "w_o": rnd(d, qd),
+            "w_gate": rnd(F, d), "w_up": rnd(F, d), "w_down": rnd(d, F),
+            "norm1": torch.ones(d, device=device), "norm2": torch.ones(d, device=device)})
+    return w
+
+
+def setup_replica(rank, device):
+    import torch
+    import rag_kv_cache_layer_gb300 as R
+    wl = W.llama_rag(seed=1 + rank)
+    shape = wl.model
+    model = R.BlendModel(shape, device_weights(shape, 1234 + rank, device), 4096, device)
+    rq = wl.requests[0]
+    store = R.ChunkStore(model, rq.n_ctx)
+    store.prefill({s.chunk_id: torch.from_numpy(s.tokens).to(device)
+                   for s in rq.segments if s.cached})
+    segs = [store.seg(s.chunk_id) if s.cached else R.Seg(len(s.tokens)) for s in rq.segments]
+    tokens_host = torch.from_numpy(rq.tokens).pin_memory()
+    tokens_dev = tokens_host.to(device)
+    reqs = [R.Req(tokens_dev, segs)]
+    plan = model.plan(reqs, RATIO_BP)
+    outs = model.alloc_outputs(plan, 1)
+    torch.cuda.synchronize()
+    return wl, model, store, reqs, plan, outs, tokens_host, tokens_dev
+
+
+def time_dominant_kernel(model, plan, device, reps=20):
+    """The SwiGLU gate/up projection of a compact layer (the largest launch
+    of the step), timed alone with CUDA events on the current stream."""
+    import torch
+    from rag_kv_cache_layer_gb300 import _lib as L
+    s = model.shape
+    M = int(plan.R_total)
+    x = torch.randn(M, s.d_model, device=device).to(torch.bfloat16)
+    g = torch.empty(M, s.d_ffn, device=device, dtype=torch.bfloat16)
+    lw = model.w["layers"][5]
+    for _ in range(3):
+        model.cb_linear(x, lw["w_gate"], g, L.CB_EPI_SWIGLU, W2=lw["w_up"])
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(reps):
+        model.cb_linear(x, lw["w_gate"], g, L.CB_EPI_SWIGLU, W2=lw["w_up"])
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    flops = 2.0 * M * s.d_model * 2 * s.d_ffn
+    return ms, flops
+
+
+# ---------------------------------------------------------- CPU oracle --
+def oracle_sample(budget_note=True):
+    """Times the CPU oracle on a bounded sample of the same request: the
+    whole first two layers of the blend (layer 0 on all 3136 rows, selection
+    and layer 1 on the 524 computed rows, LM head), plus one further compact
+    layer; TTFT is extrapolated as t(2 layers) + 30 x t(compact layer).
+    Weights of one random layer are shared by all layers and the chunk
+    caches are random (timing does not depend on the values)."""
+    import oracle as O
+    wl = W.llama_rag(n_layers=2)
+    s = wl.model
+    rng = np.random.default_rng(0)
+    f = lambda *shape: rng.standard_normal(shape) * 0.02
+    lw = {"w_qkv": f(s.qkv_rows, s.d_model), "w_o": f(s.d_model, s.n_q_heads * s.head_dim),
+          "w_gate": f(s.d_ffn, s.d_model), "w_up": f(s.d_ffn, s.d_model),
+          "w_down": f(s.d_model, s.d_ffn), "norm1": np.ones(s.d_model),
+          "norm2": np.ones(s.d_model)}
+    block = rng.standard_normal((4096, s.d_model)).astype(np.float32)
+    embed = np.tile(block, (math.ceil(s.vocab / 4096), 1))[: s.vocab]
+    m = O.Model(2, s.d_model, s.n_q_heads, s.n_kv_heads, s.head_dim, s.d_ffn, s.vocab,
+                s.rope_base, s.norm_eps, embed, np.ones(s.d_model), [lw, lw])
+    rq = wl.requests[0]
+    store = [(rng.standard_normal((2, len(sg.tokens), s.kv_row_elems)),
+              rng.standard_normal((2, len(sg.tokens), s.kv_row_elems)))
+             for sg in rq.segments if sg.cached]
+    segs = [(sg.tokens, sg.cached) for sg in rq.segments]
+    t0 = time.perf_counter()
+    r = O.blend_prefill(m, segs, store, RATIO_BP)
+    t2 = time.perf_counter() - t0
+    return m, r, t2
+
+
+def oracle_compact_layer(m, r):
+    import oracle as O
+    K, V = r.K[1].copy(), r.V[1].copy()
+    t0 = time.perf_counter()
+    O.decoder_layer(m, 1, r.hidden, r.rows, K, V, r.rows)
+    return time.perf_counter() - t0
+
+
+def cpu_cores():
+    return os.cpu_count() or 1
+
+
+def cpu_baseline_leg():
+    m, r, t2 = oracle_sample()
+    tc = oracle_compact_layer(m, r)
+    T = 6 * 512 + 64
+    ttft = t2 + 30 * tc
+    return {"value": T / ttft, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": (f"float64 numpy oracle: first 2 layers of the request "
+                       f"({t2:.1f} s) + one compact layer ({tc:.2f} s), TTFT "
+                       f"extrapolated to 32 layers = {ttft:.1f} s"),
+            "ttft_s_estimate": ttft}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    t_setup = time.perf_counter()
+    m, r, t2 = oracle_sample()
+    T = 6 * 512 + 64
+    for _ in range(args.warmup):
+        oracle_compact_layer(m, r)
+    per = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        per.append(t2 + 30 * oracle_compact_layer(m, r))
+    wall = time.perf_counter() - t0
+    ttft = statistics.median(per)
+    value = T / ttft
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ttft * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "llama3-8b-shape 32L bf16-valued, 6x512 chunks + 64 query, "
+                                   "r=15% token top-k, B=1",
+                       "global_batch": 1, "seq_len": T, "parallelism": "none (CPU)",
+                       "step": "one compact decoder layer; TTFT = t(first 2 layers, "
+                               "measured once) + 30 x t(step)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(),
+                             "kind": "oracle",
+                             "sample": f"first 2 layers once ({t2:.1f} s), then "
+                                       f"{args.steps} compact layers ({wall:.1f} s)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------- our arm --
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import rag_kv_cache_layer_gb300 as R
+    from rag_kv_cache_layer_gb300 import _lib as L
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+
+    wl, model, store, reqs, plan, outs, tok_host, tok_dev = setup_replica(rank, device)
+    T = int(plan.T_total)
+    B = 1
+    st = torch.cuda.current_stream()
+
+    def step():
+        model.cb_blend_prefill(reqs, RATIO_BP, outputs=outs)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if R.device_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    # ---- device-resident timed region
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    n0 = L.lib.cb_debug_launch_count()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(st)
+    for i in range(args.steps):
+        step()
+        ev[i + 1].record(st)
+    torch.cuda.synchronize()
+    n1 = L.lib.cb_debug_launch_count()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    if world > 1:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * B * T / (ms_per_step / 1e3)
+
+    # ---- end to end: pinned host tokens in, first token + selection out
+    sel_host = torch.empty(int(plan.K_total), dtype=torch.int32).pin_memory()
+    tok_out = torch.empty(1, dtype=torch.int32).pin_memory()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(args.steps):
+        tok_dev.copy_(tok_host, non_blocking=True)
+        step()
+        sel_host.copy_(outs["selected"][: int(plan.K_total)], non_blocking=True)
+        tok_out.copy_(outs["first_token"], non_blocking=True)
+    e1.record(st)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * B * T / (e2e_ms / args.steps / 1e3)
+    if R.device_status() != 0:
+        raise RuntimeError("device status set during the timed region")
+
+    if rank == 0:
+        peaks, src = load_peaks()
+        kms, kflops = time_dominant_kernel(model, plan, device)
+        achieved = kflops / (kms / 1e3) / 1e12
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {
+                "workload": "llama3-8b-shape 32L bf16 random-init, 6x512 chunks + 64 query, "
+                            "r=15% token top-k at layer 1, B=1 per GPU",
+                "global_batch": world * B, "seq_len": T,
+                "parallelism": "replicas" if world > 1 else "none",
+                "k_selected": int(plan.K_total), "rows_computed": int(plan.R_total),
+                "ttft_ms_median": statistics.median(per),
+                "ttft_ms_p95": float(np.percentile(per, 95)),
+                "l2": "inputs larger than L2 (14.5 GB of weights and 0.8 GB of "
+                      "chunk caches read per step)"},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * 4,
+                    "d2h_bytes_per_step": 4 * (int(plan.K_total) + 1)},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "kernel": f"gate/up SwiGLU projection, M={int(plan.R_total)} "
+                                   f"N=2x14336 K=4096, timed alone "
+                                   f"({kms:.3f} ms/launch)",
+                         "peak_source": f"bf16_tflops (burst) of {src}"},
+            "clocks": clk,
+            "gpu_launches": int(n1 - n0),
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline_leg()
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,432 @@
+/*
+ * cacheblend.h -- C ABI of a GB300 (sm_103a) library for non-prefix KV-cache
+ * fusion in RAG prefill: independently precomputed per-chunk K/V caches are
+ * re-positioned by composing RoPE rotations, the tokens whose fresh keys
+ * deviate most from the reused keys are recomputed, and only those rows run
+ * through the layer, attending over the blended cache.
+ *
+ * Sources of the operations (cited per entry point below):
+ *   [QCF]  QCFuse: Query-Aware Cache Fusion via Compressed View for Efficient
+ *          RAG Serving (arxiv 2606.05875), §2.1 Eqs. 1-7, §4.1.5.
+ *   [CB]   CacheBlend: Reusing KV Caches When Your Text Isn't a Prefix
+ *          (blog): "Why You Can't Just Concatenate", "Quantifying the
+ *          Damage", "Selective Recompute Without Skipping" (blend_layer),
+ *          "The Chicken-and-Egg Problem" (select_hkvd).
+ *   [ROM]  Request Order Matters: Cache-History Sensitivity in Selective
+ *          KV-Cache Reuse for Rolling Agents: §2.2 Eqs. 1-2, §2.3 Eq. 3.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory    Every buffer argument is caller-owned.  Pointers documented as
+ *           "device" must be device memory of the current CUDA device;
+ *           "host" pointers are read during the call only.  The library
+ *           never allocates device memory on the hot path: scratch space is
+ *           the caller's workspace, sized by the matching *_workspace call.
+ *           cb_model_create allocates only its small host-side descriptor.
+ * Streams   Calls enqueue work on `stream` and return without waiting; a
+ *           NULL stream is the legacy default stream.  Arguments read from
+ *           host memory are consumed before the call returns.
+ * Layout    Row-major.  A "row" of the KV cache is one token's keys (or
+ *           values) for all kv heads: n_kv_heads * head_dim contiguous
+ *           elements, head h at offset h * head_dim.  Leading dimensions
+ *           (ld_*) and strides count elements, not bytes.
+ * Dtypes    CB_F32 tensors are float; CB_BF16 tensors are bfloat16.  All
+ *           accumulation is fp32.  RMSNorm gains, the residual stream,
+ *           deviations and the RoPE table are always float.
+ * Alignment Device base pointers and leading dimensions of bf16/f32 tensors
+ *           must give 16-byte aligned rows; violations return
+ *           CB_ERR_INVALID_ARG.
+ * Errors    Host-side validation runs before anything is enqueued and
+ *           returns a cb_status; the message is available from
+ *           cb_last_error_message() (thread-local).  Failures detected on
+ *           the device (an index out of range, a bounded wait that expired)
+ *           are recorded in a per-device status word read by
+ *           cb_get_device_status(); kernels never trap.
+ */
+#ifndef CACHEBLEND_H_
+#define CACHEBLEND_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *cb_stream; /* same type as cudaStream_t */
+
+typedef enum {
+  CB_OK = 0,
+  CB_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or layout */
+  CB_ERR_UNSUPPORTED = 2,   /* dtype / shape / device not supported */
+  CB_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+  CB_ERR_TIMEOUT = 4,       /* a bounded device-side wait expired */
+  CB_ERR_DEVICE_INDEX = 5,  /* a device-side index check failed */
+  CB_ERR_WORKSPACE = 6      /* workspace pointer NULL or too small */
+} cb_status;
+
+typedef enum { CB_F32 = 0, CB_BF16 = 1 } cb_dtype;
+
+typedef enum {
+  CB_POLICY_TOKEN_TOPK = 0,   /* [ROM] §2.2: the k largest deviations       */
+  CB_POLICY_DOC_ALIGNED = 1   /* [ROM] §2.3: whole spans by mean deviation,
+                                 then the best window of the remainder      */
+} cb_policy;
+
+/* Largest batch of requests one call accepts. */
+#define CB_MAX_BATCH 64
+/* Largest number of spans (documents) one selection call accepts. */
+#define CB_MAX_SPANS 1024
+
+/* ------------------------------------------------------------------------ */
+/* Diagnostics                                                              */
+/* ------------------------------------------------------------------------ */
+
+/* Message of the last failing call on this thread ("" if none). */
+const char *cb_last_error_message(void);
+
+/* Library ABI version (major * 100 + minor). */
+int cb_version(void);
+
+/* Reads and clears the device status word of the current device.  Blocks
+ * until all work on the device has finished.  *out receives CB_OK or the
+ * first device-side failure (CB_ERR_TIMEOUT, CB_ERR_DEVICE_INDEX) recorded
+ * since the last read. */
+cb_status cb_get_device_status(cb_status *out);
+
+/* Runs one kernel whose single thread waits on a shared-memory mbarrier that
+ * nothing ever completes, with a bounded wait of about `limit_us`
+ * microseconds; the wait expires, the kernel records CB_ERR_TIMEOUT in the
+ * device status word and returns.  Exercises the bounded-wait path used by
+ * every pipelined kernel of the library without hanging the device. */
+cb_status cb_debug_expire_wait(int limit_us, cb_stream stream);
+
+/* Number of kernels this library has enqueued in this process (all devices,
+ * all threads).  Benchmarks difference it around a region to count the
+ * library's launches. */
+unsigned long long cb_debug_launch_count(void);
+
+/* ------------------------------------------------------------------------ */
+/* RoPE table                                                               */
+/* ------------------------------------------------------------------------ */
+
+/* Number of floats of a RoPE table for positions [0, max_positions) and
+ * head_dim: max_positions * (head_dim / 2) * 2 (cos, sin interleaved). */
+size_t cb_rope_table_elems(int max_positions, int head_dim);
+
+/* Fills table[p][e] = (cos(p * theta_e), sin(p * theta_e)) with
+ * theta_e = rope_base^(-2e / head_dim), evaluated in double precision and
+ * rounded to float.  table: device, cb_rope_table_elems() floats.
+ * Errors: CB_ERR_INVALID_ARG for NULL table, head_dim odd or <= 0,
+ * max_positions <= 0. */
+cb_status cb_rope_table_init(float *table, int max_positions, int head_dim,
+                             float rope_base, cb_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* Primitives of the hot path                                               */
+/* ------------------------------------------------------------------------ */
+
+/* One cached chunk to place into a request's cache ([QCF] Eq. 4). */
+typedef struct {
+  const void *k_src;         /* device: layer l, chunk row t at
+                                k_src + l * src_layer_stride + t * row_elems */
+  const void *v_src;         /* device, same layout as k_src                 */
+  int64_t src_layer_stride;  /* elements between consecutive layers          */
+  int len;                   /* rows in the chunk                            */
+  int dst_row;               /* first destination row in the cache           */
+  int delta;                 /* rotation to apply: request offset of the
+                                chunk minus the position its keys were
+                                computed at (0 for a standalone prefill)     */
+} cb_stitch_desc;
+
+/* Pi_i of [QCF] Eq. 4 for every chunk and every layer in
+ * [layer_begin, layer_end): keys stored at chunk-local positions t are
+ * rotated by delta (rotate-half pairs (e, e + head_dim/2), angle
+ * delta * theta_e, [CB] "Why You Can't Just Concatenate": RoPE rotations
+ * compose), values are copied unchanged:
+ *   k_cache[l][dst_row + t] = R(delta) k_src[l][t]
+ *   v_cache[l][dst_row + t] = v_src[l][t]
+ * descs: host array of n_desc descriptors (any n_desc >= 0).
+ * k_cache / v_cache: device, layer l at k_cache + l * cache_layer_stride.
+ * rope_table: device table from cb_rope_table_init with
+ *   max_positions > every |delta|.
+ * Errors: CB_ERR_INVALID_ARG for NULL pointers, |delta| >= max_positions,
+ *   head_dim not dividing row_elems, head_dim % 16 != 0, misalignment. */
+cb_status cb_rope_reposition(const cb_stitch_desc *descs, int n_desc,
+                             int layer_begin, int layer_end, void *k_cache,
+                             void *v_cache, int64_t cache_layer_stride,
+                             int row_elems, int head_dim,
+                             const float *rope_table, int max_positions,
+                             cb_dtype dtype, cb_stream stream);
+
+/* One request of a selection call. */
+typedef struct {
+  int n_ctx;                 /* reusable context tokens N of the request     */
+  int k;                     /* tokens to select, 0 <= k <= n_ctx            */
+  int64_t fresh_row0;        /* row of context token 0 in k_fresh            */
+  int64_t reused_row0;       /* row of context token 0 in k_reused           */
+  int dev_offset;            /* first entry of this request in dev_out       */
+  int idx_offset;            /* first entry of this request in idx_out       */
+  int n_spans;               /* CB_POLICY_DOC_ALIGNED: number of spans       */
+  const int32_t *span_offsets; /* host [n_spans + 1], ascending, from 0 to
+                                  n_ctx: span j = [off[j], off[j+1])         */
+} cb_select_req;
+
+/* Deviation and selection ([ROM] §2.2 Eqs. 1-2, §2.3 Eq. 3; [CB]
+ * "Quantifying the Damage").  For every request b and context token i:
+ *   d_i = sum_c (k_fresh[fresh_row0 + i][c] - k_reused[reused_row0 + i][c])^2
+ * over the row_elems columns (all kv heads), computed in fp32, written to
+ * dev_out[dev_offset + i].  Then the request's k tokens are selected:
+ *   CB_POLICY_TOKEN_TOPK  -- the k largest d_i; equal values rank the lower
+ *                            index first;
+ *   CB_POLICY_DOC_ALIGNED -- spans ranked by mean d (ties: lower span),
+ *                            whole spans while they fit, then the window of
+ *                            the remaining length with the largest total d
+ *                            (ties: leftmost) in the first span that does
+ *                            not fit; span sums are accumulated in double.
+ * The selected context indices are written ascending to
+ * idx_out[idx_offset .. idx_offset + k).
+ * k_fresh, k_reused: device [rows][ld] of dtype.  dev_out: device float.
+ * idx_out: device int32.  ws: device workspace of at least
+ * cb_select_workspace_size(n_req) bytes.
+ * Errors: CB_ERR_INVALID_ARG (n_req > CB_MAX_BATCH, k > n_ctx, spans not
+ *   covering [0, n_ctx] ascending, total spans > CB_MAX_SPANS),
+ *   CB_ERR_WORKSPACE. */
+size_t cb_select_workspace_size(int n_req);
+cb_status cb_kv_deviation_topk(const void *k_fresh, int64_t ld_fresh,
+                               const void *k_reused, int64_t ld_reused,
+                               int row_elems, cb_dtype dtype,
+                               const cb_select_req *reqs, int n_req,
+                               cb_policy policy, float *dev_out,
+                               int32_t *idx_out, void *ws, size_t ws_bytes,
+                               cb_stream stream);
+
+/* Row gather ([CB] blend_layer step 1, h[hkvd_idx]):
+ *   dst[i * ld_dst + c] = src[idx[i] * ld_src + c], i < n, c < row_elems.
+ * idx: device int32 [n]; every idx[i] must lie in [0, src_rows); an index
+ * outside records CB_ERR_DEVICE_INDEX and its row is skipped.
+ * dtype applies to src and dst (CB_F32 or CB_BF16). */
+cb_status cb_gather_rows(const void *src, int64_t ld_src, int64_t src_rows,
+                         const int32_t *idx, int n, int row_elems, void *dst,
+                         int64_t ld_dst, cb_dtype dtype, cb_stream stream);
+
+/* Scatter of fresh K/V rows over the reused cache ([CB] blend_layer step 3;
+ * [QCF] Eq. 7):
+ *   k_cache[rows[i]] = k_new[i],  v_cache[rows[i]] = v_new[i],  i < n.
+ * rows: device int32 [n], distinct, each in [0, cache_rows); an index outside
+ * records CB_ERR_DEVICE_INDEX and is skipped. */
+cb_status cb_scatter_kv(const void *k_new, const void *v_new, int64_t ld_new,
+                        const int32_t *rows, int n, void *k_cache,
+                        void *v_cache, int64_t ld_cache, int64_t cache_rows,
+                        int row_elems, cb_dtype dtype, cb_stream stream);
+
+/* One request of an attention call. */
+typedef struct {
+  int q_begin, q_end;   /* query rows [q_begin, q_end) of q / q_pos / out   */
+  int64_t kv_row0;      /* cache row of position 0 of this request          */
+  int kv_len;           /* positions of this request present in the cache   */
+} cb_attn_req;
+
+/* Selected-query attention over the blended cache ([CB] blend_layer step 4,
+ * n_sel x L work; [QCF] §2.1.3: causal over the partially fused prefix).
+ * For query row r of request b at position p = q_pos[r] (0 <= p < kv_len)
+ * and q head h (kv head g = h / (n_q_heads / n_kv_heads)):
+ *   out[r][h] = sum_{j<=p} softmax_j(scale * q[r][h] . K[j][g]) V[j][g]
+ * with K[j] = k_cache[kv_row0 + j].  Queries of a request must have
+ * ascending positions.  q, out: device [rows][ld] (n_q_heads * head_dim
+ * columns); k_cache, v_cache: device [rows][ld_kv].  dtype applies to q,
+ * the cache and out.  Errors: CB_ERR_INVALID_ARG (n_req > CB_MAX_BATCH,
+ * head counts not dividing, head_dim not 64 or 128); a position outside
+ * [0, kv_len) records CB_ERR_DEVICE_INDEX and the row is left unwritten. */
+cb_status cb_sparse_query_attention(const void *q, int64_t ld_q,
+                                    const int32_t *q_pos,
+                                    const cb_attn_req *reqs, int n_req,
+                                    const void *k_cache, const void *v_cache,
+                                    int64_t ld_kv, int n_q_heads,
+                                    int n_kv_heads, int head_dim, float scale,
+                                    void *out, int64_t ld_out, cb_dtype dtype,
+                                    cb_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* Model                                                                    */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  int n_layers, d_model, n_q_heads, n_kv_heads, head_dim, d_ffn, vocab;
+  float rope_base;      /* theta base of the rotary embedding               */
+  float norm_eps;       /* RMSNorm epsilon                                   */
+  cb_dtype dtype;       /* weights, activations fed to GEMMs, KV cache      */
+  int max_positions;    /* rows of rope_table; > every position used        */
+} cb_model_config;
+
+/* Device pointers of one decoder layer (pre-norm, no biases):
+ *   w_qkv  [(n_q_heads + 2 n_kv_heads) head_dim][d_model]  rows: W_q;W_k;W_v
+ *   w_o    [d_model][n_q_heads head_dim]
+ *   w_gate [d_ffn][d_model],  w_up [d_ffn][d_model]
+ *   w_down [d_model][d_ffn]
+ *   norm1, norm2: float [d_model] RMSNorm gains. */
+typedef struct {
+  const void *w_qkv, *w_o, *w_gate, *w_up, *w_down;
+  const float *norm1, *norm2;
+} cb_layer_weights;
+
+typedef struct {
+  const void *embed;              /* [vocab][d_model]; also the LM head     */
+  const float *final_norm;        /* [d_model]                               */
+  const cb_layer_weights *layers; /* host array [n_layers], copied           */
+  const float *rope_table;        /* device, from cb_rope_table_init         */
+} cb_weights;
+
+typedef struct cb_model cb_model;
+
+/* Records the configuration and weight pointers (no device memory is
+ * allocated or copied; the weights must outlive the model).  Errors:
+ * CB_ERR_INVALID_ARG for inconsistent shapes or NULL weights,
+ * CB_ERR_UNSUPPORTED for head_dim not 64/128, d_model % 64, d_ffn % 64,
+ * or a device older than sm_103 for CB_BF16. */
+cb_status cb_model_create(const cb_model_config *cfg, const cb_weights *w,
+                          cb_model **out);
+void cb_model_destroy(cb_model *m);
+
+/* ------------------------------------------------------------------------ */
+/* Layer and stack                                                          */
+/* ------------------------------------------------------------------------ */
+
+/* Dense projection with a fused epilogue, out = f(A W^T):
+ *   A [M][K] (ld_a), W [N][K] (ld_w) device, dtype of the model.
+ *   CB_EPI_STORE   out[m][n] = acc             (out: dtype, ld_out)
+ *   CB_EPI_RESID   out[m][n] += acc            (out: float residual stream)
+ *   CB_EPI_SWIGLU  out[m][n] = silu(acc_g) * acc_u, with acc_g from W rows
+ *                  and acc_u from W2 rows (W2 [N][K], same ld)
+ * Errors: CB_ERR_INVALID_ARG for shapes not multiples of 16 in K, NULLs. */
+typedef enum { CB_EPI_STORE = 0, CB_EPI_RESID = 1, CB_EPI_SWIGLU = 2 } cb_epilogue;
+cb_status cb_linear(const cb_model *m, const void *A, int64_t ld_a,
+                    const void *W, const void *W2, int64_t ld_w, int M, int N,
+                    int K, cb_epilogue epi, void *out, int64_t ld_out,
+                    cb_stream stream);
+
+/* A run of request tokens: cached (k_pic != NULL) or recomputed at every
+ * layer (k_pic == NULL: the user query U, or a document that has no cache
+ * yet).  All cached segments of a request come before its uncached ones;
+ * the N cached tokens are the reusable context C of [QCF] Eq. 1. */
+typedef struct {
+  int len;
+  const void *k_pic;        /* device [n_layers] x [len rows], layer l at
+                               k_pic + l * pic_layer_stride; keys computed
+                               standalone at positions pic_pos0 ..          */
+  const void *v_pic;
+  int64_t pic_layer_stride; /* elements between layers of the PIC cache   */
+  int pic_pos0;             /* position the chunk's keys were computed at
+                               (0 for a standalone chunk prefill)           */
+} cb_segment;
+
+typedef struct {
+  const int32_t *tokens;        /* device int32 [T], T = sum of lens        */
+  const cb_segment *segments;   /* host [n_segments]                         */
+  int n_segments;
+} cb_request;
+
+typedef struct {
+  int layer;  /* > sel_layer */
+  int keep;   /* rows of the current selection kept from this layer on       */
+} cb_schedule_step;
+
+typedef struct {
+  int ratio_bp;        /* recompute ratio r in basis points (1500 = 15%)    */
+  cb_policy policy;
+  int sel_layer;       /* selection layer s; layers < s run on every row    */
+  int n_schedule;      /* gradual filtering steps ([CB] select_hkvd), 0 = a
+                          single selection reused by every later layer     */
+  const cb_schedule_step *schedule;   /* host [n_schedule], layers ascending */
+  const int32_t *forced_selected;     /* device [K_total] or NULL: use these
+                          request-local context positions (ascending per
+                          request, k_b of them) instead of ranking d; d is
+                          still computed.  Lets an external selector (or a
+                          reference run) fix P.  A position outside
+                          [0, N_b) records CB_ERR_DEVICE_INDEX.            */
+} cb_blend_params;
+
+/* Outputs of a prefill call.  The fused cache of request b occupies rows
+ * [t_off_b, t_off_b + T_b) of every layer, t_off_b = sum_{c<b} T_c. */
+typedef struct {
+  void *k_cache, *v_cache;   /* device; layer l at + l * cache_layer_stride */
+  int64_t cache_layer_stride;/* elements; 0 means T_total * row_elems       */
+  float *deviation;          /* device [N_total] or NULL (d at layer s)     */
+  int32_t *selected;         /* device [K_total] or NULL: request-local
+                                context positions, ascending per request    */
+  float *hidden;             /* device [R_total][d_model] or NULL: final
+                                hidden states (before the final norm) of the
+                                rows computed at the last layer             */
+  int32_t *rows;             /* device [R_total] or NULL: request-local
+                                positions of those rows, ascending per
+                                request                                      */
+  int32_t *first_token;      /* device [B] or NULL: argmax of the last row's
+                                logits (LM head tied to the embedding)      */
+} cb_blend_out;
+
+typedef struct {
+  int64_t T_total;           /* rows of the fused cache (all requests)      */
+  int64_t N_total;           /* reusable context tokens                     */
+  int64_t K_total;           /* selected context tokens                     */
+  int64_t R_total;           /* rows computed at the last layer             */
+  size_t workspace_bytes;    /* workspace for cb_blend_prefill / full      */
+} cb_plan;
+
+/* Sizes of a blended prefill.  k_b = floor(N_b * ratio_bp / 10000), at
+ * least 1 when ratio_bp > 0 and N_b > 0 ([ROM] Eq. 2). */
+cb_status cb_blend_plan(const cb_model *m, const cb_request *reqs, int B,
+                        const cb_blend_params *p, cb_plan *out);
+
+/* Blended prefill of B independent requests ([QCF] §2.1.3 Eqs. 4-7; [CB]
+ * blend_layer; [ROM] §2.2 flow):
+ *   1. stitch: every cached segment is re-positioned into the fused cache
+ *      at layers >= sel_layer (cb_rope_reposition);
+ *   2. layers < sel_layer run on every row (their cache is fresh);
+ *   3. at sel_layer every row's keys are projected fresh, d is ranked
+ *      (cb_kv_deviation_topk) and the selected context rows plus all
+ *      uncached rows form the computed set;
+ *   4. layers >= sel_layer compute only that set: fresh K/V replace the
+ *      reused rows (Eq. 7) and the set attends over the fused cache;
+ *   5. final norm + LM head + argmax of each request's last row.
+ * Every step runs in this library's kernels on `stream`; nothing is
+ * synchronised.  ws: device workspace of >= cb_plan.workspace_bytes.
+ * Errors: CB_ERR_INVALID_ARG (B > CB_MAX_BATCH, a request whose cached
+ *   segments do not all precede its uncached ones, a request that ends in
+ *   a cached segment, positions >= max_positions), CB_ERR_WORKSPACE. */
+cb_status cb_blend_prefill(cb_model *m, const cb_request *reqs, int B,
+                           const cb_blend_params *p, const cb_blend_out *out,
+                           void *ws, size_t ws_bytes, cb_stream stream);
+
+/* Full prefill ([QCF] Eq. 2): every row of every layer is computed under
+ * the whole request (segments' caches are ignored).  Fills k_cache,
+ * v_cache, hidden (all T rows), rows (0..T_b-1) and first_token of `out`.
+ * A standalone chunk prefill ([QCF] Eq. 3) is a full prefill of a request
+ * holding just the chunk's tokens.  Workspace: cb_full_plan. */
+cb_status cb_full_plan(const cb_model *m, const cb_request *reqs, int B,
+                       cb_plan *out);
+cb_status cb_full_prefill(cb_model *m, const cb_request *reqs, int B,
+                          const cb_blend_out *out, void *ws, size_t ws_bytes,
+                          cb_stream stream);
+
+/* One blended decoder layer on a compact set of rows ([CB] blend_layer
+ * with hidden states kept compact):
+ *   x = RMSNorm(h; norm1); q, k, v = x W_qkv^T with RoPE on q and k at
+ *   pos[i]; k, v written to cache row cache_row[i] (Eq. 7); the rows attend
+ *   over the layer's cache; h += attn W_o^T; h += SwiGLU(RMSNorm(h)) W_down^T.
+ * h: device float [n_rows][d_model], updated in place.  pos, cache_row:
+ * device int32 [n_rows], ascending per request.  reqs: host, one per
+ * request (q_begin/q_end index h rows).  k_cache, v_cache: device, this
+ * layer's cache [rows][n_kv_heads * head_dim].  ws: device workspace of at
+ * least cb_layer_workspace_size(m, n_rows) bytes. */
+size_t cb_layer_workspace_size(const cb_model *m, int n_rows);
+cb_status cb_blend_layer(cb_model *m, int layer, float *h, int n_rows,
+                         const int32_t *pos, const int32_t *cache_row,
+                         const cb_attn_req *reqs, int n_req, void *k_cache,
+                         void *v_cache, void *ws, size_t ws_bytes,
+                         cb_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CACHEBLEND_H_ */

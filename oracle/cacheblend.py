@@ -45,7 +45,8 @@ __all__ = [
     "reposition_keys", "stitch", "rms_norm", "silu", "causal_attention",
     "decoder_layer", "full_prefill", "chunk_prefill", "kv_deviation",
     "select_count", "token_topk", "doc_aligned_select", "blend_prefill",
-    "first_token", "kv_bytes_per_layer", "BlendResult", "PrefillResult",
+    "first_token", "first_token_logits", "embed_rows", "kv_bytes_per_layer",
+    "BlendResult", "PrefillResult",
 ]
 
 
@@ -69,13 +70,21 @@ class Model:
 
 
 def model_from_weights(shape, weights) -> Model:
-    """Wrap generator output (float32 arrays) as float64 arrays."""
+    """Wrap generator output (float32 arrays) as float64 arrays.  The
+    embedding stays in its given (exact) float32 form and is widened to
+    float64 row by row where it is used, so a 128K-entry vocabulary does not
+    need a float64 copy."""
     f = lambda a: np.asarray(a, dtype=np.float64)
     layers = [{k: f(v) for k, v in lw.items()} for lw in weights["layers"]]
     return Model(shape.n_layers, shape.d_model, shape.n_q_heads,
                  shape.n_kv_heads, shape.head_dim, shape.d_ffn, shape.vocab,
                  float(shape.rope_base), float(shape.norm_eps),
-                 f(weights["embed"]), f(weights["final_norm"]), layers)
+                 weights["embed"], f(weights["final_norm"]), layers)
+
+
+def embed_rows(m: Model, tokens) -> np.ndarray:
+    """h = E[tokens] as float64 (the embedding lookup)."""
+    return np.asarray(m.embed[np.asarray(tokens)], dtype=np.float64)
 
 
 # --------------------------------------------------------------------------
@@ -216,8 +225,18 @@ def first_token(m: Model, h_last: np.ndarray) -> int:
     """argmax over the vocabulary of RMSNorm(h_last) E^T (LM head tied to
     the embedding); the first generated token that ends TTFT (QCFuse
     §4.1.5).  Ties resolve to the lowest id."""
-    logits = rms_norm(h_last[None, :], m.final_norm, m.norm_eps)[0] @ m.embed.T
+    logits = first_token_logits(m, h_last)
     return int(np.argmax(logits))
+
+
+def first_token_logits(m: Model, h_last: np.ndarray) -> np.ndarray:
+    """RMSNorm(h_last) E^T in float64 (the embedding is widened in blocks of
+    rows; each logit is still one plain dot product)."""
+    x = rms_norm(h_last[None, :], m.final_norm, m.norm_eps)[0]
+    out = np.empty(m.embed.shape[0])
+    for a in range(0, m.embed.shape[0], 8192):
+        out[a:a + 8192] = np.asarray(m.embed[a:a + 8192], dtype=np.float64) @ x
+    return out
 
 
 # --------------------------------------------------------------------------
@@ -239,7 +258,7 @@ def full_prefill(m: Model, tokens) -> PrefillResult:
     kvw = m.n_kv_heads * m.head_dim
     K = np.zeros((m.n_layers, T, kvw))
     V = np.zeros((m.n_layers, T, kvw))
-    h = m.embed[tokens].copy()
+    h = embed_rows(m, tokens)
     rows = np.arange(T)
     for l in range(m.n_layers):
         h, _, _ = decoder_layer(m, l, h, rows, K[l], V[l], rows)
@@ -398,7 +417,7 @@ def blend_prefill(m: Model, segments, store, ratio_bp: int,
         off += len(t)
 
     pos_all = np.arange(T)
-    h = m.embed[toks].copy()
+    h = embed_rows(m, toks)
     # 3. full layers before the selection layer
     for l in range(min(sel_layer, m.n_layers)):
         h, _, _ = decoder_layer(m, l, h, pos_all, K[l], V[l], pos_all)

@@ -1,0 +1,377 @@
+"""Python face of the C ABI.  Functions keep the C names; they turn torch
+tensors into pointers, sizes and the current CUDA stream and call the
+library.  PyTorch is used only to own device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+from . import _lib as L
+from ._lib import check, lib
+
+__all__ = [
+    "dtype_code", "torch_dtype", "cb_rope_table_init", "cb_rope_reposition",
+    "cb_kv_deviation_topk", "cb_gather_rows", "cb_scatter_kv",
+    "cb_sparse_query_attention", "cb_debug_expire_wait", "Seg", "Req",
+    "BlendModel", "ChunkStore", "select_count", "device_status",
+]
+
+device_status = L.device_status
+
+
+def dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return L.CB_BF16
+    if dt == torch.float32:
+        return L.CB_F32
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+def torch_dtype(name: str) -> torch.dtype:
+    return {"bf16": torch.bfloat16, "f32": torch.float32}[name]
+
+
+def _p(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _s(stream=None):
+    st = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(st.cuda_stream)
+
+
+def select_count(n_ctx: int, ratio_bp: int) -> int:
+    """k = max(1, floor(N r)) for r > 0, 0 for r = 0 (integer basis points)."""
+    if ratio_bp <= 0 or n_ctx <= 0:
+        return 0
+    return max(1, (n_ctx * ratio_bp) // 10000)
+
+
+# ------------------------------------------------------------ primitives --
+def cb_rope_table_init(max_positions: int, head_dim: int, rope_base: float,
+                       device="cuda", stream=None) -> torch.Tensor:
+    n = lib.cb_rope_table_elems(max_positions, head_dim)
+    t = torch.empty(n, dtype=torch.float32, device=device)
+    check(lib.cb_rope_table_init(_p(t), max_positions, head_dim,
+                                 float(rope_base), _s(stream)))
+    return t
+
+
+def cb_rope_reposition(descs, layer_begin, layer_end, k_cache, v_cache,
+                       cache_layer_stride, row_elems, head_dim, rope_table,
+                       max_positions, stream=None):
+    """descs: list of (k_src, v_src, src_layer_stride, len, dst_row, delta)
+    with k_src / v_src torch tensors (their data pointers are used)."""
+    arr = (L.StitchDesc * max(1, len(descs)))()
+    for i, (ks, vs, stride, ln, dst, delta) in enumerate(descs):
+        arr[i] = L.StitchDesc(ks.data_ptr(), vs.data_ptr(), stride, ln, dst, delta)
+    check(lib.cb_rope_reposition(arr, len(descs), layer_begin, layer_end,
+                                 _p(k_cache), _p(v_cache), cache_layer_stride,
+                                 row_elems, head_dim, _p(rope_table),
+                                 max_positions, dtype_code(k_cache.dtype),
+                                 _s(stream)))
+
+
+def cb_kv_deviation_topk(k_fresh, k_reused, reqs, policy, dev_out, idx_out,
+                         ws=None, stream=None):
+    """reqs: list of dicts with n_ctx, k, fresh_row0, reused_row0,
+    dev_offset, idx_offset and (doc-aligned) span_offsets."""
+    n = len(reqs)
+    arr = (L.SelectReq * max(1, n))()
+    keep = []
+    for i, r in enumerate(reqs):
+        spans = r.get("span_offsets")
+        sp = None
+        ns = 0
+        if spans is not None:
+            a = (C.c_int32 * len(spans))(*[int(x) for x in spans])
+            keep.append(a)
+            sp = C.cast(a, C.POINTER(C.c_int32))
+            ns = len(spans) - 1
+        arr[i] = L.SelectReq(r["n_ctx"], r["k"], r.get("fresh_row0", 0),
+                             r.get("reused_row0", 0), r.get("dev_offset", 0),
+                             r.get("idx_offset", 0), ns, sp)
+    need = lib.cb_select_workspace_size(n)
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=k_fresh.device)
+    check(lib.cb_kv_deviation_topk(
+        _p(k_fresh), k_fresh.stride(0), _p(k_reused), k_reused.stride(0),
+        k_fresh.shape[1], dtype_code(k_fresh.dtype), arr, n, policy,
+        _p(dev_out), _p(idx_out), _p(ws), ws.numel(), _s(stream)))
+
+
+def cb_gather_rows(src, idx, dst, stream=None):
+    check(lib.cb_gather_rows(_p(src), src.stride(0), src.shape[0], _p(idx),
+                             idx.numel(), src.shape[1], _p(dst), dst.stride(0),
+                             dtype_code(src.dtype), _s(stream)))
+
+
+def cb_scatter_kv(k_new, v_new, rows, k_cache, v_cache, stream=None):
+    check(lib.cb_scatter_kv(_p(k_new), _p(v_new), k_new.stride(0), _p(rows),
+                            rows.numel(), _p(k_cache), _p(v_cache),
+                            k_cache.stride(0), k_cache.shape[0], k_new.shape[1],
+                            dtype_code(k_new.dtype), _s(stream)))
+
+
+def _attn_reqs(reqs):
+    arr = (L.AttnReq * max(1, len(reqs)))()
+    for i, (qb, qe, kv0, kvl) in enumerate(reqs):
+        arr[i] = L.AttnReq(qb, qe, kv0, kvl)
+    return arr
+
+
+def cb_sparse_query_attention(q, q_pos, reqs, k_cache, v_cache, n_q_heads,
+                              n_kv_heads, head_dim, out, scale=None,
+                              stream=None):
+    """reqs: list of (q_begin, q_end, kv_row0, kv_len)."""
+    scale = 1.0 / math.sqrt(head_dim) if scale is None else scale
+    check(lib.cb_sparse_query_attention(
+        _p(q), q.stride(0), _p(q_pos), _attn_reqs(reqs), len(reqs),
+        _p(k_cache), _p(v_cache), k_cache.stride(0), n_q_heads, n_kv_heads,
+        head_dim, float(scale), _p(out), out.stride(0), dtype_code(q.dtype),
+        _s(stream)))
+
+
+def cb_debug_expire_wait(limit_us: int, stream=None):
+    check(lib.cb_debug_expire_wait(limit_us, _s(stream)))
+
+
+# ----------------------------------------------------------------- model --
+@dataclass
+class Seg:
+    """A request segment: cached (k_pic/v_pic set) or recomputed."""
+    len: int
+    k_pic: torch.Tensor | None = None     # any tensor whose data_ptr() is
+    v_pic: torch.Tensor | None = None     # the PIC base of this segment
+    pic_layer_stride: int = 0
+    pic_pos0: int = 0
+
+
+@dataclass
+class Req:
+    tokens: torch.Tensor                  # device int32 [T]
+    segs: list = field(default_factory=list)
+
+
+def _requests(reqs):
+    arr = (L.Request * len(reqs))()
+    keep = []
+    for i, r in enumerate(reqs):
+        sa = (L.Segment * len(r.segs))()
+        for j, s in enumerate(r.segs):
+            sa[j] = L.Segment(s.len, None if s.k_pic is None else s.k_pic.data_ptr(),
+                              None if s.v_pic is None else s.v_pic.data_ptr(),
+                              s.pic_layer_stride, s.pic_pos0)
+        keep.append(sa)
+        arr[i] = L.Request(r.tokens.data_ptr(), C.cast(sa, C.POINTER(L.Segment)),
+                           len(r.segs))
+    return arr, keep
+
+
+class BlendModel:
+    """Device-resident weights plus the library's model handle."""
+
+    def __init__(self, shape, dev_weights: dict, max_positions: int,
+                 device="cuda"):
+        self.shape = shape
+        self.device = torch.device(device)
+        self.dtype = torch_dtype(shape.dtype)
+        self.w = dev_weights
+        self.max_positions = max_positions
+        self.rope_table = cb_rope_table_init(max_positions, shape.head_dim,
+                                             shape.rope_base, device)
+        cfg = L.ModelConfig(shape.n_layers, shape.d_model, shape.n_q_heads,
+                            shape.n_kv_heads, shape.head_dim, shape.d_ffn,
+                            shape.vocab, shape.rope_base, shape.norm_eps,
+                            dtype_code(self.dtype), max_positions)
+        self._layers = (L.LayerWeights * shape.n_layers)()
+        for l, lw in enumerate(dev_weights["layers"]):
+            self._layers[l] = L.LayerWeights(
+                lw["w_qkv"].data_ptr(), lw["w_o"].data_ptr(),
+                lw["w_gate"].data_ptr(), lw["w_up"].data_ptr(),
+                lw["w_down"].data_ptr(), lw["norm1"].data_ptr(),
+                lw["norm2"].data_ptr())
+        wts = L.Weights(dev_weights["embed"].data_ptr(),
+                        dev_weights["final_norm"].data_ptr(),
+                        C.cast(self._layers, C.POINTER(L.LayerWeights)),
+                        self.rope_table.data_ptr())
+        h = C.c_void_p()
+        check(lib.cb_model_create(C.byref(cfg), C.byref(wts), C.byref(h)))
+        self.handle = h
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value:
+            lib.cb_model_destroy(h)
+            self.handle = None
+
+    # -------------------------------------------------------- construction
+    @classmethod
+    def from_host(cls, shape, weights: dict, max_positions: int,
+                  device="cuda"):
+        """Upload generator weights (float32 numpy arrays holding values of
+        the model dtype) to the device."""
+        dt = torch_dtype(shape.dtype)
+        up = lambda a, d=dt: torch.from_numpy(np.ascontiguousarray(a)).to(
+            device=device, dtype=d)
+        dw = {"embed": up(weights["embed"]),
+              "final_norm": up(weights["final_norm"], torch.float32),
+              "layers": []}
+        for lw in weights["layers"]:
+            dw["layers"].append({
+                "w_qkv": up(lw["w_qkv"]), "w_o": up(lw["w_o"]),
+                "w_gate": up(lw["w_gate"]), "w_up": up(lw["w_up"]),
+                "w_down": up(lw["w_down"]),
+                "norm1": up(lw["norm1"], torch.float32),
+                "norm2": up(lw["norm2"], torch.float32)})
+        return cls(shape, dw, max_positions, device)
+
+    @property
+    def kvw(self):
+        return self.shape.n_kv_heads * self.shape.head_dim
+
+    # ------------------------------------------------------------- calls
+    def cb_linear(self, A, W, out, epi=L.CB_EPI_STORE, W2=None, stream=None):
+        M, K = A.shape
+        N = W.shape[0]
+        check(lib.cb_linear(self.handle, _p(A), A.stride(0), _p(W), _p(W2),
+                            W.stride(0), M, N, K, epi, _p(out), out.stride(0),
+                            _s(stream)))
+
+    def cb_blend_layer(self, layer, h, pos, cache_row, reqs, k_cache, v_cache,
+                       ws=None, stream=None):
+        n = h.shape[0]
+        need = lib.cb_layer_workspace_size(self.handle, n)
+        if ws is None:
+            ws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
+        check(lib.cb_blend_layer(self.handle, layer, _p(h), n, _p(pos),
+                                 _p(cache_row), _attn_reqs(reqs), len(reqs),
+                                 _p(k_cache), _p(v_cache), _p(ws), ws.numel(),
+                                 _s(stream)))
+
+    def _params(self, ratio_bp, policy, sel_layer, schedule, forced=None):
+        n = len(schedule or [])
+        sch = (L.ScheduleStep * max(1, n))()
+        for i, (l, k) in enumerate(schedule or []):
+            sch[i] = L.ScheduleStep(l, k)
+        return L.BlendParams(ratio_bp, policy, sel_layer, n,
+                             C.cast(sch, C.POINTER(L.ScheduleStep)),
+                             None if forced is None else forced.data_ptr()), sch
+
+    def plan(self, reqs, ratio_bp=None, policy=0, sel_layer=1, schedule=None):
+        arr, keep = _requests(reqs)
+        out = L.Plan()
+        if ratio_bp is None:
+            check(lib.cb_full_plan(self.handle, arr, len(reqs), C.byref(out)))
+        else:
+            p, sch = self._params(ratio_bp, policy, sel_layer, schedule)
+            check(lib.cb_blend_plan(self.handle, arr, len(reqs), C.byref(p),
+                                    C.byref(out)))
+        return out
+
+    def alloc_outputs(self, plan, B, blend=True):
+        s = self.shape
+        dev, dt = self.device, self.dtype
+        T, N, K, R = plan.T_total, plan.N_total, plan.K_total, plan.R_total
+        return {
+            "k_cache": torch.empty(s.n_layers, T, self.kvw, dtype=dt, device=dev),
+            "v_cache": torch.empty(s.n_layers, T, self.kvw, dtype=dt, device=dev),
+            "deviation": torch.empty(max(N, 1), dtype=torch.float32, device=dev) if blend else None,
+            "selected": torch.empty(max(K, 1), dtype=torch.int32, device=dev) if blend else None,
+            "hidden": torch.empty(max(R, 1), s.d_model, dtype=torch.float32, device=dev),
+            "rows": torch.empty(max(R, 1), dtype=torch.int32, device=dev),
+            "first_token": torch.empty(B, dtype=torch.int32, device=dev),
+            "workspace": torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev),
+        }
+
+    def _out(self, o, layer_stride=0):
+        return L.BlendOut(o["k_cache"].data_ptr(), o["v_cache"].data_ptr(),
+                          layer_stride,
+                          None if o.get("deviation") is None else o["deviation"].data_ptr(),
+                          None if o.get("selected") is None else o["selected"].data_ptr(),
+                          None if o.get("hidden") is None else o["hidden"].data_ptr(),
+                          None if o.get("rows") is None else o["rows"].data_ptr(),
+                          None if o.get("first_token") is None else o["first_token"].data_ptr())
+
+    def cb_blend_prefill(self, reqs, ratio_bp, policy=0, sel_layer=1,
+                         schedule=None, outputs=None, forced=None,
+                         stream=None):
+        """forced: optional device int32 tensor of selected context
+        positions (ascending per request) used instead of the ranking."""
+        arr, keep = _requests(reqs)
+        p, sch = self._params(ratio_bp, policy, sel_layer, schedule, forced)
+        if outputs is None:
+            plan = L.Plan()
+            check(lib.cb_blend_plan(self.handle, arr, len(reqs), C.byref(p),
+                                    C.byref(plan)))
+            outputs = self.alloc_outputs(plan, len(reqs))
+        o = self._out(outputs)
+        ws = outputs["workspace"]
+        check(lib.cb_blend_prefill(self.handle, arr, len(reqs), C.byref(p),
+                                   C.byref(o), _p(ws), ws.numel(), _s(stream)))
+        return outputs
+
+    def cb_full_prefill(self, reqs, outputs=None, layer_stride=0, stream=None):
+        arr, keep = _requests(reqs)
+        if outputs is None:
+            plan = L.Plan()
+            check(lib.cb_full_plan(self.handle, arr, len(reqs), C.byref(plan)))
+            outputs = self.alloc_outputs(plan, len(reqs), blend=False)
+        o = self._out(outputs, layer_stride)
+        ws = outputs["workspace"]
+        check(lib.cb_full_prefill(self.handle, arr, len(reqs), C.byref(o),
+                                  _p(ws), ws.numel(), _s(stream)))
+        return outputs
+
+
+class ChunkStore:
+    """Per-chunk PIC caches kept in one device pool [n_layers][rows][kvw]
+    (QCFuse Eq. 3: each chunk prefilled alone at positions 0..|c|-1)."""
+
+    def __init__(self, model: BlendModel, capacity_rows: int):
+        s = model.shape
+        self.model = model
+        self.capacity = capacity_rows
+        self.K = torch.empty(s.n_layers, capacity_rows, model.kvw,
+                             dtype=model.dtype, device=model.device)
+        self.V = torch.empty_like(self.K)
+        self.where = {}       # chunk id -> (row, len)
+        self.used = 0
+
+    def prefill(self, chunks: dict, stream=None):
+        """chunks: {chunk_id: device int32 token tensor}; prefilled as one
+        batch of standalone requests into consecutive pool rows."""
+        items = list(chunks.items())
+        for i in range(0, len(items), L.CB_MAX_BATCH):
+            part = items[i:i + L.CB_MAX_BATCH]
+            n = sum(int(t.numel()) for _, t in part)
+            if self.used + n > self.capacity:
+                raise RuntimeError("chunk store is full")
+            reqs = [Req(t, [Seg(int(t.numel()))]) for _, t in part]
+            plan = self.model.plan(reqs)
+            dev = self.model.device
+            row0 = self.used
+            outs = {
+                "k_cache": self.K[:, row0:],
+                "v_cache": self.V[:, row0:],
+                "hidden": None, "rows": None, "first_token": None,
+                "workspace": torch.empty(max(plan.workspace_bytes, 256),
+                                         dtype=torch.uint8, device=dev),
+            }
+            self.model.cb_full_prefill(reqs, outs,
+                                       layer_stride=self.capacity * self.model.kvw,
+                                       stream=stream)
+            r = row0
+            for cid, t in part:
+                self.where[cid] = (r, int(t.numel()))
+                r += int(t.numel())
+            self.used = r
+
+    def seg(self, cid) -> Seg:
+        r, n = self.where[cid]
+        return Seg(n, self.K[0, r], self.V[0, r], self.capacity * self.model.kvw, 0)

@@ -1,0 +1,813 @@
+// C ABI of the blended-prefill library: argument validation, the device
+// status word, workspace planning and the layer / stack orchestration.  All
+// arithmetic of the path runs in the kernels of the k_*.cu files; this file
+// only enqueues them.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "cb_common.cuh"
+#include "cb_internal.h"
+
+using namespace cb;
+
+// ------------------------------------------------------------------ errors --
+static thread_local std::string g_msg;
+
+static cb_status fail(cb_status s, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_msg = buf;
+  return s;
+}
+
+#define CB_CUDA(expr)                                                        \
+  do {                                                                       \
+    cudaError_t e_ = (expr);                                                 \
+    if (e_ != cudaSuccess)                                                   \
+      return fail(CB_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_)); \
+  } while (0)
+
+#define CB_TRY(expr)                  \
+  do {                                \
+    cb_status s_ = (expr);            \
+    if (s_ != CB_OK) return s_;       \
+  } while (0)
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+static size_t dtype_bytes(cb_dtype d) { return d == CB_BF16 ? 2 : 4; }
+
+extern "C" const char *cb_last_error_message(void) { return g_msg.c_str(); }
+extern "C" int cb_version(void) { return 100; }
+
+// --------------------------------------------------------- launch counter --
+#include <atomic>
+static std::atomic<unsigned long long> g_launches{0};
+void cb::note_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
+extern "C" unsigned long long cb_debug_launch_count(void) { return g_launches.load(); }
+
+// ----------------------------------------------------------- status word --
+static __device__ int g_status_word;
+
+namespace cb {
+int *device_status_ptr() {
+  static std::mutex mu;
+  static int *ptrs[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ptrs[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = (int *)p;
+  }
+  return ptrs[dev];
+}
+}  // namespace cb
+
+static cb_status status_ptr(int **out) {
+  *out = device_status_ptr();
+  if (!*out) return fail(CB_ERR_CUDA, "cannot resolve the device status word");
+  return CB_OK;
+}
+
+extern "C" cb_status cb_get_device_status(cb_status *out) {
+  if (!out) return fail(CB_ERR_INVALID_ARG, "out is NULL");
+  CB_CUDA(cudaDeviceSynchronize());
+  int v = 0;
+  CB_CUDA(cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)));
+  const int zero = 0;
+  CB_CUDA(cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)));
+  *out = (cb_status)v;
+  return CB_OK;
+}
+
+extern "C" cb_status cb_debug_expire_wait(int limit_us, cb_stream stream) {
+  if (limit_us < 0 || limit_us > 1000000)
+    return fail(CB_ERR_INVALID_ARG, "limit_us must be in [0, 1e6]");
+  int *st;
+  CB_TRY(status_ptr(&st));
+  CB_CUDA(launch_expire_wait(limit_us, st, stream));
+  return CB_OK;
+}
+
+// ------------------------------------------------------------- RoPE table --
+extern "C" size_t cb_rope_table_elems(int max_positions, int head_dim) {
+  if (max_positions <= 0 || head_dim <= 0) return 0;
+  return (size_t)max_positions * (head_dim / 2) * 2;
+}
+
+extern "C" cb_status cb_rope_table_init(float *table, int max_positions,
+                                        int head_dim, float rope_base,
+                                        cb_stream stream) {
+  if (!table) return fail(CB_ERR_INVALID_ARG, "table is NULL");
+  if (head_dim <= 0 || head_dim % 2) return fail(CB_ERR_INVALID_ARG, "head_dim must be even and > 0");
+  if (max_positions <= 0) return fail(CB_ERR_INVALID_ARG, "max_positions must be > 0");
+  if (!(rope_base > 1.f)) return fail(CB_ERR_INVALID_ARG, "rope_base must be > 1");
+  CB_CUDA(launch_rope_table(table, max_positions, head_dim, rope_base, stream));
+  return CB_OK;
+}
+
+// ---------------------------------------------------------- reposition --
+static cb_status check_kv_geometry(int row_elems, int head_dim, cb_dtype dt) {
+  if (dt != CB_F32 && dt != CB_BF16) return fail(CB_ERR_INVALID_ARG, "bad dtype");
+  if (head_dim <= 0 || head_dim % 16) return fail(CB_ERR_INVALID_ARG, "head_dim must be a positive multiple of 16");
+  if (row_elems <= 0 || row_elems % head_dim) return fail(CB_ERR_INVALID_ARG, "row_elems must be a multiple of head_dim");
+  return CB_OK;
+}
+
+extern "C" cb_status cb_rope_reposition(const cb_stitch_desc *descs, int n_desc,
+                                        int layer_begin, int layer_end,
+                                        void *k_cache, void *v_cache,
+                                        int64_t cache_layer_stride,
+                                        int row_elems, int head_dim,
+                                        const float *rope_table,
+                                        int max_positions, cb_dtype dtype,
+                                        cb_stream stream) {
+  if (n_desc < 0 || (n_desc > 0 && !descs)) return fail(CB_ERR_INVALID_ARG, "descs");
+  if (layer_begin < 0 || layer_end < layer_begin) return fail(CB_ERR_INVALID_ARG, "layer range");
+  if (!k_cache || !v_cache || !rope_table) return fail(CB_ERR_INVALID_ARG, "NULL cache or table");
+  CB_TRY(check_kv_geometry(row_elems, head_dim, dtype));
+  const size_t eb = dtype_bytes(dtype);
+  if (!aligned16(k_cache) || !aligned16(v_cache) || (cache_layer_stride * eb) % 16)
+    return fail(CB_ERR_INVALID_ARG, "cache pointers / layer stride must be 16-byte aligned");
+  for (int i = 0; i < n_desc; ++i) {
+    const cb_stitch_desc &d = descs[i];
+    if (d.len < 0 || d.dst_row < 0) return fail(CB_ERR_INVALID_ARG, "desc %d: negative len/dst_row", i);
+    if (d.len == 0) continue;
+    if (!d.k_src || !d.v_src || !aligned16(d.k_src) || !aligned16(d.v_src) ||
+        (d.src_layer_stride * eb) % 16)
+      return fail(CB_ERR_INVALID_ARG, "desc %d: NULL or misaligned source", i);
+    if (d.delta >= max_positions || -d.delta >= max_positions)
+      return fail(CB_ERR_INVALID_ARG, "desc %d: |delta| %d >= max_positions %d", i, d.delta, max_positions);
+  }
+  int *st;
+  CB_TRY(status_ptr(&st));
+  CB_CUDA(launch_reposition(descs, n_desc, layer_begin, layer_end, k_cache, v_cache,
+                            cache_layer_stride, row_elems, head_dim, rope_table,
+                            dtype, st, stream));
+  return CB_OK;
+}
+
+// -------------------------------------------------------------- selection --
+extern "C" size_t cb_select_workspace_size(int n_req) { return select_ws_bytes(n_req); }
+
+static cb_status to_sel_reqs(const cb_select_req *reqs, int n_req, cb_policy policy,
+                             std::vector<SelReq> &out, std::vector<int32_t> &spans) {
+  if (n_req < 0 || n_req > CB_MAX_BATCH) return fail(CB_ERR_INVALID_ARG, "n_req must be in [0, %d]", CB_MAX_BATCH);
+  if (n_req > 0 && !reqs) return fail(CB_ERR_INVALID_ARG, "reqs is NULL");
+  if (policy != CB_POLICY_TOKEN_TOPK && policy != CB_POLICY_DOC_ALIGNED)
+    return fail(CB_ERR_INVALID_ARG, "unknown policy %d", (int)policy);
+  out.resize(n_req);
+  for (int i = 0; i < n_req; ++i) {
+    const cb_select_req &r = reqs[i];
+    if (r.n_ctx < 0 || r.k < 0 || r.k > r.n_ctx) return fail(CB_ERR_INVALID_ARG, "req %d: need 0 <= k <= n_ctx", i);
+    if (r.fresh_row0 < 0 || r.reused_row0 < 0 || r.dev_offset < 0 || r.idx_offset < 0)
+      return fail(CB_ERR_INVALID_ARG, "req %d: negative offset", i);
+    SelReq s{r.n_ctx, r.k, r.fresh_row0, r.reused_row0, r.dev_offset, r.idx_offset, 0, 0};
+    if (policy == CB_POLICY_DOC_ALIGNED && r.k > 0) {
+      if (r.n_spans < 1 || !r.span_offsets) return fail(CB_ERR_INVALID_ARG, "req %d: doc-aligned needs spans", i);
+      if (r.span_offsets[0] != 0 || r.span_offsets[r.n_spans] != r.n_ctx)
+        return fail(CB_ERR_INVALID_ARG, "req %d: spans must cover [0, n_ctx]", i);
+      for (int j = 0; j < r.n_spans; ++j)
+        if (r.span_offsets[j + 1] < r.span_offsets[j]) return fail(CB_ERR_INVALID_ARG, "req %d: spans not ascending", i);
+      if ((int)spans.size() + r.n_spans + 1 > CB_MAX_SPANS + CB_MAX_BATCH || r.n_spans > CB_MAX_SPANS)
+        return fail(CB_ERR_INVALID_ARG, "too many spans (max %d)", CB_MAX_SPANS);
+      s.span_begin = (int)spans.size();
+      s.n_spans = r.n_spans;
+      spans.insert(spans.end(), r.span_offsets, r.span_offsets + r.n_spans + 1);
+    }
+    out[i] = s;
+  }
+  return CB_OK;
+}
+
+static cb_status run_selection(const void *k_fresh, int64_t ld_fresh,
+                               const void *k_reused, int64_t ld_reused,
+                               int row_elems, cb_dtype dt,
+                               const std::vector<SelReq> &sr,
+                               const std::vector<int32_t> &spans,
+                               cb_policy policy, float *dev, int32_t *idx,
+                               int *st, cudaStream_t s) {
+  CB_CUDA(launch_deviation(k_fresh, ld_fresh, k_reused, ld_reused, row_elems, dt,
+                           sr.data(), (int)sr.size(), dev, s));
+  if (policy == CB_POLICY_TOKEN_TOPK)
+    CB_CUDA(launch_topk(dev, sr.data(), (int)sr.size(), idx, s));
+  else
+    CB_CUDA(launch_doc_aligned(dev, sr.data(), (int)sr.size(), spans.data(),
+                               (int)spans.size(), idx, st, s));
+  return CB_OK;
+}
+
+extern "C" cb_status cb_kv_deviation_topk(const void *k_fresh, int64_t ld_fresh,
+                                          const void *k_reused, int64_t ld_reused,
+                                          int row_elems, cb_dtype dtype,
+                                          const cb_select_req *reqs, int n_req,
+                                          cb_policy policy, float *dev_out,
+                                          int32_t *idx_out, void *ws,
+                                          size_t ws_bytes, cb_stream stream) {
+  if (!k_fresh || !k_reused || !dev_out || !idx_out) return fail(CB_ERR_INVALID_ARG, "NULL pointer");
+  if (dtype != CB_F32 && dtype != CB_BF16) return fail(CB_ERR_INVALID_ARG, "bad dtype");
+  const size_t eb = dtype_bytes(dtype);
+  if (row_elems <= 0 || (row_elems * eb) % 16 || ld_fresh < row_elems || ld_reused < row_elems ||
+      (ld_fresh * eb) % 16 || (ld_reused * eb) % 16 || !aligned16(k_fresh) || !aligned16(k_reused))
+    return fail(CB_ERR_INVALID_ARG, "rows must be 16-byte aligned and ld >= row_elems");
+  if (!ws || ws_bytes < cb_select_workspace_size(n_req)) return fail(CB_ERR_WORKSPACE, "workspace too small");
+  std::vector<SelReq> sr;
+  std::vector<int32_t> spans;
+  CB_TRY(to_sel_reqs(reqs, n_req, policy, sr, spans));
+  int *st;
+  CB_TRY(status_ptr(&st));
+  return run_selection(k_fresh, ld_fresh, k_reused, ld_reused, row_elems, dtype, sr,
+                       spans, policy, dev_out, idx_out, st, stream);
+}
+
+// -------------------------------------------------------- gather/scatter --
+extern "C" cb_status cb_gather_rows(const void *src, int64_t ld_src, int64_t src_rows,
+                                    const int32_t *idx, int n, int row_elems,
+                                    void *dst, int64_t ld_dst, cb_dtype dtype,
+                                    cb_stream stream) {
+  if (n < 0) return fail(CB_ERR_INVALID_ARG, "n < 0");
+  if (n == 0) return CB_OK;
+  if (!src || !idx || !dst) return fail(CB_ERR_INVALID_ARG, "NULL pointer");
+  if (dtype != CB_F32 && dtype != CB_BF16) return fail(CB_ERR_INVALID_ARG, "bad dtype");
+  const size_t eb = dtype_bytes(dtype);
+  if (row_elems <= 0 || (row_elems * eb) % 16 || (ld_src * eb) % 16 || (ld_dst * eb) % 16 ||
+      ld_src < row_elems || ld_dst < row_elems || !aligned16(src) || !aligned16(dst))
+    return fail(CB_ERR_INVALID_ARG, "rows must be 16-byte aligned and ld >= row_elems");
+  int *st;
+  CB_TRY(status_ptr(&st));
+  CB_CUDA(launch_gather(src, ld_src, src_rows, idx, n, row_elems, dst, ld_dst, eb, st, stream));
+  return CB_OK;
+}
+
+extern "C" cb_status cb_scatter_kv(const void *k_new, const void *v_new, int64_t ld_new,
+                                   const int32_t *rows, int n, void *k_cache,
+                                   void *v_cache, int64_t ld_cache, int64_t cache_rows,
+                                   int row_elems, cb_dtype dtype, cb_stream stream) {
+  if (n < 0) return fail(CB_ERR_INVALID_ARG, "n < 0");
+  if (n == 0) return CB_OK;
+  if (!k_new || !v_new || !rows || !k_cache || !v_cache) return fail(CB_ERR_INVALID_ARG, "NULL pointer");
+  if (dtype != CB_F32 && dtype != CB_BF16) return fail(CB_ERR_INVALID_ARG, "bad dtype");
+  const size_t eb = dtype_bytes(dtype);
+  if (row_elems <= 0 || (row_elems * eb) % 16 || (ld_new * eb) % 16 || (ld_cache * eb) % 16 ||
+      ld_new < row_elems || ld_cache < row_elems || !aligned16(k_new) || !aligned16(v_new) ||
+      !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(CB_ERR_INVALID_ARG, "rows must be 16-byte aligned and ld >= row_elems");
+  int *st;
+  CB_TRY(status_ptr(&st));
+  CB_CUDA(launch_scatter_kv(k_new, v_new, ld_new, rows, n, k_cache, v_cache, ld_cache,
+                            cache_rows, row_elems, eb, st, stream));
+  return CB_OK;
+}
+
+// -------------------------------------------------------------- attention --
+static cb_status check_attn(int Hq, int Hkv, int hd) {
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv) return fail(CB_ERR_INVALID_ARG, "n_q_heads must be a multiple of n_kv_heads");
+  if (hd != 64 && hd != 128) return fail(CB_ERR_INVALID_ARG, "head_dim must be 64 or 128");
+  return CB_OK;
+}
+
+static cb_status run_attention(const void *q, int64_t ld_q, const int32_t *q_pos,
+                               const std::vector<AttnReq> &reqs, const void *kc,
+                               const void *vc, int64_t ld_kv, int Hq, int Hkv, int hd,
+                               float scale, void *out, int64_t ld_out, cb_dtype dt,
+                               int *st, cudaStream_t s) {
+  CB_CUDA(launch_attention_simt(q, ld_q, q_pos, reqs.data(), (int)reqs.size(), kc, vc,
+                                ld_kv, Hq, Hkv, hd, scale, out, ld_out, dt, st, s));
+  return CB_OK;
+}
+
+extern "C" cb_status cb_sparse_query_attention(const void *q, int64_t ld_q,
+                                               const int32_t *q_pos,
+                                               const cb_attn_req *reqs, int n_req,
+                                               const void *k_cache, const void *v_cache,
+                                               int64_t ld_kv, int n_q_heads,
+                                               int n_kv_heads, int head_dim, float scale,
+                                               void *out, int64_t ld_out, cb_dtype dtype,
+                                               cb_stream stream) {
+  if (n_req < 0 || n_req > CB_MAX_BATCH) return fail(CB_ERR_INVALID_ARG, "n_req must be in [0, %d]", CB_MAX_BATCH);
+  if (n_req == 0) return CB_OK;
+  if (!q || !q_pos || !reqs || !k_cache || !v_cache || !out) return fail(CB_ERR_INVALID_ARG, "NULL pointer");
+  if (dtype != CB_F32 && dtype != CB_BF16) return fail(CB_ERR_INVALID_ARG, "bad dtype");
+  CB_TRY(check_attn(n_q_heads, n_kv_heads, head_dim));
+  const size_t eb = dtype_bytes(dtype);
+  if (ld_q < (int64_t)n_q_heads * head_dim || ld_out < (int64_t)n_q_heads * head_dim ||
+      ld_kv < (int64_t)n_kv_heads * head_dim || (ld_q * eb) % 16 || (ld_out * eb) % 16 ||
+      (ld_kv * eb) % 16 || !aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(CB_ERR_INVALID_ARG, "bad leading dimension or alignment");
+  std::vector<AttnReq> ar(n_req);
+  for (int i = 0; i < n_req; ++i) {
+    const cb_attn_req &r = reqs[i];
+    if (r.q_begin < 0 || r.q_end < r.q_begin || r.kv_row0 < 0 || r.kv_len < 0)
+      return fail(CB_ERR_INVALID_ARG, "req %d: bad ranges", i);
+    ar[i] = AttnReq{r.q_begin, r.q_end, r.kv_row0, r.kv_len};
+  }
+  int *st;
+  CB_TRY(status_ptr(&st));
+  return run_attention(q, ld_q, q_pos, ar, k_cache, v_cache, ld_kv, n_q_heads, n_kv_heads,
+                       head_dim, scale, out, ld_out, dtype, st, stream);
+}
+
+// ------------------------------------------------------------------ model --
+struct cb_model {
+  cb_model_config cfg;
+  cb_weights w;
+  std::vector<cb_layer_weights> layers;
+  int qw, kvw, qkv_rows;
+  size_t eb;
+};
+
+extern "C" cb_status cb_model_create(const cb_model_config *cfg, const cb_weights *w,
+                                     cb_model **out) {
+  if (!cfg || !w || !out) return fail(CB_ERR_INVALID_ARG, "NULL argument");
+  const cb_model_config &c = *cfg;
+  if (c.n_layers <= 0 || c.d_model <= 0 || c.n_q_heads <= 0 || c.n_kv_heads <= 0 ||
+      c.head_dim <= 0 || c.d_ffn <= 0 || c.vocab <= 0 || c.max_positions <= 0)
+    return fail(CB_ERR_INVALID_ARG, "non-positive model dimension");
+  if (c.n_q_heads % c.n_kv_heads) return fail(CB_ERR_INVALID_ARG, "n_q_heads %% n_kv_heads != 0");
+  if (c.head_dim != 64 && c.head_dim != 128) return fail(CB_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (c.d_model % 64 || c.d_ffn % 16) return fail(CB_ERR_UNSUPPORTED, "d_model %% 64 and d_ffn %% 16 must be 0");
+  if (c.dtype != CB_F32 && c.dtype != CB_BF16) return fail(CB_ERR_INVALID_ARG, "bad dtype");
+  if (!(c.norm_eps >= 0.f)) return fail(CB_ERR_INVALID_ARG, "norm_eps < 0");
+  if (!w->embed || !w->final_norm || !w->layers || !w->rope_table)
+    return fail(CB_ERR_INVALID_ARG, "NULL weight pointer");
+  for (int l = 0; l < c.n_layers; ++l) {
+    const cb_layer_weights &L = w->layers[l];
+    if (!L.w_qkv || !L.w_o || !L.w_gate || !L.w_up || !L.w_down || !L.norm1 || !L.norm2)
+      return fail(CB_ERR_INVALID_ARG, "layer %d: NULL weight pointer", l);
+    if (!aligned16(L.w_qkv) || !aligned16(L.w_o) || !aligned16(L.w_gate) ||
+        !aligned16(L.w_up) || !aligned16(L.w_down) || !aligned16(L.norm1) || !aligned16(L.norm2))
+      return fail(CB_ERR_INVALID_ARG, "layer %d: weights must be 16-byte aligned", l);
+  }
+  int dev = 0;
+  cudaDeviceProp prop;
+  CB_CUDA(cudaGetDevice(&dev));
+  CB_CUDA(cudaGetDeviceProperties(&prop, dev));
+  if (!(prop.major == 10 && prop.minor == 3))
+    return fail(CB_ERR_UNSUPPORTED, "device sm_%d%d: this library is built for sm_103a", prop.major, prop.minor);
+  cb_model *m = new cb_model;
+  m->cfg = c;
+  m->w = *w;
+  m->layers.assign(w->layers, w->layers + c.n_layers);
+  m->w.layers = m->layers.data();
+  m->qw = c.n_q_heads * c.head_dim;
+  m->kvw = c.n_kv_heads * c.head_dim;
+  m->qkv_rows = m->qw + 2 * m->kvw;
+  m->eb = dtype_bytes(c.dtype);
+  *out = m;
+  return CB_OK;
+}
+
+extern "C" void cb_model_destroy(cb_model *m) { delete m; }
+
+// ----------------------------------------------------------------- linear --
+static cb_status run_linear(const cb_model *m, const void *A, int64_t lda, const void *W,
+                            const void *W2, int64_t ldw, int M, int N, int K, GemmEpi epi,
+                            void *out, int64_t ldo, cudaStream_t s) {
+  CB_CUDA(launch_gemm_simt(A, lda, W, W2, ldw, M, N, K, epi, out, ldo, m->cfg.dtype, s));
+  return CB_OK;
+}
+
+extern "C" cb_status cb_linear(const cb_model *m, const void *A, int64_t ld_a,
+                               const void *W, const void *W2, int64_t ld_w, int M,
+                               int N, int K, cb_epilogue epi, void *out, int64_t ld_out,
+                               cb_stream stream) {
+  if (!m || !A || !W || !out) return fail(CB_ERR_INVALID_ARG, "NULL pointer");
+  if (M < 0 || N <= 0 || K <= 0 || K % 16) return fail(CB_ERR_INVALID_ARG, "need M >= 0, N > 0, K %% 16 == 0");
+  if (ld_a < K || ld_w < K || ld_out < N) return fail(CB_ERR_INVALID_ARG, "leading dimension too small");
+  GemmEpi e;
+  switch (epi) {
+    case CB_EPI_STORE: e = EPI_STORE; break;
+    case CB_EPI_RESID: e = EPI_RESID; break;
+    case CB_EPI_SWIGLU:
+      if (!W2) return fail(CB_ERR_INVALID_ARG, "SWIGLU needs W2");
+      e = EPI_SWIGLU;
+      break;
+    default: return fail(CB_ERR_INVALID_ARG, "unknown epilogue");
+  }
+  if (M == 0) return CB_OK;
+  return run_linear(m, A, ld_a, W, W2, ld_w, M, N, K, e, out, ld_out, stream);
+}
+
+// ------------------------------------------------------------------- plan --
+namespace {
+
+struct Carver {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) & ~(size_t)255;
+    return o;
+  }
+};
+
+// Scratch of one decoder layer over n rows.
+struct LayerScratch {
+  void *x, *q, *o, *g;
+  float *qkv32;
+};
+
+struct LayerOffsets {
+  size_t x, q, o, g, qkv32;
+};
+
+LayerOffsets carve_layer(Carver &c, const cb_model *m, int64_t n) {
+  LayerOffsets L;
+  const cb_model_config &cf = m->cfg;
+  L.x = c.take(n * cf.d_model * m->eb);
+  L.q = c.take(n * m->qw * m->eb);
+  L.o = c.take(n * m->qw * m->eb);
+  L.g = c.take(n * cf.d_ffn * m->eb);
+  L.qkv32 = c.take(n * m->qkv_rows * sizeof(float));
+  return L;
+}
+
+LayerScratch bind_layer(char *ws, const LayerOffsets &L) {
+  return LayerScratch{ws + L.x, ws + L.q, ws + L.o, ws + L.g, (float *)(ws + L.qkv32)};
+}
+
+struct Plan {
+  int B = 0;
+  BatchMeta bm;
+  std::vector<int> T, N, k, R;
+  std::vector<std::vector<int>> seg_start;  // position of each segment
+  int64_t T_total = 0, N_total = 0, K_total = 0, R_total = 0;
+  int n_off[CB_MAX_BATCH + 1];
+  // workspace
+  LayerOffsets lay;
+  size_t h_all, kf, dev, sel, pos_all, glob_all, pos_c, glob_c, h_c, lm_x, lm_best, total;
+};
+
+}  // namespace
+
+static cb_status validate_requests(const cb_model *m, const cb_request *reqs, int B,
+                                   bool blend) {
+  if (!m) return fail(CB_ERR_INVALID_ARG, "model is NULL");
+  if (B <= 0 || B > CB_MAX_BATCH) return fail(CB_ERR_INVALID_ARG, "B must be in [1, %d]", CB_MAX_BATCH);
+  if (!reqs) return fail(CB_ERR_INVALID_ARG, "reqs is NULL");
+  for (int b = 0; b < B; ++b) {
+    const cb_request &r = reqs[b];
+    if (!r.tokens || r.n_segments <= 0 || !r.segments)
+      return fail(CB_ERR_INVALID_ARG, "request %d: tokens/segments missing", b);
+    bool seen_uncached = false;
+    int64_t T = 0;
+    for (int i = 0; i < r.n_segments; ++i) {
+      const cb_segment &s = r.segments[i];
+      if (s.len < 0) return fail(CB_ERR_INVALID_ARG, "request %d segment %d: len < 0", b, i);
+      const bool cached = s.k_pic != nullptr;
+      if (blend) {
+        if (cached != (s.v_pic != nullptr))
+          return fail(CB_ERR_INVALID_ARG, "request %d segment %d: k_pic and v_pic must both be set or both NULL", b, i);
+        if (cached && seen_uncached)
+          return fail(CB_ERR_INVALID_ARG, "request %d: cached segments must precede uncached ones", b);
+        if (cached && s.len > 0) {
+          if (!aligned16(s.k_pic) || !aligned16(s.v_pic) || (s.pic_layer_stride * (int64_t)m->eb) % 16 ||
+              s.pic_layer_stride < (int64_t)s.len * m->kvw)
+            return fail(CB_ERR_INVALID_ARG, "request %d segment %d: bad PIC layout", b, i);
+          if (s.pic_pos0 < 0) return fail(CB_ERR_INVALID_ARG, "request %d segment %d: pic_pos0 < 0", b, i);
+        }
+      }
+      if (!cached) seen_uncached = true;
+      T += s.len;
+    }
+    if (T <= 0) return fail(CB_ERR_INVALID_ARG, "request %d is empty", b);
+    if (T > m->cfg.max_positions)
+      return fail(CB_ERR_INVALID_ARG, "request %d: %lld positions exceed max_positions %d", b, (long long)T, m->cfg.max_positions);
+    if (blend) {
+      const cb_segment &last = r.segments[r.n_segments - 1];
+      if (last.k_pic != nullptr || last.len == 0)
+        return fail(CB_ERR_INVALID_ARG, "request %d must end in a non-empty uncached segment (the query)", b);
+    }
+  }
+  return CB_OK;
+}
+
+static int select_count(int n_ctx, int ratio_bp) {
+  if (ratio_bp <= 0 || n_ctx <= 0) return 0;
+  const int64_t k = ((int64_t)n_ctx * ratio_bp) / 10000;
+  return (int)(k < 1 ? 1 : k);
+}
+
+static cb_status make_plan(const cb_model *m, const cb_request *reqs, int B,
+                           const cb_blend_params *p, bool blend, Plan &P) {
+  CB_TRY(validate_requests(m, reqs, B, blend));
+  if (blend) {
+    if (!p) return fail(CB_ERR_INVALID_ARG, "params is NULL");
+    if (p->ratio_bp < 0 || p->ratio_bp > 10000) return fail(CB_ERR_INVALID_ARG, "ratio_bp must be in [0, 10000]");
+    if (p->sel_layer < 0 || p->sel_layer >= m->cfg.n_layers)
+      return fail(CB_ERR_INVALID_ARG, "sel_layer must be in [0, n_layers)");
+    if (p->policy != CB_POLICY_TOKEN_TOPK && p->policy != CB_POLICY_DOC_ALIGNED)
+      return fail(CB_ERR_INVALID_ARG, "unknown policy");
+    if (p->n_schedule != 0) return fail(CB_ERR_UNSUPPORTED, "gradual schedules are not supported yet");
+  }
+  P.B = B;
+  P.bm.B = B;
+  P.T.resize(B); P.N.resize(B); P.k.resize(B); P.R.resize(B); P.seg_start.resize(B);
+  P.bm.t_off[0] = P.bm.k_off[0] = P.bm.r_off[0] = 0;
+  P.n_off[0] = 0;
+  for (int b = 0; b < B; ++b) {
+    int T = 0, N = 0;
+    for (int i = 0; i < reqs[b].n_segments; ++i) {
+      const cb_segment &s = reqs[b].segments[i];
+      P.seg_start[b].push_back(T);
+      T += s.len;
+      if (blend && s.k_pic) N += s.len;
+    }
+    const int k = blend ? select_count(N, p->ratio_bp) : 0;
+    P.T[b] = T; P.N[b] = N; P.k[b] = k;
+    P.R[b] = blend ? k + (T - N) : T;
+    P.bm.n_ctx[b] = N;
+    P.bm.t_off[b + 1] = P.bm.t_off[b] + T;
+    P.bm.k_off[b + 1] = P.bm.k_off[b] + k;
+    P.bm.r_off[b + 1] = P.bm.r_off[b] + P.R[b];
+    P.n_off[b + 1] = P.n_off[b] + N;
+  }
+  P.T_total = P.bm.t_off[B];
+  P.N_total = P.n_off[B];
+  P.K_total = P.bm.k_off[B];
+  P.R_total = P.bm.r_off[B];
+  if (P.T_total >= (1ll << 31) / 2) return fail(CB_ERR_INVALID_ARG, "too many rows in one call");
+  const cb_model_config &c = m->cfg;
+  Carver cv;
+  P.lay = carve_layer(cv, m, P.T_total);
+  P.h_all = cv.take(P.T_total * c.d_model * sizeof(float));
+  P.kf = cv.take(P.T_total * m->kvw * m->eb);
+  P.dev = cv.take((P.N_total + 1) * sizeof(float));
+  P.sel = cv.take((P.K_total + 1) * sizeof(int32_t));
+  P.pos_all = cv.take(P.T_total * sizeof(int32_t));
+  P.glob_all = cv.take(P.T_total * sizeof(int32_t));
+  P.pos_c = cv.take((P.R_total + 1) * sizeof(int32_t));
+  P.glob_c = cv.take((P.R_total + 1) * sizeof(int32_t));
+  P.h_c = cv.take((P.R_total + 1) * c.d_model * sizeof(float));
+  P.lm_x = cv.take((size_t)B * c.d_model * sizeof(float));
+  P.lm_best = cv.take((size_t)B * sizeof(unsigned long long));
+  P.total = cv.off;
+  return CB_OK;
+}
+
+static void fill_plan(const Plan &P, cb_plan *out) {
+  out->T_total = P.T_total;
+  out->N_total = P.N_total;
+  out->K_total = P.K_total;
+  out->R_total = P.R_total;
+  out->workspace_bytes = P.total;
+}
+
+extern "C" cb_status cb_blend_plan(const cb_model *m, const cb_request *reqs, int B,
+                                   const cb_blend_params *p, cb_plan *out) {
+  if (!out) return fail(CB_ERR_INVALID_ARG, "out is NULL");
+  Plan P;
+  CB_TRY(make_plan(m, reqs, B, p, true, P));
+  fill_plan(P, out);
+  return CB_OK;
+}
+
+extern "C" cb_status cb_full_plan(const cb_model *m, const cb_request *reqs, int B,
+                                  cb_plan *out) {
+  if (!out) return fail(CB_ERR_INVALID_ARG, "out is NULL");
+  Plan P;
+  CB_TRY(make_plan(m, reqs, B, nullptr, false, P));
+  fill_plan(P, out);
+  return CB_OK;
+}
+
+// ------------------------------------------------------------------ layer --
+static inline char *layer_ptr(void *base, int l, int64_t stride, size_t eb) {
+  return (char *)base + (int64_t)l * stride * (int64_t)eb;
+}
+
+// One decoder layer over n rows of h (see cb_blend_layer).
+static cb_status layer_forward(cb_model *m, int l, float *h, int n, const int32_t *pos,
+                               const int32_t *cache_row, const std::vector<AttnReq> &ar,
+                               void *kc, void *vc, const LayerScratch &S, int *st,
+                               cudaStream_t s) {
+  const cb_model_config &c = m->cfg;
+  const cb_layer_weights &L = m->layers[l];
+  const int d = c.d_model, F = c.d_ffn, hd = c.head_dim;
+  const cb_dtype dt = c.dtype;
+  CB_CUDA(launch_rmsnorm(h, d, nullptr, n, d, L.norm1, c.norm_eps, S.x, d, dt, s));
+  CB_TRY(run_linear(m, S.x, d, L.w_qkv, nullptr, d, n, m->qkv_rows, d, EPI_STORE_F32,
+                    S.qkv32, m->qkv_rows, s));
+  CB_CUDA(launch_qkv_finish(S.qkv32, m->qkv_rows, n, pos, cache_row, c.n_q_heads,
+                            c.n_kv_heads, hd, m->w.rope_table, S.q, m->qw, kc, vc, m->kvw,
+                            dt, 0, s));
+  CB_TRY(run_attention(S.q, m->qw, pos, ar, kc, vc, m->kvw, c.n_q_heads, c.n_kv_heads, hd,
+                       1.f / sqrtf((float)hd), S.o, m->qw, dt, st, s));
+  CB_TRY(run_linear(m, S.o, m->qw, L.w_o, nullptr, m->qw, n, d, m->qw, EPI_RESID, h, d, s));
+  CB_CUDA(launch_rmsnorm(h, d, nullptr, n, d, L.norm2, c.norm_eps, S.x, d, dt, s));
+  CB_TRY(run_linear(m, S.x, d, L.w_gate, L.w_up, d, n, F, d, EPI_SWIGLU, S.g, F, s));
+  CB_TRY(run_linear(m, S.g, F, L.w_down, nullptr, F, n, d, F, EPI_RESID, h, d, s));
+  return CB_OK;
+}
+
+extern "C" size_t cb_layer_workspace_size(const cb_model *m, int n_rows) {
+  if (!m || n_rows < 0) return 0;
+  Carver c;
+  carve_layer(c, m, n_rows);
+  return c.off;
+}
+
+extern "C" cb_status cb_blend_layer(cb_model *m, int layer, float *h, int n_rows,
+                                    const int32_t *pos, const int32_t *cache_row,
+                                    const cb_attn_req *reqs, int n_req, void *k_cache,
+                                    void *v_cache, void *ws, size_t ws_bytes,
+                                    cb_stream stream) {
+  if (!m) return fail(CB_ERR_INVALID_ARG, "model is NULL");
+  if (layer < 0 || layer >= m->cfg.n_layers) return fail(CB_ERR_INVALID_ARG, "layer out of range");
+  if (n_rows < 0) return fail(CB_ERR_INVALID_ARG, "n_rows < 0");
+  if (n_rows == 0) return CB_OK;
+  if (!h || !pos || !cache_row || !reqs || !k_cache || !v_cache) return fail(CB_ERR_INVALID_ARG, "NULL pointer");
+  if (n_req <= 0 || n_req > CB_MAX_BATCH) return fail(CB_ERR_INVALID_ARG, "n_req must be in [1, %d]", CB_MAX_BATCH);
+  if (!aligned16(h) || !aligned16(k_cache) || !aligned16(v_cache)) return fail(CB_ERR_INVALID_ARG, "misaligned");
+  Carver c;
+  LayerOffsets L = carve_layer(c, m, n_rows);
+  if (!ws || ws_bytes < c.off) return fail(CB_ERR_WORKSPACE, "workspace too small (%zu < %zu)", ws_bytes, c.off);
+  std::vector<AttnReq> ar(n_req);
+  for (int i = 0; i < n_req; ++i) {
+    const cb_attn_req &r = reqs[i];
+    if (r.q_begin < 0 || r.q_end < r.q_begin || r.q_end > n_rows || r.kv_row0 < 0 || r.kv_len < 0)
+      return fail(CB_ERR_INVALID_ARG, "req %d: bad ranges", i);
+    ar[i] = AttnReq{r.q_begin, r.q_end, r.kv_row0, r.kv_len};
+  }
+  int *st;
+  CB_TRY(status_ptr(&st));
+  return layer_forward(m, layer, h, n_rows, pos, cache_row, ar, k_cache, v_cache,
+                       bind_layer((char *)ws, L), st, stream);
+}
+
+// ------------------------------------------------------------------ stack --
+static cb_status check_out(const cb_model *m, const cb_blend_out *out) {
+  if (!out) return fail(CB_ERR_INVALID_ARG, "out is NULL");
+  if (!out->k_cache || !out->v_cache) return fail(CB_ERR_INVALID_ARG, "out cache is NULL");
+  if (!aligned16(out->k_cache) || !aligned16(out->v_cache) ||
+      (out->cache_layer_stride * (int64_t)m->eb) % 16)
+    return fail(CB_ERR_INVALID_ARG, "out cache must be 16-byte aligned");
+  if (out->hidden && !aligned16(out->hidden)) return fail(CB_ERR_INVALID_ARG, "out hidden misaligned");
+  return CB_OK;
+}
+
+static void full_attn_reqs(const Plan &P, std::vector<AttnReq> &ar) {
+  ar.resize(P.B);
+  for (int b = 0; b < P.B; ++b)
+    ar[b] = AttnReq{P.bm.t_off[b], P.bm.t_off[b + 1], (int64_t)P.bm.t_off[b], P.T[b]};
+}
+
+// Final norm + tied LM head + arg-max of each request's last row of h:
+// row r_off[b+1]-1 of the compact rows, or t_off[b+1]-1 of all rows.
+static cb_status run_lm_head(cb_model *m, const Plan &P, const float *h, bool compact,
+                             char *ws, int32_t *first_token, cudaStream_t s) {
+  const cb_model_config &c = m->cfg;
+  int32_t last[CB_MAX_BATCH];
+  for (int b = 0; b < P.B; ++b)
+    last[b] = (compact ? P.bm.r_off[b + 1] : P.bm.t_off[b + 1]) - 1;
+  CB_CUDA(launch_lm_head_argmax(h, c.d_model, last, P.B, m->w.final_norm, c.norm_eps,
+                                m->w.embed, c.vocab, c.d_model, c.dtype,
+                                (float *)(ws + P.lm_x), (unsigned long long *)(ws + P.lm_best),
+                                first_token, s));
+  return CB_OK;
+}
+
+extern "C" cb_status cb_blend_prefill(cb_model *m, const cb_request *reqs, int B,
+                                      const cb_blend_params *p, const cb_blend_out *out,
+                                      void *ws_v, size_t ws_bytes, cb_stream stream) {
+  Plan P;
+  CB_TRY(make_plan(m, reqs, B, p, true, P));
+  CB_TRY(check_out(m, out));
+  if (!ws_v || ws_bytes < P.total) return fail(CB_ERR_WORKSPACE, "workspace too small (%zu < %zu)", ws_bytes, P.total);
+  char *ws = (char *)ws_v;
+  const cb_model_config &c = m->cfg;
+  const int L = c.n_layers, s_layer = p->sel_layer, d = c.d_model;
+  const int64_t lstride = out->cache_layer_stride ? out->cache_layer_stride : P.T_total * m->kvw;
+  int *st;
+  CB_TRY(status_ptr(&st));
+  cudaStream_t s = stream;
+  float *h_all = (float *)(ws + P.h_all);
+  float *dev = out->deviation ? out->deviation : (float *)(ws + P.dev);
+  int32_t *sel = out->selected ? out->selected : (int32_t *)(ws + P.sel);
+  int32_t *pos_all = (int32_t *)(ws + P.pos_all), *glob_all = (int32_t *)(ws + P.glob_all);
+  int32_t *pos_c = out->rows ? out->rows : (int32_t *)(ws + P.pos_c);
+  int32_t *glob_c = (int32_t *)(ws + P.glob_c);
+  float *h_c = out->hidden ? out->hidden : (float *)(ws + P.h_c);
+  const LayerScratch S = bind_layer(ws, P.lay);
+
+  // 1. re-position + stitch of every cached segment, layers [s, L)
+  std::vector<cb_stitch_desc> descs;
+  for (int b = 0; b < B; ++b)
+    for (int i = 0; i < reqs[b].n_segments; ++i) {
+      const cb_segment &sg = reqs[b].segments[i];
+      if (!sg.k_pic || sg.len == 0) continue;
+      const int pos0 = P.seg_start[b][i];
+      descs.push_back(cb_stitch_desc{sg.k_pic, sg.v_pic, sg.pic_layer_stride, sg.len,
+                                     P.bm.t_off[b] + pos0, pos0 - sg.pic_pos0});
+    }
+  CB_CUDA(launch_reposition(descs.data(), (int)descs.size(), s_layer, L, out->k_cache,
+                            out->v_cache, lstride, m->kvw, c.head_dim, m->w.rope_table,
+                            c.dtype, st, s));
+  // 2. embeddings of every row, full layers below the selection layer
+  const int32_t *toks[CB_MAX_BATCH];
+  for (int b = 0; b < B; ++b) toks[b] = reqs[b].tokens;
+  CB_CUDA(launch_embed(toks, P.bm, m->w.embed, c.vocab, d, c.dtype, h_all, st, s));
+  CB_CUDA(launch_iota_rows(P.bm, pos_all, glob_all, (int)P.T_total, s));
+  std::vector<AttnReq> ar_full;
+  full_attn_reqs(P, ar_full);
+  for (int l = 0; l < s_layer; ++l)
+    CB_TRY(layer_forward(m, l, h_all, (int)P.T_total, pos_all, glob_all, ar_full,
+                         layer_ptr(out->k_cache, l, lstride, m->eb),
+                         layer_ptr(out->v_cache, l, lstride, m->eb), S, st, s));
+  // 3. selection layer: fresh keys of every row, deviation, ranking
+  {
+    const cb_layer_weights &Ls = m->layers[s_layer];
+    void *kf = ws + P.kf;
+    CB_CUDA(launch_rmsnorm(h_all, d, nullptr, (int)P.T_total, d, Ls.norm1, c.norm_eps, S.x, d,
+                           c.dtype, s));
+    const char *wk = (const char *)Ls.w_qkv + (int64_t)m->qw * d * m->eb;
+    CB_TRY(run_linear(m, S.x, d, wk, nullptr, d, (int)P.T_total, m->kvw, d, EPI_STORE_F32,
+                      S.qkv32, m->kvw, s));
+    CB_CUDA(launch_qkv_finish(S.qkv32, m->kvw, (int)P.T_total, pos_all, nullptr, c.n_q_heads,
+                              c.n_kv_heads, c.head_dim, m->w.rope_table, nullptr, 0, kf,
+                              nullptr, m->kvw, c.dtype, 0, s));
+    std::vector<SelReq> sr(B);
+    std::vector<int32_t> spans;
+    for (int b = 0; b < B; ++b) {
+      sr[b] = SelReq{P.N[b], P.k[b], (int64_t)P.bm.t_off[b], (int64_t)P.bm.t_off[b],
+                     P.n_off[b], P.bm.k_off[b], 0, 0};
+      if (p->policy == CB_POLICY_DOC_ALIGNED) {
+        sr[b].span_begin = (int)spans.size();
+        int n_sp = 0;
+        for (int i = 0; i < reqs[b].n_segments; ++i) {
+          if (!reqs[b].segments[i].k_pic) break;
+          spans.push_back(P.seg_start[b][i]);
+          ++n_sp;
+        }
+        spans.push_back(P.N[b]);
+        sr[b].n_spans = n_sp;
+        if ((int)spans.size() > CB_MAX_SPANS + CB_MAX_BATCH)
+          return fail(CB_ERR_INVALID_ARG, "too many spans (max %d)", CB_MAX_SPANS);
+      }
+    }
+    if (p->forced_selected) {
+      // the caller fixes P; d is still produced for inspection
+      CB_CUDA(launch_deviation(kf, m->kvw, layer_ptr(out->k_cache, s_layer, lstride, m->eb),
+                               m->kvw, m->kvw, c.dtype, sr.data(), B, dev, s));
+      if (sel != p->forced_selected && P.K_total > 0)
+        CB_CUDA(cudaMemcpyAsync(sel, p->forced_selected, P.K_total * sizeof(int32_t),
+                                cudaMemcpyDeviceToDevice, s));
+    } else {
+      CB_TRY(run_selection(kf, m->kvw, layer_ptr(out->k_cache, s_layer, lstride, m->eb),
+                           m->kvw, m->kvw, c.dtype, sr, spans, p->policy, dev, sel, st, s));
+    }
+  }
+  // 4. computed rows: selected context rows + uncached rows, gathered once
+  CB_CUDA(launch_build_rows(P.bm, sel, pos_c, glob_c, (int)P.R_total, st, s));
+  CB_CUDA(launch_gather(h_all, d, P.T_total, glob_c, (int)P.R_total, d, h_c, d, sizeof(float),
+                        st, s));
+  std::vector<AttnReq> ar_c(B);
+  for (int b = 0; b < B; ++b)
+    ar_c[b] = AttnReq{P.bm.r_off[b], P.bm.r_off[b + 1], (int64_t)P.bm.t_off[b], P.T[b]};
+  for (int l = s_layer; l < L; ++l)
+    CB_TRY(layer_forward(m, l, h_c, (int)P.R_total, pos_c, glob_c, ar_c,
+                         layer_ptr(out->k_cache, l, lstride, m->eb),
+                         layer_ptr(out->v_cache, l, lstride, m->eb), S, st, s));
+  // 5. first token from each request's last computed row (its last position)
+  if (out->first_token) CB_TRY(run_lm_head(m, P, h_c, true, ws, out->first_token, s));
+  return CB_OK;
+}
+
+extern "C" cb_status cb_full_prefill(cb_model *m, const cb_request *reqs, int B,
+                                     const cb_blend_out *out, void *ws_v, size_t ws_bytes,
+                                     cb_stream stream) {
+  Plan P;
+  CB_TRY(make_plan(m, reqs, B, nullptr, false, P));
+  CB_TRY(check_out(m, out));
+  if (!ws_v || ws_bytes < P.total) return fail(CB_ERR_WORKSPACE, "workspace too small (%zu < %zu)", ws_bytes, P.total);
+  char *ws = (char *)ws_v;
+  const cb_model_config &c = m->cfg;
+  const int64_t lstride = out->cache_layer_stride ? out->cache_layer_stride : P.T_total * m->kvw;
+  int *st;
+  CB_TRY(status_ptr(&st));
+  float *h = out->hidden ? out->hidden : (float *)(ws + P.h_all);
+  int32_t *pos_all = out->rows ? out->rows : (int32_t *)(ws + P.pos_all);
+  int32_t *glob_all = (int32_t *)(ws + P.glob_all);
+  const LayerScratch S = bind_layer(ws, P.lay);
+  const int32_t *toks[CB_MAX_BATCH];
+  for (int b = 0; b < B; ++b) toks[b] = reqs[b].tokens;
+  CB_CUDA(launch_embed(toks, P.bm, m->w.embed, c.vocab, c.d_model, c.dtype, h, st, stream));
+  CB_CUDA(launch_iota_rows(P.bm, pos_all, glob_all, (int)P.T_total, stream));
+  std::vector<AttnReq> ar;
+  full_attn_reqs(P, ar);
+  for (int l = 0; l < c.n_layers; ++l)
+    CB_TRY(layer_forward(m, l, h, (int)P.T_total, pos_all, glob_all, ar,
+                         layer_ptr(out->k_cache, l, lstride, m->eb),
+                         layer_ptr(out->v_cache, l, lstride, m->eb), S, st, stream));
+  if (out->first_token) CB_TRY(run_lm_head(m, P, h, false, ws, out->first_token, stream));
+  return CB_OK;
+}

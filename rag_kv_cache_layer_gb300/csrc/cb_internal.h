@@ -1,0 +1,133 @@
+// Host-side interface between the C ABI (cb_api.cu) and the kernel files.
+// Every launcher takes plain device pointers and a stream, enqueues its
+// kernel(s) and returns the launch error.  Nothing here allocates.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "cacheblend.h"
+
+namespace cb {
+
+// Per-request row bookkeeping of one call, passed to kernels by value.
+//   t_off: first fused-cache row of each request (prefix sums of T_b)
+//   n_ctx: reusable context tokens N_b (they are positions 0..N_b-1)
+//   k_off: prefix sums of the selected counts k_b
+//   r_off: prefix sums of the computed rows R_b = k_b + (T_b - N_b)
+struct BatchMeta {
+  int B;
+  int t_off[CB_MAX_BATCH + 1];
+  int n_ctx[CB_MAX_BATCH];
+  int k_off[CB_MAX_BATCH + 1];
+  int r_off[CB_MAX_BATCH + 1];
+};
+
+// Device address of this library's status word on the current device.
+int *device_status_ptr();
+
+// Counts kernels enqueued by the library (read through
+// cb_debug_launch_count); launchers call launched(n) after n launches.
+void note_launches(int n);
+inline cudaError_t launched(int n) {
+  note_launches(n);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------- RoPE --
+cudaError_t launch_rope_table(float *table, int max_pos, int head_dim,
+                              float base, cudaStream_t s);
+cudaError_t launch_reposition(const cb_stitch_desc *descs, int n_desc,
+                              int layer_begin, int layer_end, void *k_cache,
+                              void *v_cache, int64_t cache_layer_stride,
+                              int row_elems, int head_dim, const float *table,
+                              cb_dtype dt, int *status, cudaStream_t s);
+
+// ------------------------------------------------------------ selection --
+struct SelReq {
+  int n_ctx, k;
+  int64_t fresh_row0, reused_row0;
+  int dev_offset, idx_offset;
+  int span_begin, n_spans;  // into the packed span-offset array
+};
+size_t select_ws_bytes(int n_req);
+cudaError_t launch_deviation(const void *k_fresh, int64_t ld_fresh,
+                             const void *k_reused, int64_t ld_reused,
+                             int row_elems, cb_dtype dt, const SelReq *reqs,
+                             int n_req, float *dev_out, cudaStream_t s);
+cudaError_t launch_topk(const float *dev, const SelReq *reqs, int n_req,
+                        int32_t *idx_out, cudaStream_t s);
+cudaError_t launch_doc_aligned(const float *dev, const SelReq *reqs, int n_req,
+                               const int32_t *span_offsets, int n_spans_total,
+                               int32_t *idx_out, int *status, cudaStream_t s);
+cudaError_t launch_build_rows(const BatchMeta &bm, const int32_t *sel,
+                              int32_t *pos, int32_t *glob, int n_rows,
+                              int *status, cudaStream_t s);
+cudaError_t launch_iota_rows(const BatchMeta &bm, int32_t *pos, int32_t *glob,
+                             int n_rows, cudaStream_t s);
+
+// ----------------------------------------------------------------- rows --
+cudaError_t launch_embed(const int32_t *const *tokens, const BatchMeta &bm,
+                         const void *embed, int vocab, int d, cb_dtype dt,
+                         float *h, int *status, cudaStream_t s);
+cudaError_t launch_rmsnorm(const float *h, int64_t ld_h, const int32_t *src_rows,
+                           int n, int d, const float *gain, float eps,
+                           void *out, int64_t ld_out, cb_dtype out_dt,
+                           cudaStream_t s);
+cudaError_t launch_gather(const void *src, int64_t ld_src, int64_t src_rows,
+                          const int32_t *idx, int n, int row_elems, void *dst,
+                          int64_t ld_dst, size_t elem_bytes, int *status,
+                          cudaStream_t s);
+cudaError_t launch_scatter_kv(const void *k_new, const void *v_new,
+                              int64_t ld_new, const int32_t *rows, int n,
+                              void *k_cache, void *v_cache, int64_t ld_cache,
+                              int64_t cache_rows, int row_elems,
+                              size_t elem_bytes, int *status, cudaStream_t s);
+// qkv [n][(Hq + 2 Hkv) hd] float -> q (rotated), k (rotated) and v rows.
+// k and v go to k_dst[dst_rows[i]] / v_dst[dst_rows[i]] (ld_kv); when
+// v_dst is NULL only keys are produced (q_out may be NULL).
+cudaError_t launch_qkv_finish(const float *qkv, int64_t ld_qkv, int n,
+                              const int32_t *pos, const int32_t *dst_rows,
+                              int Hq, int Hkv, int hd, const float *table,
+                              void *q_out, int64_t ld_q, void *k_dst,
+                              void *v_dst, int64_t ld_kv, cb_dtype dt,
+                              int k_col0, cudaStream_t s);
+// logits = RMSNorm(h[row_b]) E^T for each request b, argmax -> token[b];
+// last_rows_host: host array of the B rows of h to use.
+cudaError_t launch_lm_head_argmax(const float *h, int64_t ld_h,
+                                  const int32_t *last_rows_host, int B,
+                                  const float *final_norm, float eps,
+                                  const void *embed, int vocab, int d,
+                                  cb_dtype dt, float *x_scratch,
+                                  unsigned long long *best_scratch,
+                                  int32_t *token_out, cudaStream_t s);
+cudaError_t launch_copy_f32(float *dst, const float *src, size_t n,
+                            cudaStream_t s);
+
+// ----------------------------------------------------------------- GEMM --
+enum GemmEpi { EPI_STORE_F32 = 0, EPI_STORE = 1, EPI_RESID = 2, EPI_SWIGLU = 3 };
+// out = epi(A[M][K] W[N][K]^T); A and W of dtype dt; STORE_F32 and RESID
+// write float, STORE and SWIGLU write dt.
+cudaError_t launch_gemm_simt(const void *A, int64_t lda, const void *W,
+                             const void *W2, int64_t ldw, int M, int N, int K,
+                             GemmEpi epi, void *out, int64_t ldo, cb_dtype dt,
+                             cudaStream_t s);
+
+// ------------------------------------------------------------ attention --
+struct AttnReq {
+  int q_begin, q_end;
+  int64_t kv_row0;
+  int kv_len;
+};
+cudaError_t launch_attention_simt(const void *q, int64_t ld_q,
+                                  const int32_t *q_pos, const AttnReq *reqs,
+                                  int n_req, const void *k_cache,
+                                  const void *v_cache, int64_t ld_kv, int Hq,
+                                  int Hkv, int hd, float scale, void *out,
+                                  int64_t ld_out, cb_dtype dt, int *status,
+                                  cudaStream_t s);
+
+// ---------------------------------------------------------------- debug --
+cudaError_t launch_expire_wait(int limit_us, int *status, cudaStream_t s);
+
+}  // namespace cb

@@ -1,0 +1,362 @@
+// Row-wise kernels of the decoder stack: embedding gather, RMSNorm (with an
+// optional row gather), generic row gather, K/V scatter into the fused
+// cache (QCFuse Eq. 7; CacheBlend blog blend_layer step 3), the RoPE +
+// scatter step that follows a Q/K/V projection, and the first-token LM head
+// (GEMV over the tied embedding + arg-max).  All are HBM-bound streams with
+// 16-byte vector accesses.
+#include "cb_common.cuh"
+#include "cb_internal.h"
+
+namespace cb {
+
+// -------------------------------------------------------------- embedding --
+struct TokPtrs {
+  const int32_t *p[CB_MAX_BATCH];
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+embed_kernel(const __grid_constant__ TokPtrs tp, const __grid_constant__ BatchMeta bm,
+             const T *__restrict__ E, int vocab, int d, float *__restrict__ h,
+             int *status) {
+  constexpr int VEC = 16 / sizeof(T);
+  const int row = blockIdx.x;
+  int b = 0;
+  while (bm.t_off[b + 1] <= row) ++b;
+  int tok = tp.p[b][row - bm.t_off[b]];
+  if (tok < 0 || tok >= vocab) {
+    if (threadIdx.x == 0) report(status, CB_ERR_DEVICE_INDEX);
+    tok = 0;
+  }
+  const T *src = E + (int64_t)tok * d;
+  float *dst = h + (int64_t)row * d;
+  for (int c = threadIdx.x * VEC; c < d; c += blockDim.x * VEC) {
+    float x[VEC];
+    load16<T>(src + c, x);
+#pragma unroll
+    for (int i = 0; i < VEC; i += 4)
+      *reinterpret_cast<float4 *>(dst + c + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+  }
+}
+
+cudaError_t launch_embed(const int32_t *const *tokens, const BatchMeta &bm,
+                         const void *embed, int vocab, int d, cb_dtype dt,
+                         float *h, int *status, cudaStream_t s) {
+  TokPtrs tp;
+  for (int b = 0; b < bm.B; ++b) tp.p[b] = tokens[b];
+  const int rows = bm.t_off[bm.B];
+  if (rows == 0) return cudaSuccess;
+  if (dt == CB_BF16)
+    embed_kernel<bf16><<<rows, 256, 0, s>>>(tp, bm, reinterpret_cast<const bf16 *>(embed),
+                                            vocab, d, h, status);
+  else
+    embed_kernel<float><<<rows, 256, 0, s>>>(tp, bm, reinterpret_cast<const float *>(embed),
+                                             vocab, d, h, status);
+  return launched(1);
+}
+
+// ---------------------------------------------------------------- RMSNorm --
+// out[i] = h[src(i)] / sqrt(mean(h[src(i)]^2) + eps) * gain, one CTA per row.
+template <typename T>
+__global__ void __launch_bounds__(256)
+rmsnorm_kernel(const float *__restrict__ h, int64_t ld_h,
+               const int32_t *__restrict__ src_rows, int d,
+               const float *__restrict__ gain, float eps, T *__restrict__ out,
+               int64_t ld_out) {
+  __shared__ float red[8];
+  const int i = blockIdx.x;
+  const int64_t src = src_rows ? src_rows[i] : i;
+  const float *x = h + src * ld_h;
+  float ss = 0.f;
+  for (int c = threadIdx.x * 4; c < d; c += blockDim.x * 4) {
+    const float4 v = *reinterpret_cast<const float4 *>(x + c);
+    ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) tot += red[w];
+  const float inv = rsqrtf(tot / (float)d + eps);
+  T *o = out + (int64_t)i * ld_out;
+  for (int c = threadIdx.x * 4; c < d; c += blockDim.x * 4) {
+    const float4 v = *reinterpret_cast<const float4 *>(x + c);
+    const float4 g = *reinterpret_cast<const float4 *>(gain + c);
+    o[c + 0] = from_f<T>(v.x * inv * g.x);
+    o[c + 1] = from_f<T>(v.y * inv * g.y);
+    o[c + 2] = from_f<T>(v.z * inv * g.z);
+    o[c + 3] = from_f<T>(v.w * inv * g.w);
+  }
+}
+
+cudaError_t launch_rmsnorm(const float *h, int64_t ld_h, const int32_t *src_rows,
+                           int n, int d, const float *gain, float eps,
+                           void *out, int64_t ld_out, cb_dtype out_dt,
+                           cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  if (out_dt == CB_BF16)
+    rmsnorm_kernel<bf16><<<n, 256, 0, s>>>(h, ld_h, src_rows, d, gain, eps,
+                                           reinterpret_cast<bf16 *>(out), ld_out);
+  else
+    rmsnorm_kernel<float><<<n, 256, 0, s>>>(h, ld_h, src_rows, d, gain, eps,
+                                            reinterpret_cast<float *>(out), ld_out);
+  return launched(1);
+}
+
+// ---------------------------------------------------------- gather / scatter --
+// Byte-level row moves in 16-byte units (row bytes are multiples of 16).
+__global__ void __launch_bounds__(256)
+gather_kernel(const char *__restrict__ src, int64_t ld_src_b, int64_t src_rows,
+              const int32_t *__restrict__ idx, int n, int row_units,
+              char *__restrict__ dst, int64_t ld_dst_b, int *status) {
+  const int64_t total = (int64_t)n * row_units;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int i = (int)(t / row_units), u = (int)(t % row_units);
+    const int r = idx[i];
+    if (r < 0 || r >= src_rows) { report(status, CB_ERR_DEVICE_INDEX); continue; }
+    stg16(dst + i * ld_dst_b + (int64_t)u * 16, ldg16(src + r * ld_src_b + (int64_t)u * 16));
+  }
+}
+
+static int grid_for(int64_t work, int threads) {
+  int64_t b = (work + threads - 1) / threads;
+  if (b > 152 * 16) b = 152 * 16;
+  return b < 1 ? 1 : (int)b;
+}
+
+cudaError_t launch_gather(const void *src, int64_t ld_src, int64_t src_rows,
+                          const int32_t *idx, int n, int row_elems, void *dst,
+                          int64_t ld_dst, size_t eb, int *status,
+                          cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const int units = (int)(row_elems * eb / 16);
+  gather_kernel<<<grid_for((int64_t)n * units, 256), 256, 0, s>>>(
+      (const char *)src, ld_src * (int64_t)eb, src_rows, idx, n, units,
+      (char *)dst, ld_dst * (int64_t)eb, status);
+  return launched(1);
+}
+
+__global__ void __launch_bounds__(256)
+scatter_kv_kernel(const char *__restrict__ kn, const char *__restrict__ vn,
+                  int64_t ld_new_b, const int32_t *__restrict__ rows, int n,
+                  char *__restrict__ kc, char *__restrict__ vc,
+                  int64_t ld_cache_b, int64_t cache_rows, int row_units,
+                  int *status) {
+  const int64_t total = (int64_t)n * row_units * 2;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int which = (int)(t / ((int64_t)n * row_units));
+    const int64_t tt = t - (int64_t)which * n * row_units;
+    const int i = (int)(tt / row_units), u = (int)(tt % row_units);
+    const int r = rows[i];
+    if (r < 0 || r >= cache_rows) { report(status, CB_ERR_DEVICE_INDEX); continue; }
+    const char *src = (which ? vn : kn) + i * ld_new_b + (int64_t)u * 16;
+    char *dst = (which ? vc : kc) + r * ld_cache_b + (int64_t)u * 16;
+    stg16(dst, ldg16(src));
+  }
+}
+
+cudaError_t launch_scatter_kv(const void *k_new, const void *v_new,
+                              int64_t ld_new, const int32_t *rows, int n,
+                              void *k_cache, void *v_cache, int64_t ld_cache,
+                              int64_t cache_rows, int row_elems, size_t eb,
+                              int *status, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const int units = (int)(row_elems * eb / 16);
+  scatter_kv_kernel<<<grid_for((int64_t)n * units * 2, 256), 256, 0, s>>>(
+      (const char *)k_new, (const char *)v_new, ld_new * (int64_t)eb, rows, n,
+      (char *)k_cache, (char *)v_cache, ld_cache * (int64_t)eb, cache_rows,
+      units, status);
+  return launched(1);
+}
+
+// ------------------------------------------------------------- QKV finish --
+// One CTA per row.  Column blocks of the projection: [0, Hq hd) -> q,
+// [Hq hd, (Hq+Hkv) hd) -> k, the rest -> v.  q and k are rotated at pos[i]
+// (rotate-half pairs); k and v land in cache row dst_rows[i].  When v_dst is
+// NULL the input holds keys only (k_col0 = column of key 0).
+template <typename T>
+__global__ void __launch_bounds__(128)
+qkv_finish_kernel(const float *__restrict__ qkv, int64_t ld_qkv,
+                  const int32_t *__restrict__ pos, const int32_t *__restrict__ dst_rows,
+                  int Hq, int Hkv, int hd, const float2 *__restrict__ table,
+                  T *__restrict__ q_out, int64_t ld_q, T *__restrict__ k_dst,
+                  T *__restrict__ v_dst, int64_t ld_kv, int k_col0) {
+  const int i = blockIdx.x;
+  const int p = pos[i];
+  const int64_t dr = dst_rows ? dst_rows[i] : i;
+  const float *src = qkv + (int64_t)i * ld_qkv;
+  const int half = hd / 2;
+  const float2 *cs = table + (int64_t)p * half;
+  const bool keys_only = v_dst == nullptr;
+  const int n_rot_heads = keys_only ? Hkv : Hq + Hkv;
+  // rotated heads: q heads then k heads
+  for (int t = threadIdx.x; t < n_rot_heads * half; t += blockDim.x) {
+    const int hh = t / half, e = t % half;
+    const int col = keys_only ? k_col0 + hh * hd : hh * hd;
+    const float x1 = src[col + e], x2 = src[col + e + half];
+    const float2 w = __ldg(cs + e);
+    const float o1 = x1 * w.x - x2 * w.y;
+    const float o2 = x2 * w.x + x1 * w.y;
+    if (!keys_only && hh < Hq) {
+      q_out[(int64_t)i * ld_q + hh * hd + e] = from_f<T>(o1);
+      q_out[(int64_t)i * ld_q + hh * hd + e + half] = from_f<T>(o2);
+    } else {
+      const int kh = keys_only ? hh : hh - Hq;
+      k_dst[dr * ld_kv + kh * hd + e] = from_f<T>(o1);
+      k_dst[dr * ld_kv + kh * hd + e + half] = from_f<T>(o2);
+    }
+  }
+  if (!keys_only) {
+    const int v0 = (Hq + Hkv) * hd;
+    for (int c = threadIdx.x; c < Hkv * hd; c += blockDim.x)
+      v_dst[dr * ld_kv + c] = from_f<T>(src[v0 + c]);
+  }
+}
+
+cudaError_t launch_qkv_finish(const float *qkv, int64_t ld_qkv, int n,
+                              const int32_t *pos, const int32_t *dst_rows,
+                              int Hq, int Hkv, int hd, const float *table,
+                              void *q_out, int64_t ld_q, void *k_dst,
+                              void *v_dst, int64_t ld_kv, cb_dtype dt,
+                              int k_col0, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const float2 *tab = reinterpret_cast<const float2 *>(table);
+  if (dt == CB_BF16)
+    qkv_finish_kernel<bf16><<<n, 128, 0, s>>>(qkv, ld_qkv, pos, dst_rows, Hq, Hkv, hd, tab,
+                                              (bf16 *)q_out, ld_q, (bf16 *)k_dst,
+                                              (bf16 *)v_dst, ld_kv, k_col0);
+  else
+    qkv_finish_kernel<float><<<n, 128, 0, s>>>(qkv, ld_qkv, pos, dst_rows, Hq, Hkv, hd, tab,
+                                               (float *)q_out, ld_q, (float *)k_dst,
+                                               (float *)v_dst, ld_kv, k_col0);
+  return launched(1);
+}
+
+// -------------------------------------------------------------- LM head --
+// Stage 1: x_b = RMSNorm(h[last_b]) (float, one CTA per request) and reset
+// of the packed arg-max words.  Stage 2: every CTA takes a slice of the
+// vocabulary; a warp computes whole dot products x_b . E[v] (16-byte loads
+// of E, which is read exactly once), the best (value, lowest id) per CTA is
+// merged with a 64-bit atomicMax on (order-preserving value bits, ~id).
+__device__ __forceinline__ unsigned long long pack_best(float v, int id) {
+  const uint32_t u = __float_as_uint(v);
+  const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)key << 32) | (unsigned long long)(~(uint32_t)id);
+}
+
+struct LastRows {
+  int r[CB_MAX_BATCH];
+};
+
+__global__ void lm_norm_kernel(const float *__restrict__ h, int64_t ld_h,
+                               const __grid_constant__ LastRows last_rows, int d,
+                               const float *__restrict__ g, float eps,
+                               float *__restrict__ x,
+                               unsigned long long *__restrict__ best) {
+  __shared__ float red[8];
+  const int b = blockIdx.x;
+  const float *src = h + (int64_t)last_rows.r[b] * ld_h;
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) ss = fmaf(src[c], src[c], ss);
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < 8; ++w) tot += red[w];
+  const float inv = rsqrtf(tot / (float)d + eps);
+  for (int c = threadIdx.x; c < d; c += blockDim.x) x[(int64_t)b * d + c] = src[c] * inv * g[c];
+  if (threadIdx.x == 0) best[b] = 0ull;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+lm_head_kernel(const float *__restrict__ x, int B, const T *__restrict__ E,
+               int vocab, int d, unsigned long long *__restrict__ best) {
+  constexpr int VEC = 16 / sizeof(T);
+  extern __shared__ float xs[];  // [B][d]
+  for (int i = threadIdx.x; i < B * d; i += blockDim.x) xs[i] = x[i];
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int warps = blockDim.x >> 5;
+  const int gw = blockIdx.x * warps + (threadIdx.x >> 5);
+  const int nw = gridDim.x * warps;
+  unsigned long long mine[CB_MAX_BATCH > 8 ? 8 : CB_MAX_BATCH];
+  const int bl = B < 8 ? B : 8;
+  for (int b = 0; b < bl; ++b) mine[b] = 0ull;
+  for (int v = gw; v < vocab; v += nw) {
+    const T *row = E + (int64_t)v * d;
+    float acc[8];
+    for (int b = 0; b < bl; ++b) acc[b] = 0.f;
+    for (int c = lane * VEC; c < d; c += 32 * VEC) {
+      float e[VEC];
+      load16<T>(row + c, e);
+      for (int b = 0; b < bl; ++b) {
+        const float *xb = xs + b * d + c;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) acc[b] = fmaf(e[j], xb[j], acc[b]);
+      }
+    }
+    for (int b = 0; b < bl; ++b) {
+      const float s = warp_sum(acc[b]);
+      const unsigned long long pk = pack_best(s, v);
+      if (pk > mine[b]) mine[b] = pk;
+    }
+  }
+  for (int b = 0; b < bl; ++b)
+    if (lane == 0) atomicMax(best + b, mine[b]);
+}
+
+__global__ void lm_unpack_kernel(const unsigned long long *__restrict__ best,
+                                 int B, int32_t *__restrict__ token) {
+  const int b = threadIdx.x;
+  if (b < B) token[b] = (int32_t)(~(uint32_t)(best[b] & 0xffffffffull));
+}
+
+cudaError_t launch_lm_head_argmax(const float *h, int64_t ld_h,
+                                  const int32_t *last_rows_host, int B,
+                                  const float *final_norm, float eps,
+                                  const void *embed, int vocab, int d,
+                                  cb_dtype dt, float *x_scratch,
+                                  unsigned long long *best, int32_t *token_out,
+                                  cudaStream_t s) {
+  if (B == 0) return cudaSuccess;
+  LastRows lr;
+  for (int b = 0; b < B; ++b) lr.r[b] = last_rows_host[b];
+  lm_norm_kernel<<<B, 256, 0, s>>>(h, ld_h, lr, d, final_norm, eps, x_scratch, best);
+  // up to 8 requests per pass over the vocabulary
+  for (int b0 = 0; b0 < B; b0 += 8) {
+    const int nb = B - b0 < 8 ? B - b0 : 8;
+    const size_t smem = (size_t)nb * d * sizeof(float);
+    const int blocks = 152 * 4;
+    if (dt == CB_BF16) {
+      cudaFuncSetAttribute(lm_head_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      lm_head_kernel<bf16><<<blocks, 256, smem, s>>>(x_scratch + (int64_t)b0 * d, nb,
+                                                     (const bf16 *)embed, vocab, d, best + b0);
+    } else {
+      cudaFuncSetAttribute(lm_head_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      lm_head_kernel<float><<<blocks, 256, smem, s>>>(x_scratch + (int64_t)b0 * d, nb,
+                                                      (const float *)embed, vocab, d, best + b0);
+    }
+  }
+  lm_unpack_kernel<<<1, CB_MAX_BATCH, 0, s>>>(best, B, token_out);
+  return launched(2 + (B + 7) / 8);
+}
+
+// ------------------------------------------------------------------- copy --
+__global__ void copy_f32_kernel(float *__restrict__ dst, const float *__restrict__ src, size_t n) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
+cudaError_t launch_copy_f32(float *dst, const float *src, size_t n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  copy_f32_kernel<<<grid_for((int64_t)n, 256), 256, 0, s>>>(dst, src, n);
+  return launched(1);
+}
+
+}  // namespace cb

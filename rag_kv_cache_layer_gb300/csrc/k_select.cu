@@ -1,0 +1,422 @@
+// Deviation ranking and selection.
+//
+//  * deviation_kernel -- d_i = ||K_i^fresh - K_i^reused||_2^2 over all kv
+//    heads, fp32 ("Request Order Matters" §2.2 Eq. 1).  One warp per token
+//    row, 16-byte loads; HBM-bound.
+//  * topk_kernel -- exact k largest d_i per request, ties to the lower
+//    index, indices written ascending (token top-k, same page §2.2 Eq. 2).
+//    One CTA per request: a 4-pass 8-bit radix select over the order-
+//    preserving integer image of the floats finds the k-th largest key,
+//    then a block-wide ordered compaction emits the winners by index.
+//  * doc_aligned_kernel -- document-aligned spans (same page §2.3 Eq. 3).
+//  * build_rows / iota_rows -- positions and fused-cache rows of the rows a
+//    layer computes.
+#include "cb_common.cuh"
+#include "cb_internal.h"
+
+namespace cb {
+
+constexpr int kSelThreads = 1024;
+
+struct SelParams {
+  int n_req;
+  SelReq r[CB_MAX_BATCH];
+  int row_prefix[CB_MAX_BATCH + 1];  // context rows before request i
+};
+
+// -------------------------------------------------------------- deviation --
+template <typename T>
+__global__ void __launch_bounds__(256)
+deviation_kernel(const __grid_constant__ SelParams p, const T *__restrict__ kf,
+                 int64_t ld_f, const T *__restrict__ kr, int64_t ld_r,
+                 int row_elems, float *__restrict__ dev_out) {
+  constexpr int VEC = 16 / sizeof(T);
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int total = p.row_prefix[p.n_req];
+  if (warp >= total) return;
+  int b = 0;
+  while (p.row_prefix[b + 1] <= warp) ++b;
+  const SelReq &q = p.r[b];
+  const int i = warp - p.row_prefix[b];
+  const T *a = kf + (q.fresh_row0 + i) * ld_f;
+  const T *c = kr + (q.reused_row0 + i) * ld_r;
+  float acc = 0.f;
+  for (int col = lane * VEC; col < row_elems; col += 32 * VEC) {
+    float x[VEC], y[VEC];
+    load16<T>(a + col, x);
+    load16<T>(c + col, y);
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+      const float t = x[j] - y[j];
+      acc = fmaf(t, t, acc);
+    }
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) dev_out[q.dev_offset + i] = acc;
+}
+
+static void fill_params(SelParams &p, const SelReq *reqs, int n_req) {
+  p.n_req = n_req;
+  p.row_prefix[0] = 0;
+  for (int i = 0; i < n_req; ++i) {
+    p.r[i] = reqs[i];
+    p.row_prefix[i + 1] = p.row_prefix[i] + reqs[i].n_ctx;
+  }
+}
+
+size_t select_ws_bytes(int n_req) { return 256 + (size_t)n_req * 0; }
+
+cudaError_t launch_deviation(const void *k_fresh, int64_t ld_fresh,
+                             const void *k_reused, int64_t ld_reused,
+                             int row_elems, cb_dtype dt, const SelReq *reqs,
+                             int n_req, float *dev_out, cudaStream_t s) {
+  SelParams p;
+  fill_params(p, reqs, n_req);
+  const int rows = p.row_prefix[n_req];
+  if (rows == 0) return cudaSuccess;
+  const int blocks = (rows + 7) / 8;
+  if (dt == CB_BF16)
+    deviation_kernel<bf16><<<blocks, 256, 0, s>>>(
+        p, reinterpret_cast<const bf16 *>(k_fresh), ld_fresh,
+        reinterpret_cast<const bf16 *>(k_reused), ld_reused, row_elems, dev_out);
+  else
+    deviation_kernel<float><<<blocks, 256, 0, s>>>(
+        p, reinterpret_cast<const float *>(k_fresh), ld_fresh,
+        reinterpret_cast<const float *>(k_reused), ld_reused, row_elems, dev_out);
+  return launched(1);
+}
+
+// ------------------------------------------------------------------ top-k --
+// Order-preserving map of float bits to unsigned integers: larger float ->
+// larger key (negative values below positive ones, -0 just below +0).
+__device__ __forceinline__ uint32_t float_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exclusive block scan of one int per thread (kSelThreads threads); returns
+// the exclusive prefix and writes the block total to *total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_buf,
+                                                    int *total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_buf[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int t = lane < (kSelThreads / 32) ? warp_buf[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    warp_buf[lane] = t;  // inclusive prefix of warp sums
+  }
+  __syncthreads();
+  const int before = (w > 0 ? warp_buf[w - 1] : 0) + x - v;
+  *total = warp_buf[kSelThreads / 32 - 1];
+  __syncthreads();
+  return before;
+}
+
+__global__ void __launch_bounds__(kSelThreads)
+topk_kernel(const __grid_constant__ SelParams p, const float *__restrict__ dev,
+            int32_t *__restrict__ idx_out) {
+  __shared__ uint32_t hist[256];
+  __shared__ int warp_buf[32];
+  __shared__ uint32_t s_prefix, s_mask;
+  __shared__ int s_remaining;
+  const SelReq &q = p.r[blockIdx.x];
+  const int n = q.n_ctx;
+  const int k = q.k;
+  if (k <= 0) return;
+  const float *d = dev + q.dev_offset;
+  int32_t *out = idx_out + q.idx_offset;
+  const int tid = threadIdx.x;
+
+  if (tid == 0) { s_prefix = 0; s_mask = 0; s_remaining = k; }
+  // ---- radix select of the k-th largest key, 8 bits per pass, MSB first
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int j = tid; j < 256; j += kSelThreads) hist[j] = 0;
+    __syncthreads();
+    const uint32_t prefix = s_prefix, mask = s_mask;
+    for (int base = 0; base < n; base += kSelThreads) {
+      const int i = base + tid;
+      bool active = false;
+      uint32_t digit = 0;
+      if (i < n) {
+        const uint32_t key = float_key(__ldg(d + i));
+        if ((key & mask) == prefix) { active = true; digit = (key >> shift) & 255u; }
+      }
+      // warp-aggregated histogram update: one atomic per distinct digit
+      const unsigned act = __ballot_sync(0xffffffffu, active);
+      if (active) {
+        const unsigned peers = __match_any_sync(act, digit);
+        if ((tid & 31) == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
+      }
+    }
+    __syncthreads();
+    if (tid < 32) {
+      // find the digit holding the remaining-th largest: walk digits from
+      // 255 down; each lane owns 8 consecutive digits.
+      const int lane = tid;
+      const int hi = 255 - lane * 8;
+      uint32_t cnt[8];
+      uint32_t mysum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) { cnt[j] = hist[hi - j]; mysum += cnt[j]; }
+      // inclusive scan over lanes (lane 0 holds the highest digits)
+      uint32_t incl = mysum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t excl = incl - mysum;
+      const uint32_t rem = (uint32_t)s_remaining;
+      const bool mine = excl < rem && incl >= rem;
+      const unsigned who = __ballot_sync(0xffffffffu, mine);
+      if (mine) {
+        uint32_t acc = excl;
+        int j = 0;
+        for (; j < 8; ++j) {
+          if (acc + cnt[j] >= rem) break;
+          acc += cnt[j];
+        }
+        const uint32_t dig = (uint32_t)(hi - j);
+        s_prefix = prefix | (dig << shift);
+        s_mask = mask | (255u << shift);
+        s_remaining = (int)(rem - acc);
+      }
+      (void)who;
+    }
+    __syncthreads();
+  }
+  const uint32_t thr = s_prefix;     // key of the k-th largest value
+  const int need_eq = s_remaining;   // how many keys equal to thr to take
+  // ---- ordered compaction: keep key > thr, and the first need_eq keys
+  // equal to thr in index order.
+  int taken_eq = 0, written = 0;
+  for (int base = 0; base < n; base += kSelThreads) {
+    const int i = base + tid;
+    uint32_t key = 0;
+    if (i < n) key = float_key(__ldg(d + i));
+    const int gt = (i < n && key > thr) ? 1 : 0;
+    const int eq = (i < n && key == thr) ? 1 : 0;
+    int eq_total;
+    const int eq_before = block_exclusive_scan(eq, warp_buf, &eq_total);
+    const int sel = gt || (eq && (taken_eq + eq_before) < need_eq);
+    int sel_total;
+    const int pos = block_exclusive_scan(sel, warp_buf, &sel_total);
+    if (sel) out[written + pos] = i;
+    written += sel_total;
+    taken_eq += eq_total;
+    if (written >= k) break;
+  }
+}
+
+cudaError_t launch_topk(const float *dev, const SelReq *reqs, int n_req,
+                        int32_t *idx_out, cudaStream_t s) {
+  if (n_req == 0) return cudaSuccess;
+  SelParams p;
+  fill_params(p, reqs, n_req);
+  topk_kernel<<<n_req, kSelThreads, 0, s>>>(p, dev, idx_out);
+  return launched(1);
+}
+
+// ----------------------------------------------------------- doc-aligned --
+// One CTA per request.  Spans: offsets spans[span_begin .. +n_spans] (local
+// context positions).  Steps: per-span double sums (one warp per span, fixed
+// order), rank by mean (ties: lower span), greedy whole spans, then the
+// max-total window (ties: leftmost) of the remainder inside the first span
+// that does not fit, then ordered compaction of the chosen positions.
+struct DocParams {
+  SelParams sel;
+  int n_spans_total;
+  int32_t spans[CB_MAX_SPANS + CB_MAX_BATCH];
+};
+
+__global__ void __launch_bounds__(kSelThreads)
+doc_aligned_kernel(const __grid_constant__ DocParams P,
+                   const float *__restrict__ dev, int32_t *__restrict__ idx_out,
+                   int *status) {
+  __shared__ double s_sum[CB_MAX_SPANS];
+  __shared__ int s_rank_of[CB_MAX_SPANS];    // span id at rank r
+  __shared__ unsigned char s_take[CB_MAX_SPANS];
+  __shared__ int warp_buf[32];
+  __shared__ double s_best[32];
+  __shared__ int s_best_i[32];
+  __shared__ int s_part_span, s_rem;
+  const SelReq &q = P.sel.r[blockIdx.x];
+  const int k = q.k;
+  if (k <= 0) return;
+  const int m = q.n_spans;
+  const int32_t *off = P.spans + q.span_begin;
+  const float *d = dev + q.dev_offset;
+  int32_t *out = idx_out + q.idx_offset;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+
+  for (int j = w; j < m; j += kSelThreads / 32) {
+    double acc = 0.0;
+    for (int i = off[j] + lane; i < off[j + 1]; i += 32) acc += (double)__ldg(d + i);
+    acc = warp_sum_d(acc);
+    if (lane == 0) s_sum[j] = acc;
+  }
+  for (int j = tid; j < m; j += kSelThreads) s_take[j] = 0;
+  __syncthreads();
+  // rank of span j among non-empty spans by (mean desc, index asc)
+  for (int j = tid; j < m; j += kSelThreads) {
+    const int lj = off[j + 1] - off[j];
+    if (lj <= 0) continue;
+    const double rj = s_sum[j] / lj;
+    int rank = 0;
+    for (int i = 0; i < m; ++i) {
+      const int li = off[i + 1] - off[i];
+      if (li <= 0 || i == j) continue;
+      const double ri = s_sum[i] / li;
+      if (ri > rj || (ri == rj && i < j)) ++rank;
+    }
+    s_rank_of[rank] = j;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int n_nonempty = 0;
+    for (int j = 0; j < m; ++j) n_nonempty += (off[j + 1] > off[j]);
+    int rem = k, part = -1;
+    for (int r = 0; r < n_nonempty && rem > 0; ++r) {
+      const int j = s_rank_of[r];
+      const int lj = off[j + 1] - off[j];
+      if (lj <= rem) { s_take[j] = 1; rem -= lj; }
+      else { part = j; break; }
+    }
+    s_part_span = part;
+    s_rem = part >= 0 ? rem : 0;
+    if (rem > 0 && part < 0) report(status, CB_ERR_INVALID_ARG);  // k > N
+  }
+  __syncthreads();
+  int win_start = -1;
+  const int rem = s_rem;
+  if (rem > 0) {
+    const int a = off[s_part_span], b = off[s_part_span + 1];
+    const int n_win = b - a - rem + 1;
+    double best = -1.0;
+    int best_i = 0x7fffffff;
+    for (int t = tid; t < n_win; t += kSelThreads) {
+      double acc = 0.0;
+      for (int i = a + t; i < a + t + rem; ++i) acc += (double)__ldg(d + i);
+      if (acc > best || (acc == best && a + t < best_i)) { best = acc; best_i = a + t; }
+    }
+    // block arg-max, ties to the lower start
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const double ob = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
+      if (ob > best || (ob == best && oi < best_i)) { best = ob; best_i = oi; }
+    }
+    if (lane == 0) { s_best[w] = best; s_best_i[w] = best_i; }
+    __syncthreads();
+    if (tid == 0) {
+      double bb = s_best[0];
+      int bi = s_best_i[0];
+      for (int j = 1; j < kSelThreads / 32; ++j)
+        if (s_best[j] > bb || (s_best[j] == bb && s_best_i[j] < bi)) { bb = s_best[j]; bi = s_best_i[j]; }
+      s_best_i[0] = bi;
+    }
+    __syncthreads();
+    win_start = s_best_i[0];
+  }
+  // ordered compaction over the context positions
+  const int n = q.n_ctx;
+  int written = 0;
+  int span = 0;
+  for (int base = 0; base < n; base += kSelThreads) {
+    const int i = base + tid;
+    int sel = 0;
+    if (i < n) {
+      // span of position i (binary search, spans cover [0, n))
+      int lo = 0, hi = m - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (off[mid] <= i) lo = mid; else hi = mid - 1;
+      }
+      span = lo;
+      sel = s_take[span] || (rem > 0 && i >= win_start && i < win_start + rem);
+    }
+    int total;
+    const int pos = block_exclusive_scan(sel, warp_buf, &total);
+    if (sel) out[written + pos] = i;
+    written += total;
+  }
+}
+
+cudaError_t launch_doc_aligned(const float *dev, const SelReq *reqs, int n_req,
+                               const int32_t *span_offsets, int n_spans_total,
+                               int32_t *idx_out, int *status, cudaStream_t s) {
+  if (n_req == 0) return cudaSuccess;
+  DocParams *P = new DocParams;
+  fill_params(P->sel, reqs, n_req);
+  P->n_spans_total = n_spans_total;
+  for (int i = 0; i < n_spans_total; ++i) P->spans[i] = span_offsets[i];
+  doc_aligned_kernel<<<n_req, kSelThreads, 0, s>>>(*P, dev, idx_out, status);
+  delete P;
+  return launched(1);
+}
+
+// ------------------------------------------------------------- row maps --
+// Computed row r of request b: the first k_b rows are the selected context
+// positions, the remaining ones the uncached positions N_b .. T_b-1; both
+// parts are ascending, so the rows are ascending by position.
+__global__ void build_rows_kernel(const __grid_constant__ BatchMeta bm,
+                                  const int32_t *__restrict__ sel,
+                                  int32_t *__restrict__ pos,
+                                  int32_t *__restrict__ glob, int n_rows,
+                                  int *status) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= n_rows) return;
+  int b = 0;
+  while (bm.r_off[b + 1] <= r) ++b;
+  const int j = r - bm.r_off[b];
+  const int kb = bm.k_off[b + 1] - bm.k_off[b];
+  int p = j < kb ? sel[bm.k_off[b] + j] : bm.n_ctx[b] + (j - kb);
+  if (p < 0 || p >= (j < kb ? bm.n_ctx[b] : bm.t_off[b + 1] - bm.t_off[b])) {
+    report(status, CB_ERR_DEVICE_INDEX);
+    p = 0;
+  }
+  pos[r] = p;
+  glob[r] = bm.t_off[b] + p;
+}
+
+cudaError_t launch_build_rows(const BatchMeta &bm, const int32_t *sel,
+                              int32_t *pos, int32_t *glob, int n_rows,
+                              int *status, cudaStream_t s) {
+  if (n_rows == 0) return cudaSuccess;
+  build_rows_kernel<<<(n_rows + 255) / 256, 256, 0, s>>>(bm, sel, pos, glob, n_rows,
+                                                         status);
+  return launched(1);
+}
+
+__global__ void iota_rows_kernel(const __grid_constant__ BatchMeta bm,
+                                 int32_t *__restrict__ pos,
+                                 int32_t *__restrict__ glob, int n_rows) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= n_rows) return;
+  int b = 0;
+  while (bm.t_off[b + 1] <= r) ++b;
+  pos[r] = r - bm.t_off[b];
+  glob[r] = r;
+}
+
+cudaError_t launch_iota_rows(const BatchMeta &bm, int32_t *pos, int32_t *glob,
+                             int n_rows, cudaStream_t s) {
+  if (n_rows == 0) return cudaSuccess;
+  iota_rows_kernel<<<(n_rows + 255) / 256, 256, 0, s>>>(bm, pos, glob, n_rows);
+  return launched(1);
+}
+
+}  // namespace cb

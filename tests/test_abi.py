@@ -1,0 +1,109 @@
+"""The C ABI without a GPU: the library loads, exports every entry point the
+header declares, its ctypes mirrors match the C struct layouts, and host-side
+validation rejects bad arguments before anything touches a device."""
+import ctypes as C
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+import rag_kv_cache_layer_gb300 as R
+from rag_kv_cache_layer_gb300 import _lib as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cacheblend.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(cb_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_entry_point_is_exported():
+    names = _declared()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(L.lib, n), n
+    assert sorted(L.EXPORTED) == sorted(n for n in names if n in L.EXPORTED)
+    assert set(names) <= set(L.EXPORTED) | set(getattr(L, "EXTRA_EXPORTED", []))
+
+
+STRUCTS = {
+    "cb_stitch_desc": (L.StitchDesc, ["k_src", "v_src", "src_layer_stride", "len", "dst_row", "delta"]),
+    "cb_select_req": (L.SelectReq, ["n_ctx", "k", "fresh_row0", "reused_row0", "dev_offset",
+                                    "idx_offset", "n_spans", "span_offsets"]),
+    "cb_attn_req": (L.AttnReq, ["q_begin", "q_end", "kv_row0", "kv_len"]),
+    "cb_model_config": (L.ModelConfig, ["n_layers", "d_model", "n_q_heads", "n_kv_heads",
+                                        "head_dim", "d_ffn", "vocab", "rope_base", "norm_eps",
+                                        "dtype", "max_positions"]),
+    "cb_layer_weights": (L.LayerWeights, ["w_qkv", "w_o", "w_gate", "w_up", "w_down",
+                                          "norm1", "norm2"]),
+    "cb_weights": (L.Weights, ["embed", "final_norm", "layers", "rope_table"]),
+    "cb_segment": (L.Segment, ["len", "k_pic", "v_pic", "pic_layer_stride", "pic_pos0"]),
+    "cb_request": (L.Request, ["tokens", "segments", "n_segments"]),
+    "cb_schedule_step": (L.ScheduleStep, ["layer", "keep"]),
+    "cb_blend_params": (L.BlendParams, ["ratio_bp", "policy", "sel_layer", "n_schedule",
+                                        "schedule", "forced_selected"]),
+    "cb_blend_out": (L.BlendOut, ["k_cache", "v_cache", "cache_layer_stride", "deviation",
+                                  "selected", "hidden", "rows", "first_token"]),
+    "cb_plan": (L.Plan, ["T_total", "N_total", "K_total", "R_total", "workspace_bytes"]),
+}
+
+
+def test_ctypes_mirrors_match_c_layout():
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "cacheblend.h"',
+             "int main(void) {"]
+    for cname, (_, fields) in STRUCTS.items():
+        lines.append(f'  printf("{cname} %zu\\n", sizeof({cname}));')
+        for f in fields:
+            lines.append(f'  printf("{cname}.{f} %zu\\n", offsetof({cname}, {f}));')
+    lines.append("  return 0; }")
+    with tempfile.TemporaryDirectory() as d:
+        src = os.path.join(d, "layout.c")
+        exe = os.path.join(d, "layout")
+        open(src, "w").write("\n".join(lines))
+        subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), src, "-o", exe],
+                       check=True)
+        out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout
+    got = dict(line.rsplit(" ", 1) for line in out.strip().splitlines())
+    for cname, (ct, fields) in STRUCTS.items():
+        assert int(got[cname]) == C.sizeof(ct), cname
+        for f in fields:
+            assert int(got[f"{cname}.{f}"]) == getattr(ct, f).offset, (cname, f)
+
+
+def test_host_validation_without_device():
+    lib = L.lib
+    assert lib.cb_version() >= 100
+    assert lib.cb_rope_table_elems(0, 64) == 0
+    assert lib.cb_rope_table_elems(10, 64) == 640
+    # NULL pointers are rejected before any CUDA call
+    st = lib.cb_kv_deviation_topk(None, 0, None, 0, 64, L.CB_F32, None, 0, 0,
+                                  None, None, None, 0, None)
+    assert st == L.CB_ERR_INVALID_ARG
+    assert "NULL" in lib.cb_last_error_message().decode()
+    assert lib.cb_rope_table_init(None, 10, 64, 1e4, None) == L.CB_ERR_INVALID_ARG
+    assert lib.cb_gather_rows(None, 0, 0, None, 0, 0, None, 0, 0, None) == L.CB_OK
+    h = C.c_void_p()
+    assert lib.cb_model_create(None, None, C.byref(h)) == L.CB_ERR_INVALID_ARG
+    cfg = L.ModelConfig(2, 256, 4, 2, 48, 688, 4096, 1e4, 1e-5, 0, 1024)
+    w = L.Weights(None, None, None, None)
+    assert lib.cb_model_create(C.byref(cfg), C.byref(w), C.byref(h)) == L.CB_ERR_UNSUPPORTED
+    assert lib.cb_debug_expire_wait(-1, None) == L.CB_ERR_INVALID_ARG
+    # bad doc-aligned spans are rejected on the host
+    spans = (C.c_int32 * 3)(0, 5, 4)
+    req = L.SelectReq(4, 2, 0, 0, 0, 0, 2, C.cast(spans, C.POINTER(C.c_int32)))
+    ws = C.create_string_buffer(4096)
+    st = lib.cb_kv_deviation_topk(C.c_void_p(16), 64, C.c_void_p(16), 64, 64, L.CB_F32,
+                                  C.byref(req), 1, L.CB_POLICY_DOC_ALIGNED, C.c_void_p(16),
+                                  C.c_void_p(16), ws, 4096, None)
+    assert st == L.CB_ERR_INVALID_ARG
+
+
+def test_select_count_matches_page_rule():
+    assert R.select_count(3072, 1500) == 460
+    assert R.select_count(100, 0) == 0
+    assert R.select_count(10, 1) == 1

@@ -96,7 +96,7 @@ def test_zero_recompute_is_direct_reuse():
     Kc = np.concatenate([K, np.zeros((m.n_layers, len(query), K.shape[2]))], 1)
     Vc = np.concatenate([V, np.zeros_like(Kc[:, N:])], 1)
     qrows = np.arange(N, T)
-    h = m.embed[query].copy()
+    h = O.embed_rows(m, query)
     for l in range(m.n_layers):
         h, _, _ = O.decoder_layer(m, l, h, qrows, Kc[l], Vc[l], qrows)
     _close(r.hidden, h, 1e-9)
