@@ -105,7 +105,7 @@ def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
             f"{LIB_PATH} is missing: build it with "
-            "`python -m rag_kv_cache_layer_gb300.build` (there is no CPU path)")
+            "`python rag_kv_cache_layer_gb300/build.py` (there is no CPU path)")
     lib = C.CDLL(LIB_PATH)
     S = i32  # cb_status
     sigs = {

@@ -24,6 +24,7 @@ SOURCES = [
     "k_select.cu",
     "k_rows.cu",
     "k_gemm_simt.cu",
+    "k_gemm_tc.cu",
     "k_attn_simt.cu",
 ]
 

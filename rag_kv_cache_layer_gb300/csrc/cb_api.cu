@@ -370,10 +370,20 @@ extern "C" cb_status cb_model_create(const cb_model_config *cfg, const cb_weight
 extern "C" void cb_model_destroy(cb_model *m) { delete m; }
 
 // ----------------------------------------------------------------- linear --
+// bf16 projections run on the tcgen05 kernel; the fp32 parity path keeps
+// CUDA-core FMAs (tensor cores would round its operands).
 static cb_status run_linear(const cb_model *m, const void *A, int64_t lda, const void *W,
                             const void *W2, int64_t ldw, int M, int N, int K, GemmEpi epi,
-                            void *out, int64_t ldo, cudaStream_t s) {
-  CB_CUDA(launch_gemm_simt(A, lda, W, W2, ldw, M, N, K, epi, out, ldo, m->cfg.dtype, s));
+                            void *out, int64_t ldo, cudaStream_t s,
+                            const QkvEpi *qkv = nullptr) {
+  if (m->cfg.dtype == CB_BF16) {
+    int *st;
+    CB_TRY(status_ptr(&st));
+    CB_CUDA(launch_gemm_tc(A, lda, W, W2, ldw, M, N, K, epi, out, ldo, qkv, st, s));
+  } else {
+    if (epi == EPI_QKV) return fail(CB_ERR_UNSUPPORTED, "fused QKV epilogue is bf16-only");
+    CB_CUDA(launch_gemm_simt(A, lda, W, W2, ldw, M, N, K, epi, out, ldo, m->cfg.dtype, s));
+  }
   return CB_OK;
 }
 
@@ -384,6 +394,12 @@ extern "C" cb_status cb_linear(const cb_model *m, const void *A, int64_t ld_a,
   if (!m || !A || !W || !out) return fail(CB_ERR_INVALID_ARG, "NULL pointer");
   if (M < 0 || N <= 0 || K <= 0 || K % 16) return fail(CB_ERR_INVALID_ARG, "need M >= 0, N > 0, K %% 16 == 0");
   if (ld_a < K || ld_w < K || ld_out < N) return fail(CB_ERR_INVALID_ARG, "leading dimension too small");
+  if (m->cfg.dtype == CB_BF16) {
+    // TMA: 16-byte aligned bases and row strides; 16-byte output vectors
+    if (!aligned16(A) || !aligned16(W) || (W2 && !aligned16(W2)) || !aligned16(out) ||
+        (ld_a * 2) % 16 || (ld_w * 2) % 16 || N % 8 || (ld_out * (epi == CB_EPI_RESID ? 4 : 2)) % 16)
+      return fail(CB_ERR_INVALID_ARG, "bf16 GEMM needs 16-byte aligned rows and N %% 8 == 0");
+  }
   GemmEpi e;
   switch (epi) {
     case CB_EPI_STORE: e = EPI_STORE; break;
@@ -595,11 +611,18 @@ static cb_status layer_forward(cb_model *m, int l, float *h, int n, const int32_
   const int d = c.d_model, F = c.d_ffn, hd = c.head_dim;
   const cb_dtype dt = c.dtype;
   CB_CUDA(launch_rmsnorm(h, d, nullptr, n, d, L.norm1, c.norm_eps, S.x, d, dt, s));
-  CB_TRY(run_linear(m, S.x, d, L.w_qkv, nullptr, d, n, m->qkv_rows, d, EPI_STORE_F32,
-                    S.qkv32, m->qkv_rows, s));
-  CB_CUDA(launch_qkv_finish(S.qkv32, m->qkv_rows, n, pos, cache_row, c.n_q_heads,
-                            c.n_kv_heads, hd, m->w.rope_table, S.q, m->qw, kc, vc, m->kvw,
-                            dt, 0, s));
+  if (dt == CB_BF16 && hd == 128) {
+    // projection, RoPE and the Eq. 7 scatter in one kernel
+    const QkvEpi q{pos, cache_row, kc, vc, m->kvw, m->w.rope_table, c.n_q_heads, c.n_kv_heads};
+    CB_TRY(run_linear(m, S.x, d, L.w_qkv, nullptr, d, n, m->qkv_rows, d, EPI_QKV, S.q, m->qw,
+                      s, &q));
+  } else {
+    CB_TRY(run_linear(m, S.x, d, L.w_qkv, nullptr, d, n, m->qkv_rows, d, EPI_STORE_F32,
+                      S.qkv32, m->qkv_rows, s));
+    CB_CUDA(launch_qkv_finish(S.qkv32, m->qkv_rows, n, pos, cache_row, c.n_q_heads,
+                              c.n_kv_heads, hd, m->w.rope_table, S.q, m->qw, kc, vc, m->kvw,
+                              dt, 0, s));
+  }
   CB_TRY(run_attention(S.q, m->qw, pos, ar, kc, vc, m->kvw, c.n_q_heads, c.n_kv_heads, hd,
                        1.f / sqrtf((float)hd), S.o, m->qw, dt, st, s));
   CB_TRY(run_linear(m, S.o, m->qw, L.w_o, nullptr, m->qw, n, d, m->qw, EPI_RESID, h, d, s));

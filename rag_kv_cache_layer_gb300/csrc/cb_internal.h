@@ -105,13 +105,36 @@ cudaError_t launch_copy_f32(float *dst, const float *src, size_t n,
                             cudaStream_t s);
 
 // ----------------------------------------------------------------- GEMM --
-enum GemmEpi { EPI_STORE_F32 = 0, EPI_STORE = 1, EPI_RESID = 2, EPI_SWIGLU = 3 };
+enum GemmEpi {
+  EPI_STORE_F32 = 0,
+  EPI_STORE = 1,
+  EPI_RESID = 2,
+  EPI_SWIGLU = 3,
+  EPI_QKV = 4
+};
 // out = epi(A[M][K] W[N][K]^T); A and W of dtype dt; STORE_F32 and RESID
 // write float, STORE and SWIGLU write dt.
 cudaError_t launch_gemm_simt(const void *A, int64_t lda, const void *W,
                              const void *W2, int64_t ldw, int M, int N, int K,
                              GemmEpi epi, void *out, int64_t ldo, cb_dtype dt,
                              cudaStream_t s);
+
+// Arguments of the fused Q/K/V epilogue: q heads (rotated at pos[m]) go to
+// out[m], k heads (rotated) and v heads to cache row dst_row[m] of k_cache /
+// v_cache (this layer's cache, row stride ld_kv).  head_dim must be 128.
+struct QkvEpi {
+  const int32_t *pos;
+  const int32_t *dst_row;
+  void *k_cache, *v_cache;
+  int64_t ld_kv;
+  const float *rope;  // cb_rope_table_init layout
+  int n_q_heads, n_kv_heads;
+};
+// bf16 tcgen05 GEMM (sm_103a); qkv is read for EPI_QKV only.
+cudaError_t launch_gemm_tc(const void *A, int64_t lda, const void *W,
+                           const void *W2, int64_t ldw, int M, int N, int K,
+                           GemmEpi epi, void *out, int64_t ldo,
+                           const QkvEpi *qkv, int *status, cudaStream_t s);
 
 // ------------------------------------------------------------ attention --
 struct AttnReq {

@@ -107,6 +107,8 @@ def test_deviation_and_topk_small(dt):
     # adversarial ties: identical rows -> d = 0, duplicated differences
     kr[10:40] = kf[10:40]
     kr[500:600] = kf[500:600] + 0.5
+    if dt == torch.bfloat16:
+        kr = bf16_values(kr)                      # the values the GPU sees
     reqs, f0, doff, ioff = [], 3, 0, 0
     for n, k in zip(Ns, ks):
         reqs.append(dict(n_ctx=n, k=k, fresh_row0=f0, reused_row0=f0 + 7,
@@ -284,3 +286,41 @@ def test_linear_epilogues(dt_name, M):
     A64 = A.astype(np.float64)
     ref = O.silu(A64 @ lw["w_gate"].astype(np.float64).T) * (A64 @ lw["w_up"].astype(np.float64).T)
     assert_close(host(g), ref, dt)
+
+
+@pytest.mark.parametrize("M", [524, 128, 3136])
+def test_tensor_core_gemm_llama_shapes(M):
+    """bf16 tcgen05 GEMM at the workload's projection shapes (ragged M,
+    split-K residual over K = 14336, SwiGLU over N = 14336)."""
+    rng = np.random.default_rng(M)
+    shape = W.ModelShape("g", 1, 4096, 32, 8, 128, 14336, 256, dtype="bf16")
+    w = {"embed": np.zeros((256, 4096), np.float32),
+         "final_norm": np.ones(4096, np.float32),
+         "layers": [{
+             "w_qkv": _vals(rng, (6144, 4096), torch.bfloat16, 0.02),
+             "w_o": _vals(rng, (4096, 4096), torch.bfloat16, 0.02),
+             "w_gate": _vals(rng, (14336, 4096), torch.bfloat16, 0.02),
+             "w_up": _vals(rng, (14336, 4096), torch.bfloat16, 0.02),
+             "w_down": _vals(rng, (4096, 14336), torch.bfloat16, 0.02),
+             "norm1": np.ones(4096, np.float32), "norm2": np.ones(4096, np.float32)}]}
+    model = R.BlendModel.from_host(shape, w, 1024)
+    lw = w["layers"][0]
+    dw = model.w["layers"][0]
+    A = _vals(rng, (M, 4096), torch.bfloat16)
+    A64 = A.astype(np.float64)
+    out = torch.empty(M, 6144, dtype=torch.bfloat16, device="cuda")
+    model.cb_linear(dev(A, torch.bfloat16), dw["w_qkv"], out, L.CB_EPI_STORE)
+    ref = A64 @ lw["w_qkv"].astype(np.float64).T
+    assert rms_rel(host(out), ref) < 5e-3
+    G = _vals(rng, (M, 14336), torch.bfloat16)
+    h0 = rng.standard_normal((M, 4096)).astype(np.float32)
+    h = dev(h0)
+    model.cb_linear(dev(G, torch.bfloat16), dw["w_down"], h, L.CB_EPI_RESID)
+    ref = h0 + G.astype(np.float64) @ lw["w_down"].astype(np.float64).T
+    assert rms_rel(host(h), ref) < 1e-5
+    g = torch.empty(M, 14336, dtype=torch.bfloat16, device="cuda")
+    model.cb_linear(dev(A, torch.bfloat16), dw["w_gate"], g, L.CB_EPI_SWIGLU, W2=dw["w_up"])
+    ref = O.silu(A64 @ lw["w_gate"].astype(np.float64).T) * (A64 @ lw["w_up"].astype(np.float64).T)
+    assert rms_rel(host(g), ref) < 5e-3
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
