@@ -1,0 +1,436 @@
+// bf16 tensor-core selected-query attention for sm_103a (CacheBlend blog,
+// blend_layer step 4: the computed rows attend over the whole fused cache,
+// n_sel x L work; QCFuse §2.1.3: causal over the partially fused prefix).
+//
+// Work unit: one request, one kv head g and a tile of QT = 128 / G query
+// rows, where G = n_q_heads / n_kv_heads; the G q heads of the group share
+// the kv head, so the tile is 128 MMA rows (row = h * QT + query).  Queries
+// of a request are sorted by position, so a tile only visits keys up to its
+// last query's position.
+//
+// Roles (192 threads): warp 0 TMA producer (Q once, then double-buffered
+// 128-key K and V blocks, 128-byte swizzle); warp 1 owns TMEM and issues
+// tcgen05.mma: S = Q K^T (K-major operands) into a double-buffered TMEM
+// tile, and O_j = P V (P K-major from shared memory, V MN-major); warps
+// 2..5 do the online softmax (one row per thread, log2 domain, causal mask),
+// write P as bf16 in the swizzled K-major layout, and accumulate
+// O = O * exp2(m_old - m_new) + O_j in registers.  All waits are bounded.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "cb_common.cuh"
+#include "cb_internal.h"
+
+namespace cb {
+namespace attn {
+
+constexpr int kThreads = 192;
+constexpr int HD = 128;
+constexpr int BN = 128;                    // keys per block
+constexpr int kAtom = 128 * 64 * 2;        // one [128 rows x 64 bf16] swizzle tile
+constexpr int kQ = 2 * kAtom;              // Q tile: 128 rows x 128 dims
+constexpr int kKV = 2 * kAtom;             // K or V block: 128 keys x 128 dims
+constexpr int kP = 2 * kAtom;              // P tile: 128 rows x 128 keys
+// smem: Q | K[2] | V[2] | P | barriers
+constexpr int kOffK = kQ;
+constexpr int kOffV = kOffK + 2 * kKV;
+constexpr int kOffP = kOffV + 2 * kKV;
+constexpr int kOffBar = kOffP + kP;
+constexpr int kSmem = kOffBar + 256 + 1024;
+
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;                // leading byte offset (unused)
+  d |= (uint64_t)(1024 >> 4) << 32;      // 8-row groups 1024 B apart
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;                // 128-byte swizzle
+  return d;
+}
+
+// MN-major (N contiguous) operand: 64-element N atoms lbo bytes apart,
+// 8-row K groups 1024 B apart.
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+constexpr uint32_t idesc(bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(128 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map,
+                                            uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(map), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                    uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+__device__ __forceinline__ void commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+      "[%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+        "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+struct Params {
+  int n_req;
+  int G, QT, Hkv;
+  float scale_log2;            // softmax scale times log2(e)
+  int unit_off[CB_MAX_BATCH + 1];
+  AttnReq r[CB_MAX_BATCH];
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
+               const __grid_constant__ CUtensorMap mapK,
+               const __grid_constant__ CUtensorMap mapV, const __grid_constant__ Params P,
+               const int32_t *__restrict__ q_pos, bf16 *__restrict__ out, int64_t ld_out,
+               int *status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
+  uint64_t *q_full = bar + 0;
+  uint64_t *kv_full = bar + 1;     // [2]
+  uint64_t *kv_empty = bar + 3;    // [2]
+  uint64_t *s_full = bar + 5;      // [2]
+  uint64_t *s_free = bar + 7;      // [2]
+  uint64_t *p_full = bar + 9;
+  uint64_t *pv_full = bar + 10;
+  uint64_t *pv_free = bar + 11;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 12);
+  volatile int *fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  __shared__ int s_unit[4];        // b, g, tile, n_blocks
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // ---- decode the work unit (longest tiles first within a request)
+  if (threadIdx.x == 0) {
+    const int u = blockIdx.x;
+    int b = 0;
+    while (P.unit_off[b + 1] <= u) ++b;
+    const int local = u - P.unit_off[b];
+    const int n_rows = P.r[b].q_end - P.r[b].q_begin;
+    const int n_t = (n_rows + P.QT - 1) / P.QT;
+    const int t = n_t - 1 - local / P.Hkv;
+    const int g = local % P.Hkv;
+    const int last = min(n_rows, (t + 1) * P.QT) - 1;
+    int pmax = q_pos[P.r[b].q_begin + last];
+    if (pmax < 0 || pmax >= P.r[b].kv_len) { report(status, CB_ERR_DEVICE_INDEX); pmax = -1; }
+    s_unit[0] = b; s_unit[1] = g; s_unit[2] = t;
+    s_unit[3] = pmax < 0 ? 0 : pmax / BN + 1;
+    for (int i = 0; i < 12; ++i) mbar_init(smem_u32(&bar[i]), 1);
+    mbar_init(smem_u32(p_full), 128);
+    mbar_init(smem_u32(pv_free), 128);
+    mbar_init(smem_u32(&s_free[0]), 128);
+    mbar_init(smem_u32(&s_free[1]), 128);
+    *fail = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int b = s_unit[0], g = s_unit[1], t = s_unit[2], nb = s_unit[3];
+  const AttnReq &R = P.r[b];
+  const int row0 = R.q_begin + t * P.QT;          // first q row of the tile
+  const int n_valid = min(P.QT, R.q_end - row0);  // q rows of the request in the tile
+
+  if (nb > 0 && warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    const uint32_t qb = smem_u32(q_full);
+    expect_tx(qb, kQ);
+    for (int h = 0; h < P.G; ++h)
+      for (int half = 0; half < 2; ++half)
+        tma_load_2d(smem_u32(smem + half * kAtom + h * P.QT * 128), &mapQ, qb,
+                    (g * P.G + h) * HD + half * 64, row0);
+    for (int j = 0; j < nb; ++j) {
+      const int s = j & 1;
+      if (!mbar_wait_bounded(smem_u32(&kv_empty[s]), ((j >> 1) & 1) ^ 1, kWaitLimitNs, status) ||
+          *fail) {
+        *fail = 1;
+        break;
+      }
+      const uint32_t fb = smem_u32(&kv_full[s]);
+      expect_tx(fb, 2 * kKV);
+      const int key_row = (int)R.kv_row0 + j * BN;
+      for (int half = 0; half < 2; ++half) {
+        tma_load_2d(smem_u32(smem + kOffK + s * kKV + half * kAtom), &mapK, fb,
+                    g * HD + half * 64, key_row);
+        tma_load_2d(smem_u32(smem + kOffV + s * kKV + half * kAtom), &mapV, fb,
+                    g * HD + half * 64, key_row);
+      }
+    }
+  } else if (nb > 0 && warp == 1 && lane == 0) {
+    // ----------------------------------------------------------------- MMA
+    const uint32_t idS = idesc(false), idPV = idesc(true);
+    const uint32_t q_addr = smem_u32(smem), p_addr = smem_u32(smem + kOffP);
+    bool ok = mbar_wait_bounded(smem_u32(q_full), 0, kWaitLimitNs, status);
+    auto issue_s = [&](int j) -> bool {
+      const int s = j & 1;
+      if (!mbar_wait_bounded(smem_u32(&kv_full[s]), (j >> 1) & 1, kWaitLimitNs, status)) return false;
+      if (!mbar_wait_bounded(smem_u32(&s_free[s]), ((j >> 1) & 1) ^ 1, kWaitLimitNs, status)) return false;
+      fence_after();
+      const uint32_t k_addr = smem_u32(smem + kOffK + s * kKV);
+#pragma unroll
+      for (int k = 0; k < HD / 16; ++k) {
+        const uint32_t off = (k >> 2) * kAtom + (k & 3) * 32;
+        mma(tmem + s * BN, desc_kmajor(q_addr + off), desc_kmajor(k_addr + off), idS, k > 0);
+      }
+      commit(smem_u32(&s_full[s]));
+      return true;
+    };
+    if (ok) ok = issue_s(0);
+    for (int j = 0; j < nb && ok && !*fail; ++j) {
+      const int s = j & 1;
+      if (j + 1 < nb && !issue_s(j + 1)) { ok = false; break; }
+      if (!mbar_wait_bounded(smem_u32(p_full), j & 1, kWaitLimitNs, status) ||
+          !mbar_wait_bounded(smem_u32(pv_free), (j & 1) ^ 1, kWaitLimitNs, status)) {
+        ok = false;
+        break;
+      }
+      fence_after();
+      const uint32_t v_addr = smem_u32(smem + kOffV + s * kKV);
+#pragma unroll
+      for (int k = 0; k < BN / 16; ++k) {
+        const uint32_t poff = (k >> 2) * kAtom + (k & 3) * 32;
+        mma(tmem + 2 * BN, desc_kmajor(p_addr + poff),
+            desc_mnmajor(v_addr + k * 16 * 128, kAtom), idPV, k > 0);
+      }
+      commit(smem_u32(pv_full));
+      commit(smem_u32(&kv_empty[s]));
+    }
+    if (!ok) *fail = 1;
+  } else if (nb > 0 && warp >= 2) {
+    // ------------------------------------------------------------- softmax
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;             // MMA row = h * QT + qi
+    const int h = row / P.QT, qi = row % P.QT;
+    const bool valid = qi < n_valid;
+    int p = valid ? q_pos[row0 + qi] : 0;
+    if (p < 0 || p >= R.kv_len) p = 0;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    uint8_t *prow = smem + kOffP + row * 128;
+    float o[HD];
+#pragma unroll
+    for (int i = 0; i < HD; ++i) o[i] = 0.f;
+    float m = -INFINITY, l = 0.f;
+    const float sl2 = P.scale_log2;
+    for (int j = 0; j < nb; ++j) {
+      const int s = j & 1;
+      if (!mbar_wait_bounded(smem_u32(&s_full[s]), (j >> 1) & 1, kWaitLimitNs, status) || *fail) {
+        *fail = 1;
+        break;
+      }
+      fence_after();
+      const uint32_t sbase = tmem + lane_off + s * BN;
+      const int key0 = j * BN;
+      float mloc = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        float x[32];
+        ld32(sbase + c, x);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (key0 + c + i <= p) mloc = fmaxf(mloc, x[i]);
+      }
+      const float m_new = fmaxf(m, mloc * sl2);
+      const float corr = exp2f(m - m_new);
+      l *= corr;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        float x[32];
+        ld32(sbase + c, x);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float p0 = (key0 + c + i <= p) ? exp2f(x[i] * sl2 - m_new) : 0.f;
+          const float p1 = (key0 + c + i + 1 <= p) ? exp2f(x[i + 1] * sl2 - m_new) : 0.f;
+          l += p0 + p1;
+          __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
+          pk[i / 2] = *reinterpret_cast<uint32_t *>(&v2);
+        }
+        // keys c .. c+31 -> atom c / 64, 16-byte chunks (c % 64) / 8 .. +3
+        uint8_t *atom = prow + (c >> 6) * kAtom;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int chunk = ((c & 63) >> 3) + q4;
+          *reinterpret_cast<uint4 *>(atom + ((chunk ^ (row & 7)) << 4)) =
+              make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+        }
+      }
+      fence_before();
+      arrive(smem_u32(&s_free[s]));
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      arrive(smem_u32(p_full));
+      if (!mbar_wait_bounded(smem_u32(pv_full), j & 1, kWaitLimitNs, status) || *fail) {
+        *fail = 1;
+        break;
+      }
+      fence_after();
+      const uint32_t obase = tmem + lane_off + 2 * BN;
+#pragma unroll
+      for (int c = 0; c < HD; c += 32) {
+        float y[32];
+        ld32(obase + c, y);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[c + i] = o[c + i] * corr + y[i];
+      }
+      fence_before();
+      arrive(smem_u32(pv_free));
+      m = m_new;
+    }
+    if (valid && !*fail) {
+      const float inv = 1.f / l;
+      bf16 *dst = out + (int64_t)(row0 + qi) * ld_out + (g * P.G + h) * HD;
+#pragma unroll
+      for (int c = 0; c < HD; c += 8) {
+        uint4 pk;
+        __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) e[i] = __floats2bfloat162_rn(o[c + 2 * i] * inv, o[c + 2 * i + 1] * inv);
+        *reinterpret_cast<uint4 *>(dst + c) = pk;
+      }
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 0 && lane == 0 && *fail) {
+    // drain the K/V copies this CTA may still have in flight
+    for (int s = 0; s < 2; ++s) mbar_wait_bounded(smem_u32(&kv_full[s]), 0, 10000000ull, nullptr);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host --
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+static bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols,
+                     int64_t ld, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace attn
+
+bool attention_tc_supported(int Hq, int Hkv, int hd) {
+  if (hd != attn::HD || Hq % Hkv) return false;
+  const int G = Hq / Hkv;
+  return G == 1 || G == 2 || G == 4 || G == 8;
+}
+
+cudaError_t launch_attention_tc(const void *q, int64_t ld_q, const int32_t *q_pos,
+                                const AttnReq *reqs, int n_req, const void *k_cache,
+                                const void *v_cache, int64_t ld_kv, int Hq, int Hkv,
+                                float scale, void *out, int64_t ld_out, int *status,
+                                cudaStream_t s) {
+  using namespace attn;
+  Params P;
+  P.n_req = n_req;
+  P.G = Hq / Hkv;
+  P.QT = 128 / P.G;
+  P.Hkv = Hkv;
+  P.scale_log2 = scale * 1.4426950408889634f;
+  P.unit_off[0] = 0;
+  int64_t q_rows = 0, kv_rows = 0;
+  for (int i = 0; i < n_req; ++i) {
+    P.r[i] = reqs[i];
+    const int n = reqs[i].q_end - reqs[i].q_begin;
+    P.unit_off[i + 1] = P.unit_off[i] + Hkv * ((n + P.QT - 1) / P.QT);
+    if (reqs[i].q_end > q_rows) q_rows = reqs[i].q_end;
+    if (reqs[i].kv_row0 + reqs[i].kv_len > kv_rows) kv_rows = reqs[i].kv_row0 + reqs[i].kv_len;
+  }
+  const int units = P.unit_off[n_req];
+  if (units == 0) return cudaSuccess;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, q_rows, (int64_t)Hq * HD, ld_q, P.QT) ||
+      !make_map(&mk, k_cache, kv_rows, (int64_t)Hkv * HD, ld_kv, BN) ||
+      !make_map(&mv, v_cache, kv_rows, (int64_t)Hkv * HD, ld_kv, BN))
+    return cudaErrorInvalidValue;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  attn_tc_kernel<<<units, kThreads, kSmem, s>>>(mq, mk, mv, P, q_pos,
+                                                reinterpret_cast<bf16 *>(out), ld_out, status);
+  return launched(1);
+}
+
+}  // namespace cb
