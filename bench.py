@@ -47,6 +47,11 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="warm up, then run one step between cudaProfilerStart/Stop "
+                         "(for ncu --profile-from-start off); prints no JSON")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="truncate the stack (profiling captures on a small footprint)")
     return ap.parse_args()
 
 
@@ -134,10 +139,10 @@ def device_weights(shape, seed, device):
     return w
 
 
-def setup_replica(rank, device):
+def setup_replica(rank, device, n_layers=None):
     import torch
     import rag_kv_cache_layer_gb300 as R
-    wl = W.llama_rag(seed=1 + rank)
+    wl = W.llama_rag(seed=1 + rank, n_layers=n_layers)
     shape = wl.model
     model = R.BlendModel(shape, device_weights(shape, 1234 + rank, device), 4096, device)
     rq = wl.requests[0]
@@ -283,13 +288,25 @@ def run_ours(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=device)
 
-    wl, model, store, reqs, plan, outs, tok_host, tok_dev = setup_replica(rank, device)
+    wl, model, store, reqs, plan, outs, tok_host, tok_dev = setup_replica(rank, device, args.layers)
     T = int(plan.T_total)
     B = 1
     st = torch.cuda.current_stream()
 
     def step():
         model.cb_blend_prefill(reqs, RATIO_BP, outputs=outs)
+
+    if args.profile:
+        for _ in range(max(args.warmup, 1)):
+            step()
+        torch.cuda.synchronize()
+        torch.cuda.cudart().cudaProfilerStart()
+        step()
+        torch.cuda.synchronize()
+        torch.cuda.cudart().cudaProfilerStop()
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     for _ in range(max(args.warmup, 3)):
         step()

@@ -26,6 +26,7 @@ SOURCES = [
     "k_gemm_simt.cu",
     "k_gemm_tc.cu",
     "k_attn_simt.cu",
+    "k_attn_tc.cu",
 ]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -281,8 +281,12 @@ static cb_status run_attention(const void *q, int64_t ld_q, const int32_t *q_pos
                                const void *vc, int64_t ld_kv, int Hq, int Hkv, int hd,
                                float scale, void *out, int64_t ld_out, cb_dtype dt,
                                int *st, cudaStream_t s) {
-  CB_CUDA(launch_attention_simt(q, ld_q, q_pos, reqs.data(), (int)reqs.size(), kc, vc,
-                                ld_kv, Hq, Hkv, hd, scale, out, ld_out, dt, st, s));
+  if (dt == CB_BF16 && attention_tc_supported(Hq, Hkv, hd))
+    CB_CUDA(launch_attention_tc(q, ld_q, q_pos, reqs.data(), (int)reqs.size(), kc, vc, ld_kv,
+                                Hq, Hkv, scale, out, ld_out, st, s));
+  else
+    CB_CUDA(launch_attention_simt(q, ld_q, q_pos, reqs.data(), (int)reqs.size(), kc, vc,
+                                  ld_kv, Hq, Hkv, hd, scale, out, ld_out, dt, st, s));
   return CB_OK;
 }
 

@@ -150,6 +150,15 @@ cudaError_t launch_attention_simt(const void *q, int64_t ld_q,
                                   int64_t ld_out, cb_dtype dt, int *status,
                                   cudaStream_t s);
 
+// bf16 tcgen05 attention (head_dim 128, group size 1/2/4/8); queries of a
+// request ascending by position.
+bool attention_tc_supported(int Hq, int Hkv, int hd);
+cudaError_t launch_attention_tc(const void *q, int64_t ld_q, const int32_t *q_pos,
+                                const AttnReq *reqs, int n_req, const void *k_cache,
+                                const void *v_cache, int64_t ld_kv, int Hq, int Hkv,
+                                float scale, void *out, int64_t ld_out, int *status,
+                                cudaStream_t s);
+
 // ---------------------------------------------------------------- debug --
 cudaError_t launch_expire_wait(int limit_us, int *status, cudaStream_t s);
 

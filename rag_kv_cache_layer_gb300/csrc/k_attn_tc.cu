@@ -162,11 +162,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
     if (pmax < 0 || pmax >= P.r[b].kv_len) { report(status, CB_ERR_DEVICE_INDEX); pmax = -1; }
     s_unit[0] = b; s_unit[1] = g; s_unit[2] = t;
     s_unit[3] = pmax < 0 ? 0 : pmax / BN + 1;
-    for (int i = 0; i < 12; ++i) mbar_init(smem_u32(&bar[i]), 1);
+    // single-arrival barriers (TMA transactions or tcgen05.commit) ...
+    mbar_init(smem_u32(q_full), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&kv_full[i]), 1);
+      mbar_init(smem_u32(&kv_empty[i]), 1);
+      mbar_init(smem_u32(&s_full[i]), 1);
+      mbar_init(smem_u32(&s_free[i]), 128);   // ... and the 128 softmax threads
+    }
     mbar_init(smem_u32(p_full), 128);
+    mbar_init(smem_u32(pv_full), 1);
     mbar_init(smem_u32(pv_free), 128);
-    mbar_init(smem_u32(&s_free[0]), 128);
-    mbar_init(smem_u32(&s_free[1]), 128);
     *fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -268,7 +274,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
     const float sl2 = P.scale_log2;
     for (int j = 0; j < nb; ++j) {
       const int s = j & 1;
-      if (!mbar_wait_bounded(smem_u32(&s_full[s]), (j >> 1) & 1, kWaitLimitNs, status) || *fail) {
+      // failures leave the loop warp-uniformly (the TMEM loads are .sync.aligned)
+      bool bad = !mbar_wait_bounded(smem_u32(&s_full[s]), (j >> 1) & 1, kWaitLimitNs, status) ||
+                 *fail;
+      if (__any_sync(0xffffffffu, bad)) {
         *fail = 1;
         break;
       }
@@ -313,7 +322,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
       arrive(smem_u32(&s_free[s]));
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       arrive(smem_u32(p_full));
-      if (!mbar_wait_bounded(smem_u32(pv_full), j & 1, kWaitLimitNs, status) || *fail) {
+      bad = !mbar_wait_bounded(smem_u32(pv_full), j & 1, kWaitLimitNs, status) || *fail;
+      if (__any_sync(0xffffffffu, bad)) {
         *fail = 1;
         break;
       }

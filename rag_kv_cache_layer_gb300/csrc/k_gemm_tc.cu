@@ -302,8 +302,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
       const int m_blk = u % n_m;
       const int rest = u / n_m;
       const int n_blk = rest / splits;
-      if (!mbar_wait_bounded(smem_u32(&tfull[buf]), bphase, kWaitLimitNs, status) ||
-          *fail_flag) {
+      // leave warp-uniformly on failure: the TMEM loads are .sync.aligned
+      const bool bad =
+          !mbar_wait_bounded(smem_u32(&tfull[buf]), bphase, kWaitLimitNs, status) || *fail_flag;
+      if (__any_sync(0xffffffffu, bad)) {
         *fail_flag = 1;
         break;
       }
