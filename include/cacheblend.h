@@ -202,6 +202,30 @@ cb_status cb_kv_deviation_topk(const void *k_fresh, int64_t ld_fresh,
                                int32_t *idx_out, void *ws, size_t ws_bytes,
                                cb_stream stream);
 
+/* The same deviation and selection as cb_kv_deviation_topk, for callers that
+ * cannot allocate device memory (code enqueuing work while another component
+ * owns every device allocation, or where an allocation's implicit device
+ * synchronisation is not acceptable).  The pages have no counterpart: this
+ * is an integration variant.  The per-token deviations live in a fixed 4 MiB
+ * device array inside the library instead of caller memory, so a call takes
+ * no dev_out and no workspace; req.dev_offset is ignored (the library packs
+ * the deviations request after request) and the selected indices go to
+ * idx_out exactly as in cb_kv_deviation_topk.
+ * Limit: at most 1048576 context tokens (sum of n_ctx) per call; larger calls
+ * return CB_ERR_INVALID_ARG and enqueue nothing.
+ * The first call on each device resolves the array's device address, so make
+ * it before capturing a stream into a CUDA graph.  Every call shares the
+ * array (it keeps the last call's contents; nothing in it needs to start at
+ * zero), so calls whose execution overlaps on the GPU race and must be
+ * serialised by the caller.  The array is held by every device that loads
+ * the library until the process exits.  Allocates nothing. */
+cb_status cb_kv_deviation_topk_noalloc(const void *k_fresh, int64_t ld_fresh,
+                                       const void *k_reused, int64_t ld_reused,
+                                       int row_elems, cb_dtype dtype,
+                                       const cb_select_req *reqs, int n_req,
+                                       cb_policy policy, int32_t *idx_out,
+                                       cb_stream stream);
+
 /* Row gather ([CB] blend_layer step 1, h[hkvd_idx]):
  *   dst[i * ld_dst + c] = src[idx[i] * ld_src + c], i < n, c < row_elems.
  * idx: device int32 [n]; every idx[i] must lie in [0, src_rows); an index

@@ -122,6 +122,8 @@ def _load():
         "cb_kv_deviation_topk": (S, [vp, i64, vp, i64, i32, i32,
                                      C.POINTER(SelectReq), i32, i32, vp, vp, vp,
                                      C.c_size_t, vp]),
+        "cb_kv_deviation_topk_noalloc": (S, [vp, i64, vp, i64, i32, i32,
+                                             C.POINTER(SelectReq), i32, i32, vp, vp]),
         "cb_gather_rows": (S, [vp, i64, i64, vp, i32, i32, vp, i64, i32, vp]),
         "cb_scatter_kv": (S, [vp, vp, i64, vp, i32, vp, vp, i64, i64, i32, i32, vp]),
         "cb_sparse_query_attention": (S, [vp, i64, vp, C.POINTER(AttnReq), i32,
@@ -158,6 +160,7 @@ EXPORTED = [
     "cb_debug_expire_wait", "cb_debug_launch_count", "cb_rope_table_elems",
     "cb_rope_table_init",
     "cb_rope_reposition", "cb_select_workspace_size", "cb_kv_deviation_topk",
+    "cb_kv_deviation_topk_noalloc",
     "cb_gather_rows", "cb_scatter_kv", "cb_sparse_query_attention",
     "cb_model_create", "cb_model_destroy", "cb_linear", "cb_blend_plan",
     "cb_blend_prefill", "cb_full_plan", "cb_full_prefill",

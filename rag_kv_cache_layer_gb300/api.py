@@ -16,7 +16,8 @@ from ._lib import check, lib
 
 __all__ = [
     "dtype_code", "torch_dtype", "cb_rope_table_init", "cb_rope_reposition",
-    "cb_kv_deviation_topk", "cb_gather_rows", "cb_scatter_kv",
+    "cb_kv_deviation_topk", "cb_kv_deviation_topk_noalloc", "cb_gather_rows",
+    "cb_scatter_kv",
     "cb_sparse_query_attention", "cb_debug_expire_wait", "Seg", "Req",
     "BlendModel", "ChunkStore", "select_count", "device_status",
 ]
@@ -103,6 +104,31 @@ def cb_kv_deviation_topk(k_fresh, k_reused, reqs, policy, dev_out, idx_out,
         _p(k_fresh), k_fresh.stride(0), _p(k_reused), k_reused.stride(0),
         k_fresh.shape[1], dtype_code(k_fresh.dtype), arr, n, policy,
         _p(dev_out), _p(idx_out), _p(ws), ws.numel(), _s(stream)))
+
+
+def cb_kv_deviation_topk_noalloc(k_fresh, k_reused, reqs, policy, idx_out,
+                                 stream=None):
+    """cb_kv_deviation_topk without caller scratch: for callers that cannot
+    allocate device memory, the deviations live in the library's fixed
+    device array (at most 1048576 context tokens per call).  reqs as for
+    cb_kv_deviation_topk; dev_offset is ignored."""
+    n = len(reqs)
+    arr = (L.SelectReq * max(1, n))()
+    keep = []
+    for i, r in enumerate(reqs):
+        spans = r.get("span_offsets")
+        sp, ns = None, 0
+        if spans is not None:
+            a = (C.c_int32 * len(spans))(*[int(x) for x in spans])
+            keep.append(a)
+            sp = C.cast(a, C.POINTER(C.c_int32))
+            ns = len(spans) - 1
+        arr[i] = L.SelectReq(r["n_ctx"], r["k"], r.get("fresh_row0", 0),
+                             r.get("reused_row0", 0), 0, r.get("idx_offset", 0), ns, sp)
+    check(lib.cb_kv_deviation_topk_noalloc(
+        _p(k_fresh), k_fresh.stride(0), _p(k_reused), k_reused.stride(0),
+        k_fresh.shape[1], dtype_code(k_fresh.dtype), arr, n, policy,
+        _p(idx_out), _s(stream)))
 
 
 def cb_gather_rows(src, idx, dst, stream=None):

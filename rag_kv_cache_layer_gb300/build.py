@@ -27,6 +27,7 @@ SOURCES = [
     "k_gemm_tc.cu",
     "k_attn_simt.cu",
     "k_attn_tc.cu",
+    "k_noalloc.cu",
 ]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -46,6 +46,11 @@ static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 static size_t dtype_bytes(cb_dtype d) { return d == CB_BF16 ? 2 : 4; }
 
 extern "C" const char *cb_last_error_message(void) { return g_msg.c_str(); }
+
+cb_status cb::record_error(cb_status s, const char *msg) {
+  g_msg = msg ? msg : "";
+  return s;
+}
 extern "C" int cb_version(void) { return 100; }
 
 // --------------------------------------------------------- launch counter --

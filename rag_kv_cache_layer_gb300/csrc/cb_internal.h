@@ -26,6 +26,9 @@ struct BatchMeta {
 // Device address of this library's status word on the current device.
 int *device_status_ptr();
 
+// Sets the thread's cb_last_error_message and returns s.
+cb_status record_error(cb_status s, const char *msg);
+
 // Counts kernels enqueued by the library (read through
 // cb_debug_launch_count); launchers call launched(n) after n launches.
 void note_launches(int n);

@@ -1,0 +1,117 @@
+// Deviation ranking for callers that cannot allocate device memory.
+//
+// Some callers may not call cudaMalloc: code that enqueues work while
+// another component owns every device allocation (an inference engine's
+// memory pool, a plugin host), or that runs where an allocation's implicit
+// device synchronisation is not acceptable.  For them
+// cb_kv_deviation_topk_noalloc keeps the per-token deviations -- the
+// scratch that cb_kv_deviation_topk takes from the caller -- in a
+// file-scope device array of fixed size instead.  The caller still passes
+// its inputs and the selected-index output.
+//
+// The array holds kNoAllocMaxCtx floats (4 MiB) on every device that loads
+// the library, until the process exits.  All calls share it and it keeps
+// the last call's contents; each call first writes every deviation it later
+// reads, so nothing has to start at zero.  Calls whose execution overlaps on
+// the GPU (concurrent streams, other threads) race on the array and must be
+// serialised by the caller.
+#include <mutex>
+#include <vector>
+
+#include "cb_common.cuh"
+#include "cb_internal.h"
+
+namespace cb {
+
+constexpr int64_t kNoAllocMaxCtx = 1 << 20;   // context tokens per call
+
+static __device__ __align__(256) float g_noalloc_dev[kNoAllocMaxCtx];
+
+// Device address of the array on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is resolved
+// once per device (with that device current) and cached.
+static cudaError_t noalloc_scratch(float **out) {
+  static std::mutex mu;
+  static float *ptrs[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ptrs[dev]) {
+    float *p = nullptr;
+    e = cudaGetSymbolAddress((void **)&p, g_noalloc_dev);
+    if (e != cudaSuccess) return e;
+    ptrs[dev] = p;
+  }
+  *out = ptrs[dev];
+  return cudaSuccess;
+}
+
+}  // namespace cb
+
+using namespace cb;
+
+extern "C" cb_status cb_kv_deviation_topk_noalloc(const void *k_fresh, int64_t ld_fresh,
+                                                  const void *k_reused, int64_t ld_reused,
+                                                  int row_elems, cb_dtype dtype,
+                                                  const cb_select_req *reqs, int n_req,
+                                                  cb_policy policy, int32_t *idx_out,
+                                                  cb_stream stream) {
+  if (!k_fresh || !k_reused || !idx_out) return record_error(CB_ERR_INVALID_ARG, "NULL pointer");
+  if (dtype != CB_F32 && dtype != CB_BF16) return record_error(CB_ERR_INVALID_ARG, "bad dtype");
+  if (policy != CB_POLICY_TOKEN_TOPK && policy != CB_POLICY_DOC_ALIGNED)
+    return record_error(CB_ERR_INVALID_ARG, "unknown policy");
+  if (n_req < 0 || n_req > CB_MAX_BATCH || (n_req > 0 && !reqs))
+    return record_error(CB_ERR_INVALID_ARG, "n_req must be in [0, CB_MAX_BATCH] with reqs set");
+  const size_t eb = dtype == CB_BF16 ? 2 : 4;
+  if (row_elems <= 0 || (row_elems * eb) % 16 || ld_fresh < row_elems || ld_reused < row_elems ||
+      (ld_fresh * eb) % 16 || (ld_reused * eb) % 16 || ((uintptr_t)k_fresh & 15) ||
+      ((uintptr_t)k_reused & 15))
+    return record_error(CB_ERR_INVALID_ARG, "rows must be 16-byte aligned and ld >= row_elems");
+  std::vector<SelReq> sr(n_req);
+  std::vector<int32_t> spans;
+  int64_t total = 0;
+  for (int i = 0; i < n_req; ++i) {
+    const cb_select_req &r = reqs[i];
+    if (r.n_ctx < 0 || r.k < 0 || r.k > r.n_ctx || r.fresh_row0 < 0 || r.reused_row0 < 0 ||
+        r.idx_offset < 0)
+      return record_error(CB_ERR_INVALID_ARG, "bad request sizes or offsets");
+    // deviations are packed request after request into the static array
+    sr[i] = SelReq{r.n_ctx, r.k, r.fresh_row0, r.reused_row0, (int)total, r.idx_offset, 0, 0};
+    total += r.n_ctx;
+    if (total > kNoAllocMaxCtx)
+      return record_error(CB_ERR_INVALID_ARG,
+                          "cb_kv_deviation_topk_noalloc: more than 1048576 context tokens in one "
+                          "call (the fixed scratch limit); split the call");
+    if (policy == CB_POLICY_DOC_ALIGNED && r.k > 0) {
+      if (r.n_spans < 1 || !r.span_offsets || r.span_offsets[0] != 0 ||
+          r.span_offsets[r.n_spans] != r.n_ctx || r.n_spans > CB_MAX_SPANS)
+        return record_error(CB_ERR_INVALID_ARG, "spans must cover [0, n_ctx]");
+      for (int j = 0; j < r.n_spans; ++j)
+        if (r.span_offsets[j + 1] < r.span_offsets[j])
+          return record_error(CB_ERR_INVALID_ARG, "spans not ascending");
+      if ((int)spans.size() + r.n_spans + 1 > CB_MAX_SPANS + CB_MAX_BATCH)
+        return record_error(CB_ERR_INVALID_ARG, "too many spans");
+      sr[i].span_begin = (int)spans.size();
+      sr[i].n_spans = r.n_spans;
+      spans.insert(spans.end(), r.span_offsets, r.span_offsets + r.n_spans + 1);
+    }
+  }
+  float *dev = nullptr;
+  cudaError_t e = noalloc_scratch(&dev);
+  if (e != cudaSuccess) return record_error(CB_ERR_CUDA, cudaGetErrorString(e));
+  int *st = device_status_ptr();
+  if (!st) return record_error(CB_ERR_CUDA, "cannot resolve the device status word");
+  e = launch_deviation(k_fresh, ld_fresh, k_reused, ld_reused, row_elems, dtype, sr.data(), n_req,
+                       dev, stream);
+  if (e == cudaSuccess) {
+    if (policy == CB_POLICY_TOKEN_TOPK)
+      e = launch_topk(dev, sr.data(), n_req, idx_out, stream);
+    else
+      e = launch_doc_aligned(dev, sr.data(), n_req, spans.data(), (int)spans.size(), idx_out, st,
+                             stream);
+  }
+  if (e != cudaSuccess) return record_error(CB_ERR_CUDA, cudaGetErrorString(e));
+  return CB_OK;
+}
