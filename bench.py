@@ -308,11 +308,27 @@ def run_ours(args):
             dist.destroy_process_group()
         return
 
+    host_ms = []
     for _ in range(max(args.warmup, 3)):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
         step()
+        host_ms.append((time.perf_counter() - t0) * 1e3)   # enqueue only
     torch.cuda.synchronize()
     if R.device_status() != 0:
         raise RuntimeError("device status set during warm-up")
+
+    # The step is captured once into a CUDA graph (the call allocates
+    # nothing, never synchronises and passes host metadata by value) and
+    # replayed; the end-to-end leg below calls the C ABI directly.
+    n0 = L.lib.cb_debug_launch_count()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    launches_per_step = int(L.lib.cb_debug_launch_count() - n0)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
 
     # ---- device-resident timed region
     if world > 1:
@@ -321,14 +337,12 @@ def run_ours(args):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    n0 = L.lib.cb_debug_launch_count()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     ev[0].record(st)
     for i in range(args.steps):
-        step()
+        graph.replay()
         ev[i + 1].record(st)
     torch.cuda.synchronize()
-    n1 = L.lib.cb_debug_launch_count()
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
@@ -383,6 +397,9 @@ def run_ours(args):
                 "k_selected": int(plan.K_total), "rows_computed": int(plan.R_total),
                 "ttft_ms_median": statistics.median(per),
                 "ttft_ms_p95": float(np.percentile(per, 95)),
+                "execution": "step captured once in a CUDA graph and replayed; "
+                             "e2e calls cb_blend_prefill directly every step",
+                "host_enqueue_ms_per_call": statistics.median(host_ms),
                 "l2": "inputs larger than L2 (14.5 GB of weights and 0.8 GB of "
                       "chunk caches read per step)"},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * 4,
@@ -394,7 +411,7 @@ def run_ours(args):
                                    f"({kms:.3f} ms/launch)",
                          "peak_source": f"bf16_tflops (burst) of {src}"},
             "clocks": clk,
-            "gpu_launches": int(n1 - n0),
+            "gpu_launches": launches_per_step * args.steps,
         }
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline_leg()

@@ -260,9 +260,15 @@ typedef struct {
  * with K[j] = k_cache[kv_row0 + j].  Queries of a request must have
  * ascending positions.  q, out: device [rows][ld] (n_q_heads * head_dim
  * columns); k_cache, v_cache: device [rows][ld_kv].  dtype applies to q,
- * the cache and out.  Errors: CB_ERR_INVALID_ARG (n_req > CB_MAX_BATCH,
+ * the cache and out.  ws: device scratch of at least
+ * cb_attention_workspace_size(...) bytes for the same requests (partial
+ * results when the key range of a query tile is split across SMs; may be
+ * 0 bytes).  Errors: CB_ERR_WORKSPACE if ws is too small; CB_ERR_INVALID_ARG (n_req > CB_MAX_BATCH,
  * head counts not dividing, head_dim not 64 or 128); a position outside
  * [0, kv_len) records CB_ERR_DEVICE_INDEX and the row is left unwritten. */
+size_t cb_attention_workspace_size(const cb_attn_req *reqs, int n_req,
+                                   int n_q_heads, int n_kv_heads, int head_dim,
+                                   cb_dtype dtype);
 cb_status cb_sparse_query_attention(const void *q, int64_t ld_q,
                                     const int32_t *q_pos,
                                     const cb_attn_req *reqs, int n_req,
@@ -270,6 +276,7 @@ cb_status cb_sparse_query_attention(const void *q, int64_t ld_q,
                                     int64_t ld_kv, int n_q_heads,
                                     int n_kv_heads, int head_dim, float scale,
                                     void *out, int64_t ld_out, cb_dtype dtype,
+                                    void *ws, size_t ws_bytes,
                                     cb_stream stream);
 
 /* ------------------------------------------------------------------------ */
@@ -307,7 +314,7 @@ typedef struct cb_model cb_model;
 /* Records the configuration and weight pointers (no device memory is
  * allocated or copied; the weights must outlive the model).  Errors:
  * CB_ERR_INVALID_ARG for inconsistent shapes or NULL weights,
- * CB_ERR_UNSUPPORTED for head_dim not 64/128, d_model % 64, d_ffn % 64,
+ * CB_ERR_UNSUPPORTED for head_dim not 64/128, d_model % 64 or > 8192, d_ffn % 16,
  * or a device older than sm_103 for CB_BF16. */
 cb_status cb_model_create(const cb_model_config *cfg, const cb_weights *w,
                           cb_model **out);

@@ -126,9 +126,11 @@ def _load():
                                              C.POINTER(SelectReq), i32, i32, vp, vp]),
         "cb_gather_rows": (S, [vp, i64, i64, vp, i32, i32, vp, i64, i32, vp]),
         "cb_scatter_kv": (S, [vp, vp, i64, vp, i32, vp, vp, i64, i64, i32, i32, vp]),
+        "cb_attention_workspace_size": (C.c_size_t, [C.POINTER(AttnReq), i32, i32,
+                                                     i32, i32, i32]),
         "cb_sparse_query_attention": (S, [vp, i64, vp, C.POINTER(AttnReq), i32,
                                           vp, vp, i64, i32, i32, i32, C.c_float,
-                                          vp, i64, i32, vp]),
+                                          vp, i64, i32, vp, C.c_size_t, vp]),
         "cb_model_create": (S, [C.POINTER(ModelConfig), C.POINTER(Weights),
                                 C.POINTER(vp)]),
         "cb_model_destroy": (None, [vp]),
@@ -161,7 +163,8 @@ EXPORTED = [
     "cb_rope_table_init",
     "cb_rope_reposition", "cb_select_workspace_size", "cb_kv_deviation_topk",
     "cb_kv_deviation_topk_noalloc",
-    "cb_gather_rows", "cb_scatter_kv", "cb_sparse_query_attention",
+    "cb_gather_rows", "cb_scatter_kv", "cb_attention_workspace_size",
+    "cb_sparse_query_attention",
     "cb_model_create", "cb_model_destroy", "cb_linear", "cb_blend_plan",
     "cb_blend_prefill", "cb_full_plan", "cb_full_prefill",
     "cb_layer_workspace_size", "cb_blend_layer",

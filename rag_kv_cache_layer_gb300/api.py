@@ -152,15 +152,20 @@ def _attn_reqs(reqs):
 
 
 def cb_sparse_query_attention(q, q_pos, reqs, k_cache, v_cache, n_q_heads,
-                              n_kv_heads, head_dim, out, scale=None,
+                              n_kv_heads, head_dim, out, scale=None, ws=None,
                               stream=None):
     """reqs: list of (q_begin, q_end, kv_row0, kv_len)."""
     scale = 1.0 / math.sqrt(head_dim) if scale is None else scale
+    ar = _attn_reqs(reqs)
+    need = lib.cb_attention_workspace_size(ar, len(reqs), n_q_heads, n_kv_heads,
+                                           head_dim, dtype_code(q.dtype))
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     check(lib.cb_sparse_query_attention(
-        _p(q), q.stride(0), _p(q_pos), _attn_reqs(reqs), len(reqs),
+        _p(q), q.stride(0), _p(q_pos), ar, len(reqs),
         _p(k_cache), _p(v_cache), k_cache.stride(0), n_q_heads, n_kv_heads,
         head_dim, float(scale), _p(out), out.stride(0), dtype_code(q.dtype),
-        _s(stream)))
+        _p(ws), ws.numel(), _s(stream)))
 
 
 def cb_debug_expire_wait(limit_us: int, stream=None):

@@ -285,14 +285,31 @@ static cb_status run_attention(const void *q, int64_t ld_q, const int32_t *q_pos
                                const std::vector<AttnReq> &reqs, const void *kc,
                                const void *vc, int64_t ld_kv, int Hq, int Hkv, int hd,
                                float scale, void *out, int64_t ld_out, cb_dtype dt,
-                               int *st, cudaStream_t s) {
-  if (dt == CB_BF16 && attention_tc_supported(Hq, Hkv, hd))
+                               void *ws, size_t ws_bytes, int *st, cudaStream_t s) {
+  if (dt == CB_BF16 && attention_tc_supported(Hq, Hkv, hd)) {
+    const size_t need = attention_tc_ws_bytes(reqs.data(), (int)reqs.size(), Hq, Hkv);
+    if (need > 0 && (!ws || ws_bytes < need))
+      return fail(CB_ERR_WORKSPACE, "attention workspace too small (%zu < %zu)", ws_bytes, need);
     CB_CUDA(launch_attention_tc(q, ld_q, q_pos, reqs.data(), (int)reqs.size(), kc, vc, ld_kv,
-                                Hq, Hkv, scale, out, ld_out, st, s));
-  else
+                                Hq, Hkv, scale, out, ld_out, ws, ws_bytes, st, s));
+  } else {
     CB_CUDA(launch_attention_simt(q, ld_q, q_pos, reqs.data(), (int)reqs.size(), kc, vc,
                                   ld_kv, Hq, Hkv, hd, scale, out, ld_out, dt, st, s));
+  }
   return CB_OK;
+}
+
+extern "C" size_t cb_attention_workspace_size(const cb_attn_req *reqs, int n_req,
+                                              int n_q_heads, int n_kv_heads, int head_dim,
+                                              cb_dtype dtype) {
+  if (!reqs || n_req <= 0 || n_req > CB_MAX_BATCH || dtype != CB_BF16 || n_kv_heads <= 0 ||
+      !attention_tc_supported(n_q_heads, n_kv_heads, head_dim))
+    return 256;
+  std::vector<AttnReq> ar(n_req);
+  for (int i = 0; i < n_req; ++i)
+    ar[i] = AttnReq{reqs[i].q_begin, reqs[i].q_end, reqs[i].kv_row0, reqs[i].kv_len};
+  const size_t n = attention_tc_ws_bytes(ar.data(), n_req, n_q_heads, n_kv_heads);
+  return n > 256 ? n : 256;
 }
 
 extern "C" cb_status cb_sparse_query_attention(const void *q, int64_t ld_q,
@@ -302,6 +319,7 @@ extern "C" cb_status cb_sparse_query_attention(const void *q, int64_t ld_q,
                                                int64_t ld_kv, int n_q_heads,
                                                int n_kv_heads, int head_dim, float scale,
                                                void *out, int64_t ld_out, cb_dtype dtype,
+                                               void *ws, size_t ws_bytes,
                                                cb_stream stream) {
   if (n_req < 0 || n_req > CB_MAX_BATCH) return fail(CB_ERR_INVALID_ARG, "n_req must be in [0, %d]", CB_MAX_BATCH);
   if (n_req == 0) return CB_OK;
@@ -323,7 +341,7 @@ extern "C" cb_status cb_sparse_query_attention(const void *q, int64_t ld_q,
   int *st;
   CB_TRY(status_ptr(&st));
   return run_attention(q, ld_q, q_pos, ar, k_cache, v_cache, ld_kv, n_q_heads, n_kv_heads,
-                       head_dim, scale, out, ld_out, dtype, st, stream);
+                       head_dim, scale, out, ld_out, dtype, ws, ws_bytes, st, stream);
 }
 
 // ------------------------------------------------------------------ model --
@@ -345,6 +363,7 @@ extern "C" cb_status cb_model_create(const cb_model_config *cfg, const cb_weight
   if (c.n_q_heads % c.n_kv_heads) return fail(CB_ERR_INVALID_ARG, "n_q_heads %% n_kv_heads != 0");
   if (c.head_dim != 64 && c.head_dim != 128) return fail(CB_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
   if (c.d_model % 64 || c.d_ffn % 16) return fail(CB_ERR_UNSUPPORTED, "d_model %% 64 and d_ffn %% 16 must be 0");
+  if (c.d_model > 8192) return fail(CB_ERR_UNSUPPORTED, "d_model > 8192");
   if (c.dtype != CB_F32 && c.dtype != CB_BF16) return fail(CB_ERR_INVALID_ARG, "bad dtype");
   if (!(c.norm_eps >= 0.f)) return fail(CB_ERR_INVALID_ARG, "norm_eps < 0");
   if (!w->embed || !w->final_norm || !w->layers || !w->rope_table)
@@ -439,10 +458,12 @@ struct Carver {
 struct LayerScratch {
   void *x, *q, *o, *g;
   float *qkv32;
+  void *attn;          // attention partials (split key ranges)
+  size_t attn_bytes;
 };
 
 struct LayerOffsets {
-  size_t x, q, o, g, qkv32;
+  size_t x, q, o, g, qkv32, attn, attn_bytes;
 };
 
 LayerOffsets carve_layer(Carver &c, const cb_model *m, int64_t n) {
@@ -453,11 +474,17 @@ LayerOffsets carve_layer(Carver &c, const cb_model *m, int64_t n) {
   L.o = c.take(n * m->qw * m->eb);
   L.g = c.take(n * cf.d_ffn * m->eb);
   L.qkv32 = c.take(n * m->qkv_rows * sizeof(float));
+  L.attn_bytes = (cf.dtype == CB_BF16 &&
+                  attention_tc_supported(cf.n_q_heads, cf.n_kv_heads, cf.head_dim))
+                     ? attention_tc_ws_bound()
+                     : 0;
+  L.attn = c.take(L.attn_bytes);
   return L;
 }
 
 LayerScratch bind_layer(char *ws, const LayerOffsets &L) {
-  return LayerScratch{ws + L.x, ws + L.q, ws + L.o, ws + L.g, (float *)(ws + L.qkv32)};
+  return LayerScratch{ws + L.x, ws + L.q, ws + L.o, ws + L.g, (float *)(ws + L.qkv32),
+                      ws + L.attn, L.attn_bytes};
 }
 
 struct Plan {
@@ -633,7 +660,7 @@ static cb_status layer_forward(cb_model *m, int l, float *h, int n, const int32_
                               dt, 0, s));
   }
   CB_TRY(run_attention(S.q, m->qw, pos, ar, kc, vc, m->kvw, c.n_q_heads, c.n_kv_heads, hd,
-                       1.f / sqrtf((float)hd), S.o, m->qw, dt, st, s));
+                       1.f / sqrtf((float)hd), S.o, m->qw, dt, S.attn, S.attn_bytes, st, s));
   CB_TRY(run_linear(m, S.o, m->qw, L.w_o, nullptr, m->qw, n, d, m->qw, EPI_RESID, h, d, s));
   CB_CUDA(launch_rmsnorm(h, d, nullptr, n, d, L.norm2, c.norm_eps, S.x, d, dt, s));
   CB_TRY(run_linear(m, S.x, d, L.w_gate, L.w_up, d, n, F, d, EPI_SWIGLU, S.g, F, s));

@@ -155,12 +155,16 @@ cudaError_t launch_attention_simt(const void *q, int64_t ld_q,
 
 // bf16 tcgen05 attention (head_dim 128, group size 1/2/4/8); queries of a
 // request ascending by position.
+// Scratch: attention_tc_ws_bytes for a given call (0 when its key ranges
+// are not split); attention_tc_ws_bound covers any call on this device.
 bool attention_tc_supported(int Hq, int Hkv, int hd);
+size_t attention_tc_ws_bytes(const AttnReq *reqs, int n_req, int Hq, int Hkv);
+size_t attention_tc_ws_bound();
 cudaError_t launch_attention_tc(const void *q, int64_t ld_q, const int32_t *q_pos,
                                 const AttnReq *reqs, int n_req, const void *k_cache,
                                 const void *v_cache, int64_t ld_kv, int Hq, int Hkv,
-                                float scale, void *out, int64_t ld_out, int *status,
-                                cudaStream_t s);
+                                float scale, void *out, int64_t ld_out, void *ws,
+                                size_t ws_bytes, int *status, cudaStream_t s);
 
 // ---------------------------------------------------------------- debug --
 cudaError_t launch_expire_wait(int limit_us, int *status, cudaStream_t s);

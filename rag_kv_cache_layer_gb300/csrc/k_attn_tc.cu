@@ -10,11 +10,17 @@
 //
 // Roles (192 threads): warp 0 TMA producer (Q once, then double-buffered
 // 128-key K and V blocks, 128-byte swizzle); warp 1 owns TMEM and issues
-// tcgen05.mma: S = Q K^T (K-major operands) into a double-buffered TMEM
-// tile, and O_j = P V (P K-major from shared memory, V MN-major); warps
-// 2..5 do the online softmax (one row per thread, log2 domain, causal mask),
-// write P as bf16 in the swizzled K-major layout, and accumulate
-// O = O * exp2(m_old - m_new) + O_j in registers.  All waits are bounded.
+// tcgen05.mma: S_j = Q K_j^T (K-major operands) and O_j = P_j V_j (P K-major
+// from shared memory, V MN-major), each double-buffered in TMEM; warps 2..5
+// do the online softmax (one row per thread, log2 domain, causal mask),
+// write P_j as bf16 in the swizzled K-major layout (double-buffered), and
+// fold O_{j-1} into registers, O = O * exp2(m_old - m_new) + O_{j-1}, while
+// the tensor core computes O_j.  All waits are bounded.
+//
+// When the query tiles alone cannot fill the SMs (the compact layers), the
+// key range of every tile is split into chunks processed by separate CTAs;
+// each writes its un-normalised (O, m, l) and a combine kernel merges them:
+// O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -33,12 +39,13 @@ constexpr int kAtom = 128 * 64 * 2;        // one [128 rows x 64 bf16] swizzle t
 constexpr int kQ = 2 * kAtom;              // Q tile: 128 rows x 128 dims
 constexpr int kKV = 2 * kAtom;             // K or V block: 128 keys x 128 dims
 constexpr int kP = 2 * kAtom;              // P tile: 128 rows x 128 keys
-// smem: Q | K[2] | V[2] | P | barriers
+// smem: Q | K[2] | V[2] | P[2] | barriers   (224 KB + barriers)
 constexpr int kOffK = kQ;
 constexpr int kOffV = kOffK + 2 * kKV;
 constexpr int kOffP = kOffV + 2 * kKV;
-constexpr int kOffBar = kOffP + kP;
+constexpr int kOffBar = kOffP + 2 * kP;
 constexpr int kSmem = kOffBar + 256 + 1024;
+static_assert(kSmem <= 232448, "attention tile exceeds shared memory");
 
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) {
   uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
@@ -117,62 +124,87 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 2^x with the SFU's approximate base-2 exponential (PTX ex2.approx.ftz;
+// documented maximum relative error about 2^-22), far below the bf16
+// rounding of the probabilities it feeds.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 struct Params {
   int n_req;
   int G, QT, Hkv;
   float scale_log2;            // softmax scale times log2(e)
-  int unit_off[CB_MAX_BATCH + 1];
+  int n_chunks, chunk_blocks;  // key-range split of every tile
+  int tile_off[CB_MAX_BATCH + 1];
   AttnReq r[CB_MAX_BATCH];
 };
+
+// (request, kv head, query tile) of a tile index; longest tiles first
+// within a request.
+struct TileId {
+  int b, g, t;
+};
+__device__ __forceinline__ TileId decode_tile(const Params &P, int tile) {
+  int b = 0;
+  while (P.tile_off[b + 1] <= tile) ++b;
+  const int local = tile - P.tile_off[b];
+  const int n_rows = P.r[b].q_end - P.r[b].q_begin;
+  const int n_t = (n_rows + P.QT - 1) / P.QT;
+  return TileId{b, local % P.Hkv, n_t - 1 - local / P.Hkv};
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
                const __grid_constant__ CUtensorMap mapK,
                const __grid_constant__ CUtensorMap mapV, const __grid_constant__ Params P,
                const int32_t *__restrict__ q_pos, bf16 *__restrict__ out, int64_t ld_out,
-               int *status) {
+               float *__restrict__ part_o, float2 *__restrict__ part_ml, int *status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
   uint64_t *q_full = bar + 0;
-  uint64_t *kv_full = bar + 1;     // [2]
-  uint64_t *kv_empty = bar + 3;    // [2]
-  uint64_t *s_full = bar + 5;      // [2]
-  uint64_t *s_free = bar + 7;      // [2]
-  uint64_t *p_full = bar + 9;
-  uint64_t *pv_full = bar + 10;
-  uint64_t *pv_free = bar + 11;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 12);
+  uint64_t *k_full = bar + 1;      // [2]  K ring: freed once S = Q K^T is done
+  uint64_t *k_empty = bar + 3;     // [2]
+  uint64_t *v_full = bar + 5;      // [2]  V ring: freed once O_j = P V is done
+  uint64_t *v_empty = bar + 7;     // [2]
+  uint64_t *s_full = bar + 9;      // [2]
+  uint64_t *s_free = bar + 11;     // [2]
+  uint64_t *p_full = bar + 13;     // [2]
+  uint64_t *pv_full = bar + 15;    // [2]
+  uint64_t *pv_free = bar + 17;    // [2]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 19);
   volatile int *fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  __shared__ int s_unit[4];        // b, g, tile, n_blocks
+  __shared__ int s_unit[6];        // b, g, tile, first block, end block
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // ---- decode the work unit (longest tiles first within a request)
   if (threadIdx.x == 0) {
-    const int u = blockIdx.x;
-    int b = 0;
-    while (P.unit_off[b + 1] <= u) ++b;
-    const int local = u - P.unit_off[b];
-    const int n_rows = P.r[b].q_end - P.r[b].q_begin;
-    const int n_t = (n_rows + P.QT - 1) / P.QT;
-    const int t = n_t - 1 - local / P.Hkv;
-    const int g = local % P.Hkv;
-    const int last = min(n_rows, (t + 1) * P.QT) - 1;
-    int pmax = q_pos[P.r[b].q_begin + last];
-    if (pmax < 0 || pmax >= P.r[b].kv_len) { report(status, CB_ERR_DEVICE_INDEX); pmax = -1; }
-    s_unit[0] = b; s_unit[1] = g; s_unit[2] = t;
-    s_unit[3] = pmax < 0 ? 0 : pmax / BN + 1;
-    // single-arrival barriers (TMA transactions or tcgen05.commit) ...
+    const int tile = blockIdx.x / P.n_chunks, chunk = blockIdx.x % P.n_chunks;
+    const TileId id = decode_tile(P, tile);
+    const AttnReq &R = P.r[id.b];
+    const int n_rows = R.q_end - R.q_begin;
+    const int last = min(n_rows, (id.t + 1) * P.QT) - 1;
+    int pmax = q_pos[R.q_begin + last];
+    if (pmax < 0 || pmax >= R.kv_len) { report(status, CB_ERR_DEVICE_INDEX); pmax = -1; }
+    const int nb_tile = pmax < 0 ? 0 : pmax / BN + 1;
+    const int jb = chunk * P.chunk_blocks;
+    s_unit[0] = id.b; s_unit[1] = id.g; s_unit[2] = id.t;
+    s_unit[3] = jb;
+    s_unit[4] = max(jb, min(nb_tile, jb + P.chunk_blocks));
     mbar_init(smem_u32(q_full), 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&kv_full[i]), 1);
-      mbar_init(smem_u32(&kv_empty[i]), 1);
+      mbar_init(smem_u32(&k_full[i]), 1);
+      mbar_init(smem_u32(&k_empty[i]), 1);
+      mbar_init(smem_u32(&v_full[i]), 1);
+      mbar_init(smem_u32(&v_empty[i]), 1);
       mbar_init(smem_u32(&s_full[i]), 1);
-      mbar_init(smem_u32(&s_free[i]), 128);   // ... and the 128 softmax threads
+      mbar_init(smem_u32(&s_free[i]), 128);
+      mbar_init(smem_u32(&p_full[i]), 128);
+      mbar_init(smem_u32(&pv_full[i]), 1);
+      mbar_init(smem_u32(&pv_free[i]), 128);
     }
-    mbar_init(smem_u32(p_full), 128);
-    mbar_init(smem_u32(pv_full), 1);
-    mbar_init(smem_u32(pv_free), 128);
     *fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -187,44 +219,51 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int b = s_unit[0], g = s_unit[1], t = s_unit[2], nb = s_unit[3];
+  const int b = s_unit[0], g = s_unit[1], t = s_unit[2], jb = s_unit[3], je = s_unit[4];
+  const int nb = je - jb;                         // key blocks of this unit
   const AttnReq &R = P.r[b];
   const int row0 = R.q_begin + t * P.QT;          // first q row of the tile
   const int n_valid = min(P.QT, R.q_end - row0);  // q rows of the request in the tile
+  // TMEM columns: S[0] 0..127, S[1] 128..255, O_j[0] 256..383, O_j[1] 384..511
 
-  if (nb > 0 && warp == 0 && lane == 0) {
-    // ------------------------------------------------------------ producer
-    const uint32_t qb = smem_u32(q_full);
-    expect_tx(qb, kQ);
-    for (int h = 0; h < P.G; ++h)
-      for (int half = 0; half < 2; ++half)
-        tma_load_2d(smem_u32(smem + half * kAtom + h * P.QT * 128), &mapQ, qb,
-                    (g * P.G + h) * HD + half * 64, row0);
+  if (nb > 0 && warp == 0 && lane < 2) {
+    // ----------------------------------------------- producers (K: lane 0, V: lane 1)
+    // Two independent loaders, so a K block can be fetched as soon as the
+    // previous S = Q K^T has finished with its slot, whatever V is doing.
+    const CUtensorMap *map = lane == 0 ? &mapK : &mapV;
+    uint64_t *full = lane == 0 ? k_full : v_full;
+    uint64_t *empty = lane == 0 ? k_empty : v_empty;
+    const int off = lane == 0 ? kOffK : kOffV;
+    if (lane == 0) {
+      const uint32_t qb = smem_u32(q_full);
+      expect_tx(qb, kQ);
+      for (int h = 0; h < P.G; ++h)
+        for (int half = 0; half < 2; ++half)
+          tma_load_2d(smem_u32(smem + half * kAtom + h * P.QT * 128), &mapQ, qb,
+                      (g * P.G + h) * HD + half * 64, row0);
+    }
     for (int j = 0; j < nb; ++j) {
       const int s = j & 1;
-      if (!mbar_wait_bounded(smem_u32(&kv_empty[s]), ((j >> 1) & 1) ^ 1, kWaitLimitNs, status) ||
+      if (!mbar_wait_bounded(smem_u32(&empty[s]), ((j >> 1) & 1) ^ 1, kWaitLimitNs, status) ||
           *fail) {
         *fail = 1;
         break;
       }
-      const uint32_t fb = smem_u32(&kv_full[s]);
-      expect_tx(fb, 2 * kKV);
-      const int key_row = (int)R.kv_row0 + j * BN;
-      for (int half = 0; half < 2; ++half) {
-        tma_load_2d(smem_u32(smem + kOffK + s * kKV + half * kAtom), &mapK, fb,
-                    g * HD + half * 64, key_row);
-        tma_load_2d(smem_u32(smem + kOffV + s * kKV + half * kAtom), &mapV, fb,
-                    g * HD + half * 64, key_row);
-      }
+      const uint32_t fb = smem_u32(&full[s]);
+      expect_tx(fb, kKV);
+      const int key_row = (int)R.kv_row0 + (jb + j) * BN;
+      for (int half = 0; half < 2; ++half)
+        tma_load_2d(smem_u32(smem + off + s * kKV + half * kAtom), map, fb, g * HD + half * 64,
+                    key_row);
     }
   } else if (nb > 0 && warp == 1 && lane == 0) {
     // ----------------------------------------------------------------- MMA
     const uint32_t idS = idesc(false), idPV = idesc(true);
-    const uint32_t q_addr = smem_u32(smem), p_addr = smem_u32(smem + kOffP);
+    const uint32_t q_addr = smem_u32(smem);
     bool ok = mbar_wait_bounded(smem_u32(q_full), 0, kWaitLimitNs, status);
     auto issue_s = [&](int j) -> bool {
       const int s = j & 1;
-      if (!mbar_wait_bounded(smem_u32(&kv_full[s]), (j >> 1) & 1, kWaitLimitNs, status)) return false;
+      if (!mbar_wait_bounded(smem_u32(&k_full[s]), (j >> 1) & 1, kWaitLimitNs, status)) return false;
       if (!mbar_wait_bounded(smem_u32(&s_free[s]), ((j >> 1) & 1) ^ 1, kWaitLimitNs, status)) return false;
       fence_after();
       const uint32_t k_addr = smem_u32(smem + kOffK + s * kKV);
@@ -234,30 +273,33 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
         mma(tmem + s * BN, desc_kmajor(q_addr + off), desc_kmajor(k_addr + off), idS, k > 0);
       }
       commit(smem_u32(&s_full[s]));
+      commit(smem_u32(&k_empty[s]));
       return true;
     };
     if (ok) ok = issue_s(0);
     for (int j = 0; j < nb && ok && !*fail; ++j) {
       const int s = j & 1;
       if (j + 1 < nb && !issue_s(j + 1)) { ok = false; break; }
-      if (!mbar_wait_bounded(smem_u32(p_full), j & 1, kWaitLimitNs, status) ||
-          !mbar_wait_bounded(smem_u32(pv_free), (j & 1) ^ 1, kWaitLimitNs, status)) {
+      if (!mbar_wait_bounded(smem_u32(&p_full[s]), (j >> 1) & 1, kWaitLimitNs, status) ||
+          !mbar_wait_bounded(smem_u32(&pv_free[s]), ((j >> 1) & 1) ^ 1, kWaitLimitNs, status) ||
+          !mbar_wait_bounded(smem_u32(&v_full[s]), (j >> 1) & 1, kWaitLimitNs, status)) {
         ok = false;
         break;
       }
       fence_after();
+      const uint32_t p_addr = smem_u32(smem + kOffP + s * kP);
       const uint32_t v_addr = smem_u32(smem + kOffV + s * kKV);
 #pragma unroll
       for (int k = 0; k < BN / 16; ++k) {
         const uint32_t poff = (k >> 2) * kAtom + (k & 3) * 32;
-        mma(tmem + 2 * BN, desc_kmajor(p_addr + poff),
+        mma(tmem + 2 * BN + s * BN, desc_kmajor(p_addr + poff),
             desc_mnmajor(v_addr + k * 16 * 128, kAtom), idPV, k > 0);
       }
-      commit(smem_u32(pv_full));
-      commit(smem_u32(&kv_empty[s]));
+      commit(smem_u32(&pv_full[s]));
+      commit(smem_u32(&v_empty[s]));
     }
     if (!ok) *fail = 1;
-  } else if (nb > 0 && warp >= 2) {
+  } else if (warp >= 2) {
     // ------------------------------------------------------------- softmax
     const int quad = warp & 3;
     const int row = quad * 32 + lane;             // MMA row = h * QT + qi
@@ -266,36 +308,68 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
     int p = valid ? q_pos[row0 + qi] : 0;
     if (p < 0 || p >= R.kv_len) p = 0;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    uint8_t *prow = smem + kOffP + row * 128;
     float o[HD];
 #pragma unroll
     for (int i = 0; i < HD; ++i) o[i] = 0.f;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f, corr_pending = 1.f;
     const float sl2 = P.scale_log2;
+    bool failed = false;
+    // folds O_j (TMEM buffer j & 1) into the register accumulator
+    auto fold = [&](int j, float corr) -> bool {
+      const int s = j & 1;
+      const bool bad = !mbar_wait_bounded(smem_u32(&pv_full[s]), (j >> 1) & 1, kWaitLimitNs,
+                                          status) || *fail;
+      if (__any_sync(0xffffffffu, bad)) return false;
+      fence_after();
+      const uint32_t obase = tmem + lane_off + 2 * BN + s * BN;
+#pragma unroll
+      for (int c = 0; c < HD; c += 32) {
+        float y[32];
+        ld32(obase + c, y);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[c + i] = o[c + i] * corr + y[i];
+      }
+      fence_before();
+      arrive(smem_u32(&pv_free[s]));
+      return true;
+    };
     for (int j = 0; j < nb; ++j) {
       const int s = j & 1;
-      // failures leave the loop warp-uniformly (the TMEM loads are .sync.aligned)
-      bool bad = !mbar_wait_bounded(smem_u32(&s_full[s]), (j >> 1) & 1, kWaitLimitNs, status) ||
-                 *fail;
-      if (__any_sync(0xffffffffu, bad)) {
-        *fail = 1;
-        break;
-      }
+      const bool bad =
+          !mbar_wait_bounded(smem_u32(&s_full[s]), (j >> 1) & 1, kWaitLimitNs, status) || *fail;
+      if (__any_sync(0xffffffffu, bad)) { failed = true; break; }
       fence_after();
       const uint32_t sbase = tmem + lane_off + s * BN;
-      const int key0 = j * BN;
-      float mloc = -INFINITY;
+      const int key0 = (jb + j) * BN;
+      // Keys visible to this row: key0 .. p.  Blocks wholly at or before p
+      // take the mask-free path.  Eight partial maxima / sums keep the
+      // dependency chains short (one softmax warp per scheduler).
+      const int n_vis = p - key0 + 1;               // >= BN: no masking
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         float x[32];
         ld32(sbase + c, x);
+        if (n_vis >= BN) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (key0 + c + i <= p) mloc = fmaxf(mloc, x[i]);
+          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c + i < n_vis) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+        }
       }
+      const float mloc = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float m_new = fmaxf(m, mloc * sl2);
-      const float corr = exp2f(m - m_new);
-      l *= corr;
+      // a row whose keys are all masked so far keeps m = -inf and p = 0
+      const float corr = m_new == -INFINITY ? 1.f : fast_exp2(m - m_new);
+      float ls[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ls[i] = 0.f;
+      uint8_t *prow = smem + kOffP + s * kP + row * 128;
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         float x[32];
@@ -303,9 +377,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float p0 = (key0 + c + i <= p) ? exp2f(x[i] * sl2 - m_new) : 0.f;
-          const float p1 = (key0 + c + i + 1 <= p) ? exp2f(x[i + 1] * sl2 - m_new) : 0.f;
-          l += p0 + p1;
+          float p0 = fast_exp2(fmaf(x[i], sl2, -m_new));
+          float p1 = fast_exp2(fmaf(x[i + 1], sl2, -m_new));
+          if (n_vis < BN) {
+            p0 = c + i < n_vis ? p0 : 0.f;
+            p1 = c + i + 1 < n_vis ? p1 : 0.f;
+          }
+          ls[(i >> 1) & 7] += p0 + p1;
           __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
           pk[i / 2] = *reinterpret_cast<uint32_t *>(&v2);
         }
@@ -318,38 +396,40 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
               make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
         }
       }
+      l = fmaf(l, corr, ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
       fence_before();
       arrive(smem_u32(&s_free[s]));
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      arrive(smem_u32(p_full));
-      bad = !mbar_wait_bounded(smem_u32(pv_full), j & 1, kWaitLimitNs, status) || *fail;
-      if (__any_sync(0xffffffffu, bad)) {
-        *fail = 1;
-        break;
-      }
-      fence_after();
-      const uint32_t obase = tmem + lane_off + 2 * BN;
-#pragma unroll
-      for (int c = 0; c < HD; c += 32) {
-        float y[32];
-        ld32(obase + c, y);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[c + i] = o[c + i] * corr + y[i];
-      }
-      fence_before();
-      arrive(smem_u32(pv_free));
+      arrive(smem_u32(&p_full[s]));
       m = m_new;
+      // the tensor core now computes O_j; fold the previous block meanwhile
+      if (j > 0 && !fold(j - 1, corr_pending)) { failed = true; break; }
+      corr_pending = corr;
     }
+    if (!failed && nb > 0 && !fold(nb - 1, corr_pending)) failed = true;
+    if (failed) *fail = 1;
     if (valid && !*fail) {
-      const float inv = 1.f / l;
-      bf16 *dst = out + (int64_t)(row0 + qi) * ld_out + (g * P.G + h) * HD;
+      const int q_row = row0 + qi, head = g * P.G + h;
+      if (P.n_chunks == 1) {
+        const float inv = 1.f / l;
+        bf16 *dst = out + (int64_t)q_row * ld_out + head * HD;
 #pragma unroll
-      for (int c = 0; c < HD; c += 8) {
-        uint4 pk;
-        __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&pk);
+        for (int c = 0; c < HD; c += 8) {
+          uint4 pk;
+          __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&pk);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) e[i] = __floats2bfloat162_rn(o[c + 2 * i] * inv, o[c + 2 * i + 1] * inv);
-        *reinterpret_cast<uint4 *>(dst + c) = pk;
+          for (int i = 0; i < 4; ++i)
+            e[i] = __floats2bfloat162_rn(o[c + 2 * i] * inv, o[c + 2 * i + 1] * inv);
+          *reinterpret_cast<uint4 *>(dst + c) = pk;
+        }
+      } else {
+        // un-normalised partial of this key chunk (m = -inf, l = 0 when no
+        // key of the chunk is visible to the row)
+        const int64_t slot = (int64_t)blockIdx.x * 128 + row;
+        float4 *po = reinterpret_cast<float4 *>(part_o + slot * HD);
+#pragma unroll
+        for (int c = 0; c < HD; c += 4) po[c / 4] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+        part_ml[slot] = make_float2(m, l);
       }
     }
   }
@@ -357,7 +437,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   __syncthreads();
   if (warp == 0 && lane == 0 && *fail) {
     // drain the K/V copies this CTA may still have in flight
-    for (int s = 0; s < 2; ++s) mbar_wait_bounded(smem_u32(&kv_full[s]), 0, 10000000ull, nullptr);
+    for (int s = 0; s < 2; ++s) {
+      mbar_wait_bounded(smem_u32(&k_full[s]), 0, 10000000ull, nullptr);
+      mbar_wait_bounded(smem_u32(&v_full[s]), 0, 10000000ull, nullptr);
+    }
   }
   __syncthreads();
   if (warp == 1) {
@@ -365,6 +448,44 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512)
                  : "memory");
   }
+}
+
+// Merges the key-chunk partials of every (query row, q head).  One warp
+// per tile row; each lane owns four of the 128 output dimensions, so every
+// partial row is read as one coalesced 512-byte access.
+__global__ void __launch_bounds__(256)
+attn_combine_kernel(const __grid_constant__ Params P, const float *__restrict__ part_o,
+                    const float2 *__restrict__ part_ml, bf16 *__restrict__ out, int64_t ld_out) {
+  const int tile = blockIdx.x / 16;
+  const int row = (blockIdx.x % 16) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const TileId id = decode_tile(P, tile);
+  const AttnReq &R = P.r[id.b];
+  const int h = row / P.QT, qi = row % P.QT;
+  const int row0 = R.q_begin + id.t * P.QT;
+  if (qi >= min(P.QT, R.q_end - row0)) return;
+  float M = -INFINITY;
+  for (int c = 0; c < P.n_chunks; ++c)
+    M = fmaxf(M, part_ml[((int64_t)tile * P.n_chunks + c) * 128 + row].x);
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  float l = 0.f;
+  for (int c = 0; c < P.n_chunks; ++c) {
+    const int64_t slot = ((int64_t)tile * P.n_chunks + c) * 128 + row;
+    const float2 ml = part_ml[slot];
+    if (ml.x == -INFINITY) continue;
+    const float w = exp2f(ml.x - M);
+    l += w * ml.y;
+    const float4 v = reinterpret_cast<const float4 *>(part_o + slot * HD)[lane];
+    o.x += w * v.x; o.y += w * v.y; o.z += w * v.z; o.w += w * v.w;
+  }
+  const float inv = 1.f / l;
+  bf16 *dst = out + (int64_t)(row0 + qi) * ld_out + (id.g * P.G + h) * HD + lane * 4;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(o.x * inv, o.y * inv);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(o.z * inv, o.w * inv);
+  uint2 pk;
+  pk.x = *reinterpret_cast<uint32_t *>(&lo);
+  pk.y = *reinterpret_cast<uint32_t *>(&hi);
+  *reinterpret_cast<uint2 *>(dst) = pk;
 }
 
 // ------------------------------------------------------------------ host --
@@ -395,6 +516,48 @@ static bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t c
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+static int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+// Tiles of a call and the key-range split: tiles that alone fill fewer than
+// all SMs get their key blocks split into chunks so that about two waves of
+// CTAs run; chunks past a tile's last query position exit at once.
+static void plan_split(Params &P, const AttnReq *reqs, int n_req, int Hq, int Hkv) {
+  P.n_req = n_req;
+  P.G = Hq / Hkv;
+  P.QT = 128 / P.G;
+  P.Hkv = Hkv;
+  P.tile_off[0] = 0;
+  int max_nb = 0;
+  for (int i = 0; i < n_req; ++i) {
+    P.r[i] = reqs[i];
+    const int n = reqs[i].q_end - reqs[i].q_begin;
+    P.tile_off[i + 1] = P.tile_off[i] + Hkv * ((n + P.QT - 1) / P.QT);
+    const int nb = (reqs[i].kv_len + BN - 1) / BN;
+    if (n > 0 && nb > max_nb) max_nb = nb;
+  }
+  const int tiles = P.tile_off[n_req];
+  P.n_chunks = 1;
+  P.chunk_blocks = max_nb > 0 ? max_nb : 1;
+  const int sms = num_sms();
+  if (tiles > 0 && tiles < sms && max_nb > 1) {
+    int want = (2 * sms + tiles - 1) / tiles;
+    if (want > max_nb) want = max_nb;
+    P.chunk_blocks = (max_nb + want - 1) / want;
+    P.n_chunks = (max_nb + P.chunk_blocks - 1) / P.chunk_blocks;
+  }
+}
+
+constexpr size_t kPartBytes = 128 * (HD * sizeof(float) + sizeof(float2));
+
 }  // namespace attn
 
 bool attention_tc_supported(int Hq, int Hkv, int hd) {
@@ -403,29 +566,40 @@ bool attention_tc_supported(int Hq, int Hkv, int hd) {
   return G == 1 || G == 2 || G == 4 || G == 8;
 }
 
+size_t attention_tc_ws_bound() { return (size_t)3 * attn::num_sms() * attn::kPartBytes + 256; }
+
+size_t attention_tc_ws_bytes(const AttnReq *reqs, int n_req, int Hq, int Hkv) {
+  attn::Params P;
+  attn::plan_split(P, reqs, n_req, Hq, Hkv);
+  if (P.n_chunks == 1) return 0;
+  return (size_t)P.tile_off[n_req] * P.n_chunks * attn::kPartBytes + 256;
+}
+
 cudaError_t launch_attention_tc(const void *q, int64_t ld_q, const int32_t *q_pos,
                                 const AttnReq *reqs, int n_req, const void *k_cache,
                                 const void *v_cache, int64_t ld_kv, int Hq, int Hkv,
-                                float scale, void *out, int64_t ld_out, int *status,
-                                cudaStream_t s) {
+                                float scale, void *out, int64_t ld_out, void *ws,
+                                size_t ws_bytes, int *status, cudaStream_t s) {
   using namespace attn;
   Params P;
-  P.n_req = n_req;
-  P.G = Hq / Hkv;
-  P.QT = 128 / P.G;
-  P.Hkv = Hkv;
+  plan_split(P, reqs, n_req, Hq, Hkv);
   P.scale_log2 = scale * 1.4426950408889634f;
-  P.unit_off[0] = 0;
   int64_t q_rows = 0, kv_rows = 0;
   for (int i = 0; i < n_req; ++i) {
-    P.r[i] = reqs[i];
-    const int n = reqs[i].q_end - reqs[i].q_begin;
-    P.unit_off[i + 1] = P.unit_off[i] + Hkv * ((n + P.QT - 1) / P.QT);
     if (reqs[i].q_end > q_rows) q_rows = reqs[i].q_end;
     if (reqs[i].kv_row0 + reqs[i].kv_len > kv_rows) kv_rows = reqs[i].kv_row0 + reqs[i].kv_len;
   }
-  const int units = P.unit_off[n_req];
-  if (units == 0) return cudaSuccess;
+  const int tiles = P.tile_off[n_req];
+  if (tiles == 0) return cudaSuccess;
+  float *part_o = nullptr;
+  float2 *part_ml = nullptr;
+  if (P.n_chunks > 1) {
+    const size_t need = (size_t)tiles * P.n_chunks * kPartBytes;
+    if (!ws || ws_bytes < need) return cudaErrorInvalidValue;
+    part_o = reinterpret_cast<float *>(ws);
+    part_ml = reinterpret_cast<float2 *>(reinterpret_cast<char *>(ws) +
+                                         (size_t)tiles * P.n_chunks * 128 * HD * sizeof(float));
+  }
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, q_rows, (int64_t)Hq * HD, ld_q, P.QT) ||
       !make_map(&mk, k_cache, kv_rows, (int64_t)Hkv * HD, ld_kv, BN) ||
@@ -438,9 +612,12 @@ cudaError_t launch_attention_tc(const void *q, int64_t ld_q, const int32_t *q_po
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  attn_tc_kernel<<<units, kThreads, kSmem, s>>>(mq, mk, mv, P, q_pos,
-                                                reinterpret_cast<bf16 *>(out), ld_out, status);
-  return launched(1);
+  attn_tc_kernel<<<tiles * P.n_chunks, kThreads, kSmem, s>>>(
+      mq, mk, mv, P, q_pos, reinterpret_cast<bf16 *>(out), ld_out, part_o, part_ml, status);
+  if (P.n_chunks == 1) return launched(1);
+  attn_combine_kernel<<<tiles * 16, 256, 0, s>>>(P, part_o, part_ml,
+                                                 reinterpret_cast<bf16 *>(out), ld_out);
+  return launched(2);
 }
 
 }  // namespace cb

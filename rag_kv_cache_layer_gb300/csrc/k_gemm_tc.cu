@@ -152,13 +152,55 @@ struct Cfg {
   static constexpr int kSmem = kStages * kStage + 1024 /*align*/ + 256 /*barriers*/;
 };
 
+// Work of one persistent CTA.  Tile mode: output tiles blockIdx.x,
+// blockIdx.x + gridDim.x, ... over the whole K range.  Stream-K mode (the
+// residual epilogue, whose atomic add makes any K split legal): the
+// tiles x k-blocks of the GEMM are laid end to end and every CTA takes an
+// equal contiguous share, which may start or end inside a tile.  Tiles are
+// numbered M-fastest so that CTAs running together share weight tiles.
+struct Work {
+  int n_m, num_kb;
+  bool sk;
+  int64_t w, w_end;
+  __device__ Work(int n_m_, int n_n, int num_kb_, bool sk_) : n_m(n_m_), num_kb(num_kb_), sk(sk_) {
+    const int64_t tiles = (int64_t)n_m_ * n_n;
+    if (sk) {
+      const int64_t total = tiles * num_kb_;
+      w = total * blockIdx.x / gridDim.x;
+      w_end = total * (blockIdx.x + 1) / gridDim.x;
+    } else {
+      w = blockIdx.x;
+      w_end = tiles;
+    }
+  }
+  __device__ bool next(int &m_blk, int &n_blk, int &kb0, int &kb1) {
+    if (w >= w_end) return false;
+    int tile;
+    if (sk) {
+      tile = (int)(w / num_kb);
+      kb0 = (int)(w % num_kb);
+      const int64_t left = w_end - w;
+      kb1 = (int)(kb0 + left < num_kb ? kb0 + left : num_kb);
+      w += kb1 - kb0;
+    } else {
+      tile = (int)w;
+      kb0 = 0;
+      kb1 = num_kb;
+      w += gridDim.x;
+    }
+    m_blk = tile % n_m;
+    n_blk = tile / n_m;
+    return true;
+  }
+};
+
 // ---------------------------------------------------------------- kernel --
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
                const __grid_constant__ CUtensorMap mapB,
                const __grid_constant__ CUtensorMap mapB2, int M, int N, int K,
-               int splits, const EpiParams ep, int *status) {
+               int stream_k, const EpiParams ep, int *status) {
   using C = Cfg<BN, EPI>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -174,8 +216,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
   const int n_m = (M + BM - 1) / BM;
   const int n_n = (N + C::kOutN - 1) / C::kOutN;
   const int num_kb = (K + BK - 1) / BK;
-  const int kb_per = (num_kb + splits - 1) / splits;
-  const int n_units = n_m * n_n * splits;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -213,13 +253,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
       uint32_t phase = 0;
       int issued[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const int m_blk = u % n_m;
-        const int rest = u / n_m;
-        const int split = rest % splits;
-        const int n_blk = rest / splits;
-        const int kb0 = split * kb_per;
-        const int kb1 = min(num_kb, kb0 + kb_per);
+      Work wk(n_m, n_n, num_kb, stream_k != 0);
+      int m_blk, n_blk, kb0, kb1;
+      while (ok && wk.next(m_blk, n_blk, kb0, kb1)) {
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, kWaitLimitNs, status) ||
               *fail_flag) {
@@ -259,11 +295,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
       int buf = 0;
       uint32_t bphase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const int rest = u / n_m;
-        const int split = rest % splits;
-        const int kb0 = split * kb_per;
-        const int kb1 = min(num_kb, kb0 + kb_per);
+      Work wk(n_m, n_n, num_kb, stream_k != 0);
+      int m_blk, n_blk, kb0, kb1;
+      while (ok && wk.next(m_blk, n_blk, kb0, kb1)) {
         if (!mbar_wait_bounded(smem_u32(&tempty[buf]), bphase ^ 1, kWaitLimitNs, status) ||
             *fail_flag) {
           ok = false;
@@ -298,10 +332,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
     const int row_in_tile = quad * 32 + lane;
     int buf = 0;
     uint32_t bphase = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const int m_blk = u % n_m;
-      const int rest = u / n_m;
-      const int n_blk = rest / splits;
+    Work wk(n_m, n_n, num_kb, stream_k != 0);
+    int m_blk, n_blk, kb0, kb1;
+    while (wk.next(m_blk, n_blk, kb0, kb1)) {
+      // a tile covered by one CTA alone is updated in place; pieces of a
+      // tile shared between CTAs are added atomically
+      const bool whole = kb0 == 0 && kb1 == num_kb;
       // leave warp-uniformly on failure: the TMEM loads are .sync.aligned
       const bool bad =
           !mbar_wait_bounded(smem_u32(&tfull[buf]), bphase, kWaitLimitNs, status) || *fail_flag;
@@ -329,51 +365,51 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
           }
         }
       } else if (EPI == EPI_QKV) {
-        // BN == head_dim == 128: this tile is one head of q, k or v.
-        const int head = n_blk;
+        // head_dim 128: the tile holds BN / 128 consecutive heads of the
+        // stacked [q heads | k heads | v heads] projection.
         const int Hq = ep.n_q_heads, Hkv = ep.n_kv_heads;
         const int p = row_ok ? ep.pos[m] : 0;
         const int64_t dr = row_ok ? ep.dst_row[m] : 0;
-        if (head < Hq + Hkv) {
-          bf16 *dst = head < Hq
-                          ? reinterpret_cast<bf16 *>(ep.out) + (int64_t)m * ep.ldo + head * 128
-                          : reinterpret_cast<bf16 *>(ep.k_cache) + dr * ep.ld_kv + (head - Hq) * 128;
-          const float2 *cs = ep.rope + (int64_t)p * 64;
+        const float2 *cs = ep.rope + (int64_t)p * 64;
 #pragma unroll 1
-          for (int c = 0; c < 64; c += 32) {
-            float x1[32], x2[32];
-            tmem_ld32(tbase + c, x1);
-            tmem_ld32(tbase + 64 + c, x2);
-            if (row_ok) {
-              uint4 p1[4], p2[4];
-              bf16 *e1 = reinterpret_cast<bf16 *>(p1);
-              bf16 *e2 = reinterpret_cast<bf16 *>(p2);
+        for (int hh = 0; hh < BN / 128; ++hh) {
+          const int head = n_blk * (BN / 128) + hh;
+          if (head >= Hq + 2 * Hkv) break;               // uniform across the warp
+          const uint32_t hbase = tbase + hh * 128;
+          if (head < Hq + Hkv) {
+            bf16 *dst = head < Hq
+                            ? reinterpret_cast<bf16 *>(ep.out) + (int64_t)m * ep.ldo + head * 128
+                            : reinterpret_cast<bf16 *>(ep.k_cache) + dr * ep.ld_kv + (head - Hq) * 128;
+#pragma unroll 1
+            for (int c = 0; c < 64; c += 32) {
+              float x1[32], x2[32];
+              tmem_ld32(hbase + c, x1);
+              tmem_ld32(hbase + 64 + c, x2);
+              if (row_ok) {
+                uint4 p1[4], p2[4];
+                bf16 *e1 = reinterpret_cast<bf16 *>(p1);
+                bf16 *e2 = reinterpret_cast<bf16 *>(p2);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const float2 w = __ldg(cs + c + i);
-                e1[i] = __float2bfloat16_rn(x1[i] * w.x - x2[i] * w.y);
-                e2[i] = __float2bfloat16_rn(x2[i] * w.x + x1[i] * w.y);
-              }
+                for (int i = 0; i < 32; ++i) {
+                  const float2 w = __ldg(cs + c + i);
+                  e1[i] = __float2bfloat16_rn(x1[i] * w.x - x2[i] * w.y);
+                  e2[i] = __float2bfloat16_rn(x2[i] * w.x + x1[i] * w.y);
+                }
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                reinterpret_cast<uint4 *>(dst + c)[i] = p1[i];
-                reinterpret_cast<uint4 *>(dst + 64 + c)[i] = p2[i];
+                for (int i = 0; i < 4; ++i) {
+                  reinterpret_cast<uint4 *>(dst + c)[i] = p1[i];
+                  reinterpret_cast<uint4 *>(dst + 64 + c)[i] = p2[i];
+                }
               }
             }
-          }
-        } else {
-          bf16 *dst = reinterpret_cast<bf16 *>(ep.v_cache) + dr * ep.ld_kv + (head - Hq - Hkv) * 128;
+          } else {
+            bf16 *dst = reinterpret_cast<bf16 *>(ep.v_cache) + dr * ep.ld_kv +
+                        (head - Hq - Hkv) * 128;
 #pragma unroll 1
-          for (int c = 0; c < 128; c += 32) {
-            float x[32];
-            tmem_ld32(tbase + c, x);
-            if (row_ok) {
-              uint4 pk[4];
-              bf16 *pe = reinterpret_cast<bf16 *>(pk);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) pe[i] = __float2bfloat16_rn(x[i]);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) reinterpret_cast<uint4 *>(dst + c)[i] = pk[i];
+            for (int c = 0; c < 128; c += 32) {
+              float x[32];
+              tmem_ld32(hbase + c, x);
+              if (row_ok) store_bf16_chunk(dst + c, x, 32);
             }
           }
         }
@@ -391,7 +427,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
             float *o = reinterpret_cast<float *>(ep.out) + (int64_t)m * ep.ldo + n0 + c;
             for (int i = 0; i < valid; ++i) {
               if (EPI == EPI_STORE_F32) o[i] = x[i];
-              else if (splits == 1) o[i] += x[i];
+              else if (whole) o[i] += x[i];
               else atomicAdd(o + i, x[i]);
             }
           } else if (EPI == EPI_STORE_F32) {
@@ -403,7 +439,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
           } else {  // EPI_RESID
             float4 *o = reinterpret_cast<float4 *>(reinterpret_cast<float *>(ep.out) +
                                                    (int64_t)m * ep.ldo + n0 + c);
-            if (splits == 1) {
+            if (whole) {
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 float4 h = o[i];
@@ -476,23 +512,9 @@ static int num_sms() {
   return n;
 }
 
-// Split-K factor for the residual epilogue: the number of K slices that
-// minimises (waves of work units) x (k-blocks per unit + fixed cost).
-static int choose_splits(int tiles, int num_kb, int sms) {
-  int best = 1;
-  double best_t = 1e30;
-  for (int s = 1; s <= 8 && s <= num_kb / 4; ++s) {
-    const int units = tiles * s;
-    const int waves = (units + sms - 1) / sms;
-    const double t = waves * ((double)((num_kb + s - 1) / s) + 6.0);
-    if (t < best_t - 1e-9) { best_t = t; best = s; }
-  }
-  return best;
-}
-
 template <int BN, int EPI>
 static cudaError_t run(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mb2,
-                       int M, int N, int K, int splits, const EpiParams &ep, int *status,
+                       int M, int N, int K, bool stream_k, const EpiParams &ep, int *status,
                        cudaStream_t s) {
   using C = Cfg<BN, EPI>;
   static bool attr = false;
@@ -502,10 +524,11 @@ static cudaError_t run(const CUtensorMap &ma, const CUtensorMap &mb, const CUten
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int n_units = ((M + BM - 1) / BM) * ((N + C::kOutN - 1) / C::kOutN) * splits;
-  const int grid = n_units < num_sms() ? n_units : num_sms();
-  gemm_tc_kernel<BN, EPI><<<grid, kThreads, C::kSmem, s>>>(ma, mb, mb2, M, N, K, splits, ep,
-                                                           status);
+  const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + C::kOutN - 1) / C::kOutN);
+  const int64_t work = stream_k ? tiles * ((K + BK - 1) / BK) : tiles;
+  const int grid = work < num_sms() ? (int)work : num_sms();
+  gemm_tc_kernel<BN, EPI><<<grid, kThreads, C::kSmem, s>>>(ma, mb, mb2, M, N, K,
+                                                           stream_k ? 1 : 0, ep, status);
   return launched(1);
 }
 
@@ -521,15 +544,14 @@ cudaError_t launch_gemm_tc(const void *A, int64_t lda, const void *W, const void
   ep.out = out;
   ep.ldo = ldo;
   if (!make_map(&ma, A, M, K, lda, BM)) return cudaErrorInvalidValue;
-  const int num_kb = (K + BK - 1) / BK;
   switch (epi) {
     case EPI_SWIGLU: {
       if (!make_map(&mb, W, N, K, ldw, 128) || !make_map(&mb2, W2, N, K, ldw, 128))
         return cudaErrorInvalidValue;
-      return run<128, EPI_SWIGLU>(ma, mb, mb2, M, N, K, 1, ep, status, s);
+      return run<128, EPI_SWIGLU>(ma, mb, mb2, M, N, K, false, ep, status, s);
     }
     case EPI_QKV: {
-      if (!qkv || !make_map(&mb, W, N, K, ldw, 128)) return cudaErrorInvalidValue;
+      if (!qkv || !make_map(&mb, W, N, K, ldw, 256)) return cudaErrorInvalidValue;
       ep.pos = qkv->pos;
       ep.dst_row = qkv->dst_row;
       ep.k_cache = qkv->k_cache;
@@ -538,26 +560,24 @@ cudaError_t launch_gemm_tc(const void *A, int64_t lda, const void *W, const void
       ep.rope = reinterpret_cast<const float2 *>(qkv->rope);
       ep.n_q_heads = qkv->n_q_heads;
       ep.n_kv_heads = qkv->n_kv_heads;
-      return run<128, EPI_QKV>(ma, mb, mb, M, N, K, 1, ep, status, s);
+      return run<256, EPI_QKV>(ma, mb, mb, M, N, K, false, ep, status, s);
     }
     case EPI_RESID: {
       const bool wide = N % 256 == 0;
       if (!make_map(&mb, W, N, K, ldw, wide ? 256 : 128)) return cudaErrorInvalidValue;
-      const int tiles = ((M + BM - 1) / BM) * (N / (wide ? 256 : 128));
-      const int splits = choose_splits(tiles, num_kb, num_sms());
-      if (wide) return run<256, EPI_RESID>(ma, mb, mb, M, N, K, splits, ep, status, s);
-      return run<128, EPI_RESID>(ma, mb, mb, M, N, K, splits, ep, status, s);
+      if (wide) return run<256, EPI_RESID>(ma, mb, mb, M, N, K, true, ep, status, s);
+      return run<128, EPI_RESID>(ma, mb, mb, M, N, K, true, ep, status, s);
     }
     case EPI_STORE:
     case EPI_STORE_F32: {
       const bool wide = N % 256 == 0;
       if (!make_map(&mb, W, N, K, ldw, wide ? 256 : 128)) return cudaErrorInvalidValue;
       if (epi == EPI_STORE) {
-        if (wide) return run<256, EPI_STORE>(ma, mb, mb, M, N, K, 1, ep, status, s);
-        return run<128, EPI_STORE>(ma, mb, mb, M, N, K, 1, ep, status, s);
+        if (wide) return run<256, EPI_STORE>(ma, mb, mb, M, N, K, false, ep, status, s);
+        return run<128, EPI_STORE>(ma, mb, mb, M, N, K, false, ep, status, s);
       }
-      if (wide) return run<256, EPI_STORE_F32>(ma, mb, mb, M, N, K, 1, ep, status, s);
-      return run<128, EPI_STORE_F32>(ma, mb, mb, M, N, K, 1, ep, status, s);
+      if (wide) return run<256, EPI_STORE_F32>(ma, mb, mb, M, N, K, false, ep, status, s);
+      return run<128, EPI_STORE_F32>(ma, mb, mb, M, N, K, false, ep, status, s);
     }
   }
   return cudaErrorInvalidValue;

@@ -56,38 +56,79 @@ cudaError_t launch_embed(const int32_t *const *tokens, const BatchMeta &bm,
 }
 
 // ---------------------------------------------------------------- RMSNorm --
-// out[i] = h[src(i)] / sqrt(mean(h[src(i)]^2) + eps) * gain, one CTA per row.
+// out[i] = h[src(i)] / sqrt(mean(h[src(i)]^2) + eps) * gain, written as
+// 16-byte bf16 vectors (or float4 pairs).
+template <typename T>
+__device__ __forceinline__ void store8(T *p, const float (&v)[8]);
+template <>
+__device__ __forceinline__ void store8<bf16>(bf16 *p, const float (&v)[8]) {
+  uint4 pk;
+  __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) e[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+  *reinterpret_cast<uint4 *>(p) = pk;
+}
+template <>
+__device__ __forceinline__ void store8<float>(float *p, const float (&v)[8]) {
+  reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// Rows of up to kNormMaxD floats; 128 threads per row, two rows per CTA.
+// Every load of a thread is issued before the first is used (the row stays
+// in registers), so a row costs one memory round trip.
+constexpr int kNormMaxD = 8192;
+constexpr int kNormSteps = kNormMaxD / (128 * 8);
+
 template <typename T>
 __global__ void __launch_bounds__(256)
 rmsnorm_kernel(const float *__restrict__ h, int64_t ld_h,
-               const int32_t *__restrict__ src_rows, int d,
+               const int32_t *__restrict__ src_rows, int n, int d,
                const float *__restrict__ gain, float eps, T *__restrict__ out,
                int64_t ld_out) {
-  __shared__ float red[8];
-  const int i = blockIdx.x;
-  const int64_t src = src_rows ? src_rows[i] : i;
+  __shared__ float red[2][4];
+  const int sub = threadIdx.x >> 7, t = threadIdx.x & 127;
+  const int i = blockIdx.x * 2 + sub;
+  const bool ok = i < n;
+  const int64_t src = ok ? (src_rows ? src_rows[i] : i) : 0;
   const float *x = h + src * ld_h;
+  float v[kNormSteps][8];
   float ss = 0.f;
-  for (int c = threadIdx.x * 4; c < d; c += blockDim.x * 4) {
-    const float4 v = *reinterpret_cast<const float4 *>(x + c);
-    ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss);
-    ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
-  }
-  ss = warp_sum(ss);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  float tot = 0.f;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) tot += red[w];
+  for (int k = 0; k < kNormSteps; ++k) {
+    const int c = (k * 128 + t) * 8;
+    if (ok && c < d) {
+      const float4 a = *reinterpret_cast<const float4 *>(x + c);
+      const float4 b = *reinterpret_cast<const float4 *>(x + c + 4);
+      v[k][0] = a.x; v[k][1] = a.y; v[k][2] = a.z; v[k][3] = a.w;
+      v[k][4] = b.x; v[k][5] = b.y; v[k][6] = b.z; v[k][7] = b.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[k][e] = 0.f;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kNormSteps; ++k)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = fmaf(v[k][e], v[k][e], ss);
+  ss = warp_sum(ss);
+  if ((t & 31) == 0) red[sub][t >> 5] = ss;
+  __syncthreads();
+  if (!ok) return;
+  const float tot = red[sub][0] + red[sub][1] + red[sub][2] + red[sub][3];
   const float inv = rsqrtf(tot / (float)d + eps);
   T *o = out + (int64_t)i * ld_out;
-  for (int c = threadIdx.x * 4; c < d; c += blockDim.x * 4) {
-    const float4 v = *reinterpret_cast<const float4 *>(x + c);
-    const float4 g = *reinterpret_cast<const float4 *>(gain + c);
-    o[c + 0] = from_f<T>(v.x * inv * g.x);
-    o[c + 1] = from_f<T>(v.y * inv * g.y);
-    o[c + 2] = from_f<T>(v.z * inv * g.z);
-    o[c + 3] = from_f<T>(v.w * inv * g.w);
+#pragma unroll
+  for (int k = 0; k < kNormSteps; ++k) {
+    const int c = (k * 128 + t) * 8;
+    if (c < d) {
+      const float4 ga = *reinterpret_cast<const float4 *>(gain + c);
+      const float4 gb = *reinterpret_cast<const float4 *>(gain + c + 4);
+      const float y[8] = {v[k][0] * inv * ga.x, v[k][1] * inv * ga.y, v[k][2] * inv * ga.z,
+                          v[k][3] * inv * ga.w, v[k][4] * inv * gb.x, v[k][5] * inv * gb.y,
+                          v[k][6] * inv * gb.z, v[k][7] * inv * gb.w};
+      store8<T>(o + c, y);
+    }
   }
 }
 
@@ -96,12 +137,14 @@ cudaError_t launch_rmsnorm(const float *h, int64_t ld_h, const int32_t *src_rows
                            void *out, int64_t ld_out, cb_dtype out_dt,
                            cudaStream_t s) {
   if (n == 0) return cudaSuccess;
+  if (d > kNormMaxD) return cudaErrorInvalidValue;
+  const int blocks = (n + 1) / 2;
   if (out_dt == CB_BF16)
-    rmsnorm_kernel<bf16><<<n, 256, 0, s>>>(h, ld_h, src_rows, d, gain, eps,
-                                           reinterpret_cast<bf16 *>(out), ld_out);
+    rmsnorm_kernel<bf16><<<blocks, 256, 0, s>>>(h, ld_h, src_rows, n, d, gain, eps,
+                                                reinterpret_cast<bf16 *>(out), ld_out);
   else
-    rmsnorm_kernel<float><<<n, 256, 0, s>>>(h, ld_h, src_rows, d, gain, eps,
-                                            reinterpret_cast<float *>(out), ld_out);
+    rmsnorm_kernel<float><<<blocks, 256, 0, s>>>(h, ld_h, src_rows, n, d, gain, eps,
+                                                 reinterpret_cast<float *>(out), ld_out);
   return launched(1);
 }
 

@@ -215,3 +215,37 @@ def test_bf16_llama_truncated_free_selection(llama2):
     jac = len(set(sel) & set(ref.selected)) / len(set(sel) | set(ref.selected))
     print(f"bf16 free-selection Jaccard vs oracle: {jac:.3f}")
     assert jac > 0.5
+
+
+def test_blend_replays_from_a_cuda_graph(tiny, llama2):
+    """cb_blend_prefill allocates nothing and never synchronises, so one call
+    captured into a CUDA graph replays the same computation.  The fp32 path
+    is deterministic (bit-exact); the bf16 path's split-K residual adds use
+    atomics, so it is compared within rounding."""
+    for setup, exact in ((tiny, True), (llama2, False)):
+        reqs = setup.gpu_reqs()
+        direct = setup.model.cb_blend_prefill(reqs, 1500)
+        outs = {k: (torch.empty_like(v) if v is not None else None) for k, v in direct.items()}
+        outs["workspace"] = torch.empty_like(direct["workspace"])
+        setup.model.cb_blend_prefill(reqs, 1500, outputs=outs)      # warm-up
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            setup.model.cb_blend_prefill(reqs, 1500, outputs=outs)
+        for key in ("k_cache", "hidden"):
+            outs[key].zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert R.device_status() == 0
+        if exact:
+            assert torch.equal(outs["selected"], direct["selected"])
+        else:   # a deviation tie at fp32 rounding level may swap one index
+            a = set(outs["selected"].tolist())
+            b = set(direct["selected"].tolist())
+            assert len(a & b) >= 0.99 * len(b)
+            if a != b:
+                continue
+        for key in ("k_cache", "v_cache", "hidden"):
+            if exact:
+                assert torch.equal(outs[key], direct[key]), key
+            else:
+                assert rms_rel(host(outs[key]), host(direct[key])) < 1e-3, key

@@ -317,7 +317,7 @@ def test_tensor_core_gemm_llama_shapes(M):
     h = dev(h0)
     model.cb_linear(dev(G, torch.bfloat16), dw["w_down"], h, L.CB_EPI_RESID)
     ref = h0 + G.astype(np.float64) @ lw["w_down"].astype(np.float64).T
-    assert rms_rel(host(h), ref) < 1e-5
+    assert rms_rel(host(h), ref) < 5e-5      # fp32 accumulation over K = 14336
     g = torch.empty(M, 14336, dtype=torch.bfloat16, device="cuda")
     model.cb_linear(dev(A, torch.bfloat16), dw["w_gate"], g, L.CB_EPI_SWIGLU, W2=dw["w_up"])
     ref = O.silu(A64 @ lw["w_gate"].astype(np.float64).T) * (A64 @ lw["w_up"].astype(np.float64).T)
