@@ -116,6 +116,22 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+# --------------------------------------------------------------- ranks --
+def combine_ranks(local_ms, local_units, device=None):
+    """Whole-job view of a timed region run by independent replicas: the
+    slowest rank's interval and the work units of all ranks together.  The
+    local values are returned unchanged outside torch.distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(local_ms), int(local_units)
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    u = torch.tensor([float(local_units)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(round(u.item()))
+
+
 # ------------------------------------------------------------ GPU setup --
 def device_weights(shape, seed, device):
     """Random-init weights generated on the device (seeded): projections
@@ -347,13 +363,9 @@ def run_ours(args):
         dist.barrier()
     clk = clocks.stop()
     per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    total_ms = ev[0].elapsed_time(ev[-1])
-    if world > 1:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, tokens = combine_ranks(ev[0].elapsed_time(ev[-1]), B * T * args.steps, device)
     ms_per_step = total_ms / args.steps
-    value = world * B * T / (ms_per_step / 1e3)
+    value = tokens / (total_ms / 1e3)
 
     # ---- end to end: pinned host tokens in, first token + selection out
     sel_host = torch.empty(int(plan.K_total), dtype=torch.int32).pin_memory()
@@ -370,12 +382,8 @@ def run_ours(args):
         tok_out.copy_(outs["first_token"], non_blocking=True)
     e1.record(st)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * B * T / (e2e_ms / args.steps / 1e3)
+    e2e_ms, e2e_tokens = combine_ranks(e0.elapsed_time(e1), B * T * args.steps, device)
+    e2e_value = e2e_tokens / (e2e_ms / 1e3)
     if R.device_status() != 0:
         raise RuntimeError("device status set during the timed region")
 

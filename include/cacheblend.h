@@ -107,6 +107,18 @@ cb_status cb_debug_expire_wait(int limit_us, cb_stream stream);
  * library's launches. */
 unsigned long long cb_debug_launch_count(void);
 
+/* Which bf16 tensor-core GEMM the library uses for every projection issued
+ * after the call (process-wide):
+ *   CB_GEMM_AUTO (0)     per epilogue and row count, the faster of the two;
+ *   CB_GEMM_TOKEN_M (1)  token rows on the MMA's M side (128-row tiles);
+ *   CB_GEMM_SWAP_AB (2)  weight rows on M, tokens on N (few-row form).
+ * Both compute the same function; tests use the switch to check each one
+ * on every epilogue.  Returns CB_ERR_INVALID_ARG for any other value. */
+#define CB_GEMM_AUTO 0
+#define CB_GEMM_TOKEN_M 1
+#define CB_GEMM_SWAP_AB 2
+cb_status cb_debug_gemm_path(int path);
+
 /* ------------------------------------------------------------------------ */
 /* RoPE table                                                               */
 /* ------------------------------------------------------------------------ */

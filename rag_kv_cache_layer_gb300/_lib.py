@@ -21,6 +21,7 @@ STATUS_NAMES = {0: "CB_OK", 1: "CB_ERR_INVALID_ARG", 2: "CB_ERR_UNSUPPORTED",
 CB_F32, CB_BF16 = 0, 1
 CB_POLICY_TOKEN_TOPK, CB_POLICY_DOC_ALIGNED = 0, 1
 CB_EPI_STORE, CB_EPI_RESID, CB_EPI_SWIGLU = 0, 1, 2
+CB_GEMM_AUTO, CB_GEMM_TOKEN_M, CB_GEMM_SWAP_AB = 0, 1, 2
 CB_MAX_BATCH = 64
 CB_MAX_SPANS = 1024
 
@@ -114,6 +115,7 @@ def _load():
         "cb_get_device_status": (S, [C.POINTER(i32)]),
         "cb_debug_expire_wait": (S, [i32, vp]),
         "cb_debug_launch_count": (C.c_ulonglong, []),
+        "cb_debug_gemm_path": (S, [i32]),
         "cb_rope_table_elems": (C.c_size_t, [i32, i32]),
         "cb_rope_table_init": (S, [vp, i32, i32, C.c_float, vp]),
         "cb_rope_reposition": (S, [C.POINTER(StitchDesc), i32, i32, i32, vp, vp,
@@ -159,7 +161,8 @@ lib = _load()
 # names every build of the library must export (include/cacheblend.h)
 EXPORTED = [
     "cb_last_error_message", "cb_version", "cb_get_device_status",
-    "cb_debug_expire_wait", "cb_debug_launch_count", "cb_rope_table_elems",
+    "cb_debug_expire_wait", "cb_debug_launch_count", "cb_debug_gemm_path",
+    "cb_rope_table_elems",
     "cb_rope_table_init",
     "cb_rope_reposition", "cb_select_workspace_size", "cb_kv_deviation_topk",
     "cb_kv_deviation_topk_noalloc",

@@ -18,7 +18,7 @@ __all__ = [
     "dtype_code", "torch_dtype", "cb_rope_table_init", "cb_rope_reposition",
     "cb_kv_deviation_topk", "cb_kv_deviation_topk_noalloc", "cb_gather_rows",
     "cb_scatter_kv",
-    "cb_sparse_query_attention", "cb_debug_expire_wait", "Seg", "Req",
+    "cb_sparse_query_attention", "cb_debug_expire_wait", "cb_debug_gemm_path", "Seg", "Req",
     "BlendModel", "ChunkStore", "select_count", "device_status",
 ]
 
@@ -170,6 +170,10 @@ def cb_sparse_query_attention(q, q_pos, reqs, k_cache, v_cache, n_q_heads,
 
 def cb_debug_expire_wait(limit_us: int, stream=None):
     check(lib.cb_debug_expire_wait(limit_us, _s(stream)))
+
+
+def cb_debug_gemm_path(path: int):
+    check(lib.cb_debug_gemm_path(path))
 
 
 # ----------------------------------------------------------------- model --

@@ -25,6 +25,7 @@ SOURCES = [
     "k_rows.cu",
     "k_gemm_simt.cu",
     "k_gemm_tc.cu",
+    "k_gemm_sab.cu",
     "k_attn_simt.cu",
     "k_attn_tc.cu",
     "k_noalloc.cu",

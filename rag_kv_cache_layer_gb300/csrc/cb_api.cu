@@ -59,6 +59,14 @@ static std::atomic<unsigned long long> g_launches{0};
 void cb::note_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
 extern "C" unsigned long long cb_debug_launch_count(void) { return g_launches.load(); }
 
+static std::atomic<int> g_gemm_path{CB_GEMM_AUTO};
+extern "C" cb_status cb_debug_gemm_path(int path) {
+  if (path != CB_GEMM_AUTO && path != CB_GEMM_TOKEN_M && path != CB_GEMM_SWAP_AB)
+    return fail(CB_ERR_INVALID_ARG, "path must be CB_GEMM_AUTO, _TOKEN_M or _SWAP_AB");
+  g_gemm_path.store(path);
+  return CB_OK;
+}
+
 // ----------------------------------------------------------- status word --
 static __device__ int g_status_word;
 
@@ -407,7 +415,13 @@ static cb_status run_linear(const cb_model *m, const void *A, int64_t lda, const
   if (m->cfg.dtype == CB_BF16) {
     int *st;
     CB_TRY(status_ptr(&st));
-    CB_CUDA(launch_gemm_tc(A, lda, W, W2, ldw, M, N, K, epi, out, ldo, qkv, st, s));
+    const int path = g_gemm_path.load(std::memory_order_relaxed);
+    const bool sab = path == CB_GEMM_SWAP_AB ||
+                     (path == CB_GEMM_AUTO && gemm_sab_preferred(M, epi));
+    if (sab)
+      CB_CUDA(launch_gemm_sab(A, lda, W, W2, ldw, M, N, K, epi, out, ldo, qkv, st, s));
+    else
+      CB_CUDA(launch_gemm_tc(A, lda, W, W2, ldw, M, N, K, epi, out, ldo, qkv, st, s));
   } else {
     if (epi == EPI_QKV) return fail(CB_ERR_UNSUPPORTED, "fused QKV epilogue is bf16-only");
     CB_CUDA(launch_gemm_simt(A, lda, W, W2, ldw, M, N, K, epi, out, ldo, m->cfg.dtype, s));

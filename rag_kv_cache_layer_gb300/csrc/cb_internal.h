@@ -138,6 +138,13 @@ cudaError_t launch_gemm_tc(const void *A, int64_t lda, const void *W,
                            const void *W2, int64_t ldw, int M, int N, int K,
                            GemmEpi epi, void *out, int64_t ldo,
                            const QkvEpi *qkv, int *status, cudaStream_t s);
+// The same GEMM with the operands swapped (weights on the MMA's M side,
+// tokens on N), for few rows; gemm_sab_preferred says when to use it.
+bool gemm_sab_preferred(int M, GemmEpi epi);
+cudaError_t launch_gemm_sab(const void *A, int64_t lda, const void *W,
+                            const void *W2, int64_t ldw, int M, int N, int K,
+                            GemmEpi epi, void *out, int64_t ldo,
+                            const QkvEpi *qkv, int *status, cudaStream_t s);
 
 // ------------------------------------------------------------ attention --
 struct AttnReq {

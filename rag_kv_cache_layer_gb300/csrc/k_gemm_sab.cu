@@ -1,0 +1,419 @@
+// bf16 tcgen05 GEMM for few rows (the compact layers' ~500 rows), operands
+// swapped: out[tok][f] = epi(sum_k A[tok][k] W[f][k]) is computed as
+// D[f][tok] = W_tile A_tile^T with the 128 weight rows of a tile as the MMA's
+// M side and the tokens as its N side (N = BT, a multiple of 16 up to 256).
+// Splitting M_tok rows into ceil(M_tok / 256) token tiles of equal width
+// (176 for 524 rows) wastes 1% of the work where 128-row tiles waste 18%.
+//
+// Roles as in the standard kernel: warp 0 TMA producer, warp 1 TMEM owner and
+// MMA issuer, warps 2..5 epilogue; the fp32 accumulator [128 features][BT
+// tokens] is double-buffered in TMEM (columns 0 and 256).  Epilogue thread r
+// owns feature r of the tile, so for every token the 32 lanes of a warp
+// write 32 consecutive features.  Two epilogues pair feature r with r + 64
+// through a shared-memory exchange: SwiGLU (tile rows 0..63 are W_gate rows,
+// 64..127 the matching W_up rows) and the QKV RoPE (rotate-half pairs
+// (e, e + 64) of a 128-wide head).  Residual outputs may use stream-K.
+#include "cb_internal.h"
+#include "cb_tc.cuh"
+
+namespace cb {
+namespace sab {
+
+using namespace tcx;
+
+constexpr int FM = 128;                      // weight rows per tile
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+constexpr int kTileW = FM * BK * 2;          // 16 KB
+constexpr int kTrStride = 132;               // floats per transposed token row
+constexpr int kTr = 32 * kTrStride * 4;      // 32 tokens x 128 features, fp32
+constexpr int kSmemMax = 232448;
+
+struct Params {
+  int M, N, K;           // tokens, output features, reduction
+  int BT, n_tt, n_ft;    // token tile width, token tiles, feature tiles
+  int stream_k;
+  int stages, stage_bytes;
+  uint32_t idesc;
+  // epilogue
+  void *out;
+  int64_t ldo;
+  const int32_t *pos, *dst_row;
+  void *k_cache, *v_cache;
+  int64_t ld_kv;
+  const float2 *rope;
+  int Hq, Hkv;
+};
+
+struct Work {
+  int n_tt, num_kb;
+  bool sk;
+  int64_t w, w_end;
+  __device__ Work(const Params &p, int num_kb_) : n_tt(p.n_tt), num_kb(num_kb_), sk(p.stream_k != 0) {
+    const int64_t tiles = (int64_t)p.n_tt * p.n_ft;
+    if (sk) {
+      const int64_t total = tiles * num_kb_;
+      w = total * blockIdx.x / gridDim.x;
+      w_end = total * (blockIdx.x + 1) / gridDim.x;
+    } else {
+      w = blockIdx.x;
+      w_end = tiles;
+    }
+  }
+  // token tile fastest: CTAs running together share the weight tile
+  __device__ bool next(int &tt, int &ft, int &kb0, int &kb1) {
+    if (w >= w_end) return false;
+    int tile;
+    if (sk) {
+      tile = (int)(w / num_kb);
+      kb0 = (int)(w % num_kb);
+      const int64_t left = w_end - w;
+      kb1 = (int)(kb0 + left < num_kb ? kb0 + left : num_kb);
+      w += kb1 - kb0;
+    } else {
+      tile = (int)w;
+      kb0 = 0;
+      kb1 = num_kb;
+      w += gridDim.x;
+    }
+    tt = tile % n_tt;
+    ft = tile / n_tt;
+    return true;
+  }
+};
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void store_bf16x8(bf16 *dst, const float *v) {
+  uint4 pk;
+  __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) e[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+  *reinterpret_cast<uint4 *>(dst) = pk;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW,
+                const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ Params p,
+                int *status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  float *tr = reinterpret_cast<float *>(smem + p.stages * p.stage_bytes);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.stages * p.stage_bytes + kTr);
+  uint64_t *full = bars;                 // [stages]
+  uint64_t *empty = bars + 8;            // [stages]
+  uint64_t *tfull = bars + 16;           // [2]
+  uint64_t *tempty = bars + 18;          // [2]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 20);
+  volatile int *fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_kb = (p.K + BK - 1) / BK;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), 128);
+    }
+    *fail = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      bool ok = true;
+      Work wk(p, num_kb);
+      int tt, ft, kb0, kb1;
+      while (ok && wk.next(tt, ft, kb0, kb1)) {
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, kWaitLimitNs, status) ||
+              *fail) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full[stage]);
+          expect_tx(fb, p.stage_bytes);
+          uint8_t *sw = smem + stage * p.stage_bytes;
+          uint8_t *sx = sw + kTileW;
+          if (EPI == EPI_SWIGLU) {
+            tma_load_2d(smem_u32(sw), &mapW, fb, kb * BK, ft * 64);
+            tma_load_2d(smem_u32(sw + 64 * 128), &mapW2, fb, kb * BK, ft * 64);
+          } else {
+            tma_load_2d(smem_u32(sw), &mapW, fb, kb * BK, ft * FM);
+          }
+          tma_load_2d(smem_u32(sx), &mapX, fb, kb * BK, tt * p.BT);
+          ++issued[stage];
+          if (++stage == p.stages) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) {
+        *fail = 1;
+        for (int s = 0; s < p.stages; ++s)
+          if (issued[s] > 0)
+            mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((issued[s] - 1) & 1), 10000000ull,
+                              nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int buf = 0;
+      uint32_t bphase = 0;
+      bool ok = true;
+      Work wk(p, num_kb);
+      int tt, ft, kb0, kb1;
+      while (ok && wk.next(tt, ft, kb0, kb1)) {
+        if (!mbar_wait_bounded(smem_u32(&tempty[buf]), bphase ^ 1, kWaitLimitNs, status) ||
+            *fail) {
+          ok = false;
+          break;
+        }
+        fence_after();
+        const uint32_t d = tmem + buf * 256;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, kWaitLimitNs, status) || *fail) {
+            ok = false;
+            break;
+          }
+          fence_after();
+          const uint32_t sw = smem_u32(smem + stage * p.stage_bytes);
+          const uint64_t dw = desc_kmajor(sw), dx = desc_kmajor(sw + kTileW);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma(d, dw + 2 * k, dx + 2 * k, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          commit(smem_u32(&empty[stage]));
+          if (++stage == p.stages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        commit(smem_u32(&tfull[buf]));
+        if (++buf == 2) { buf = 0; bphase ^= 1; }
+      }
+      if (!ok) *fail = 1;
+    }
+  } else {
+    // ----------------------------------------------------------- epilogue
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;                 // feature row of the tile
+    int buf = 0;
+    uint32_t bphase = 0;
+    Work wk(p, num_kb);
+    int tt, ft, kb0, kb1;
+    while (wk.next(tt, ft, kb0, kb1)) {
+      const bool whole = kb0 == 0 && kb1 == num_kb;
+      const bool bad =
+          !mbar_wait_bounded(smem_u32(&tfull[buf]), bphase, kWaitLimitNs, status) || *fail;
+      if (__any_sync(0xffffffffu, bad)) {
+        *fail = 1;
+        break;
+      }
+      fence_after();
+      const uint32_t tbase = tmem + buf * 256 + ((uint32_t)(quad * 32) << 16);
+      const int tok0 = tt * p.BT;
+      int head = 0;
+      bool rotate = false;
+      if (EPI == EPI_QKV) {
+        head = ft;
+        rotate = head < p.Hq + p.Hkv;
+      }
+      const int t = threadIdx.x - 64;                // 0..127 among the epilogue threads
+#pragma unroll 1
+      for (int c = 0; c < p.BT; c += 32) {
+        float x[32];
+        tmem_ld32(tbase + c, x);
+        // transpose: feature column r of 32 tokens -> rows of the chunk
+#pragma unroll
+        for (int i = 0; i < 32; ++i) tr[i * kTrStride + r] = x[i];
+        epi_bar();
+        if (EPI == EPI_STORE) {
+          // 32 tokens x 16 vectors of 8 bf16 features
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int v = t + 128 * q, i = v >> 4, j = v & 15;
+            const int tok = tok0 + c + i, f = ft * FM + 8 * j;
+            if (c + i < p.BT && tok < p.M && f < p.N)
+              store_bf16x8(reinterpret_cast<bf16 *>(p.out) + (int64_t)tok * p.ldo + f,
+                           tr + i * kTrStride + 8 * j);
+          }
+        } else if (EPI == EPI_STORE_F32 || EPI == EPI_RESID) {
+          // 32 tokens x 32 vectors of 4 fp32 features
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int v = t + 128 * q, i = v >> 5, j = v & 31;
+            const int tok = tok0 + c + i, f = ft * FM + 4 * j;
+            if (c + i < p.BT && tok < p.M && f < p.N) {
+              const float4 a = *reinterpret_cast<const float4 *>(tr + i * kTrStride + 4 * j);
+              float4 *o = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) +
+                                                     (int64_t)tok * p.ldo + f);
+              if (EPI == EPI_STORE_F32) {
+                *o = a;
+              } else if (whole) {
+                float4 h = *o;
+                h.x += a.x; h.y += a.y; h.z += a.z; h.w += a.w;
+                *o = h;
+              } else {
+                atomicAdd(o, a);
+              }
+            }
+          }
+        } else if (EPI == EPI_SWIGLU) {
+          // tile rows 0..63 gate, 64..127 up: 32 tokens x 8 vectors of 8
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int v = t + 128 * q, i = v >> 3, j = v & 7;
+            const int tok = tok0 + c + i, f = ft * 64 + 8 * j;
+            if (c + i < p.BT && tok < p.M && f < p.N) {
+              const float *g = tr + i * kTrStride + 8 * j;
+              const float *u = g + 64;
+              float y[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) y[e] = g[e] / (1.f + __expf(-g[e])) * u[e];
+              store_bf16x8(reinterpret_cast<bf16 *>(p.out) + (int64_t)tok * p.ldo + f, y);
+            }
+          }
+        } else {  // EPI_QKV: one head per tile
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int v = t + 128 * q, i = v >> 4, j = v & 15;
+            const int tok = tok0 + c + i;
+            if (c + i >= p.BT || tok >= p.M) continue;
+            const float *row = tr + i * kTrStride;
+            float y[8];
+            bf16 *dst;
+            if (rotate) {
+              // rotate-half pairs (e, e + 64) at the token's position
+              const int e0 = 8 * (j & 7);
+              const float2 *cs = p.rope + (int64_t)p.pos[tok] * 64 + e0;
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float2 w = __ldg(cs + e);
+                const float x1 = row[e0 + e], x2 = row[64 + e0 + e];
+                y[e] = j < 8 ? x1 * w.x - x2 * w.y : x2 * w.x + x1 * w.y;
+              }
+              dst = head < p.Hq
+                        ? reinterpret_cast<bf16 *>(p.out) + (int64_t)tok * p.ldo + head * 128
+                        : reinterpret_cast<bf16 *>(p.k_cache) + (int64_t)p.dst_row[tok] * p.ld_kv +
+                              (head - p.Hq) * 128;
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) y[e] = row[8 * j + e];
+              dst = reinterpret_cast<bf16 *>(p.v_cache) + (int64_t)p.dst_row[tok] * p.ld_kv +
+                    (head - p.Hq - p.Hkv) * 128;
+            }
+            store_bf16x8(dst + 8 * j, y);
+          }
+        }
+        epi_bar();
+      }
+      fence_before();
+      arrive(smem_u32(&tempty[buf]));
+      if (++buf == 2) { buf = 0; bphase ^= 1; }
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int EPI>
+static cudaError_t run(const CUtensorMap &mx, const CUtensorMap &mw, const CUtensorMap &mw2,
+                       Params &p, int *status, cudaStream_t s) {
+  const int fixed = kTr + 256 + 1024;
+  p.stage_bytes = kTileW + p.BT * BK * 2;
+  p.stages = (kSmemMax - fixed) / p.stage_bytes;
+  if (p.stages > 8) p.stages = 8;
+  if (p.stages < 2) return cudaErrorInvalidValue;
+  const int smem = p.stages * p.stage_bytes + fixed;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_sab_kernel<EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int64_t tiles = (int64_t)p.n_tt * p.n_ft;
+  const int64_t work = p.stream_k ? tiles * ((p.K + BK - 1) / BK) : tiles;
+  const int grid = work < num_sms() ? (int)work : num_sms();
+  gemm_sab_kernel<EPI><<<grid, kThreads, smem, s>>>(mx, mw, mw2, p, status);
+  return launched(1);
+}
+
+}  // namespace sab
+
+// Measured at the Llama-3-8B projection shapes with M = 524 token rows: the
+// swapped form wins on the residual projections (O, down: 27 and 61 us
+// against 32 and 67 us) and loses on the fused Q/K/V and SwiGLU epilogues.
+bool gemm_sab_preferred(int M, GemmEpi epi) {
+  return M > 0 && M <= 1024 && epi == EPI_RESID;
+}
+
+cudaError_t launch_gemm_sab(const void *A, int64_t lda, const void *W, const void *W2,
+                            int64_t ldw, int M, int N, int K, GemmEpi epi, void *out,
+                            int64_t ldo, const QkvEpi *qkv, int *status, cudaStream_t s) {
+  using namespace sab;
+  if (M == 0 || N == 0) return cudaSuccess;
+  Params p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.n_tt = (M + 255) / 256;
+  p.BT = ((M + p.n_tt - 1) / p.n_tt + 15) / 16 * 16;
+  p.idesc = idesc_bf16(FM, p.BT);
+  p.out = out;
+  p.ldo = ldo;
+  CUtensorMap mx, mw, mw2;
+  if (!make_map(&mx, A, M, K, lda, p.BT)) return cudaErrorInvalidValue;
+  switch (epi) {
+    case EPI_SWIGLU:
+      p.n_ft = (N + 63) / 64;
+      if (!make_map(&mw, W, N, K, ldw, 64) || !make_map(&mw2, W2, N, K, ldw, 64))
+        return cudaErrorInvalidValue;
+      return run<EPI_SWIGLU>(mx, mw, mw2, p, status, s);
+    case EPI_QKV:
+      if (!qkv) return cudaErrorInvalidValue;
+      p.n_ft = N / 128;
+      p.pos = qkv->pos;
+      p.dst_row = qkv->dst_row;
+      p.k_cache = qkv->k_cache;
+      p.v_cache = qkv->v_cache;
+      p.ld_kv = qkv->ld_kv;
+      p.rope = reinterpret_cast<const float2 *>(qkv->rope);
+      p.Hq = qkv->n_q_heads;
+      p.Hkv = qkv->n_kv_heads;
+      if (!make_map(&mw, W, N, K, ldw, FM)) return cudaErrorInvalidValue;
+      return run<EPI_QKV>(mx, mw, mw, p, status, s);
+    case EPI_RESID:
+      p.n_ft = (N + FM - 1) / FM;
+      p.stream_k = 1;
+      if (!make_map(&mw, W, N, K, ldw, FM)) return cudaErrorInvalidValue;
+      return run<EPI_RESID>(mx, mw, mw, p, status, s);
+    case EPI_STORE:
+      p.n_ft = (N + FM - 1) / FM;
+      if (!make_map(&mw, W, N, K, ldw, FM)) return cudaErrorInvalidValue;
+      return run<EPI_STORE>(mx, mw, mw, p, status, s);
+    case EPI_STORE_F32:
+      p.n_ft = (N + FM - 1) / FM;
+      if (!make_map(&mw, W, N, K, ldw, FM)) return cudaErrorInvalidValue;
+      return run<EPI_STORE_F32>(mx, mw, mw, p, status, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace cb

@@ -93,6 +93,8 @@ def test_host_validation_without_device():
     w = L.Weights(None, None, None, None)
     assert lib.cb_model_create(C.byref(cfg), C.byref(w), C.byref(h)) == L.CB_ERR_UNSUPPORTED
     assert lib.cb_debug_expire_wait(-1, None) == L.CB_ERR_INVALID_ARG
+    assert lib.cb_debug_gemm_path(3) == L.CB_ERR_INVALID_ARG
+    assert lib.cb_debug_gemm_path(L.CB_GEMM_AUTO) == L.CB_OK
     # bad doc-aligned spans are rejected on the host
     spans = (C.c_int32 * 3)(0, 5, 4)
     req = L.SelectReq(4, 2, 0, 0, 0, 0, 2, C.cast(spans, C.POINTER(C.c_int32)))

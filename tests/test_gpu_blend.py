@@ -188,9 +188,24 @@ def llama2():
     return Setup(wl, max_pos=4096)
 
 
-def test_bf16_llama_truncated_forced(llama2):
-    rq = llama2.wl.requests[0]
-    ref = llama2.oracle_blend(rq, 1500)
+@pytest.fixture(scope="module")
+def llama2_ref(llama2):
+    return llama2.oracle_blend(llama2.wl.requests[0], 1500)
+
+
+@pytest.fixture
+def gemm_path(request):
+    R.cb_debug_gemm_path(request.param)
+    yield request.param
+    R.cb_debug_gemm_path(L.CB_GEMM_AUTO)
+
+
+@pytest.mark.parametrize("gemm_path", [L.CB_GEMM_AUTO, L.CB_GEMM_TOKEN_M, L.CB_GEMM_SWAP_AB],
+                         indirect=True)
+def test_bf16_llama_truncated_forced(llama2, llama2_ref, gemm_path):
+    """Every projection of the stack (fused Q/K/V with RoPE and cache
+    scatter, O and down with residual, SwiGLU) on each tensor-core GEMM."""
+    ref = llama2_ref
     forced = torch.from_numpy(ref.selected.astype(np.int32)).cuda()
     out = llama2.model.cb_blend_prefill(llama2.gpu_reqs(), 1500, forced=forced)
     torch.cuda.synchronize()
@@ -203,10 +218,10 @@ def test_bf16_llama_truncated_forced(llama2):
     assert np.array_equal(out["rows"][:Rn].cpu().numpy(), ref.rows)
 
 
-def test_bf16_llama_truncated_free_selection(llama2):
+def test_bf16_llama_truncated_free_selection(llama2, llama2_ref):
     rq = llama2.wl.requests[0]
     out = llama2.model.cb_blend_prefill(llama2.gpu_reqs(), 1500)
-    ref = llama2.oracle_blend(rq, 1500)
+    ref = llama2_ref
     N, k = rq.n_ctx, len(ref.selected)
     d = out["deviation"][:N].cpu().numpy().astype(np.float64)
     sel = out["selected"][:k].cpu().numpy()

@@ -288,10 +288,19 @@ def test_linear_epilogues(dt_name, M):
     assert_close(host(g), ref, dt)
 
 
-@pytest.mark.parametrize("M", [524, 128, 3136])
-def test_tensor_core_gemm_llama_shapes(M):
-    """bf16 tcgen05 GEMM at the workload's projection shapes (ragged M,
-    split-K residual over K = 14336, SwiGLU over N = 14336)."""
+@pytest.fixture
+def gemm_path(request):
+    R.cb_debug_gemm_path(request.param)
+    yield request.param
+    R.cb_debug_gemm_path(L.CB_GEMM_AUTO)
+
+
+@pytest.mark.parametrize("gemm_path", [L.CB_GEMM_TOKEN_M, L.CB_GEMM_SWAP_AB], indirect=True)
+@pytest.mark.parametrize("M", [524, 128, 3136, 1])
+def test_tensor_core_gemm_llama_shapes(M, gemm_path):
+    """bf16 tcgen05 GEMMs (token rows on M, and the swapped form) at the
+    workload's projection shapes: ragged M, stream-K residual over
+    K = 14336, SwiGLU over N = 14336."""
     rng = np.random.default_rng(M)
     shape = W.ModelShape("g", 1, 4096, 32, 8, 128, 14336, 256, dtype="bf16")
     w = {"embed": np.zeros((256, 4096), np.float32),
