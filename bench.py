@@ -133,34 +133,13 @@ def combine_ranks(local_ms, local_units, device=None):
 
 
 # ------------------------------------------------------------ GPU setup --
-def device_weights(shape, seed, device):
-    """Random-init weights generated on the device (seeded): projections
-    N(0, 0.02), embeddings N(0, 1), bf16; RMSNorm gains 1."""
-    import torch
-    g = torch.Generator(device=device)
-    g.manual_seed(seed)
-    dt = torch.bfloat16
-
-    def rnd(*s, std=0.02):
-        return (torch.randn(*s, generator=g, device=device, dtype=torch.float32) * std).to(dt)
-    d, F = shape.d_model, shape.d_ffn
-    qd = shape.n_q_heads * shape.head_dim
-    w = {"embed": rnd(shape.vocab, d, std=1.0),
-         "final_norm": torch.ones(d, device=device), "layers": []}
-    for _ in range(shape.n_layers):
-        w["layers"].append({
-            "w_qkv": rnd(shape.qkv_rows, d), "w_o": rnd(d, qd),
-            "w_gate": rnd(F, d), "w_up": rnd(F, d), "w_down": rnd(d, F),
-            "norm1": torch.ones(d, device=device), "norm2": torch.ones(d, device=device)})
-    return w
-
-
 def setup_replica(rank, device, n_layers=None):
     import torch
     import rag_kv_cache_layer_gb300 as R
     wl = W.llama_rag(seed=1 + rank, n_layers=n_layers)
     shape = wl.model
-    model = R.BlendModel(shape, device_weights(shape, 1234 + rank, device), 4096, device)
+    model = R.BlendModel(shape, W.make_weights_device(shape, 1234 + rank, device), 4096,
+                         device)
     rq = wl.requests[0]
     store = R.ChunkStore(model, rq.n_ctx)
     store.prefill({s.chunk_id: torch.from_numpy(s.tokens).to(device)
@@ -175,28 +154,42 @@ def setup_replica(rank, device, n_layers=None):
     return wl, model, store, reqs, plan, outs, tokens_host, tokens_dev
 
 
-def time_dominant_kernel(model, plan, device, reps=20):
-    """The SwiGLU gate/up projection of a compact layer (the largest launch
-    of the step), timed alone with CUDA events on the current stream."""
-    import torch
-    from rag_kv_cache_layer_gb300 import _lib as L
-    s = model.shape
-    M = int(plan.R_total)
-    x = torch.randn(M, s.d_model, device=device).to(torch.bfloat16)
-    g = torch.empty(M, s.d_ffn, device=device, dtype=torch.bfloat16)
-    lw = model.w["layers"][5]
-    for _ in range(3):
-        model.cb_linear(x, lw["w_gate"], g, L.CB_EPI_SWIGLU, W2=lw["w_up"])
-    st = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for _ in range(reps):
-        model.cb_linear(x, lw["w_gate"], g, L.CB_EPI_SWIGLU, W2=lw["w_up"])
-    e1.record(st)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / reps
-    flops = 2.0 * M * s.d_model * 2 * s.d_ffn
-    return ms, flops
+# DRAM traffic of the dominant kernel from one ncu capture (dram__bytes_read
+# + dram__bytes_write of the gate/up SwiGLU launch at M = 524 rows of a
+# compact layer), valid only for the kernel source it was taken on.
+TRAFFIC_CAPTURE = {"source": "rag_kv_cache_layer_gb300/csrc/k_gemm_tc.cu",
+                   "sha256": "1ad63e322072cb59eae2bde90f0e4f403e1cd16f3591d34cf164563c528850be",
+                   "bytes_per_launch": 241595136 + 11919104,
+                   "profile": "profiles/gemm_swiglu_M524_llama8b.md"}
+
+
+def captured_traffic():
+    import hashlib
+    if TRAFFIC_CAPTURE["sha256"] is None:
+        return None
+    with open(os.path.join(ROOT, TRAFFIC_CAPTURE["source"]), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != TRAFFIC_CAPTURE["sha256"]:
+            return None      # the kernel changed since the counters were taken
+    return TRAFFIC_CAPTURE["bytes_per_launch"]
+
+
+def layer_rows(plan, n_layers, sel_layer=1):
+    """Rows each decoder layer runs on in one blended step: every row below
+    the selection layer, the compact rows from it on."""
+    return [int(plan.T_total)] * sel_layer + [int(plan.R_total)] * (n_layers - sel_layer)
+
+
+def probe_steps(L, kind, n_launches, run):
+    """Runs `run()` with the library's launch probe on one kernel class and
+    returns (launches, summed device ms)."""
+    import ctypes as C
+    L.check(L.lib.cb_debug_probe_start(kind, n_launches))
+    try:
+        run()
+    finally:
+        n, ms = C.c_int(0), C.c_float(0.0)
+        L.check(L.lib.cb_debug_probe_stop(C.byref(n), C.byref(ms)))
+    return n.value, float(ms.value)
 
 
 # ---------------------------------------------------------- CPU oracle --
@@ -374,24 +367,45 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for _ in range(args.steps):
-        tok_dev.copy_(tok_host, non_blocking=True)
-        step()
-        sel_host.copy_(outs["selected"][: int(plan.K_total)], non_blocking=True)
-        tok_out.copy_(outs["first_token"], non_blocking=True)
-    e1.record(st)
-    torch.cuda.synchronize()
+    n_layers = wl.model.n_layers
+
+    def e2e_loop():
+        e0.record(st)
+        for _ in range(args.steps):
+            tok_dev.copy_(tok_host, non_blocking=True)
+            step()
+            sel_host.copy_(outs["selected"][: int(plan.K_total)], non_blocking=True)
+            tok_out.copy_(outs["first_token"], non_blocking=True)
+        e1.record(st)
+        torch.cuda.synchronize()
+    # the dominant kernel's launches are bracketed by events on their own
+    # stream inside this timed region
+    n_dom, ms_dom = probe_steps(L, L.CB_PROBE_SWIGLU, n_layers * args.steps, e2e_loop)
     e2e_ms, e2e_tokens = combine_ranks(e0.elapsed_time(e1), B * T * args.steps, device)
     e2e_value = e2e_tokens / (e2e_ms / 1e3)
     if R.device_status() != 0:
         raise RuntimeError("device status set during the timed region")
 
+    # per-class device time of one step (untimed; the same probe)
+    kernel_us = {}
+    for name, kind in (("qkv", L.CB_PROBE_QKV), ("attention", L.CB_PROBE_ATTENTION),
+                       ("o_proj", L.CB_PROBE_O), ("swiglu", L.CB_PROBE_SWIGLU),
+                       ("down_proj", L.CB_PROBE_DOWN)):
+        n, ms = probe_steps(L, kind, n_layers, lambda: (step(), torch.cuda.synchronize()))
+        kernel_us[name] = round(ms * 1e3, 1)
+    torch.cuda.synchronize()
+    if R.device_status() != 0:
+        raise RuntimeError("device status set during the probe steps")
+
     if rank == 0:
         peaks, src = load_peaks()
-        kms, kflops = time_dominant_kernel(model, plan, device)
-        achieved = kflops / (kms / 1e3) / 1e12
-        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        s_ = wl.model
+        rows = layer_rows(plan, n_layers)
+        # algorithmic FLOPs of the gate/up projection: 2 d (2F) per row
+        kflops = args.steps * sum(rows) * 2.0 * s_.d_model * 2 * s_.d_ffn
+        kms = ms_dom / max(n_dom, 1)
+        achieved = kflops / (ms_dom / 1e3) / 1e12
+        peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": max(args.warmup, 3),
@@ -413,11 +427,16 @@ def run_ours(args):
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * 4,
                     "d2h_bytes_per_step": 4 * (int(plan.K_total) + 1)},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
-                         "kernel": f"gate/up SwiGLU projection, M={int(plan.R_total)} "
-                                   f"N=2x14336 K=4096, timed alone "
-                                   f"({kms:.3f} ms/launch)",
-                         "peak_source": f"bf16_tflops (burst) of {src}"},
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "traffic": captured_traffic(),
+                         "kernel": (f"gate/up SwiGLU projection (N=2x{s_.d_ffn}, "
+                                    f"K={s_.d_model}), {n_dom} launches inside the e2e "
+                                    f"timed region: 1 per step at M={rows[0]}, "
+                                    f"{n_layers - 1} at M={rows[-1]}; "
+                                    f"{kms * 1e3:.1f} us/launch on average"),
+                         "traffic_note": "ncu dram bytes of one M=524 launch",
+                         "peak_source": f"bf16_tflops_sustained of {src}"},
+            "kernel_us_per_step": kernel_us,
             "clocks": clk,
             "gpu_launches": launches_per_step * args.steps,
         }

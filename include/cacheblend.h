@@ -119,6 +119,22 @@ unsigned long long cb_debug_launch_count(void);
 #define CB_GEMM_SWAP_AB 2
 cb_status cb_debug_gemm_path(int path);
 
+/* Launch probe: times the launches of one kernel class of the decoder layer
+ * inside real calls.  After cb_debug_probe_start(kind, max_launches) every
+ * launch of that class (up to max_launches, on any call's stream, outside
+ * stream capture) is bracketed by two CUDA events on its own stream;
+ * cb_debug_probe_stop waits for the recorded launches and returns their
+ * count and summed device time in milliseconds, then releases the events.
+ * The attention class includes its split-KV combine kernel.  Debug use only
+ * (one probe per process; start discards an unfinished probe). */
+#define CB_PROBE_QKV 1       /* fused Q/K/V projection (+ RoPE, cache scatter) */
+#define CB_PROBE_O 2         /* attention output projection + residual */
+#define CB_PROBE_SWIGLU 3    /* gate/up projection with SiLU gating */
+#define CB_PROBE_DOWN 4      /* down projection + residual */
+#define CB_PROBE_ATTENTION 5 /* selected-query attention */
+cb_status cb_debug_probe_start(int kind, int max_launches);
+cb_status cb_debug_probe_stop(int *n_launches, float *total_ms);
+
 /* ------------------------------------------------------------------------ */
 /* RoPE table                                                               */
 /* ------------------------------------------------------------------------ */
@@ -370,9 +386,14 @@ typedef struct {
   int n_segments;
 } cb_request;
 
+/* One gradual-filtering step ([CB] select_hkvd): before layer `layer`, the
+ * context rows still selected are ranked again by the deviation of their
+ * fresh keys of that layer from the reused keys in its fused cache, and
+ * each request keeps its min(keep, current count) largest (ties to the
+ * lower position); the uncached rows are always kept. */
 typedef struct {
-  int layer;  /* > sel_layer */
-  int keep;   /* rows of the current selection kept from this layer on       */
+  int layer;  /* > sel_layer (and > the previous step's layer), < n_layers */
+  int keep;   /* >= 0: selected rows kept per request from this layer on    */
 } cb_schedule_step;
 
 typedef struct {
@@ -397,10 +418,14 @@ typedef struct {
   int64_t cache_layer_stride;/* elements; 0 means T_total * row_elems       */
   float *deviation;          /* device [N_total] or NULL (d at layer s)     */
   int32_t *selected;         /* device [K_total] or NULL: request-local
-                                context positions, ascending per request    */
+                                context positions selected at the last
+                                layer, ascending per request; the first
+                                K_final entries are used (request b's k'_b
+                                after the requests before it)               */
   float *hidden;             /* device [R_total][d_model] or NULL: final
                                 hidden states (before the final norm) of the
-                                rows computed at the last layer             */
+                                rows computed at the last layer (R_final
+                                rows, packed per request)                   */
   int32_t *rows;             /* device [R_total] or NULL: request-local
                                 positions of those rows, ascending per
                                 request                                      */
@@ -411,9 +436,13 @@ typedef struct {
 typedef struct {
   int64_t T_total;           /* rows of the fused cache (all requests)      */
   int64_t N_total;           /* reusable context tokens                     */
-  int64_t K_total;           /* selected context tokens                     */
-  int64_t R_total;           /* rows computed at the last layer             */
+  int64_t K_total;           /* context tokens selected at sel_layer        */
+  int64_t R_total;           /* rows computed at sel_layer (K_total plus the
+                                uncached rows)                              */
   size_t workspace_bytes;    /* workspace for cb_blend_prefill / full      */
+  int64_t K_final;           /* selected tokens after the last gradual step
+                                (K_total without a schedule)                */
+  int64_t R_final;           /* rows computed at the last layer             */
 } cb_plan;
 
 /* Sizes of a blended prefill.  k_b = floor(N_b * ratio_bp / 10000), at

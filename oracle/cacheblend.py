@@ -36,14 +36,14 @@ Parity unpinned: none of the functions below -- every one has a pin in
 from __future__ import annotations
 
 import math
-from dataclasses import dataclass
+from dataclasses import dataclass, field
 
 import numpy as np
 
 __all__ = [
     "Model", "model_from_weights", "rope_inv_freq", "rope_rotate",
     "reposition_keys", "stitch", "rms_norm", "silu", "causal_attention",
-    "decoder_layer", "full_prefill", "chunk_prefill", "kv_deviation",
+    "qkv_rows", "decoder_layer", "full_prefill", "chunk_prefill", "kv_deviation",
     "select_count", "token_topk", "doc_aligned_select", "blend_prefill",
     "first_token", "first_token_logits", "embed_rows", "kv_bytes_per_layer",
     "BlendResult", "PrefillResult",
@@ -183,6 +183,24 @@ def causal_attention(q, q_pos, K, V, n_q_heads, n_kv_heads):
     return out
 
 
+def qkv_rows(m: Model, l: int, h_rows, pos_rows):
+    """The attention inputs of layer l for the rows ``h_rows`` [n, d] at
+    request positions ``pos_rows``: x = RMSNorm(h; norm1), then q, k, v =
+    x W_q^T, x W_k^T, x W_v^T with q and k rotated at their positions.
+    Returns q [n, Hq, hd] and the cache rows k, v [n, Hkv*hd]."""
+    L = m.layers[l]
+    n = h_rows.shape[0]
+    Hq, Hkv, hd = m.n_q_heads, m.n_kv_heads, m.head_dim
+    x = rms_norm(h_rows, L["norm1"], m.norm_eps)
+    qkv = x @ L["w_qkv"].T
+    q = qkv[:, :Hq * hd].reshape(n, Hq, hd)
+    k = qkv[:, Hq * hd:(Hq + Hkv) * hd].reshape(n, Hkv, hd)
+    v = qkv[:, (Hq + Hkv) * hd:].reshape(n, Hkv, hd)
+    q = rope_rotate(q, pos_rows, m.rope_base)
+    k = rope_rotate(k, pos_rows, m.rope_base)
+    return q, k.reshape(n, Hkv * hd), v.reshape(n, Hkv * hd)
+
+
 def decoder_layer(m: Model, l: int, h_rows, pos_rows, K_cache, V_cache,
                   cache_rows, write_kv=True):
     """One pre-norm decoder layer for the rows ``h_rows`` [n, d] at request
@@ -199,15 +217,7 @@ def decoder_layer(m: Model, l: int, h_rows, pos_rows, K_cache, V_cache,
     L = m.layers[l]
     n = h_rows.shape[0]
     Hq, Hkv, hd = m.n_q_heads, m.n_kv_heads, m.head_dim
-    x = rms_norm(h_rows, L["norm1"], m.norm_eps)
-    qkv = x @ L["w_qkv"].T
-    q = qkv[:, :Hq * hd].reshape(n, Hq, hd)
-    k = qkv[:, Hq * hd:(Hq + Hkv) * hd].reshape(n, Hkv, hd)
-    v = qkv[:, (Hq + Hkv) * hd:].reshape(n, Hkv, hd)
-    q = rope_rotate(q, pos_rows, m.rope_base)
-    k = rope_rotate(k, pos_rows, m.rope_base)
-    k_new = k.reshape(n, Hkv * hd)
-    v_new = v.reshape(n, Hkv * hd)
+    q, k_new, v_new = qkv_rows(m, l, h_rows, pos_rows)
     if write_kv:
         K_cache[cache_rows] = k_new
         V_cache[cache_rows] = v_new
@@ -349,6 +359,9 @@ class BlendResult:
     hidden: np.ndarray         # final hidden states of ``rows`` [R][d]
     token: int
     selected_per_layer: dict   # layer -> P used at that layer
+    deviation_per_layer: dict = field(default_factory=dict)
+    # layer of a gradual-filtering step -> {position: deviation} of the rows
+    # ranked there
 
 
 def blend_prefill(m: Model, segments, store, ratio_bp: int,
@@ -446,6 +459,7 @@ def blend_prefill(m: Model, segments, store, ratio_bp: int,
         else:
             raise ValueError(policy)
         sched = dict(schedule or [])
+        dev_steps = {}
         h_act = None
         active = None
         for l in range(sel_layer, m.n_layers):
@@ -458,6 +472,7 @@ def blend_prefill(m: Model, segments, store, ratio_bp: int,
                 kp = (xp @ Lw["w_qkv"][qd:qd + kvw].T).reshape(-1, Hkv, hd)
                 kp = rope_rotate(kp, rows_p, m.rope_base).reshape(-1, kvw)
                 dp = kv_deviation(kp, K[l][rows_p])
+                dev_steps[l] = dict(zip(P.tolist(), dp.tolist()))
                 keep = token_topk(dp, min(sched[l], len(P)))
                 P = P[keep]
             new_active = np.union1d(ctx_rows[P], always).astype(np.int64)
@@ -471,7 +486,7 @@ def blend_prefill(m: Model, segments, store, ratio_bp: int,
             h_act, _, _ = decoder_layer(m, l, h_act, active, K[l], V[l], active)
         h_final_rows = active
         tok = first_token(m, h_act[-1])
-        return BlendResult(K, V, P, d, h_final_rows, h_act, tok, per_layer)
+        return BlendResult(K, V, P, d, h_final_rows, h_act, tok, per_layer, dev_steps)
     tok = first_token(m, h[-1])
     return BlendResult(K, V, P, d, active, h, tok, per_layer)
 

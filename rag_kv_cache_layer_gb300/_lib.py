@@ -22,6 +22,7 @@ CB_F32, CB_BF16 = 0, 1
 CB_POLICY_TOKEN_TOPK, CB_POLICY_DOC_ALIGNED = 0, 1
 CB_EPI_STORE, CB_EPI_RESID, CB_EPI_SWIGLU = 0, 1, 2
 CB_GEMM_AUTO, CB_GEMM_TOKEN_M, CB_GEMM_SWAP_AB = 0, 1, 2
+CB_PROBE_QKV, CB_PROBE_O, CB_PROBE_SWIGLU, CB_PROBE_DOWN, CB_PROBE_ATTENTION = 1, 2, 3, 4, 5
 CB_MAX_BATCH = 64
 CB_MAX_SPANS = 1024
 
@@ -99,7 +100,8 @@ class BlendOut(C.Structure):
 
 class Plan(C.Structure):
     _fields_ = [("T_total", i64), ("N_total", i64), ("K_total", i64),
-                ("R_total", i64), ("workspace_bytes", C.c_size_t)]
+                ("R_total", i64), ("workspace_bytes", C.c_size_t),
+                ("K_final", i64), ("R_final", i64)]
 
 
 def _load():
@@ -116,6 +118,8 @@ def _load():
         "cb_debug_expire_wait": (S, [i32, vp]),
         "cb_debug_launch_count": (C.c_ulonglong, []),
         "cb_debug_gemm_path": (S, [i32]),
+        "cb_debug_probe_start": (S, [i32, i32]),
+        "cb_debug_probe_stop": (S, [C.POINTER(i32), C.POINTER(C.c_float)]),
         "cb_rope_table_elems": (C.c_size_t, [i32, i32]),
         "cb_rope_table_init": (S, [vp, i32, i32, C.c_float, vp]),
         "cb_rope_reposition": (S, [C.POINTER(StitchDesc), i32, i32, i32, vp, vp,
@@ -162,6 +166,7 @@ lib = _load()
 EXPORTED = [
     "cb_last_error_message", "cb_version", "cb_get_device_status",
     "cb_debug_expire_wait", "cb_debug_launch_count", "cb_debug_gemm_path",
+    "cb_debug_probe_start", "cb_debug_probe_stop",
     "cb_rope_table_elems",
     "cb_rope_table_init",
     "cb_rope_reposition", "cb_select_workspace_size", "cb_kv_deviation_topk",

@@ -67,6 +67,80 @@ extern "C" cb_status cb_debug_gemm_path(int path) {
   return CB_OK;
 }
 
+// ------------------------------------------------------------ launch probe --
+// Brackets the launches of one class of the layer's kernels with CUDA events
+// on their own stream, so a caller can time that kernel inside a real step.
+static std::mutex g_probe_mu;
+static std::atomic<int> g_probe_kind{0};
+static std::vector<cudaEvent_t> g_probe_ev;  // start, stop per launch
+static int g_probe_n = 0;
+static bool g_probe_open = false;
+
+static void probe_mark(int kind, bool begin, cudaStream_t s) {
+  if (g_probe_kind.load(std::memory_order_relaxed) != kind) return;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+    return;  // a captured record would only fire at replay
+  std::lock_guard<std::mutex> lk(g_probe_mu);
+  if (g_probe_kind.load() != kind) return;
+  if (begin) {
+    if (2 * (size_t)g_probe_n + 1 >= g_probe_ev.size()) return;
+    if (cudaEventRecord(g_probe_ev[2 * g_probe_n], s) == cudaSuccess) g_probe_open = true;
+  } else if (g_probe_open) {
+    g_probe_open = false;
+    if (cudaEventRecord(g_probe_ev[2 * g_probe_n + 1], s) == cudaSuccess) ++g_probe_n;
+  }
+}
+
+static void probe_release() {
+  for (cudaEvent_t e : g_probe_ev) cudaEventDestroy(e);
+  g_probe_ev.clear();
+  g_probe_n = 0;
+  g_probe_open = false;
+}
+
+extern "C" cb_status cb_debug_probe_start(int kind, int max_launches) {
+  if (kind < CB_PROBE_QKV || kind > CB_PROBE_ATTENTION || max_launches <= 0 ||
+      max_launches > 65536)
+    return fail(CB_ERR_INVALID_ARG, "bad probe kind or max_launches");
+  std::lock_guard<std::mutex> lk(g_probe_mu);
+  g_probe_kind.store(0);
+  probe_release();
+  g_probe_ev.resize(2 * (size_t)max_launches);
+  for (auto &e : g_probe_ev) {
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      e = nullptr;
+      probe_release();
+      return fail(CB_ERR_CUDA, "cudaEventCreate failed");
+    }
+  }
+  g_probe_kind.store(kind);
+  return CB_OK;
+}
+
+extern "C" cb_status cb_debug_probe_stop(int *n_launches, float *total_ms) {
+  if (!n_launches || !total_ms) return fail(CB_ERR_INVALID_ARG, "NULL output");
+  std::lock_guard<std::mutex> lk(g_probe_mu);
+  g_probe_kind.store(0);
+  *n_launches = 0;
+  *total_ms = 0.f;
+  cb_status rc = CB_OK;
+  float sum = 0.f;
+  for (int i = 0; i < g_probe_n && rc == CB_OK; ++i) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(g_probe_ev[2 * i + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, g_probe_ev[2 * i], g_probe_ev[2 * i + 1]) != cudaSuccess)
+      rc = fail(CB_ERR_CUDA, "probe event timing failed");
+    sum += ms;
+  }
+  if (rc == CB_OK) {
+    *n_launches = g_probe_n;
+    *total_ms = sum;
+  }
+  probe_release();
+  return rc;
+}
+
 // ----------------------------------------------------------- status word --
 static __device__ int g_status_word;
 
@@ -508,9 +582,18 @@ struct Plan {
   std::vector<std::vector<int>> seg_start;  // position of each segment
   int64_t T_total = 0, N_total = 0, K_total = 0, R_total = 0;
   int n_off[CB_MAX_BATCH + 1];
+  // gradual filtering: the rows of every request from `layer` on
+  struct Step {
+    int layer;
+    BatchMeta bm;
+    int64_t K_total, R_total;
+  };
+  std::vector<Step> sched;
+  int64_t K_final = 0, R_final = 0;
   // workspace
   LayerOffsets lay;
   size_t h_all, kf, dev, sel, pos_all, glob_all, pos_c, glob_c, h_c, lm_x, lm_best, total;
+  size_t g_dev = 0, g_keep = 0, g_sel = 0, g_pos = 0, g_glob = 0, g_src = 0, g_h = 0;
 };
 
 }  // namespace
@@ -573,7 +656,16 @@ static cb_status make_plan(const cb_model *m, const cb_request *reqs, int B,
       return fail(CB_ERR_INVALID_ARG, "sel_layer must be in [0, n_layers)");
     if (p->policy != CB_POLICY_TOKEN_TOPK && p->policy != CB_POLICY_DOC_ALIGNED)
       return fail(CB_ERR_INVALID_ARG, "unknown policy");
-    if (p->n_schedule != 0) return fail(CB_ERR_UNSUPPORTED, "gradual schedules are not supported yet");
+    if (p->n_schedule < 0 || p->n_schedule > m->cfg.n_layers)
+      return fail(CB_ERR_INVALID_ARG, "n_schedule must be in [0, n_layers]");
+    if (p->n_schedule > 0 && !p->schedule) return fail(CB_ERR_INVALID_ARG, "schedule is NULL");
+    for (int i = 0; i < p->n_schedule; ++i) {
+      const cb_schedule_step &st = p->schedule[i];
+      const int prev = i ? p->schedule[i - 1].layer : p->sel_layer;
+      if (st.layer <= prev || st.layer >= m->cfg.n_layers)
+        return fail(CB_ERR_INVALID_ARG, "schedule layers must ascend strictly, above sel_layer and below n_layers");
+      if (st.keep < 0) return fail(CB_ERR_INVALID_ARG, "schedule keep must be >= 0");
+    }
   }
   P.B = B;
   P.bm.B = B;
@@ -601,6 +693,27 @@ static cb_status make_plan(const cb_model *m, const cb_request *reqs, int B,
   P.N_total = P.n_off[B];
   P.K_total = P.bm.k_off[B];
   P.R_total = P.bm.r_off[B];
+  P.K_final = P.K_total;
+  P.R_final = P.R_total;
+  if (blend) {
+    // every request keeps min(keep, its current count) at each step
+    BatchMeta cur = P.bm;
+    for (int i = 0; i < p->n_schedule; ++i) {
+      Plan::Step st{p->schedule[i].layer, cur, 0, 0};
+      for (int b = 0; b < B; ++b) {
+        const int kc = cur.k_off[b + 1] - cur.k_off[b];
+        const int kn = p->schedule[i].keep < kc ? p->schedule[i].keep : kc;
+        st.bm.k_off[b + 1] = st.bm.k_off[b] + kn;
+        st.bm.r_off[b + 1] = st.bm.r_off[b] + kn + (P.T[b] - P.N[b]);
+      }
+      st.K_total = st.bm.k_off[B];
+      st.R_total = st.bm.r_off[B];
+      P.sched.push_back(st);
+      cur = st.bm;
+      P.K_final = st.K_total;
+      P.R_final = st.R_total;
+    }
+  }
   if (P.T_total >= (1ll << 31) / 2) return fail(CB_ERR_INVALID_ARG, "too many rows in one call");
   const cb_model_config &c = m->cfg;
   Carver cv;
@@ -616,6 +729,16 @@ static cb_status make_plan(const cb_model *m, const cb_request *reqs, int B,
   P.h_c = cv.take((P.R_total + 1) * c.d_model * sizeof(float));
   P.lm_x = cv.take((size_t)B * c.d_model * sizeof(float));
   P.lm_best = cv.take((size_t)B * sizeof(unsigned long long));
+  if (!P.sched.empty()) {
+    // second set of compact buffers; the filtered rows ping-pong between them
+    P.g_dev = cv.take((P.K_total + 1) * sizeof(float));
+    P.g_keep = cv.take((P.K_total + 1) * sizeof(int32_t));
+    P.g_sel = cv.take((P.K_total + 1) * sizeof(int32_t));
+    P.g_pos = cv.take((P.R_total + 1) * sizeof(int32_t));
+    P.g_glob = cv.take((P.R_total + 1) * sizeof(int32_t));
+    P.g_src = cv.take((P.R_total + 1) * sizeof(int32_t));
+    P.g_h = cv.take((P.R_total + 1) * c.d_model * sizeof(float));
+  }
   P.total = cv.off;
   return CB_OK;
 }
@@ -626,6 +749,8 @@ static void fill_plan(const Plan &P, cb_plan *out) {
   out->K_total = P.K_total;
   out->R_total = P.R_total;
   out->workspace_bytes = P.total;
+  out->K_final = P.K_final;
+  out->R_final = P.R_final;
 }
 
 extern "C" cb_status cb_blend_plan(const cb_model *m, const cb_request *reqs, int B,
@@ -661,6 +786,7 @@ static cb_status layer_forward(cb_model *m, int l, float *h, int n, const int32_
   const int d = c.d_model, F = c.d_ffn, hd = c.head_dim;
   const cb_dtype dt = c.dtype;
   CB_CUDA(launch_rmsnorm(h, d, nullptr, n, d, L.norm1, c.norm_eps, S.x, d, dt, s));
+  probe_mark(CB_PROBE_QKV, true, s);
   if (dt == CB_BF16 && hd == 128) {
     // projection, RoPE and the Eq. 7 scatter in one kernel
     const QkvEpi q{pos, cache_row, kc, vc, m->kvw, m->w.rope_table, c.n_q_heads, c.n_kv_heads};
@@ -673,12 +799,21 @@ static cb_status layer_forward(cb_model *m, int l, float *h, int n, const int32_
                               c.n_kv_heads, hd, m->w.rope_table, S.q, m->qw, kc, vc, m->kvw,
                               dt, 0, s));
   }
+  probe_mark(CB_PROBE_QKV, false, s);
+  probe_mark(CB_PROBE_ATTENTION, true, s);
   CB_TRY(run_attention(S.q, m->qw, pos, ar, kc, vc, m->kvw, c.n_q_heads, c.n_kv_heads, hd,
                        1.f / sqrtf((float)hd), S.o, m->qw, dt, S.attn, S.attn_bytes, st, s));
+  probe_mark(CB_PROBE_ATTENTION, false, s);
+  probe_mark(CB_PROBE_O, true, s);
   CB_TRY(run_linear(m, S.o, m->qw, L.w_o, nullptr, m->qw, n, d, m->qw, EPI_RESID, h, d, s));
+  probe_mark(CB_PROBE_O, false, s);
   CB_CUDA(launch_rmsnorm(h, d, nullptr, n, d, L.norm2, c.norm_eps, S.x, d, dt, s));
+  probe_mark(CB_PROBE_SWIGLU, true, s);
   CB_TRY(run_linear(m, S.x, d, L.w_gate, L.w_up, d, n, F, d, EPI_SWIGLU, S.g, F, s));
+  probe_mark(CB_PROBE_SWIGLU, false, s);
+  probe_mark(CB_PROBE_DOWN, true, s);
   CB_TRY(run_linear(m, S.g, F, L.w_down, nullptr, F, n, d, F, EPI_RESID, h, d, s));
+  probe_mark(CB_PROBE_DOWN, false, s);
   return CB_OK;
 }
 
@@ -736,16 +871,56 @@ static void full_attn_reqs(const Plan &P, std::vector<AttnReq> &ar) {
 
 // Final norm + tied LM head + arg-max of each request's last row of h:
 // row r_off[b+1]-1 of the compact rows, or t_off[b+1]-1 of all rows.
-static cb_status run_lm_head(cb_model *m, const Plan &P, const float *h, bool compact,
+// row_end: per request, one past its last row of h (B + 1 prefix sums)
+static cb_status run_lm_head(cb_model *m, const Plan &P, const float *h, const int *row_end,
                              char *ws, int32_t *first_token, cudaStream_t s) {
   const cb_model_config &c = m->cfg;
   int32_t last[CB_MAX_BATCH];
-  for (int b = 0; b < P.B; ++b)
-    last[b] = (compact ? P.bm.r_off[b + 1] : P.bm.t_off[b + 1]) - 1;
+  for (int b = 0; b < P.B; ++b) last[b] = row_end[b + 1] - 1;
   CB_CUDA(launch_lm_head_argmax(h, c.d_model, last, P.B, m->w.final_norm, c.norm_eps,
                                 m->w.embed, c.vocab, c.d_model, c.dtype,
                                 (float *)(ws + P.lm_x), (unsigned long long *)(ws + P.lm_best),
                                 first_token, s));
+  return CB_OK;
+}
+
+// One gradual-filtering step before layer l (CacheBlend blog, select_hkvd):
+// the current rows' fresh keys of layer l are compared with the reused keys
+// still in the layer's fused cache at the selected rows, each request keeps
+// its k'_b largest deviations among its selected rows, and the hidden
+// states of the kept rows (and of the uncached rows) are gathered.
+static cb_status filter_rows(cb_model *m, int l, const BatchMeta &cur, const BatchMeta &nxt,
+                             int R_nxt, const float *h, const int32_t *pos,
+                             const int32_t *glob, const int32_t *sel, float *h_n,
+                             int32_t *pos_n, int32_t *glob_n, int32_t *sel_n, int R_cur,
+                             char *ws, const Plan &P, const LayerScratch &S,
+                             const cb_blend_out *out, int64_t lstride, int *st,
+                             cudaStream_t s) {
+  const cb_model_config &c = m->cfg;
+  const cb_layer_weights &Lw = m->layers[l];
+  const int d = c.d_model, B = cur.B;
+  void *kf = ws + P.kf;
+  float *dp = (float *)(ws + P.g_dev);
+  int32_t *keep = (int32_t *)(ws + P.g_keep);
+  int32_t *src = (int32_t *)(ws + P.g_src);
+  CB_CUDA(launch_rmsnorm(h, d, nullptr, R_cur, d, Lw.norm1, c.norm_eps, S.x, d, c.dtype, s));
+  const char *wk = (const char *)Lw.w_qkv + (int64_t)m->qw * d * m->eb;
+  CB_TRY(run_linear(m, S.x, d, wk, nullptr, d, R_cur, m->kvw, d, EPI_STORE_F32, S.qkv32,
+                    m->kvw, s));
+  CB_CUDA(launch_qkv_finish(S.qkv32, m->kvw, R_cur, pos, nullptr, c.n_q_heads, c.n_kv_heads,
+                            c.head_dim, m->w.rope_table, nullptr, 0, kf, nullptr, m->kvw,
+                            c.dtype, 0, s));
+  std::vector<SelReq> sr(B);
+  for (int b = 0; b < B; ++b) {
+    const int kc = cur.k_off[b + 1] - cur.k_off[b];
+    sr[b] = SelReq{kc, nxt.k_off[b + 1] - nxt.k_off[b], (int64_t)cur.r_off[b], 0,
+                   cur.k_off[b], nxt.k_off[b], 0, 0};
+  }
+  CB_CUDA(launch_deviation(kf, m->kvw, layer_ptr(out->k_cache, l, lstride, m->eb), m->kvw,
+                           m->kvw, c.dtype, sr.data(), B, dp, s, glob));
+  CB_CUDA(launch_topk(dp, sr.data(), B, keep, s));
+  CB_CUDA(launch_filter_rows(cur, nxt, keep, sel, sel_n, pos_n, glob_n, src, R_nxt, st, s));
+  CB_CUDA(launch_gather(h, d, R_cur, src, R_nxt, d, h_n, d, sizeof(float), st, s));
   return CB_OK;
 }
 
@@ -843,15 +1018,44 @@ extern "C" cb_status cb_blend_prefill(cb_model *m, const cb_request *reqs, int B
   CB_CUDA(launch_build_rows(P.bm, sel, pos_c, glob_c, (int)P.R_total, st, s));
   CB_CUDA(launch_gather(h_all, d, P.T_total, glob_c, (int)P.R_total, d, h_c, d, sizeof(float),
                         st, s));
+  // 5. layers >= s on the computed rows; gradual filtering steps shrink the
+  // set between layers (the rows alternate between two buffer sets)
+  int32_t *sel_b[2] = {sel, (int32_t *)(ws + P.g_sel)};
+  int32_t *pos_b[2] = {pos_c, (int32_t *)(ws + P.g_pos)};
+  int32_t *glob_b[2] = {glob_c, (int32_t *)(ws + P.g_glob)};
+  float *h_b[2] = {h_c, (float *)(ws + P.g_h)};
+  int cur = 0;
+  BatchMeta bm = P.bm;
+  int R_cur = (int)P.R_total;
+  size_t next_step = 0;
   std::vector<AttnReq> ar_c(B);
-  for (int b = 0; b < B; ++b)
-    ar_c[b] = AttnReq{P.bm.r_off[b], P.bm.r_off[b + 1], (int64_t)P.bm.t_off[b], P.T[b]};
-  for (int l = s_layer; l < L; ++l)
-    CB_TRY(layer_forward(m, l, h_c, (int)P.R_total, pos_c, glob_c, ar_c,
+  for (int l = s_layer; l < L; ++l) {
+    if (next_step < P.sched.size() && P.sched[next_step].layer == l) {
+      const Plan::Step &stp = P.sched[next_step++];
+      CB_TRY(filter_rows(m, l, bm, stp.bm, (int)stp.R_total, h_b[cur], pos_b[cur], glob_b[cur],
+                         sel_b[cur], h_b[cur ^ 1], pos_b[cur ^ 1], glob_b[cur ^ 1],
+                         sel_b[cur ^ 1], R_cur, ws, P, S, out, lstride, st, s));
+      cur ^= 1;
+      bm = stp.bm;
+      R_cur = (int)stp.R_total;
+    }
+    for (int b = 0; b < B; ++b)
+      ar_c[b] = AttnReq{bm.r_off[b], bm.r_off[b + 1], (int64_t)P.bm.t_off[b], P.T[b]};
+    CB_TRY(layer_forward(m, l, h_b[cur], R_cur, pos_b[cur], glob_b[cur], ar_c,
                          layer_ptr(out->k_cache, l, lstride, m->eb),
                          layer_ptr(out->v_cache, l, lstride, m->eb), S, st, s));
-  // 5. first token from each request's last computed row (its last position)
-  if (out->first_token) CB_TRY(run_lm_head(m, P, h_c, true, ws, out->first_token, s));
+  }
+  if (cur == 1) {
+    // the final set is in the second buffers: move it to the outputs
+    CB_CUDA(cudaMemcpyAsync(sel_b[0], sel_b[1], P.K_final * sizeof(int32_t),
+                            cudaMemcpyDeviceToDevice, s));
+    CB_CUDA(cudaMemcpyAsync(pos_b[0], pos_b[1], P.R_final * sizeof(int32_t),
+                            cudaMemcpyDeviceToDevice, s));
+    CB_CUDA(cudaMemcpyAsync(h_b[0], h_b[1], P.R_final * d * sizeof(float),
+                            cudaMemcpyDeviceToDevice, s));
+  }
+  // 6. first token from each request's last computed row (its last position)
+  if (out->first_token) CB_TRY(run_lm_head(m, P, h_b[0], bm.r_off, ws, out->first_token, s));
   return CB_OK;
 }
 
@@ -881,6 +1085,6 @@ extern "C" cb_status cb_full_prefill(cb_model *m, const cb_request *reqs, int B,
     CB_TRY(layer_forward(m, l, h, (int)P.T_total, pos_all, glob_all, ar,
                          layer_ptr(out->k_cache, l, lstride, m->eb),
                          layer_ptr(out->v_cache, l, lstride, m->eb), S, st, stream));
-  if (out->first_token) CB_TRY(run_lm_head(m, P, h, false, ws, out->first_token, stream));
+  if (out->first_token) CB_TRY(run_lm_head(m, P, h, P.bm.t_off, ws, out->first_token, stream));
   return CB_OK;
 }

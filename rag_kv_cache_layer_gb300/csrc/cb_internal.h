@@ -57,7 +57,10 @@ size_t select_ws_bytes(int n_req);
 cudaError_t launch_deviation(const void *k_fresh, int64_t ld_fresh,
                              const void *k_reused, int64_t ld_reused,
                              int row_elems, cb_dtype dt, const SelReq *reqs,
-                             int n_req, float *dev_out, cudaStream_t s);
+                             int n_req, float *dev_out, cudaStream_t s,
+                             const int32_t *reused_rows = nullptr);
+// With reused_rows, the reused key of fresh row f is row
+// reused_row0 + reused_rows[f] instead of reused_row0 + i.
 cudaError_t launch_topk(const float *dev, const SelReq *reqs, int n_req,
                         int32_t *idx_out, cudaStream_t s);
 cudaError_t launch_doc_aligned(const float *dev, const SelReq *reqs, int n_req,
@@ -66,6 +69,13 @@ cudaError_t launch_doc_aligned(const float *dev, const SelReq *reqs, int n_req,
 cudaError_t launch_build_rows(const BatchMeta &bm, const int32_t *sel,
                               int32_t *pos, int32_t *glob, int n_rows,
                               int *status, cudaStream_t s);
+// One gradual-filtering step: from the current rows (cur) to the rows kept
+// (nxt, same requests, k'_b <= k_b); keep holds k'_b ascending local
+// indices per request at nxt.k_off[b].
+cudaError_t launch_filter_rows(const BatchMeta &cur, const BatchMeta &nxt,
+                               const int32_t *keep, const int32_t *sel_cur,
+                               int32_t *sel_nxt, int32_t *pos, int32_t *glob,
+                               int32_t *src, int n_rows, int *status, cudaStream_t s);
 cudaError_t launch_iota_rows(const BatchMeta &bm, int32_t *pos, int32_t *glob,
                              int n_rows, cudaStream_t s);
 

@@ -45,39 +45,46 @@ struct Params {
   int Hq, Hkv;
 };
 
+// Work decomposition.  Whole tiles: tile index with the token tile fastest,
+// so the CTAs running together share a weight tile.  Stream-K: the grid is
+// n_tt-CTA groups; group g owns a contiguous range of the n_ft x num_kb
+// (weight tile, k-block) units and each CTA of the group runs that range
+// for its own token tile, so the group reads every weight tile at the same
+// time and HBM serves it once (the other n_tt - 1 reads hit L2).
 struct Work {
-  int n_tt, num_kb;
+  int n_tt, num_kb, my_tt;
   bool sk;
   int64_t w, w_end;
   __device__ Work(const Params &p, int num_kb_) : n_tt(p.n_tt), num_kb(num_kb_), sk(p.stream_k != 0) {
-    const int64_t tiles = (int64_t)p.n_tt * p.n_ft;
     if (sk) {
-      const int64_t total = tiles * num_kb_;
-      w = total * blockIdx.x / gridDim.x;
-      w_end = total * (blockIdx.x + 1) / gridDim.x;
+      const int64_t total = (int64_t)p.n_ft * num_kb_;
+      const int groups = gridDim.x / p.n_tt;
+      const int g = blockIdx.x / p.n_tt;
+      my_tt = blockIdx.x % p.n_tt;
+      w = g < groups ? total * g / groups : 0;
+      w_end = g < groups ? total * (g + 1) / groups : 0;
     } else {
+      my_tt = 0;
       w = blockIdx.x;
-      w_end = tiles;
+      w_end = (int64_t)p.n_tt * p.n_ft;
     }
   }
-  // token tile fastest: CTAs running together share the weight tile
   __device__ bool next(int &tt, int &ft, int &kb0, int &kb1) {
     if (w >= w_end) return false;
-    int tile;
     if (sk) {
-      tile = (int)(w / num_kb);
+      ft = (int)(w / num_kb);
       kb0 = (int)(w % num_kb);
       const int64_t left = w_end - w;
       kb1 = (int)(kb0 + left < num_kb ? kb0 + left : num_kb);
       w += kb1 - kb0;
+      tt = my_tt;
     } else {
-      tile = (int)w;
+      tt = (int)(w % n_tt);
+      ft = (int)(w / n_tt);
       kb0 = 0;
       kb1 = num_kb;
       w += gridDim.x;
     }
-    tt = tile % n_tt;
-    ft = tile / n_tt;
     return true;
   }
 };
@@ -349,8 +356,17 @@ static cudaError_t run(const CUtensorMap &mx, const CUtensorMap &mw, const CUten
     attr = true;
   }
   const int64_t tiles = (int64_t)p.n_tt * p.n_ft;
-  const int64_t work = p.stream_k ? tiles * ((p.K + BK - 1) / BK) : tiles;
-  const int grid = work < num_sms() ? (int)work : num_sms();
+  int grid;
+  if (p.stream_k) {
+    // whole groups of n_tt CTAs, at most one group per weight unit
+    const int64_t units = (int64_t)p.n_ft * ((p.K + BK - 1) / BK);
+    int64_t groups = num_sms() / p.n_tt;
+    if (groups < 1) groups = 1;
+    if (groups > units) groups = units;
+    grid = (int)(groups * p.n_tt);
+  } else {
+    grid = tiles < num_sms() ? (int)tiles : num_sms();
+  }
   gemm_sab_kernel<EPI><<<grid, kThreads, smem, s>>>(mx, mw, mw2, p, status);
   return launched(1);
 }

@@ -29,7 +29,8 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 deviation_kernel(const __grid_constant__ SelParams p, const T *__restrict__ kf,
                  int64_t ld_f, const T *__restrict__ kr, int64_t ld_r,
-                 int row_elems, float *__restrict__ dev_out) {
+                 const int32_t *__restrict__ reused_rows, int row_elems,
+                 float *__restrict__ dev_out) {
   constexpr int VEC = 16 / sizeof(T);
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -40,7 +41,10 @@ deviation_kernel(const __grid_constant__ SelParams p, const T *__restrict__ kf,
   const SelReq &q = p.r[b];
   const int i = warp - p.row_prefix[b];
   const T *a = kf + (q.fresh_row0 + i) * ld_f;
-  const T *c = kr + (q.reused_row0 + i) * ld_r;
+
+  const int64_t fr = q.fresh_row0 + i;
+  const int64_t rr = reused_rows ? q.reused_row0 + reused_rows[fr] : q.reused_row0 + i;
+  const T *c = kr + rr * ld_r;
   float acc = 0.f;
   for (int col = lane * VEC; col < row_elems; col += 32 * VEC) {
     float x[VEC], y[VEC];
@@ -70,7 +74,8 @@ size_t select_ws_bytes(int n_req) { return 256 + (size_t)n_req * 0; }
 cudaError_t launch_deviation(const void *k_fresh, int64_t ld_fresh,
                              const void *k_reused, int64_t ld_reused,
                              int row_elems, cb_dtype dt, const SelReq *reqs,
-                             int n_req, float *dev_out, cudaStream_t s) {
+                             int n_req, float *dev_out, cudaStream_t s,
+                             const int32_t *reused_rows) {
   SelParams p;
   fill_params(p, reqs, n_req);
   const int rows = p.row_prefix[n_req];
@@ -79,11 +84,12 @@ cudaError_t launch_deviation(const void *k_fresh, int64_t ld_fresh,
   if (dt == CB_BF16)
     deviation_kernel<bf16><<<blocks, 256, 0, s>>>(
         p, reinterpret_cast<const bf16 *>(k_fresh), ld_fresh,
-        reinterpret_cast<const bf16 *>(k_reused), ld_reused, row_elems, dev_out);
+        reinterpret_cast<const bf16 *>(k_reused), ld_reused, reused_rows, row_elems, dev_out);
   else
     deviation_kernel<float><<<blocks, 256, 0, s>>>(
         p, reinterpret_cast<const float *>(k_fresh), ld_fresh,
-        reinterpret_cast<const float *>(k_reused), ld_reused, row_elems, dev_out);
+        reinterpret_cast<const float *>(k_reused), ld_reused, reused_rows, row_elems,
+        dev_out);
   return launched(1);
 }
 
@@ -398,6 +404,54 @@ cudaError_t launch_build_rows(const BatchMeta &bm, const int32_t *sel,
   if (n_rows == 0) return cudaSuccess;
   build_rows_kernel<<<(n_rows + 255) / 256, 256, 0, s>>>(bm, sel, pos, glob, n_rows,
                                                          status);
+  return launched(1);
+}
+
+// Rows of the next layer after a gradual-filtering step (CacheBlend blog,
+// select_hkvd): request b keeps keep[j], j < k'_b (ascending local indices
+// into its current selection) and all its uncached rows.  Writes the new
+// selection, the rows' positions and fused-cache rows, and the current row
+// each new row comes from (src) for the hidden-state gather.
+__global__ void filter_rows_kernel(const __grid_constant__ BatchMeta cur,
+                                   const __grid_constant__ BatchMeta nxt,
+                                   const int32_t *__restrict__ keep,
+                                   const int32_t *__restrict__ sel_cur,
+                                   int32_t *__restrict__ sel_nxt,
+                                   int32_t *__restrict__ pos, int32_t *__restrict__ glob,
+                                   int32_t *__restrict__ src, int n_rows, int *status) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= n_rows) return;
+  int b = 0;
+  while (nxt.r_off[b + 1] <= r) ++b;
+  const int j = r - nxt.r_off[b];
+  const int kn = nxt.k_off[b + 1] - nxt.k_off[b];
+  const int kc = cur.k_off[b + 1] - cur.k_off[b];
+  int p, from;
+  if (j < kn) {
+    int kk = keep[nxt.k_off[b] + j];
+    if (kk < 0 || kk >= kc) {
+      report(status, CB_ERR_DEVICE_INDEX);
+      kk = 0;
+    }
+    p = sel_cur[cur.k_off[b] + kk];
+    sel_nxt[nxt.k_off[b] + j] = p;
+    from = cur.r_off[b] + kk;
+  } else {
+    p = nxt.n_ctx[b] + (j - kn);
+    from = cur.r_off[b] + kc + (j - kn);
+  }
+  pos[r] = p;
+  glob[r] = nxt.t_off[b] + p;
+  src[r] = from;
+}
+
+cudaError_t launch_filter_rows(const BatchMeta &cur, const BatchMeta &nxt,
+                               const int32_t *keep, const int32_t *sel_cur,
+                               int32_t *sel_nxt, int32_t *pos, int32_t *glob,
+                               int32_t *src, int n_rows, int *status, cudaStream_t s) {
+  if (n_rows == 0) return cudaSuccess;
+  filter_rows_kernel<<<(n_rows + 255) / 256, 256, 0, s>>>(cur, nxt, keep, sel_cur, sel_nxt, pos,
+                                                          glob, src, n_rows, status);
   return launched(1);
 }
 

@@ -49,7 +49,8 @@ STRUCTS = {
                                         "schedule", "forced_selected"]),
     "cb_blend_out": (L.BlendOut, ["k_cache", "v_cache", "cache_layer_stride", "deviation",
                                   "selected", "hidden", "rows", "first_token"]),
-    "cb_plan": (L.Plan, ["T_total", "N_total", "K_total", "R_total", "workspace_bytes"]),
+    "cb_plan": (L.Plan, ["T_total", "N_total", "K_total", "R_total", "workspace_bytes",
+                         "K_final", "R_final"]),
 }
 
 
@@ -95,6 +96,9 @@ def test_host_validation_without_device():
     assert lib.cb_debug_expire_wait(-1, None) == L.CB_ERR_INVALID_ARG
     assert lib.cb_debug_gemm_path(3) == L.CB_ERR_INVALID_ARG
     assert lib.cb_debug_gemm_path(L.CB_GEMM_AUTO) == L.CB_OK
+    assert lib.cb_debug_probe_start(0, 4) == L.CB_ERR_INVALID_ARG
+    assert lib.cb_debug_probe_start(L.CB_PROBE_SWIGLU, 0) == L.CB_ERR_INVALID_ARG
+    assert lib.cb_debug_probe_stop(None, None) == L.CB_ERR_INVALID_ARG
     # bad doc-aligned spans are rejected on the host
     spans = (C.c_int32 * 3)(0, 5, 4)
     req = L.SelectReq(4, 2, 0, 0, 0, 0, 2, C.cast(spans, C.POINTER(C.c_int32)))

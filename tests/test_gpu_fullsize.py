@@ -1,0 +1,188 @@
+"""Parity at the benchmark's full size: the Llama-3-8B-shaped 32-layer bf16
+stack, one request of 6 x 512 cached tokens + 64 query tokens, 15% token
+top-k at layer 1, run exactly as bench.py times it (one cb_blend_prefill
+call captured in a CUDA graph and replayed).
+
+The oracle cannot run the whole request (about 9 TFLOP in float64), so it
+computes sampled outputs one by one from the weights and tokens alone:
+
+* the layer-0 K/V rows of sampled positions (layer 0 sees only each row's
+  own embedding, so every row is fresh there);
+* for sampled context rows: the layer-0 output over the request prefix, the
+  fresh layer-1 key, the chunk-alone (PIC) layer-1 key and value moved to
+  the request offset (QCFuse Eqs. 3-4), and their deviation d_i ("Request
+  Order Matters" §2.2 Eq. 1);
+* the fused layer-1 K/V of each sampled row: fresh if the GPU selected it,
+  the re-positioned PIC otherwise (QCFuse Eq. 7).
+
+Properties that hold at any size cover the rest: the selection is the
+exact top-k of the GPU's own deviations; every unselected row of every
+layer >= 1 equals, bit for bit, the same row of a r = 0 call (pure stitch);
+r = 100% equals full prefill through all 32 layers; the first token is the
+arg-max of the tied LM head on the GPU's final hidden state.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bench
+import oracle as O
+from rag_kv_cache_layer_gb300 import _lib as L
+import rag_kv_cache_layer_gb300 as R
+from gpu_common import rms_rel
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2          # bf16 path against the float64 oracle, RMS-relative
+
+
+def _f64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+@pytest.fixture(scope="module")
+def full():
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl, model, store, reqs, plan, outs, _, _ = bench.setup_replica(0, dev)
+    # the benchmark's launch configuration: the call captured once, replayed
+    model.cb_blend_prefill(reqs, bench.RATIO_BP, outputs=outs)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        model.cb_blend_prefill(reqs, bench.RATIO_BP, outputs=outs)
+    for key in ("k_cache", "v_cache", "hidden", "deviation"):
+        outs[key].zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    return wl, model, reqs, plan, outs
+
+
+@pytest.fixture(scope="module")
+def oracle_rows(full):
+    """The oracle's sampled rows, from the (seeded) weights and tokens."""
+    wl, model, reqs, plan, outs = full
+    s = wl.model
+    rq = wl.requests[0]
+    toks = rq.tokens
+    T, N = rq.n_tokens, rq.n_ctx
+    w = model.w
+    uniq, inv = np.unique(toks, return_inverse=True)
+    idx = torch.from_numpy(uniq.astype(np.int64)).cuda()
+    embed = w["embed"].index_select(0, idx).float().cpu().numpy()   # exact bf16 values
+
+    def layer(l, keys):
+        return {k: _f64(w["layers"][l][k]) for k in keys}
+    lw0 = layer(0, ("w_qkv", "w_o", "w_gate", "w_up", "w_down", "norm1", "norm2"))
+    lw1 = layer(1, ("w_qkv", "norm1"))
+    m = O.Model(2, s.d_model, s.n_q_heads, s.n_kv_heads, s.head_dim, s.d_ffn, len(uniq),
+                s.rope_base, s.norm_eps, embed, np.ones(s.d_model), [lw0, lw1])
+    Hkv, hd = s.n_kv_heads, s.head_dim
+
+    sel = outs["selected"][:plan.K_total].cpu().numpy()
+    ctx = sorted({0, 5, 511, 512, 777, 1535, 1536, 2047, 2600, 3071,
+                  *sel[:3].tolist(), *sel[-3:].tolist()})
+    query = [N, N + 31, T - 1]
+    pos = np.arange(T)
+    E = O.embed_rows(m, inv)
+    _, K0, V0 = O.qkv_rows(m, 0, E, pos)                     # layer 0, request positions
+    S = np.array(ctx)
+    h1 = O.decoder_layer(m, 0, E[S], S, K0.copy(), V0.copy(), S, write_kv=False)[0]
+    _, k1f, v1f = O.qkv_rows(m, 1, h1, S)                     # fresh layer-1 K/V
+    # the chunk alone at local positions, then moved to its request offset
+    offs = np.concatenate([[0], np.cumsum([len(sg.tokens) for sg in rq.segments if sg.cached])])
+    k1p, v1p = np.empty_like(k1f), np.empty_like(v1f)
+    chunk_of = np.searchsorted(offs, S, side="right") - 1
+    local = {}                                   # chunk -> its layer-0 K/V, local positions
+    for c in np.unique(chunk_of):
+        o, jmax = int(offs[c]), int(S[chunk_of == c].max() - offs[c])
+        local[c] = O.qkv_rows(m, 0, E[o:o + jmax + 1], np.arange(jmax + 1))[1:]
+    for n, i in enumerate(S):
+        c = int(chunk_of[n])
+        o, j = int(offs[c]), int(i - offs[c])
+        K0c, V0c = (a[:j + 1].copy() for a in local[c])
+        hc = O.decoder_layer(m, 0, E[[i]], [j], K0c, V0c, [j], write_kv=False)[0]
+        _, kc, vc = O.qkv_rows(m, 1, hc, [j])
+        k1p[n] = O.reposition_keys(kc, o, Hkv, hd, s.rope_base)[0]
+        v1p[n] = vc[0]
+    d = O.kv_deviation(k1f, k1p)
+    return dict(S=S, query=np.array(query), K0=K0, V0=V0, k1f=k1f, v1f=v1f,
+                k1p=k1p, v1p=v1p, d=d, sel=sel)
+
+
+def test_fullsize_layer0_rows(full, oracle_rows):
+    wl, model, reqs, plan, outs = full
+    rows = np.concatenate([oracle_rows["S"], oracle_rows["query"]])
+    k = _f64(outs["k_cache"][0][torch.from_numpy(rows).cuda()])
+    v = _f64(outs["v_cache"][0][torch.from_numpy(rows).cuda()])
+    assert rms_rel(k, oracle_rows["K0"][rows]) <= TOL
+    assert rms_rel(v, oracle_rows["V0"][rows]) <= TOL
+
+
+def test_fullsize_sampled_deviations(full, oracle_rows):
+    wl, model, reqs, plan, outs = full
+    S = oracle_rows["S"]
+    d_gpu = outs["deviation"][torch.from_numpy(S).cuda()].cpu().numpy().astype(np.float64)
+    print("sampled d: gpu", np.round(d_gpu, 2), "oracle", np.round(oracle_rows["d"], 2))
+    assert rms_rel(d_gpu, oracle_rows["d"]) <= TOL
+    assert np.all(d_gpu[S < 512] <= 1e-2 * d_gpu.max())     # first chunk: prefix unchanged
+
+
+def test_fullsize_selection_is_exact_top_k_of_own_deviation(full):
+    wl, model, reqs, plan, outs = full
+    N = wl.requests[0].n_ctx
+    k = int(plan.K_total)
+    assert k == O.select_count(N, bench.RATIO_BP) == 460
+    d = outs["deviation"][:N].cpu().numpy().astype(np.float64)
+    assert list(outs["selected"][:k].cpu().numpy()) == list(O.token_topk(d, k))
+
+
+def test_fullsize_fused_layer1_rows(full, oracle_rows):
+    """Eq. 7 at the selection layer: fresh K/V for selected rows, the
+    re-positioned chunk cache for the others."""
+    wl, model, reqs, plan, outs = full
+    S = oracle_rows["S"]
+    chosen = np.isin(S, oracle_rows["sel"])
+    assert chosen.any() and (~chosen).any()
+    k_ref = np.where(chosen[:, None], oracle_rows["k1f"], oracle_rows["k1p"])
+    v_ref = np.where(chosen[:, None], oracle_rows["v1f"], oracle_rows["v1p"])
+    ix = torch.from_numpy(S).cuda()
+    assert rms_rel(_f64(outs["k_cache"][1][ix]), k_ref) <= TOL
+    assert rms_rel(_f64(outs["v_cache"][1][ix]), v_ref) <= TOL
+
+
+def test_fullsize_unselected_rows_are_the_stitched_cache(full):
+    wl, model, reqs, plan, outs = full
+    N = wl.requests[0].n_ctx
+    stitched = model.cb_blend_prefill(reqs, 0)
+    torch.cuda.synchronize()
+    keep = torch.ones(N, dtype=torch.bool, device="cuda")
+    keep[outs["selected"][:plan.K_total].long()] = False
+    for l in range(1, wl.model.n_layers):
+        assert torch.equal(outs["k_cache"][l][:N][keep], stitched["k_cache"][l][:N][keep])
+        assert torch.equal(outs["v_cache"][l][:N][keep], stitched["v_cache"][l][:N][keep])
+
+
+def test_fullsize_all_rows_selected_equals_full_prefill(full):
+    wl, model, reqs, plan, outs = full
+    T = wl.requests[0].n_tokens
+    b = model.cb_blend_prefill(reqs, 10000)
+    f = model.cb_full_prefill(reqs)
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    for l in (0, 1, 16, wl.model.n_layers - 1):
+        assert rms_rel(_f64(b["k_cache"][l]), _f64(f["k_cache"][l])) <= TOL
+        assert rms_rel(_f64(b["v_cache"][l]), _f64(f["v_cache"][l])) <= TOL
+    assert rms_rel(_f64(b["hidden"][:T]), _f64(f["hidden"][:T])) <= TOL
+
+
+def test_fullsize_first_token_is_argmax_of_tied_head(full):
+    wl, model, reqs, plan, outs = full
+    s = wl.model
+    h = outs["hidden"][int(plan.R_total) - 1].double()
+    x = (h / torch.sqrt((h * h).mean() + s.norm_eps)).float()
+    E = model.w["embed"]
+    logits = torch.cat([E[i:i + 16384].float() @ x for i in range(0, s.vocab, 16384)])
+    tok = int(outs["first_token"][0])
+    top = float(logits.max())
+    assert float(logits[tok]) >= top - 1e-3 * abs(top)

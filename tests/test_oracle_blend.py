@@ -163,6 +163,47 @@ def test_gradual_filtering_only_shrinks():
     assert p3 <= p2 <= p1
 
 
+def test_gradual_keep_at_least_current_count_changes_nothing():
+    m = _model(n_layers=4)
+    chunks, query, segs, store = _request(m)
+    a = O.blend_prefill(m, segs, store, ratio_bp=2000)
+    b = O.blend_prefill(m, segs, store, ratio_bp=2000, schedule=[(2, 10 ** 6), (3, 10 ** 6)])
+    assert np.array_equal(a.K, b.K) and np.array_equal(a.hidden, b.hidden)
+    assert np.array_equal(a.selected, b.selected)
+
+
+def test_gradual_step_reranks_the_current_set_by_its_fresh_keys():
+    """CacheBlend blog, "The Chicken-and-Egg Problem" (select_hkvd): at a
+    filtering layer the rows still selected are ranked again by how far
+    their fresh keys of that layer deviate from the reused keys, and the
+    largest deviations are kept.  The hidden states entering that layer are
+    taken from the same blend truncated just below it."""
+    m = _model(n_layers=4)
+    chunks, query, segs, store = _request(m)
+    Hkv, hd = m.n_kv_heads, m.head_dim
+    r = O.blend_prefill(m, segs, store, ratio_bp=2000, schedule=[(2, 3)])
+    cut = O.Model(2, m.d_model, m.n_q_heads, Hkv, hd, m.d_ffn, m.vocab, m.rope_base,
+                  m.norm_eps, m.embed, m.final_norm, m.layers[:2])
+    u = O.blend_prefill(cut, segs, [(k[:2], v[:2]) for k, v in store], ratio_bp=2000)
+    P = u.selected
+    assert np.array_equal(P, r.selected_per_layer[1])
+    # fresh layer-2 keys of the selected rows, rotated at their positions
+    lw = m.layers[2]
+    h = u.hidden[np.searchsorted(u.rows, P)]
+    x = h / np.sqrt(np.mean(h * h, axis=1, keepdims=True) + m.norm_eps) * lw["norm1"]
+    qd = m.n_q_heads * hd
+    kf = O.rope_rotate((x @ lw["w_qkv"][qd:qd + Hkv * hd].T).reshape(-1, Hkv, hd), P,
+                       m.rope_base).reshape(len(P), -1)
+    # reused layer-2 keys: every chunk's stored keys moved to its offset
+    offs = np.concatenate([[0], np.cumsum([len(c) for c in chunks])])
+    kr = np.concatenate([O.reposition_keys(k[2], int(o), Hkv, hd, m.rope_base)
+                         for (k, _), o in zip(store, offs[:-1])])[P]
+    d = ((kf - kr) ** 2).sum(axis=1)
+    order = sorted(range(len(P)), key=lambda i: (-d[i], i))[:3]
+    assert list(r.selected_per_layer[2]) == sorted(P[order].tolist())
+    assert list(r.selected) == sorted(P[order].tolist())
+
+
 def test_selection_past_last_layer_is_full_prefill():
     m = _model()
     chunks, query, segs, store = _request(m)

@@ -160,6 +160,31 @@ def make_weights(model: ModelShape, seed: int, std: float = 0.02,
     return w
 
 
+def make_weights_device(model: ModelShape, seed: int, device, std: float = 0.02,
+                        embed_std: float = 1.0) -> dict:
+    """Random-init bf16 weights generated on a CUDA device with torch's seeded
+    generator (for stacks too large to draw on the host): projections
+    N(0, std), embeddings N(0, embed_std), RMSNorm gains 1.  Same layout as
+    make_weights, as device tensors."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+
+    def rnd(*shape, s=std):
+        return (torch.randn(*shape, generator=g, device=device, dtype=torch.float32)
+                * s).to(torch.bfloat16)
+    d, F = model.d_model, model.d_ffn
+    qd = model.n_q_heads * model.head_dim
+    w = {"embed": rnd(model.vocab, d, s=embed_std),
+         "final_norm": torch.ones(d, device=device), "layers": []}
+    for _ in range(model.n_layers):
+        w["layers"].append({
+            "w_qkv": rnd(model.qkv_rows, d), "w_o": rnd(d, qd),
+            "w_gate": rnd(F, d), "w_up": rnd(F, d), "w_down": rnd(d, F),
+            "norm1": torch.ones(d, device=device), "norm2": torch.ones(d, device=device)})
+    return w
+
+
 def make_tokens(rng, n, vocab) -> np.ndarray:
     return rng.integers(0, vocab, size=n, dtype=np.int64).astype(np.int32)
 
@@ -178,10 +203,12 @@ def make_kv_store(model: ModelShape, n_rows: int, seed: int, std: float = 1.0):
 # the five workloads
 # --------------------------------------------------------------------------
 def tiny_blend(seed: int = 0, n_chunks: int = 3, chunk_len: int = 128,
-               n_query: int = 32, ratio_bp: int = 1500) -> Workload:
-    """2-layer fp32 model; 3 chunks x 128 tokens + 32 query tokens; 15%."""
+               n_query: int = 32, ratio_bp: int = 1500,
+               n_layers: int | None = None) -> Workload:
+    """2-layer fp32 model (deeper with n_layers); 3 chunks x 128 tokens + 32
+    query tokens; 15%."""
     rng = np.random.default_rng(seed + 1000)
-    m = TINY_F32
+    m = TINY_F32 if n_layers is None else TINY_F32.truncated(n_layers)
     chunks = [make_tokens(rng, chunk_len, m.vocab) for _ in range(n_chunks)]
     segs = [Segment(c, i) for i, c in enumerate(chunks)]
     segs.append(Segment(make_tokens(rng, n_query, m.vocab)))
