@@ -111,12 +111,15 @@ unsigned long long cb_debug_launch_count(void);
  * after the call (process-wide):
  *   CB_GEMM_AUTO (0)     per epilogue and row count, the faster of the two;
  *   CB_GEMM_TOKEN_M (1)  token rows on the MMA's M side (128-row tiles);
- *   CB_GEMM_SWAP_AB (2)  weight rows on M, tokens on N (few-row form).
- * Both compute the same function; tests use the switch to check each one
+ *   CB_GEMM_SWAP_AB (2)  weight rows on M, tokens on N (few-row form);
+ *   CB_GEMM_SWAP_AB_PAIR (3)  the same with each MMA spanning a pair of SMs
+ *                        (2-CTA cluster, 256 weight rows per tile).
+ * All compute the same function; tests use the switch to check each one
  * on every epilogue.  Returns CB_ERR_INVALID_ARG for any other value. */
 #define CB_GEMM_AUTO 0
 #define CB_GEMM_TOKEN_M 1
 #define CB_GEMM_SWAP_AB 2
+#define CB_GEMM_SWAP_AB_PAIR 3
 cb_status cb_debug_gemm_path(int path);
 
 /* Launch probe: times the launches of one kernel class of the decoder layer

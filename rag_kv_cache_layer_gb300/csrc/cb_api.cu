@@ -61,8 +61,8 @@ extern "C" unsigned long long cb_debug_launch_count(void) { return g_launches.lo
 
 static std::atomic<int> g_gemm_path{CB_GEMM_AUTO};
 extern "C" cb_status cb_debug_gemm_path(int path) {
-  if (path != CB_GEMM_AUTO && path != CB_GEMM_TOKEN_M && path != CB_GEMM_SWAP_AB)
-    return fail(CB_ERR_INVALID_ARG, "path must be CB_GEMM_AUTO, _TOKEN_M or _SWAP_AB");
+  if (path < CB_GEMM_AUTO || path > CB_GEMM_SWAP_AB_PAIR)
+    return fail(CB_ERR_INVALID_ARG, "path must be CB_GEMM_AUTO, _TOKEN_M, _SWAP_AB or _SWAP_AB_PAIR");
   g_gemm_path.store(path);
   return CB_OK;
 }
@@ -490,10 +490,11 @@ static cb_status run_linear(const cb_model *m, const void *A, int64_t lda, const
     int *st;
     CB_TRY(status_ptr(&st));
     const int path = g_gemm_path.load(std::memory_order_relaxed);
-    const bool sab = path == CB_GEMM_SWAP_AB ||
+    const bool sab = path == CB_GEMM_SWAP_AB || path == CB_GEMM_SWAP_AB_PAIR ||
                      (path == CB_GEMM_AUTO && gemm_sab_preferred(M, epi));
     if (sab)
-      CB_CUDA(launch_gemm_sab(A, lda, W, W2, ldw, M, N, K, epi, out, ldo, qkv, st, s));
+      CB_CUDA(launch_gemm_sab(A, lda, W, W2, ldw, M, N, K, epi, out, ldo, qkv, st, s,
+                              path == CB_GEMM_SWAP_AB_PAIR ? 2 : 1));
     else
       CB_CUDA(launch_gemm_tc(A, lda, W, W2, ldw, M, N, K, epi, out, ldo, qkv, st, s));
   } else {

@@ -151,10 +151,13 @@ cudaError_t launch_gemm_tc(const void *A, int64_t lda, const void *W,
 // The same GEMM with the operands swapped (weights on the MMA's M side,
 // tokens on N), for few rows; gemm_sab_preferred says when to use it.
 bool gemm_sab_preferred(int M, GemmEpi epi);
+// cta_group 2 runs each MMA on a pair of SMs (a 2-CTA cluster): 256 weight
+// rows per tile, the token operand split between the two CTAs.
 cudaError_t launch_gemm_sab(const void *A, int64_t lda, const void *W,
                             const void *W2, int64_t ldw, int M, int N, int K,
                             GemmEpi epi, void *out, int64_t ldo,
-                            const QkvEpi *qkv, int *status, cudaStream_t s);
+                            const QkvEpi *qkv, int *status, cudaStream_t s,
+                            int cta_group = 1);
 
 // ------------------------------------------------------------ attention --
 struct AttnReq {

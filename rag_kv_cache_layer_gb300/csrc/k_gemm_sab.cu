@@ -51,22 +51,28 @@ struct Params {
 // (weight tile, k-block) units and each CTA of the group runs that range
 // for its own token tile, so the group reads every weight tile at the same
 // time and HBM serves it once (the other n_tt - 1 reads hit L2).
+// A "unit" is one CTA, or one CTA pair when the MMA spans two SMs (CG = 2);
+// both CTAs of a pair walk the same sequence, ft then counting pair tiles.
+template <int CG>
 struct Work {
   int n_tt, num_kb, my_tt;
   bool sk;
-  int64_t w, w_end;
+  int64_t w, w_end, step;
   __device__ Work(const Params &p, int num_kb_) : n_tt(p.n_tt), num_kb(num_kb_), sk(p.stream_k != 0) {
+    const int unit = blockIdx.x / CG, n_units = gridDim.x / CG;
+    const int n_ft = (p.n_ft + CG - 1) / CG;
+    step = n_units;
     if (sk) {
-      const int64_t total = (int64_t)p.n_ft * num_kb_;
-      const int groups = gridDim.x / p.n_tt;
-      const int g = blockIdx.x / p.n_tt;
-      my_tt = blockIdx.x % p.n_tt;
+      const int64_t total = (int64_t)n_ft * num_kb_;
+      const int groups = n_units / p.n_tt;
+      const int g = unit / p.n_tt;
+      my_tt = unit % p.n_tt;
       w = g < groups ? total * g / groups : 0;
       w_end = g < groups ? total * (g + 1) / groups : 0;
     } else {
       my_tt = 0;
-      w = blockIdx.x;
-      w_end = (int64_t)p.n_tt * p.n_ft;
+      w = unit;
+      w_end = (int64_t)p.n_tt * n_ft;
     }
   }
   __device__ bool next(int &tt, int &ft, int &kb0, int &kb1) {
@@ -83,7 +89,7 @@ struct Work {
       ft = (int)(w / n_tt);
       kb0 = 0;
       kb1 = num_kb;
-      w += gridDim.x;
+      w += step;
     }
     return true;
   }
@@ -99,7 +105,7 @@ __device__ __forceinline__ void store_bf16x8(bf16 *dst, const float *v) {
   *reinterpret_cast<uint4 *>(dst) = pk;
 }
 
-template <int EPI>
+template <int EPI, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW,
                 const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ Params p,
@@ -117,6 +123,9 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_kb = (p.K + BK - 1) / BK;
+  // CG = 2: this CTA's rank in its pair; the leader (rank 0) issues the MMAs
+  const uint32_t rank = CG == 2 ? cluster_rank() : 0u;
+  const bool leader = rank == 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
@@ -124,14 +133,19 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
-      mbar_init(smem_u32(&tempty[b]), 128);
+      // CG = 2: lane 0 of each epilogue warp of both CTAs
+      mbar_init(smem_u32(&tempty[b]), CG == 2 ? 8 : 128);
     }
     *fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+  if (warp == 1) {
+    if (CG == 2) tmem_alloc_pair(smem_u32(tmem_slot), 512);
+    else tmem_alloc(smem_u32(tmem_slot), 512);
+  }
   fence_before();
   __syncthreads();
+  if (CG == 2) cluster_sync();   // the peer's barriers exist before any remote use
   fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -142,47 +156,70 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
       uint32_t phase = 0;
       int issued[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       bool ok = true;
-      Work wk(p, num_kb);
+      Work<CG> wk(p, num_kb);
       int tt, ft, kb0, kb1;
+      const int bt = p.BT / CG;           // token rows of B held by this CTA
       while (ok && wk.next(tt, ft, kb0, kb1)) {
+        const int fct = ft * CG + (int)rank;   // this CTA's 128-row weight tile
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, kWaitLimitNs, status) ||
               *fail) {
             ok = false;
             break;
           }
-          const uint32_t fb = smem_u32(&full[stage]);
-          expect_tx(fb, p.stage_bytes);
+          // the pair's operands all complete on the leader's barrier
+          uint32_t fb = smem_u32(&full[stage]);
+          if (leader) expect_tx(fb, CG * p.stage_bytes);
+          if (CG == 2) fb = map_to_rank(fb, 0);
           uint8_t *sw = smem + stage * p.stage_bytes;
           uint8_t *sx = sw + kTileW;
-          if (EPI == EPI_SWIGLU) {
-            tma_load_2d(smem_u32(sw), &mapW, fb, kb * BK, ft * 64);
-            tma_load_2d(smem_u32(sw + 64 * 128), &mapW2, fb, kb * BK, ft * 64);
+          const int ty = tt * p.BT + (int)rank * bt;
+          if (CG == 2) {
+            if (EPI == EPI_SWIGLU) {
+              tma_load_2d_pair(smem_u32(sw), &mapW, fb, kb * BK, fct * 64);
+              tma_load_2d_pair(smem_u32(sw + 64 * 128), &mapW2, fb, kb * BK, fct * 64);
+            } else {
+              tma_load_2d_pair(smem_u32(sw), &mapW, fb, kb * BK, fct * FM);
+            }
+            tma_load_2d_pair(smem_u32(sx), &mapX, fb, kb * BK, ty);
           } else {
-            tma_load_2d(smem_u32(sw), &mapW, fb, kb * BK, ft * FM);
+            if (EPI == EPI_SWIGLU) {
+              tma_load_2d(smem_u32(sw), &mapW, fb, kb * BK, fct * 64);
+              tma_load_2d(smem_u32(sw + 64 * 128), &mapW2, fb, kb * BK, fct * 64);
+            } else {
+              tma_load_2d(smem_u32(sw), &mapW, fb, kb * BK, fct * FM);
+            }
+            tma_load_2d(smem_u32(sx), &mapX, fb, kb * BK, ty);
           }
-          tma_load_2d(smem_u32(sx), &mapX, fb, kb * BK, tt * p.BT);
           ++issued[stage];
           if (++stage == p.stages) { stage = 0; phase ^= 1; }
         }
       }
       if (!ok) {
         *fail = 1;
-        for (int s = 0; s < p.stages; ++s)
-          if (issued[s] > 0)
-            mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((issued[s] - 1) & 1), 10000000ull,
-                              nullptr);
+        if (CG == 1 || leader) {
+          for (int s = 0; s < p.stages; ++s)
+            if (issued[s] > 0)
+              mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((issued[s] - 1) & 1), 10000000ull,
+                                nullptr);
+        } else {
+          // this CTA's copies complete on the leader's barriers: give them
+          // time to land before the pair can retire
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 10000000ull) {
+          }
+        }
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int buf = 0;
       uint32_t bphase = 0;
       bool ok = true;
-      Work wk(p, num_kb);
+      Work<CG> wk(p, num_kb);
       int tt, ft, kb0, kb1;
       while (ok && wk.next(tt, ft, kb0, kb1)) {
         if (!mbar_wait_bounded(smem_u32(&tempty[buf]), bphase ^ 1, kWaitLimitNs, status) ||
@@ -201,13 +238,19 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
           const uint32_t sw = smem_u32(smem + stage * p.stage_bytes);
           const uint64_t dw = desc_kmajor(sw), dx = desc_kmajor(sw + kTileW);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            mma(d, dw + 2 * k, dx + 2 * k, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-          commit(smem_u32(&empty[stage]));
+          for (int k = 0; k < BK / 16; ++k) {
+            if (CG == 2)
+              mma_pair(d, dw + 2 * k, dx + 2 * k, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            else
+              mma(d, dw + 2 * k, dx + 2 * k, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          }
+          if (CG == 2) commit_pair(smem_u32(&empty[stage]), 3);
+          else commit(smem_u32(&empty[stage]));
           if (++stage == p.stages) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        commit(smem_u32(&tfull[buf]));
+        if (CG == 2) commit_pair(smem_u32(&tfull[buf]), 3);
+        else commit(smem_u32(&tfull[buf]));
         if (++buf == 2) { buf = 0; bphase ^= 1; }
       }
       if (!ok) *fail = 1;
@@ -218,7 +261,7 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
     const int r = quad * 32 + lane;                 // feature row of the tile
     int buf = 0;
     uint32_t bphase = 0;
-    Work wk(p, num_kb);
+    Work<CG> wk(p, num_kb);
     int tt, ft, kb0, kb1;
     while (wk.next(tt, ft, kb0, kb1)) {
       const bool whole = kb0 == 0 && kb1 == num_kb;
@@ -229,6 +272,7 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
         break;
       }
       fence_after();
+      ft = ft * CG + (int)rank;                      // this CTA's 128 weight rows
       const uint32_t tbase = tmem + buf * 256 + ((uint32_t)(quad * 32) << 16);
       const int tok0 = tt * p.BT;
       int head = 0;
@@ -327,48 +371,110 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
         epi_bar();
       }
       fence_before();
-      arrive(smem_u32(&tempty[buf]));
+      if (CG == 2) {
+        __syncwarp();
+        if (lane == 0) arrive_remote(map_to_rank(smem_u32(&tempty[buf]), 0));
+      } else {
+        arrive(smem_u32(&tempty[buf]));
+      }
       if (++buf == 2) { buf = 0; bphase ^= 1; }
     }
   }
   fence_before();
   __syncthreads();
+  if (CG == 2) cluster_sync();   // neither CTA retires while the pair may touch it
   if (warp == 1) {
     fence_after();
-    tmem_dealloc(tmem, 512);
+    if (CG == 2) tmem_dealloc_pair(tmem, 512);
+    else tmem_dealloc(tmem, 512);
   }
 }
 
+// Largest number of CTA pairs of this kernel that fit on the device at once
+// (a pair needs two SMs of one GPC).
 template <int EPI>
+static int max_pairs(int smem) {
+  static int cached = 0;
+  if (cached) return cached;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * num_sms(), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_sab_kernel<EPI, 2>, &cfg) != cudaSuccess || n <= 0)
+    n = num_sms() / 2;
+  cached = n;
+  return n;
+}
+
+template <int EPI, int CG>
 static cudaError_t run(const CUtensorMap &mx, const CUtensorMap &mw, const CUtensorMap &mw2,
                        Params &p, int *status, cudaStream_t s) {
   const int fixed = kTr + 256 + 1024;
-  p.stage_bytes = kTileW + p.BT * BK * 2;
+  p.stage_bytes = kTileW + (p.BT / CG) * BK * 2;
   p.stages = (kSmemMax - fixed) / p.stage_bytes;
   if (p.stages > 8) p.stages = 8;
   if (p.stages < 2) return cudaErrorInvalidValue;
   const int smem = p.stages * p.stage_bytes + fixed;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_sab_kernel<EPI>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_sab_kernel<EPI, CG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (e != cudaSuccess) return e;
+    if (CG == 2) {
+      e = cudaFuncSetAttribute(gemm_sab_kernel<EPI, CG>,
+                               cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+      if (e != cudaSuccess) return e;
+    }
     attr = true;
   }
-  const int64_t tiles = (int64_t)p.n_tt * p.n_ft;
-  int grid;
+  // units: CTAs, or CTA pairs
+  const int max_units = CG == 2 ? max_pairs<EPI>(kSmemMax) : num_sms();
+  const int n_ft = (p.n_ft + CG - 1) / CG;
+  const int64_t tiles = (int64_t)p.n_tt * n_ft;
+  int units;
   if (p.stream_k) {
-    // whole groups of n_tt CTAs, at most one group per weight unit
-    const int64_t units = (int64_t)p.n_ft * ((p.K + BK - 1) / BK);
-    int64_t groups = num_sms() / p.n_tt;
+    // whole groups of n_tt units, at most one group per weight unit
+    const int64_t wunits = (int64_t)n_ft * ((p.K + BK - 1) / BK);
+    int64_t groups = max_units / p.n_tt;
     if (groups < 1) groups = 1;
-    if (groups > units) groups = units;
-    grid = (int)(groups * p.n_tt);
+    if (groups > wunits) groups = wunits;
+    units = (int)(groups * p.n_tt);
   } else {
-    grid = tiles < num_sms() ? (int)tiles : num_sms();
+    units = tiles < max_units ? (int)tiles : max_units;
   }
-  gemm_sab_kernel<EPI><<<grid, kThreads, smem, s>>>(mx, mw, mw2, p, status);
+  if (CG == 1) {
+    gemm_sab_kernel<EPI, 1><<<units, kThreads, smem, s>>>(mx, mw, mw2, p, status);
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * units, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_sab_kernel<EPI, 2>, mx, mw, mw2, p, status);
+    if (e != cudaSuccess) return e;
+  }
   return launched(1);
+}
+
+template <int EPI>
+static cudaError_t run_cg(const CUtensorMap &mx, const CUtensorMap &mw, const CUtensorMap &mw2,
+                          Params &p, int cg, int *status, cudaStream_t s) {
+  return cg == 2 ? run<EPI, 2>(mx, mw, mw2, p, status, s) : run<EPI, 1>(mx, mw, mw2, p, status, s);
 }
 
 }  // namespace sab
@@ -382,26 +488,32 @@ bool gemm_sab_preferred(int M, GemmEpi epi) {
 
 cudaError_t launch_gemm_sab(const void *A, int64_t lda, const void *W, const void *W2,
                             int64_t ldw, int M, int N, int K, GemmEpi epi, void *out,
-                            int64_t ldo, const QkvEpi *qkv, int *status, cudaStream_t s) {
+                            int64_t ldo, const QkvEpi *qkv, int *status, cudaStream_t s,
+                            int cta_group) {
   using namespace sab;
   if (M == 0 || N == 0) return cudaSuccess;
+  if (cta_group != 1 && cta_group != 2) return cudaErrorInvalidValue;
   Params p{};
   p.M = M;
   p.N = N;
   p.K = K;
   p.n_tt = (M + 255) / 256;
   p.BT = ((M + p.n_tt - 1) / p.n_tt + 15) / 16 * 16;
-  p.idesc = idesc_bf16(FM, p.BT);
+  if (epi == EPI_QKV && (N / 128) % 2) cta_group = 1;   // pairs take two heads
+  if (p.BT < 32) cta_group = 1;                           // keep each CTA's half >= 16 rows
+  const int cg = cta_group;
+  p.idesc = idesc_bf16(FM * cg, p.BT);
   p.out = out;
   p.ldo = ldo;
   CUtensorMap mx, mw, mw2;
-  if (!make_map(&mx, A, M, K, lda, p.BT)) return cudaErrorInvalidValue;
+  // each CTA of a pair holds half of the token rows of B
+  if (!make_map(&mx, A, M, K, lda, p.BT / cg)) return cudaErrorInvalidValue;
   switch (epi) {
     case EPI_SWIGLU:
       p.n_ft = (N + 63) / 64;
       if (!make_map(&mw, W, N, K, ldw, 64) || !make_map(&mw2, W2, N, K, ldw, 64))
         return cudaErrorInvalidValue;
-      return run<EPI_SWIGLU>(mx, mw, mw2, p, status, s);
+      return run_cg<EPI_SWIGLU>(mx, mw, mw2, p, cg, status, s);
     case EPI_QKV:
       if (!qkv) return cudaErrorInvalidValue;
       p.n_ft = N / 128;
@@ -414,20 +526,20 @@ cudaError_t launch_gemm_sab(const void *A, int64_t lda, const void *W, const voi
       p.Hq = qkv->n_q_heads;
       p.Hkv = qkv->n_kv_heads;
       if (!make_map(&mw, W, N, K, ldw, FM)) return cudaErrorInvalidValue;
-      return run<EPI_QKV>(mx, mw, mw, p, status, s);
+      return run_cg<EPI_QKV>(mx, mw, mw, p, cg, status, s);
     case EPI_RESID:
       p.n_ft = (N + FM - 1) / FM;
       p.stream_k = 1;
       if (!make_map(&mw, W, N, K, ldw, FM)) return cudaErrorInvalidValue;
-      return run<EPI_RESID>(mx, mw, mw, p, status, s);
+      return run_cg<EPI_RESID>(mx, mw, mw, p, cg, status, s);
     case EPI_STORE:
       p.n_ft = (N + FM - 1) / FM;
       if (!make_map(&mw, W, N, K, ldw, FM)) return cudaErrorInvalidValue;
-      return run<EPI_STORE>(mx, mw, mw, p, status, s);
+      return run_cg<EPI_STORE>(mx, mw, mw, p, cg, status, s);
     case EPI_STORE_F32:
       p.n_ft = (N + FM - 1) / FM;
       if (!make_map(&mw, W, N, K, ldw, FM)) return cudaErrorInvalidValue;
-      return run<EPI_STORE_F32>(mx, mw, mw, p, status, s);
+      return run_cg<EPI_STORE_F32>(mx, mw, mw, p, cg, status, s);
   }
   return cudaErrorInvalidValue;
 }

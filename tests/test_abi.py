@@ -94,7 +94,7 @@ def test_host_validation_without_device():
     w = L.Weights(None, None, None, None)
     assert lib.cb_model_create(C.byref(cfg), C.byref(w), C.byref(h)) == L.CB_ERR_UNSUPPORTED
     assert lib.cb_debug_expire_wait(-1, None) == L.CB_ERR_INVALID_ARG
-    assert lib.cb_debug_gemm_path(3) == L.CB_ERR_INVALID_ARG
+    assert lib.cb_debug_gemm_path(4) == L.CB_ERR_INVALID_ARG
     assert lib.cb_debug_gemm_path(L.CB_GEMM_AUTO) == L.CB_OK
     assert lib.cb_debug_probe_start(0, 4) == L.CB_ERR_INVALID_ARG
     assert lib.cb_debug_probe_start(L.CB_PROBE_SWIGLU, 0) == L.CB_ERR_INVALID_ARG

@@ -200,8 +200,8 @@ def gemm_path(request):
     R.cb_debug_gemm_path(L.CB_GEMM_AUTO)
 
 
-@pytest.mark.parametrize("gemm_path", [L.CB_GEMM_AUTO, L.CB_GEMM_TOKEN_M, L.CB_GEMM_SWAP_AB],
-                         indirect=True)
+@pytest.mark.parametrize("gemm_path", [L.CB_GEMM_AUTO, L.CB_GEMM_TOKEN_M, L.CB_GEMM_SWAP_AB,
+                                       L.CB_GEMM_SWAP_AB_PAIR], indirect=True)
 def test_bf16_llama_truncated_forced(llama2, llama2_ref, gemm_path):
     """Every projection of the stack (fused Q/K/V with RoPE and cache
     scatter, O and down with residual, SwiGLU) on each tensor-core GEMM."""

@@ -295,7 +295,8 @@ def gemm_path(request):
     R.cb_debug_gemm_path(L.CB_GEMM_AUTO)
 
 
-@pytest.mark.parametrize("gemm_path", [L.CB_GEMM_TOKEN_M, L.CB_GEMM_SWAP_AB], indirect=True)
+@pytest.mark.parametrize("gemm_path", [L.CB_GEMM_TOKEN_M, L.CB_GEMM_SWAP_AB,
+                                       L.CB_GEMM_SWAP_AB_PAIR], indirect=True)
 @pytest.mark.parametrize("M", [524, 128, 3136, 1])
 def test_tensor_core_gemm_llama_shapes(M, gemm_path):
     """bf16 tcgen05 GEMMs (token rows on M, and the swapped form) at the
