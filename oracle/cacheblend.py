@@ -46,6 +46,7 @@ __all__ = [
     "qkv_rows", "decoder_layer", "full_prefill", "chunk_prefill", "kv_deviation",
     "select_count", "token_topk", "doc_aligned_select", "blend_prefill",
     "first_token", "first_token_logits", "embed_rows", "kv_bytes_per_layer",
+    "selection_segments", "captured_deviation",
     "BlendResult", "PrefillResult",
 ]
 
@@ -494,6 +495,23 @@ def blend_prefill(m: Model, segments, store, ratio_bp: int,
 # --------------------------------------------------------------------------
 # byte model
 # --------------------------------------------------------------------------
+def selection_segments(P) -> int:
+    """Number of separate contiguous regions a selection occupies: maximal
+    runs of consecutive positions in the ascending set P ("Request Order
+    Matters" §4.4, Table 2, "segments")."""
+    P = [int(i) for i in P]
+    return sum(1 for j, i in enumerate(P) if j == 0 or i != P[j - 1] + 1)
+
+
+def captured_deviation(P, d) -> float:
+    """Share of the selection-layer deviation carried by the selected tokens:
+    sum of d_i over P divided by the sum over all reusable tokens ("Request
+    Order Matters" §4.4, Table 2, "captured deviation")."""
+    d = np.asarray(d, dtype=np.float64)
+    total = float(d.sum())
+    return float(d[np.asarray(P, dtype=np.int64)].sum()) / total if total > 0 else 0.0
+
+
 def kv_bytes_per_layer(context_len: int, kv_heads: int, head_dim: int,
                        bytes_per_elem: int = 2) -> int:
     """K plus V bytes of one layer's cache: 2 * L * kv_heads * hd * 2 for

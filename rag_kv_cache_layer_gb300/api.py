@@ -19,7 +19,8 @@ __all__ = [
     "cb_kv_deviation_topk", "cb_kv_deviation_topk_noalloc", "cb_gather_rows",
     "cb_scatter_kv",
     "cb_sparse_query_attention", "cb_debug_expire_wait", "cb_debug_gemm_path", "Seg", "Req",
-    "BlendModel", "ChunkStore", "select_count", "device_status",
+    "BlendModel", "ChunkStore", "RollingWindow", "selection_stats", "select_count",
+    "device_status",
 ]
 
 device_status = L.device_status
@@ -366,7 +367,9 @@ class BlendModel:
 
 class ChunkStore:
     """Per-chunk PIC caches kept in one device pool [n_layers][rows][kvw]
-    (QCFuse Eq. 3: each chunk prefilled alone at positions 0..|c|-1)."""
+    (QCFuse Eq. 3: each chunk prefilled alone at positions 0..|c|-1).
+    Chunks occupy runs of pool rows; evicted runs are reused first-fit, so a
+    rolling window of equal-length documents cycles through fixed slots."""
 
     def __init__(self, model: BlendModel, capacity_rows: int):
         s = model.shape
@@ -375,22 +378,49 @@ class ChunkStore:
         self.K = torch.empty(s.n_layers, capacity_rows, model.kvw,
                              dtype=model.dtype, device=model.device)
         self.V = torch.empty_like(self.K)
-        self.where = {}       # chunk id -> (row, len)
-        self.used = 0
+        self.where = {}                      # chunk id -> (row, len)
+        self.free = [(0, capacity_rows)]     # free row runs, ascending
+
+    @property
+    def used(self) -> int:
+        return self.capacity - sum(n for _, n in self.free)
+
+    def _alloc(self, n: int) -> int:
+        for i, (r, m) in enumerate(self.free):
+            if m >= n:
+                if m == n:
+                    self.free.pop(i)
+                else:
+                    self.free[i] = (r + n, m - n)
+                return r
+        raise RuntimeError("chunk store is full")
+
+    def evict(self, cid):
+        """Drops a chunk; its rows become free (merged with neighbours)."""
+        r, n = self.where.pop(cid)
+        runs = sorted(self.free + [(r, n)])
+        merged = []
+        for a, m in runs:
+            if merged and merged[-1][0] + merged[-1][1] == a:
+                merged[-1] = (merged[-1][0], merged[-1][1] + m)
+            else:
+                merged.append((a, m))
+        self.free = merged
 
     def prefill(self, chunks: dict, stream=None):
         """chunks: {chunk_id: device int32 token tensor}; prefilled as one
-        batch of standalone requests into consecutive pool rows."""
+        batch of standalone requests into one run of pool rows per batch."""
         items = list(chunks.items())
+        for cid, _ in items:
+            if cid in self.where:
+                raise ValueError(f"chunk {cid!r} is already stored")
         for i in range(0, len(items), L.CB_MAX_BATCH):
             part = items[i:i + L.CB_MAX_BATCH]
             n = sum(int(t.numel()) for _, t in part)
-            if self.used + n > self.capacity:
-                raise RuntimeError("chunk store is full")
+            row0 = self._alloc(n)
             reqs = [Req(t, [Seg(int(t.numel()))]) for _, t in part]
             plan = self.model.plan(reqs)
             dev = self.model.device
-            row0 = self.used
             outs = {
                 "k_cache": self.K[:, row0:],
                 "v_cache": self.V[:, row0:],
@@ -405,8 +435,69 @@ class ChunkStore:
             for cid, t in part:
                 self.where[cid] = (r, int(t.numel()))
                 r += int(t.numel())
-            self.used = r
 
     def seg(self, cid) -> Seg:
         r, n = self.where[cid]
         return Seg(n, self.K[0, r], self.V[0, r], self.capacity * self.model.kvw, 0)
+
+
+class RollingWindow:
+    """Serving loop of a rolling-agent window ("Request Order Matters" §4.1):
+    every request holds the window's documents and a query.  The documents
+    already seen are cached chunks in a persistent store; the newest one has
+    no cache when its request is evaluated, so it is recomputed as an
+    uncached segment.  After the request it is prefilled into the store and
+    the oldest document is evicted (stride 1)."""
+
+    def __init__(self, model: BlendModel, window: int, doc_rows: int,
+                 ratio_bp: int, policy: int = L.CB_POLICY_DOC_ALIGNED):
+        self.model = model
+        self.window = window
+        self.ratio_bp = ratio_bp
+        self.policy = policy
+        # the window's cached documents plus the one being added
+        self.store = ChunkStore(model, (window + 1) * doc_rows)
+        self.docs = []        # cached document ids, window order
+        self.tokens = {}      # id -> device int32 tokens
+
+    def seed(self, docs: dict, stream=None):
+        """Prefills the documents that precede the first request."""
+        self.store.prefill(docs, stream)
+        for cid, t in docs.items():
+            self.docs.append(cid)
+            self.tokens[cid] = t
+
+    def request(self, new_tokens, query_tokens):
+        """The request for the current window plus one new document."""
+        segs = [self.store.seg(c) for c in self.docs]
+        segs += [Seg(int(new_tokens.numel())), Seg(int(query_tokens.numel()))]
+        toks = torch.cat([self.tokens[c] for c in self.docs] + [new_tokens, query_tokens])
+        return Req(toks.to(torch.int32).contiguous(), segs)
+
+    def blend(self, req, outputs=None, stream=None):
+        return self.model.cb_blend_prefill([req], self.ratio_bp, self.policy,
+                                           outputs=outputs, stream=stream)
+
+    def advance(self, new_id, new_tokens, stream=None):
+        """Stores the new document's chunk cache; evicts the oldest once the
+        window is full."""
+        self.store.prefill({new_id: new_tokens}, stream)
+        self.docs.append(new_id)
+        self.tokens[new_id] = new_tokens
+        if len(self.docs) > self.window - 1:
+            old = self.docs.pop(0)
+            self.store.evict(old)
+            del self.tokens[old]
+
+
+def selection_stats(selected: torch.Tensor, deviation: torch.Tensor):
+    """Diagnostics of one request's selection ("Request Order Matters" §4.4,
+    Table 2): the number of contiguous regions it occupies and the share of
+    the total deviation it carries.  selected: ascending positions; deviation:
+    d over the request's reusable tokens (host-side reporting only)."""
+    sel = selected.detach().to("cpu", torch.int64)
+    d = deviation.detach().to("cpu", torch.float64)
+    segments = 0 if sel.numel() == 0 else 1 + int((sel[1:] - sel[:-1] != 1).sum())
+    total = float(d.sum())
+    captured = float(d[sel].sum()) / total if total > 0 else 0.0
+    return segments, captured

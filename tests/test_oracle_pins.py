@@ -346,3 +346,26 @@ def test_byte_model_matches_printed_numbers():
         b = O.kv_bytes_per_layer(g["context_len"], c["kv_heads"], g["head_dim"])
         assert round(b / 1e6, 1) == c["printed_MB"]
         assert round(b / g["bandwidth_bytes_per_s"] * 1e3, 1) == c["printed_ms"]
+
+
+# ------------------------------------------------------ Table 2 diagnostics --
+def test_selection_segments_by_hand():
+    """"Request Order Matters" §4.4 Table 2: segments = separate contiguous
+    regions.  Counted by hand: {} none; {3} one; {1,2,3 | 7,8 | 10} three;
+    a single 400-token window one."""
+    assert O.selection_segments([]) == 0
+    assert O.selection_segments([3]) == 1
+    assert O.selection_segments([1, 2, 3, 7, 8, 10]) == 3
+    assert O.selection_segments(list(range(400, 800))) == 1
+    assert O.selection_segments([0, 2, 4, 6]) == 4
+
+
+def test_captured_deviation_by_hand():
+    """Same table: the selected tokens' share of the total deviation.
+    d = (1, 2, 3, 4): P = {1, 3} carries (2 + 4) / 10; all of it is 1; the
+    top-1 token carries 0.4."""
+    d = [1.0, 2.0, 3.0, 4.0]
+    assert O.captured_deviation([1, 3], d) == 0.6
+    assert O.captured_deviation([0, 1, 2, 3], d) == 1.0
+    assert O.captured_deviation([3], d) == 0.4
+    assert O.captured_deviation([], d) == 0.0

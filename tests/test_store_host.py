@@ -1,0 +1,56 @@
+"""Host logic without a GPU: the chunk store's row allocator (first-fit
+runs, eviction with merging) and the selection diagnostics against the
+oracle's definitions ("Request Order Matters" §4.4, Table 2)."""
+import types
+
+import numpy as np
+import torch
+
+import oracle as O
+from rag_kv_cache_layer_gb300 import api
+
+
+def _store(rows):
+    shape = types.SimpleNamespace(n_layers=2)
+    model = types.SimpleNamespace(shape=shape, kvw=4, dtype=torch.float32,
+                                  device=torch.device("cpu"))
+    return api.ChunkStore(model, rows)
+
+
+def test_rows_are_reused_first_fit_and_merged():
+    st = _store(100)
+    a = st._alloc(30); st.where["a"] = (a, 30)
+    b = st._alloc(30); st.where["b"] = (b, 30)
+    c = st._alloc(30); st.where["c"] = (c, 30)
+    assert (a, b, c) == (0, 30, 60) and st.used == 90
+    st.evict("b")
+    assert st.free == [(30, 30), (90, 10)] and st.used == 60
+    d = st._alloc(25); st.where["d"] = (d, 25)
+    assert d == 30                       # first fit: the evicted run
+    st.evict("a")
+    st.evict("c")
+    assert st.free == [(0, 30), (55, 45)]
+    st.evict("d")
+    assert st.free == [(0, 100)] and st.used == 0
+
+
+def test_store_full_is_an_error():
+    st = _store(10)
+    st._alloc(8)
+    try:
+        st._alloc(3)
+    except RuntimeError:
+        return
+    raise AssertionError("allocation past capacity must fail")
+
+
+def test_selection_stats_match_the_definitions():
+    rng = np.random.default_rng(0)
+    for _ in range(20):
+        n = int(rng.integers(1, 60))
+        d = rng.random(n)
+        k = int(rng.integers(0, n + 1))
+        P = np.sort(rng.choice(n, size=k, replace=False))
+        seg, cap = api.selection_stats(torch.from_numpy(P), torch.from_numpy(d))
+        assert seg == O.selection_segments(P)
+        assert abs(cap - O.captured_deviation(P, d)) < 1e-12
