@@ -182,6 +182,52 @@ def layer_rows(plan, n_layers, sel_layer=1):
     return [int(plan.T_total)] * sel_layer + [int(plan.R_total)] * (n_layers - sel_layer)
 
 
+def kernel_table(L, run_step, shape, plan, outs, peaks, reps=3):
+    """Device time per step of each kernel class (launch probe over `reps`
+    steps), its algorithmic work per step and the fraction of the measured
+    peak: tensor-bound classes against the sustained bf16 rate (they run
+    inside a long step), memory-bound ones against the copy bandwidth.
+
+    Work per step: GEMM FLOP 2 x in x out per computed row and layer (rows:
+    T at layer 0, R after); attention 4 hd Hq sum(p + 1) over the rows a
+    layer computes; stitch reads and writes K and V of every context row of
+    every stitched layer; selection reads fresh and reused keys of every
+    context row; gather moves R hidden rows; the LM head reads the
+    embedding once."""
+    n_layers = shape.n_layers
+    d, F, hd = shape.d_model, shape.d_ffn, shape.head_dim
+    qw, kvw = shape.n_q_heads * hd, shape.n_kv_heads * hd
+    T, N, R = int(plan.T_total), int(plan.N_total), int(plan.R_total)
+    rows = layer_rows(plan, n_layers)
+    pos = outs["rows"][:R].cpu().numpy().astype(np.float64)
+    att_rows = T * (T + 1) / 2 + (n_layers - 1) * float((pos + 1).sum())
+    tensor_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    spec = [
+        ("qkv", L.CB_PROBE_QKV, n_layers, "tensor", sum(rows) * 2.0 * d * (qw + 2 * kvw)),
+        ("attention", L.CB_PROBE_ATTENTION, n_layers, "tensor", 4.0 * hd * shape.n_q_heads * att_rows),
+        ("o_proj", L.CB_PROBE_O, n_layers, "tensor", sum(rows) * 2.0 * qw * d),
+        ("swiglu", L.CB_PROBE_SWIGLU, n_layers, "tensor", sum(rows) * 2.0 * d * 2 * F),
+        ("down_proj", L.CB_PROBE_DOWN, n_layers, "tensor", sum(rows) * 2.0 * F * d),
+        ("stitch", L.CB_PROBE_STITCH, 1, "hbm", (n_layers - 1) * N * kvw * 2.0 * 4),
+        ("select", L.CB_PROBE_SELECT, 1, "hbm", 2.0 * N * kvw * 2 + 4.0 * N),
+        ("gather", L.CB_PROBE_GATHER, 1, "hbm", 2.0 * R * d * 4),
+        ("lm_head", L.CB_PROBE_LM_HEAD, 1, "hbm", 2.0 * shape.vocab * d),
+    ]
+    out = {}
+    for name, kind, per_step, bound, work in spec:
+        n, ms = probe_steps(L, kind, per_step * reps, lambda: [run_step() for _ in range(reps)])
+        us = ms * 1e3 / reps
+        if bound == "tensor":
+            ach, unit, peak = work / (us * 1e-6) / 1e12, "TFLOP/s", tensor_peak
+        else:
+            ach, unit, peak = work / (us * 1e-6) / 1e9, "GB/s", hbm_peak
+        out[name] = {"us_per_step": round(us, 1), "launches_per_step": n // reps,
+                     "bound": bound, "achieved": round(ach, 1), "unit": unit,
+                     "frac": round(ach / peak, 3)}
+    return out
+
+
 def probe_steps(L, kind, n_launches, run):
     """Runs `run()` with the library's launch probe on one kernel class and
     returns (launches, summed device ms)."""
@@ -389,16 +435,29 @@ def run_ours(args):
     if R.device_status() != 0:
         raise RuntimeError("device status set during the timed region")
 
-    # per-class device time of one step (untimed; the same probe)
-    kernel_us = {}
-    for name, kind in (("qkv", L.CB_PROBE_QKV), ("attention", L.CB_PROBE_ATTENTION),
-                       ("o_proj", L.CB_PROBE_O), ("swiglu", L.CB_PROBE_SWIGLU),
-                       ("down_proj", L.CB_PROBE_DOWN)):
-        n, ms = probe_steps(L, kind, n_layers, lambda: (step(), torch.cuda.synchronize()))
-        kernel_us[name] = round(ms * 1e3, 1)
-    torch.cuda.synchronize()
+    # per-kernel-class device time, algorithmic work and roofline fraction
+    # (extra untimed steps, the same probe)
+    peaks_all, _ = load_peaks()
+    kernels = kernel_table(L, lambda: (step(), torch.cuda.synchronize()), wl.model, plan, outs,
+                           peaks_all)
     if R.device_status() != 0:
         raise RuntimeError("device status set during the probe steps")
+
+    # full prefill of the same request on the same kernels (its own graph)
+    full_outs = model.alloc_outputs(model.plan(reqs), 1, blend=False)
+    model.cb_full_prefill(reqs, outputs=full_outs)
+    gf = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gf):
+        model.cb_full_prefill(reqs, outputs=full_outs)
+    full_ms = []
+    for _ in range(5):
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(st)
+        gf.replay()
+        f1.record(st)
+        torch.cuda.synchronize()
+        full_ms.append(f0.elapsed_time(f1))
+    del gf, full_outs
 
     if rank == 0:
         peaks, src = load_peaks()
@@ -439,7 +498,9 @@ def run_ours(args):
                                     f"{kms * 1e3:.1f} us/launch on average"),
                          "traffic_note": "ncu dram bytes of one M=524 launch",
                          "peak_source": f"bf16_tflops_sustained of {src}"},
-            "kernel_us_per_step": kernel_us,
+            "kernels": kernels,
+            "full_prefill_ms": statistics.median(full_ms),
+            "speedup_vs_full_prefill": statistics.median(full_ms) / statistics.median(per),
             "clocks": clk,
             "gpu_launches": launches_per_step * args.steps,
         }

@@ -128,13 +128,18 @@ cb_status cb_debug_gemm_path(int path);
  * stream capture) is bracketed by two CUDA events on its own stream;
  * cb_debug_probe_stop waits for the recorded launches and returns their
  * count and summed device time in milliseconds, then releases the events.
- * The attention class includes its split-KV combine kernel.  Debug use only
+ * The attention class includes its split-KV combine kernel; classes 6-9
+ * bracket the once-per-call steps of cb_blend_prefill.  Debug use only
  * (one probe per process; start discards an unfinished probe). */
 #define CB_PROBE_QKV 1       /* fused Q/K/V projection (+ RoPE, cache scatter) */
 #define CB_PROBE_O 2         /* attention output projection + residual */
 #define CB_PROBE_SWIGLU 3    /* gate/up projection with SiLU gating */
 #define CB_PROBE_DOWN 4      /* down projection + residual */
 #define CB_PROBE_ATTENTION 5 /* selected-query attention */
+#define CB_PROBE_STITCH 6    /* re-position + stitch of the cached segments */
+#define CB_PROBE_SELECT 7    /* deviation + ranking at the selection layer */
+#define CB_PROBE_GATHER 8    /* computed-row list + hidden-state gather */
+#define CB_PROBE_LM_HEAD 9   /* final norm + tied LM head + arg-max */
 cb_status cb_debug_probe_start(int kind, int max_launches);
 cb_status cb_debug_probe_stop(int *n_launches, float *total_ms);
 

@@ -23,6 +23,7 @@ CB_POLICY_TOKEN_TOPK, CB_POLICY_DOC_ALIGNED = 0, 1
 CB_EPI_STORE, CB_EPI_RESID, CB_EPI_SWIGLU = 0, 1, 2
 CB_GEMM_AUTO, CB_GEMM_TOKEN_M, CB_GEMM_SWAP_AB, CB_GEMM_SWAP_AB_PAIR = 0, 1, 2, 3
 CB_PROBE_QKV, CB_PROBE_O, CB_PROBE_SWIGLU, CB_PROBE_DOWN, CB_PROBE_ATTENTION = 1, 2, 3, 4, 5
+CB_PROBE_STITCH, CB_PROBE_SELECT, CB_PROBE_GATHER, CB_PROBE_LM_HEAD = 6, 7, 8, 9
 CB_MAX_BATCH = 64
 CB_MAX_SPANS = 1024
 

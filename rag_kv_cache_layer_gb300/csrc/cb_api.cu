@@ -100,7 +100,7 @@ static void probe_release() {
 }
 
 extern "C" cb_status cb_debug_probe_start(int kind, int max_launches) {
-  if (kind < CB_PROBE_QKV || kind > CB_PROBE_ATTENTION || max_launches <= 0 ||
+  if (kind < CB_PROBE_QKV || kind > CB_PROBE_LM_HEAD || max_launches <= 0 ||
       max_launches > 65536)
     return fail(CB_ERR_INVALID_ARG, "bad probe kind or max_launches");
   std::lock_guard<std::mutex> lk(g_probe_mu);
@@ -958,9 +958,11 @@ extern "C" cb_status cb_blend_prefill(cb_model *m, const cb_request *reqs, int B
       descs.push_back(cb_stitch_desc{sg.k_pic, sg.v_pic, sg.pic_layer_stride, sg.len,
                                      P.bm.t_off[b] + pos0, pos0 - sg.pic_pos0});
     }
+  probe_mark(CB_PROBE_STITCH, true, s);
   CB_CUDA(launch_reposition(descs.data(), (int)descs.size(), s_layer, L, out->k_cache,
                             out->v_cache, lstride, m->kvw, c.head_dim, m->w.rope_table,
                             c.dtype, st, s));
+  probe_mark(CB_PROBE_STITCH, false, s);
   // 2. embeddings of every row, full layers below the selection layer
   const int32_t *toks[CB_MAX_BATCH];
   for (int b = 0; b < B; ++b) toks[b] = reqs[b].tokens;
@@ -1003,6 +1005,7 @@ extern "C" cb_status cb_blend_prefill(cb_model *m, const cb_request *reqs, int B
           return fail(CB_ERR_INVALID_ARG, "too many spans (max %d)", CB_MAX_SPANS);
       }
     }
+    probe_mark(CB_PROBE_SELECT, true, s);
     if (p->forced_selected) {
       // the caller fixes P; d is still produced for inspection
       CB_CUDA(launch_deviation(kf, m->kvw, layer_ptr(out->k_cache, s_layer, lstride, m->eb),
@@ -1014,11 +1017,14 @@ extern "C" cb_status cb_blend_prefill(cb_model *m, const cb_request *reqs, int B
       CB_TRY(run_selection(kf, m->kvw, layer_ptr(out->k_cache, s_layer, lstride, m->eb),
                            m->kvw, m->kvw, c.dtype, sr, spans, p->policy, dev, sel, st, s));
     }
+    probe_mark(CB_PROBE_SELECT, false, s);
   }
   // 4. computed rows: selected context rows + uncached rows, gathered once
+  probe_mark(CB_PROBE_GATHER, true, s);
   CB_CUDA(launch_build_rows(P.bm, sel, pos_c, glob_c, (int)P.R_total, st, s));
   CB_CUDA(launch_gather(h_all, d, P.T_total, glob_c, (int)P.R_total, d, h_c, d, sizeof(float),
                         st, s));
+  probe_mark(CB_PROBE_GATHER, false, s);
   // 5. layers >= s on the computed rows; gradual filtering steps shrink the
   // set between layers (the rows alternate between two buffer sets)
   int32_t *sel_b[2] = {sel, (int32_t *)(ws + P.g_sel)};
@@ -1056,7 +1062,9 @@ extern "C" cb_status cb_blend_prefill(cb_model *m, const cb_request *reqs, int B
                             cudaMemcpyDeviceToDevice, s));
   }
   // 6. first token from each request's last computed row (its last position)
+  probe_mark(CB_PROBE_LM_HEAD, true, s);
   if (out->first_token) CB_TRY(run_lm_head(m, P, h_b[0], bm.r_off, ws, out->first_token, s));
+  probe_mark(CB_PROBE_LM_HEAD, false, s);
   return CB_OK;
 }
 

@@ -10,12 +10,16 @@
 //
 // Roles (192 threads): warp 0 TMA producer (Q once, then double-buffered
 // 128-key K and V blocks, 128-byte swizzle); warp 1 owns TMEM and issues
-// tcgen05.mma: S_j = Q K_j^T (K-major operands) and O_j = P_j V_j (P K-major
-// from shared memory, V MN-major), each double-buffered in TMEM; warps 2..5
-// do the online softmax (one row per thread, log2 domain, causal mask),
-// write P_j as bf16 in the swizzled K-major layout (double-buffered), and
-// fold O_{j-1} into registers, O = O * exp2(m_old - m_new) + O_{j-1}, while
-// the tensor core computes O_j.  All waits are bounded.
+// tcgen05.mma: S_j = Q K_j^T (K-major operands, double-buffered in TMEM)
+// and O += P_j V_j (P K-major from shared memory, V MN-major) into one TMEM
+// accumulator; warps 2..5 do the online softmax (one row per thread, log2
+// domain, causal mask) and write P_j as bf16 in the swizzled K-major layout
+// (double-buffered).  The row's reference maximum m only moves when a block
+// raises the maximum by more than 2^kRescale: then O (in TMEM, after the
+// previous P V has landed) and l are scaled by 2^(m_old - m_new).  Between
+// moves the probabilities stay below 2^kRescale, and O / l is unchanged by
+// the choice of reference, so the result is the same softmax.  All waits
+// are bounded.
 //
 // When the query tiles alone cannot fill the SMs (the compact layers), the
 // key range of every tile is split into chunks processed by separate CTAs;
@@ -33,6 +37,7 @@ namespace cb {
 namespace attn {
 
 constexpr int kThreads = 192;
+constexpr float kRescale = 8.f;            // log2 of the largest p between rescales
 constexpr int HD = 128;
 constexpr int BN = 128;                    // keys per block
 constexpr int kAtom = 128 * 64 * 2;        // one [128 rows x 64 bf16] swizzle tile
@@ -124,6 +129,28 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Writes 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+          taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // 2^x with the SFU's approximate base-2 exponential (PTX ex2.approx.ftz;
 // documented maximum relative error about 2^-22), far below the bf16
 // rounding of the probabilities it feeds.
@@ -172,9 +199,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   uint64_t *v_empty = bar + 7;     // [2]
   uint64_t *s_full = bar + 9;      // [2]
   uint64_t *s_free = bar + 11;     // [2]
-  uint64_t *p_full = bar + 13;     // [2]
-  uint64_t *pv_full = bar + 15;    // [2]
-  uint64_t *pv_free = bar + 17;    // [2]
+  uint64_t *p_full = bar + 13;     // [2]  P_j written (and O rescaled)
+  uint64_t *pv_done = bar + 15;    // [2]  O += P_j V_j has landed
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 19);
   volatile int *fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
   __shared__ int s_unit[6];        // b, g, tile, first block, end block
@@ -202,8 +228,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
       mbar_init(smem_u32(&s_full[i]), 1);
       mbar_init(smem_u32(&s_free[i]), 128);
       mbar_init(smem_u32(&p_full[i]), 128);
-      mbar_init(smem_u32(&pv_full[i]), 1);
-      mbar_init(smem_u32(&pv_free[i]), 128);
+      mbar_init(smem_u32(&pv_done[i]), 1);
     }
     *fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -224,7 +249,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   const AttnReq &R = P.r[b];
   const int row0 = R.q_begin + t * P.QT;          // first q row of the tile
   const int n_valid = min(P.QT, R.q_end - row0);  // q rows of the request in the tile
-  // TMEM columns: S[0] 0..127, S[1] 128..255, O_j[0] 256..383, O_j[1] 384..511
+  // TMEM columns: S[0] 0..127, S[1] 128..255, O 256..383
 
   if (nb > 0 && warp == 0 && lane < 2) {
     // ----------------------------------------------- producers (K: lane 0, V: lane 1)
@@ -281,7 +306,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
       const int s = j & 1;
       if (j + 1 < nb && !issue_s(j + 1)) { ok = false; break; }
       if (!mbar_wait_bounded(smem_u32(&p_full[s]), (j >> 1) & 1, kWaitLimitNs, status) ||
-          !mbar_wait_bounded(smem_u32(&pv_free[s]), ((j >> 1) & 1) ^ 1, kWaitLimitNs, status) ||
           !mbar_wait_bounded(smem_u32(&v_full[s]), (j >> 1) & 1, kWaitLimitNs, status)) {
         ok = false;
         break;
@@ -292,10 +316,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
 #pragma unroll
       for (int k = 0; k < BN / 16; ++k) {
         const uint32_t poff = (k >> 2) * kAtom + (k & 3) * 32;
-        mma(tmem + 2 * BN + s * BN, desc_kmajor(p_addr + poff),
-            desc_mnmajor(v_addr + k * 16 * 128, kAtom), idPV, k > 0);
+        mma(tmem + 2 * BN, desc_kmajor(p_addr + poff),
+            desc_mnmajor(v_addr + k * 16 * 128, kAtom), idPV, (j > 0 || k > 0) ? 1u : 0u);
       }
-      commit(smem_u32(&pv_full[s]));
+      commit(smem_u32(&pv_done[s]));
       commit(smem_u32(&v_empty[s]));
     }
     if (!ok) *fail = 1;
@@ -308,29 +332,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
     int p = valid ? q_pos[row0 + qi] : 0;
     if (p < 0 || p >= R.kv_len) p = 0;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    float o[HD];
-#pragma unroll
-    for (int i = 0; i < HD; ++i) o[i] = 0.f;
-    float m = -INFINITY, l = 0.f, corr_pending = 1.f;
+    const uint32_t obase = tmem + lane_off + 2 * BN;
+    float m = -INFINITY, l = 0.f;                 // reference max (log2 domain), sum
     const float sl2 = P.scale_log2;
     bool failed = false;
-    // folds O_j (TMEM buffer j & 1) into the register accumulator
-    auto fold = [&](int j, float corr) -> bool {
-      const int s = j & 1;
-      const bool bad = !mbar_wait_bounded(smem_u32(&pv_full[s]), (j >> 1) & 1, kWaitLimitNs,
+    // waits until O += P_j V_j has landed in TMEM
+    auto pv_landed = [&](int j) -> bool {
+      const bool bad = !mbar_wait_bounded(smem_u32(&pv_done[j & 1]), (j >> 1) & 1, kWaitLimitNs,
                                           status) || *fail;
       if (__any_sync(0xffffffffu, bad)) return false;
       fence_after();
-      const uint32_t obase = tmem + lane_off + 2 * BN + s * BN;
-#pragma unroll
-      for (int c = 0; c < HD; c += 32) {
-        float y[32];
-        ld32(obase + c, y);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[c + i] = o[c + i] * corr + y[i];
-      }
-      fence_before();
-      arrive(smem_u32(&pv_free[s]));
       return true;
     };
     for (int j = 0; j < nb; ++j) {
@@ -345,40 +356,58 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
       // take the mask-free path.  Eight partial maxima / sums keep the
       // dependency chains short (one softmax warp per scheduler).
       const int n_vis = p - key0 + 1;               // >= BN: no masking
+      float x[BN];
+#pragma unroll
+      for (int c = 0; c < BN; c += 32) ld32(sbase + c, *reinterpret_cast<float(*)[32]>(x + c));
+      // S_j is in registers: its TMEM slot may take S_{j+2}
+      fence_before();
+      arrive(smem_u32(&s_free[s]));
       float mx[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        float x[32];
-        ld32(sbase + c, x);
-        if (n_vis >= BN) {
+      if (n_vis >= BN) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
-        } else {
+        for (int i = 0; i < BN; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+      } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c + i < n_vis) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
-        }
+        for (int i = 0; i < BN; ++i)
+          if (i < n_vis) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
       }
       const float mloc = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float m_new = fmaxf(m, mloc * sl2);
-      // a row whose keys are all masked so far keeps m = -inf and p = 0
-      const float corr = m_new == -INFINITY ? 1.f : fast_exp2(m - m_new);
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+      // move the reference only for a large rise; the first visible key
+      // always sets it (m = -inf before)
+      const bool move = mloc > m + kRescale;
+      const bool rescale = move && m != -INFINITY;  // O and l hold earlier blocks
+      if (__any_sync(0xffffffffu, rescale) && j > 0) {
+        // O must hold P_{j-1} V_{j-1} before it is scaled; the TMEM
+        // loads / stores are warp-wide, rows that keep m scale by 1
+        if (!pv_landed(j - 1)) { failed = true; break; }
+        const float corr = rescale ? fast_exp2(m - mloc) : 1.f;
+#pragma unroll
+        for (int c = 0; c < HD; c += 32) {
+          float y[32];
+          ld32(obase + c, y);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) y[i] *= corr;
+          st32(obase + c, y);
+        }
+        l *= corr;
+      }
+      if (move) m = mloc;
+      // P_j reuses the buffer of P_{j-2}: its P V must have finished
+      if (j >= 2 && !pv_landed(j - 2)) { failed = true; break; }
       float ls[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) ls[i] = 0.f;
       uint8_t *prow = smem + kOffP + s * kP + row * 128;
-#pragma unroll 1
+#pragma unroll
       for (int c = 0; c < BN; c += 32) {
-        float x[32];
-        ld32(sbase + c, x);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          float p0 = fast_exp2(fmaf(x[i], sl2, -m_new));
-          float p1 = fast_exp2(fmaf(x[i + 1], sl2, -m_new));
+          float p0 = fast_exp2(fmaf(x[c + i], sl2, -m));
+          float p1 = fast_exp2(fmaf(x[c + i + 1], sl2, -m));
           if (n_vis < BN) {
             p0 = c + i < n_vis ? p0 : 0.f;
             p1 = c + i + 1 < n_vis ? p1 : 0.f;
@@ -396,17 +425,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
               make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
         }
       }
-      l = fmaf(l, corr, ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       fence_before();
-      arrive(smem_u32(&s_free[s]));
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       arrive(smem_u32(&p_full[s]));
-      m = m_new;
-      // the tensor core now computes O_j; fold the previous block meanwhile
-      if (j > 0 && !fold(j - 1, corr_pending)) { failed = true; break; }
-      corr_pending = corr;
     }
-    if (!failed && nb > 0 && !fold(nb - 1, corr_pending)) failed = true;
+    // the whole key range is in O once the last P V has landed
+    if (!failed && nb > 0 && !pv_landed(nb - 1)) failed = true;
+    float o[HD];
+    if (!failed && nb > 0) {
+#pragma unroll
+      for (int c = 0; c < HD; c += 32) ld32(obase + c, *reinterpret_cast<float(*)[32]>(o + c));
+    } else {
+#pragma unroll
+      for (int i = 0; i < HD; ++i) o[i] = 0.f;
+    }
     if (failed) *fail = 1;
     if (valid && !*fail) {
       const int q_row = row0 + qi, head = g * P.G + h;
