@@ -8,18 +8,21 @@
 // of a request are sorted by position, so a tile only visits keys up to its
 // last query's position.
 //
-// Roles (192 threads): warp 0 TMA producer (Q once, then double-buffered
-// 128-key K and V blocks, 128-byte swizzle); warp 1 owns TMEM and issues
-// tcgen05.mma: S_j = Q K_j^T (K-major operands, double-buffered in TMEM)
-// and O += P_j V_j (P K-major from shared memory, V MN-major) into one TMEM
-// accumulator; warps 2..5 do the online softmax (one row per thread, log2
-// domain, causal mask) and write P_j as bf16 in the swizzled K-major layout
-// (double-buffered).  The row's reference maximum m only moves when a block
-// raises the maximum by more than 2^kRescale: then O (in TMEM, after the
-// previous P V has landed) and l are scaled by 2^(m_old - m_new).  Between
-// moves the probabilities stay below 2^kRescale, and O / l is unchanged by
-// the choice of reference, so the result is the same softmax.  All waits
-// are bounded.
+// Roles (192 threads, two CTAs per SM): warp 0 TMA producer (Q once, then
+// 128-key K and V blocks, 128-byte swizzle); warp 1 owns 256 TMEM columns
+// and issues tcgen05.mma: S_j = Q K_j^T into columns 0..127 (K-major
+// operands) and O += P_j V_j into columns 128..255 with P_j read from TMEM
+// (it overwrites S_j) and V MN-major from shared memory; warps 2..5 do the
+// online softmax (one row per thread, log2 domain, causal mask) and store
+// P_j as packed bf16 into TMEM.  Within a CTA the steps are serial
+// (S_{j+1} waits for P_j V_j); the SM's other CTA keeps the tensor core
+// busy meanwhile.  The row's reference maximum m only moves when a block
+// raises the maximum by more than 2^kRescale: then O and l are scaled by
+// 2^(m_old - m_new) (O is stable then: P_{j-1} V_{j-1} completed before
+// S_j was issued).  Between moves the probabilities stay below 2^kRescale,
+// and O / l does not depend on the reference, so the result is the same
+// softmax.  One exponential in four runs on the FMA pipe (exp2_poly) to
+// relieve the SFU.  All waits are bounded.
 //
 // When the query tiles alone cannot fill the SMs (the compact layers), the
 // key range of every tile is split into chunks processed by separate CTAs;
@@ -43,14 +46,14 @@ constexpr int BN = 128;                    // keys per block
 constexpr int kAtom = 128 * 64 * 2;        // one [128 rows x 64 bf16] swizzle tile
 constexpr int kQ = 2 * kAtom;              // Q tile: 128 rows x 128 dims
 constexpr int kKV = 2 * kAtom;             // K or V block: 128 keys x 128 dims
-constexpr int kP = 2 * kAtom;              // P tile: 128 rows x 128 keys
-// smem: Q | K[2] | V[2] | P[2] | barriers   (224 KB + barriers)
+// smem: Q | K | V | barriers   (96 KB + barriers): two CTAs fit on an SM
 constexpr int kOffK = kQ;
-constexpr int kOffV = kOffK + 2 * kKV;
-constexpr int kOffP = kOffV + 2 * kKV;
-constexpr int kOffBar = kOffP + 2 * kP;
+constexpr int kOffV = kOffK + kKV;
+constexpr int kOffBar = kOffV + kKV;
 constexpr int kSmem = kOffBar + 256 + 1024;
-static_assert(kSmem <= 232448, "attention tile exceeds shared memory");
+constexpr int kCtasPerSm = 2;
+constexpr int kTmemCols = 256;             // S/P 0..127, O 128..255
+static_assert(kCtasPerSm * (kSmem + 1024) <= 233472, "two attention CTAs must fit an SM");
 
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) {
   uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
@@ -160,6 +163,43 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// 2^x on the FMA pipe: x = n + f with n = round(x), |f| <= 1/2, 2^f from a
+// cubic fitted by least squares on the relative error at Chebyshev nodes
+// of [-1/2, 1/2] (relative error below 8e-5), and n added to the exponent
+// field.  The rounding uses the 1.5 * 2^23 shift (the float spacing there
+// is 1), so no conversion instruction is needed; the low bits of t then
+// hold n, and t << 23 is n << 23.  Inputs are clamped at -126 (2^x is then
+// far below what the bf16 probabilities resolve).  Valid for x <= 64.
+constexpr float kExpC0 = 0.99992895f, kExpC1 = 0.6932762f, kExpC2 = 0.24260405f,
+                kExpC3 = 0.05508868f;
+__device__ __forceinline__ float exp2_poly(float x) {
+  x = fmaxf(x, -126.f);
+  const float t = x + 12582912.f;
+  const float f = x - (t - 12582912.f);
+  const float p = fmaf(fmaf(fmaf(kExpC3, f, kExpC2), f, kExpC1), f, kExpC0);
+  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
+
+// Writes 16 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+
+// D (TMEM) += A (TMEM, M lanes x K packed in columns) * B (shared memory).
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id,
+                                       uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(id), "r"(acc));
+}
+
 struct Params {
   int n_req;
   int G, QT, Hkv;
@@ -183,7 +223,7 @@ __device__ __forceinline__ TileId decode_tile(const Params &P, int tile) {
   return TileId{b, local % P.Hkv, n_t - 1 - local / P.Hkv};
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
                const __grid_constant__ CUtensorMap mapK,
                const __grid_constant__ CUtensorMap mapV, const __grid_constant__ Params P,
@@ -193,15 +233,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
   uint64_t *q_full = bar + 0;
-  uint64_t *k_full = bar + 1;      // [2]  K ring: freed once S = Q K^T is done
-  uint64_t *k_empty = bar + 3;     // [2]
-  uint64_t *v_full = bar + 5;      // [2]  V ring: freed once O_j = P V is done
-  uint64_t *v_empty = bar + 7;     // [2]
-  uint64_t *s_full = bar + 9;      // [2]
-  uint64_t *s_free = bar + 11;     // [2]
-  uint64_t *p_full = bar + 13;     // [2]  P_j written (and O rescaled)
-  uint64_t *pv_done = bar + 15;    // [2]  O += P_j V_j has landed
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 19);
+  uint64_t *k_full = bar + 1;      // K_j landed
+  uint64_t *k_empty = bar + 2;     // S_j = Q K_j^T done with K_j
+  uint64_t *v_full = bar + 3;      // V_j landed
+  uint64_t *v_empty = bar + 4;     // P_j V_j done with V_j
+  uint64_t *s_full = bar + 5;      // S_j in TMEM
+  uint64_t *p_full = bar + 6;      // P_j in TMEM (and O rescaled)
+  uint64_t *pv_done = bar + 7;     // O += P_j V_j has landed
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 8);
   volatile int *fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
   __shared__ int s_unit[6];        // b, g, tile, first block, end block
 
@@ -220,23 +259,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
     s_unit[3] = jb;
     s_unit[4] = max(jb, min(nb_tile, jb + P.chunk_blocks));
     mbar_init(smem_u32(q_full), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&k_full[i]), 1);
-      mbar_init(smem_u32(&k_empty[i]), 1);
-      mbar_init(smem_u32(&v_full[i]), 1);
-      mbar_init(smem_u32(&v_empty[i]), 1);
-      mbar_init(smem_u32(&s_full[i]), 1);
-      mbar_init(smem_u32(&s_free[i]), 128);
-      mbar_init(smem_u32(&p_full[i]), 128);
-      mbar_init(smem_u32(&pv_done[i]), 1);
-    }
+    mbar_init(smem_u32(k_full), 1);
+    mbar_init(smem_u32(k_empty), 1);
+    mbar_init(smem_u32(v_full), 1);
+    mbar_init(smem_u32(v_empty), 1);
+    mbar_init(smem_u32(s_full), 1);
+    mbar_init(smem_u32(p_full), 128);
+    mbar_init(smem_u32(pv_done), 1);
     *fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
-                 "r"(512)
+                 "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -249,12 +285,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   const AttnReq &R = P.r[b];
   const int row0 = R.q_begin + t * P.QT;          // first q row of the tile
   const int n_valid = min(P.QT, R.q_end - row0);  // q rows of the request in the tile
-  // TMEM columns: S[0] 0..127, S[1] 128..255, O 256..383
 
   if (nb > 0 && warp == 0 && lane < 2) {
     // ----------------------------------------------- producers (K: lane 0, V: lane 1)
-    // Two independent loaders, so a K block can be fetched as soon as the
-    // previous S = Q K^T has finished with its slot, whatever V is doing.
+    // Two loaders, so K_{j+1} is fetched as soon as S_j has used K_j,
+    // whatever V is doing.
     const CUtensorMap *map = lane == 0 ? &mapK : &mapV;
     uint64_t *full = lane == 0 ? k_full : v_full;
     uint64_t *empty = lane == 0 ? k_empty : v_empty;
@@ -268,59 +303,50 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
                       (g * P.G + h) * HD + half * 64, row0);
     }
     for (int j = 0; j < nb; ++j) {
-      const int s = j & 1;
-      if (!mbar_wait_bounded(smem_u32(&empty[s]), ((j >> 1) & 1) ^ 1, kWaitLimitNs, status) ||
-          *fail) {
+      if (!mbar_wait_bounded(smem_u32(empty), (j & 1) ^ 1, kWaitLimitNs, status) || *fail) {
         *fail = 1;
         break;
       }
-      const uint32_t fb = smem_u32(&full[s]);
+      const uint32_t fb = smem_u32(full);
       expect_tx(fb, kKV);
       const int key_row = (int)R.kv_row0 + (jb + j) * BN;
       for (int half = 0; half < 2; ++half)
-        tma_load_2d(smem_u32(smem + off + s * kKV + half * kAtom), map, fb, g * HD + half * 64,
-                    key_row);
+        tma_load_2d(smem_u32(smem + off + half * kAtom), map, fb, g * HD + half * 64, key_row);
     }
   } else if (nb > 0 && warp == 1 && lane == 0) {
     // ----------------------------------------------------------------- MMA
     const uint32_t idS = idesc(false), idPV = idesc(true);
     const uint32_t q_addr = smem_u32(smem);
+    const uint32_t k_addr = smem_u32(smem + kOffK), v_addr = smem_u32(smem + kOffV);
     bool ok = mbar_wait_bounded(smem_u32(q_full), 0, kWaitLimitNs, status);
-    auto issue_s = [&](int j) -> bool {
-      const int s = j & 1;
-      if (!mbar_wait_bounded(smem_u32(&k_full[s]), (j >> 1) & 1, kWaitLimitNs, status)) return false;
-      if (!mbar_wait_bounded(smem_u32(&s_free[s]), ((j >> 1) & 1) ^ 1, kWaitLimitNs, status)) return false;
-      fence_after();
-      const uint32_t k_addr = smem_u32(smem + kOffK + s * kKV);
-#pragma unroll
-      for (int k = 0; k < HD / 16; ++k) {
-        const uint32_t off = (k >> 2) * kAtom + (k & 3) * 32;
-        mma(tmem + s * BN, desc_kmajor(q_addr + off), desc_kmajor(k_addr + off), idS, k > 0);
-      }
-      commit(smem_u32(&s_full[s]));
-      commit(smem_u32(&k_empty[s]));
-      return true;
-    };
-    if (ok) ok = issue_s(0);
     for (int j = 0; j < nb && ok && !*fail; ++j) {
-      const int s = j & 1;
-      if (j + 1 < nb && !issue_s(j + 1)) { ok = false; break; }
-      if (!mbar_wait_bounded(smem_u32(&p_full[s]), (j >> 1) & 1, kWaitLimitNs, status) ||
-          !mbar_wait_bounded(smem_u32(&v_full[s]), (j >> 1) & 1, kWaitLimitNs, status)) {
+      const uint32_t ph = j & 1;
+      // S_j overwrites P_{j-1}: its P V must have completed
+      if (!mbar_wait_bounded(smem_u32(k_full), ph, kWaitLimitNs, status) ||
+          (j > 0 && !mbar_wait_bounded(smem_u32(pv_done), ph ^ 1, kWaitLimitNs, status))) {
         ok = false;
         break;
       }
       fence_after();
-      const uint32_t p_addr = smem_u32(smem + kOffP + s * kP);
-      const uint32_t v_addr = smem_u32(smem + kOffV + s * kKV);
 #pragma unroll
-      for (int k = 0; k < BN / 16; ++k) {
-        const uint32_t poff = (k >> 2) * kAtom + (k & 3) * 32;
-        mma(tmem + 2 * BN, desc_kmajor(p_addr + poff),
-            desc_mnmajor(v_addr + k * 16 * 128, kAtom), idPV, (j > 0 || k > 0) ? 1u : 0u);
+      for (int k = 0; k < HD / 16; ++k) {
+        const uint32_t off = (k >> 2) * kAtom + (k & 3) * 32;
+        mma(tmem, desc_kmajor(q_addr + off), desc_kmajor(k_addr + off), idS, k > 0);
       }
-      commit(smem_u32(&pv_done[s]));
-      commit(smem_u32(&v_empty[s]));
+      commit(smem_u32(s_full));
+      commit(smem_u32(k_empty));
+      if (!mbar_wait_bounded(smem_u32(p_full), ph, kWaitLimitNs, status) ||
+          !mbar_wait_bounded(smem_u32(v_full), ph, kWaitLimitNs, status)) {
+        ok = false;
+        break;
+      }
+      fence_after();
+#pragma unroll
+      for (int k = 0; k < BN / 16; ++k)
+        mma_ts(tmem + BN, tmem + k * 8, desc_mnmajor(v_addr + k * 16 * 128, kAtom), idPV,
+               (j > 0 || k > 0) ? 1u : 0u);
+      commit(smem_u32(pv_done));
+      commit(smem_u32(v_empty));
     }
     if (!ok) *fail = 1;
   } else if (warp >= 2) {
@@ -332,46 +358,37 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
     int p = valid ? q_pos[row0 + qi] : 0;
     if (p < 0 || p >= R.kv_len) p = 0;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t obase = tmem + lane_off + 2 * BN;
+    const uint32_t sbase = tmem + lane_off;       // S_j, then P_j (packed bf16)
+    const uint32_t obase = tmem + lane_off + BN;
     float m = -INFINITY, l = 0.f;                 // reference max (log2 domain), sum
     const float sl2 = P.scale_log2;
     bool failed = false;
-    // waits until O += P_j V_j has landed in TMEM
-    auto pv_landed = [&](int j) -> bool {
-      const bool bad = !mbar_wait_bounded(smem_u32(&pv_done[j & 1]), (j >> 1) & 1, kWaitLimitNs,
-                                          status) || *fail;
-      if (__any_sync(0xffffffffu, bad)) return false;
-      fence_after();
-      return true;
-    };
     for (int j = 0; j < nb; ++j) {
-      const int s = j & 1;
+      const uint32_t ph = j & 1;
       const bool bad =
-          !mbar_wait_bounded(smem_u32(&s_full[s]), (j >> 1) & 1, kWaitLimitNs, status) || *fail;
+          !mbar_wait_bounded(smem_u32(s_full), ph, kWaitLimitNs, status) || *fail;
       if (__any_sync(0xffffffffu, bad)) { failed = true; break; }
       fence_after();
-      const uint32_t sbase = tmem + lane_off + s * BN;
       const int key0 = (jb + j) * BN;
       // Keys visible to this row: key0 .. p.  Blocks wholly at or before p
       // take the mask-free path.  Eight partial maxima / sums keep the
-      // dependency chains short (one softmax warp per scheduler).
+      // dependency chains short.
       const int n_vis = p - key0 + 1;               // >= BN: no masking
-      float x[BN];
-#pragma unroll
-      for (int c = 0; c < BN; c += 32) ld32(sbase + c, *reinterpret_cast<float(*)[32]>(x + c));
-      // S_j is in registers: its TMEM slot may take S_{j+2}
-      fence_before();
-      arrive(smem_u32(&s_free[s]));
       float mx[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-      if (n_vis >= BN) {
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        float x[32];
+        ld32(sbase + c, x);
+        if (n_vis >= BN) {
 #pragma unroll
-        for (int i = 0; i < BN; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
-      } else {
+          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+        } else {
 #pragma unroll
-        for (int i = 0; i < BN; ++i)
-          if (i < n_vis) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+          for (int i = 0; i < 32; ++i)
+            if (c + i < n_vis) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+        }
       }
       const float mloc = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
@@ -379,12 +396,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
       // always sets it (m = -inf before)
       const bool move = mloc > m + kRescale;
       const bool rescale = move && m != -INFINITY;  // O and l hold earlier blocks
-      if (__any_sync(0xffffffffu, rescale) && j > 0) {
-        // O must hold P_{j-1} V_{j-1} before it is scaled; the TMEM
-        // loads / stores are warp-wide, rows that keep m scale by 1
-        if (!pv_landed(j - 1)) { failed = true; break; }
+      if (__any_sync(0xffffffffu, rescale)) {
+        // the TMEM loads / stores are warp-wide; rows that keep m scale by 1
         const float corr = rescale ? fast_exp2(m - mloc) : 1.f;
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < HD; c += 32) {
           float y[32];
           ld32(obase + c, y);
@@ -395,19 +410,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
         l *= corr;
       }
       if (move) m = mloc;
-      // P_j reuses the buffer of P_{j-2}: its P V must have finished
-      if (j >= 2 && !pv_landed(j - 2)) { failed = true; break; }
       float ls[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) ls[i] = 0.f;
-      uint8_t *prow = smem + kOffP + s * kP + row * 128;
-#pragma unroll
+      // P_j for keys c..c+31 -> TMEM columns c/2 .. c/2+15, all already read
+#pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
+        float x[32];
+        ld32(sbase + c, x);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          float p0 = fast_exp2(fmaf(x[c + i], sl2, -m));
-          float p1 = fast_exp2(fmaf(x[c + i + 1], sl2, -m));
+          const float a0 = fmaf(x[i], sl2, -m), a1 = fmaf(x[i + 1], sl2, -m);
+          float p0 = fast_exp2(a0);
+          float p1 = (i & 2) ? exp2_poly(a1) : fast_exp2(a1);
           if (n_vis < BN) {
             p0 = c + i < n_vis ? p0 : 0.f;
             p1 = c + i + 1 < n_vis ? p1 : 0.f;
@@ -416,69 +432,72 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
           __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
           pk[i / 2] = *reinterpret_cast<uint32_t *>(&v2);
         }
-        // keys c .. c+31 -> atom c / 64, 16-byte chunks (c % 64) / 8 .. +3
-        uint8_t *atom = prow + (c >> 6) * kAtom;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int chunk = ((c & 63) >> 3) + q4;
-          *reinterpret_cast<uint4 *>(atom + ((chunk ^ (row & 7)) << 4)) =
-              make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-        }
+        st16(sbase + c / 2, pk);
       }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       fence_before();
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      arrive(smem_u32(&p_full[s]));
+      arrive(smem_u32(p_full));
     }
     // the whole key range is in O once the last P V has landed
-    if (!failed && nb > 0 && !pv_landed(nb - 1)) failed = true;
-    float o[HD];
     if (!failed && nb > 0) {
-#pragma unroll
-      for (int c = 0; c < HD; c += 32) ld32(obase + c, *reinterpret_cast<float(*)[32]>(o + c));
-    } else {
-#pragma unroll
-      for (int i = 0; i < HD; ++i) o[i] = 0.f;
+      const bool bad = !mbar_wait_bounded(smem_u32(pv_done), (nb - 1) & 1, kWaitLimitNs,
+                                          status) || *fail;
+      if (__any_sync(0xffffffffu, bad)) failed = true;
+      fence_after();
     }
     if (failed) *fail = 1;
-    if (valid && !*fail) {
+    const bool ok = !failed && !*fail;
+    if (__any_sync(0xffffffffu, ok && nb > 0)) {
+      // O chunks straight from TMEM to the output (warp-wide loads)
       const int q_row = row0 + qi, head = g * P.G + h;
-      if (P.n_chunks == 1) {
-        const float inv = 1.f / l;
-        bf16 *dst = out + (int64_t)q_row * ld_out + head * HD;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int64_t slot = (int64_t)blockIdx.x * 128 + row;
+#pragma unroll 1
+      for (int c = 0; c < HD; c += 32) {
+        float o[32];
+        ld32(obase + c, o);
+        if (!(valid && ok)) continue;
+        if (P.n_chunks == 1) {
+          bf16 *dst = out + (int64_t)q_row * ld_out + head * HD + c;
 #pragma unroll
-        for (int c = 0; c < HD; c += 8) {
-          uint4 pk;
-          __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&pk);
+          for (int c8 = 0; c8 < 32; c8 += 8) {
+            uint4 pk;
+            __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&pk);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            e[i] = __floats2bfloat162_rn(o[c + 2 * i] * inv, o[c + 2 * i + 1] * inv);
-          *reinterpret_cast<uint4 *>(dst + c) = pk;
+            for (int i = 0; i < 4; ++i)
+              e[i] = __floats2bfloat162_rn(o[c8 + 2 * i] * inv, o[c8 + 2 * i + 1] * inv);
+            *reinterpret_cast<uint4 *>(dst + c8) = pk;
+          }
+        } else {
+          // un-normalised partial of this key chunk
+          float4 *po = reinterpret_cast<float4 *>(part_o + slot * HD + c);
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) po[i / 4] = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
         }
-      } else {
-        // un-normalised partial of this key chunk (m = -inf, l = 0 when no
-        // key of the chunk is visible to the row)
-        const int64_t slot = (int64_t)blockIdx.x * 128 + row;
-        float4 *po = reinterpret_cast<float4 *>(part_o + slot * HD);
-#pragma unroll
-        for (int c = 0; c < HD; c += 4) po[c / 4] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
-        part_ml[slot] = make_float2(m, l);
       }
+      if (valid && ok && P.n_chunks > 1) part_ml[slot] = make_float2(m, l);
+    } else if (valid && !*fail && P.n_chunks > 1) {
+      // no key of the chunk is visible to the tile: an empty partial
+      const int64_t slot = (int64_t)blockIdx.x * 128 + row;
+      float4 *po = reinterpret_cast<float4 *>(part_o + slot * HD);
+#pragma unroll
+      for (int i = 0; i < HD; i += 4) po[i / 4] = make_float4(0.f, 0.f, 0.f, 0.f);
+      part_ml[slot] = make_float2(-INFINITY, 0.f);
     }
   }
   fence_before();
   __syncthreads();
   if (warp == 0 && lane == 0 && *fail) {
     // drain the K/V copies this CTA may still have in flight
-    for (int s = 0; s < 2; ++s) {
-      mbar_wait_bounded(smem_u32(&k_full[s]), 0, 10000000ull, nullptr);
-      mbar_wait_bounded(smem_u32(&v_full[s]), 0, 10000000ull, nullptr);
-    }
+    mbar_wait_bounded(smem_u32(k_full), 0, 10000000ull, nullptr);
+    mbar_wait_bounded(smem_u32(v_full), 0, 10000000ull, nullptr);
   }
   __syncthreads();
   if (warp == 1) {
     fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
                  : "memory");
   }
 }
@@ -581,8 +600,9 @@ static void plan_split(Params &P, const AttnReq *reqs, int n_req, int Hq, int Hk
   P.n_chunks = 1;
   P.chunk_blocks = max_nb > 0 ? max_nb : 1;
   const int sms = num_sms();
-  if (tiles > 0 && tiles < sms && max_nb > 1) {
-    int want = (2 * sms + tiles - 1) / tiles;
+  const int slots = kCtasPerSm * sms;            // CTAs resident at once
+  if (tiles > 0 && tiles < slots && max_nb > 1) {
+    int want = (2 * slots + tiles - 1) / tiles;
     if (want > max_nb) want = max_nb;
     P.chunk_blocks = (max_nb + want - 1) / want;
     P.n_chunks = (max_nb + P.chunk_blocks - 1) / P.chunk_blocks;
@@ -599,7 +619,10 @@ bool attention_tc_supported(int Hq, int Hkv, int hd) {
   return G == 1 || G == 2 || G == 4 || G == 8;
 }
 
-size_t attention_tc_ws_bound() { return (size_t)3 * attn::num_sms() * attn::kPartBytes + 256; }
+// tiles * chunks < 2 slots + tiles < 3 slots whenever the key range is split
+size_t attention_tc_ws_bound() {
+  return (size_t)3 * attn::kCtasPerSm * attn::num_sms() * attn::kPartBytes + 256;
+}
 
 size_t attention_tc_ws_bytes(const AttnReq *reqs, int n_req, int Hq, int Hkv) {
   attn::Params P;
