@@ -132,6 +132,30 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 consecutive fp32 columns of this thread's lane, without waiting: the
+// registers are valid after wait_ld(), so several loads share one latency.
+__device__ __forceinline__ void ld32_nw(uint32_t taddr, float *v) {
+  uint32_t *r = reinterpret_cast<uint32_t *>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+      "[%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+        "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Writes 32 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
@@ -269,6 +293,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
     *fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  __syncthreads();
+  const int b = s_unit[0], g = s_unit[1], t = s_unit[2], jb = s_unit[3], je = s_unit[4];
+  const int nb = je - jb;                         // key blocks of this unit
+  const AttnReq &R = P.r[b];
+  const int row0 = R.q_begin + t * P.QT;          // first q row of the tile
+  const int n_valid = min(P.QT, R.q_end - row0);  // q rows of the request in the tile
+  if (nb == 0) {
+    // a key chunk past the tile's last query: an empty partial, nothing else
+    if (P.n_chunks > 1 && threadIdx.x < 128 && (int)threadIdx.x % P.QT < n_valid)
+      part_ml[(int64_t)blockIdx.x * 128 + threadIdx.x] = make_float2(-INFINITY, 0.f);
+    return;
+  }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
@@ -280,11 +316,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int b = s_unit[0], g = s_unit[1], t = s_unit[2], jb = s_unit[3], je = s_unit[4];
-  const int nb = je - jb;                         // key blocks of this unit
-  const AttnReq &R = P.r[b];
-  const int row0 = R.q_begin + t * P.QT;          // first q row of the tile
-  const int n_valid = min(P.QT, R.q_end - row0);  // q rows of the request in the tile
 
   if (nb > 0 && warp == 0 && lane < 2) {
     // ----------------------------------------------- producers (K: lane 0, V: lane 1)
@@ -371,27 +402,29 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
       fence_after();
       const int key0 = (jb + j) * BN;
       // Keys visible to this row: key0 .. p.  Blocks wholly at or before p
-      // take the mask-free path.  Eight partial maxima / sums keep the
+      // take the mask-free path.  Four partial maxima / sums keep the
       // dependency chains short.
       const int n_vis = p - key0 + 1;               // >= BN: no masking
-      float mx[8];
+      // S_j: four loads in flight, one wait (the maximum); the P pass below
+      // reloads it in two halves
+      float mx[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        float x[32];
-        ld32(sbase + c, x);
+      for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
+      {
+        float x[BN];
+#pragma unroll
+        for (int c = 0; c < BN; c += 32) ld32_nw(sbase + c, x + c);
+        wait_ld();
         if (n_vis >= BN) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+          for (int i = 0; i < BN; ++i) mx[i & 3] = fmaxf(mx[i & 3], x[i]);
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c + i < n_vis) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+          for (int i = 0; i < BN; ++i)
+            if (i < n_vis) mx[i & 3] = fmaxf(mx[i & 3], x[i]);
         }
       }
-      const float mloc = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+      const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
       // move the reference only for a large rise; the first visible key
       // always sets it (m = -inf before)
       const bool move = mloc > m + kRescale;
@@ -410,32 +443,37 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
         l *= corr;
       }
       if (move) m = mloc;
-      float ls[8];
+      float ls[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ls[i] = 0.f;
-      // P_j for keys c..c+31 -> TMEM columns c/2 .. c/2+15, all already read
-#pragma unroll 1
+      for (int i = 0; i < 4; ++i) ls[i] = 0.f;
+      float x[BN];
+      // P_j for keys c..c+31 -> TMEM columns c/2 .. c/2+15; the first half of
+      // S_j is in registers before P overwrites any of it
+#pragma unroll
       for (int c = 0; c < BN; c += 32) {
-        float x[32];
-        ld32(sbase + c, x);
+        if ((c & 63) == 0) {
+          ld32_nw(sbase + c, x + c);
+          ld32_nw(sbase + c + 32, x + c + 32);
+          wait_ld();
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float a0 = fmaf(x[i], sl2, -m), a1 = fmaf(x[i + 1], sl2, -m);
+          const float a0 = fmaf(x[c + i], sl2, -m), a1 = fmaf(x[c + i + 1], sl2, -m);
           float p0 = fast_exp2(a0);
           float p1 = (i & 2) ? exp2_poly(a1) : fast_exp2(a1);
           if (n_vis < BN) {
             p0 = c + i < n_vis ? p0 : 0.f;
             p1 = c + i + 1 < n_vis ? p1 : 0.f;
           }
-          ls[(i >> 1) & 7] += p0 + p1;
+          ls[(i >> 1) & 3] += p0 + p1;
           __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
           pk[i / 2] = *reinterpret_cast<uint32_t *>(&v2);
         }
         st16(sbase + c / 2, pk);
       }
-      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      wait_st();
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       fence_before();
       arrive(smem_u32(p_full));
     }
@@ -477,13 +515,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
         }
       }
       if (valid && ok && P.n_chunks > 1) part_ml[slot] = make_float2(m, l);
-    } else if (valid && !*fail && P.n_chunks > 1) {
-      // no key of the chunk is visible to the tile: an empty partial
-      const int64_t slot = (int64_t)blockIdx.x * 128 + row;
-      float4 *po = reinterpret_cast<float4 *>(part_o + slot * HD);
-#pragma unroll
-      for (int i = 0; i < HD; i += 4) po[i / 4] = make_float4(0.f, 0.f, 0.f, 0.f);
-      part_ml[slot] = make_float2(-INFINITY, 0.f);
     }
   }
   fence_before();

@@ -330,27 +330,17 @@ lm_head_kernel(const float *__restrict__ x, int B, const T *__restrict__ E,
   unsigned long long mine[CB_MAX_BATCH > 8 ? 8 : CB_MAX_BATCH];
   const int bl = B < 8 ? B : 8;
   for (int b = 0; b < bl; ++b) mine[b] = 0ull;
-  constexpr int U = 4;            // 16-byte loads in flight per lane
   for (int v = gw; v < vocab; v += nw) {
     const T *row = E + (int64_t)v * d;
     float acc[8];
     for (int b = 0; b < bl; ++b) acc[b] = 0.f;
-    for (int c0 = lane * VEC; c0 < d; c0 += U * 32 * VEC) {
-      float e[U][VEC];
+    for (int c = lane * VEC; c < d; c += 32 * VEC) {
+      float e[VEC];
+      load16<T>(row + c, e);
+      for (int b = 0; b < bl; ++b) {
+        const float *xb = xs + b * d + c;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int c = c0 + u * 32 * VEC;
-        if (c < d) load16<T>(row + c, e[u]);
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int c = c0 + u * 32 * VEC;
-        if (c >= d) break;
-        for (int b = 0; b < bl; ++b) {
-          const float *xb = xs + b * d + c;
-#pragma unroll
-          for (int j = 0; j < VEC; ++j) acc[b] = fmaf(e[u][j], xb[j], acc[b]);
-        }
+        for (int j = 0; j < VEC; ++j) acc[b] = fmaf(e[j], xb[j], acc[b]);
       }
     }
     for (int b = 0; b < bl; ++b) {
