@@ -43,7 +43,7 @@ import numpy as np
 __all__ = [
     "Model", "model_from_weights", "rope_inv_freq", "rope_rotate",
     "reposition_keys", "stitch", "rms_norm", "silu", "causal_attention",
-    "qkv_rows", "decoder_layer", "full_prefill", "chunk_prefill", "kv_deviation",
+    "qkv_rows", "kv_rows", "decoder_layer", "full_prefill", "chunk_prefill", "kv_deviation",
     "select_count", "token_topk", "doc_aligned_select", "blend_prefill",
     "first_token", "first_token_logits", "embed_rows", "kv_bytes_per_layer",
     "selection_segments", "captured_deviation",
@@ -200,6 +200,19 @@ def qkv_rows(m: Model, l: int, h_rows, pos_rows):
     q = rope_rotate(q, pos_rows, m.rope_base)
     k = rope_rotate(k, pos_rows, m.rope_base)
     return q, k.reshape(n, Hkv * hd), v.reshape(n, Hkv * hd)
+
+
+def kv_rows(m: Model, l: int, h_rows, pos_rows):
+    """The cache rows of layer l alone: x = RMSNorm(h; norm1), k = x W_k^T
+    rotated at the rows' positions and v = x W_v^T ([n, Hkv*hd] each)."""
+    L = m.layers[l]
+    n = h_rows.shape[0]
+    Hq, Hkv, hd = m.n_q_heads, m.n_kv_heads, m.head_dim
+    x = rms_norm(h_rows, L["norm1"], m.norm_eps)
+    k = x @ L["w_qkv"][Hq * hd:(Hq + Hkv) * hd].T
+    v = x @ L["w_qkv"][(Hq + Hkv) * hd:].T
+    k = rope_rotate(k.reshape(n, Hkv, hd), pos_rows, m.rope_base)
+    return k.reshape(n, Hkv * hd), v
 
 
 def decoder_layer(m: Model, l: int, h_rows, pos_rows, K_cache, V_cache,

@@ -121,6 +121,20 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
                : "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic
+// stream serialization may start while the previous kernel of the stream is
+// still running.  It does only shared-memory / TMEM setup before
+// grid_dep_wait(), which returns once the previous grid has completed and
+// its writes are visible; it then calls grid_dep_launch() so that the next
+// kernel may start its own setup.  The next grid is scheduled only after
+// every CTA of this grid has called grid_dep_launch() or exited.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Default limit for pipeline waits: two seconds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "cacheblend.h"
 
 namespace cb {
@@ -35,6 +37,25 @@ void note_launches(int n);
 inline cudaError_t launched(int n) {
   note_launches(n);
   return cudaGetLastError();
+}
+
+// Launches a kernel that follows the grid_dep_wait / grid_dep_launch
+// protocol with programmatic stream serialization, so its setup overlaps
+// the end of the previous kernel on the stream.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // ----------------------------------------------------------------- RoPE --

@@ -269,6 +269,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   __shared__ int s_unit[6];        // b, g, tile, first block, end block
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dep_wait();      // q, the cache and q_pos come from earlier kernels
+  grid_dep_launch();
   if (threadIdx.x == 0) {
     const int tile = blockIdx.x / P.n_chunks, chunk = blockIdx.x % P.n_chunks;
     const TileId id = decode_tile(P, tile);
@@ -539,6 +541,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
 __global__ void __launch_bounds__(256)
 attn_combine_kernel(const __grid_constant__ Params P, const float *__restrict__ part_o,
                     const float2 *__restrict__ part_ml, bf16 *__restrict__ out, int64_t ld_out) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int tile = blockIdx.x / 16;
   const int row = (blockIdx.x % 16) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -699,11 +703,15 @@ cudaError_t launch_attention_tc(const void *q, int64_t ld_q, const int32_t *q_po
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  attn_tc_kernel<<<tiles * P.n_chunks, kThreads, kSmem, s>>>(
-      mq, mk, mv, P, q_pos, reinterpret_cast<bf16 *>(out), ld_out, part_o, part_ml, status);
+  cudaError_t e = launch_pdl(attn_tc_kernel, dim3(tiles * P.n_chunks), dim3(kThreads), kSmem, s,
+                             mq, mk, mv, P, q_pos, reinterpret_cast<bf16 *>(out), ld_out, part_o,
+                             part_ml, status);
+  if (e != cudaSuccess) return e;
   if (P.n_chunks == 1) return launched(1);
-  attn_combine_kernel<<<tiles * 16, 256, 0, s>>>(P, part_o, part_ml,
-                                                 reinterpret_cast<bf16 *>(out), ld_out);
+  e = launch_pdl(attn_combine_kernel, dim3(tiles * 16), dim3(256), 0, s, P,
+                 (const float *)part_o, (const float2 *)part_ml, reinterpret_cast<bf16 *>(out),
+                 ld_out);
+  if (e != cudaSuccess) return e;
   return launched(2);
 }
 

@@ -148,6 +148,8 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
   if (CG == 2) cluster_sync();   // the peer's barriers exist before any remote use
   fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();      // inputs of the previous kernel are visible from here
+  grid_dep_launch();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -451,20 +453,24 @@ static cudaError_t run(const CUtensorMap &mx, const CUtensorMap &mw, const CUten
     units = tiles < max_units ? (int)tiles : max_units;
   }
   if (CG == 1) {
-    gemm_sab_kernel<EPI, 1><<<units, kThreads, smem, s>>>(mx, mw, mw2, p, status);
+    cudaError_t e = launch_pdl(gemm_sab_kernel<EPI, 1>, dim3(units), dim3(kThreads), smem, s, mx,
+                               mw, mw2, p, status);
+    if (e != cudaSuccess) return e;
   } else {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * units, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 2;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_sab_kernel<EPI, 2>, mx, mw, mw2, p, status);
     if (e != cudaSuccess) return e;
   }

@@ -245,6 +245,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dep_wait();      // inputs of the previous kernel are visible from here
+  grid_dep_launch();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -527,8 +529,9 @@ static cudaError_t run(const CUtensorMap &ma, const CUtensorMap &mb, const CUten
   const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + C::kOutN - 1) / C::kOutN);
   const int64_t work = stream_k ? tiles * ((K + BK - 1) / BK) : tiles;
   const int grid = work < num_sms() ? (int)work : num_sms();
-  gemm_tc_kernel<BN, EPI><<<grid, kThreads, C::kSmem, s>>>(ma, mb, mb2, M, N, K,
-                                                           stream_k ? 1 : 0, ep, status);
+  cudaError_t e = launch_pdl(gemm_tc_kernel<BN, EPI>, dim3(grid), dim3(kThreads), C::kSmem, s,
+                             ma, mb, mb2, M, N, K, stream_k ? 1 : 0, ep, status);
+  if (e != cudaSuccess) return e;
   return launched(1);
 }
 

@@ -87,6 +87,8 @@ rmsnorm_kernel(const float *__restrict__ h, int64_t ld_h,
                const float *__restrict__ gain, float eps, T *__restrict__ out,
                int64_t ld_out) {
   __shared__ float red[2][4];
+  grid_dep_wait();
+  grid_dep_launch();
   const int sub = threadIdx.x >> 7, t = threadIdx.x & 127;
   const int i = blockIdx.x * 2 + sub;
   const bool ok = i < n;
@@ -139,12 +141,14 @@ cudaError_t launch_rmsnorm(const float *h, int64_t ld_h, const int32_t *src_rows
   if (n == 0) return cudaSuccess;
   if (d > kNormMaxD) return cudaErrorInvalidValue;
   const int blocks = (n + 1) / 2;
+  cudaError_t e;
   if (out_dt == CB_BF16)
-    rmsnorm_kernel<bf16><<<blocks, 256, 0, s>>>(h, ld_h, src_rows, n, d, gain, eps,
-                                                reinterpret_cast<bf16 *>(out), ld_out);
+    e = launch_pdl(rmsnorm_kernel<bf16>, dim3(blocks), dim3(256), 0, s, h, ld_h, src_rows, n, d,
+                   gain, eps, reinterpret_cast<bf16 *>(out), ld_out);
   else
-    rmsnorm_kernel<float><<<blocks, 256, 0, s>>>(h, ld_h, src_rows, n, d, gain, eps,
-                                                 reinterpret_cast<float *>(out), ld_out);
+    e = launch_pdl(rmsnorm_kernel<float>, dim3(blocks), dim3(256), 0, s, h, ld_h, src_rows, n, d,
+                   gain, eps, reinterpret_cast<float *>(out), ld_out);
+  if (e != cudaSuccess) return e;
   return launched(1);
 }
 

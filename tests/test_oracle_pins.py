@@ -12,6 +12,7 @@ import torch
 import torch.nn.functional as F
 
 import oracle as O
+import workload as W
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -369,3 +370,15 @@ def test_captured_deviation_by_hand():
     assert O.captured_deviation([0, 1, 2, 3], d) == 1.0
     assert O.captured_deviation([3], d) == 0.4
     assert O.captured_deviation([], d) == 0.0
+
+
+def test_kv_rows_is_the_cache_part_of_the_projection():
+    """kv_rows gives the k and v of qkv_rows (the same definition without
+    the query heads): checked against the fused projection on random rows."""
+    shape = W.ModelShape("t", 1, 48, 4, 2, 12, 40, 97, dtype="f32")
+    m = O.model_from_weights(shape, W.make_weights(shape, 3, std=0.2))
+    h = np.random.default_rng(1).standard_normal((9, 48))
+    pos = np.array([0, 1, 5, 7, 30, 31, 100, 101, 4000])
+    _, k, v = O.qkv_rows(m, 0, h, pos)
+    k2, v2 = O.kv_rows(m, 0, h, pos)
+    assert np.allclose(k, k2, rtol=0, atol=1e-12) and np.allclose(v, v2, rtol=0, atol=1e-12)
