@@ -52,9 +52,11 @@ def parse_args():
                          "(for ncu --profile-from-start off); prints no JSON")
     ap.add_argument("--layers", type=int, default=None,
                     help="truncate the stack (profiling captures on a small footprint)")
-    ap.add_argument("--workload", choices=["rag", "rolling"], default="rag",
+    ap.add_argument("--workload", choices=["rag", "rolling", "qwen", "long"], default="rag",
                     help="rag: the headline request (default); rolling: the 50-request "
-                         "rolling-agent window, token top-k vs document-aligned at 5%%")
+                         "rolling-agent window, token top-k vs document-aligned at 5%%; "
+                         "qwen: the Qwen3-8B-shaped batch of 4 at 30%%; long: the 32K "
+                         "batch of 2 at r = 5/10/20/30%% against full prefill")
     return ap.parse_args()
 
 
@@ -602,12 +604,112 @@ def run_rolling(args):
     print(json.dumps(line), flush=True)
 
 
+# -------------------------------------------------- batched workloads --
+def _graph_ms(fn, steps, st):
+    """Median device time of `fn` replayed from a CUDA graph (3 warm-ups)."""
+    import torch
+    fn()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    per = []
+    for _ in range(steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        g.replay()
+        e1.record(st)
+        torch.cuda.synchronize()
+        per.append(e0.elapsed_time(e1))
+    del g
+    return statistics.median(per), float(np.percentile(per, 95))
+
+
+def run_batch(args):
+    """Secondary workloads, one JSON line each (not the headline metric):
+    qwen: 4 requests x (10 of a 40-chunk pool x 1024 + 128), Qwen3-8B shape,
+    r = 30%; long: 2 x (32 x 1024 + 256), Llama-3-8B shape, r = 5/10/20/30%.
+    TTFT is one cb_blend_prefill call for the whole batch (graph replay);
+    full prefill of the same batch gives the speedup, and the probe gives the
+    attention time (n_sel x L for the blend, L x L for full prefill)."""
+    import torch
+    import rag_kv_cache_layer_gb300 as R
+    from rag_kv_cache_layer_gb300 import _lib as L
+
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(device)
+    wl = W.qwen_pool(n_layers=args.layers) if args.workload == "qwen" else \
+        W.long_context(n_layers=args.layers)
+    shape = wl.model
+    max_pos = max(rq.n_tokens for rq in wl.requests) + 16
+    model = R.BlendModel(shape, W.make_weights_device(shape, 2345, device), max_pos, device)
+    cached = {}
+    for rq in wl.requests:
+        for sg in rq.segments:
+            if sg.cached:
+                cached[sg.chunk_id] = sg.tokens
+    store = R.ChunkStore(model, sum(len(t) for t in cached.values()))
+    store.prefill({c: torch.from_numpy(t).to(device) for c, t in cached.items()})
+    reqs = [R.Req(torch.from_numpy(rq.tokens).to(device),
+                  [store.seg(sg.chunk_id) if sg.cached else R.Seg(len(sg.tokens))
+                   for sg in rq.segments]) for rq in wl.requests]
+    st = torch.cuda.current_stream()
+    T = sum(rq.n_tokens for rq in wl.requests)
+    n_layers = shape.n_layers
+
+    def attn_us(fn):
+        n, ms = probe_steps(L, L.CB_PROBE_ATTENTION, n_layers,
+                            lambda: (fn(), torch.cuda.synchronize()))
+        return ms * 1e3
+
+    full_outs = model.alloc_outputs(model.plan(reqs), len(reqs), blend=False)
+    full_fn = lambda: model.cb_full_prefill(reqs, outputs=full_outs)
+    full_ms, _ = _graph_ms(full_fn, args.steps, st)
+    full_attn = attn_us(full_fn)
+    del full_outs
+    torch.cuda.empty_cache()
+    ratios = [wl.ratio_bp] if args.workload == "qwen" else [500, 1000, 2000, 3000]
+    rows = {}
+    for r in ratios:
+        outs = model.alloc_outputs(model.plan(reqs, r), len(reqs))
+        fn = lambda: model.cb_blend_prefill(reqs, r, outputs=outs)
+        med, p95 = _graph_ms(fn, args.steps, st)
+        rows[f"r={r / 100:g}%"] = {"ttft_ms_median": med, "ttft_ms_p95": p95,
+                                   "context_tokens_per_s": T / (med / 1e3),
+                                   "speedup_vs_full_prefill": full_ms / med,
+                                   "attention_us_per_call": attn_us(fn)}
+        del outs
+        torch.cuda.empty_cache()
+    if R.device_status() != 0:
+        raise RuntimeError("device status set during the batched workload")
+    name = ("qwen3-8b-shape 36L, 4 requests x (10 of a 40-chunk pool x 1024 + 128), r=30%"
+            if args.workload == "qwen" else
+            "llama3-8b-shape 32L, 2 requests x (32 x 1024 + 256), r = 5/10/20/30%")
+    key = rows[f"r={ratios[0] / 100:g}%"]
+    line = {"metric": "blended-prefill context tokens/s and TTFT (batched workload)",
+            "value": key["context_tokens_per_s"], "unit": "tokens/s",
+            "higher_is_better": True, "n_gpus": 1, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": name, "global_batch": len(reqs), "seq_len": T,
+                       "steps": args.steps},
+            "full_prefill_ms": full_ms, "full_prefill_attention_us": full_attn,
+            "ratios": rows,
+            "context": "pages: CacheBlend 2.2-3.3x TTFT, QCFuse 1.7x prefill over full "
+                       "prefill (their hardware)"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
     elif args.workload == "rolling":
         run_rolling(args)
+    elif args.workload in ("qwen", "long"):
+        run_batch(args)
     else:
         run_ours(args)
 
