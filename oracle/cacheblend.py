@@ -46,7 +46,8 @@ __all__ = [
     "qkv_rows", "kv_rows", "decoder_layer", "full_prefill", "chunk_prefill", "kv_deviation",
     "select_count", "token_topk", "doc_aligned_select", "blend_prefill",
     "first_token", "first_token_logits", "embed_rows", "kv_bytes_per_layer",
-    "selection_segments", "captured_deviation",
+    "selection_segments", "captured_deviation", "single_window_select",
+    "fixed_chunk_offsets", "first_tokens_select",
     "BlendResult", "PrefillResult",
 ]
 
@@ -323,7 +324,7 @@ def token_topk(d: np.ndarray, k: int) -> np.ndarray:
     return np.array(sorted(order[:k]), dtype=np.int64)
 
 
-def doc_aligned_select(d: np.ndarray, span_offsets, k: int) -> np.ndarray:
+def doc_aligned_select(d: np.ndarray, span_offsets, k: int, order=None) -> np.ndarray:
     """Document-aligned recomputation ("Request Order Matters" §2.3).
 
     Spans S_j = [span_offsets[j], span_offsets[j+1]).  rho_j is the mean
@@ -332,13 +333,22 @@ def doc_aligned_select(d: np.ndarray, span_offsets, k: int) -> np.ndarray:
     at the first span that does not fit, the contiguous window of the
     remaining length with the largest total deviation inside that span is
     taken (ties: leftmost) and selection stops.  Exactly k tokens.  Empty
-    spans are skipped.  Sums are float64."""
+    spans are skipped.  Sums are float64.
+
+    order: optional visiting order (a permutation of the span indices) that
+    replaces the ranking by rho_j -- the random-document control of §2.3,
+    whose random order is drawn by the caller."""
     offs = list(span_offsets)
-    spans = [(offs[j], offs[j + 1]) for j in range(len(offs) - 1)
-             if offs[j + 1] > offs[j]]
-    idx = [j for j in range(len(spans))]
-    rho = [float(np.sum(d[a:b], dtype=np.float64)) / (b - a) for a, b in spans]
-    idx.sort(key=lambda j: (-rho[j], j))
+    m = len(offs) - 1
+    rho = [float(np.sum(d[offs[j]:offs[j + 1]], dtype=np.float64)) / (offs[j + 1] - offs[j])
+           if offs[j + 1] > offs[j] else 0.0 for j in range(m)]
+    if order is None:
+        idx = sorted(range(m), key=lambda j: (-rho[j], j))
+    else:
+        idx = [int(j) for j in order]
+        assert sorted(idx) == list(range(m)), "order must be a permutation of the spans"
+    idx = [j for j in idx if offs[j + 1] > offs[j]]
+    spans = [(offs[j], offs[j + 1]) for j in range(m)]
     rem = k
     chosen = []
     for j in idx:
@@ -358,6 +368,58 @@ def doc_aligned_select(d: np.ndarray, span_offsets, k: int) -> np.ndarray:
         rem = 0
         break
     return np.array(sorted(chosen), dtype=np.int64)
+
+
+def single_window_select(d: np.ndarray, k: int) -> np.ndarray:
+    """Single-window control ("Request Order Matters" §2.3): the contiguous
+    k-token window of the reusable tokens with the largest total deviation
+    (ties: leftmost).  Sums are float64."""
+    n = len(d)
+    if k <= 0:
+        return np.zeros(0, dtype=np.int64)
+    if k >= n:
+        return np.arange(n, dtype=np.int64)
+    best, best_s = 0, -math.inf
+    for t in range(n - k + 1):
+        tot = float(np.sum(d[t:t + k], dtype=np.float64))
+        if tot > best_s:
+            best, best_s = t, tot
+    return np.arange(best, best + k, dtype=np.int64)
+
+
+def fixed_chunk_offsets(n: int, span_len: int, offset: int):
+    """Fixed-chunk spans ("Request Order Matters" §2.3, §4.4): equal spans of
+    span_len tokens over the reusable prompt, shifted by `offset` so that
+    they cross document boundaries; the first span is [0, offset) and the
+    last one is cut at n."""
+    offs = [0]
+    if 0 < offset < n:
+        offs.append(offset)
+    while offs[-1] < n:
+        offs.append(min(n, offs[-1] + span_len))
+    return offs
+
+
+def first_tokens_select(span_offsets, k: int) -> np.ndarray:
+    """Chunk-boundary rule of EPIC's LegoLink (as the QCFuse page describes
+    it, §2): a fixed number of the first tokens of every chunk.  The budget
+    k is shared out evenly over the non-empty chunks, the first k mod m
+    chunks taking one more; a chunk shorter than its share gives the rest
+    to the following chunks in order.  Exactly min(k, N) tokens."""
+    offs = list(span_offsets)
+    spans = [(offs[j], offs[j + 1]) for j in range(len(offs) - 1) if offs[j + 1] > offs[j]]
+    m = len(spans)
+    if m == 0 or k <= 0:
+        return np.zeros(0, dtype=np.int64)
+    quota = [k // m + (1 if j < k % m else 0) for j in range(m)]
+    take = [min(q, b - a) for q, (a, b) in zip(quota, spans)]
+    left = k - sum(take)
+    for j, (a, b) in enumerate(spans):
+        extra = min(left, (b - a) - take[j])
+        take[j] += extra
+        left -= extra
+    chosen = [i for (a, b), t in zip(spans, take) for i in range(a, a + t)]
+    return np.array(chosen, dtype=np.int64)
 
 
 # --------------------------------------------------------------------------
@@ -380,6 +442,7 @@ class BlendResult:
 
 def blend_prefill(m: Model, segments, store, ratio_bp: int,
                   policy: str = "token_topk", sel_layer: int = 1,
+                  span_len: int = 0, span_offset: int = -1, span_order=None,
                   forced=None, schedule=None) -> BlendResult:
     """Selective KV recomputation over a partially reused cache (QCFuse
     §2.1.3 Eqs. 6-7; CacheBlend blog ``blend_layer``; LMCache flow of
@@ -393,6 +456,11 @@ def blend_prefill(m: Model, segments, store, ratio_bp: int,
     forced:   if given, the selected context positions P (ascending) are
       taken from it instead of being ranked (the "forced" mode used for bf16
       parity, where ranking near the k-th deviation is precision dependent).
+    policy:   "token_topk" (Eq. 2), "doc_aligned" (Eq. 3), or the §2.3 / §4.4
+      controls "single_window", "fixed_chunk" (span_len tokens, default the
+      median document length, shifted by span_offset, default half a span),
+      "random_doc" (document spans in the order span_order), and
+      "first_tokens" (EPIC's chunk-boundary rule).
     schedule: optional gradual filtering (CacheBlend blog select_hkvd):
       list of (layer, keep_count) with layer > sel_layer; at that layer the
       current P is re-ranked by the deviation of its fresh keys and only
@@ -470,6 +538,18 @@ def blend_prefill(m: Model, segments, store, ratio_bp: int,
         elif policy == "doc_aligned":
             offs = np.concatenate([[0], np.cumsum(lens)])
             P = doc_aligned_select(d, offs, k)
+        elif policy == "random_doc":
+            offs = np.concatenate([[0], np.cumsum(lens)])
+            P = doc_aligned_select(d, offs, k, order=span_order)
+        elif policy == "single_window":
+            P = single_window_select(d, k)
+        elif policy == "fixed_chunk":
+            L_ = span_len if span_len > 0 else int(np.median(lens))
+            o_ = span_offset if span_offset >= 0 else L_ // 2
+            P = doc_aligned_select(d, fixed_chunk_offsets(N, L_, o_), k)
+        elif policy == "first_tokens":
+            offs = np.concatenate([[0], np.cumsum(lens)])
+            P = first_tokens_select(offs, k)
         else:
             raise ValueError(policy)
         sched = dict(schedule or [])

@@ -382,3 +382,52 @@ def test_kv_rows_is_the_cache_part_of_the_projection():
     _, k, v = O.qkv_rows(m, 0, h, pos)
     k2, v2 = O.kv_rows(m, 0, h, pos)
     assert np.allclose(k, k2, rtol=0, atol=1e-12) and np.allclose(v, v2, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------- span-policy controls --
+def test_single_window_is_doc_aligned_over_one_span():
+    """"Request Order Matters" §2.3: single-window is the k-token window of
+    largest total deviation -- the document-aligned rule with the whole
+    reusable prompt as its only span (k < N takes the window fill)."""
+    rng = np.random.default_rng(5)
+    for n in range(1, 12):
+        for k in range(0, n):
+            d = rng.integers(0, 4, size=n).astype(np.float64)     # ties included
+            assert list(O.single_window_select(d, k)) == list(O.doc_aligned_select(d, [0, n], k))
+    assert list(O.single_window_select(np.array([1., 5., 1., 5., 1.]), 2)) == [0, 1]   # leftmost
+    assert list(O.single_window_select(np.array([0., 0., 3., 4., 0.]), 2)) == [2, 3]
+    assert list(O.single_window_select(np.array([1., 2.]), 5)) == [0, 1]
+
+
+def test_fixed_chunk_offsets_by_hand():
+    """Same page §4.4: equal spans shifted so they cross document boundaries."""
+    assert O.fixed_chunk_offsets(10, 4, 2) == [0, 2, 6, 10]
+    assert O.fixed_chunk_offsets(10, 4, 0) == [0, 4, 8, 10]
+    assert O.fixed_chunk_offsets(8, 4, 4) == [0, 4, 8]
+    assert O.fixed_chunk_offsets(3, 4, 2) == [0, 2, 3]
+
+
+def test_random_document_order_by_hand():
+    """Same page §2.3: random-document keeps the document spans and the fill
+    rule but visits spans in a caller-drawn order.  d = 1,1,1 | 5,5,5 |
+    2,2,2 with k = 4: visiting (0, 2, 1) takes span 0 whole, then one token
+    of span 2 (all equal: leftmost); ranking by mean takes span 1, then
+    span 2's first token."""
+    d = np.array([1., 1., 1., 5., 5., 5., 2., 2., 2.])
+    offs = [0, 3, 6, 9]
+    assert list(O.doc_aligned_select(d, offs, 4, order=[0, 2, 1])) == [0, 1, 2, 6]
+    assert list(O.doc_aligned_select(d, offs, 4)) == [3, 4, 5, 6]
+    # the mean ranking given explicitly reproduces the default
+    assert list(O.doc_aligned_select(d, offs, 4, order=[1, 2, 0])) == [3, 4, 5, 6]
+
+
+def test_first_tokens_by_hand():
+    """EPIC's chunk-boundary rule as the QCFuse page describes it (§2): the
+    first tokens of every chunk.  Chunks of 5, 4, 6 tokens with k = 7 share
+    3, 2, 2; chunks of 2 and 8 with k = 6 share 3, 3, and the short first
+    chunk hands its missing token to the second."""
+    assert list(O.first_tokens_select([0, 5, 9, 15], 7)) == [0, 1, 2, 5, 6, 9, 10]
+    assert list(O.first_tokens_select([0, 2, 10], 6)) == [0, 1, 2, 3, 4, 5]
+    assert list(O.first_tokens_select([0, 3, 3, 6], 2)) == [0, 3]          # empty span skipped
+    assert list(O.first_tokens_select([0, 4], 9)) == [0, 1, 2, 3]          # k > N
+    assert len(O.first_tokens_select([0, 400, 800, 1200], 60)) == 60
