@@ -542,6 +542,9 @@ def run_rolling(args):
     queries = [dev(rq.segments[-1].tokens) for rq in wl.requests]
     result = {}
     for name, policy in (("token_topk", L.CB_POLICY_TOKEN_TOPK),
+                         ("single_window", L.CB_POLICY_SINGLE_WINDOW),
+                         ("fixed_chunk", L.CB_POLICY_FIXED_CHUNK),
+                         ("random_doc", L.CB_POLICY_RANDOM_DOC),
                          ("doc_aligned", L.CB_POLICY_DOC_ALIGNED)):
         rw = R.RollingWindow(model, window, doc_len, wl.ratio_bp, policy)
         rw.seed({i: docs[i] for i in range(window - 1)})
@@ -551,18 +554,21 @@ def run_rolling(args):
             k = t - args.warmup if t >= args.warmup else 0
             new_id = k + window - 1
             req = rw.request(docs[new_id], queries[k])
+            # random-document: a seeded order of the window's cached documents
+            kw = ({"span_order": np.random.default_rng(100 + k).permutation(window - 1).tolist()}
+                  if policy == L.CB_POLICY_RANDOM_DOC else {})
             if outs is None:
-                outs = model.alloc_outputs(model.plan([req], wl.ratio_bp, policy), 1)
+                outs = model.alloc_outputs(model.plan([req], wl.ratio_bp, policy, **kw), 1)
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(st)
-            rw.blend(req, outputs=outs)
+            rw.blend(req, outputs=outs, **kw)
             e1.record(st)
             torch.cuda.synchronize()
             if t < args.warmup:
                 continue                       # warm-ups replay request 0's window
             ttft.append(e0.elapsed_time(e1))
-            plan = model.plan([req], wl.ratio_bp, policy)
+            plan = model.plan([req], wl.ratio_bp, policy, **kw)
             n_ctx, kk = int(plan.N_total), int(plan.K_total)
             sg, cp = R.selection_stats(outs["selected"][:kk], outs["deviation"][:n_ctx])
             segs.append(sg)
@@ -585,7 +591,7 @@ def run_rolling(args):
             result["full_prefill_ttft_ms_median"] = statistics.median(fulls)
     T = len(wl.requests[0].tokens)
     full = result.get("full_prefill_ttft_ms_median")
-    for name in ("token_topk", "doc_aligned"):
+    for name in ("token_topk", "single_window", "fixed_chunk", "random_doc", "doc_aligned"):
         r = result[name]
         r["tokens_per_s"] = T / (r["ttft_ms_median"] / 1e3)
         if full:

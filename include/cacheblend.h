@@ -70,8 +70,21 @@ typedef enum { CB_F32 = 0, CB_BF16 = 1 } cb_dtype;
 
 typedef enum {
   CB_POLICY_TOKEN_TOPK = 0,   /* [ROM] §2.2: the k largest deviations       */
-  CB_POLICY_DOC_ALIGNED = 1   /* [ROM] §2.3: whole spans by mean deviation,
+  CB_POLICY_DOC_ALIGNED = 1,  /* [ROM] §2.3: whole spans by mean deviation,
                                  then the best window of the remainder      */
+  CB_POLICY_SINGLE_WINDOW = 2,/* [ROM] §2.3: the k-token window of largest
+                                 total deviation over all reusable tokens   */
+  CB_POLICY_FIXED_CHUNK = 3,  /* [ROM] §2.3, §4.4: equal spans of span_len
+                                 tokens shifted by span_offset (they cross
+                                 document boundaries), ranked and filled as
+                                 DOC_ALIGNED                                 */
+  CB_POLICY_RANDOM_DOC = 4,   /* [ROM] §2.3: document spans visited in the
+                                 caller's span_order (its random draw),
+                                 filled as DOC_ALIGNED                       */
+  CB_POLICY_FIRST_TOKENS = 5  /* [QCF] §2 (EPIC's chunk-boundary rule): the
+                                 first tokens of every span, k shared out
+                                 evenly (the first k mod m spans one more; a
+                                 short span passes its surplus on in order)  */
 } cb_policy;
 
 /* Largest batch of requests one call accepts. */
@@ -204,9 +217,15 @@ typedef struct {
   int64_t reused_row0;       /* row of context token 0 in k_reused           */
   int dev_offset;            /* first entry of this request in dev_out       */
   int idx_offset;            /* first entry of this request in idx_out       */
-  int n_spans;               /* CB_POLICY_DOC_ALIGNED: number of spans       */
+  int n_spans;               /* DOC_ALIGNED, RANDOM_DOC, FIRST_TOKENS: number
+                                of spans (documents / chunks)                */
   const int32_t *span_offsets; /* host [n_spans + 1], ascending, from 0 to
                                   n_ctx: span j = [off[j], off[j+1])         */
+  const int32_t *span_order; /* RANDOM_DOC: host [n_spans], a permutation of
+                                the spans, first visited first               */
+  int span_len;              /* FIXED_CHUNK: span length (> 0)              */
+  int span_offset;           /* FIXED_CHUNK: the first span is [0, offset),
+                                0 <= span_offset <= span_len                */
 } cb_select_req;
 
 /* Deviation and selection ([ROM] §2.2 Eqs. 1-2, §2.3 Eq. 3; [CB]
@@ -220,7 +239,11 @@ typedef struct {
  *                            whole spans while they fit, then the window of
  *                            the remaining length with the largest total d
  *                            (ties: leftmost) in the first span that does
- *                            not fit; span sums are accumulated in double.
+ *                            not fit; span sums are accumulated in double;
+ *   CB_POLICY_SINGLE_WINDOW, _FIXED_CHUNK, _RANDOM_DOC, _FIRST_TOKENS -- the
+ *                            controls of the enum above (spans from
+ *                            span_len / span_offset for FIXED_CHUNK, one
+ *                            span [0, n_ctx) for SINGLE_WINDOW).
  * The selected context indices are written ascending to
  * idx_out[idx_offset .. idx_offset + k).
  * k_fresh, k_reused: device [rows][ld] of dtype.  dev_out: device float.
@@ -411,6 +434,12 @@ typedef struct {
   int n_schedule;      /* gradual filtering steps ([CB] select_hkvd), 0 = a
                           single selection reused by every later layer     */
   const cb_schedule_step *schedule;   /* host [n_schedule], layers ascending */
+  int span_len;        /* FIXED_CHUNK: span length; 0 = the median length
+                          of the request's cached segments, shifted by half
+                          a span (the spans then straddle documents)        */
+  int span_offset;     /* FIXED_CHUNK with span_len > 0: first span [0, off) */
+  const int32_t *span_order;  /* RANDOM_DOC: host, per request in order, a
+                          permutation of its cached segments                */
   const int32_t *forced_selected;     /* device [K_total] or NULL: use these
                           request-local context positions (ascending per
                           request, k_b of them) instead of ranking d; d is

@@ -442,7 +442,7 @@ class BlendResult:
 
 def blend_prefill(m: Model, segments, store, ratio_bp: int,
                   policy: str = "token_topk", sel_layer: int = 1,
-                  span_len: int = 0, span_offset: int = -1, span_order=None,
+                  span_len: int = 0, span_offset: int = 0, span_order=None,
                   forced=None, schedule=None) -> BlendResult:
     """Selective KV recomputation over a partially reused cache (QCFuse
     §2.1.3 Eqs. 6-7; CacheBlend blog ``blend_layer``; LMCache flow of
@@ -457,8 +457,9 @@ def blend_prefill(m: Model, segments, store, ratio_bp: int,
       taken from it instead of being ranked (the "forced" mode used for bf16
       parity, where ranking near the k-th deviation is precision dependent).
     policy:   "token_topk" (Eq. 2), "doc_aligned" (Eq. 3), or the §2.3 / §4.4
-      controls "single_window", "fixed_chunk" (span_len tokens, default the
-      median document length, shifted by span_offset, default half a span),
+      controls "single_window", "fixed_chunk" (span_len tokens shifted by
+      span_offset; span_len 0 means the median document length shifted by
+      half a span),
       "random_doc" (document spans in the order span_order), and
       "first_tokens" (EPIC's chunk-boundary rule).
     schedule: optional gradual filtering (CacheBlend blog select_hkvd):
@@ -544,8 +545,9 @@ def blend_prefill(m: Model, segments, store, ratio_bp: int,
         elif policy == "single_window":
             P = single_window_select(d, k)
         elif policy == "fixed_chunk":
-            L_ = span_len if span_len > 0 else int(np.median(lens))
-            o_ = span_offset if span_offset >= 0 else L_ // 2
+            # span_len 0: the median document length, shifted by half a span
+            L_ = span_len if span_len > 0 else max(1, int(np.median(lens)))
+            o_ = span_offset if span_len > 0 else L_ // 2
             P = doc_aligned_select(d, fixed_chunk_offsets(N, L_, o_), k)
         elif policy == "first_tokens":
             offs = np.concatenate([[0], np.cumsum(lens)])

@@ -20,6 +20,8 @@ STATUS_NAMES = {0: "CB_OK", 1: "CB_ERR_INVALID_ARG", 2: "CB_ERR_UNSUPPORTED",
                 6: "CB_ERR_WORKSPACE"}
 CB_F32, CB_BF16 = 0, 1
 CB_POLICY_TOKEN_TOPK, CB_POLICY_DOC_ALIGNED = 0, 1
+CB_POLICY_SINGLE_WINDOW, CB_POLICY_FIXED_CHUNK, CB_POLICY_RANDOM_DOC = 2, 3, 4
+CB_POLICY_FIRST_TOKENS = 5
 CB_EPI_STORE, CB_EPI_RESID, CB_EPI_SWIGLU = 0, 1, 2
 CB_GEMM_AUTO, CB_GEMM_TOKEN_M, CB_GEMM_SWAP_AB, CB_GEMM_SWAP_AB_PAIR = 0, 1, 2, 3
 CB_PROBE_QKV, CB_PROBE_O, CB_PROBE_SWIGLU, CB_PROBE_DOWN, CB_PROBE_ATTENTION = 1, 2, 3, 4, 5
@@ -47,7 +49,9 @@ class StitchDesc(C.Structure):
 class SelectReq(C.Structure):
     _fields_ = [("n_ctx", i32), ("k", i32), ("fresh_row0", i64),
                 ("reused_row0", i64), ("dev_offset", i32), ("idx_offset", i32),
-                ("n_spans", i32), ("span_offsets", C.POINTER(C.c_int32))]
+                ("n_spans", i32), ("span_offsets", C.POINTER(C.c_int32)),
+                ("span_order", C.POINTER(C.c_int32)), ("span_len", i32),
+                ("span_offset", i32)]
 
 
 class AttnReq(C.Structure):
@@ -90,7 +94,8 @@ class ScheduleStep(C.Structure):
 class BlendParams(C.Structure):
     _fields_ = [("ratio_bp", i32), ("policy", i32), ("sel_layer", i32),
                 ("n_schedule", i32), ("schedule", C.POINTER(ScheduleStep)),
-                ("forced_selected", vp)]
+                ("span_len", i32), ("span_offset", i32),
+                ("span_order", C.POINTER(C.c_int32)), ("forced_selected", vp)]
 
 
 class BlendOut(C.Structure):

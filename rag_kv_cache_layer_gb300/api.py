@@ -84,20 +84,7 @@ def cb_kv_deviation_topk(k_fresh, k_reused, reqs, policy, dev_out, idx_out,
     """reqs: list of dicts with n_ctx, k, fresh_row0, reused_row0,
     dev_offset, idx_offset and (doc-aligned) span_offsets."""
     n = len(reqs)
-    arr = (L.SelectReq * max(1, n))()
-    keep = []
-    for i, r in enumerate(reqs):
-        spans = r.get("span_offsets")
-        sp = None
-        ns = 0
-        if spans is not None:
-            a = (C.c_int32 * len(spans))(*[int(x) for x in spans])
-            keep.append(a)
-            sp = C.cast(a, C.POINTER(C.c_int32))
-            ns = len(spans) - 1
-        arr[i] = L.SelectReq(r["n_ctx"], r["k"], r.get("fresh_row0", 0),
-                             r.get("reused_row0", 0), r.get("dev_offset", 0),
-                             r.get("idx_offset", 0), ns, sp)
+    arr, keep = _select_reqs(reqs)
     need = lib.cb_select_workspace_size(n)
     if ws is None:
         ws = torch.empty(max(need, 256), dtype=torch.uint8, device=k_fresh.device)
@@ -107,6 +94,32 @@ def cb_kv_deviation_topk(k_fresh, k_reused, reqs, policy, dev_out, idx_out,
         _p(dev_out), _p(idx_out), _p(ws), ws.numel(), _s(stream)))
 
 
+def _select_reqs(reqs, dev_offsets=True):
+    """ctypes cb_select_req array from dicts (n_ctx, k, fresh_row0,
+    reused_row0, dev_offset, idx_offset, span_offsets, span_order, span_len,
+    span_offset); the second value keeps the host arrays alive."""
+    n = len(reqs)
+    arr = (L.SelectReq * max(1, n))()
+    keep = []
+
+    def ints(v):
+        if v is None:
+            return None
+        a = (C.c_int32 * max(1, len(v)))(*[int(x) for x in v])
+        keep.append(a)
+        return C.cast(a, C.POINTER(C.c_int32))
+    for i, r in enumerate(reqs):
+        spans = r.get("span_offsets")
+        ns = len(spans) - 1 if spans is not None else 0
+        arr[i] = L.SelectReq(r["n_ctx"], r["k"], r.get("fresh_row0", 0),
+                             r.get("reused_row0", 0),
+                             r.get("dev_offset", 0) if dev_offsets else 0,
+                             r.get("idx_offset", 0), ns, ints(spans),
+                             ints(r.get("span_order")), r.get("span_len", 0),
+                             r.get("span_offset", 0))
+    return arr, keep
+
+
 def cb_kv_deviation_topk_noalloc(k_fresh, k_reused, reqs, policy, idx_out,
                                  stream=None):
     """cb_kv_deviation_topk without caller scratch: for callers that cannot
@@ -114,18 +127,7 @@ def cb_kv_deviation_topk_noalloc(k_fresh, k_reused, reqs, policy, idx_out,
     device array (at most 1048576 context tokens per call).  reqs as for
     cb_kv_deviation_topk; dev_offset is ignored."""
     n = len(reqs)
-    arr = (L.SelectReq * max(1, n))()
-    keep = []
-    for i, r in enumerate(reqs):
-        spans = r.get("span_offsets")
-        sp, ns = None, 0
-        if spans is not None:
-            a = (C.c_int32 * len(spans))(*[int(x) for x in spans])
-            keep.append(a)
-            sp = C.cast(a, C.POINTER(C.c_int32))
-            ns = len(spans) - 1
-        arr[i] = L.SelectReq(r["n_ctx"], r["k"], r.get("fresh_row0", 0),
-                             r.get("reused_row0", 0), 0, r.get("idx_offset", 0), ns, sp)
+    arr, keep = _select_reqs(reqs, dev_offsets=False)
     check(lib.cb_kv_deviation_topk_noalloc(
         _p(k_fresh), k_fresh.stride(0), _p(k_reused), k_reused.stride(0),
         k_fresh.shape[1], dtype_code(k_fresh.dtype), arr, n, policy,
@@ -290,22 +292,29 @@ class BlendModel:
                                  _p(k_cache), _p(v_cache), _p(ws), ws.numel(),
                                  _s(stream)))
 
-    def _params(self, ratio_bp, policy, sel_layer, schedule, forced=None):
+    def _params(self, ratio_bp, policy, sel_layer, schedule, forced=None, span_len=0,
+                span_offset=0, span_order=None):
         n = len(schedule or [])
         sch = (L.ScheduleStep * max(1, n))()
         for i, (l, k) in enumerate(schedule or []):
             sch[i] = L.ScheduleStep(l, k)
+        order = None
+        if span_order is not None:
+            order = (C.c_int32 * max(1, len(span_order)))(*[int(x) for x in span_order])
         return L.BlendParams(ratio_bp, policy, sel_layer, n,
-                             C.cast(sch, C.POINTER(L.ScheduleStep)),
-                             None if forced is None else forced.data_ptr()), sch
+                             C.cast(sch, C.POINTER(L.ScheduleStep)), span_len, span_offset,
+                             None if order is None else C.cast(order, C.POINTER(C.c_int32)),
+                             None if forced is None else forced.data_ptr()), (sch, order)
 
-    def plan(self, reqs, ratio_bp=None, policy=0, sel_layer=1, schedule=None):
+    def plan(self, reqs, ratio_bp=None, policy=0, sel_layer=1, schedule=None, span_len=0,
+             span_offset=0, span_order=None):
         arr, keep = _requests(reqs)
         out = L.Plan()
         if ratio_bp is None:
             check(lib.cb_full_plan(self.handle, arr, len(reqs), C.byref(out)))
         else:
-            p, sch = self._params(ratio_bp, policy, sel_layer, schedule)
+            p, sch = self._params(ratio_bp, policy, sel_layer, schedule, None, span_len,
+                                  span_offset, span_order)
             check(lib.cb_blend_plan(self.handle, arr, len(reqs), C.byref(p),
                                     C.byref(out)))
         return out
@@ -336,11 +345,14 @@ class BlendModel:
 
     def cb_blend_prefill(self, reqs, ratio_bp, policy=0, sel_layer=1,
                          schedule=None, outputs=None, forced=None,
-                         stream=None):
+                         stream=None, span_len=0, span_offset=0, span_order=None):
         """forced: optional device int32 tensor of selected context
-        positions (ascending per request) used instead of the ranking."""
+        positions (ascending per request) used instead of the ranking.
+        span_len / span_offset (fixed-chunk) and span_order (random-document,
+        all requests' segment orders concatenated) as in cb_blend_params."""
         arr, keep = _requests(reqs)
-        p, sch = self._params(ratio_bp, policy, sel_layer, schedule, forced)
+        p, sch = self._params(ratio_bp, policy, sel_layer, schedule, forced, span_len,
+                              span_offset, span_order)
         if outputs is None:
             plan = L.Plan()
             check(lib.cb_blend_plan(self.handle, arr, len(reqs), C.byref(p),
@@ -474,9 +486,10 @@ class RollingWindow:
         toks = torch.cat([self.tokens[c] for c in self.docs] + [new_tokens, query_tokens])
         return Req(toks.to(torch.int32).contiguous(), segs)
 
-    def blend(self, req, outputs=None, stream=None):
+    def blend(self, req, outputs=None, stream=None, **span_args):
+        """span_args: span_len / span_offset / span_order of cb_blend_params."""
         return self.model.cb_blend_prefill([req], self.ratio_bp, self.policy,
-                                           outputs=outputs, stream=stream)
+                                           outputs=outputs, stream=stream, **span_args)
 
     def advance(self, new_id, new_tokens, stream=None):
         """Stores the new document's chunk cache; evicts the oldest once the

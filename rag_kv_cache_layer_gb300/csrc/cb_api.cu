@@ -7,6 +7,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -247,50 +248,13 @@ extern "C" cb_status cb_rope_reposition(const cb_stitch_desc *descs, int n_desc,
 // -------------------------------------------------------------- selection --
 extern "C" size_t cb_select_workspace_size(int n_req) { return select_ws_bytes(n_req); }
 
-static cb_status to_sel_reqs(const cb_select_req *reqs, int n_req, cb_policy policy,
-                             std::vector<SelReq> &out, std::vector<int32_t> &spans) {
-  if (n_req < 0 || n_req > CB_MAX_BATCH) return fail(CB_ERR_INVALID_ARG, "n_req must be in [0, %d]", CB_MAX_BATCH);
-  if (n_req > 0 && !reqs) return fail(CB_ERR_INVALID_ARG, "reqs is NULL");
-  if (policy != CB_POLICY_TOKEN_TOPK && policy != CB_POLICY_DOC_ALIGNED)
-    return fail(CB_ERR_INVALID_ARG, "unknown policy %d", (int)policy);
-  out.resize(n_req);
-  for (int i = 0; i < n_req; ++i) {
-    const cb_select_req &r = reqs[i];
-    if (r.n_ctx < 0 || r.k < 0 || r.k > r.n_ctx) return fail(CB_ERR_INVALID_ARG, "req %d: need 0 <= k <= n_ctx", i);
-    if (r.fresh_row0 < 0 || r.reused_row0 < 0 || r.dev_offset < 0 || r.idx_offset < 0)
-      return fail(CB_ERR_INVALID_ARG, "req %d: negative offset", i);
-    SelReq s{r.n_ctx, r.k, r.fresh_row0, r.reused_row0, r.dev_offset, r.idx_offset, 0, 0};
-    if (policy == CB_POLICY_DOC_ALIGNED && r.k > 0) {
-      if (r.n_spans < 1 || !r.span_offsets) return fail(CB_ERR_INVALID_ARG, "req %d: doc-aligned needs spans", i);
-      if (r.span_offsets[0] != 0 || r.span_offsets[r.n_spans] != r.n_ctx)
-        return fail(CB_ERR_INVALID_ARG, "req %d: spans must cover [0, n_ctx]", i);
-      for (int j = 0; j < r.n_spans; ++j)
-        if (r.span_offsets[j + 1] < r.span_offsets[j]) return fail(CB_ERR_INVALID_ARG, "req %d: spans not ascending", i);
-      if ((int)spans.size() + r.n_spans + 1 > CB_MAX_SPANS + CB_MAX_BATCH || r.n_spans > CB_MAX_SPANS)
-        return fail(CB_ERR_INVALID_ARG, "too many spans (max %d)", CB_MAX_SPANS);
-      s.span_begin = (int)spans.size();
-      s.n_spans = r.n_spans;
-      spans.insert(spans.end(), r.span_offsets, r.span_offsets + r.n_spans + 1);
-    }
-    out[i] = s;
-  }
-  return CB_OK;
-}
-
 static cb_status run_selection(const void *k_fresh, int64_t ld_fresh,
                                const void *k_reused, int64_t ld_reused,
-                               int row_elems, cb_dtype dt,
-                               const std::vector<SelReq> &sr,
-                               const std::vector<int32_t> &spans,
-                               cb_policy policy, float *dev, int32_t *idx,
-                               int *st, cudaStream_t s) {
+                               int row_elems, cb_dtype dt, const SelPlan &plan,
+                               float *dev, int32_t *idx, int *st, cudaStream_t s) {
   CB_CUDA(launch_deviation(k_fresh, ld_fresh, k_reused, ld_reused, row_elems, dt,
-                           sr.data(), (int)sr.size(), dev, s));
-  if (policy == CB_POLICY_TOKEN_TOPK)
-    CB_CUDA(launch_topk(dev, sr.data(), (int)sr.size(), idx, s));
-  else
-    CB_CUDA(launch_doc_aligned(dev, sr.data(), (int)sr.size(), spans.data(),
-                               (int)spans.size(), idx, st, s));
+                           plan.reqs.data(), (int)plan.reqs.size(), dev, s));
+  CB_CUDA(launch_selection(dev, plan, idx, st, s));
   return CB_OK;
 }
 
@@ -308,13 +272,13 @@ extern "C" cb_status cb_kv_deviation_topk(const void *k_fresh, int64_t ld_fresh,
       (ld_fresh * eb) % 16 || (ld_reused * eb) % 16 || !aligned16(k_fresh) || !aligned16(k_reused))
     return fail(CB_ERR_INVALID_ARG, "rows must be 16-byte aligned and ld >= row_elems");
   if (!ws || ws_bytes < cb_select_workspace_size(n_req)) return fail(CB_ERR_WORKSPACE, "workspace too small");
-  std::vector<SelReq> sr;
-  std::vector<int32_t> spans;
-  CB_TRY(to_sel_reqs(reqs, n_req, policy, sr, spans));
+  SelPlan plan;
+  const char *err = "";
+  if (make_sel_plan(reqs, n_req, policy, plan, &err) != CB_OK) return fail(CB_ERR_INVALID_ARG, "%s", err);
   int *st;
   CB_TRY(status_ptr(&st));
-  return run_selection(k_fresh, ld_fresh, k_reused, ld_reused, row_elems, dtype, sr,
-                       spans, policy, dev_out, idx_out, st, stream);
+  return run_selection(k_fresh, ld_fresh, k_reused, ld_reused, row_elems, dtype, plan, dev_out,
+                       idx_out, st, stream);
 }
 
 // -------------------------------------------------------- gather/scatter --
@@ -655,8 +619,13 @@ static cb_status make_plan(const cb_model *m, const cb_request *reqs, int B,
     if (p->ratio_bp < 0 || p->ratio_bp > 10000) return fail(CB_ERR_INVALID_ARG, "ratio_bp must be in [0, 10000]");
     if (p->sel_layer < 0 || p->sel_layer >= m->cfg.n_layers)
       return fail(CB_ERR_INVALID_ARG, "sel_layer must be in [0, n_layers)");
-    if (p->policy != CB_POLICY_TOKEN_TOPK && p->policy != CB_POLICY_DOC_ALIGNED)
+    if (p->policy < CB_POLICY_TOKEN_TOPK || p->policy > CB_POLICY_FIRST_TOKENS)
       return fail(CB_ERR_INVALID_ARG, "unknown policy");
+    if (p->policy == CB_POLICY_RANDOM_DOC && !p->span_order)
+      return fail(CB_ERR_INVALID_ARG, "random-document needs span_order");
+    if (p->policy == CB_POLICY_FIXED_CHUNK &&
+        (p->span_len < 0 || (p->span_len > 0 && (p->span_offset < 0 || p->span_offset > p->span_len))))
+      return fail(CB_ERR_INVALID_ARG, "fixed-chunk needs 0 <= span_offset <= span_len");
     if (p->n_schedule < 0 || p->n_schedule > m->cfg.n_layers)
       return fail(CB_ERR_INVALID_ARG, "n_schedule must be in [0, n_layers]");
     if (p->n_schedule > 0 && !p->schedule) return fail(CB_ERR_INVALID_ARG, "schedule is NULL");
@@ -986,25 +955,39 @@ extern "C" cb_status cb_blend_prefill(cb_model *m, const cb_request *reqs, int B
     CB_CUDA(launch_qkv_finish(S.qkv32, m->kvw, (int)P.T_total, pos_all, nullptr, c.n_q_heads,
                               c.n_kv_heads, c.head_dim, m->w.rope_table, nullptr, 0, kf,
                               nullptr, m->kvw, c.dtype, 0, s));
-    std::vector<SelReq> sr(B);
-    std::vector<int32_t> spans;
+    // selection requests: every request's cached segments are its spans
+    std::vector<cb_select_req> cr(B);
+    std::vector<std::vector<int32_t>> seg_offs(B);
+    int order_at = 0;
     for (int b = 0; b < B; ++b) {
-      sr[b] = SelReq{P.N[b], P.k[b], (int64_t)P.bm.t_off[b], (int64_t)P.bm.t_off[b],
-                     P.n_off[b], P.bm.k_off[b], 0, 0};
-      if (p->policy == CB_POLICY_DOC_ALIGNED) {
-        sr[b].span_begin = (int)spans.size();
-        int n_sp = 0;
-        for (int i = 0; i < reqs[b].n_segments; ++i) {
-          if (!reqs[b].segments[i].k_pic) break;
-          spans.push_back(P.seg_start[b][i]);
-          ++n_sp;
-        }
-        spans.push_back(P.N[b]);
-        sr[b].n_spans = n_sp;
-        if ((int)spans.size() > CB_MAX_SPANS + CB_MAX_BATCH)
-          return fail(CB_ERR_INVALID_ARG, "too many spans (max %d)", CB_MAX_SPANS);
+      std::vector<int32_t> &o = seg_offs[b];
+      std::vector<int> lens;
+      for (int i = 0; i < reqs[b].n_segments; ++i) {
+        if (!reqs[b].segments[i].k_pic) break;
+        o.push_back(P.seg_start[b][i]);
+        lens.push_back(reqs[b].segments[i].len);
       }
+      o.push_back(P.N[b]);
+      int L_ = p->span_len, off_ = p->span_offset;
+      if (L_ == 0) {
+        // the median cached-segment length, shifted by half a span
+        std::vector<int> sl = lens;
+        std::sort(sl.begin(), sl.end());
+        L_ = sl.empty() ? 1 : (sl.size() % 2 ? sl[sl.size() / 2]
+                                             : (sl[sl.size() / 2 - 1] + sl[sl.size() / 2]) / 2);
+        if (L_ < 1) L_ = 1;
+        off_ = L_ / 2;
+      }
+      cr[b] = cb_select_req{P.N[b], P.k[b], (int64_t)P.bm.t_off[b], (int64_t)P.bm.t_off[b],
+                            P.n_off[b], P.bm.k_off[b], (int)o.size() - 1, o.data(),
+                            p->span_order ? p->span_order + order_at : nullptr, L_, off_};
+      order_at += (int)o.size() - 1;
     }
+    SelPlan plan;
+    const char *err = "";
+    if (make_sel_plan(cr.data(), B, p->policy, plan, &err) != CB_OK)
+      return fail(CB_ERR_INVALID_ARG, "%s", err);
+    const std::vector<SelReq> &sr = plan.reqs;
     probe_mark(CB_PROBE_SELECT, true, s);
     if (p->forced_selected) {
       // the caller fixes P; d is still produced for inspection
@@ -1015,7 +998,7 @@ extern "C" cb_status cb_blend_prefill(cb_model *m, const cb_request *reqs, int B
                                 cudaMemcpyDeviceToDevice, s));
     } else {
       CB_TRY(run_selection(kf, m->kvw, layer_ptr(out->k_cache, s_layer, lstride, m->eb),
-                           m->kvw, m->kvw, c.dtype, sr, spans, p->policy, dev, sel, st, s));
+                           m->kvw, m->kvw, c.dtype, plan, dev, sel, st, s));
     }
     probe_mark(CB_PROBE_SELECT, false, s);
   }

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <utility>
+#include <vector>
 
 #include "cacheblend.h"
 
@@ -84,9 +85,19 @@ cudaError_t launch_deviation(const void *k_fresh, int64_t ld_fresh,
 // reused_row0 + reused_rows[f] instead of reused_row0 + i.
 cudaError_t launch_topk(const float *dev, const SelReq *reqs, int n_req,
                         int32_t *idx_out, cudaStream_t s);
-cudaError_t launch_doc_aligned(const float *dev, const SelReq *reqs, int n_req,
-                               const int32_t *span_offsets, int n_spans_total,
-                               int32_t *idx_out, int *status, cudaStream_t s);
+// A selection call after validation: the requests, their packed spans and,
+// per span, the visiting order (random document) or the token counts
+// (first tokens).  make_sel_plan builds the spans every policy uses.
+struct SelPlan {
+  cb_policy policy = CB_POLICY_TOKEN_TOPK;
+  std::vector<SelReq> reqs;
+  std::vector<int32_t> spans, aux;
+};
+cb_status make_sel_plan(const cb_select_req *reqs, int n_req, cb_policy policy, SelPlan &out,
+                        const char **err);
+// The ranking of a plan over deviations already in dev (top-k or spans).
+cudaError_t launch_selection(const float *dev, const SelPlan &plan, int32_t *idx_out,
+                             int *status, cudaStream_t s);
 cudaError_t launch_build_rows(const BatchMeta &bm, const int32_t *sel,
                               int32_t *pos, int32_t *glob, int n_rows,
                               int *status, cudaStream_t s);

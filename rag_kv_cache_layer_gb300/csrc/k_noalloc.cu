@@ -60,58 +60,33 @@ extern "C" cb_status cb_kv_deviation_topk_noalloc(const void *k_fresh, int64_t l
                                                   cb_stream stream) {
   if (!k_fresh || !k_reused || !idx_out) return record_error(CB_ERR_INVALID_ARG, "NULL pointer");
   if (dtype != CB_F32 && dtype != CB_BF16) return record_error(CB_ERR_INVALID_ARG, "bad dtype");
-  if (policy != CB_POLICY_TOKEN_TOPK && policy != CB_POLICY_DOC_ALIGNED)
-    return record_error(CB_ERR_INVALID_ARG, "unknown policy");
-  if (n_req < 0 || n_req > CB_MAX_BATCH || (n_req > 0 && !reqs))
-    return record_error(CB_ERR_INVALID_ARG, "n_req must be in [0, CB_MAX_BATCH] with reqs set");
   const size_t eb = dtype == CB_BF16 ? 2 : 4;
   if (row_elems <= 0 || (row_elems * eb) % 16 || ld_fresh < row_elems || ld_reused < row_elems ||
       (ld_fresh * eb) % 16 || (ld_reused * eb) % 16 || ((uintptr_t)k_fresh & 15) ||
       ((uintptr_t)k_reused & 15))
     return record_error(CB_ERR_INVALID_ARG, "rows must be 16-byte aligned and ld >= row_elems");
-  std::vector<SelReq> sr(n_req);
-  std::vector<int32_t> spans;
+  SelPlan plan;
+  const char *err = "";
+  if (make_sel_plan(reqs, n_req, policy, plan, &err) != CB_OK)
+    return record_error(CB_ERR_INVALID_ARG, err);
+  // deviations are packed request after request into the static array
   int64_t total = 0;
-  for (int i = 0; i < n_req; ++i) {
-    const cb_select_req &r = reqs[i];
-    if (r.n_ctx < 0 || r.k < 0 || r.k > r.n_ctx || r.fresh_row0 < 0 || r.reused_row0 < 0 ||
-        r.idx_offset < 0)
-      return record_error(CB_ERR_INVALID_ARG, "bad request sizes or offsets");
-    // deviations are packed request after request into the static array
-    sr[i] = SelReq{r.n_ctx, r.k, r.fresh_row0, r.reused_row0, (int)total, r.idx_offset, 0, 0};
+  for (SelReq &r : plan.reqs) {
+    r.dev_offset = (int)total;
     total += r.n_ctx;
     if (total > kNoAllocMaxCtx)
       return record_error(CB_ERR_INVALID_ARG,
                           "cb_kv_deviation_topk_noalloc: more than 1048576 context tokens in one "
                           "call (the fixed scratch limit); split the call");
-    if (policy == CB_POLICY_DOC_ALIGNED && r.k > 0) {
-      if (r.n_spans < 1 || !r.span_offsets || r.span_offsets[0] != 0 ||
-          r.span_offsets[r.n_spans] != r.n_ctx || r.n_spans > CB_MAX_SPANS)
-        return record_error(CB_ERR_INVALID_ARG, "spans must cover [0, n_ctx]");
-      for (int j = 0; j < r.n_spans; ++j)
-        if (r.span_offsets[j + 1] < r.span_offsets[j])
-          return record_error(CB_ERR_INVALID_ARG, "spans not ascending");
-      if ((int)spans.size() + r.n_spans + 1 > CB_MAX_SPANS + CB_MAX_BATCH)
-        return record_error(CB_ERR_INVALID_ARG, "too many spans");
-      sr[i].span_begin = (int)spans.size();
-      sr[i].n_spans = r.n_spans;
-      spans.insert(spans.end(), r.span_offsets, r.span_offsets + r.n_spans + 1);
-    }
   }
   float *dev = nullptr;
   cudaError_t e = noalloc_scratch(&dev);
   if (e != cudaSuccess) return record_error(CB_ERR_CUDA, cudaGetErrorString(e));
   int *st = device_status_ptr();
   if (!st) return record_error(CB_ERR_CUDA, "cannot resolve the device status word");
-  e = launch_deviation(k_fresh, ld_fresh, k_reused, ld_reused, row_elems, dtype, sr.data(), n_req,
-                       dev, stream);
-  if (e == cudaSuccess) {
-    if (policy == CB_POLICY_TOKEN_TOPK)
-      e = launch_topk(dev, sr.data(), n_req, idx_out, stream);
-    else
-      e = launch_doc_aligned(dev, sr.data(), n_req, spans.data(), (int)spans.size(), idx_out, st,
-                             stream);
-  }
+  e = launch_deviation(k_fresh, ld_fresh, k_reused, ld_reused, row_elems, dtype,
+                       plan.reqs.data(), (int)plan.reqs.size(), dev, stream);
+  if (e == cudaSuccess) e = launch_selection(dev, plan, idx_out, st, stream);
   if (e != cudaSuccess) return record_error(CB_ERR_CUDA, cudaGetErrorString(e));
   return CB_OK;
 }

@@ -236,16 +236,27 @@ cudaError_t launch_topk(const float *dev, const SelReq *reqs, int n_req,
   return launched(1);
 }
 
-// ----------------------------------------------------------- doc-aligned --
+// ----------------------------------------------------------- span policies --
 // One CTA per request.  Spans: offsets spans[span_begin .. +n_spans] (local
-// context positions).  Steps: per-span double sums (one warp per span, fixed
-// order), rank by mean (ties: lower span), greedy whole spans, then the
-// max-total window (ties: leftmost) of the remainder inside the first span
-// that does not fit, then ordered compaction of the chosen positions.
+// context positions).  Modes:
+//   kSpanMean  -- rank spans by mean deviation (ties: lower span), take whole
+//                 spans while they fit, then the max-total window (ties:
+//                 leftmost) of the remainder inside the first span that does
+//                 not fit (document-aligned, fixed-chunk and single-window,
+//                 "Request Order Matters" §2.3 Eq. 3);
+//   kSpanOrder -- the same fill with the visiting order given in aux (the
+//                 random-document control of §2.3);
+//   kSpanFirst -- the first aux[j] tokens of every span j (EPIC's
+//                 chunk-boundary rule).
+// Span sums are accumulated in double in a fixed order; the chosen positions
+// are written ascending by a block-wide ordered compaction.
+enum { kSpanMean = 0, kSpanOrder = 1, kSpanFirst = 2 };
+
 struct DocParams {
   SelParams sel;
-  int n_spans_total;
+  int n_spans_total, mode;
   int32_t spans[CB_MAX_SPANS + CB_MAX_BATCH];
+  int32_t aux[CB_MAX_SPANS + CB_MAX_BATCH];    // order or counts, per span
 };
 
 __global__ void __launch_bounds__(kSelThreads)
@@ -264,83 +275,93 @@ doc_aligned_kernel(const __grid_constant__ DocParams P,
   if (k <= 0) return;
   const int m = q.n_spans;
   const int32_t *off = P.spans + q.span_begin;
+  const int32_t *aux = P.aux + q.span_begin;
   const float *d = dev + q.dev_offset;
   int32_t *out = idx_out + q.idx_offset;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int mode = P.mode;
 
-  for (int j = w; j < m; j += kSelThreads / 32) {
-    double acc = 0.0;
-    for (int i = off[j] + lane; i < off[j + 1]; i += 32) acc += (double)__ldg(d + i);
-    acc = warp_sum_d(acc);
-    if (lane == 0) s_sum[j] = acc;
-  }
-  for (int j = tid; j < m; j += kSelThreads) s_take[j] = 0;
-  __syncthreads();
-  // rank of span j among non-empty spans by (mean desc, index asc)
-  for (int j = tid; j < m; j += kSelThreads) {
-    const int lj = off[j + 1] - off[j];
-    if (lj <= 0) continue;
-    const double rj = s_sum[j] / lj;
-    int rank = 0;
-    for (int i = 0; i < m; ++i) {
-      const int li = off[i + 1] - off[i];
-      if (li <= 0 || i == j) continue;
-      const double ri = s_sum[i] / li;
-      if (ri > rj || (ri == rj && i < j)) ++rank;
-    }
-    s_rank_of[rank] = j;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int n_nonempty = 0;
-    for (int j = 0; j < m; ++j) n_nonempty += (off[j + 1] > off[j]);
-    int rem = k, part = -1;
-    for (int r = 0; r < n_nonempty && rem > 0; ++r) {
-      const int j = s_rank_of[r];
-      const int lj = off[j + 1] - off[j];
-      if (lj <= rem) { s_take[j] = 1; rem -= lj; }
-      else { part = j; break; }
-    }
-    s_part_span = part;
-    s_rem = part >= 0 ? rem : 0;
-    if (rem > 0 && part < 0) report(status, CB_ERR_INVALID_ARG);  // k > N
-  }
-  __syncthreads();
-  int win_start = -1;
-  const int rem = s_rem;
-  if (rem > 0) {
-    const int a = off[s_part_span], b = off[s_part_span + 1];
-    const int n_win = b - a - rem + 1;
-    double best = -1.0;
-    int best_i = 0x7fffffff;
-    for (int t = tid; t < n_win; t += kSelThreads) {
+  int rem = 0, win_start = -1;
+  if (mode != kSpanFirst) {
+    for (int j = w; j < m; j += kSelThreads / 32) {
       double acc = 0.0;
-      for (int i = a + t; i < a + t + rem; ++i) acc += (double)__ldg(d + i);
-      if (acc > best || (acc == best && a + t < best_i)) { best = acc; best_i = a + t; }
+      for (int i = off[j] + lane; i < off[j + 1]; i += 32) acc += (double)__ldg(d + i);
+      acc = warp_sum_d(acc);
+      if (lane == 0) s_sum[j] = acc;
     }
-    // block arg-max, ties to the lower start
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const double ob = __shfl_xor_sync(0xffffffffu, best, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
-      if (ob > best || (ob == best && oi < best_i)) { best = ob; best_i = oi; }
+    for (int j = tid; j < m; j += kSelThreads) s_take[j] = 0;
+    __syncthreads();
+    if (mode == kSpanOrder) {
+      for (int r = tid; r < m; r += kSelThreads) s_rank_of[r] = aux[r];
+    } else {
+      // rank of span j by (mean desc, index asc); empty spans after all
+      // non-empty ones, by index
+      for (int j = tid; j < m; j += kSelThreads) {
+        const int lj = off[j + 1] - off[j];
+        int rank = 0;
+        if (lj > 0) {
+          const double rj = s_sum[j] / lj;
+          for (int i = 0; i < m; ++i) {
+            const int li = off[i + 1] - off[i];
+            if (li <= 0 || i == j) continue;
+            const double ri = s_sum[i] / li;
+            if (ri > rj || (ri == rj && i < j)) ++rank;
+          }
+        } else {
+          for (int i = 0; i < m; ++i) rank += (off[i + 1] > off[i]) || (i < j);
+        }
+        s_rank_of[rank] = j;
+      }
     }
-    if (lane == 0) { s_best[w] = best; s_best_i[w] = best_i; }
     __syncthreads();
     if (tid == 0) {
-      double bb = s_best[0];
-      int bi = s_best_i[0];
-      for (int j = 1; j < kSelThreads / 32; ++j)
-        if (s_best[j] > bb || (s_best[j] == bb && s_best_i[j] < bi)) { bb = s_best[j]; bi = s_best_i[j]; }
-      s_best_i[0] = bi;
+      int left = k, part = -1;
+      for (int r = 0; r < m && left > 0; ++r) {
+        const int j = s_rank_of[r];
+        const int lj = off[j + 1] - off[j];
+        if (lj <= 0) continue;
+        if (lj <= left) { s_take[j] = 1; left -= lj; }
+        else { part = j; break; }
+      }
+      s_part_span = part;
+      s_rem = part >= 0 ? left : 0;
+      if (left > 0 && part < 0) report(status, CB_ERR_INVALID_ARG);  // k > N
     }
     __syncthreads();
-    win_start = s_best_i[0];
+    rem = s_rem;
+    if (rem > 0) {
+      const int a = off[s_part_span], b = off[s_part_span + 1];
+      const int n_win = b - a - rem + 1;
+      double best = -1.0;
+      int best_i = 0x7fffffff;
+      for (int t = tid; t < n_win; t += kSelThreads) {
+        double acc = 0.0;
+        for (int i = a + t; i < a + t + rem; ++i) acc += (double)__ldg(d + i);
+        if (acc > best || (acc == best && a + t < best_i)) { best = acc; best_i = a + t; }
+      }
+      // block arg-max, ties to the lower start
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const double ob = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
+        if (ob > best || (ob == best && oi < best_i)) { best = ob; best_i = oi; }
+      }
+      if (lane == 0) { s_best[w] = best; s_best_i[w] = best_i; }
+      __syncthreads();
+      if (tid == 0) {
+        double bb = s_best[0];
+        int bi = s_best_i[0];
+        for (int j = 1; j < kSelThreads / 32; ++j)
+          if (s_best[j] > bb || (s_best[j] == bb && s_best_i[j] < bi)) { bb = s_best[j]; bi = s_best_i[j]; }
+        s_best_i[0] = bi;
+      }
+      __syncthreads();
+      win_start = s_best_i[0];
+    }
   }
   // ordered compaction over the context positions
   const int n = q.n_ctx;
   int written = 0;
-  int span = 0;
   for (int base = 0; base < n; base += kSelThreads) {
     const int i = base + tid;
     int sel = 0;
@@ -351,8 +372,10 @@ doc_aligned_kernel(const __grid_constant__ DocParams P,
         const int mid = (lo + hi + 1) >> 1;
         if (off[mid] <= i) lo = mid; else hi = mid - 1;
       }
-      span = lo;
-      sel = s_take[span] || (rem > 0 && i >= win_start && i < win_start + rem);
+      if (mode == kSpanFirst)
+        sel = i - off[lo] < aux[lo];
+      else
+        sel = s_take[lo] || (rem > 0 && i >= win_start && i < win_start + rem);
     }
     int total;
     const int pos = block_exclusive_scan(sel, warp_buf, &total);
@@ -361,17 +384,113 @@ doc_aligned_kernel(const __grid_constant__ DocParams P,
   }
 }
 
-cudaError_t launch_doc_aligned(const float *dev, const SelReq *reqs, int n_req,
-                               const int32_t *span_offsets, int n_spans_total,
-                               int32_t *idx_out, int *status, cudaStream_t s) {
+cudaError_t launch_selection(const float *dev, const SelPlan &plan, int32_t *idx_out,
+                             int *status, cudaStream_t s) {
+  const int n_req = (int)plan.reqs.size();
   if (n_req == 0) return cudaSuccess;
+  if (plan.policy == CB_POLICY_TOKEN_TOPK) return launch_topk(dev, plan.reqs.data(), n_req, idx_out, s);
   DocParams *P = new DocParams;
-  fill_params(P->sel, reqs, n_req);
-  P->n_spans_total = n_spans_total;
-  for (int i = 0; i < n_spans_total; ++i) P->spans[i] = span_offsets[i];
+  fill_params(P->sel, plan.reqs.data(), n_req);
+  P->n_spans_total = (int)plan.spans.size();
+  P->mode = plan.policy == CB_POLICY_RANDOM_DOC    ? kSpanOrder
+            : plan.policy == CB_POLICY_FIRST_TOKENS ? kSpanFirst
+                                                    : kSpanMean;
+  for (size_t i = 0; i < plan.spans.size(); ++i) P->spans[i] = plan.spans[i];
+  for (size_t i = 0; i < plan.aux.size(); ++i) P->aux[i] = plan.aux[i];
   doc_aligned_kernel<<<n_req, kSelThreads, 0, s>>>(*P, dev, idx_out, status);
   delete P;
   return launched(1);
+}
+
+// Tokens each span contributes under the chunk-boundary rule: k shared out
+// evenly over the non-empty spans (the first k mod m one more), a short span
+// passing what it cannot hold to the following spans in order.
+static void first_token_counts(const int32_t *off, int n_spans, int k, int32_t *cnt) {
+  int m = 0;
+  for (int j = 0; j < n_spans; ++j) m += off[j + 1] > off[j];
+  int left = k, r = 0;
+  for (int j = 0; j < n_spans; ++j) {
+    cnt[j] = 0;
+    const int lj = off[j + 1] - off[j];
+    if (lj <= 0) continue;
+    const int quota = k / m + (r < k % m ? 1 : 0);
+    ++r;
+    cnt[j] = quota < lj ? quota : lj;
+    left -= cnt[j];
+  }
+  for (int j = 0; j < n_spans && left > 0; ++j) {
+    const int room = (off[j + 1] - off[j]) - cnt[j];
+    const int e = room < left ? room : left;
+    cnt[j] += e;
+    left -= e;
+  }
+}
+
+cb_status make_sel_plan(const cb_select_req *reqs, int n_req, cb_policy policy, SelPlan &out,
+                        const char **err) {
+  auto bad = [&](const char *msg) { *err = msg; return CB_ERR_INVALID_ARG; };
+  if (n_req < 0 || n_req > CB_MAX_BATCH) return bad("n_req must be in [0, CB_MAX_BATCH]");
+  if (n_req > 0 && !reqs) return bad("reqs is NULL");
+  if (policy < CB_POLICY_TOKEN_TOPK || policy > CB_POLICY_FIRST_TOKENS) return bad("unknown policy");
+  out.policy = policy;
+  out.reqs.assign(n_req, SelReq{});
+  out.spans.clear();
+  out.aux.clear();
+  std::vector<int32_t> offs;
+  for (int i = 0; i < n_req; ++i) {
+    const cb_select_req &r = reqs[i];
+    if (r.n_ctx < 0 || r.k < 0 || r.k > r.n_ctx) return bad("need 0 <= k <= n_ctx");
+    if (r.fresh_row0 < 0 || r.reused_row0 < 0 || r.dev_offset < 0 || r.idx_offset < 0)
+      return bad("negative offset");
+    SelReq s{r.n_ctx, r.k, r.fresh_row0, r.reused_row0, r.dev_offset, r.idx_offset, 0, 0};
+    if (policy != CB_POLICY_TOKEN_TOPK && r.k > 0) {
+      offs.clear();
+      if (policy == CB_POLICY_SINGLE_WINDOW) {
+        offs = {0, r.n_ctx};
+      } else if (policy == CB_POLICY_FIXED_CHUNK) {
+        if (r.span_len <= 0 || r.span_offset < 0 || r.span_offset > r.span_len)
+          return bad("fixed-chunk needs span_len > 0 and 0 <= span_offset <= span_len");
+        offs.push_back(0);
+        if (r.span_offset > 0 && r.span_offset < r.n_ctx) offs.push_back(r.span_offset);
+        while (offs.back() < r.n_ctx) {
+          const int64_t nx = (int64_t)offs.back() + r.span_len;
+          offs.push_back((int32_t)(nx < r.n_ctx ? nx : r.n_ctx));
+          if ((int)offs.size() > CB_MAX_SPANS + 1) return bad("too many fixed-chunk spans");
+        }
+      } else {
+        if (r.n_spans < 1 || !r.span_offsets) return bad("this policy needs spans");
+        if (r.n_spans > CB_MAX_SPANS) return bad("too many spans");
+        if (r.span_offsets[0] != 0 || r.span_offsets[r.n_spans] != r.n_ctx)
+          return bad("spans must cover [0, n_ctx]");
+        for (int j = 0; j < r.n_spans; ++j)
+          if (r.span_offsets[j + 1] < r.span_offsets[j]) return bad("spans not ascending");
+        offs.assign(r.span_offsets, r.span_offsets + r.n_spans + 1);
+      }
+      const int ns = (int)offs.size() - 1;
+      if (ns > CB_MAX_SPANS || (int)out.spans.size() + ns + 1 > CB_MAX_SPANS + CB_MAX_BATCH)
+        return bad("too many spans in one call");
+      s.span_begin = (int)out.spans.size();
+      s.n_spans = ns;
+      out.spans.insert(out.spans.end(), offs.begin(), offs.end());
+      // aux shares the span indexing (one entry per offset; the last unused)
+      std::vector<int32_t> a(ns + 1, 0);
+      if (policy == CB_POLICY_RANDOM_DOC) {
+        if (!r.span_order) return bad("random-document needs span_order");
+        std::vector<unsigned char> seen(ns, 0);
+        for (int j = 0; j < ns; ++j) {
+          const int o = r.span_order[j];
+          if (o < 0 || o >= ns || seen[o]) return bad("span_order must be a permutation of the spans");
+          seen[o] = 1;
+          a[j] = o;
+        }
+      } else if (policy == CB_POLICY_FIRST_TOKENS) {
+        first_token_counts(offs.data(), ns, r.k, a.data());
+      }
+      out.aux.insert(out.aux.end(), a.begin(), a.end());
+    }
+    out.reqs[i] = s;
+  }
+  return CB_OK;
 }
 
 // ------------------------------------------------------------- row maps --

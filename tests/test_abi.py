@@ -34,7 +34,8 @@ def test_every_declared_entry_point_is_exported():
 STRUCTS = {
     "cb_stitch_desc": (L.StitchDesc, ["k_src", "v_src", "src_layer_stride", "len", "dst_row", "delta"]),
     "cb_select_req": (L.SelectReq, ["n_ctx", "k", "fresh_row0", "reused_row0", "dev_offset",
-                                    "idx_offset", "n_spans", "span_offsets"]),
+                                    "idx_offset", "n_spans", "span_offsets", "span_order",
+                                    "span_len", "span_offset"]),
     "cb_attn_req": (L.AttnReq, ["q_begin", "q_end", "kv_row0", "kv_len"]),
     "cb_model_config": (L.ModelConfig, ["n_layers", "d_model", "n_q_heads", "n_kv_heads",
                                         "head_dim", "d_ffn", "vocab", "rope_base", "norm_eps",
@@ -46,7 +47,8 @@ STRUCTS = {
     "cb_request": (L.Request, ["tokens", "segments", "n_segments"]),
     "cb_schedule_step": (L.ScheduleStep, ["layer", "keep"]),
     "cb_blend_params": (L.BlendParams, ["ratio_bp", "policy", "sel_layer", "n_schedule",
-                                        "schedule", "forced_selected"]),
+                                        "schedule", "span_len", "span_offset", "span_order",
+                                        "forced_selected"]),
     "cb_blend_out": (L.BlendOut, ["k_cache", "v_cache", "cache_layer_stride", "deviation",
                                   "selected", "hidden", "rows", "first_token"]),
     "cb_plan": (L.Plan, ["T_total", "N_total", "K_total", "R_total", "workspace_bytes",
@@ -101,12 +103,38 @@ def test_host_validation_without_device():
     assert lib.cb_debug_probe_stop(None, None) == L.CB_ERR_INVALID_ARG
     # bad doc-aligned spans are rejected on the host
     spans = (C.c_int32 * 3)(0, 5, 4)
-    req = L.SelectReq(4, 2, 0, 0, 0, 0, 2, C.cast(spans, C.POINTER(C.c_int32)))
+    req = L.SelectReq(4, 2, 0, 0, 0, 0, 2, C.cast(spans, C.POINTER(C.c_int32)), None, 0, 0)
     ws = C.create_string_buffer(4096)
     st = lib.cb_kv_deviation_topk(C.c_void_p(16), 64, C.c_void_p(16), 64, 64, L.CB_F32,
                                   C.byref(req), 1, L.CB_POLICY_DOC_ALIGNED, C.c_void_p(16),
                                   C.c_void_p(16), ws, 4096, None)
     assert st == L.CB_ERR_INVALID_ARG
+
+
+def test_span_policy_requests_are_validated_on_the_host():
+    """Malformed span-policy requests fail before anything is enqueued
+    (no GPU needed): a random-document order that is not a permutation or
+    is missing, fixed chunks without a length or with an offset past it, and
+    an unknown policy."""
+    lib = L.lib
+    ws = C.create_string_buffer(4096)
+    spans = (C.c_int32 * 3)(0, 5, 10)
+    sp = C.cast(spans, C.POINTER(C.c_int32))
+    dup = (C.c_int32 * 2)(1, 1)
+    cases = [
+        (L.CB_POLICY_RANDOM_DOC, L.SelectReq(10, 3, 0, 0, 0, 0, 2, sp,
+                                             C.cast(dup, C.POINTER(C.c_int32)), 0, 0)),
+        (L.CB_POLICY_RANDOM_DOC, L.SelectReq(10, 3, 0, 0, 0, 0, 2, sp, None, 0, 0)),
+        (L.CB_POLICY_FIXED_CHUNK, L.SelectReq(10, 3, 0, 0, 0, 0, 0, None, None, 0, 0)),
+        (L.CB_POLICY_FIXED_CHUNK, L.SelectReq(10, 3, 0, 0, 0, 0, 0, None, None, 4, 5)),
+        (7, L.SelectReq(10, 3, 0, 0, 0, 0, 2, sp, None, 0, 0)),
+    ]
+    for policy, req in cases:
+        st = lib.cb_kv_deviation_topk(C.c_void_p(16), 64, C.c_void_p(16), 64, 64, L.CB_F32,
+                                      C.byref(req), 1, policy, C.c_void_p(16), C.c_void_p(16),
+                                      ws, 4096, None)
+        assert st == L.CB_ERR_INVALID_ARG, policy
+        assert lib.cb_last_error_message()
 
 
 def test_select_count_matches_page_rule():

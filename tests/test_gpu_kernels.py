@@ -188,6 +188,80 @@ def test_doc_aligned_rolling_shape():
     assert idx[379] - idx[0] == 379                           # one contiguous window
 
 
+def test_span_policy_controls_match_oracle():
+    """"Request Order Matters" §2.3 / §4.4 controls and EPIC's first-token
+    rule, each exactly against the oracle on the GPU's own deviations;
+    integer-valued deviations in half of the cases give exact ties."""
+    rng = np.random.default_rng(15)
+    kvw = 64
+    for trial in range(30):
+        m = int(rng.integers(1, 10))
+        lens = rng.integers(0, 50, size=m)
+        offs = [0] + [int(x) for x in np.cumsum(lens)]
+        n = offs[-1]
+        if n == 0:
+            continue
+        k = int(rng.integers(1, n + 1))
+        if trial % 2 == 0:
+            kf = (rng.random((n, kvw)) < 0.1).astype(np.float32)
+        else:
+            kf = rng.standard_normal((n, kvw)).astype(np.float32)
+        kr = np.zeros_like(kf)
+        order = [int(x) for x in rng.permutation(m)]
+        L_, off_ = int(rng.integers(1, 40)), 0
+        off_ = int(rng.integers(0, L_ + 1))
+        cases = [
+            (L.CB_POLICY_SINGLE_WINDOW, dict(), lambda d: O.single_window_select(d, k)),
+            (L.CB_POLICY_FIXED_CHUNK, dict(span_len=L_, span_offset=off_),
+             lambda d: O.doc_aligned_select(d, O.fixed_chunk_offsets(n, L_, off_), k)),
+            (L.CB_POLICY_RANDOM_DOC, dict(span_offsets=offs, span_order=order),
+             lambda d: O.doc_aligned_select(d, offs, k, order=order)),
+            (L.CB_POLICY_FIRST_TOKENS, dict(span_offsets=offs),
+             lambda d: O.first_tokens_select(offs, k)),
+        ]
+        for policy, extra, ref_fn in cases:
+            d, idx = _sel_call(dev(kf), dev(kr), [dict(n_ctx=n, k=k, **extra)], policy)
+            ref = ref_fn(d[:n].astype(np.float64))
+            assert list(idx[:k]) == list(ref), (policy, offs, k)
+
+
+def test_span_policies_rolling_shape():
+    # 19 cached 400-token documents, k = 380 (5%); fixed 92-token spans
+    rng = np.random.default_rng(16)
+    n, kvw, k = 7600, 1024, 380
+    kf = bf16_values(rng.standard_normal((n, kvw)).astype(np.float32))
+    kr = bf16_values(kf + (rng.standard_normal((n, kvw)) * 0.3).astype(np.float32))
+    offs = list(range(0, n + 1, 400))
+    order = [int(x) for x in rng.permutation(19)]
+    for policy, extra, ref_fn in (
+            (L.CB_POLICY_SINGLE_WINDOW, dict(), lambda d: O.single_window_select(d, k)),
+            (L.CB_POLICY_FIXED_CHUNK, dict(span_len=92, span_offset=46),
+             lambda d: O.doc_aligned_select(d, O.fixed_chunk_offsets(n, 92, 46), k)),
+            (L.CB_POLICY_RANDOM_DOC, dict(span_offsets=offs, span_order=order),
+             lambda d: O.doc_aligned_select(d, offs, k, order=order)),
+            (L.CB_POLICY_FIRST_TOKENS, dict(span_offsets=offs),
+             lambda d: O.first_tokens_select(offs, k))):
+        d, idx = _sel_call(dev(kf, torch.bfloat16), dev(kr, torch.bfloat16),
+                           [dict(n_ctx=n, k=k, **extra)], policy)
+        assert list(idx[:k]) == list(ref_fn(d[:n].astype(np.float64))), policy
+        assert O.selection_segments(idx[:k]) >= 1
+
+
+def test_span_policy_arguments_are_validated():
+    kf = torch.zeros(10, 64, device="cuda")
+    bad = [
+        (L.CB_POLICY_RANDOM_DOC, dict(n_ctx=10, k=3, span_offsets=[0, 5, 10], span_order=[0, 0])),
+        (L.CB_POLICY_RANDOM_DOC, dict(n_ctx=10, k=3, span_offsets=[0, 5, 10])),
+        (L.CB_POLICY_FIXED_CHUNK, dict(n_ctx=10, k=3, span_len=0)),
+        (L.CB_POLICY_FIXED_CHUNK, dict(n_ctx=10, k=3, span_len=4, span_offset=5)),
+        (L.CB_POLICY_FIRST_TOKENS, dict(n_ctx=10, k=3, span_offsets=[0, 5, 9])),
+    ]
+    for policy, r in bad:
+        with pytest.raises(L.CBError):
+            R.cb_kv_deviation_topk(kf, kf, [r], policy, torch.empty(10, device="cuda"),
+                                   torch.empty(10, dtype=torch.int32, device="cuda"))
+
+
 # ------------------------------------------------------- gather / scatter --
 @pytest.mark.parametrize("dt", DTYPES)
 def test_gather_scatter_exact(dt):
