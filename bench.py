@@ -52,11 +52,14 @@ def parse_args():
                          "(for ncu --profile-from-start off); prints no JSON")
     ap.add_argument("--layers", type=int, default=None,
                     help="truncate the stack (profiling captures on a small footprint)")
-    ap.add_argument("--workload", choices=["rag", "rolling", "qwen", "long"], default="rag",
+    ap.add_argument("--workload", choices=["rag", "rolling", "qwen", "long", "host_kv"],
+                    default="rag",
                     help="rag: the headline request (default); rolling: the 50-request "
                          "rolling-agent window, token top-k vs document-aligned at 5%%; "
                          "qwen: the Qwen3-8B-shaped batch of 4 at 30%%; long: the 32K "
-                         "batch of 2 at r = 5/10/20/30%% against full prefill")
+                         "batch of 2 at r = 5/10/20/30%% against full prefill; host_kv: "
+                         "the headline request with its chunk caches in pinned host "
+                         "memory, loaded layer by layer")
     return ap.parse_args()
 
 
@@ -708,6 +711,72 @@ def run_batch(args):
     print(json.dumps(line), flush=True)
 
 
+def run_host_kv(args):
+    """The headline request with its chunk caches in pinned host memory
+    (CacheBlend blog, "Hiding Recompute Behind I/O"): TTFT with the store in
+    HBM and with the store on the host, loaded layer by layer on a copy
+    stream while earlier layers compute; the per-layer KV load time against
+    the per-layer recompute time at several ratios, and the ratio the
+    loading controller picks (r = max(r_load, 15%))."""
+    import torch
+    import rag_kv_cache_layer_gb300 as R
+
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(device)
+    wl, model, store, reqs, plan, outs, _, tok_dev = setup_replica(0, device, args.layers)
+    rq = wl.requests[0]
+    n_layers = wl.model.n_layers
+    st = torch.cuda.current_stream()
+    hs = R.HostChunkStore(model, rq.n_ctx)
+    hs.prefill({sg.chunk_id: torch.from_numpy(sg.tokens).to(device)
+                for sg in rq.segments if sg.cached})
+    hreq = [R.Req(tok_dev, [hs.seg(sg.chunk_id) if sg.cached else R.Seg(len(sg.tokens))
+                            for sg in rq.segments])]
+    cs = torch.cuda.Stream(device)
+    dev_ms, _ = _graph_ms(lambda: model.cb_blend_prefill(reqs, RATIO_BP, outputs=outs),
+                          args.steps, st)
+    houts = model.alloc_outputs(model.plan_host_kv(hreq, RATIO_BP), 1)
+    host_ms, host_p95 = _graph_ms(
+        lambda: model.cb_blend_prefill_host_kv(hreq, RATIO_BP, cs, outputs=houts), args.steps, st)
+    # one layer of the request's chunk K/V, host -> device on a copy stream
+    kvw = model.kvw
+    n = rq.n_ctx
+    dst = torch.empty(2, n, kvw, dtype=model.dtype, device=device)
+    per = []
+    for _ in range(5 + args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(cs):
+            e0.record(cs)
+            dst[0].copy_(hs.K[5, :n], non_blocking=True)
+            dst[1].copy_(hs.V[5, :n], non_blocking=True)
+            e1.record(cs)
+        cs.synchronize()
+        per.append(e0.elapsed_time(e1))
+    load_ms = statistics.median(per[5:])
+    layer_bytes = 2 * n * kvw * dst.element_size()
+    table = {}
+    for r in (500, 1000, 1500, 3000, 5000, 10000):
+        o = model.alloc_outputs(model.plan(reqs, r), 1)
+        ms, _ = _graph_ms(lambda: model.cb_blend_prefill(reqs, r, outputs=o), args.steps, st)
+        table[r] = ms / n_layers
+        del o
+    chosen = R.loading_controller(load_ms, table)
+    line = {"metric": "blended-prefill TTFT with host-resident chunk caches (layer-wise load)",
+            "value": host_ms, "unit": "ms", "higher_is_better": False, "n_gpus": 1,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "llama3-8b-shape 32L, 6x512 chunks + 64 query, r=15%, "
+                                   "chunk K/V in pinned host memory", "seq_len": rq.n_tokens},
+            "ttft_ms_device_store": dev_ms, "ttft_ms_host_store": host_ms,
+            "ttft_ms_host_store_p95": host_p95,
+            "load_ms_per_layer": load_ms,
+            "h2d_GBps": layer_bytes / (load_ms / 1e3) / 1e9,
+            "recompute_ms_per_layer": {f"r={r / 100:g}%": v for r, v in table.items()},
+            "loading_controller_ratio": f"{chosen / 100:g}%"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -716,6 +785,8 @@ def main():
         run_rolling(args)
     elif args.workload in ("qwen", "long"):
         run_batch(args)
+    elif args.workload == "host_kv":
+        run_host_kv(args)
     else:
         run_ours(args)
 

@@ -507,6 +507,27 @@ cb_status cb_blend_prefill(cb_model *m, const cb_request *reqs, int B,
                            const cb_blend_params *p, const cb_blend_out *out,
                            void *ws, size_t ws_bytes, cb_stream stream);
 
+/* The same blended prefill with the chunk caches in pinned host memory
+ * ([CB] "Hiding Recompute Behind I/O"; [QCF] §4.4, layer-wise pipeline):
+ * every cached segment's k_pic / v_pic must be pinned (page-locked) host
+ * memory with the usual layer stride.  Layer l's slice of every segment is
+ * copied by the copy engines, on copy_stream, into a two-layer staging area
+ * of the workspace and re-positioned into the fused cache just before
+ * layer l runs on `stream`, so loading layer l + 2 overlaps computing layer
+ * l.  The copy stream is forked from and joined back into `stream` with the
+ * model's events, so a call can be captured into a CUDA graph; calls that
+ * share a model must be issued one at a time.  Results are those of
+ * cb_blend_prefill.  Workspace: cb_blend_plan_host_kv (cb_blend_plan plus
+ * the staging area, 4 * N_total * row_elems * dtype bytes).
+ * Errors: as cb_blend_prefill; CB_ERR_INVALID_ARG when a chunk cache is not
+ * pinned host memory or copy_stream is NULL or equal to stream. */
+cb_status cb_blend_plan_host_kv(const cb_model *m, const cb_request *reqs, int B,
+                                const cb_blend_params *p, cb_plan *out);
+cb_status cb_blend_prefill_host_kv(cb_model *m, const cb_request *reqs, int B,
+                                   const cb_blend_params *p, const cb_blend_out *out,
+                                   void *ws, size_t ws_bytes, cb_stream stream,
+                                   cb_stream copy_stream);
+
 /* Full prefill ([QCF] Eq. 2): every row of every layer is computed under
  * the whole request (segments' caches are ignored).  Fills k_cache,
  * v_cache, hidden (all T rows), rows (0..T_b-1) and first_token of `out`.

@@ -152,6 +152,11 @@ def _load():
         "cb_blend_prefill": (S, [vp, C.POINTER(Request), i32,
                                  C.POINTER(BlendParams), C.POINTER(BlendOut), vp,
                                  C.c_size_t, vp]),
+        "cb_blend_plan_host_kv": (S, [vp, C.POINTER(Request), i32, C.POINTER(BlendParams),
+                                      C.POINTER(Plan)]),
+        "cb_blend_prefill_host_kv": (S, [vp, C.POINTER(Request), i32,
+                                         C.POINTER(BlendParams), C.POINTER(BlendOut), vp,
+                                         C.c_size_t, vp, vp]),
         "cb_full_plan": (S, [vp, C.POINTER(Request), i32, C.POINTER(Plan)]),
         "cb_full_prefill": (S, [vp, C.POINTER(Request), i32, C.POINTER(BlendOut),
                                 vp, C.c_size_t, vp]),
@@ -180,7 +185,8 @@ EXPORTED = [
     "cb_gather_rows", "cb_scatter_kv", "cb_attention_workspace_size",
     "cb_sparse_query_attention",
     "cb_model_create", "cb_model_destroy", "cb_linear", "cb_blend_plan",
-    "cb_blend_prefill", "cb_full_plan", "cb_full_prefill",
+    "cb_blend_prefill", "cb_blend_plan_host_kv", "cb_blend_prefill_host_kv",
+    "cb_full_plan", "cb_full_prefill",
     "cb_layer_workspace_size", "cb_blend_layer",
 ]
 

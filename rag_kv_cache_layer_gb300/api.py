@@ -19,7 +19,8 @@ __all__ = [
     "cb_kv_deviation_topk", "cb_kv_deviation_topk_noalloc", "cb_gather_rows",
     "cb_scatter_kv",
     "cb_sparse_query_attention", "cb_debug_expire_wait", "cb_debug_gemm_path", "Seg", "Req",
-    "BlendModel", "ChunkStore", "RollingWindow", "selection_stats", "select_count",
+    "BlendModel", "ChunkStore", "HostChunkStore", "RollingWindow", "selection_stats",
+    "loading_controller", "select_count",
     "device_status",
 ]
 
@@ -364,6 +365,34 @@ class BlendModel:
                                    C.byref(o), _p(ws), ws.numel(), _s(stream)))
         return outputs
 
+    def cb_blend_prefill_host_kv(self, reqs, ratio_bp, copy_stream, policy=0, sel_layer=1,
+                                 outputs=None, stream=None, span_len=0, span_offset=0,
+                                 span_order=None, schedule=None):
+        """cb_blend_prefill with the requests' chunk caches in pinned host
+        memory (HostChunkStore segments), loaded layer by layer on
+        copy_stream while earlier layers compute."""
+        arr, keep = _requests(reqs)
+        p, sch = self._params(ratio_bp, policy, sel_layer, schedule, None, span_len,
+                              span_offset, span_order)
+        if outputs is None:
+            plan = L.Plan()
+            check(lib.cb_blend_plan_host_kv(self.handle, arr, len(reqs), C.byref(p),
+                                            C.byref(plan)))
+            outputs = self.alloc_outputs(plan, len(reqs))
+        o = self._out(outputs)
+        ws = outputs["workspace"]
+        check(lib.cb_blend_prefill_host_kv(self.handle, arr, len(reqs), C.byref(p),
+                                           C.byref(o), _p(ws), ws.numel(), _s(stream),
+                                           _s(copy_stream)))
+        return outputs
+
+    def plan_host_kv(self, reqs, ratio_bp, policy=0, sel_layer=1):
+        arr, keep = _requests(reqs)
+        p, sch = self._params(ratio_bp, policy, sel_layer, None)
+        out = L.Plan()
+        check(lib.cb_blend_plan_host_kv(self.handle, arr, len(reqs), C.byref(p), C.byref(out)))
+        return out
+
     def cb_full_prefill(self, reqs, outputs=None, layer_stride=0, stream=None):
         arr, keep = _requests(reqs)
         if outputs is None:
@@ -451,6 +480,54 @@ class ChunkStore:
     def seg(self, cid) -> Seg:
         r, n = self.where[cid]
         return Seg(n, self.K[0, r], self.V[0, r], self.capacity * self.model.kvw, 0)
+
+
+class HostChunkStore:
+    """Chunk caches kept in pinned host memory, [n_layers][rows][kvw] per K
+    and V (the store CacheBlend loads from CPU memory or disk, "Hiding
+    Recompute Behind I/O").  A chunk is prefilled standalone on the device
+    (QCFuse Eq. 3) and its caches are copied to the host pool; requests use
+    it through BlendModel.cb_blend_prefill_host_kv."""
+
+    def __init__(self, model: BlendModel, capacity_rows: int):
+        s = model.shape
+        self.model = model
+        self.capacity = capacity_rows
+        self.K = torch.empty(s.n_layers, capacity_rows, model.kvw, dtype=model.dtype).pin_memory()
+        self.V = torch.empty_like(self.K).pin_memory()
+        self.where = {}
+        self.used = 0
+
+    def prefill(self, chunks: dict, stream=None):
+        """chunks: {chunk_id: device int32 tokens}; computed on the device,
+        then copied to the host pool (not part of a request's TTFT)."""
+        n = sum(int(t.numel()) for t in chunks.values())
+        if self.used + n > self.capacity:
+            raise RuntimeError("host chunk store is full")
+        tmp = ChunkStore(self.model, n)
+        tmp.prefill(chunks, stream)
+        torch.cuda.synchronize()
+        for cid, t in chunks.items():
+            r, m = tmp.where[cid]
+            self.K[:, self.used:self.used + m].copy_(tmp.K[:, r:r + m])
+            self.V[:, self.used:self.used + m].copy_(tmp.V[:, r:r + m])
+            self.where[cid] = (self.used, m)
+            self.used += m
+        del tmp
+
+    def seg(self, cid) -> Seg:
+        r, n = self.where[cid]
+        return Seg(n, self.K[0, r], self.V[0, r], self.capacity * self.model.kvw, 0)
+
+
+def loading_controller(load_ms_per_layer: float, compute_ms_per_layer: dict,
+                       min_ratio_bp: int = 1500) -> int:
+    """Recompute ratio that the layer-wise load hides ([CB] "Hiding
+    Recompute Behind I/O": r = max(r_load, 15%)): the largest measured ratio
+    whose per-layer recompute time does not exceed the per-layer KV load
+    time, and at least min_ratio_bp.  compute_ms_per_layer: {ratio_bp: ms}."""
+    fits = [r for r, ms in compute_ms_per_layer.items() if ms <= load_ms_per_layer]
+    return max([min_ratio_bp] + fits)
 
 
 class RollingWindow:

@@ -397,6 +397,14 @@ struct cb_model {
   std::vector<cb_layer_weights> layers;
   int qw, kvw, qkv_rows;
   size_t eb;
+  // ordering events of the host-resident chunk path (copy stream <-> compute
+  // stream): fork, per staging buffer "copied" and "consumed"
+  cudaEvent_t ev_fork = nullptr, ev_copied[2] = {nullptr, nullptr},
+              ev_free[2] = {nullptr, nullptr};
+  ~cb_model() {
+    for (cudaEvent_t e : {ev_fork, ev_copied[0], ev_copied[1], ev_free[0], ev_free[1]})
+      if (e) cudaEventDestroy(e);
+  }
 };
 
 extern "C" cb_status cb_model_create(const cb_model_config *cfg, const cb_weights *w,
@@ -429,6 +437,13 @@ extern "C" cb_status cb_model_create(const cb_model_config *cfg, const cb_weight
   if (!(prop.major == 10 && prop.minor == 3))
     return fail(CB_ERR_UNSUPPORTED, "device sm_%d%d: this library is built for sm_103a", prop.major, prop.minor);
   cb_model *m = new cb_model;
+  for (cudaEvent_t *e : {&m->ev_fork, &m->ev_copied[0], &m->ev_copied[1], &m->ev_free[0],
+                         &m->ev_free[1]}) {
+    if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) {
+      delete m;
+      return fail(CB_ERR_CUDA, "cudaEventCreate failed");
+    }
+  }
   m->cfg = c;
   m->w = *w;
   m->layers.assign(w->layers, w->layers + c.n_layers);
@@ -559,6 +574,8 @@ struct Plan {
   LayerOffsets lay;
   size_t h_all, kf, dev, sel, pos_all, glob_all, pos_c, glob_c, h_c, lm_x, lm_best, total;
   size_t g_dev = 0, g_keep = 0, g_sel = 0, g_pos = 0, g_glob = 0, g_src = 0, g_h = 0;
+  // host-resident chunk path: two layers of the context K/V in flight
+  size_t stage = 0, stage_bytes = 0;     // stage_bytes: K of one layer (V follows)
 };
 
 }  // namespace
@@ -612,7 +629,8 @@ static int select_count(int n_ctx, int ratio_bp) {
 }
 
 static cb_status make_plan(const cb_model *m, const cb_request *reqs, int B,
-                           const cb_blend_params *p, bool blend, Plan &P) {
+                           const cb_blend_params *p, bool blend, Plan &P,
+                           bool host_kv = false) {
   CB_TRY(validate_requests(m, reqs, B, blend));
   if (blend) {
     if (!p) return fail(CB_ERR_INVALID_ARG, "params is NULL");
@@ -708,6 +726,11 @@ static cb_status make_plan(const cb_model *m, const cb_request *reqs, int B,
     P.g_glob = cv.take((P.R_total + 1) * sizeof(int32_t));
     P.g_src = cv.take((P.R_total + 1) * sizeof(int32_t));
     P.g_h = cv.take((P.R_total + 1) * c.d_model * sizeof(float));
+  }
+  if (host_kv) {
+    P.stage_bytes = (size_t)(P.N_total + 1) * m->kvw * m->eb;
+    P.stage_bytes = (P.stage_bytes + 255) / 256 * 256;
+    P.stage = cv.take(4 * P.stage_bytes);         // [buffer][K, V]
   }
   P.total = cv.off;
   return CB_OK;
@@ -894,11 +917,16 @@ static cb_status filter_rows(cb_model *m, int l, const BatchMeta &cur, const Bat
   return CB_OK;
 }
 
-extern "C" cb_status cb_blend_prefill(cb_model *m, const cb_request *reqs, int B,
-                                      const cb_blend_params *p, const cb_blend_out *out,
-                                      void *ws_v, size_t ws_bytes, cb_stream stream) {
+// host_kv: the cached segments' K/V are in pinned host memory; each layer's
+// slice is copied (copy engines, on copy_stream) into a two-layer staging
+// area and stitched right before the layer runs, so the load of layer l + 1
+// overlaps the compute of layer l ([CB] "Hiding Recompute Behind I/O").
+static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
+                            const cb_blend_params *p, const cb_blend_out *out, void *ws_v,
+                            size_t ws_bytes, cudaStream_t stream, bool host_kv,
+                            cudaStream_t copy_stream) {
   Plan P;
-  CB_TRY(make_plan(m, reqs, B, p, true, P));
+  CB_TRY(make_plan(m, reqs, B, p, true, P, host_kv));
   CB_TRY(check_out(m, out));
   if (!ws_v || ws_bytes < P.total) return fail(CB_ERR_WORKSPACE, "workspace too small (%zu < %zu)", ws_bytes, P.total);
   char *ws = (char *)ws_v;
@@ -927,11 +955,60 @@ extern "C" cb_status cb_blend_prefill(cb_model *m, const cb_request *reqs, int B
       descs.push_back(cb_stitch_desc{sg.k_pic, sg.v_pic, sg.pic_layer_stride, sg.len,
                                      P.bm.t_off[b] + pos0, pos0 - sg.pic_pos0});
     }
-  probe_mark(CB_PROBE_STITCH, true, s);
-  CB_CUDA(launch_reposition(descs.data(), (int)descs.size(), s_layer, L, out->k_cache,
-                            out->v_cache, lstride, m->kvw, c.head_dim, m->w.rope_table,
-                            c.dtype, st, s));
-  probe_mark(CB_PROBE_STITCH, false, s);
+  // host-resident chunks: per-layer copies into the staging area, stitched
+  // one layer at a time; stage[l & 1] holds layer l as [N_total][kvw]
+  const size_t sb = P.stage_bytes;
+  auto stage_k = [&](int l) { return ws + P.stage + (size_t)(l & 1) * 2 * sb; };
+  auto stage_v = [&](int l) { return ws + P.stage + (size_t)(l & 1) * 2 * sb + sb; };
+  auto issue_copies = [&](int l) -> cb_status {
+    CB_CUDA(cudaStreamWaitEvent(copy_stream, m->ev_free[l & 1], 0));
+    for (int b = 0; b < B; ++b)
+      for (int i = 0; i < reqs[b].n_segments; ++i) {
+        const cb_segment &sg = reqs[b].segments[i];
+        if (!sg.k_pic || sg.len == 0) continue;
+        const size_t off = ((size_t)P.n_off[b] + P.seg_start[b][i]) * m->kvw * m->eb;
+        const size_t bytes = (size_t)sg.len * m->kvw * m->eb;
+        const size_t src = (size_t)l * sg.pic_layer_stride * m->eb;
+        CB_CUDA(cudaMemcpyAsync(stage_k(l) + off, (const char *)sg.k_pic + src, bytes,
+                                cudaMemcpyHostToDevice, copy_stream));
+        CB_CUDA(cudaMemcpyAsync(stage_v(l) + off, (const char *)sg.v_pic + src, bytes,
+                                cudaMemcpyHostToDevice, copy_stream));
+      }
+    CB_CUDA(cudaEventRecord(m->ev_copied[l & 1], copy_stream));
+    return CB_OK;
+  };
+  auto stitch_layer = [&](int l) -> cb_status {
+    std::vector<cb_stitch_desc> ld;
+    for (int b = 0; b < B; ++b)
+      for (int i = 0; i < reqs[b].n_segments; ++i) {
+        const cb_segment &sg = reqs[b].segments[i];
+        if (!sg.k_pic || sg.len == 0) continue;
+        const int pos0 = P.seg_start[b][i];
+        const size_t off = ((size_t)P.n_off[b] + pos0) * m->kvw * m->eb;
+        ld.push_back(cb_stitch_desc{stage_k(l) + off, stage_v(l) + off, 0, sg.len,
+                                    P.bm.t_off[b] + pos0, pos0 - sg.pic_pos0});
+      }
+    CB_CUDA(cudaStreamWaitEvent(s, m->ev_copied[l & 1], 0));
+    CB_CUDA(launch_reposition(ld.data(), (int)ld.size(), l, l + 1, out->k_cache, out->v_cache,
+                              lstride, m->kvw, c.head_dim, m->w.rope_table, c.dtype, st, s));
+    CB_CUDA(cudaEventRecord(m->ev_free[l & 1], s));
+    return CB_OK;
+  };
+  if (host_kv) {
+    // fork the copy stream from the compute stream (a graph capture then
+    // covers both); both staging buffers start free
+    CB_CUDA(cudaEventRecord(m->ev_fork, s));
+    CB_CUDA(cudaStreamWaitEvent(copy_stream, m->ev_fork, 0));
+    CB_CUDA(cudaEventRecord(m->ev_free[0], s));
+    CB_CUDA(cudaEventRecord(m->ev_free[1], s));
+    for (int l = s_layer; l < L && l < s_layer + 2; ++l) CB_TRY(issue_copies(l));
+  } else {
+    probe_mark(CB_PROBE_STITCH, true, s);
+    CB_CUDA(launch_reposition(descs.data(), (int)descs.size(), s_layer, L, out->k_cache,
+                              out->v_cache, lstride, m->kvw, c.head_dim, m->w.rope_table,
+                              c.dtype, st, s));
+    probe_mark(CB_PROBE_STITCH, false, s);
+  }
   // 2. embeddings of every row, full layers below the selection layer
   const int32_t *toks[CB_MAX_BATCH];
   for (int b = 0; b < B; ++b) toks[b] = reqs[b].tokens;
@@ -944,6 +1021,7 @@ extern "C" cb_status cb_blend_prefill(cb_model *m, const cb_request *reqs, int B
                          layer_ptr(out->k_cache, l, lstride, m->eb),
                          layer_ptr(out->v_cache, l, lstride, m->eb), S, st, s));
   // 3. selection layer: fresh keys of every row, deviation, ranking
+  if (host_kv) CB_TRY(stitch_layer(s_layer));
   {
     const cb_layer_weights &Ls = m->layers[s_layer];
     void *kf = ws + P.kf;
@@ -1020,6 +1098,10 @@ extern "C" cb_status cb_blend_prefill(cb_model *m, const cb_request *reqs, int B
   size_t next_step = 0;
   std::vector<AttnReq> ar_c(B);
   for (int l = s_layer; l < L; ++l) {
+    if (host_kv) {
+      if (l > s_layer) CB_TRY(stitch_layer(l));
+      if (l + 2 < L) CB_TRY(issue_copies(l + 2));
+    }
     if (next_step < P.sched.size() && P.sched[next_step].layer == l) {
       const Plan::Step &stp = P.sched[next_step++];
       CB_TRY(filter_rows(m, l, bm, stp.bm, (int)stp.R_total, h_b[cur], pos_b[cur], glob_b[cur],
@@ -1049,6 +1131,42 @@ extern "C" cb_status cb_blend_prefill(cb_model *m, const cb_request *reqs, int B
   if (out->first_token) CB_TRY(run_lm_head(m, P, h_b[0], bm.r_off, ws, out->first_token, s));
   probe_mark(CB_PROBE_LM_HEAD, false, s);
   return CB_OK;
+}
+
+extern "C" cb_status cb_blend_prefill(cb_model *m, const cb_request *reqs, int B,
+                                      const cb_blend_params *p, const cb_blend_out *out,
+                                      void *ws, size_t ws_bytes, cb_stream stream) {
+  return blend_impl(m, reqs, B, p, out, ws, ws_bytes, stream, false, nullptr);
+}
+
+extern "C" cb_status cb_blend_plan_host_kv(const cb_model *m, const cb_request *reqs, int B,
+                                           const cb_blend_params *p, cb_plan *out) {
+  if (!out) return fail(CB_ERR_INVALID_ARG, "out is NULL");
+  Plan P;
+  CB_TRY(make_plan(m, reqs, B, p, true, P, true));
+  fill_plan(P, out);
+  return CB_OK;
+}
+
+extern "C" cb_status cb_blend_prefill_host_kv(cb_model *m, const cb_request *reqs, int B,
+                                              const cb_blend_params *p,
+                                              const cb_blend_out *out, void *ws,
+                                              size_t ws_bytes, cb_stream stream,
+                                              cb_stream copy_stream) {
+  if (!copy_stream || copy_stream == stream)
+    return fail(CB_ERR_INVALID_ARG, "copy_stream must be a stream other than stream");
+  if (!m || !reqs || B <= 0 || B > CB_MAX_BATCH) return fail(CB_ERR_INVALID_ARG, "bad model or requests");
+  for (int b = 0; b < B; ++b)
+    for (int i = 0; i < reqs[b].n_segments; ++i) {
+      const cb_segment &sg = reqs[b].segments[i];
+      if (!sg.k_pic || sg.len == 0) continue;
+      for (const void *ptr : {sg.k_pic, sg.v_pic}) {
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess || a.type != cudaMemoryTypeHost)
+          return fail(CB_ERR_INVALID_ARG, "request %d segment %d: chunk caches must be pinned host memory", b, i);
+      }
+    }
+  return blend_impl(m, reqs, B, p, out, ws, ws_bytes, stream, true, copy_stream);
 }
 
 extern "C" cb_status cb_full_prefill(cb_model *m, const cb_request *reqs, int B,

@@ -380,3 +380,52 @@ def test_span_policies_in_blend_match_oracle(tiny, name, policy, kw):
     assert_close(host(out["v_cache"]), ref.V, torch.float32)
     Rn = len(ref.rows)
     assert_close(host(out["hidden"][:Rn]), ref.hidden, torch.float32)
+
+
+# ------------------------------------------- host-resident chunk caches --
+def test_host_resident_chunks_match_device_store(tiny):
+    """[CB] "Hiding Recompute Behind I/O": the chunk caches stay in pinned
+    host memory and are loaded layer by layer on a second stream; the fused
+    cache, selection and hidden states equal the device-resident blend bit
+    for bit (the fp32 path is deterministic), also when replayed from a CUDA
+    graph."""
+    rq = tiny.wl.requests[0]
+    hs = R.HostChunkStore(tiny.model, sum(len(sg.tokens) for sg in rq.segments if sg.cached))
+    hs.prefill({sg.chunk_id: torch.from_numpy(sg.tokens).cuda() for sg in rq.segments if sg.cached})
+    toks = torch.from_numpy(rq.tokens).cuda()
+    hreq = [R.Req(toks, [hs.seg(sg.chunk_id) if sg.cached else R.Seg(len(sg.tokens))
+                         for sg in rq.segments])]
+    ref = tiny.model.cb_blend_prefill(tiny.gpu_reqs(), 1500)
+    cs = torch.cuda.Stream()
+    out = tiny.model.cb_blend_prefill_host_kv(hreq, 1500, cs)
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    for key in ("k_cache", "v_cache", "selected", "deviation", "rows", "first_token"):
+        assert torch.equal(out[key], ref[key]), key
+    Rn = int((ref["rows"] >= 0).sum())
+    assert torch.equal(out["hidden"][:Rn], ref["hidden"][:Rn])
+    # CUDA graph: both streams are captured through the fork / join events
+    outs = {k: torch.empty_like(v) for k, v in out.items()}
+    tiny.model.cb_blend_prefill_host_kv(hreq, 1500, cs, outputs=outs)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        tiny.model.cb_blend_prefill_host_kv(hreq, 1500, cs, outputs=outs)
+    outs["k_cache"].zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(outs["k_cache"], ref["k_cache"])
+
+
+def test_host_resident_path_rejects_device_memory_and_one_stream(tiny):
+    cs = torch.cuda.Stream()
+    with pytest.raises(L.CBError):          # chunk caches on the device
+        tiny.model.cb_blend_prefill_host_kv(tiny.gpu_reqs(), 1500, cs)
+    rq = tiny.wl.requests[0]
+    hs = R.HostChunkStore(tiny.model, sum(len(sg.tokens) for sg in rq.segments if sg.cached))
+    hs.prefill({sg.chunk_id: torch.from_numpy(sg.tokens).cuda() for sg in rq.segments if sg.cached})
+    hreq = [R.Req(torch.from_numpy(rq.tokens).cuda(),
+                  [hs.seg(sg.chunk_id) if sg.cached else R.Seg(len(sg.tokens))
+                   for sg in rq.segments])]
+    st = torch.cuda.current_stream()
+    with pytest.raises(L.CBError):          # copy stream must differ
+        tiny.model.cb_blend_prefill_host_kv(hreq, 1500, st, stream=st)

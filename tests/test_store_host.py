@@ -54,3 +54,14 @@ def test_selection_stats_match_the_definitions():
         seg, cap = api.selection_stats(torch.from_numpy(P), torch.from_numpy(d))
         assert seg == O.selection_segments(P)
         assert abs(cap - O.captured_deviation(P, d)) < 1e-12
+
+
+def test_loading_controller_picks_the_largest_hidden_ratio():
+    """CacheBlend blog, "Hiding Recompute Behind I/O": r = max(r_load, 15%),
+    r_load the largest ratio whose per-layer recompute fits in the per-layer
+    load time."""
+    table = {500: 0.10, 1500: 0.25, 3000: 0.45, 5000: 0.70, 10000: 1.30}
+    assert api.loading_controller(0.50, table) == 3000
+    assert api.loading_controller(0.05, table) == 1500      # nothing hidden: the floor
+    assert api.loading_controller(2.00, table) == 10000
+    assert api.loading_controller(0.30, table, min_ratio_bp=2000) == 2000
