@@ -47,7 +47,7 @@ __all__ = [
     "select_count", "token_topk", "doc_aligned_select", "blend_prefill",
     "first_token", "first_token_logits", "embed_rows", "kv_bytes_per_layer",
     "selection_segments", "captured_deviation", "single_window_select",
-    "fixed_chunk_offsets", "first_tokens_select",
+    "fixed_chunk_offsets", "first_tokens_select", "write_back",
     "BlendResult", "PrefillResult",
 ]
 
@@ -605,6 +605,28 @@ def captured_deviation(P, d) -> float:
     d = np.asarray(d, dtype=np.float64)
     total = float(d.sum())
     return float(d[np.asarray(P, dtype=np.int64)].sum()) / total if total > 0 else 0.0
+
+
+def write_back(result: "BlendResult", segments, m: Model):
+    """Cache write-back ("Request Order Matters" §4.2 and §5: each call both
+    consumes and updates the persistent cache): after a blended prefill,
+    every cached segment's fused K/V rows -- fresh where recomputed, reused
+    elsewhere -- are moved back to chunk-local positions (keys rotated by
+    minus the segment's request offset, QCFuse Eq. 4 inverted) and become
+    that chunk's stored caches.  Returns the new (K, V) [n_layers][len][kvw]
+    of each cached segment, in request order."""
+    out = []
+    off = 0
+    for toks, cached in segments:
+        n = len(toks)
+        if cached:
+            K = np.stack([reposition_keys(result.K[l, off:off + n], -off, m.n_kv_heads,
+                                          m.head_dim, m.rope_base)
+                          for l in range(m.n_layers)])
+            V = result.V[:, off:off + n].copy()
+            out.append((K, V))
+        off += n
+    return out
 
 
 def kv_bytes_per_layer(context_len: int, kv_heads: int, head_dim: int,

@@ -232,3 +232,47 @@ def test_tiny_workload_runs():
     segs = [(s.tokens, s.cached) for s in req.segments]
     r = O.blend_prefill(m, segs, store, wl.ratio_bp)
     assert len(r.selected) == 57 and r.hidden.shape == (89, 256)
+
+
+# ------------------------------------------------------------ write-back --
+def test_write_back_of_a_full_recompute_is_the_full_prefill_cache():
+    """With every context token recomputed (rho = 1) the fused cache is the
+    full prefill's, so writing it back stores each chunk's full-prefill K/V
+    moved to position 0; re-stitching that store at the same offsets gives
+    the full prefill's cache again (rotations compose, QCFuse Eq. 4)."""
+    m = _model()
+    chunks, query, segs, store = _request(m)
+    full = O.full_prefill(m, np.concatenate(chunks + [query]))
+    r = O.blend_prefill(m, segs, store, ratio_bp=10000)
+    new = O.write_back(r, segs, m)
+    K, V = O.stitch(new, [len(c) for c in chunks], m.n_kv_heads, m.head_dim, m.rope_base)
+    N = sum(len(c) for c in chunks)
+    _close(K, full.K[:, :N], 1e-10)
+    _close(V, full.V[:, :N], 1e-12)
+
+
+def test_write_back_without_recompute_keeps_the_store():
+    """rho = 0 above layer 0: the fused cache of every layer >= 1 is the
+    stitched store, so write-back returns the stored caches there (up to
+    the rotation round trip); layer 0 (always recomputed) is the chunk's
+    own context-free layer-0 K/V, also unchanged."""
+    m = _model()
+    chunks, query, segs, store = _request(m)
+    r = O.blend_prefill(m, segs, store, ratio_bp=0)
+    new = O.write_back(r, segs, m)
+    for (k0, v0), (k1, v1) in zip(store, new):
+        _close(k1, k0, 1e-10)
+        _close(v1, v0, 1e-12)
+
+
+def test_write_back_makes_the_store_depend_on_history():
+    """"Request Order Matters" §4.2: the same chunk's stored caches differ
+    after it was reused behind different predecessors."""
+    m = _model()
+    chunks, query, segs, store = _request(m)
+    a = O.write_back(O.blend_prefill(m, segs, store, ratio_bp=5000), segs, m)
+    segs2 = [segs[1], segs[0], segs[2], segs[3]]
+    store2 = [store[1], store[0], store[2]]
+    b = O.write_back(O.blend_prefill(m, segs2, store2, ratio_bp=5000), segs2, m)
+    # chunk 1 was first in the second request: its layer >= 1 caches differ
+    assert np.abs(a[1][0][1:] - b[0][0][1:]).max() > 1e-6
