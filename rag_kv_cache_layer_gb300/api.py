@@ -481,6 +481,24 @@ class ChunkStore:
         r, n = self.where[cid]
         return Seg(n, self.K[0, r], self.V[0, r], self.capacity * self.model.kvw, 0)
 
+    def write_back(self, items, outputs, stream=None):
+        """Cache write-back ("Request Order Matters" §4.2, §5): replaces
+        stored chunks by their fused K/V from a blended prefill, keys rotated
+        back to chunk-local positions (cb_rope_reposition with a negative
+        shift, all layers).  items: (chunk_id, fused-cache row of the chunk's
+        first token, its request position); outputs: the prefill's outputs
+        (k_cache / v_cache [n_layers][T_total][kvw])."""
+        K, V = outputs["k_cache"], outputs["v_cache"]
+        descs = []
+        for cid, row, pos0 in items:
+            r, n = self.where[cid]
+            descs.append((K[0, row], V[0, row], K.stride(0), n, r, -int(pos0)))
+        for i in range(0, len(descs), 64):
+            cb_rope_reposition(descs[i:i + 64], 0, self.model.shape.n_layers, self.K, self.V,
+                               self.capacity * self.model.kvw, self.model.kvw,
+                               self.model.shape.head_dim, self.model.rope_table,
+                               self.model.max_positions, stream)
+
 
 class HostChunkStore:
     """Chunk caches kept in pinned host memory, [n_layers][rows][kvw] per K
@@ -539,8 +557,10 @@ class RollingWindow:
     the oldest document is evicted (stride 1)."""
 
     def __init__(self, model: BlendModel, window: int, doc_rows: int,
-                 ratio_bp: int, policy: int = L.CB_POLICY_DOC_ALIGNED):
+                 ratio_bp: int, policy: int = L.CB_POLICY_DOC_ALIGNED,
+                 write_back: bool = False):
         self.model = model
+        self.write_back = write_back      # store each request's fused caches back
         self.window = window
         self.ratio_bp = ratio_bp
         self.policy = policy
@@ -564,9 +584,18 @@ class RollingWindow:
         return Req(toks.to(torch.int32).contiguous(), segs)
 
     def blend(self, req, outputs=None, stream=None, **span_args):
-        """span_args: span_len / span_offset / span_order of cb_blend_params."""
-        return self.model.cb_blend_prefill([req], self.ratio_bp, self.policy,
-                                           outputs=outputs, stream=stream, **span_args)
+        """span_args: span_len / span_offset / span_order of cb_blend_params.
+        With write_back, the cached documents' fused K/V replace their
+        stored caches afterwards (the store then depends on history)."""
+        out = self.model.cb_blend_prefill([req], self.ratio_bp, self.policy,
+                                          outputs=outputs, stream=stream, **span_args)
+        if self.write_back:
+            items, pos = [], 0
+            for cid in self.docs:
+                items.append((cid, pos, pos))
+                pos += self.store.where[cid][1]
+            self.store.write_back(items, out, stream)
+        return out
 
     def advance(self, new_id, new_tokens, stream=None):
         """Stores the new document's chunk cache; evicts the oldest once the

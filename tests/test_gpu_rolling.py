@@ -32,11 +32,17 @@ def setup():
     return model, om, docs, queries, pic
 
 
+@pytest.mark.parametrize("write_back", [False, True])
 @pytest.mark.parametrize("policy", [L.CB_POLICY_TOKEN_TOPK, L.CB_POLICY_DOC_ALIGNED])
-def test_rolling_window_matches_oracle(setup, policy):
-    model, om, docs, queries, pic = setup
+def test_rolling_window_matches_oracle(setup, policy, write_back):
+    """With write_back the store is history dependent ("Request Order
+    Matters" §4.2): after every request the cached documents' fused K/V,
+    moved back to position 0, replace their stored caches -- on both
+    sides, so every later request checks the accumulated state."""
+    model, om, docs, queries, pic0 = setup
+    pic = dict(pic0)
     dev = lambda a: torch.from_numpy(np.asarray(a, np.int32)).cuda()
-    rw = R.RollingWindow(model, WINDOW, DOC, RATIO, policy)
+    rw = R.RollingWindow(model, WINDOW, DOC, RATIO, policy, write_back=write_back)
     rw.seed({i: dev(docs[i]) for i in range(WINDOW - 1)})
     name = "token_topk" if policy == L.CB_POLICY_TOKEN_TOPK else "doc_aligned"
     for t in range(N_REQ):
@@ -53,12 +59,22 @@ def test_rolling_window_matches_oracle(setup, policy):
         sel = out["selected"][:k].cpu().numpy()
         if policy == L.CB_POLICY_TOKEN_TOPK:
             assert ties_ok(sel, ref.selected, ref.deviation, k)
-        if set(sel) == set(ref.selected):  # else a deviation tie moved the set
+        if set(sel) != set(ref.selected):
+            assert not write_back, "the stores would diverge"
+        else:                               # else a deviation tie moved the set
             assert_close(host(out["k_cache"]), ref.K, torch.float32)
             assert_close(host(out["v_cache"]), ref.V, torch.float32)
             Rn = len(ref.rows)
             assert np.array_equal(out["rows"][:Rn].cpu().numpy(), ref.rows)
             assert_close(host(out["hidden"][:Rn]), ref.hidden, torch.float32)
+        if write_back:
+            for cid, kv in zip(cached, O.write_back(ref, segs, om)):
+                pic[cid] = kv
+            torch.cuda.synchronize()
+            for cid in cached:             # the GPU store holds the same state
+                r0, n = rw.store.where[cid]
+                assert_close(host(rw.store.K[:, r0:r0 + n]), pic[cid][0], torch.float32)
+                assert_close(host(rw.store.V[:, r0:r0 + n]), pic[cid][1], torch.float32)
         rw.advance(new_id, dev(docs[new_id]))
     # the store cycles through fixed slots: one window of documents
     assert rw.store.used == (WINDOW - 1) * DOC
