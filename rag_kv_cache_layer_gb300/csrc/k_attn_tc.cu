@@ -9,20 +9,21 @@
 // last query's position.
 //
 // Roles (192 threads, two CTAs per SM): warp 0 TMA producer (Q once, then
-// 128-key K and V blocks, 128-byte swizzle); warp 1 owns 256 TMEM columns
-// and issues tcgen05.mma: S_j = Q K_j^T into columns 0..127 (K-major
-// operands) and O += P_j V_j into columns 128..255 with P_j read from TMEM
-// (it overwrites S_j) and V MN-major from shared memory; warps 2..5 do the
-// online softmax (one row per thread, log2 domain, causal mask) and store
-// P_j as packed bf16 into TMEM.  Within a CTA the steps are serial
-// (S_{j+1} waits for P_j V_j); the SM's other CTA keeps the tensor core
-// busy meanwhile.  The row's reference maximum m only moves when a block
-// raises the maximum by more than 2^kRescale: then O and l are scaled by
-// 2^(m_old - m_new) (O is stable then: P_{j-1} V_{j-1} completed before
-// S_j was issued).  Between moves the probabilities stay below 2^kRescale,
-// and O / l does not depend on the reference, so the result is the same
-// softmax.  One exponential in four runs on the FMA pipe (exp2_poly) to
-// relieve the SFU.  All waits are bounded.
+// double-buffered 64-key K and V blocks, 128-byte swizzle); warp 1 owns 256
+// TMEM columns and issues tcgen05.mma: S_j = Q K_j^T into slot j & 1
+// (columns 0..63 or 64..127, K-major operands) and O += P_j V_j into columns
+// 128..255 with P_j read from TMEM (it overwrites S_j in its slot) and V
+// MN-major from shared memory; warps 2..5 do the online softmax (one row
+// per thread, log2 domain, causal mask) and store P_j as packed bf16 into
+// TMEM.  With two S slots the tensor core computes S_{j+1} while the
+// softmax works on S_j, so the softmax warps run block after block; the
+// SM's other CTA fills the remaining tensor-core time.  The row's reference
+// maximum m only moves when a block raises the maximum by more than
+// 2^kRescale: then O (after P_{j-1} V_{j-1} has landed) and l are scaled by
+// 2^(m_old - m_new).  Between moves the probabilities stay below
+// 2^kRescale, and O / l does not depend on the reference, so the result is
+// the same softmax.  One exponential in four runs on the FMA pipe
+// (exp2_poly) to relieve the SFU.  All waits are bounded.
 //
 // When the query tiles alone cannot fill the SMs (the compact layers), the
 // key range of every tile is split into chunks processed by separate CTAs;
@@ -42,17 +43,18 @@ namespace attn {
 constexpr int kThreads = 192;
 constexpr float kRescale = 8.f;            // log2 of the largest p between rescales
 constexpr int HD = 128;
-constexpr int BN = 128;                    // keys per block
-constexpr int kAtom = 128 * 64 * 2;        // one [128 rows x 64 bf16] swizzle tile
+constexpr int BN = 64;                     // keys per block
+constexpr int kAtom = 128 * 64 * 2;        // one [128 rows x 64 bf16] swizzle tile (Q)
+constexpr int kAtomKV = BN * 64 * 2;       // one [64 keys x 64 bf16] swizzle tile
 constexpr int kQ = 2 * kAtom;              // Q tile: 128 rows x 128 dims
-constexpr int kKV = 2 * kAtom;             // K or V block: 128 keys x 128 dims
-// smem: Q | K | V | barriers   (96 KB + barriers): two CTAs fit on an SM
+constexpr int kKV = 2 * kAtomKV;           // K or V block: 64 keys x 128 dims
+// smem: Q | K[2] | V[2] | barriers   (96 KB + barriers): two CTAs fit on an SM
 constexpr int kOffK = kQ;
-constexpr int kOffV = kOffK + kKV;
-constexpr int kOffBar = kOffV + kKV;
+constexpr int kOffV = kOffK + 2 * kKV;
+constexpr int kOffBar = kOffV + 2 * kKV;
 constexpr int kSmem = kOffBar + 256 + 1024;
 constexpr int kCtasPerSm = 2;
-constexpr int kTmemCols = 256;             // S/P 0..127, O 128..255
+constexpr int kTmemCols = 256;             // S/P slots 0..63, 64..127; O 128..255
 static_assert(kCtasPerSm * (kSmem + 1024) <= 233472, "two attention CTAs must fit an SM");
 
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) {
@@ -75,9 +77,9 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t saddr, uint32_t lbo) {
   return d;
 }
 
-constexpr uint32_t idesc(bool b_mn_major) {
+constexpr uint32_t idesc(bool b_mn_major, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-         ((uint32_t)(128 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map,
@@ -257,14 +259,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
   uint64_t *q_full = bar + 0;
-  uint64_t *k_full = bar + 1;      // K_j landed
-  uint64_t *k_empty = bar + 2;     // S_j = Q K_j^T done with K_j
-  uint64_t *v_full = bar + 3;      // V_j landed
-  uint64_t *v_empty = bar + 4;     // P_j V_j done with V_j
-  uint64_t *s_full = bar + 5;      // S_j in TMEM
-  uint64_t *p_full = bar + 6;      // P_j in TMEM (and O rescaled)
-  uint64_t *pv_done = bar + 7;     // O += P_j V_j has landed
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 8);
+  uint64_t *k_full = bar + 1;      // [2] K_j landed
+  uint64_t *k_empty = bar + 3;     // [2] S_j = Q K_j^T done with K_j
+  uint64_t *v_full = bar + 5;      // [2] V_j landed
+  uint64_t *v_empty = bar + 7;     // [2] P_j V_j done with V_j
+  uint64_t *s_full = bar + 9;      // [2] S_j in its TMEM slot
+  uint64_t *p_full = bar + 11;     // [2] P_j in the slot (and O rescaled)
+  uint64_t *pv_done = bar + 13;    // [2] O += P_j V_j has landed
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 15);
   volatile int *fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
   __shared__ int s_unit[6];        // b, g, tile, first block, end block
 
@@ -285,13 +287,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
     s_unit[3] = jb;
     s_unit[4] = max(jb, min(nb_tile, jb + P.chunk_blocks));
     mbar_init(smem_u32(q_full), 1);
-    mbar_init(smem_u32(k_full), 1);
-    mbar_init(smem_u32(k_empty), 1);
-    mbar_init(smem_u32(v_full), 1);
-    mbar_init(smem_u32(v_empty), 1);
-    mbar_init(smem_u32(s_full), 1);
-    mbar_init(smem_u32(p_full), 128);
-    mbar_init(smem_u32(pv_done), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&k_full[i]), 1);
+      mbar_init(smem_u32(&k_empty[i]), 1);
+      mbar_init(smem_u32(&v_full[i]), 1);
+      mbar_init(smem_u32(&v_empty[i]), 1);
+      mbar_init(smem_u32(&s_full[i]), 1);
+      mbar_init(smem_u32(&p_full[i]), 128);
+      mbar_init(smem_u32(&pv_done[i]), 1);
+    }
     *fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -319,10 +323,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (nb > 0 && warp == 0 && lane < 2) {
+  if (warp == 0 && lane < 2) {
     // ----------------------------------------------- producers (K: lane 0, V: lane 1)
-    // Two loaders, so K_{j+1} is fetched as soon as S_j has used K_j,
-    // whatever V is doing.
     const CUtensorMap *map = lane == 0 ? &mapK : &mapV;
     uint64_t *full = lane == 0 ? k_full : v_full;
     uint64_t *empty = lane == 0 ? k_empty : v_empty;
@@ -336,50 +338,62 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
                       (g * P.G + h) * HD + half * 64, row0);
     }
     for (int j = 0; j < nb; ++j) {
-      if (!mbar_wait_bounded(smem_u32(empty), (j & 1) ^ 1, kWaitLimitNs, status) || *fail) {
+      const int sl = j & 1;
+      if (!mbar_wait_bounded(smem_u32(&empty[sl]), ((j >> 1) & 1) ^ 1, kWaitLimitNs, status) ||
+          *fail) {
         *fail = 1;
         break;
       }
-      const uint32_t fb = smem_u32(full);
+      const uint32_t fb = smem_u32(&full[sl]);
       expect_tx(fb, kKV);
       const int key_row = (int)R.kv_row0 + (jb + j) * BN;
       for (int half = 0; half < 2; ++half)
-        tma_load_2d(smem_u32(smem + off + half * kAtom), map, fb, g * HD + half * 64, key_row);
+        tma_load_2d(smem_u32(smem + off + sl * kKV + half * kAtomKV), map, fb,
+                    g * HD + half * 64, key_row);
     }
-  } else if (nb > 0 && warp == 1 && lane == 0) {
+  } else if (warp == 1 && lane == 0) {
     // ----------------------------------------------------------------- MMA
-    const uint32_t idS = idesc(false), idPV = idesc(true);
+    const uint32_t idS = idesc(false, BN), idPV = idesc(true, HD);
     const uint32_t q_addr = smem_u32(smem);
-    const uint32_t k_addr = smem_u32(smem + kOffK), v_addr = smem_u32(smem + kOffV);
     bool ok = mbar_wait_bounded(smem_u32(q_full), 0, kWaitLimitNs, status);
-    for (int j = 0; j < nb && ok && !*fail; ++j) {
-      const uint32_t ph = j & 1;
-      // S_j overwrites P_{j-1}: its P V must have completed
-      if (!mbar_wait_bounded(smem_u32(k_full), ph, kWaitLimitNs, status) ||
-          (j > 0 && !mbar_wait_bounded(smem_u32(pv_done), ph ^ 1, kWaitLimitNs, status))) {
-        ok = false;
-        break;
-      }
+    // S_j into slot j & 1; the slot held P_{j-2}, so P_{j-2} V_{j-2} must be done
+    auto issue_s = [&](int j) -> bool {
+      const int sl = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!mbar_wait_bounded(smem_u32(&k_full[sl]), ph, kWaitLimitNs, status)) return false;
+      if (j >= 2 && !mbar_wait_bounded(smem_u32(&pv_done[sl]), ph ^ 1, kWaitLimitNs, status))
+        return false;
       fence_after();
+      const uint32_t k_addr = smem_u32(smem + kOffK + sl * kKV);
 #pragma unroll
       for (int k = 0; k < HD / 16; ++k) {
-        const uint32_t off = (k >> 2) * kAtom + (k & 3) * 32;
-        mma(tmem, desc_kmajor(q_addr + off), desc_kmajor(k_addr + off), idS, k > 0);
+        const uint32_t qo = (k >> 2) * kAtom + (k & 3) * 32;
+        const uint32_t ko = (k >> 2) * kAtomKV + (k & 3) * 32;
+        mma(tmem + sl * BN, desc_kmajor(q_addr + qo), desc_kmajor(k_addr + ko), idS, k > 0);
       }
-      commit(smem_u32(s_full));
-      commit(smem_u32(k_empty));
-      if (!mbar_wait_bounded(smem_u32(p_full), ph, kWaitLimitNs, status) ||
-          !mbar_wait_bounded(smem_u32(v_full), ph, kWaitLimitNs, status)) {
+      commit(smem_u32(&s_full[sl]));
+      commit(smem_u32(&k_empty[sl]));
+      return true;
+    };
+    if (ok) ok = issue_s(0);
+    for (int j = 0; j < nb && ok && !*fail; ++j) {
+      const int sl = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (j + 1 < nb && !issue_s(j + 1)) { ok = false; break; }
+      if (!mbar_wait_bounded(smem_u32(&p_full[sl]), ph, kWaitLimitNs, status) ||
+          !mbar_wait_bounded(smem_u32(&v_full[sl]), ph, kWaitLimitNs, status)) {
         ok = false;
         break;
       }
       fence_after();
+      const uint32_t v_addr = smem_u32(smem + kOffV + sl * kKV);
 #pragma unroll
       for (int k = 0; k < BN / 16; ++k)
-        mma_ts(tmem + BN, tmem + k * 8, desc_mnmajor(v_addr + k * 16 * 128, kAtom), idPV,
+        mma_ts(tmem + 2 * BN, tmem + sl * BN + k * 8,
+               desc_mnmajor(v_addr + k * 16 * 128, kAtomKV), idPV,
                (j > 0 || k > 0) ? 1u : 0u);
-      commit(smem_u32(pv_done));
-      commit(smem_u32(v_empty));
+      commit(smem_u32(&pv_done[sl]));
+      commit(smem_u32(&v_empty[sl]));
     }
     if (!ok) *fail = 1;
   } else if (warp >= 2) {
@@ -391,48 +405,54 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
     int p = valid ? q_pos[row0 + qi] : 0;
     if (p < 0 || p >= R.kv_len) p = 0;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t sbase = tmem + lane_off;       // S_j, then P_j (packed bf16)
-    const uint32_t obase = tmem + lane_off + BN;
+    const uint32_t obase = tmem + lane_off + 2 * BN;
     float m = -INFINITY, l = 0.f;                 // reference max (log2 domain), sum
     const float sl2 = P.scale_log2;
     bool failed = false;
+    auto pv_landed = [&](int j) -> bool {
+      const bool bad = !mbar_wait_bounded(smem_u32(&pv_done[j & 1]), (j >> 1) & 1,
+                                          kWaitLimitNs, status) || *fail;
+      if (__any_sync(0xffffffffu, bad)) return false;
+      fence_after();
+      return true;
+    };
     for (int j = 0; j < nb; ++j) {
-      const uint32_t ph = j & 1;
+      const int sl = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
       const bool bad =
-          !mbar_wait_bounded(smem_u32(s_full), ph, kWaitLimitNs, status) || *fail;
+          !mbar_wait_bounded(smem_u32(&s_full[sl]), ph, kWaitLimitNs, status) || *fail;
       if (__any_sync(0xffffffffu, bad)) { failed = true; break; }
       fence_after();
+      const uint32_t sbase = tmem + lane_off + sl * BN;
       const int key0 = (jb + j) * BN;
       // Keys visible to this row: key0 .. p.  Blocks wholly at or before p
       // take the mask-free path.  Four partial maxima / sums keep the
       // dependency chains short.
       const int n_vis = p - key0 + 1;               // >= BN: no masking
-      // S_j: four loads in flight, one wait (the maximum); the P pass below
-      // reloads it in two halves
+      float x[BN];
+      ld32_nw(sbase, x);
+      ld32_nw(sbase + 32, x + 32);
+      wait_ld();
       float mx[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
-      {
-        float x[BN];
+      if (n_vis >= BN) {
 #pragma unroll
-        for (int c = 0; c < BN; c += 32) ld32_nw(sbase + c, x + c);
-        wait_ld();
-        if (n_vis >= BN) {
+        for (int i = 0; i < BN; ++i) mx[i & 3] = fmaxf(mx[i & 3], x[i]);
+      } else {
 #pragma unroll
-          for (int i = 0; i < BN; ++i) mx[i & 3] = fmaxf(mx[i & 3], x[i]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < BN; ++i)
-            if (i < n_vis) mx[i & 3] = fmaxf(mx[i & 3], x[i]);
-        }
+        for (int i = 0; i < BN; ++i)
+          if (i < n_vis) mx[i & 3] = fmaxf(mx[i & 3], x[i]);
       }
       const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
       // move the reference only for a large rise; the first visible key
       // always sets it (m = -inf before)
       const bool move = mloc > m + kRescale;
       const bool rescale = move && m != -INFINITY;  // O and l hold earlier blocks
-      if (__any_sync(0xffffffffu, rescale)) {
-        // the TMEM loads / stores are warp-wide; rows that keep m scale by 1
+      if (__any_sync(0xffffffffu, rescale) && j > 0) {
+        // O must hold P_{j-1} V_{j-1} first; the TMEM loads / stores are
+        // warp-wide, rows that keep m scale by 1
+        if (!pv_landed(j - 1)) { failed = true; break; }
         const float corr = rescale ? fast_exp2(m - mloc) : 1.f;
 #pragma unroll 1
         for (int c = 0; c < HD; c += 32) {
@@ -448,16 +468,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
       float ls[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) ls[i] = 0.f;
-      float x[BN];
-      // P_j for keys c..c+31 -> TMEM columns c/2 .. c/2+15; the first half of
-      // S_j is in registers before P overwrites any of it
+      // P_j for keys c..c+31 -> slot columns c/2 .. c/2+15 (S_j is in registers)
 #pragma unroll
       for (int c = 0; c < BN; c += 32) {
-        if ((c & 63) == 0) {
-          ld32_nw(sbase + c, x + c);
-          ld32_nw(sbase + c + 32, x + c + 32);
-          wait_ld();
-        }
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
@@ -477,18 +490,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
       wait_st();
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       fence_before();
-      arrive(smem_u32(p_full));
+      arrive(smem_u32(&p_full[sl]));
     }
     // the whole key range is in O once the last P V has landed
-    if (!failed && nb > 0) {
-      const bool bad = !mbar_wait_bounded(smem_u32(pv_done), (nb - 1) & 1, kWaitLimitNs,
-                                          status) || *fail;
-      if (__any_sync(0xffffffffu, bad)) failed = true;
-      fence_after();
-    }
+    if (!failed && !pv_landed(nb - 1)) failed = true;
     if (failed) *fail = 1;
     const bool ok = !failed && !*fail;
-    if (__any_sync(0xffffffffu, ok && nb > 0)) {
+    if (__any_sync(0xffffffffu, ok)) {
       // O chunks straight from TMEM to the output (warp-wide loads)
       const int q_row = row0 + qi, head = g * P.G + h;
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -523,8 +531,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   __syncthreads();
   if (warp == 0 && lane == 0 && *fail) {
     // drain the K/V copies this CTA may still have in flight
-    mbar_wait_bounded(smem_u32(k_full), 0, 10000000ull, nullptr);
-    mbar_wait_bounded(smem_u32(v_full), 0, 10000000ull, nullptr);
+    for (int i = 0; i < 2; ++i) {
+      mbar_wait_bounded(smem_u32(&k_full[i]), 0, 10000000ull, nullptr);
+      mbar_wait_bounded(smem_u32(&v_full[i]), 0, 10000000ull, nullptr);
+    }
   }
   __syncthreads();
   if (warp == 1) {
