@@ -122,9 +122,10 @@ unsigned long long cb_debug_launch_count(void);
 
 /* Which bf16 tensor-core GEMM the library uses for every projection issued
  * after the call (process-wide):
- *   CB_GEMM_AUTO (0)     per epilogue and row count, the faster of the two;
+ *   CB_GEMM_AUTO (0)     per epilogue, reduction length and row count, the
+ *                        form measured fastest;
  *   CB_GEMM_TOKEN_M (1)  token rows on the MMA's M side (128-row tiles);
- *   CB_GEMM_SWAP_AB (2)  weight rows on M, tokens on N (few-row form);
+ *   CB_GEMM_SWAP_AB (2)  weight rows on M, tokens on N;
  *   CB_GEMM_SWAP_AB_PAIR (3)  the same with each MMA spanning a pair of SMs
  *                        (2-CTA cluster, 256 weight rows per tile).
  * All compute the same function; tests use the switch to check each one

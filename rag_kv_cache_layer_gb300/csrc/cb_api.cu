@@ -469,11 +469,12 @@ static cb_status run_linear(const cb_model *m, const void *A, int64_t lda, const
     int *st;
     CB_TRY(status_ptr(&st));
     const int path = g_gemm_path.load(std::memory_order_relaxed);
-    const bool sab = path == CB_GEMM_SWAP_AB || path == CB_GEMM_SWAP_AB_PAIR ||
-                     (path == CB_GEMM_AUTO && gemm_sab_preferred(M, epi));
-    if (sab)
-      CB_CUDA(launch_gemm_sab(A, lda, W, W2, ldw, M, N, K, epi, out, ldo, qkv, st, s,
-                              path == CB_GEMM_SWAP_AB_PAIR ? 2 : 1));
+    const int form = path == CB_GEMM_AUTO        ? gemm_auto_form(M, K, epi)
+                     : path == CB_GEMM_SWAP_AB      ? 1
+                     : path == CB_GEMM_SWAP_AB_PAIR ? 2
+                                                    : 0;
+    if (form)
+      CB_CUDA(launch_gemm_sab(A, lda, W, W2, ldw, M, N, K, epi, out, ldo, qkv, st, s, form));
     else
       CB_CUDA(launch_gemm_tc(A, lda, W, W2, ldw, M, N, K, epi, out, ldo, qkv, st, s));
   } else {

@@ -181,8 +181,9 @@ cudaError_t launch_gemm_tc(const void *A, int64_t lda, const void *W,
                            GemmEpi epi, void *out, int64_t ldo,
                            const QkvEpi *qkv, int *status, cudaStream_t s);
 // The same GEMM with the operands swapped (weights on the MMA's M side,
-// tokens on N), for few rows; gemm_sab_preferred says when to use it.
-bool gemm_sab_preferred(int M, GemmEpi epi);
+// tokens on N).  gemm_auto_form picks the form for a shape: 0 = token rows
+// on M (launch_gemm_tc), 1 or 2 = swapped with that many CTAs per MMA.
+int gemm_auto_form(int M, int K, GemmEpi epi);
 // cta_group 2 runs each MMA on a pair of SMs (a 2-CTA cluster): 256 weight
 // rows per tile, the token operand split between the two CTAs.
 cudaError_t launch_gemm_sab(const void *A, int64_t lda, const void *W,

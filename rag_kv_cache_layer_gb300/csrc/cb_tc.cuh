@@ -72,6 +72,18 @@ __device__ __forceinline__ void commit(uint32_t bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
 }
+// One lane of a converged warp (elect.sync).  The producer and MMA roles run
+// their loops with the whole warp converged and issue through the elected
+// lane: a tcgen05.mma issued from a lone diverged lane costs several times
+// more issue time per instruction, which caps narrow (N < 256) tiles below
+// the tensor pipe's rate.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
 __device__ __forceinline__ void fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }

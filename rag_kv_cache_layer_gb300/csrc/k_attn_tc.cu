@@ -36,6 +36,7 @@
 
 #include "cb_common.cuh"
 #include "cb_internal.h"
+#include "cb_tc.cuh"
 
 namespace cb {
 namespace attn {
@@ -351,51 +352,61 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
         tma_load_2d(smem_u32(smem + off + sl * kKV + half * kAtomKV), map, fb,
                     g * HD + half * 64, key_row);
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
+    // The warp waits converged and one elected lane issues: tcgen05.mma from
+    // a lone diverged lane costs several times more issue time.
     const uint32_t idS = idesc(false, BN), idPV = idesc(true, HD);
     const uint32_t q_addr = smem_u32(smem);
-    bool ok = mbar_wait_bounded(smem_u32(q_full), 0, kWaitLimitNs, status);
+    auto wait_all = [&](uint64_t *b, uint32_t ph) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(b), ph, kWaitLimitNs, status));
+    };
+    bool ok = wait_all(q_full, 0);
     // S_j into slot j & 1; the slot held P_{j-2}, so P_{j-2} V_{j-2} must be done
     auto issue_s = [&](int j) -> bool {
       const int sl = j & 1;
       const uint32_t ph = (j >> 1) & 1;
-      if (!mbar_wait_bounded(smem_u32(&k_full[sl]), ph, kWaitLimitNs, status)) return false;
-      if (j >= 2 && !mbar_wait_bounded(smem_u32(&pv_done[sl]), ph ^ 1, kWaitLimitNs, status))
-        return false;
+      if (!wait_all(&k_full[sl], ph)) return false;
+      if (j >= 2 && !wait_all(&pv_done[sl], ph ^ 1)) return false;
       fence_after();
-      const uint32_t k_addr = smem_u32(smem + kOffK + sl * kKV);
+      if (tcx::elect_one()) {
+        const uint32_t k_addr = smem_u32(smem + kOffK + sl * kKV);
 #pragma unroll
-      for (int k = 0; k < HD / 16; ++k) {
-        const uint32_t qo = (k >> 2) * kAtom + (k & 3) * 32;
-        const uint32_t ko = (k >> 2) * kAtomKV + (k & 3) * 32;
-        mma(tmem + sl * BN, desc_kmajor(q_addr + qo), desc_kmajor(k_addr + ko), idS, k > 0);
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint32_t qo = (k >> 2) * kAtom + (k & 3) * 32;
+          const uint32_t ko = (k >> 2) * kAtomKV + (k & 3) * 32;
+          mma(tmem + sl * BN, desc_kmajor(q_addr + qo), desc_kmajor(k_addr + ko), idS, k > 0);
+        }
+        commit(smem_u32(&s_full[sl]));
+        commit(smem_u32(&k_empty[sl]));
       }
-      commit(smem_u32(&s_full[sl]));
-      commit(smem_u32(&k_empty[sl]));
+      __syncwarp();
       return true;
     };
     if (ok) ok = issue_s(0);
-    for (int j = 0; j < nb && ok && !*fail; ++j) {
+    for (int j = 0; j < nb && ok; ++j) {
+      if (__any_sync(0xffffffffu, *fail != 0)) break;
       const int sl = j & 1;
       const uint32_t ph = (j >> 1) & 1;
       if (j + 1 < nb && !issue_s(j + 1)) { ok = false; break; }
-      if (!mbar_wait_bounded(smem_u32(&p_full[sl]), ph, kWaitLimitNs, status) ||
-          !mbar_wait_bounded(smem_u32(&v_full[sl]), ph, kWaitLimitNs, status)) {
+      if (!wait_all(&p_full[sl], ph) || !wait_all(&v_full[sl], ph)) {
         ok = false;
         break;
       }
       fence_after();
-      const uint32_t v_addr = smem_u32(smem + kOffV + sl * kKV);
+      if (tcx::elect_one()) {
+        const uint32_t v_addr = smem_u32(smem + kOffV + sl * kKV);
 #pragma unroll
-      for (int k = 0; k < BN / 16; ++k)
-        mma_ts(tmem + 2 * BN, tmem + sl * BN + k * 8,
-               desc_mnmajor(v_addr + k * 16 * 128, kAtomKV), idPV,
-               (j > 0 || k > 0) ? 1u : 0u);
-      commit(smem_u32(&pv_done[sl]));
-      commit(smem_u32(&v_empty[sl]));
+        for (int k = 0; k < BN / 16; ++k)
+          mma_ts(tmem + 2 * BN, tmem + sl * BN + k * 8,
+                 desc_mnmajor(v_addr + k * 16 * 128, kAtomKV), idPV,
+                 (j > 0 || k > 0) ? 1u : 0u);
+        commit(smem_u32(&pv_done[sl]));
+        commit(smem_u32(&v_empty[sl]));
+      }
+      __syncwarp();
     }
-    if (!ok) *fail = 1;
+    if (!ok && lane == 0) *fail = 1;
   } else if (warp >= 2) {
     // ------------------------------------------------------------- softmax
     const int quad = warp & 3;

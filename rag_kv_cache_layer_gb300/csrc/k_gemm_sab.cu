@@ -27,6 +27,7 @@ constexpr int kThreads = 192;
 constexpr int kTileW = FM * BK * 2;          // 16 KB
 constexpr int kTrStride = 132;               // floats per transposed token row
 constexpr int kTr = 32 * kTrStride * 4;      // 32 tokens x 128 features, fp32
+constexpr int kTokTab = 256 * 12;            // Q/K/V epilogue: a tile's positions, cache rows
 constexpr int kSmemMax = 232448;
 
 struct Params {
@@ -114,6 +115,8 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   float *tr = reinterpret_cast<float *>(smem + p.stages * p.stage_bytes);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.stages * p.stage_bytes + kTr);
+  int64_t *s_dst = reinterpret_cast<int64_t *>(smem + p.stages * p.stage_bytes + kTr + 256);
+  int32_t *s_pos = reinterpret_cast<int32_t *>(s_dst + 256);
   uint64_t *full = bars;                 // [stages]
   uint64_t *empty = bars + 8;            // [stages]
   uint64_t *tfull = bars + 16;           // [2]
@@ -153,29 +156,31 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int issued[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      bool ok = true;
-      Work<CG> wk(p, num_kb);
-      int tt, ft, kb0, kb1;
-      const int bt = p.BT / CG;           // token rows of B held by this CTA
-      while (ok && wk.next(tt, ft, kb0, kb1)) {
-        const int fct = ft * CG + (int)rank;   // this CTA's 128-row weight tile
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, kWaitLimitNs, status) ||
-              *fail) {
-            ok = false;
-            break;
-          }
+    // The warp runs the loop converged; the elected lane issues the copies.
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    bool ok = true;
+    Work<CG> wk(p, num_kb);
+    int tt, ft, kb0, kb1;
+    const int bt = p.BT / CG;             // token rows of B held by this CTA
+    while (ok && wk.next(tt, ft, kb0, kb1)) {
+      const int fct = ft * CG + (int)rank;   // this CTA's 128-row weight tile
+      const int ty = tt * p.BT + (int)rank * bt;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        const bool got =
+            mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, kWaitLimitNs, status) && !*fail;
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        if (elect_one()) {
           // the pair's operands all complete on the leader's barrier
           uint32_t fb = smem_u32(&full[stage]);
           if (leader) expect_tx(fb, CG * p.stage_bytes);
           if (CG == 2) fb = map_to_rank(fb, 0);
           uint8_t *sw = smem + stage * p.stage_bytes;
           uint8_t *sx = sw + kTileW;
-          const int ty = tt * p.BT + (int)rank * bt;
           if (CG == 2) {
             if (EPI == EPI_SWIGLU) {
               tma_load_2d_pair(smem_u32(sw), &mapW, fb, kb * BK, fct * 64);
@@ -193,29 +198,32 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
             }
             tma_load_2d(smem_u32(sx), &mapX, fb, kb * BK, ty);
           }
-          ++issued[stage];
-          if (++stage == p.stages) { stage = 0; phase ^= 1; }
         }
+        __syncwarp();
+        ++issued[stage];
+        if (++stage == p.stages) { stage = 0; phase ^= 1; }
       }
-      if (!ok) {
-        *fail = 1;
-        if (CG == 1 || leader) {
-          for (int s = 0; s < p.stages; ++s)
-            if (issued[s] > 0)
-              mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((issued[s] - 1) & 1), 10000000ull,
-                                nullptr);
-        } else {
-          // this CTA's copies complete on the leader's barriers: give them
-          // time to land before the pair can retire
-          const uint64_t t0 = globaltimer_ns();
-          while (globaltimer_ns() - t0 < 10000000ull) {
-          }
+    }
+    if (!ok && lane == 0) {
+      *fail = 1;
+      if (CG == 1 || leader) {
+        for (int s = 0; s < p.stages; ++s)
+          if (issued[s] > 0)
+            mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((issued[s] - 1) & 1), 10000000ull,
+                              nullptr);
+      } else {
+        // this CTA's copies complete on the leader's barriers: give them
+        // time to land before the pair can retire
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 10000000ull) {
         }
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
-    if (lane == 0 && leader) {
+    // Converged warp, elected lane issues; the failure flag is polled once
+    // per tile (a stalled producer also ends the bounded waits below).
+    if (leader) {
       int stage = 0;
       uint32_t phase = 0;
       int buf = 0;
@@ -224,38 +232,46 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
       Work<CG> wk(p, num_kb);
       int tt, ft, kb0, kb1;
       while (ok && wk.next(tt, ft, kb0, kb1)) {
-        if (!mbar_wait_bounded(smem_u32(&tempty[buf]), bphase ^ 1, kWaitLimitNs, status) ||
-            *fail) {
+        const bool got =
+            mbar_wait_bounded(smem_u32(&tempty[buf]), bphase ^ 1, kWaitLimitNs, status) && !*fail;
+        if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
         fence_after();
         const uint32_t d = tmem + buf * 256;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, kWaitLimitNs, status) || *fail) {
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[stage]), phase,
+                                                          kWaitLimitNs, status))) {
             ok = false;
             break;
           }
           fence_after();
-          const uint32_t sw = smem_u32(smem + stage * p.stage_bytes);
-          const uint64_t dw = desc_kmajor(sw), dx = desc_kmajor(sw + kTileW);
+          if (elect_one()) {
+            const uint32_t sw = smem_u32(smem + stage * p.stage_bytes);
+            const uint64_t dw = desc_kmajor(sw), dx = desc_kmajor(sw + kTileW);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            if (CG == 2)
-              mma_pair(d, dw + 2 * k, dx + 2 * k, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-            else
-              mma(d, dw + 2 * k, dx + 2 * k, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < BK / 16; ++k) {
+              if (CG == 2)
+                mma_pair(d, dw + 2 * k, dx + 2 * k, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+              else
+                mma(d, dw + 2 * k, dx + 2 * k, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            }
+            if (CG == 2) commit_pair(smem_u32(&empty[stage]), 3);
+            else commit(smem_u32(&empty[stage]));
           }
-          if (CG == 2) commit_pair(smem_u32(&empty[stage]), 3);
-          else commit(smem_u32(&empty[stage]));
+          __syncwarp();
           if (++stage == p.stages) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        if (CG == 2) commit_pair(smem_u32(&tfull[buf]), 3);
-        else commit(smem_u32(&tfull[buf]));
+        if (elect_one()) {
+          if (CG == 2) commit_pair(smem_u32(&tfull[buf]), 3);
+          else commit(smem_u32(&tfull[buf]));
+        }
+        __syncwarp();
         if (++buf == 2) { buf = 0; bphase ^= 1; }
       }
-      if (!ok) *fail = 1;
+      if (!ok && lane == 0) *fail = 1;
     }
   } else {
     // ----------------------------------------------------------- epilogue
@@ -265,8 +281,19 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
     uint32_t bphase = 0;
     Work<CG> wk(p, num_kb);
     int tt, ft, kb0, kb1;
+    const int t = threadIdx.x - 64;                  // 0..127 among the epilogue threads
     while (wk.next(tt, ft, kb0, kb1)) {
       const bool whole = kb0 == 0 && kb1 == num_kb;
+      if (EPI == EPI_QKV) {
+        // the tile's positions and fused-cache rows, read while the MMAs run;
+        // the previous tile's last barrier ended every read of the table
+        for (int i = t; i < p.BT; i += 128) {
+          const int tok = tt * p.BT + i;
+          s_pos[i] = tok < p.M ? p.pos[tok] : 0;
+          s_dst[i] = tok < p.M ? (int64_t)p.dst_row[tok] : 0;
+        }
+        epi_bar();     // the table is read across threads before the chunk barriers
+      }
       const bool bad =
           !mbar_wait_bounded(smem_u32(&tfull[buf]), bphase, kWaitLimitNs, status) || *fail;
       if (__any_sync(0xffffffffu, bad)) {
@@ -283,11 +310,24 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
         head = ft;
         rotate = head < p.Hq + p.Hkv;
       }
-      const int t = threadIdx.x - 64;                // 0..127 among the epilogue threads
 #pragma unroll 1
       for (int c = 0; c < p.BT; c += 32) {
         float x[32];
         tmem_ld32(tbase + c, x);
+        // Q/K heads: this thread's rotation factors for the chunk, loaded
+        // before the transpose so that their latency overlaps it
+        float4 rf[EPI == EPI_QKV ? 4 : 1][EPI == EPI_QKV ? 4 : 1];
+        if (EPI == EPI_QKV && rotate) {
+          const int e0 = 8 * ((t & 15) & 7);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int i = (t >> 4) + 8 * q;
+            const int ci = (c + i < p.BT && tok0 + c + i < p.M) ? c + i : 0;
+            const float4 *src = reinterpret_cast<const float4 *>(p.rope + (int64_t)s_pos[ci] * 64 + e0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) rf[q][u] = __ldg(src + u);
+          }
+        }
         // transpose: feature column r of 32 tokens -> rows of the chunk
 #pragma unroll
         for (int i = 0; i < 32; ++i) tr[i * kTrStride + r] = x[i];
@@ -350,21 +390,21 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
             if (rotate) {
               // rotate-half pairs (e, e + 64) at the token's position
               const int e0 = 8 * (j & 7);
-              const float2 *cs = p.rope + (int64_t)p.pos[tok] * 64 + e0;
+              const float *w = reinterpret_cast<const float *>(rf[q]);   // (cos, sin) x 8
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
-                const float2 w = __ldg(cs + e);
                 const float x1 = row[e0 + e], x2 = row[64 + e0 + e];
-                y[e] = j < 8 ? x1 * w.x - x2 * w.y : x2 * w.x + x1 * w.y;
+                const float co = w[2 * e], si = w[2 * e + 1];
+                y[e] = j < 8 ? x1 * co - x2 * si : x2 * co + x1 * si;
               }
               dst = head < p.Hq
                         ? reinterpret_cast<bf16 *>(p.out) + (int64_t)tok * p.ldo + head * 128
-                        : reinterpret_cast<bf16 *>(p.k_cache) + (int64_t)p.dst_row[tok] * p.ld_kv +
+                        : reinterpret_cast<bf16 *>(p.k_cache) + s_dst[c + i] * p.ld_kv +
                               (head - p.Hq) * 128;
             } else {
 #pragma unroll
               for (int e = 0; e < 8; ++e) y[e] = row[8 * j + e];
-              dst = reinterpret_cast<bf16 *>(p.v_cache) + (int64_t)p.dst_row[tok] * p.ld_kv +
+              dst = reinterpret_cast<bf16 *>(p.v_cache) + s_dst[c + i] * p.ld_kv +
                     (head - p.Hq - p.Hkv) * 128;
             }
             store_bf16x8(dst + 8 * j, y);
@@ -419,7 +459,7 @@ static int max_pairs(int smem) {
 template <int EPI, int CG>
 static cudaError_t run(const CUtensorMap &mx, const CUtensorMap &mw, const CUtensorMap &mw2,
                        Params &p, int *status, cudaStream_t s) {
-  const int fixed = kTr + 256 + 1024;
+  const int fixed = kTr + 256 + kTokTab + 1024;
   p.stage_bytes = kTileW + (p.BT / CG) * BK * 2;
   p.stages = (kSmemMax - fixed) / p.stage_bytes;
   if (p.stages > 8) p.stages = 8;
@@ -485,11 +525,18 @@ static cudaError_t run_cg(const CUtensorMap &mx, const CUtensorMap &mw, const CU
 
 }  // namespace sab
 
-// Measured at the Llama-3-8B projection shapes with M = 524 token rows: the
-// swapped form wins on the residual projections (O, down: 27 and 61 us
-// against 32 and 67 us) and loses on the fused Q/K/V and SwiGLU epilogues.
-bool gemm_sab_preferred(int M, GemmEpi epi) {
-  return M > 0 && M <= 1024 && epi == EPI_RESID;
+// Automatic form, measured at the Llama-3-8B projection shapes for 512 to
+// 4096 token rows: the CTA-pair swapped form is fastest for the SwiGLU,
+// down and Q/K/V projections at every size (524 rows: 92, 45 and 22 us
+// against 107, 49 and 29 us for the best single-CTA form; 4096 rows of
+// SwiGLU: 2.0 PFLOP/s).  The K = 4096 residual projection (O) has few weight
+// tiles; it takes the single-CTA swapped form up to 1024 rows and token rows
+// on M above that.  Returns 0 (token rows on M), 1 or 2 (swapped, CTAs per
+// MMA).
+int gemm_auto_form(int M, int K, GemmEpi epi) {
+  if (M <= 0) return 0;
+  if (epi == EPI_RESID && K <= 4096) return M <= 1024 ? 1 : 0;
+  return 2;
 }
 
 cudaError_t launch_gemm_sab(const void *A, int64_t lda, const void *W, const void *W2,

@@ -26,6 +26,7 @@
 
 #include "cb_common.cuh"
 #include "cb_internal.h"
+#include "cb_tc.cuh"
 
 namespace cb {
 namespace tc {
@@ -250,20 +251,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int issued[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      bool ok = true;
-      Work wk(n_m, n_n, num_kb, stream_k != 0);
-      int m_blk, n_blk, kb0, kb1;
-      while (ok && wk.next(m_blk, n_blk, kb0, kb1)) {
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, kWaitLimitNs, status) ||
-              *fail_flag) {
-            ok = false;
-            break;
-          }
+    // The warp runs the loop converged; the elected lane issues the copies.
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    bool ok = true;
+    Work wk(n_m, n_n, num_kb, stream_k != 0);
+    int m_blk, n_blk, kb0, kb1;
+    while (ok && wk.next(m_blk, n_blk, kb0, kb1)) {
+      for (int kb = kb0; kb < kb1; ++kb) {
+        const bool got = mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, kWaitLimitNs,
+                                           status) &&
+                         !*fail_flag;
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        if (tcx::elect_one()) {
           const uint32_t fb = smem_u32(&full[stage]);
           mbar_expect_tx(fb, C::kStage);
           uint8_t *sa = smem + stage * C::kStage;
@@ -275,59 +279,66 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
           } else {
             tma_load_2d(smem_u32(sb), &mapB, fb, kb * BK, n_blk * BN);
           }
-          ++issued[stage];
-          if (++stage == C::kStages) { stage = 0; phase ^= 1; }
         }
+        __syncwarp();
+        ++issued[stage];
+        if (++stage == C::kStages) { stage = 0; phase ^= 1; }
       }
-      if (!ok) {
-        *fail_flag = 1;
-        // drain this thread's copies still in flight before the CTA exits
-        for (int s = 0; s < C::kStages; ++s)
-          if (issued[s] > 0)
-            mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((issued[s] - 1) & 1),
-                              10000000ull, nullptr);
-      }
+    }
+    if (!ok && lane == 0) {
+      *fail_flag = 1;
+      // drain this warp's copies still in flight before the CTA exits
+      for (int s = 0; s < C::kStages; ++s)
+        if (issued[s] > 0)
+          mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((issued[s] - 1) & 1), 10000000ull,
+                            nullptr);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(BM, C::kMmaN);
-      int stage = 0;
-      uint32_t phase = 0;
-      int buf = 0;
-      uint32_t bphase = 0;
-      bool ok = true;
-      Work wk(n_m, n_n, num_kb, stream_k != 0);
-      int m_blk, n_blk, kb0, kb1;
-      while (ok && wk.next(m_blk, n_blk, kb0, kb1)) {
-        if (!mbar_wait_bounded(smem_u32(&tempty[buf]), bphase ^ 1, kWaitLimitNs, status) ||
-            *fail_flag) {
+    // Converged warp, elected lane issues; the failure flag is polled once
+    // per tile (a stalled producer also ends the bounded waits below).
+    constexpr uint32_t idesc = make_idesc(BM, C::kMmaN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int buf = 0;
+    uint32_t bphase = 0;
+    bool ok = true;
+    Work wk(n_m, n_n, num_kb, stream_k != 0);
+    int m_blk, n_blk, kb0, kb1;
+    while (ok && wk.next(m_blk, n_blk, kb0, kb1)) {
+      const bool got =
+          mbar_wait_bounded(smem_u32(&tempty[buf]), bphase ^ 1, kWaitLimitNs, status) &&
+          !*fail_flag;
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d = tmem_base + buf * C::kMmaN;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait_bounded(smem_u32(&full[stage]), phase, kWaitLimitNs, status))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + buf * C::kMmaN;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, kWaitLimitNs, status) ||
-              *fail_flag) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+        if (tcx::elect_one()) {
           const uint32_t sa = smem_u32(smem + stage * C::kStage);
           const uint64_t da = smem_desc(sa), db = smem_desc(sa + kTileA);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             umma(d, da + 2 * k, db + 2 * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
           umma_commit(smem_u32(&empty[stage]));
-          if (++stage == C::kStages) { stage = 0; phase ^= 1; }
         }
-        if (!ok) break;
-        umma_commit(smem_u32(&tfull[buf]));
-        if (++buf == 2) { buf = 0; bphase ^= 1; }
+        __syncwarp();
+        if (++stage == C::kStages) { stage = 0; phase ^= 1; }
       }
-      if (!ok) *fail_flag = 1;
+      if (!ok) break;
+      if (tcx::elect_one()) umma_commit(smem_u32(&tfull[buf]));
+      __syncwarp();
+      if (++buf == 2) { buf = 0; bphase ^= 1; }
     }
+    if (!ok && lane == 0) *fail_flag = 1;
   } else {
     // ----------------------------------------------------------- epilogue
     const int quad = warp & 3;                 // TMEM lanes 32*quad .. +31
