@@ -331,13 +331,14 @@ static cb_status run_attention(const void *q, int64_t ld_q, const int32_t *q_pos
                                const std::vector<AttnReq> &reqs, const void *kc,
                                const void *vc, int64_t ld_kv, int Hq, int Hkv, int hd,
                                float scale, void *out, int64_t ld_out, cb_dtype dt,
-                               void *ws, size_t ws_bytes, int *st, cudaStream_t s) {
+                               void *ws, size_t ws_bytes, int *st, cudaStream_t s,
+                               const int *plan = nullptr) {
   if (dt == CB_BF16 && attention_tc_supported(Hq, Hkv, hd)) {
-    const size_t need = attention_tc_ws_bytes(reqs.data(), (int)reqs.size(), Hq, Hkv);
+    const size_t need = plan ? 0 : attention_tc_ws_bytes(reqs.data(), (int)reqs.size(), Hq, Hkv);
     if (need > 0 && (!ws || ws_bytes < need))
       return fail(CB_ERR_WORKSPACE, "attention workspace too small (%zu < %zu)", ws_bytes, need);
     CB_CUDA(launch_attention_tc(q, ld_q, q_pos, reqs.data(), (int)reqs.size(), kc, vc, ld_kv,
-                                Hq, Hkv, scale, out, ld_out, ws, ws_bytes, st, s));
+                                Hq, Hkv, scale, out, ld_out, ws, ws_bytes, st, s, plan));
   } else {
     CB_CUDA(launch_attention_simt(q, ld_q, q_pos, reqs.data(), (int)reqs.size(), kc, vc,
                                   ld_kv, Hq, Hkv, hd, scale, out, ld_out, dt, st, s));
@@ -574,6 +575,7 @@ struct Plan {
   // workspace
   LayerOffsets lay;
   size_t h_all, kf, dev, sel, pos_all, glob_all, pos_c, glob_c, h_c, lm_x, lm_best, total;
+  size_t attn_plan = 0, attn_plan_bytes = 0;   // unit table of the compact layers' attention
   size_t g_dev = 0, g_keep = 0, g_sel = 0, g_pos = 0, g_glob = 0, g_src = 0, g_h = 0;
   // host-resident chunk path: two layers of the context K/V in flight
   size_t stage = 0, stage_bytes = 0;     // stage_bytes: K of one layer (V follows)
@@ -718,6 +720,14 @@ static cb_status make_plan(const cb_model *m, const cb_request *reqs, int B,
   P.h_c = cv.take((P.R_total + 1) * c.d_model * sizeof(float));
   P.lm_x = cv.take((size_t)B * c.d_model * sizeof(float));
   P.lm_best = cv.take((size_t)B * sizeof(unsigned long long));
+  if (c.dtype == CB_BF16 && attention_tc_supported(c.n_q_heads, c.n_kv_heads, c.head_dim)) {
+    // the compact rows of each request (the largest set; filtering only shrinks it)
+    std::vector<AttnReq> ar(B);
+    for (int b = 0; b < B; ++b)
+      ar[b] = AttnReq{P.bm.r_off[b], P.bm.r_off[b + 1], (int64_t)P.bm.t_off[b], P.T[b]};
+    P.attn_plan_bytes = attention_plan_bytes(ar.data(), B, c.n_q_heads, c.n_kv_heads);
+    P.attn_plan = cv.take(P.attn_plan_bytes);
+  }
   if (!P.sched.empty()) {
     // second set of compact buffers; the filtered rows ping-pong between them
     P.g_dev = cv.take((P.K_total + 1) * sizeof(float));
@@ -774,7 +784,7 @@ static inline char *layer_ptr(void *base, int l, int64_t stride, size_t eb) {
 static cb_status layer_forward(cb_model *m, int l, float *h, int n, const int32_t *pos,
                                const int32_t *cache_row, const std::vector<AttnReq> &ar,
                                void *kc, void *vc, const LayerScratch &S, int *st,
-                               cudaStream_t s) {
+                               cudaStream_t s, const int *attn_plan = nullptr) {
   const cb_model_config &c = m->cfg;
   const cb_layer_weights &L = m->layers[l];
   const int d = c.d_model, F = c.d_ffn, hd = c.head_dim;
@@ -796,7 +806,8 @@ static cb_status layer_forward(cb_model *m, int l, float *h, int n, const int32_
   probe_mark(CB_PROBE_QKV, false, s);
   probe_mark(CB_PROBE_ATTENTION, true, s);
   CB_TRY(run_attention(S.q, m->qw, pos, ar, kc, vc, m->kvw, c.n_q_heads, c.n_kv_heads, hd,
-                       1.f / sqrtf((float)hd), S.o, m->qw, dt, S.attn, S.attn_bytes, st, s));
+                       1.f / sqrtf((float)hd), S.o, m->qw, dt, S.attn, S.attn_bytes, st, s,
+                       attn_plan));
   probe_mark(CB_PROBE_ATTENTION, false, s);
   probe_mark(CB_PROBE_O, true, s);
   CB_TRY(run_linear(m, S.o, m->qw, L.w_o, nullptr, m->qw, n, d, m->qw, EPI_RESID, h, d, s));
@@ -1098,6 +1109,10 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
   int R_cur = (int)P.R_total;
   size_t next_step = 0;
   std::vector<AttnReq> ar_c(B);
+  // the compact layers' attention units, planned from the rows' positions
+  // whenever the set changes (its first layer, each filtering step)
+  int *attn_plan = P.attn_plan_bytes ? (int *)(ws + P.attn_plan) : nullptr;
+  bool plan_stale = true;
   for (int l = s_layer; l < L; ++l) {
     if (host_kv) {
       if (l > s_layer) CB_TRY(stitch_layer(l));
@@ -1111,12 +1126,18 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
       cur ^= 1;
       bm = stp.bm;
       R_cur = (int)stp.R_total;
+      plan_stale = true;
     }
     for (int b = 0; b < B; ++b)
       ar_c[b] = AttnReq{bm.r_off[b], bm.r_off[b + 1], (int64_t)P.bm.t_off[b], P.T[b]};
+    if (attn_plan && plan_stale) {
+      CB_CUDA(launch_attention_plan(pos_b[cur], ar_c.data(), B, c.n_q_heads, c.n_kv_heads,
+                                    attn_plan, P.attn_plan_bytes, s));
+      plan_stale = false;
+    }
     CB_TRY(layer_forward(m, l, h_b[cur], R_cur, pos_b[cur], glob_b[cur], ar_c,
                          layer_ptr(out->k_cache, l, lstride, m->eb),
-                         layer_ptr(out->v_cache, l, lstride, m->eb), S, st, s));
+                         layer_ptr(out->v_cache, l, lstride, m->eb), S, st, s, attn_plan));
   }
   if (cur == 1) {
     // the final set is in the second buffers: move it to the outputs

@@ -213,11 +213,22 @@ cudaError_t launch_attention_simt(const void *q, int64_t ld_q,
 bool attention_tc_supported(int Hq, int Hkv, int hd);
 size_t attention_tc_ws_bytes(const AttnReq *reqs, int n_req, int Hq, int Hkv);
 size_t attention_tc_ws_bound();
+// plan: a unit table from launch_attention_plan for these requests and query
+// positions, or nullptr for a uniform split of every tile's key range.  With
+// a table the scratch is at most attention_tc_ws_bound.
 cudaError_t launch_attention_tc(const void *q, int64_t ld_q, const int32_t *q_pos,
                                 const AttnReq *reqs, int n_req, const void *k_cache,
                                 const void *v_cache, int64_t ld_kv, int Hq, int Hkv,
                                 float scale, void *out, int64_t ld_out, void *ws,
-                                size_t ws_bytes, int *status, cudaStream_t s);
+                                size_t ws_bytes, int *status, cudaStream_t s,
+                                const int *plan = nullptr);
+// Unit table for launch_attention_tc, built on the device from the query
+// positions: every tile's key range is cut so that all units run in one wave
+// of CTAs.  Valid for as long as the requests and q_pos stay the same (the
+// compact layers of one blended call share it).
+size_t attention_plan_bytes(const AttnReq *reqs, int n_req, int Hq, int Hkv);
+cudaError_t launch_attention_plan(const int32_t *q_pos, const AttnReq *reqs, int n_req, int Hq,
+                                  int Hkv, int *plan, size_t plan_bytes, cudaStream_t s);
 
 // ---------------------------------------------------------------- debug --
 cudaError_t launch_expire_wait(int limit_us, int *status, cudaStream_t s);

@@ -231,10 +231,20 @@ struct Params {
   int n_req;
   int G, QT, Hkv;
   float scale_log2;            // softmax scale times log2(e)
-  int n_chunks, chunk_blocks;  // key-range split of every tile
+  int n_chunks, chunk_blocks;  // uniform key-range split of every tile (plan == nullptr)
+  const int *plan;             // device unit table (attn_plan_kernel) or nullptr
   int tile_off[CB_MAX_BATCH + 1];
   AttnReq r[CB_MAX_BATCH];
 };
+
+// Unit table written by attn_plan_kernel (int32 words): [0] units, [1] key
+// blocks per unit at most, [2] tiles, [3] 0; then per tile t the pair
+// (first unit, unit count) at [4 + 2t]; then, 16-byte aligned, one int4
+// {tile, first key block, end key block, 0} per unit, the units of a tile
+// consecutive.
+__host__ __device__ inline size_t plan_units_off(int tiles) {
+  return ((size_t)(4 + 2 * tiles) * 4 + 15) / 16 * 16;
+}
 
 // (request, kv head, query tile) of a tile index; longest tiles first
 // within a request.
@@ -248,6 +258,117 @@ __device__ __forceinline__ TileId decode_tile(const Params &P, int tile) {
   const int n_rows = P.r[b].q_end - P.r[b].q_begin;
   const int n_t = (n_rows + P.QT - 1) / P.QT;
   return TileId{b, local % P.Hkv, n_t - 1 - local / P.Hkv};
+}
+
+
+// ------------------------------------------------------------ unit plan --
+// Splits the tiles' key ranges so that every unit fits in one wave of CTA
+// slots: B, the key blocks per unit at most, is the smallest value for which
+// sum_t ceil(nb_t / B) <= slots (nb_t: key blocks up to the tile's last query
+// position); tile t is cut into ceil(nb_t / B) near-equal consecutive
+// ranges.  With at least as many tiles as slots nothing is split.  One CTA.
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanCache = 8192;           // tiles whose block counts stay in smem
+static_assert(kPlanThreads == 1024, "the block reductions assume 32 warps");
+
+__device__ int block_sum(int v, int *red) {
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  int t = red[threadIdx.x & 31];               // 32 warps: every warp reduces all
+  for (int o = 16; o; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  return t;                                  // every warp of the block holds the sum
+}
+__device__ int block_max(int v, int *red) {
+  for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  int t = red[threadIdx.x & 31];               // 32 warps: every warp reduces all
+  for (int o = 16; o; o >>= 1) t = max(t, __shfl_xor_sync(0xffffffffu, t, o));
+  return t;
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+attn_plan_kernel(const __grid_constant__ Params P, const int32_t *__restrict__ q_pos, int slots,
+                 int *__restrict__ plan) {
+  __shared__ int red[kPlanThreads / 32];
+  __shared__ int s_nb[kPlanCache];
+  grid_dep_wait();      // q_pos comes from earlier kernels
+  grid_dep_launch();
+  const int tiles = P.tile_off[P.n_req];
+  auto nb_of = [&](int tile) -> int {
+    const TileId id = decode_tile(P, tile);
+    const AttnReq &R = P.r[id.b];
+    const int last = min(R.q_end - R.q_begin, (id.t + 1) * P.QT) - 1;
+    const int pmax = q_pos[R.q_begin + last];
+    return (pmax < 0 || pmax >= R.kv_len) ? 0 : pmax / BN + 1;   // the kernel reports bad rows
+  };
+  auto nb_at = [&](int tile) -> int { return tile < kPlanCache ? s_nb[tile] : nb_of(tile); };
+  int mx = 0, sum = 0;
+  for (int t = threadIdx.x; t < tiles; t += kPlanThreads) {
+    const int nb = nb_of(t);
+    if (t < kPlanCache) s_nb[t] = nb;
+    mx = max(mx, nb);
+    sum += nb;
+  }
+  const int max_nb = block_max(mx, red);
+  const int total = block_sum(sum, red);
+  int B = max(max_nb, 1);
+  if (tiles < slots && max_nb > 1) {
+    int lo = max(1, (total + slots - 1) / slots), hi = max_nb;
+    while (lo < hi) {                           // uniform across the block
+      const int mid = (lo + hi) / 2;
+      int cnt = 0;
+      for (int t = threadIdx.x; t < tiles; t += kPlanThreads)
+        cnt += max(1, (nb_at(t) + mid - 1) / mid);
+      if (block_sum(cnt, red) <= slots) hi = mid;
+      else lo = mid + 1;
+    }
+    B = lo;
+  }
+  int4 *units = reinterpret_cast<int4 *>(reinterpret_cast<char *>(plan) + plan_units_off(tiles));
+  int base = 0;
+  for (int t0 = 0; t0 < tiles; t0 += kPlanThreads) {
+    const int t = t0 + threadIdx.x;
+    const int nb = t < tiles ? nb_at(t) : 0;
+    const int cnt = t < tiles ? max(1, (nb + B - 1) / B) : 0;
+    // exclusive scan of cnt over the block
+    int incl = cnt;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    __syncthreads();
+    if (lane == 31) red[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+      int x = red[lane];
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += v;
+      }
+      red[lane] = x;                           // inclusive warp totals
+    }
+    __syncthreads();
+    const int first = base + (w ? red[w - 1] : 0) + incl - cnt;
+    if (t < tiles) {
+      plan[4 + 2 * t] = first;
+      plan[5 + 2 * t] = cnt;
+      for (int u = 0; u < cnt; ++u)
+        units[first + u] = make_int4(t, nb * u / cnt, nb * (u + 1) / cnt, 0);
+    }
+    base += red[kPlanThreads / 32 - 1];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    plan[0] = base;
+    plan[1] = B;
+    plan[2] = tiles;
+    plan[3] = 0;
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
@@ -269,24 +390,45 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   uint64_t *pv_done = bar + 13;    // [2] O += P_j V_j has landed
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 15);
   volatile int *fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  __shared__ int s_unit[6];        // b, g, tile, first block, end block
+  __shared__ int s_unit[6];        // b, g, tile, first block, end block, split (-1: none)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   grid_dep_wait();      // q, the cache and q_pos come from earlier kernels
   grid_dep_launch();
   if (threadIdx.x == 0) {
-    const int tile = blockIdx.x / P.n_chunks, chunk = blockIdx.x % P.n_chunks;
-    const TileId id = decode_tile(P, tile);
-    const AttnReq &R = P.r[id.b];
-    const int n_rows = R.q_end - R.q_begin;
-    const int last = min(n_rows, (id.t + 1) * P.QT) - 1;
-    int pmax = q_pos[R.q_begin + last];
-    if (pmax < 0 || pmax >= R.kv_len) { report(status, CB_ERR_DEVICE_INDEX); pmax = -1; }
-    const int nb_tile = pmax < 0 ? 0 : pmax / BN + 1;
-    const int jb = chunk * P.chunk_blocks;
-    s_unit[0] = id.b; s_unit[1] = id.g; s_unit[2] = id.t;
-    s_unit[3] = jb;
-    s_unit[4] = max(jb, min(nb_tile, jb + P.chunk_blocks));
+    // this CTA's unit: a tile and a range of its key blocks
+    int tile, jb, jcap, split;
+    if (P.plan) {
+      if ((int)blockIdx.x >= P.plan[0]) {
+        tile = -1;
+        jb = jcap = split = 0;
+      } else {
+        const int4 u = reinterpret_cast<const int4 *>(
+            reinterpret_cast<const char *>(P.plan) + plan_units_off(P.plan[2]))[blockIdx.x];
+        tile = u.x;
+        jb = u.y;
+        jcap = u.z;
+        split = P.plan[5 + 2 * tile] > 1;
+      }
+    } else {
+      tile = blockIdx.x / P.n_chunks;
+      jb = (blockIdx.x % P.n_chunks) * P.chunk_blocks;
+      jcap = jb + P.chunk_blocks;
+      split = P.n_chunks > 1;
+    }
+    s_unit[5] = tile < 0 ? -1 : split;
+    if (tile >= 0) {
+      const TileId id = decode_tile(P, tile);
+      const AttnReq &R = P.r[id.b];
+      const int n_rows = R.q_end - R.q_begin;
+      const int last = min(n_rows, (id.t + 1) * P.QT) - 1;
+      int pmax = q_pos[R.q_begin + last];
+      if (pmax < 0 || pmax >= R.kv_len) { report(status, CB_ERR_DEVICE_INDEX); pmax = -1; }
+      const int nb_tile = pmax < 0 ? 0 : pmax / BN + 1;
+      s_unit[0] = id.b; s_unit[1] = id.g; s_unit[2] = id.t;
+      s_unit[3] = jb;
+      s_unit[4] = max(jb, min(nb_tile, jcap));
+    }
     mbar_init(smem_u32(q_full), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&k_full[i]), 1);
@@ -301,6 +443,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  if (s_unit[5] < 0) return;                      // no unit for this CTA
+  const bool split = s_unit[5] != 0;              // partial of a split tile
   const int b = s_unit[0], g = s_unit[1], t = s_unit[2], jb = s_unit[3], je = s_unit[4];
   const int nb = je - jb;                         // key blocks of this unit
   const AttnReq &R = P.r[b];
@@ -308,7 +452,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   const int n_valid = min(P.QT, R.q_end - row0);  // q rows of the request in the tile
   if (nb == 0) {
     // a key chunk past the tile's last query: an empty partial, nothing else
-    if (P.n_chunks > 1 && threadIdx.x < 128 && (int)threadIdx.x % P.QT < n_valid)
+    if (split && threadIdx.x < 128 && (int)threadIdx.x % P.QT < n_valid)
       part_ml[(int64_t)blockIdx.x * 128 + threadIdx.x] = make_float2(-INFINITY, 0.f);
     return;
   }
@@ -517,7 +661,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
         float o[32];
         ld32(obase + c, o);
         if (!(valid && ok)) continue;
-        if (P.n_chunks == 1) {
+        if (!split) {
           bf16 *dst = out + (int64_t)q_row * ld_out + head * HD + c;
 #pragma unroll
           for (int c8 = 0; c8 < 32; c8 += 8) {
@@ -535,7 +679,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
           for (int i = 0; i < 32; i += 4) po[i / 4] = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
         }
       }
-      if (valid && ok && P.n_chunks > 1) part_ml[slot] = make_float2(m, l);
+      if (valid && ok && split) part_ml[slot] = make_float2(m, l);
     }
   }
   fence_before();
@@ -567,18 +711,24 @@ attn_combine_kernel(const __grid_constant__ Params P, const float *__restrict__ 
   const int tile = blockIdx.x / 16;
   const int row = (blockIdx.x % 16) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  // the tile's partial units: consecutive slots from `first`
+  int first = tile * P.n_chunks, count = P.n_chunks;
+  if (P.plan) {
+    first = P.plan[4 + 2 * tile];
+    count = P.plan[5 + 2 * tile];
+    if (count <= 1) return;                       // written directly by its unit
+  }
   const TileId id = decode_tile(P, tile);
   const AttnReq &R = P.r[id.b];
   const int h = row / P.QT, qi = row % P.QT;
   const int row0 = R.q_begin + id.t * P.QT;
   if (qi >= min(P.QT, R.q_end - row0)) return;
   float M = -INFINITY;
-  for (int c = 0; c < P.n_chunks; ++c)
-    M = fmaxf(M, part_ml[((int64_t)tile * P.n_chunks + c) * 128 + row].x);
+  for (int c = 0; c < count; ++c) M = fmaxf(M, part_ml[((int64_t)first + c) * 128 + row].x);
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   float l = 0.f;
-  for (int c = 0; c < P.n_chunks; ++c) {
-    const int64_t slot = ((int64_t)tile * P.n_chunks + c) * 128 + row;
+  for (int c = 0; c < count; ++c) {
+    const int64_t slot = ((int64_t)first + c) * 128 + row;
     const float2 ml = part_ml[slot];
     if (ml.x == -INFINITY) continue;
     const float w = exp2f(ml.x - M);
@@ -640,6 +790,7 @@ static int num_sms() {
 // CTAs run; chunks past a tile's last query position exit at once.
 static void plan_split(Params &P, const AttnReq *reqs, int n_req, int Hq, int Hkv) {
   P.n_req = n_req;
+  P.plan = nullptr;
   P.G = Hq / Hkv;
   P.QT = 128 / P.G;
   P.Hkv = Hkv;
@@ -680,6 +831,27 @@ size_t attention_tc_ws_bound() {
   return (size_t)3 * attn::kCtasPerSm * attn::num_sms() * attn::kPartBytes + 256;
 }
 
+size_t attention_plan_bytes(const AttnReq *reqs, int n_req, int Hq, int Hkv) {
+  attn::Params P;
+  attn::plan_split(P, reqs, n_req, Hq, Hkv);
+  const int tiles = P.tile_off[n_req];
+  const int slots = attn::kCtasPerSm * attn::num_sms();
+  return attn::plan_units_off(tiles) + (size_t)16 * (tiles > slots ? tiles : slots) + 256;
+}
+
+cudaError_t launch_attention_plan(const int32_t *q_pos, const AttnReq *reqs, int n_req, int Hq,
+                                  int Hkv, int *plan, size_t plan_bytes, cudaStream_t s) {
+  using namespace attn;
+  Params P;
+  plan_split(P, reqs, n_req, Hq, Hkv);
+  if (!plan || plan_bytes < attention_plan_bytes(reqs, n_req, Hq, Hkv))
+    return cudaErrorInvalidValue;
+  cudaError_t e = launch_pdl(attn_plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, P, q_pos,
+                             kCtasPerSm * num_sms(), plan);
+  if (e != cudaSuccess) return e;
+  return launched(1);
+}
+
 size_t attention_tc_ws_bytes(const AttnReq *reqs, int n_req, int Hq, int Hkv) {
   attn::Params P;
   attn::plan_split(P, reqs, n_req, Hq, Hkv);
@@ -691,10 +863,11 @@ cudaError_t launch_attention_tc(const void *q, int64_t ld_q, const int32_t *q_po
                                 const AttnReq *reqs, int n_req, const void *k_cache,
                                 const void *v_cache, int64_t ld_kv, int Hq, int Hkv,
                                 float scale, void *out, int64_t ld_out, void *ws,
-                                size_t ws_bytes, int *status, cudaStream_t s) {
+                                size_t ws_bytes, int *status, cudaStream_t s, const int *plan) {
   using namespace attn;
   Params P;
   plan_split(P, reqs, n_req, Hq, Hkv);
+  P.plan = plan;
   P.scale_log2 = scale * 1.4426950408889634f;
   int64_t q_rows = 0, kv_rows = 0;
   for (int i = 0; i < n_req; ++i) {
@@ -703,14 +876,19 @@ cudaError_t launch_attention_tc(const void *q, int64_t ld_q, const int32_t *q_po
   }
   const int tiles = P.tile_off[n_req];
   if (tiles == 0) return cudaSuccess;
+  // CTAs and partial slots: with a unit table, one wave of slots (or one
+  // unit per tile when the tiles alone fill the slots); else tiles x chunks
+  const int slots = kCtasPerSm * num_sms();
+  const int grid = plan ? (tiles > slots ? tiles : slots) : tiles * P.n_chunks;
+  const bool split = plan ? tiles < slots : P.n_chunks > 1;
   float *part_o = nullptr;
   float2 *part_ml = nullptr;
-  if (P.n_chunks > 1) {
-    const size_t need = (size_t)tiles * P.n_chunks * kPartBytes;
+  if (split) {
+    const size_t need = (size_t)grid * kPartBytes;
     if (!ws || ws_bytes < need) return cudaErrorInvalidValue;
     part_o = reinterpret_cast<float *>(ws);
     part_ml = reinterpret_cast<float2 *>(reinterpret_cast<char *>(ws) +
-                                         (size_t)tiles * P.n_chunks * 128 * HD * sizeof(float));
+                                         (size_t)grid * 128 * HD * sizeof(float));
   }
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, q_rows, (int64_t)Hq * HD, ld_q, P.QT) ||
@@ -724,11 +902,11 @@ cudaError_t launch_attention_tc(const void *q, int64_t ld_q, const int32_t *q_po
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  cudaError_t e = launch_pdl(attn_tc_kernel, dim3(tiles * P.n_chunks), dim3(kThreads), kSmem, s,
+  cudaError_t e = launch_pdl(attn_tc_kernel, dim3(grid), dim3(kThreads), kSmem, s,
                              mq, mk, mv, P, q_pos, reinterpret_cast<bf16 *>(out), ld_out, part_o,
                              part_ml, status);
   if (e != cudaSuccess) return e;
-  if (P.n_chunks == 1) return launched(1);
+  if (!split) return launched(1);
   e = launch_pdl(attn_combine_kernel, dim3(tiles * 16), dim3(256), 0, s, P,
                  (const float *)part_o, (const float2 *)part_ml, reinterpret_cast<bf16 *>(out),
                  ld_out);
