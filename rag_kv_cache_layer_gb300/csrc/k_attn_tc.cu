@@ -723,19 +723,31 @@ attn_combine_kernel(const __grid_constant__ Params P, const float *__restrict__ 
   const int h = row / P.QT, qi = row % P.QT;
   const int row0 = R.q_begin + id.t * P.QT;
   if (qi >= min(P.QT, R.q_end - row0)) return;
+  // lane c holds partial c's (m, l): the weights come from two warp
+  // reductions, and the partial rows are then read back to back
+  const float2 *ml_row = part_ml + (int64_t)first * 128 + row;
   float M = -INFINITY;
-  for (int c = 0; c < count; ++c) M = fmaxf(M, part_ml[((int64_t)first + c) * 128 + row].x);
+  for (int c = lane; c < count; c += 32) M = fmaxf(M, ml_row[(int64_t)c * 128].x);
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   float l = 0.f;
-  for (int c = 0; c < count; ++c) {
-    const int64_t slot = ((int64_t)first + c) * 128 + row;
-    const float2 ml = part_ml[slot];
-    if (ml.x == -INFINITY) continue;
-    const float w = exp2f(ml.x - M);
+  for (int c0 = 0; c0 < count; c0 += 32) {
+    const float2 ml = c0 + lane < count ? ml_row[(int64_t)(c0 + lane) * 128]
+                                        : make_float2(-INFINITY, 0.f);
+    const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);   // empty chunk: no rows
     l += w * ml.y;
-    const float4 v = reinterpret_cast<const float4 *>(part_o + slot * HD)[lane];
-    o.x += w * v.x; o.y += w * v.y; o.z += w * v.z; o.w += w * v.w;
+    const int n = min(32, count - c0);
+#pragma unroll 4
+    for (int i = 0; i < n; ++i) {
+      const float wi = __shfl_sync(0xffffffffu, w, i);
+      if (wi != 0.f) {
+        const float4 v = reinterpret_cast<const float4 *>(
+            part_o + (((int64_t)first + c0 + i) * 128 + row) * HD)[lane];
+        o.x += wi * v.x; o.y += wi * v.y; o.z += wi * v.z; o.w += wi * v.w;
+      }
+    }
   }
+  for (int s = 16; s; s >>= 1) l += __shfl_xor_sync(0xffffffffu, l, s);
   const float inv = 1.f / l;
   bf16 *dst = out + (int64_t)(row0 + qi) * ld_out + (id.g * P.G + h) * HD + lane * 4;
   __nv_bfloat162 lo = __floats2bfloat162_rn(o.x * inv, o.y * inv);
