@@ -700,17 +700,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   }
 }
 
-// Merges the key-chunk partials of every (query row, q head).  One warp
-// per tile row; each lane owns four of the 128 output dimensions, so every
-// partial row is read as one coalesced 512-byte access.
+// Merges the key-chunk partials of every (query row, q head).  A CTA of
+// eight warps takes 32 rows of a tile, four per warp, and issues the loads
+// of all four rows before using them; each lane owns four of the 128 output
+// dimensions, so every partial row is read as one coalesced 512-byte access.
+constexpr int kCombineRows = 4;            // rows per warp
 __global__ void __launch_bounds__(256)
 attn_combine_kernel(const __grid_constant__ Params P, const float *__restrict__ part_o,
                     const float2 *__restrict__ part_ml, bf16 *__restrict__ out, int64_t ld_out) {
   grid_dep_wait();
   grid_dep_launch();
-  const int tile = blockIdx.x / 16;
-  const int row = (blockIdx.x % 16) * 8 + (threadIdx.x >> 5);
+  const int tile = blockIdx.x / 4;
   const int lane = threadIdx.x & 31;
+  const int row_base = (blockIdx.x % 4) * 32 + (threadIdx.x >> 5);   // rows row_base + 8 r
   // the tile's partial units: consecutive slots from `first`
   int first = tile * P.n_chunks, count = P.n_chunks;
   if (P.plan) {
@@ -720,42 +722,64 @@ attn_combine_kernel(const __grid_constant__ Params P, const float *__restrict__ 
   }
   const TileId id = decode_tile(P, tile);
   const AttnReq &R = P.r[id.b];
-  const int h = row / P.QT, qi = row % P.QT;
   const int row0 = R.q_begin + id.t * P.QT;
-  if (qi >= min(P.QT, R.q_end - row0)) return;
-  // lane c holds partial c's (m, l): the weights come from two warp
-  // reductions, and the partial rows are then read back to back
-  const float2 *ml_row = part_ml + (int64_t)first * 128 + row;
-  float M = -INFINITY;
-  for (int c = lane; c < count; c += 32) M = fmaxf(M, ml_row[(int64_t)c * 128].x);
-  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  float l = 0.f;
+  const int n_valid = min(P.QT, R.q_end - row0);
+  // lane c holds partial c's (m, l) of each row: the weights come from warp
+  // reductions, then the partial rows are read back to back
+  float M[kCombineRows], l[kCombineRows];
+  float4 o[kCombineRows];
+#pragma unroll
+  for (int r = 0; r < kCombineRows; ++r) {
+    M[r] = -INFINITY;
+    l[r] = 0.f;
+    o[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int c = lane; c < count; c += 32) {
+#pragma unroll
+    for (int r = 0; r < kCombineRows; ++r)
+      M[r] = fmaxf(M[r], part_ml[((int64_t)first + c) * 128 + row_base + 8 * r].x);
+  }
+#pragma unroll
+  for (int r = 0; r < kCombineRows; ++r)
+    for (int s = 16; s; s >>= 1) M[r] = fmaxf(M[r], __shfl_xor_sync(0xffffffffu, M[r], s));
   for (int c0 = 0; c0 < count; c0 += 32) {
-    const float2 ml = c0 + lane < count ? ml_row[(int64_t)(c0 + lane) * 128]
-                                        : make_float2(-INFINITY, 0.f);
-    const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);   // empty chunk: no rows
-    l += w * ml.y;
+    float w[kCombineRows];
+#pragma unroll
+    for (int r = 0; r < kCombineRows; ++r) {
+      const float2 ml = c0 + lane < count
+                            ? part_ml[((int64_t)first + c0 + lane) * 128 + row_base + 8 * r]
+                            : make_float2(-INFINITY, 0.f);
+      w[r] = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M[r]);     // empty chunk: no rows
+      l[r] += w[r] * ml.y;
+    }
     const int n = min(32, count - c0);
-#pragma unroll 4
     for (int i = 0; i < n; ++i) {
-      const float wi = __shfl_sync(0xffffffffu, w, i);
-      if (wi != 0.f) {
-        const float4 v = reinterpret_cast<const float4 *>(
-            part_o + (((int64_t)first + c0 + i) * 128 + row) * HD)[lane];
-        o.x += wi * v.x; o.y += wi * v.y; o.z += wi * v.z; o.w += wi * v.w;
+#pragma unroll
+      for (int r = 0; r < kCombineRows; ++r) {
+        const float wi = __shfl_sync(0xffffffffu, w[r], i);
+        if (wi != 0.f) {
+          const float4 v = reinterpret_cast<const float4 *>(
+              part_o + (((int64_t)first + c0 + i) * 128 + row_base + 8 * r) * HD)[lane];
+          o[r].x += wi * v.x; o[r].y += wi * v.y; o[r].z += wi * v.z; o[r].w += wi * v.w;
+        }
       }
     }
   }
-  for (int s = 16; s; s >>= 1) l += __shfl_xor_sync(0xffffffffu, l, s);
-  const float inv = 1.f / l;
-  bf16 *dst = out + (int64_t)(row0 + qi) * ld_out + (id.g * P.G + h) * HD + lane * 4;
-  __nv_bfloat162 lo = __floats2bfloat162_rn(o.x * inv, o.y * inv);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(o.z * inv, o.w * inv);
-  uint2 pk;
-  pk.x = *reinterpret_cast<uint32_t *>(&lo);
-  pk.y = *reinterpret_cast<uint32_t *>(&hi);
-  *reinterpret_cast<uint2 *>(dst) = pk;
+#pragma unroll
+  for (int r = 0; r < kCombineRows; ++r) {
+    for (int s = 16; s; s >>= 1) l[r] += __shfl_xor_sync(0xffffffffu, l[r], s);
+    const int row = row_base + 8 * r;
+    const int h = row / P.QT, qi = row % P.QT;
+    if (qi >= n_valid) continue;
+    const float inv = 1.f / l[r];
+    bf16 *dst = out + (int64_t)(row0 + qi) * ld_out + (id.g * P.G + h) * HD + lane * 4;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(o[r].x * inv, o[r].y * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(o[r].z * inv, o[r].w * inv);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t *>(&lo);
+    pk.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(dst) = pk;
+  }
 }
 
 // ------------------------------------------------------------------ host --
@@ -919,7 +943,7 @@ cudaError_t launch_attention_tc(const void *q, int64_t ld_q, const int32_t *q_po
                              part_ml, status);
   if (e != cudaSuccess) return e;
   if (!split) return launched(1);
-  e = launch_pdl(attn_combine_kernel, dim3(tiles * 16), dim3(256), 0, s, P,
+  e = launch_pdl(attn_combine_kernel, dim3(tiles * 4), dim3(256), 0, s, P,
                  (const float *)part_o, (const float2 *)part_ml, reinterpret_cast<bf16 *>(out),
                  ld_out);
   if (e != cudaSuccess) return e;
