@@ -164,10 +164,11 @@ def setup_replica(rank, device, n_layers=None):
 
 # DRAM traffic of the dominant kernel from one ncu capture (dram__bytes_read
 # + dram__bytes_write of the gate/up SwiGLU launch at M = 524 rows of a
-# compact layer), valid only for the kernel source it was taken on.
-TRAFFIC_CAPTURE = {"source": "rag_kv_cache_layer_gb300/csrc/k_gemm_tc.cu",
-                   "sha256": "1ad63e322072cb59eae2bde90f0e4f403e1cd16f3591d34cf164563c528850be",
-                   "bytes_per_launch": 241595136 + 11919104,
+# compact layer: the CTA-pair swapped GEMM), valid only for the kernel source
+# it was taken on.
+TRAFFIC_CAPTURE = {"source": "rag_kv_cache_layer_gb300/csrc/k_gemm_sab.cu",
+                   "sha256": "fe5bdf145740dcbcdf5e0c7c69e9f4e1c5447944bc66dbc3e712e9cf604a5318",
+                   "bytes_per_launch": 243631616 + 12040448,
                    "profile": "profiles/gemm_swiglu_M524_llama8b.md"}
 
 
