@@ -6,3 +6,4 @@ product path (``rag_kv_cache_layer_gb300``) never imports it and has no CPU
 fallback.
 """
 from .cacheblend import *  # noqa: F401,F403
+from .qcfuse import *  # noqa: F401,F403
