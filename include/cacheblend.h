@@ -81,11 +81,27 @@ typedef enum {
   CB_POLICY_RANDOM_DOC = 4,   /* [ROM] §2.3: document spans visited in the
                                  caller's span_order (its random draw),
                                  filled as DOC_ALIGNED                       */
-  CB_POLICY_FIRST_TOKENS = 5  /* [QCF] §2 (EPIC's chunk-boundary rule): the
+  CB_POLICY_FIRST_TOKENS = 5, /* [QCF] §2 (EPIC's chunk-boundary rule): the
                                  first tokens of every span, k shared out
                                  evenly (the first k mod m spans one more; a
                                  short span passes its surplus on in order)  */
+  CB_POLICY_QUERY_PROBE = 6,  /* [QCF] §3.3-3.4: per-chunk anchors (Eq. 14),
+                                 the query rows probed over the anchor cache
+                                 (Eqs. 15-17), P = top-k of their attention
+                                 mass on the context summed over the
+                                 critical layers (Eqs. 20, 11)               */
+  CB_POLICY_QUERY_FULL = 7    /* [QCF] §3.2.1: the full-view reference
+                                 (Eqs. 9-11): every context position is an
+                                 anchor and every layer is critical          */
 } cb_policy;
+
+/* Anchor rule of [QCF] Eq. 14: the score G_i(r) of chunk-local position r. */
+typedef enum {
+  CB_ANCHOR_SINK = 0,   /* -r: the chunk's first positions                  */
+  CB_ANCHOR_KNORM = 1   /* minus the squared L2 norm of the position's PIC
+                           keys summed over all layers and kv heads: the
+                           lowest-norm keys first                            */
+} cb_anchor_rule;
 
 /* Largest batch of requests one call accepts. */
 #define CB_MAX_BATCH 64
@@ -447,7 +463,32 @@ typedef struct {
                           still computed.  Lets an external selector (or a
                           reference run) fix P.  A position outside
                           [0, N_b) records CB_ERR_DEVICE_INDEX.            */
+  /* CB_POLICY_QUERY_PROBE: anchors and critical layers.  Both query
+     policies select before layer 0 (sel_layer and the schedule must be 0):
+     every layer recomputes P and the uncached rows, and `deviation` of the
+     outputs receives the score I(t) in place of d. */
+  cb_anchor_rule anchor_rule;
+  int anchor_bp;       /* r_a in basis points: ceil(r_a |c_i|) anchors per
+                          chunk                                             */
+  int n_crit;          /* the critical-layer set L*: n_crit >= 1 distinct  */
+  const int32_t *crit_layers; /* host [n_crit] layers in [0, n_layers)     */
 } cb_blend_params;
+
+/* Per-chunk anchors of [QCF] Eq. 14, as the offline cache preparation of
+ * [QCF] §3.1 would store them: for each of n_chunks cached segments (given
+ * as for cb_request, k_pic read on the device), the scores G_i(r) of its
+ * positions by `rule` (cb_anchor_rule), then A_i = the ceil(ratio_bp |c_i| /
+ * 10000) highest (equal scores: the lower position first), ascending
+ * chunk-local positions.
+ *   scores_out:  device float [sum len] or NULL, chunk after chunk;
+ *   anchors_out: device int32 [sum ceil(...)], chunk after chunk.
+ * ws: device workspace of cb_anchor_workspace_size(n_chunks) bytes.
+ * Errors: CB_ERR_INVALID_ARG (NULL pointers, ratio_bp outside [0, 10000],
+ * a bad rule or PIC layout), CB_ERR_WORKSPACE. */
+size_t cb_anchor_workspace_size(const cb_model *m, const cb_segment *chunks, int n_chunks);
+cb_status cb_anchor_select(const cb_model *m, const cb_segment *chunks, int n_chunks,
+                           cb_anchor_rule rule, int ratio_bp, float *scores_out,
+                           int32_t *anchors_out, void *ws, size_t ws_bytes, cb_stream stream);
 
 /* Outputs of a prefill call.  The fused cache of request b occupies rows
  * [t_off_b, t_off_b + T_b) of every layer, t_off_b = sum_{c<b} T_c. */

@@ -22,6 +22,8 @@ CB_F32, CB_BF16 = 0, 1
 CB_POLICY_TOKEN_TOPK, CB_POLICY_DOC_ALIGNED = 0, 1
 CB_POLICY_SINGLE_WINDOW, CB_POLICY_FIXED_CHUNK, CB_POLICY_RANDOM_DOC = 2, 3, 4
 CB_POLICY_FIRST_TOKENS = 5
+CB_POLICY_QUERY_PROBE, CB_POLICY_QUERY_FULL = 6, 7
+CB_ANCHOR_SINK, CB_ANCHOR_KNORM = 0, 1
 CB_EPI_STORE, CB_EPI_RESID, CB_EPI_SWIGLU = 0, 1, 2
 CB_GEMM_AUTO, CB_GEMM_TOKEN_M, CB_GEMM_SWAP_AB, CB_GEMM_SWAP_AB_PAIR = 0, 1, 2, 3
 CB_PROBE_QKV, CB_PROBE_O, CB_PROBE_SWIGLU, CB_PROBE_DOWN, CB_PROBE_ATTENTION = 1, 2, 3, 4, 5
@@ -95,7 +97,9 @@ class BlendParams(C.Structure):
     _fields_ = [("ratio_bp", i32), ("policy", i32), ("sel_layer", i32),
                 ("n_schedule", i32), ("schedule", C.POINTER(ScheduleStep)),
                 ("span_len", i32), ("span_offset", i32),
-                ("span_order", C.POINTER(C.c_int32)), ("forced_selected", vp)]
+                ("span_order", C.POINTER(C.c_int32)), ("forced_selected", vp),
+                ("anchor_rule", i32), ("anchor_bp", i32), ("n_crit", i32),
+                ("crit_layers", C.POINTER(C.c_int32))]
 
 
 class BlendOut(C.Structure):
@@ -163,6 +167,9 @@ def _load():
         "cb_layer_workspace_size": (C.c_size_t, [vp, i32]),
         "cb_blend_layer": (S, [vp, i32, vp, i32, vp, vp, C.POINTER(AttnReq), i32,
                                vp, vp, vp, C.c_size_t, vp]),
+        "cb_anchor_workspace_size": (C.c_size_t, [vp, C.POINTER(Segment), i32]),
+        "cb_anchor_select": (S, [vp, C.POINTER(Segment), i32, i32, i32, vp, vp, vp,
+                                 C.c_size_t, vp]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(lib, name)
@@ -188,6 +195,7 @@ EXPORTED = [
     "cb_blend_prefill", "cb_blend_plan_host_kv", "cb_blend_prefill_host_kv",
     "cb_full_plan", "cb_full_prefill",
     "cb_layer_workspace_size", "cb_blend_layer",
+    "cb_anchor_workspace_size", "cb_anchor_select",
 ]
 
 

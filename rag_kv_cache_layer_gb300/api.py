@@ -294,7 +294,9 @@ class BlendModel:
                                  _s(stream)))
 
     def _params(self, ratio_bp, policy, sel_layer, schedule, forced=None, span_len=0,
-                span_offset=0, span_order=None):
+                span_offset=0, span_order=None, query=None):
+        """query: for the query-aware policies, a dict with anchor_rule,
+        anchor_bp and crit_layers (QCFuse Eqs. 14, 20)."""
         n = len(schedule or [])
         sch = (L.ScheduleStep * max(1, n))()
         for i, (l, k) in enumerate(schedule or []):
@@ -302,20 +304,26 @@ class BlendModel:
         order = None
         if span_order is not None:
             order = (C.c_int32 * max(1, len(span_order)))(*[int(x) for x in span_order])
+        q = query or {}
+        crit = [int(x) for x in q.get("crit_layers", [])]
+        crit_arr = (C.c_int32 * max(1, len(crit)))(*crit)
         return L.BlendParams(ratio_bp, policy, sel_layer, n,
                              C.cast(sch, C.POINTER(L.ScheduleStep)), span_len, span_offset,
                              None if order is None else C.cast(order, C.POINTER(C.c_int32)),
-                             None if forced is None else forced.data_ptr()), (sch, order)
+                             None if forced is None else forced.data_ptr(),
+                             int(q.get("anchor_rule", L.CB_ANCHOR_SINK)),
+                             int(q.get("anchor_bp", 0)), len(crit),
+                             C.cast(crit_arr, C.POINTER(C.c_int32))), (sch, order, crit_arr)
 
     def plan(self, reqs, ratio_bp=None, policy=0, sel_layer=1, schedule=None, span_len=0,
-             span_offset=0, span_order=None):
+             span_offset=0, span_order=None, query=None):
         arr, keep = _requests(reqs)
         out = L.Plan()
         if ratio_bp is None:
             check(lib.cb_full_plan(self.handle, arr, len(reqs), C.byref(out)))
         else:
             p, sch = self._params(ratio_bp, policy, sel_layer, schedule, None, span_len,
-                                  span_offset, span_order)
+                                  span_offset, span_order, query)
             check(lib.cb_blend_plan(self.handle, arr, len(reqs), C.byref(p),
                                     C.byref(out)))
         return out
@@ -346,14 +354,17 @@ class BlendModel:
 
     def cb_blend_prefill(self, reqs, ratio_bp, policy=0, sel_layer=1,
                          schedule=None, outputs=None, forced=None,
-                         stream=None, span_len=0, span_offset=0, span_order=None):
+                         stream=None, span_len=0, span_offset=0, span_order=None,
+                         query=None):
         """forced: optional device int32 tensor of selected context
         positions (ascending per request) used instead of the ranking.
         span_len / span_offset (fixed-chunk) and span_order (random-document,
-        all requests' segment orders concatenated) as in cb_blend_params."""
+        all requests' segment orders concatenated) as in cb_blend_params.
+        query: anchor_rule / anchor_bp / crit_layers of the query-aware
+        policies (sel_layer must then be 0)."""
         arr, keep = _requests(reqs)
         p, sch = self._params(ratio_bp, policy, sel_layer, schedule, forced, span_len,
-                              span_offset, span_order)
+                              span_offset, span_order, query)
         if outputs is None:
             plan = L.Plan()
             check(lib.cb_blend_plan(self.handle, arr, len(reqs), C.byref(p),
@@ -385,6 +396,26 @@ class BlendModel:
                                            C.byref(o), _p(ws), ws.numel(), _s(stream),
                                            _s(copy_stream)))
         return outputs
+
+    def cb_anchor_select(self, segs, rule, ratio_bp, with_scores=True, stream=None):
+        """Per-chunk anchors of QCFuse Eq. 14 for cached segments (Seg):
+        returns (anchors int32 [sum ceil(r_a |c|)], scores float [sum len] or
+        None), chunk after chunk, chunk-local positions ascending."""
+        sa = (L.Segment * len(segs))()
+        for j, sg in enumerate(segs):
+            sa[j] = L.Segment(sg.len, None if sg.k_pic is None else sg.k_pic.data_ptr(),
+                              None if sg.v_pic is None else sg.v_pic.data_ptr(),
+                              sg.pic_layer_stride, sg.pic_pos0)
+        n_a = sum((sg.len * ratio_bp + 9999) // 10000 for sg in segs)
+        n = sum(sg.len for sg in segs)
+        anchors = torch.empty(max(n_a, 1), dtype=torch.int32, device=self.device)
+        scores = torch.empty(max(n, 1), dtype=torch.float32, device=self.device) if with_scores else None
+        need = lib.cb_anchor_workspace_size(self.handle, sa, len(segs))
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
+        check(lib.cb_anchor_select(self.handle, sa, len(segs), rule, ratio_bp,
+                                   None if scores is None else scores.data_ptr(),
+                                   anchors.data_ptr(), _p(ws), ws.numel(), _s(stream)))
+        return anchors[:n_a], (None if scores is None else scores[:n])
 
     def plan_host_kv(self, reqs, ratio_bp, policy=0, sel_layer=1):
         arr, keep = _requests(reqs)

@@ -28,6 +28,7 @@ SOURCES = [
     "k_gemm_sab.cu",
     "k_attn_simt.cu",
     "k_attn_tc.cu",
+    "k_qprobe.cu",
     "k_noalloc.cu",
 ]
 
@@ -66,7 +67,8 @@ def build(verbose: bool = False, ptxas_verbose: bool = False) -> str:
         objs = list(ex.map(lambda s: _compile(s, verbose or ptxas_verbose, extra),
                            SOURCES))
     tmp = LIB + ".tmp"
-    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
+    # every symbol must resolve inside the library or its runtime deps
+    cmd = [nvcc(), *ARCH, "-shared", "-Xlinker", "--no-undefined", "-o", tmp, *objs, "-lcuda"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)

@@ -576,6 +576,11 @@ struct Plan {
   LayerOffsets lay;
   size_t h_all, kf, dev, sel, pos_all, glob_all, pos_c, glob_c, h_c, lm_x, lm_best, total;
   size_t attn_plan = 0, attn_plan_bytes = 0;   // unit table of the compact layers' attention
+  // query-aware selection ([QCF] §3.3-3.4)
+  ProbeLayout probe;
+  int n_anchor_total = 0;
+  size_t qp_scores = 0, qp_anchors = 0, qp_rows = 0, qp_u = 0, qp_k = 0, qp_v = 0, qp_h = 0,
+         qp_mass = 0, qp_mass_bytes = 0;
   size_t g_dev = 0, g_keep = 0, g_sel = 0, g_pos = 0, g_glob = 0, g_src = 0, g_h = 0;
   // host-resident chunk path: two layers of the context K/V in flight
   size_t stage = 0, stage_bytes = 0;     // stage_bytes: K of one layer (V follows)
@@ -631,6 +636,10 @@ static int select_count(int n_ctx, int ratio_bp) {
   return (int)(k < 1 ? 1 : k);
 }
 
+static bool is_query_policy(cb_policy p) {
+  return p == CB_POLICY_QUERY_PROBE || p == CB_POLICY_QUERY_FULL;
+}
+
 static cb_status make_plan(const cb_model *m, const cb_request *reqs, int B,
                            const cb_blend_params *p, bool blend, Plan &P,
                            bool host_kv = false) {
@@ -640,8 +649,32 @@ static cb_status make_plan(const cb_model *m, const cb_request *reqs, int B,
     if (p->ratio_bp < 0 || p->ratio_bp > 10000) return fail(CB_ERR_INVALID_ARG, "ratio_bp must be in [0, 10000]");
     if (p->sel_layer < 0 || p->sel_layer >= m->cfg.n_layers)
       return fail(CB_ERR_INVALID_ARG, "sel_layer must be in [0, n_layers)");
-    if (p->policy < CB_POLICY_TOKEN_TOPK || p->policy > CB_POLICY_FIRST_TOKENS)
+    if (p->policy < CB_POLICY_TOKEN_TOPK || p->policy > CB_POLICY_QUERY_FULL)
       return fail(CB_ERR_INVALID_ARG, "unknown policy");
+    if (is_query_policy(p->policy)) {
+      // [QCF] §3.5: P exists before layer 0, every layer recomputes it
+      if (p->sel_layer != 0 || p->n_schedule != 0)
+        return fail(CB_ERR_INVALID_ARG, "query-aware policies select before layer 0: sel_layer and n_schedule must be 0");
+      if (host_kv)
+        return fail(CB_ERR_UNSUPPORTED, "query-aware policies need the chunk caches on the device");
+      if (m->cfg.dtype != CB_BF16 || m->cfg.head_dim != 128)
+        return fail(CB_ERR_UNSUPPORTED, "query-aware policies run on bf16 models with head_dim 128");
+      if (p->policy == CB_POLICY_QUERY_PROBE) {
+        if (p->anchor_rule != CB_ANCHOR_SINK && p->anchor_rule != CB_ANCHOR_KNORM)
+          return fail(CB_ERR_INVALID_ARG, "unknown anchor rule");
+        if (p->anchor_bp < 0 || p->anchor_bp > 10000)
+          return fail(CB_ERR_INVALID_ARG, "anchor_bp must be in [0, 10000]");
+        if (p->n_crit < 1 || p->n_crit > m->cfg.n_layers || !p->crit_layers)
+          return fail(CB_ERR_INVALID_ARG, "the critical-layer set needs 1..n_layers layers");
+        for (int i = 0; i < p->n_crit; ++i) {
+          if (p->crit_layers[i] < 0 || p->crit_layers[i] >= m->cfg.n_layers)
+            return fail(CB_ERR_INVALID_ARG, "critical layer out of range");
+          for (int j = 0; j < i; ++j)
+            if (p->crit_layers[j] == p->crit_layers[i])
+              return fail(CB_ERR_INVALID_ARG, "critical layers must be distinct");
+        }
+      }
+    }
     if (p->policy == CB_POLICY_RANDOM_DOC && !p->span_order)
       return fail(CB_ERR_INVALID_ARG, "random-document needs span_order");
     if (p->policy == CB_POLICY_FIXED_CHUNK &&
@@ -738,6 +771,53 @@ static cb_status make_plan(const cb_model *m, const cb_request *reqs, int B,
     P.g_src = cv.take((P.R_total + 1) * sizeof(int32_t));
     P.g_h = cv.take((P.R_total + 1) * c.d_model * sizeof(float));
   }
+  if (blend && is_query_policy(p->policy)) {
+    // [QCF] Eqs. 14-17: anchors, the probe cache [anchors; query rows] of
+    // each request, the query rows' hidden states and the mass scratch
+    const bool all = p->policy == CB_POLICY_QUERY_FULL;
+    ProbeLayout &Q = P.probe;
+    Q.B = B;
+    Q.all = all;
+    int probe_off = 0, u_off = 0, anchor_off = 0;
+    size_t mass = 0;
+    for (int b = 0; b < B; ++b) {
+      ProbeLayout::Req r{};
+      r.t_off = P.bm.t_off[b];
+      r.n_ctx = P.N[b];
+      r.n_u = P.T[b] - P.N[b];
+      r.seg_begin = (int)Q.segs.size();
+      for (int i = 0; i < reqs[b].n_segments; ++i) {
+        const cb_segment &sg = reqs[b].segments[i];
+        if (!sg.k_pic || sg.len == 0) continue;
+        const int cnt = all ? sg.len : (int)(((int64_t)sg.len * p->anchor_bp + 9999) / 10000);
+        Q.segs.push_back(ProbeLayout::Seg{anchor_off, cnt, P.seg_start[b][i], sg.len});
+        anchor_off += cnt;
+        r.n_anchor += cnt;
+      }
+      r.seg_end = (int)Q.segs.size();
+      r.probe_off = probe_off;
+      r.u_off = u_off;
+      Q.reqs[b] = r;
+      probe_off += r.n_anchor + r.n_u;
+      u_off += r.n_u;
+      const size_t mb = mass_ws_bytes(r.n_u, c.n_q_heads, r.n_ctx);
+      if (mb > mass) mass = mb;
+    }
+    if ((int)Q.segs.size() > CB_MAX_SPANS)
+      return fail(CB_ERR_INVALID_ARG, "more than %d cached segments in one query-aware call", CB_MAX_SPANS);
+    Q.n_probe = probe_off;
+    Q.n_u = u_off;
+    P.n_anchor_total = anchor_off;
+    P.qp_scores = cv.take((P.N_total + 1) * sizeof(float));
+    P.qp_anchors = cv.take((size_t)(anchor_off + 1) * sizeof(int32_t));
+    P.qp_rows = cv.take((size_t)(probe_off + 1) * sizeof(int32_t));
+    P.qp_u = cv.take((size_t)4 * (u_off + 1) * sizeof(int32_t));
+    P.qp_k = cv.take((size_t)(probe_off + 1) * m->kvw * m->eb);
+    P.qp_v = cv.take((size_t)(probe_off + 1) * m->kvw * m->eb);
+    P.qp_h = cv.take((size_t)(u_off + 1) * c.d_model * sizeof(float));
+    P.qp_mass_bytes = mass;
+    P.qp_mass = cv.take(mass);
+  }
   if (host_kv) {
     P.stage_bytes = (size_t)(P.N_total + 1) * m->kvw * m->eb;
     P.stage_bytes = (P.stage_bytes + 255) / 256 * 256;
@@ -784,7 +864,8 @@ static inline char *layer_ptr(void *base, int l, int64_t stride, size_t eb) {
 static cb_status layer_forward(cb_model *m, int l, float *h, int n, const int32_t *pos,
                                const int32_t *cache_row, const std::vector<AttnReq> &ar,
                                void *kc, void *vc, const LayerScratch &S, int *st,
-                               cudaStream_t s, const int *attn_plan = nullptr) {
+                               cudaStream_t s, const int *attn_plan = nullptr,
+                               const int32_t *attn_pos = nullptr) {
   const cb_model_config &c = m->cfg;
   const cb_layer_weights &L = m->layers[l];
   const int d = c.d_model, F = c.d_ffn, hd = c.head_dim;
@@ -805,7 +886,10 @@ static cb_status layer_forward(cb_model *m, int l, float *h, int n, const int32_
   }
   probe_mark(CB_PROBE_QKV, false, s);
   probe_mark(CB_PROBE_ATTENTION, true, s);
-  CB_TRY(run_attention(S.q, m->qw, pos, ar, kc, vc, m->kvw, c.n_q_heads, c.n_kv_heads, hd,
+  // attn_pos: the rows' causal-mask positions in kc / vc when these are not
+  // their request positions (the query probe's compact cache)
+  CB_TRY(run_attention(S.q, m->qw, attn_pos ? attn_pos : pos, ar, kc, vc, m->kvw, c.n_q_heads,
+                       c.n_kv_heads, hd,
                        1.f / sqrtf((float)hd), S.o, m->qw, dt, S.attn, S.attn_bytes, st, s,
                        attn_plan));
   probe_mark(CB_PROBE_ATTENTION, false, s);
@@ -933,6 +1017,129 @@ static cb_status filter_rows(cb_model *m, int l, const BatchMeta &cur, const Bat
 // slice is copied (copy engines, on copy_stream) into a two-layer staging
 // area and stitched right before the layer runs, so the load of layer l + 1
 // overlaps the compute of layer l ([CB] "Hiding Recompute Behind I/O").
+// Per-chunk anchors ([QCF] Eq. 14): scores of every position, then each
+// chunk's count highest (ties to the lower position), ascending.
+static cb_status rank_anchors(const cb_model *m, const std::vector<AnchorChunk> &ch,
+                              const std::vector<ProbeLayout::Seg> &segs, int rule,
+                              float *scores, int32_t *anchors, cudaStream_t s) {
+  CB_CUDA(launch_anchor_scores(ch.data(), (int)ch.size(), rule, m->cfg.n_layers, m->kvw,
+                               m->cfg.dtype, scores, s));
+  for (size_t base = 0; base < ch.size(); base += CB_MAX_BATCH) {
+    SelReq r[CB_MAX_BATCH];
+    int n = 0;
+    for (size_t i = base; i < ch.size() && n < CB_MAX_BATCH; ++i, ++n)
+      r[n] = SelReq{ch[i].len, segs[i].count, 0, 0, ch[i].score_off, segs[i].anchor_off, 0, 0};
+    CB_CUDA(launch_topk(scores, r, n, anchors, s));
+  }
+  return CB_OK;
+}
+
+// [QCF] §3.3-3.4: every request's query rows (its uncached rows) run layers
+// 0 .. max(L*) over the probe cache [anchors; query rows] (Eqs. 15-17: the
+// anchors' stitched PIC entries at their request positions, read only);
+// after each critical layer their attention mass on the request's context
+// keys is added into I (Eq. 20).  QUERY_FULL: every position is an anchor
+// and every layer critical (Eqs. 9-10).
+static cb_status query_probe(cb_model *m, const cb_request *reqs, int B,
+                             const cb_blend_params *p, const Plan &P, char *ws,
+                             const cb_blend_out *out, int64_t lstride, const LayerScratch &S,
+                             const float *h_all, float *I, int *st, cudaStream_t s) {
+  const cb_model_config &c = m->cfg;
+  const ProbeLayout &Q = P.probe;
+  const int d = c.d_model;
+  int32_t *anchors = (int32_t *)(ws + P.qp_anchors);
+  if (!Q.all) {
+    std::vector<AnchorChunk> ch;
+    for (int b = 0; b < B; ++b)
+      for (int i = 0; i < reqs[b].n_segments; ++i) {
+        const cb_segment &sg = reqs[b].segments[i];
+        if (!sg.k_pic || sg.len == 0) continue;
+        ch.push_back(AnchorChunk{sg.k_pic, sg.pic_layer_stride, sg.len,
+                                 P.n_off[b] + P.seg_start[b][i]});
+      }
+    CB_TRY(rank_anchors(m, ch, Q.segs, p->anchor_rule, (float *)(ws + P.qp_scores), anchors, s));
+  }
+  const int nu = Q.n_u;
+  int32_t *u = (int32_t *)(ws + P.qp_u);
+  int32_t *u_pos = u, *u_src = u + (nu + 1), *u_cache = u + 2 * (nu + 1), *u_mask = u + 3 * (nu + 1);
+  int32_t *rows = (int32_t *)(ws + P.qp_rows);
+  CB_CUDA(launch_probe_rows(Q, anchors, rows, u_pos, u_src, u_cache, u_mask, st, s));
+  float *h_u = (float *)(ws + P.qp_h);
+  CB_CUDA(launch_gather(h_all, d, P.T_total, u_src, nu, d, h_u, d, sizeof(float), st, s));
+  CB_CUDA(cudaMemsetAsync(I, 0, (size_t)P.N_total * sizeof(float), s));
+  std::vector<char> crit(c.n_layers, p->policy == CB_POLICY_QUERY_FULL ? 1 : 0);
+  int last = c.n_layers - 1;
+  if (p->policy == CB_POLICY_QUERY_PROBE) {
+    last = 0;
+    for (int i = 0; i < p->n_crit; ++i) {
+      crit[p->crit_layers[i]] = 1;
+      if (p->crit_layers[i] > last) last = p->crit_layers[i];
+    }
+  }
+  std::vector<AttnReq> ar(B);
+  for (int b = 0; b < B; ++b) {
+    const ProbeLayout::Req &r = Q.reqs[b];
+    ar[b] = AttnReq{r.u_off, r.u_off + r.n_u, (int64_t)r.probe_off, r.n_anchor + r.n_u};
+  }
+  void *pk = ws + P.qp_k, *pv = ws + P.qp_v;
+  for (int l = 0; l <= last; ++l) {
+    const char *kl = layer_ptr(out->k_cache, l, lstride, m->eb);
+    const char *vl = layer_ptr(out->v_cache, l, lstride, m->eb);
+    CB_CUDA(launch_gather(kl, m->kvw, P.T_total, rows, Q.n_probe, m->kvw, pk, m->kvw, m->eb, st, s));
+    CB_CUDA(launch_gather(vl, m->kvw, P.T_total, rows, Q.n_probe, m->kvw, pv, m->kvw, m->eb, st, s));
+    CB_TRY(layer_forward(m, l, h_u, nu, u_pos, u_cache, ar, pk, pv, S, st, s, nullptr, u_mask));
+    if (!crit[l]) continue;
+    for (int b = 0; b < B; ++b) {
+      const ProbeLayout::Req &r = Q.reqs[b];
+      CB_CUDA(launch_attention_mass(S.q, m->qw, r.u_off, r.n_u, kl, m->kvw, r.t_off, r.n_ctx,
+                                    c.n_q_heads, c.n_kv_heads, c.head_dim, ws + P.qp_mass,
+                                    P.qp_mass_bytes, I + P.n_off[b], s));
+    }
+  }
+  return CB_OK;
+}
+
+extern "C" size_t cb_anchor_workspace_size(const cb_model *m, const cb_segment *chunks,
+                                           int n_chunks) {
+  if (!m || !chunks || n_chunks <= 0) return 256;
+  int64_t total = 0;
+  for (int i = 0; i < n_chunks; ++i) total += chunks[i].len > 0 ? chunks[i].len : 0;
+  return (size_t)(total + 1) * sizeof(float) + 256;
+}
+
+extern "C" cb_status cb_anchor_select(const cb_model *m, const cb_segment *chunks, int n_chunks,
+                                      cb_anchor_rule rule, int ratio_bp, float *scores_out,
+                                      int32_t *anchors_out, void *ws, size_t ws_bytes,
+                                      cb_stream stream) {
+  if (!m || !chunks || !anchors_out) return fail(CB_ERR_INVALID_ARG, "NULL pointer");
+  if (n_chunks <= 0) return fail(CB_ERR_INVALID_ARG, "n_chunks must be >= 1");
+  if (rule != CB_ANCHOR_SINK && rule != CB_ANCHOR_KNORM) return fail(CB_ERR_INVALID_ARG, "unknown anchor rule");
+  if (ratio_bp < 0 || ratio_bp > 10000) return fail(CB_ERR_INVALID_ARG, "ratio_bp must be in [0, 10000]");
+  std::vector<AnchorChunk> ch;
+  std::vector<ProbeLayout::Seg> segs;
+  int score_off = 0, anchor_off = 0;
+  for (int i = 0; i < n_chunks; ++i) {
+    const cb_segment &sg = chunks[i];
+    if (sg.len < 0) return fail(CB_ERR_INVALID_ARG, "chunk %d: len < 0", i);
+    if (rule == CB_ANCHOR_KNORM && sg.len > 0 &&
+        (!sg.k_pic || !aligned16(sg.k_pic) || (sg.pic_layer_stride * (int64_t)m->eb) % 16 ||
+         sg.pic_layer_stride < (int64_t)sg.len * m->kvw))
+      return fail(CB_ERR_INVALID_ARG, "chunk %d: bad PIC layout", i);
+    const int cnt = (int)(((int64_t)sg.len * ratio_bp + 9999) / 10000);
+    ch.push_back(AnchorChunk{sg.k_pic, sg.pic_layer_stride, sg.len, score_off});
+    segs.push_back(ProbeLayout::Seg{anchor_off, cnt, 0, sg.len});
+    score_off += sg.len;
+    anchor_off += cnt;
+  }
+  float *scores = scores_out;
+  if (!scores) {
+    if (!ws || ws_bytes < (size_t)(score_off + 1) * sizeof(float))
+      return fail(CB_ERR_WORKSPACE, "anchor workspace too small");
+    scores = (float *)ws;
+  }
+  return rank_anchors(m, ch, segs, rule, scores, anchors_out, stream);
+}
+
 static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
                             const cb_blend_params *p, const cb_blend_out *out, void *ws_v,
                             size_t ws_bytes, cudaStream_t stream, bool host_kv,
@@ -1032,19 +1239,23 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
     CB_TRY(layer_forward(m, l, h_all, (int)P.T_total, pos_all, glob_all, ar_full,
                          layer_ptr(out->k_cache, l, lstride, m->eb),
                          layer_ptr(out->v_cache, l, lstride, m->eb), S, st, s));
-  // 3. selection layer: fresh keys of every row, deviation, ranking
+  // 3. selection layer: fresh keys of every row, deviation, ranking; the
+  // query-aware policies score the context with the query probe instead
   if (host_kv) CB_TRY(stitch_layer(s_layer));
+  const bool query = is_query_policy(p->policy);
   {
     const cb_layer_weights &Ls = m->layers[s_layer];
     void *kf = ws + P.kf;
-    CB_CUDA(launch_rmsnorm(h_all, d, nullptr, (int)P.T_total, d, Ls.norm1, c.norm_eps, S.x, d,
-                           c.dtype, s));
-    const char *wk = (const char *)Ls.w_qkv + (int64_t)m->qw * d * m->eb;
-    CB_TRY(run_linear(m, S.x, d, wk, nullptr, d, (int)P.T_total, m->kvw, d, EPI_STORE_F32,
-                      S.qkv32, m->kvw, s));
-    CB_CUDA(launch_qkv_finish(S.qkv32, m->kvw, (int)P.T_total, pos_all, nullptr, c.n_q_heads,
-                              c.n_kv_heads, c.head_dim, m->w.rope_table, nullptr, 0, kf,
-                              nullptr, m->kvw, c.dtype, 0, s));
+    if (!query) {
+      CB_CUDA(launch_rmsnorm(h_all, d, nullptr, (int)P.T_total, d, Ls.norm1, c.norm_eps, S.x, d,
+                             c.dtype, s));
+      const char *wk = (const char *)Ls.w_qkv + (int64_t)m->qw * d * m->eb;
+      CB_TRY(run_linear(m, S.x, d, wk, nullptr, d, (int)P.T_total, m->kvw, d, EPI_STORE_F32,
+                        S.qkv32, m->kvw, s));
+      CB_CUDA(launch_qkv_finish(S.qkv32, m->kvw, (int)P.T_total, pos_all, nullptr, c.n_q_heads,
+                                c.n_kv_heads, c.head_dim, m->w.rope_table, nullptr, 0, kf,
+                                nullptr, m->kvw, c.dtype, 0, s));
+    }
     // selection requests: every request's cached segments are its spans
     std::vector<cb_select_req> cr(B);
     std::vector<std::vector<int32_t>> seg_offs(B);
@@ -1075,11 +1286,22 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
     }
     SelPlan plan;
     const char *err = "";
-    if (make_sel_plan(cr.data(), B, p->policy, plan, &err) != CB_OK)
+    if (make_sel_plan(cr.data(), B, query ? CB_POLICY_TOKEN_TOPK : p->policy, plan, &err) !=
+        CB_OK)
       return fail(CB_ERR_INVALID_ARG, "%s", err);
     const std::vector<SelReq> &sr = plan.reqs;
     probe_mark(CB_PROBE_SELECT, true, s);
-    if (p->forced_selected) {
+    if (query) {
+      // I(t) in the deviation buffer, then P = TopK(I, k) ([QCF] Eq. 11)
+      CB_TRY(query_probe(m, reqs, B, p, P, ws, out, lstride, S, h_all, dev, st, s));
+      if (p->forced_selected) {
+        if (sel != p->forced_selected && P.K_total > 0)
+          CB_CUDA(cudaMemcpyAsync(sel, p->forced_selected, P.K_total * sizeof(int32_t),
+                                  cudaMemcpyDeviceToDevice, s));
+      } else {
+        CB_CUDA(launch_selection(dev, plan, sel, st, s));
+      }
+    } else if (p->forced_selected) {
       // the caller fixes P; d is still produced for inspection
       CB_CUDA(launch_deviation(kf, m->kvw, layer_ptr(out->k_cache, s_layer, lstride, m->eb),
                                m->kvw, m->kvw, c.dtype, sr.data(), B, dev, s));

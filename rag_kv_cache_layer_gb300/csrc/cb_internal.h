@@ -230,6 +230,42 @@ size_t attention_plan_bytes(const AttnReq *reqs, int n_req, int Hq, int Hkv);
 cudaError_t launch_attention_plan(const int32_t *q_pos, const AttnReq *reqs, int n_req, int Hq,
                                   int Hkv, int *plan, size_t plan_bytes, cudaStream_t s);
 
+// ------------------------------------------------- query-aware selection --
+// QCFuse §3.3-3.4 (k_qprobe.cu).  Anchor scores G_i(r) of one chunk's
+// positions (CB_ANCHOR_SINK: -r; CB_ANCHOR_KNORM: minus the squared norm of
+// its PIC keys over all layers and kv heads) at scores[score_off + r].
+struct AnchorChunk {
+  const void *k;          // PIC keys, layer l at k + l * layer_stride elements
+  int64_t layer_stride;
+  int len, score_off;
+};
+cudaError_t launch_anchor_scores(const AnchorChunk *chunks, int n, int rule, int n_layers,
+                                 int kvw, cb_dtype dt, float *scores, cudaStream_t s);
+// Layout of the probe cache: request b's rows [probe_off, + n_anchor + n_u)
+// hold its anchors (chunk by chunk, ascending) then its query rows.
+struct ProbeLayout {
+  struct Req {
+    int t_off, n_ctx, n_u, seg_begin, seg_end, probe_off, n_anchor, u_off;
+  };
+  struct Seg {
+    int anchor_off, count, ctx_off, len;
+  };
+  int B = 0, all = 0;            // all: every context position is an anchor
+  Req reqs[CB_MAX_BATCH];
+  std::vector<Seg> segs;
+  int n_probe = 0, n_u = 0;
+};
+cudaError_t launch_probe_rows(const ProbeLayout &L, const int32_t *anchors, int32_t *probe_rows,
+                              int32_t *u_pos, int32_t *u_src, int32_t *u_cache, int32_t *u_mask,
+                              int *status, cudaStream_t s);
+// mass[t] += sum over the request's query rows u and q heads h of the
+// softmax over its n_ctx context keys of q.k / sqrt(hd) (head_dim 128, bf16).
+size_t mass_ws_bytes(int n_u, int Hq, int n_ctx);
+cudaError_t launch_attention_mass(const void *q, int64_t ld_q, int u_off, int n_u,
+                                  const void *k_cache, int64_t ld_k, int t_off, int n_ctx,
+                                  int Hq, int Hkv, int hd, void *ws, size_t ws_bytes,
+                                  float *mass, cudaStream_t s);
+
 // ---------------------------------------------------------------- debug --
 cudaError_t launch_expire_wait(int limit_us, int *status, cudaStream_t s);
 

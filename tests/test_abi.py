@@ -48,7 +48,8 @@ STRUCTS = {
     "cb_schedule_step": (L.ScheduleStep, ["layer", "keep"]),
     "cb_blend_params": (L.BlendParams, ["ratio_bp", "policy", "sel_layer", "n_schedule",
                                         "schedule", "span_len", "span_offset", "span_order",
-                                        "forced_selected"]),
+                                        "forced_selected", "anchor_rule", "anchor_bp",
+                                        "n_crit", "crit_layers"]),
     "cb_blend_out": (L.BlendOut, ["k_cache", "v_cache", "cache_layer_stride", "deviation",
                                   "selected", "hidden", "rows", "first_token"]),
     "cb_plan": (L.Plan, ["T_total", "N_total", "K_total", "R_total", "workspace_bytes",
@@ -101,6 +102,9 @@ def test_host_validation_without_device():
     assert lib.cb_debug_probe_start(0, 4) == L.CB_ERR_INVALID_ARG
     assert lib.cb_debug_probe_start(L.CB_PROBE_SWIGLU, 0) == L.CB_ERR_INVALID_ARG
     assert lib.cb_debug_probe_stop(None, None) == L.CB_ERR_INVALID_ARG
+    # anchors: NULL model / chunks / output, bad rule or ratio
+    assert lib.cb_anchor_select(None, None, 1, 0, 1000, None, None, None, 0, None) == \
+        L.CB_ERR_INVALID_ARG
     # bad doc-aligned spans are rejected on the host
     spans = (C.c_int32 * 3)(0, 5, 4)
     req = L.SelectReq(4, 2, 0, 0, 0, 0, 2, C.cast(spans, C.POINTER(C.c_int32)), None, 0, 0)
