@@ -52,14 +52,15 @@ def parse_args():
                          "(for ncu --profile-from-start off); prints no JSON")
     ap.add_argument("--layers", type=int, default=None,
                     help="truncate the stack (profiling captures on a small footprint)")
-    ap.add_argument("--workload", choices=["rag", "rolling", "qwen", "long", "host_kv"],
+    ap.add_argument("--workload", choices=["rag", "rolling", "qwen", "long", "host_kv", "qcf"],
                     default="rag",
                     help="rag: the headline request (default); rolling: the 50-request "
                          "rolling-agent window, token top-k vs document-aligned at 5%%; "
                          "qwen: the Qwen3-8B-shaped batch of 4 at 30%%; long: the 32K "
                          "batch of 2 at r = 5/10/20/30%% against full prefill; host_kv: "
                          "the headline request with its chunk caches in pinned host "
-                         "memory, loaded layer by layer")
+                         "memory, loaded layer by layer; qcf: the headline request under "
+                         "the query-aware selectors (anchor probe and full view)")
     return ap.parse_args()
 
 
@@ -778,6 +779,69 @@ def run_host_kv(args):
     print(json.dumps(line), flush=True)
 
 
+def run_qcf(args):
+    """The headline request under the query-aware selectors of QCFuse
+    (§3.2-3.4): TTFT of the anchor probe (Knorm anchors at r_a = 10%, the
+    page's default ratio, and a critical-layer set of three middle layers:
+    the page profiles L* per model on span-labelled data that is not used
+    here, so the middle layers stand in) and of the full-view reference
+    (every position an anchor, every layer critical), against token top-k at
+    layer 1 and full prefill, at r = 15% and 30%.  The selection stage alone
+    (probe + attention mass + ranking) is timed with the library's probe."""
+    import torch
+    import rag_kv_cache_layer_gb300 as R
+    from rag_kv_cache_layer_gb300 import _lib as L
+
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(device)
+    wl, model, store, reqs, plan, outs, _, _ = setup_replica(0, device, args.layers)
+    n_layers = wl.model.n_layers
+    T = wl.requests[0].n_tokens
+    st = torch.cuda.current_stream()
+    mid = n_layers // 2
+    crit = sorted({min(max(l, 0), n_layers - 1) for l in (mid - 1, mid, mid + 1)})
+    full_outs = model.alloc_outputs(model.plan(reqs), 1, blend=False)
+    full_ms, _ = _graph_ms(lambda: model.cb_full_prefill(reqs, outputs=full_outs), args.steps, st)
+    del full_outs
+    pols = {
+        "token_topk": dict(policy=L.CB_POLICY_TOKEN_TOPK, sel_layer=1, query=None),
+        "query_probe": dict(policy=L.CB_POLICY_QUERY_PROBE, sel_layer=0,
+                            query={"anchor_rule": L.CB_ANCHOR_KNORM, "anchor_bp": 1000,
+                                   "crit_layers": crit}),
+        "query_full": dict(policy=L.CB_POLICY_QUERY_FULL, sel_layer=0, query=None),
+    }
+    rows = {}
+    for r in (1500, 3000):
+        for name, kw in pols.items():
+            o = model.alloc_outputs(model.plan(reqs, r, **kw), 1)
+            fn = lambda: model.cb_blend_prefill(reqs, r, outputs=o, **kw)
+            med, p95 = _graph_ms(fn, args.steps, st)
+            _, sel_ms = probe_steps(L, L.CB_PROBE_SELECT, 1,
+                                    lambda: (fn(), torch.cuda.synchronize()))
+            rows[f"{name} r={r / 100:g}%"] = {
+                "ttft_ms_median": med, "ttft_ms_p95": p95,
+                "context_tokens_per_s": T / (med / 1e3),
+                "speedup_vs_full_prefill": full_ms / med,
+                "selection_ms": sel_ms}
+            del o
+            torch.cuda.empty_cache()
+    if R.device_status() != 0:
+        raise RuntimeError("device status set during the query-aware workload")
+    key = rows["query_probe r=15%"]
+    line = {"metric": "blended-prefill TTFT with query-aware selection (QCFuse anchor probe)",
+            "value": key["ttft_ms_median"], "unit": "ms", "higher_is_better": False,
+            "n_gpus": 1, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "llama3-8b-shape 32L, 6x512 chunks + 64 query; Knorm "
+                                   "anchors r_a=10%, critical layers " + str(crit),
+                       "seq_len": T, "steps": args.steps},
+            "full_prefill_ms": full_ms, "policies": rows,
+            "context": "QCFuse page: 1.7x TTFT over full prefill at matched quality "
+                       "(its hardware; quality needs trained weights and is not measured)"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -788,6 +852,8 @@ def main():
         run_batch(args)
     elif args.workload == "host_kv":
         run_host_kv(args)
+    elif args.workload == "qcf":
+        run_qcf(args)
     else:
         run_ours(args)
 

@@ -135,62 +135,106 @@ __global__ void probe_rows_kernel(const __grid_constant__ ProbeParams p,
 // h * 128), context keys in the fused cache rows t_off + t, t < N.  Score
 // rows are ordered r = h * n_u + u, so a kv head's rows are contiguous.
 constexpr int HD = 128;
-constexpr int KC = 32;                  // keys per CTA of the score pass
-constexpr int kRowThreads = 256;
+constexpr int KC = 64;                  // keys per score tile
+constexpr int RC = 64;                  // rows per score tile
+constexpr int kTileThreads = 256;       // 16 x 16 threads, 4 rows x 4 keys each
+constexpr int kScoreSmem = 2 * HD * 64 * 4;
 
-// Scores s[t][r] = log2(e) q_r.k_t / sqrt(hd) of the chunk's keys for the
-// rows of kv head g, and each row's (max, sum of 2^(s - max)) over the chunk.
-__global__ void __launch_bounds__(kRowThreads)
+// Scores s[t][r] = log2(e) q_r.k_t / sqrt(hd) of a 64-row x 64-key tile
+// (all rows of one kv head's group), and each row's (max, sum of
+// 2^(s - max)) over the tile's keys.  Q and K are staged transposed in shared
+// memory ([dim][row], [dim][key]), so each step of the dot products reads
+// one float4 of rows and one of keys for 16 FMAs.
+__global__ void __launch_bounds__(kTileThreads)
 mass_score_kernel(const bf16 *__restrict__ q, int64_t ld_q, int u_off, int n_u,
                   const bf16 *__restrict__ kc, int64_t ld_k, int t_off, int n_ctx, int Hq,
                   int Hkv, float scale_log2, float *__restrict__ s,
                   float2 *__restrict__ part) {
   grid_dep_wait();
   grid_dep_launch();
-  __shared__ float ks[KC][HD + 4];
-  const int chunk = blockIdx.x, g = blockIdx.y;
+  extern __shared__ __align__(16) float sm[];
+  float *qs = sm;                        // [HD][RC]
+  float *ks = sm + HD * RC;              // [HD][KC]
   const int G = Hq / Hkv;
-  const int t0 = chunk * KC;
+  const int group_rows = G * n_u;
+  const int tiles_per_group = (group_rows + RC - 1) / RC;
+  const int g = blockIdx.y / tiles_per_group;
+  const int rt = blockIdx.y % tiles_per_group;
+  const int r0 = g * group_rows + rt * RC;           // first row of the tile
+  const int nr = min(RC, group_rows - rt * RC);
+  const int t0 = blockIdx.x * KC;
   const int nk = min(KC, n_ctx - t0);
   const int n_rows = Hq * n_u;
-  for (int e = threadIdx.x; e < KC * HD; e += kRowThreads) {
-    const int t = e / HD, c = e % HD;
-    ks[t][c] = t < nk ? __bfloat162float(kc[(int64_t)(t_off + t0 + t) * ld_k + g * HD + c]) : 0.f;
-  }
-  __syncthreads();
-  for (int rr = threadIdx.x; rr < G * n_u; rr += kRowThreads) {
-    const int r = g * G * n_u + rr;           // row of q head g*G + rr / n_u
-    const int h = r / n_u, u = r % n_u;
-    float qv[HD];
-    const bf16 *qr = q + (int64_t)(u_off + u) * ld_q + h * HD;
-#pragma unroll
-    for (int c = 0; c < HD; c += 8) {
-      const uint4 raw = *reinterpret_cast<const uint4 *>(qr + c);
+  // stage: entry i is row (and key) i % 64, dims 8 * (i / 64) .. + 7
+  for (int i = threadIdx.x; i < RC * (HD / 8); i += kTileThreads) {
+    const int row = i % RC, e = 8 * (i / RC);
+    float qv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (row < nr) {
+      const int r = r0 + row, h = r / n_u, u = r % n_u;
+      const uint4 raw =
+          *reinterpret_cast<const uint4 *>(q + (int64_t)(u_off + u) * ld_q + h * HD + e);
       const bf16 *v = reinterpret_cast<const bf16 *>(&raw);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) qv[c + j] = __bfloat162float(v[j]) * scale_log2;
+      for (int j = 0; j < 8; ++j) qv[j] = __bfloat162float(v[j]) * scale_log2;
     }
-    float mx = -INFINITY, sum = 0.f;
-    for (int t = 0; t < nk; ++t) {
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-      for (int c = 0; c < HD; c += 4) {
-        const float4 k4 = *reinterpret_cast<const float4 *>(&ks[t][c]);
-        a0 = fmaf(qv[c], k4.x, a0);
-        a1 = fmaf(qv[c + 1], k4.y, a1);
-        a2 = fmaf(qv[c + 2], k4.z, a2);
-        a3 = fmaf(qv[c + 3], k4.w, a3);
-      }
-      const float sc = (a0 + a1) + (a2 + a3);
-      s[(int64_t)(t0 + t) * n_rows + r] = sc;
-      if (sc > mx) {
-        sum = sum * exp2f(mx - sc) + 1.f;
-        mx = sc;
+    for (int j = 0; j < 8; ++j) qs[(e + j) * RC + row] = qv[j];
+    float kv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (row < nk) {
+      const uint4 raw = *reinterpret_cast<const uint4 *>(
+          kc + (int64_t)(t_off + t0 + row) * ld_k + g * HD + e);
+      const bf16 *v = reinterpret_cast<const bf16 *>(&raw);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) kv[j] = __bfloat162float(v[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ks[(e + j) * KC + row] = kv[j];
+  }
+  __syncthreads();
+  const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+#pragma unroll 8
+  for (int e = 0; e < HD; ++e) {
+    const float4 a = *reinterpret_cast<const float4 *>(qs + e * RC + 4 * ty);
+    const float4 b = *reinterpret_cast<const float4 *>(ks + e * KC + 4 * tx);
+    const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+  }
+  // scores out (4 consecutive rows per key), then each row's statistics over
+  // the tile's keys: the 16 threads of a row group are 16 consecutive lanes
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int t = 4 * tx + j;
+    if (t < nk && 4 * ty < nr) {
+      float *dst = s + (int64_t)(t0 + t) * n_rows + r0 + 4 * ty;
+      if (4 * ty + 4 <= nr && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+        *reinterpret_cast<float4 *>(dst) = make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
       } else {
-        sum += exp2f(sc - mx);
+        for (int i = 0; i < 4 && 4 * ty + i < nr; ++i) dst[i] = acc[i][j];
       }
     }
-    part[(int64_t)chunk * n_rows + r] = make_float2(mx, sum);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (4 * tx + j < nk) mx = fmaxf(mx, acc[i][j]);
+    for (int o = 8; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (4 * tx + j < nk) sum += exp2f(acc[i][j] - mx);
+    for (int o = 8; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (tx == 0 && 4 * ty + i < nr)
+      part[(int64_t)blockIdx.x * n_rows + r0 + 4 * ty + i] = make_float2(mx, sum);
   }
 }
 
@@ -314,7 +358,16 @@ cudaError_t launch_attention_mass(const void *q, int64_t ld_q, int u_off, int n_
   w += ((size_t)n_chunks * n_rows * 8 + 255) / 256 * 256;
   float2 *ml = reinterpret_cast<float2 *>(w);
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
-  cudaError_t e = launch_pdl(mass_score_kernel, dim3(n_chunks, Hkv), dim3(kRowThreads), 0, s,
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(mass_score_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int tiles_per_group = ((Hq / Hkv) * n_u + RC - 1) / RC;
+  cudaError_t e = launch_pdl(mass_score_kernel, dim3(n_chunks, Hkv * tiles_per_group),
+                             dim3(kTileThreads), kScoreSmem, s,
                              reinterpret_cast<const bf16 *>(q), ld_q, u_off, n_u,
                              reinterpret_cast<const bf16 *>(k_cache), ld_k, t_off, n_ctx, Hq, Hkv,
                              scale_log2, sc, part);
