@@ -357,6 +357,61 @@ lm_head_kernel(const float *__restrict__ x, int B, const T *__restrict__ E,
     if (lane == 0) atomicMax(best + b, mine[b]);
 }
 
+// SMs of the current device (one persistent CTA each for the GEMV).
+static int num_sms_rows() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+// One request, d = 4096, bf16 embedding: each lane holds its 128 entries of
+// the normed hidden state in registers (dims 8 * lane + 256 k) and issues the
+// 16 loads of a vocabulary row before using any of them, so a warp keeps the
+// whole 8 KB row in flight.  Same ranking as lm_head_kernel.
+constexpr int kLmD = 4096;
+__global__ void __launch_bounds__(256, 1)
+lm_head_one_kernel(const float *__restrict__ x, const bf16 *__restrict__ E, int vocab,
+                   unsigned long long *__restrict__ best) {
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int nw = gridDim.x * 8;
+  float xr[kLmD / 32];
+#pragma unroll
+  for (int k = 0; k < kLmD / 256; ++k) {
+    const float4 a = *reinterpret_cast<const float4 *>(x + 256 * k + 8 * lane);
+    const float4 b = *reinterpret_cast<const float4 *>(x + 256 * k + 8 * lane + 4);
+    xr[8 * k] = a.x; xr[8 * k + 1] = a.y; xr[8 * k + 2] = a.z; xr[8 * k + 3] = a.w;
+    xr[8 * k + 4] = b.x; xr[8 * k + 5] = b.y; xr[8 * k + 6] = b.z; xr[8 * k + 7] = b.w;
+  }
+  unsigned long long mine = 0ull;
+  for (int v = gw; v < vocab; v += nw) {
+    const uint4 *row = reinterpret_cast<const uint4 *>(E + (int64_t)v * kLmD) + lane;
+    uint4 raw[kLmD / 256];
+#pragma unroll
+    for (int k = 0; k < kLmD / 256; ++k) raw[k] = __ldg(row + 32 * k);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < kLmD / 256; ++k) {
+      const __nv_bfloat162 *e = reinterpret_cast<const __nv_bfloat162 *>(&raw[k]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __bfloat1622float2(e[j]);
+        acc[j] = fmaf(f.x, xr[8 * k + 2 * j], acc[j]);
+        acc[j] = fmaf(f.y, xr[8 * k + 2 * j + 1], acc[j]);
+      }
+    }
+    const float sum = warp_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
+    const unsigned long long pk = pack_best(sum, v);
+    if (pk > mine) mine = pk;
+  }
+  if (lane == 0) atomicMax(best, mine);
+}
+
 __global__ void lm_unpack_kernel(const unsigned long long *__restrict__ best,
                                  int B, int32_t *__restrict__ token) {
   const int b = threadIdx.x;
@@ -374,6 +429,12 @@ cudaError_t launch_lm_head_argmax(const float *h, int64_t ld_h,
   LastRows lr;
   for (int b = 0; b < B; ++b) lr.r[b] = last_rows_host[b];
   lm_norm_kernel<<<B, 256, 0, s>>>(h, ld_h, lr, d, final_norm, eps, x_scratch, best);
+  if (B == 1 && d == kLmD && dt == CB_BF16) {
+    lm_head_one_kernel<<<num_sms_rows(), 256, 0, s>>>(x_scratch, (const bf16 *)embed, vocab,
+                                                      best);
+    lm_unpack_kernel<<<1, 32, 0, s>>>(best, B, token_out);
+    return launched(3);
+  }
   // up to 8 requests per pass over the vocabulary
   for (int b0 = 0; b0 < B; b0 += 8) {
     const int nb = B - b0 < 8 ? B - b0 : 8;
