@@ -27,8 +27,9 @@
 //
 // When the query tiles alone cannot fill the SMs (the compact layers), the
 // key range of every tile is split into chunks processed by separate CTAs;
-// each writes its un-normalised (O, m, l) and a combine kernel merges them:
-// O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
+// each writes its normalised output O_c / l_c (bf16) with (m_c, l_c), and a
+// combine kernel merges them: O = sum_c w_c (O_c / l_c) / sum_c w_c with
+// w_c = 2^(m_c - M) l_c.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -376,7 +377,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
                const __grid_constant__ CUtensorMap mapK,
                const __grid_constant__ CUtensorMap mapV, const __grid_constant__ Params P,
                const int32_t *__restrict__ q_pos, bf16 *__restrict__ out, int64_t ld_out,
-               float *__restrict__ part_o, float2 *__restrict__ part_ml, int *status) {
+               bf16 *__restrict__ part_o, float2 *__restrict__ part_ml, int *status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
@@ -661,22 +662,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
         float o[32];
         ld32(obase + c, o);
         if (!(valid && ok)) continue;
-        if (!split) {
-          bf16 *dst = out + (int64_t)q_row * ld_out + head * HD + c;
+        // the output row, or this key chunk's normalised partial (bf16, with
+        // its (m, l) beside it for the combine)
+        bf16 *dst = split ? part_o + slot * HD + c : out + (int64_t)q_row * ld_out + head * HD + c;
 #pragma unroll
-          for (int c8 = 0; c8 < 32; c8 += 8) {
-            uint4 pk;
-            __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&pk);
+        for (int c8 = 0; c8 < 32; c8 += 8) {
+          uint4 pk;
+          __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&pk);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              e[i] = __floats2bfloat162_rn(o[c8 + 2 * i] * inv, o[c8 + 2 * i + 1] * inv);
-            *reinterpret_cast<uint4 *>(dst + c8) = pk;
-          }
-        } else {
-          // un-normalised partial of this key chunk
-          float4 *po = reinterpret_cast<float4 *>(part_o + slot * HD + c);
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) po[i / 4] = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+          for (int i = 0; i < 4; ++i)
+            e[i] = __floats2bfloat162_rn(o[c8 + 2 * i] * inv, o[c8 + 2 * i + 1] * inv);
+          *reinterpret_cast<uint4 *>(dst + c8) = pk;
         }
       }
       if (valid && ok && split) part_ml[slot] = make_float2(m, l);
@@ -703,10 +699,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
 // Merges the key-chunk partials of every (query row, q head).  A CTA of
 // eight warps takes 32 rows of a tile, four per warp, and issues the loads
 // of all four rows before using them; each lane owns four of the 128 output
-// dimensions, so every partial row is read as one coalesced 512-byte access.
+// dimensions, so every partial row (bf16) is read as one coalesced 256-byte
+// access.
 constexpr int kCombineRows = 4;            // rows per warp
 __global__ void __launch_bounds__(256)
-attn_combine_kernel(const __grid_constant__ Params P, const float *__restrict__ part_o,
+attn_combine_kernel(const __grid_constant__ Params P, const bf16 *__restrict__ part_o,
                     const float2 *__restrict__ part_ml, bf16 *__restrict__ out, int64_t ld_out) {
   grid_dep_wait();
   grid_dep_launch();
@@ -749,8 +746,10 @@ attn_combine_kernel(const __grid_constant__ Params P, const float *__restrict__ 
       const float2 ml = c0 + lane < count
                             ? part_ml[((int64_t)first + c0 + lane) * 128 + row_base + 8 * r]
                             : make_float2(-INFINITY, 0.f);
-      w[r] = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M[r]);     // empty chunk: no rows
-      l[r] += w[r] * ml.y;
+      // a chunk's weight is its sum l rescaled to the common maximum (its
+      // partial is already divided by l); an empty chunk has none
+      w[r] = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M[r]) * ml.y;
+      l[r] += w[r];
     }
     const int n = min(32, count - c0);
     for (int i = 0; i < n; ++i) {
@@ -758,9 +757,11 @@ attn_combine_kernel(const __grid_constant__ Params P, const float *__restrict__ 
       for (int r = 0; r < kCombineRows; ++r) {
         const float wi = __shfl_sync(0xffffffffu, w[r], i);
         if (wi != 0.f) {
-          const float4 v = reinterpret_cast<const float4 *>(
+          const uint2 raw = reinterpret_cast<const uint2 *>(
               part_o + (((int64_t)first + c0 + i) * 128 + row_base + 8 * r) * HD)[lane];
-          o[r].x += wi * v.x; o[r].y += wi * v.y; o[r].z += wi * v.z; o[r].w += wi * v.w;
+          const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
+          const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
+          o[r].x += wi * a.x; o[r].y += wi * a.y; o[r].z += wi * b.x; o[r].w += wi * b.y;
         }
       }
     }
@@ -852,7 +853,7 @@ static void plan_split(Params &P, const AttnReq *reqs, int n_req, int Hq, int Hk
   }
 }
 
-constexpr size_t kPartBytes = 128 * (HD * sizeof(float) + sizeof(float2));
+constexpr size_t kPartBytes = 128 * (HD * sizeof(bf16) + sizeof(float2));
 
 }  // namespace attn
 
@@ -917,14 +918,14 @@ cudaError_t launch_attention_tc(const void *q, int64_t ld_q, const int32_t *q_po
   const int slots = kCtasPerSm * num_sms();
   const int grid = plan ? (tiles > slots ? tiles : slots) : tiles * P.n_chunks;
   const bool split = plan ? tiles < slots : P.n_chunks > 1;
-  float *part_o = nullptr;
+  bf16 *part_o = nullptr;
   float2 *part_ml = nullptr;
   if (split) {
     const size_t need = (size_t)grid * kPartBytes;
     if (!ws || ws_bytes < need) return cudaErrorInvalidValue;
-    part_o = reinterpret_cast<float *>(ws);
+    part_o = reinterpret_cast<bf16 *>(ws);
     part_ml = reinterpret_cast<float2 *>(reinterpret_cast<char *>(ws) +
-                                         (size_t)grid * 128 * HD * sizeof(float));
+                                         (size_t)grid * 128 * HD * sizeof(bf16));
   }
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, q_rows, (int64_t)Hq * HD, ld_q, P.QT) ||
@@ -944,7 +945,7 @@ cudaError_t launch_attention_tc(const void *q, int64_t ld_q, const int32_t *q_po
   if (e != cudaSuccess) return e;
   if (!split) return launched(1);
   e = launch_pdl(attn_combine_kernel, dim3(tiles * 4), dim3(256), 0, s, P,
-                 (const float *)part_o, (const float2 *)part_ml, reinterpret_cast<bf16 *>(out),
+                 (const bf16 *)part_o, (const float2 *)part_ml, reinterpret_cast<bf16 *>(out),
                  ld_out);
   if (e != cudaSuccess) return e;
   return launched(2);
