@@ -5,11 +5,13 @@
 // Splitting M_tok rows into ceil(M_tok / 256) token tiles of equal width
 // (176 for 524 rows) wastes 1% of the work where 128-row tiles waste 18%.
 //
-// Roles as in the standard kernel: warp 0 TMA producer, warp 1 TMEM owner and
-// MMA issuer, warps 2..5 epilogue; the fp32 accumulator [128 features][BT
+// Roles: warp 0 TMA producer, warp 1 TMEM owner and MMA issuer, warps 2..9
+// epilogue in two groups of four (warps 2..5 and 6..9, each covering the
+// four TMEM lane quarters) that take alternate 32-token chunks of a tile,
+// each with its own transpose buffer; the fp32 accumulator [128 features][BT
 // tokens] is double-buffered in TMEM (columns 0 and 256).  Epilogue thread r
-// owns feature r of the tile, so for every token the 32 lanes of a warp
-// write 32 consecutive features.  Two epilogues pair feature r with r + 64
+// of a group owns feature r of the tile, so for every token the 32 lanes of
+// a warp write 32 consecutive features.  Two epilogues pair feature r with r + 64
 // through a shared-memory exchange: SwiGLU (tile rows 0..63 are W_gate rows,
 // 64..127 the matching W_up rows) and the QKV RoPE (rotate-half pairs
 // (e, e + 64) of a 128-wide head).  Residual outputs may use stream-K.
@@ -23,7 +25,7 @@ using namespace tcx;
 
 constexpr int FM = 128;                      // weight rows per tile
 constexpr int BK = 64;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kTileW = FM * BK * 2;          // 16 KB
 constexpr int kTrStride = 132;               // floats per transposed token row
 constexpr int kTr = 32 * kTrStride * 4;      // 32 tokens x 128 features, fp32
@@ -96,7 +98,12 @@ struct Work {
   }
 };
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Barriers of one epilogue group (128 threads) and of all eight epilogue warps.
+__device__ __forceinline__ void epi_bar(int grp) {
+  if (grp == 0) asm volatile("bar.sync 1, 128;" ::: "memory");
+  else asm volatile("bar.sync 2, 128;" ::: "memory");
+}
+__device__ __forceinline__ void epi_all_bar() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
 
 __device__ __forceinline__ void store_bf16x8(bf16 *dst, const float *v) {
   uint4 pk;
@@ -113,9 +120,8 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
                 int *status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  float *tr = reinterpret_cast<float *>(smem + p.stages * p.stage_bytes);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.stages * p.stage_bytes + kTr);
-  int64_t *s_dst = reinterpret_cast<int64_t *>(smem + p.stages * p.stage_bytes + kTr + 256);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.stages * p.stage_bytes + 2 * kTr);
+  int64_t *s_dst = reinterpret_cast<int64_t *>(smem + p.stages * p.stage_bytes + 2 * kTr + 256);
   int32_t *s_pos = reinterpret_cast<int32_t *>(s_dst + 256);
   uint64_t *full = bars;                 // [stages]
   uint64_t *empty = bars + 8;            // [stages]
@@ -123,6 +129,8 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
   uint64_t *tempty = bars + 18;          // [2]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 20);
   volatile int *fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  // epilogue stop votes [tile parity][epilogue warp] (bytes 192..255 of the barrier area)
+  volatile int *vote = reinterpret_cast<volatile int *>(bars + 24);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_kb = (p.K + BK - 1) / BK;
@@ -137,7 +145,7 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
       // CG = 2: lane 0 of each epilogue warp of both CTAs
-      mbar_init(smem_u32(&tempty[b]), CG == 2 ? 8 : 128);
+      mbar_init(smem_u32(&tempty[b]), CG == 2 ? 16 : 256);
     }
     *fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -275,31 +283,43 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
     }
   } else {
     // ----------------------------------------------------------- epilogue
+    // Every decision to stop is taken by all eight warps together (a vote
+    // behind a barrier), so no group waits at a barrier for a warp that left.
     const int quad = warp & 3;
     const int r = quad * 32 + lane;                 // feature row of the tile
+    const int grp = (threadIdx.x - 64) >> 7;        // epilogue group 0 / 1
+    const int t = (threadIdx.x - 64) & 127;         // 0..127 within the group
+    float *tr = reinterpret_cast<float *>(smem + p.stages * p.stage_bytes) + grp * (kTr / 4);
     int buf = 0;
     uint32_t bphase = 0;
+    int n_tile = 0;
     Work<CG> wk(p, num_kb);
     int tt, ft, kb0, kb1;
-    const int t = threadIdx.x - 64;                  // 0..127 among the epilogue threads
     while (wk.next(tt, ft, kb0, kb1)) {
       const bool whole = kb0 == 0 && kb1 == num_kb;
       if (EPI == EPI_QKV) {
-        // the tile's positions and fused-cache rows, read while the MMAs run;
-        // the previous tile's last barrier ended every read of the table
-        for (int i = t; i < p.BT; i += 128) {
+        // the tile's positions and fused-cache rows, read while the MMAs run,
+        // once every warp is done with the previous tile's table
+        epi_all_bar();
+        for (int i = threadIdx.x - 64; i < p.BT; i += 256) {
           const int tok = tt * p.BT + i;
           s_pos[i] = tok < p.M ? p.pos[tok] : 0;
           s_dst[i] = tok < p.M ? (int64_t)p.dst_row[tok] : 0;
         }
-        epi_bar();     // the table is read across threads before the chunk barriers
       }
-      const bool bad =
-          !mbar_wait_bounded(smem_u32(&tfull[buf]), bphase, kWaitLimitNs, status) || *fail;
-      if (__any_sync(0xffffffffu, bad)) {
-        *fail = 1;
+      const bool bad_w = __any_sync(
+          0xffffffffu,
+          !mbar_wait_bounded(smem_u32(&tfull[buf]), bphase, kWaitLimitNs, status) || *fail);
+      if (lane == 0) vote[(n_tile & 1) * 8 + warp - 2] = bad_w ? 1 : 0;
+      epi_all_bar();               // also publishes the table to both groups
+      bool bad = false;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) bad |= vote[(n_tile & 1) * 8 + w] != 0;
+      if (bad) {
+        if (lane == 0) *fail = 1;
         break;
       }
+      ++n_tile;
       fence_after();
       ft = ft * CG + (int)rank;                      // this CTA's 128 weight rows
       const uint32_t tbase = tmem + buf * 256 + ((uint32_t)(quad * 32) << 16);
@@ -311,7 +331,7 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
         rotate = head < p.Hq + p.Hkv;
       }
 #pragma unroll 1
-      for (int c = 0; c < p.BT; c += 32) {
+      for (int c = 32 * grp; c < p.BT; c += 64) {
         float x[32];
         tmem_ld32(tbase + c, x);
         // Q/K heads: this thread's rotation factors for the chunk, loaded
@@ -331,7 +351,7 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
         // transpose: feature column r of 32 tokens -> rows of the chunk
 #pragma unroll
         for (int i = 0; i < 32; ++i) tr[i * kTrStride + r] = x[i];
-        epi_bar();
+        epi_bar(grp);
         if (EPI == EPI_STORE) {
           // 32 tokens x 16 vectors of 8 bf16 features
 #pragma unroll
@@ -410,7 +430,7 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
             store_bf16x8(dst + 8 * j, y);
           }
         }
-        epi_bar();
+        epi_bar(grp);
       }
       fence_before();
       if (CG == 2) {
@@ -459,7 +479,7 @@ static int max_pairs(int smem) {
 template <int EPI, int CG>
 static cudaError_t run(const CUtensorMap &mx, const CUtensorMap &mw, const CUtensorMap &mw2,
                        Params &p, int *status, cudaStream_t s) {
-  const int fixed = kTr + 256 + kTokTab + 1024;
+  const int fixed = 2 * kTr + 256 + (EPI == EPI_QKV ? kTokTab : 0) + 1024;
   p.stage_bytes = kTileW + (p.BT / CG) * BK * 2;
   p.stages = (kSmemMax - fixed) / p.stage_bytes;
   if (p.stages > 8) p.stages = 8;
