@@ -22,8 +22,8 @@
 // 2^kRescale: then O (after P_{j-1} V_{j-1} has landed) and l are scaled by
 // 2^(m_old - m_new).  Between moves the probabilities stay below
 // 2^kRescale, and O / l does not depend on the reference, so the result is
-// the same softmax.  One exponential in four runs on the FMA pipe
-// (exp2_poly) to relieve the SFU.  All waits are bounded.
+// the same softmax.  Every exponential runs on the SFU (ex2.approx): with
+// two CTAs per SM it is under half busy.  All waits are bounded.
 //
 // When the query tiles alone cannot fill the SMs (the compact layers), the
 // key range of every tile is split into chunks processed by separate CTAs;
@@ -189,23 +189,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// 2^x on the FMA pipe: x = n + f with n = round(x), |f| <= 1/2, 2^f from a
-// cubic fitted by least squares on the relative error at Chebyshev nodes
-// of [-1/2, 1/2] (relative error below 8e-5), and n added to the exponent
-// field.  The rounding uses the 1.5 * 2^23 shift (the float spacing there
-// is 1), so no conversion instruction is needed; the low bits of t then
-// hold n, and t << 23 is n << 23.  Inputs are clamped at -126 (2^x is then
-// far below what the bf16 probabilities resolve).  Valid for x <= 64.
-constexpr float kExpC0 = 0.99992895f, kExpC1 = 0.6932762f, kExpC2 = 0.24260405f,
-                kExpC3 = 0.05508868f;
-__device__ __forceinline__ float exp2_poly(float x) {
-  x = fmaxf(x, -126.f);
-  const float t = x + 12582912.f;
-  const float f = x - (t - 12582912.f);
-  const float p = fmaf(fmaf(fmaf(kExpC3, f, kExpC2), f, kExpC1), f, kExpC0);
-  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
 }
 
 // Writes 16 consecutive 32-bit TMEM columns of this thread's lane.
@@ -632,7 +615,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
         for (int i = 0; i < 32; i += 2) {
           const float a0 = fmaf(x[c + i], sl2, -m), a1 = fmaf(x[c + i + 1], sl2, -m);
           float p0 = fast_exp2(a0);
-          float p1 = (i & 2) ? exp2_poly(a1) : fast_exp2(a1);
+          float p1 = fast_exp2(a1);
           if (n_vis < BN) {
             p0 = c + i < n_vis ? p0 : 0.f;
             p1 = c + i + 1 < n_vis ? p1 : 0.f;
