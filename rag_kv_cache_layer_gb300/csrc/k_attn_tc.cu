@@ -185,6 +185,12 @@ __device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
 // 2^x with the SFU's approximate base-2 exponential (PTX ex2.approx.ftz;
 // documented maximum relative error about 2^-22), far below the bf16
 // rounding of the probabilities it feeds.
+// max(a, b, c) in one instruction (three-input max.f32 of the sm_100 family).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -577,7 +583,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
       for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
       if (n_vis >= BN) {
 #pragma unroll
-        for (int i = 0; i < BN; ++i) mx[i & 3] = fmaxf(mx[i & 3], x[i]);
+        for (int i = 0; i < BN; i += 8) {
+          mx[0] = max3(mx[0], x[i], x[i + 1]);
+          mx[1] = max3(mx[1], x[i + 2], x[i + 3]);
+          mx[2] = max3(mx[2], x[i + 4], x[i + 5]);
+          mx[3] = max3(mx[3], x[i + 6], x[i + 7]);
+        }
       } else {
 #pragma unroll
         for (int i = 0; i < BN; ++i)
