@@ -185,6 +185,26 @@ __device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
 // 2^x with the SFU's approximate base-2 exponential (PTX ex2.approx.ftz;
 // documented maximum relative error about 2^-22), far below the bf16
 // rounding of the probabilities it feeds.
+// Packed fp32 pairs (fma / add on .f32x2 of the sm_100 family): two
+// softmax elements per instruction.
+__device__ __forceinline__ unsigned long long pack2(float a, float b) {
+  return ((unsigned long long)__float_as_uint(b) << 32) | __float_as_uint(a);
+}
+__device__ __forceinline__ float lo2(unsigned long long v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi2(unsigned long long v) {
+  return __uint_as_float((uint32_t)(v >> 32));
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 // max(a, b, c) in one instruction (three-input max.f32 of the sm_100 family).
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
@@ -615,30 +635,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
         l *= corr;
       }
       if (move) m = mloc;
-      float ls[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) ls[i] = 0.f;
-      // P_j for keys c..c+31 -> slot columns c/2 .. c/2+15 (S_j is in registers)
+      // P_j for keys c..c+31 -> slot columns c/2 .. c/2+15 (S_j is in
+      // registers); the scale-and-shift and the sums run on packed pairs
+      const unsigned long long s2 = pack2(sl2, sl2), nm2 = pack2(-m, -m);
+      unsigned long long ls2[2] = {0ull, 0ull};
 #pragma unroll
       for (int c = 0; c < BN; c += 32) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float a0 = fmaf(x[c + i], sl2, -m), a1 = fmaf(x[c + i + 1], sl2, -m);
-          float p0 = fast_exp2(a0);
-          float p1 = fast_exp2(a1);
+          const unsigned long long a = fma2(pack2(x[c + i], x[c + i + 1]), s2, nm2);
+          float p0 = fast_exp2(lo2(a));
+          float p1 = fast_exp2(hi2(a));
           if (n_vis < BN) {
             p0 = c + i < n_vis ? p0 : 0.f;
             p1 = c + i + 1 < n_vis ? p1 : 0.f;
           }
-          ls[(i >> 1) & 3] += p0 + p1;
+          ls2[(i >> 1) & 1] = add2(ls2[(i >> 1) & 1], pack2(p0, p1));
           __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
           pk[i / 2] = *reinterpret_cast<uint32_t *>(&v2);
         }
         st16(sbase + c / 2, pk);
       }
       wait_st();
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      l += (lo2(ls2[0]) + hi2(ls2[0])) + (lo2(ls2[1]) + hi2(ls2[1]));
       fence_before();
       arrive(smem_u32(&p_full[sl]));
     }
