@@ -168,8 +168,8 @@ def setup_replica(rank, device, n_layers=None):
 # compact layer: the CTA-pair swapped GEMM), valid only for the kernel source
 # it was taken on.
 TRAFFIC_CAPTURE = {"source": "rag_kv_cache_layer_gb300/csrc/k_gemm_sab.cu",
-                   "sha256": "fe5bdf145740dcbcdf5e0c7c69e9f4e1c5447944bc66dbc3e712e9cf604a5318",
-                   "bytes_per_launch": 243631616 + 12040448,
+                   "sha256": "4adb90fb0c5d9123ef3d5955da7ddac61ababe5ad5431fcb9df9a65baad80dac",
+                   "bytes_per_launch": 241867776 + 12049408,
                    "profile": "profiles/gemm_swiglu_M524_llama8b.md"}
 
 
