@@ -413,6 +413,21 @@ cb_status cb_linear(const cb_model *m, const void *A, int64_t ld_a,
                     int K, cb_epilogue epi, void *out, int64_t ld_out,
                     cb_stream stream);
 
+/* cb_linear with a device workspace of cb_linear_workspace_size() bytes
+ * (16-byte aligned, owned by the caller, contents need no initialisation).
+ * With it the bf16 swapped-operand forms split the tiles of a partial last
+ * wave along K over the otherwise idle SMs: the later k-segments leave fp32
+ * partials there and the unit of segment 0 adds them in segment order, so
+ * results stay deterministic.  CB_EPI_RESID does not use it (its stream-K
+ * adds into the residual).  Calls that share a workspace must be ordered on
+ * one stream.  ws == NULL is cb_linear.  Errors: as cb_linear, and
+ * CB_ERR_WORKSPACE when ws is too small or misaligned. */
+size_t cb_linear_workspace_size(void);
+cb_status cb_linear_ws(const cb_model *m, const void *A, int64_t ld_a,
+                       const void *W, const void *W2, int64_t ld_w, int M, int N,
+                       int K, cb_epilogue epi, void *out, int64_t ld_out,
+                       void *ws, size_t ws_bytes, cb_stream stream);
+
 /* A run of request tokens: cached (k_pic != NULL) or recomputed at every
  * layer (k_pic == NULL: the user query U, or a document that has no cache
  * yet).  All cached segments of a request come before its uncached ones;

@@ -151,6 +151,9 @@ def _load():
                                 C.POINTER(vp)]),
         "cb_model_destroy": (None, [vp]),
         "cb_linear": (S, [vp, vp, i64, vp, vp, i64, i32, i32, i32, i32, vp, i64, vp]),
+        "cb_linear_workspace_size": (C.c_size_t, []),
+        "cb_linear_ws": (S, [vp, vp, i64, vp, vp, i64, i32, i32, i32, i32, vp, i64, vp,
+                             C.c_size_t, vp]),
         "cb_blend_plan": (S, [vp, C.POINTER(Request), i32, C.POINTER(BlendParams),
                               C.POINTER(Plan)]),
         "cb_blend_prefill": (S, [vp, C.POINTER(Request), i32,
@@ -191,7 +194,8 @@ EXPORTED = [
     "cb_kv_deviation_topk_noalloc",
     "cb_gather_rows", "cb_scatter_kv", "cb_attention_workspace_size",
     "cb_sparse_query_attention",
-    "cb_model_create", "cb_model_destroy", "cb_linear", "cb_blend_plan",
+    "cb_model_create", "cb_model_destroy", "cb_linear", "cb_linear_workspace_size",
+    "cb_linear_ws", "cb_blend_plan",
     "cb_blend_prefill", "cb_blend_plan_host_kv", "cb_blend_prefill_host_kv",
     "cb_full_plan", "cb_full_prefill",
     "cb_layer_workspace_size", "cb_blend_layer",

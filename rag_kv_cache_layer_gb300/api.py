@@ -282,6 +282,17 @@ class BlendModel:
                             W.stride(0), M, N, K, epi, _p(out), out.stride(0),
                             _s(stream)))
 
+    def cb_linear_ws(self, A, W, out, epi=L.CB_EPI_STORE, W2=None, ws=None, stream=None):
+        """cb_linear with the tail-split workspace (allocated here when ws is None)."""
+        M, K = A.shape
+        N = W.shape[0]
+        need = lib.cb_linear_workspace_size()
+        if ws is None:
+            ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        check(lib.cb_linear_ws(self.handle, _p(A), A.stride(0), _p(W), _p(W2),
+                               W.stride(0), M, N, K, epi, _p(out), out.stride(0),
+                               _p(ws), ws.numel() * ws.element_size(), _s(stream)))
+
     def cb_blend_layer(self, layer, h, pos, cache_row, reqs, k_cache, v_cache,
                        ws=None, stream=None):
         n = h.shape[0]

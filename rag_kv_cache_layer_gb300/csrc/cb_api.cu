@@ -462,10 +462,11 @@ extern "C" void cb_model_destroy(cb_model *m) { delete m; }
 // ----------------------------------------------------------------- linear --
 // bf16 projections run on the tcgen05 kernel; the fp32 parity path keeps
 // CUDA-core FMAs (tensor cores would round its operands).
+// split_ws: the swapped GEMM's tail-split workspace (NULL: no split).
 static cb_status run_linear(const cb_model *m, const void *A, int64_t lda, const void *W,
                             const void *W2, int64_t ldw, int M, int N, int K, GemmEpi epi,
                             void *out, int64_t ldo, cudaStream_t s,
-                            const QkvEpi *qkv = nullptr) {
+                            const QkvEpi *qkv = nullptr, void *split_ws = nullptr) {
   if (m->cfg.dtype == CB_BF16) {
     int *st;
     CB_TRY(status_ptr(&st));
@@ -475,7 +476,8 @@ static cb_status run_linear(const cb_model *m, const void *A, int64_t lda, const
                      : path == CB_GEMM_SWAP_AB_PAIR ? 2
                                                     : 0;
     if (form)
-      CB_CUDA(launch_gemm_sab(A, lda, W, W2, ldw, M, N, K, epi, out, ldo, qkv, st, s, form));
+      CB_CUDA(launch_gemm_sab(A, lda, W, W2, ldw, M, N, K, epi, out, ldo, qkv, st, s, form,
+                              split_ws));
     else
       CB_CUDA(launch_gemm_tc(A, lda, W, W2, ldw, M, N, K, epi, out, ldo, qkv, st, s));
   } else {
@@ -485,11 +487,23 @@ static cb_status run_linear(const cb_model *m, const void *A, int64_t lda, const
   return CB_OK;
 }
 
+extern "C" size_t cb_linear_workspace_size(void) { return gemm_split_ws_bytes(); }
+
 extern "C" cb_status cb_linear(const cb_model *m, const void *A, int64_t ld_a,
                                const void *W, const void *W2, int64_t ld_w, int M,
                                int N, int K, cb_epilogue epi, void *out, int64_t ld_out,
                                cb_stream stream) {
+  return cb_linear_ws(m, A, ld_a, W, W2, ld_w, M, N, K, epi, out, ld_out, nullptr, 0, stream);
+}
+
+extern "C" cb_status cb_linear_ws(const cb_model *m, const void *A, int64_t ld_a,
+                                  const void *W, const void *W2, int64_t ld_w, int M,
+                                  int N, int K, cb_epilogue epi, void *out, int64_t ld_out,
+                                  void *ws, size_t ws_bytes, cb_stream stream) {
   if (!m || !A || !W || !out) return fail(CB_ERR_INVALID_ARG, "NULL pointer");
+  if (ws && (ws_bytes < gemm_split_ws_bytes() || !aligned16(ws)))
+    return fail(CB_ERR_WORKSPACE, "linear workspace too small or misaligned (%zu < %zu)", ws_bytes,
+                gemm_split_ws_bytes());
   if (M < 0 || N <= 0 || K <= 0 || K % 16) return fail(CB_ERR_INVALID_ARG, "need M >= 0, N > 0, K %% 16 == 0");
   if (ld_a < K || ld_w < K || ld_out < N) return fail(CB_ERR_INVALID_ARG, "leading dimension too small");
   if (m->cfg.dtype == CB_BF16) {
@@ -509,7 +523,11 @@ extern "C" cb_status cb_linear(const cb_model *m, const void *A, int64_t ld_a,
     default: return fail(CB_ERR_INVALID_ARG, "unknown epilogue");
   }
   if (M == 0) return CB_OK;
-  return run_linear(m, A, ld_a, W, W2, ld_w, M, N, K, e, out, ld_out, stream);
+  if (ws && m->cfg.dtype == CB_BF16)
+    CB_CUDA(cudaMemsetAsync((char *)ws + gemm_split_flags_offset(), 0,
+                            gemm_split_ws_bytes() - gemm_split_flags_offset(), stream));
+  return run_linear(m, A, ld_a, W, W2, ld_w, M, N, K, e, out, ld_out, stream, nullptr,
+                    m->cfg.dtype == CB_BF16 ? ws : nullptr);
 }
 
 // ------------------------------------------------------------------- plan --
@@ -530,10 +548,11 @@ struct LayerScratch {
   float *qkv32;
   void *attn;          // attention partials (split key ranges)
   size_t attn_bytes;
+  void *split;         // the swapped GEMM's tail-split partials and counters (bf16)
 };
 
 struct LayerOffsets {
-  size_t x, q, o, g, qkv32, attn, attn_bytes;
+  size_t x, q, o, g, qkv32, attn, attn_bytes, split, split_bytes;
 };
 
 LayerOffsets carve_layer(Carver &c, const cb_model *m, int64_t n) {
@@ -549,12 +568,21 @@ LayerOffsets carve_layer(Carver &c, const cb_model *m, int64_t n) {
                      ? attention_tc_ws_bound()
                      : 0;
   L.attn = c.take(L.attn_bytes);
+  L.split_bytes = cf.dtype == CB_BF16 ? gemm_split_ws_bytes() : 0;
+  L.split = c.take(L.split_bytes);
   return L;
 }
 
 LayerScratch bind_layer(char *ws, const LayerOffsets &L) {
   return LayerScratch{ws + L.x, ws + L.q, ws + L.o, ws + L.g, (float *)(ws + L.qkv32),
-                      ws + L.attn, L.attn_bytes};
+                      ws + L.attn, L.attn_bytes, L.split_bytes ? ws + L.split : nullptr};
+}
+
+// The tail-split counters start at zero in every call (each GEMM leaves them zero).
+cudaError_t reset_split(const LayerScratch &S, cudaStream_t s) {
+  if (!S.split) return cudaSuccess;
+  return cudaMemsetAsync((char *)S.split + gemm_split_flags_offset(), 0,
+                         gemm_split_ws_bytes() - gemm_split_flags_offset(), s);
 }
 
 struct Plan {
@@ -876,7 +904,7 @@ static cb_status layer_forward(cb_model *m, int l, float *h, int n, const int32_
     // projection, RoPE and the Eq. 7 scatter in one kernel
     const QkvEpi q{pos, cache_row, kc, vc, m->kvw, m->w.rope_table, c.n_q_heads, c.n_kv_heads};
     CB_TRY(run_linear(m, S.x, d, L.w_qkv, nullptr, d, n, m->qkv_rows, d, EPI_QKV, S.q, m->qw,
-                      s, &q));
+                      s, &q, S.split));
   } else {
     CB_TRY(run_linear(m, S.x, d, L.w_qkv, nullptr, d, n, m->qkv_rows, d, EPI_STORE_F32,
                       S.qkv32, m->qkv_rows, s));
@@ -898,7 +926,8 @@ static cb_status layer_forward(cb_model *m, int l, float *h, int n, const int32_
   probe_mark(CB_PROBE_O, false, s);
   CB_CUDA(launch_rmsnorm(h, d, nullptr, n, d, L.norm2, c.norm_eps, S.x, d, dt, s));
   probe_mark(CB_PROBE_SWIGLU, true, s);
-  CB_TRY(run_linear(m, S.x, d, L.w_gate, L.w_up, d, n, F, d, EPI_SWIGLU, S.g, F, s));
+  CB_TRY(run_linear(m, S.x, d, L.w_gate, L.w_up, d, n, F, d, EPI_SWIGLU, S.g, F, s, nullptr,
+                    S.split));
   probe_mark(CB_PROBE_SWIGLU, false, s);
   probe_mark(CB_PROBE_DOWN, true, s);
   CB_TRY(run_linear(m, S.g, F, L.w_down, nullptr, F, n, d, F, EPI_RESID, h, d, s));
@@ -937,8 +966,9 @@ extern "C" cb_status cb_blend_layer(cb_model *m, int layer, float *h, int n_rows
   }
   int *st;
   CB_TRY(status_ptr(&st));
-  return layer_forward(m, layer, h, n_rows, pos, cache_row, ar, k_cache, v_cache,
-                       bind_layer((char *)ws, L), st, stream);
+  const LayerScratch S = bind_layer((char *)ws, L);
+  CB_CUDA(reset_split(S, stream));
+  return layer_forward(m, layer, h, n_rows, pos, cache_row, ar, k_cache, v_cache, S, st, stream);
 }
 
 // ------------------------------------------------------------------ stack --
@@ -1163,6 +1193,7 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
   int32_t *glob_c = (int32_t *)(ws + P.glob_c);
   float *h_c = out->hidden ? out->hidden : (float *)(ws + P.h_c);
   const LayerScratch S = bind_layer(ws, P.lay);
+  CB_CUDA(reset_split(S, stream));
 
   // 1. re-position + stitch of every cached segment, layers [s, L)
   std::vector<cb_stitch_desc> descs;
@@ -1429,6 +1460,7 @@ extern "C" cb_status cb_full_prefill(cb_model *m, const cb_request *reqs, int B,
   int32_t *pos_all = out->rows ? out->rows : (int32_t *)(ws + P.pos_all);
   int32_t *glob_all = (int32_t *)(ws + P.glob_all);
   const LayerScratch S = bind_layer(ws, P.lay);
+  CB_CUDA(reset_split(S, stream));
   const int32_t *toks[CB_MAX_BATCH];
   for (int b = 0; b < B; ++b) toks[b] = reqs[b].tokens;
   CB_CUDA(launch_embed(toks, P.bm, m->w.embed, c.vocab, c.d_model, c.dtype, h, st, stream));

@@ -186,11 +186,18 @@ cudaError_t launch_gemm_tc(const void *A, int64_t lda, const void *W,
 int gemm_auto_form(int M, int K, GemmEpi epi);
 // cta_group 2 runs each MMA on a pair of SMs (a 2-CTA cluster): 256 weight
 // rows per tile, the token operand split between the two CTAs.
+// split_ws (may be NULL, gemm_split_ws_bytes() bytes) lets the non-residual
+// epilogues split the tiles of a partial last wave along K; the 32-bit
+// counters at gemm_split_flags_offset() must be zero before the first launch
+// that uses the workspace, and each launch leaves them zero.  Launches that
+// share one workspace must be ordered on one stream.
 cudaError_t launch_gemm_sab(const void *A, int64_t lda, const void *W,
                             const void *W2, int64_t ldw, int M, int N, int K,
                             GemmEpi epi, void *out, int64_t ldo,
                             const QkvEpi *qkv, int *status, cudaStream_t s,
-                            int cta_group = 1);
+                            int cta_group = 1, void *split_ws = nullptr);
+size_t gemm_split_ws_bytes();
+size_t gemm_split_flags_offset();
 
 // ------------------------------------------------------------ attention --
 struct AttnReq {

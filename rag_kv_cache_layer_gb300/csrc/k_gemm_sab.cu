@@ -15,6 +15,10 @@
 // through a shared-memory exchange: SwiGLU (tile rows 0..63 are W_gate rows,
 // 64..127 the matching W_up rows) and the QKV RoPE (rotate-half pairs
 // (e, e + 64) of a 128-wide head).  Residual outputs may use stream-K.
+// Other outputs may split the tiles of a partial last wave along K: the
+// units that run the later k-segments leave fp32 partials in a workspace
+// and the unit that runs segment 0 adds them, in segment order, before its
+// epilogue.
 #include "cb_internal.h"
 #include "cb_tc.cuh"
 
@@ -31,11 +35,22 @@ constexpr int kTrStride = 132;               // floats per transposed token row
 constexpr int kTr = 32 * kTrStride * 4;      // 32 tokens x 128 features, fp32
 constexpr int kTokTab = 256 * 12;            // Q/K/V epilogue: a tile's positions, cache rows
 constexpr int kSmemMax = 232448;
+constexpr int kPartFloats = 8 * FM * 32;     // one CTA's partial: 8 chunks x 128 features x 32 tokens
+constexpr int kSplitFlagBytes = 4096;       // arrival counters: one per tail tile and CTA (<= SMs)
+// Epilogues that take the tail split.  The residual one uses stream-K; the
+// Q/K/V one is at its register limit and keeps whole tiles.
+template <int EPI>
+constexpr bool can_split() { return EPI == EPI_SWIGLU || EPI == EPI_STORE || EPI == EPI_STORE_F32; }
 
 struct Params {
   int M, N, K;           // tokens, output features, reduction
   int BT, n_tt, n_ft;    // token tile width, token tiles, feature tiles
   int stream_k;
+  // tail split: tiles [0, n_whole) run whole; every later tile runs as
+  // `split` k-segments on as many units (split = 1: no split)
+  int n_whole, split;
+  float *part;           // [tail tile][segment][CG][kPartFloats] partials
+  int *flag;             // [tail tile][CG] arrivals of segments 1.., zero between launches
   int stages, stage_bytes;
   uint32_t idesc;
   // epilogue
@@ -54,14 +69,25 @@ struct Params {
 // (weight tile, k-block) units and each CTA of the group runs that range
 // for its own token tile, so the group reads every weight tile at the same
 // time and HBM serves it once (the other n_tt - 1 reads hit L2).
+// Whole tiles with a tail split: item j * split + g (< n_seg) is k-segment g
+// of tile n_whole + j, and item n_seg + i is whole tile i.  The segments
+// come first, at most one per unit, so those of a tile start together on
+// different units and the fixup of segment 0 overlaps its unit's next tile
+// (the accumulator is double-buffered).  n_whole is a multiple of the unit
+// count, so every unit still ends after the same number of whole tiles.
 // A "unit" is one CTA, or one CTA pair when the MMA spans two SMs (CG = 2);
 // both CTAs of a pair walk the same sequence, ft then counting pair tiles.
 template <int CG>
 struct Work {
   int n_tt, num_kb, my_tt;
   bool sk;
+  int n_whole, split;
+  int seg, tj;           // tail split: k-segment of the current item (-1: whole) and tail tile
+  int64_t n_seg;         // items that are k-segments
   int64_t w, w_end, step;
-  __device__ Work(const Params &p, int num_kb_) : n_tt(p.n_tt), num_kb(num_kb_), sk(p.stream_k != 0) {
+  __device__ Work(const Params &p, int num_kb_)
+      : n_tt(p.n_tt), num_kb(num_kb_), sk(p.stream_k != 0), n_whole(p.n_whole), split(p.split),
+        seg(-1), tj(0), n_seg(0) {
     const int unit = blockIdx.x / CG, n_units = gridDim.x / CG;
     const int n_ft = (p.n_ft + CG - 1) / CG;
     step = n_units;
@@ -75,7 +101,8 @@ struct Work {
     } else {
       my_tt = 0;
       w = unit;
-      w_end = (int64_t)p.n_tt * n_ft;
+      n_seg = split > 1 ? ((int64_t)p.n_tt * n_ft - n_whole) * split : 0;
+      w_end = n_seg + n_whole;
     }
   }
   __device__ bool next(int &tt, int &ft, int &kb0, int &kb1) {
@@ -88,10 +115,19 @@ struct Work {
       w += kb1 - kb0;
       tt = my_tt;
     } else {
-      tt = (int)(w % n_tt);
-      ft = (int)(w / n_tt);
+      int64_t tile = w - n_seg;
       kb0 = 0;
       kb1 = num_kb;
+      seg = -1;
+      if (w < n_seg) {
+        tj = (int)(w / split);
+        seg = (int)(w % split);
+        tile = n_whole + tj;
+        kb0 = num_kb * seg / split;
+        kb1 = num_kb * (seg + 1) / split;
+      }
+      tt = (int)(tile % n_tt);
+      ft = (int)(tile / n_tt);
       w += step;
     }
     return true;
@@ -104,6 +140,29 @@ __device__ __forceinline__ void epi_bar(int grp) {
   else asm volatile("bar.sync 2, 128;" ::: "memory");
 }
 __device__ __forceinline__ void epi_all_bar() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
+
+// Arrival counters of the tail split (global memory, GPU scope).
+__device__ __forceinline__ void signal_add(int *flag) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(flag) : "memory");
+}
+__device__ __forceinline__ int load_acquire(const int *flag) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+  return v;
+}
+// Waits until *flag == want; false (after recording CB_ERR_TIMEOUT) past the limit.
+__device__ __forceinline__ bool flag_wait_bounded(const int *flag, int want, uint64_t limit_ns,
+                                                  int *status) {
+  if (load_acquire(flag) == want) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (load_acquire(flag) == want) return true;
+    if ((it & 15u) == 15u && globaltimer_ns() - t0 > limit_ns) {
+      report(status, CB_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
 
 __device__ __forceinline__ void store_bf16x8(bf16 *dst, const float *v) {
   uint4 pk;
@@ -307,9 +366,17 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
           s_dst[i] = tok < p.M ? (int64_t)p.dst_row[tok] : 0;
         }
       }
-      const bool bad_w = __any_sync(
-          0xffffffffu,
-          !mbar_wait_bounded(smem_u32(&tfull[buf]), bphase, kWaitLimitNs, status) || *fail);
+      // tail split: segment 0 finishes the tile once the other segments'
+      // partials have arrived; the later segments only leave partials
+      const bool helper = can_split<EPI>() && wk.seg > 0;
+      const bool finisher = can_split<EPI>() && wk.seg == 0 && wk.split > 1;
+      int *flag = wk.split > 1 ? p.flag + (int64_t)wk.tj * CG + rank : nullptr;
+      bool bad_l = !mbar_wait_bounded(smem_u32(&tfull[buf]), bphase, kWaitLimitNs, status) || *fail;
+      if (finisher && warp == 2 && lane == 0 && !bad_l) {
+        bad_l = !flag_wait_bounded(flag, wk.split - 1, kWaitLimitNs, status);
+        if (!bad_l) *flag = 0;        // every segment has arrived: ready for the next launch
+      }
+      const bool bad_w = __any_sync(0xffffffffu, bad_l);
       if (lane == 0) vote[(n_tile & 1) * 8 + warp - 2] = bad_w ? 1 : 0;
       epi_all_bar();               // also publishes the table to both groups
       bool bad = false;
@@ -330,10 +397,38 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
         head = ft;
         rotate = head < p.Hq + p.Hkv;
       }
+      // this tile's partial slots: [segment][CG][kPartFloats]
+      float *part = wk.split > 1 ? p.part + ((int64_t)wk.tj * wk.split * CG + rank) * kPartFloats
+                                 : nullptr;
 #pragma unroll 1
       for (int c = 32 * grp; c < p.BT; c += 64) {
         float x[32];
         tmem_ld32(tbase + c, x);
+        // partial layout: [chunk][token quad v][feature] float4s, so the 32
+        // lanes of a warp move 512 contiguous bytes per instruction
+        const int64_t po = (int64_t)(c >> 5) * (FM * 32) + r * 4;
+        if (helper) {
+          float4 *dst = reinterpret_cast<float4 *>(part + (int64_t)wk.seg * CG * kPartFloats + po);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            __stcg(dst + v * FM, make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]));
+          continue;
+        }
+        if (finisher) {
+#pragma unroll 1
+          for (int g = 1; g < wk.split; ++g) {
+            const float4 *src =
+                reinterpret_cast<const float4 *>(part + (int64_t)g * CG * kPartFloats + po);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const float4 a = __ldcg(src + v * FM);
+              x[4 * v] += a.x;
+              x[4 * v + 1] += a.y;
+              x[4 * v + 2] += a.z;
+              x[4 * v + 3] += a.w;
+            }
+          }
+        }
         // Q/K heads: this thread's rotation factors for the chunk, loaded
         // before the transpose so that their latency overlaps it
         float4 rf[EPI == EPI_QKV ? 4 : 1][EPI == EPI_QKV ? 4 : 1];
@@ -432,6 +527,12 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
         }
         epi_bar(grp);
       }
+      if (helper) {
+        // every epilogue thread's partial is written before the arrival
+        __threadfence();
+        epi_all_bar();
+        if (threadIdx.x == 64) signal_add(flag);
+      }
       fence_before();
       if (CG == 2) {
         __syncwarp();
@@ -502,6 +603,8 @@ static cudaError_t run(const CUtensorMap &mx, const CUtensorMap &mw, const CUten
   const int n_ft = (p.n_ft + CG - 1) / CG;
   const int64_t tiles = (int64_t)p.n_tt * n_ft;
   int units;
+  p.n_whole = (int)tiles;
+  p.split = 1;
   if (p.stream_k) {
     // whole groups of n_tt units, at most one group per weight unit
     const int64_t wunits = (int64_t)n_ft * ((p.K + BK - 1) / BK);
@@ -511,6 +614,19 @@ static cudaError_t run(const CUtensorMap &mx, const CUtensorMap &mw, const CUten
     units = (int)(groups * p.n_tt);
   } else {
     units = tiles < max_units ? (int)tiles : max_units;
+    if (p.part && can_split<EPI>()) {
+      // the partial last wave: split its tiles along K over the idle units
+      const int64_t rem = tiles % max_units;
+      const int num_kb = (p.K + BK - 1) / BK;
+      int split = rem ? (int)(max_units / rem) : 1;
+      if (split > num_kb / 8) split = num_kb / 8;     // segments of at least 8 k-blocks
+      if (split > 8) split = 8;
+      if (split >= 2) {
+        p.split = split;
+        p.n_whole = (int)(tiles - rem);
+        units = p.n_whole > 0 ? max_units : (int)(rem * split);
+      }
+    }
   }
   if (CG == 1) {
     cudaError_t e = launch_pdl(gemm_sab_kernel<EPI, 1>, dim3(units), dim3(kThreads), smem, s, mx,
@@ -545,6 +661,9 @@ static cudaError_t run_cg(const CUtensorMap &mx, const CUtensorMap &mw, const CU
 
 }  // namespace sab
 
+size_t gemm_split_flags_offset() { return (size_t)tcx::num_sms() * sab::kPartFloats * sizeof(float); }
+size_t gemm_split_ws_bytes() { return gemm_split_flags_offset() + sab::kSplitFlagBytes; }
+
 // Automatic form, measured at the Llama-3-8B projection shapes for 512 to
 // 4096 token rows: the CTA-pair swapped form is fastest for the SwiGLU,
 // down and Q/K/V projections at every size (524 rows: 92, 45 and 22 us
@@ -562,7 +681,7 @@ int gemm_auto_form(int M, int K, GemmEpi epi) {
 cudaError_t launch_gemm_sab(const void *A, int64_t lda, const void *W, const void *W2,
                             int64_t ldw, int M, int N, int K, GemmEpi epi, void *out,
                             int64_t ldo, const QkvEpi *qkv, int *status, cudaStream_t s,
-                            int cta_group) {
+                            int cta_group, void *split_ws) {
   using namespace sab;
   if (M == 0 || N == 0) return cudaSuccess;
   if (cta_group != 1 && cta_group != 2) return cudaErrorInvalidValue;
@@ -578,6 +697,10 @@ cudaError_t launch_gemm_sab(const void *A, int64_t lda, const void *W, const voi
   p.idesc = idesc_bf16(FM * cg, p.BT);
   p.out = out;
   p.ldo = ldo;
+  if (split_ws) {
+    p.part = reinterpret_cast<float *>(split_ws);
+    p.flag = reinterpret_cast<int *>(reinterpret_cast<char *>(split_ws) + gemm_split_flags_offset());
+  }
   CUtensorMap mx, mw, mw2;
   // each CTA of a pair holds half of the token rows of B
   if (!make_map(&mx, A, M, K, lda, p.BT / cg)) return cudaErrorInvalidValue;

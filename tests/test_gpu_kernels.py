@@ -408,3 +408,69 @@ def test_tensor_core_gemm_llama_shapes(M, gemm_path):
     assert rms_rel(host(g), ref) < 5e-3
     torch.cuda.synchronize()
     assert R.device_status() == 0
+
+
+@pytest.fixture(scope="module")
+def llama_proj():
+    rng = np.random.default_rng(7)
+    shape = W.ModelShape("g", 1, 4096, 32, 8, 128, 14336, 256, dtype="bf16")
+    w = {"embed": np.zeros((256, 4096), np.float32),
+         "final_norm": np.ones(4096, np.float32),
+         "layers": [{
+             "w_qkv": _vals(rng, (6144, 4096), torch.bfloat16, 0.02),
+             "w_o": _vals(rng, (4096, 4096), torch.bfloat16, 0.02),
+             "w_gate": _vals(rng, (14336, 4096), torch.bfloat16, 0.02),
+             "w_up": _vals(rng, (14336, 4096), torch.bfloat16, 0.02),
+             "w_down": _vals(rng, (4096, 14336), torch.bfloat16, 0.02),
+             "norm1": np.ones(4096, np.float32), "norm2": np.ones(4096, np.float32)}]}
+    return w, R.BlendModel.from_host(shape, w, 1024)
+
+
+@pytest.mark.parametrize("gemm_path", [L.CB_GEMM_SWAP_AB, L.CB_GEMM_SWAP_AB_PAIR], indirect=True)
+@pytest.mark.parametrize("M", [524, 128, 3136, 1])
+def test_gemm_tail_split(M, gemm_path, llama_proj):
+    """The swapped GEMM with the tail-split workspace.  At these shapes the
+    tiles of the partial last wave run as 2 to 9 k-segments on otherwise idle
+    SMs (SwiGLU over N = 14336 at every M; the N = 6144 projection at 128,
+    3136 and 1 rows); segment 0 adds the others' fp32 partials in segment
+    order.  Checked: the oracle's product, bit-identical repeats, and the
+    unsplit launch up to fp32 summation order."""
+    w, model = llama_proj
+    lw = w["layers"][0]
+    dw = model.w["layers"][0]
+    rng = np.random.default_rng(100 + M)
+    A = _vals(rng, (M, 4096), torch.bfloat16)
+    A64 = A.astype(np.float64)
+    Ad = dev(A, torch.bfloat16)
+    ws = torch.empty(L.lib.cb_linear_workspace_size(), dtype=torch.uint8, device="cuda")
+    ws.fill_(0xAB)            # the call needs no initialised workspace
+    outs = []
+    for _ in range(2):
+        out = torch.empty(M, 6144, dtype=torch.bfloat16, device="cuda")
+        model.cb_linear_ws(Ad, dw["w_qkv"], out, L.CB_EPI_STORE, ws=ws)
+        g = torch.empty(M, 14336, dtype=torch.bfloat16, device="cuda")
+        model.cb_linear_ws(Ad, dw["w_gate"], g, L.CB_EPI_SWIGLU, W2=dw["w_up"], ws=ws)
+        outs.append((out, g))
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    ref = A64 @ lw["w_qkv"].astype(np.float64).T
+    assert rms_rel(host(outs[0][0]), ref) < 5e-3
+    ref = O.silu(A64 @ lw["w_gate"].astype(np.float64).T) * (A64 @ lw["w_up"].astype(np.float64).T)
+    assert rms_rel(host(outs[0][1]), ref) < 5e-3
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    # the unsplit launch: the same sums in another fp32 order
+    g1 = torch.empty(M, 14336, dtype=torch.bfloat16, device="cuda")
+    model.cb_linear(Ad, dw["w_gate"], g1, L.CB_EPI_SWIGLU, W2=dw["w_up"])
+    torch.cuda.synchronize()
+    assert rms_rel(host(outs[0][1]), host(g1)) < 2e-3
+
+
+def test_linear_workspace_is_validated(llama_proj):
+    w, model = llama_proj
+    dw = model.w["layers"][0]
+    A = torch.zeros(8, 4096, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(8, 6144, dtype=torch.bfloat16, device="cuda")
+    small = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(L.CBError) as e:
+        model.cb_linear_ws(A, dw["w_qkv"], out, L.CB_EPI_STORE, ws=small)
+    assert e.value.status == L.CB_ERR_WORKSPACE
