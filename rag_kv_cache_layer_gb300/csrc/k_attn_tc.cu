@@ -277,8 +277,15 @@ __device__ __forceinline__ TileId decode_tile(const Params &P, int tile) {
 // sum_t ceil(nb_t / B) <= slots (nb_t: key blocks up to the tile's last query
 // position); tile t is cut into ceil(nb_t / B) near-equal consecutive
 // ranges.  With at least as many tiles as slots nothing is split.  One CTA.
+// Entry u of the table is {tile, first block, end block, partial slot}; the
+// slots of a tile's units are consecutive (the combine reads them there).
+// Split plans of at most kPlanSort units are stored longest unit first: a
+// launch places blocks 0 .. SMs-1 one per SM before the second CTA of each
+// SM, and that second wave starts a few microseconds later, so it gets the
+// shorter units.
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanCache = 8192;           // tiles whose block counts stay in smem
+constexpr int kPlanSort = 512;
 static_assert(kPlanThreads == 1024, "the block reductions assume 32 warps");
 
 __device__ int block_sum(int v, int *red) {
@@ -305,6 +312,8 @@ attn_plan_kernel(const __grid_constant__ Params P, const int32_t *__restrict__ q
                  int *__restrict__ plan) {
   __shared__ int red[kPlanThreads / 32];
   __shared__ int s_nb[kPlanCache];
+  __shared__ int4 s_units[kPlanSort];
+  __shared__ int s_len[kPlanSort];
   grid_dep_wait();      // q_pos comes from earlier kernels
   grid_dep_launch();
   const int tiles = P.tile_off[P.n_req];
@@ -339,6 +348,10 @@ attn_plan_kernel(const __grid_constant__ Params P, const int32_t *__restrict__ q
     B = lo;
   }
   int4 *units = reinterpret_cast<int4 *>(reinterpret_cast<char *>(plan) + plan_units_off(tiles));
+  int n_cnt = 0;
+  for (int t = threadIdx.x; t < tiles; t += kPlanThreads) n_cnt += max(1, (nb_at(t) + B - 1) / B);
+  const int n_units = block_sum(n_cnt, red);
+  const bool sorted = tiles < slots && n_units <= kPlanSort;
   int base = 0;
   for (int t0 = 0; t0 < tiles; t0 += kPlanThreads) {
     const int t = t0 + threadIdx.x;
@@ -367,11 +380,30 @@ attn_plan_kernel(const __grid_constant__ Params P, const int32_t *__restrict__ q
     if (t < tiles) {
       plan[4 + 2 * t] = first;
       plan[5 + 2 * t] = cnt;
-      for (int u = 0; u < cnt; ++u)
-        units[first + u] = make_int4(t, nb * u / cnt, nb * (u + 1) / cnt, 0);
+      for (int u = 0; u < cnt; ++u) {
+        const int4 e = make_int4(t, nb * u / cnt, nb * (u + 1) / cnt, first + u);
+        if (sorted) {
+          s_units[first + u] = e;
+          s_len[first + u] = e.z - e.y;
+        } else {
+          units[first + u] = e;
+        }
+      }
     }
     base += red[kPlanThreads / 32 - 1];
     __syncthreads();
+  }
+  if (sorted) {
+    // stable order by length, longest first: the rank of unit u
+    for (int u = threadIdx.x; u < n_units; u += kPlanThreads) {
+      const int len = s_len[u];
+      int pos = 0;
+      for (int v = 0; v < n_units; ++v) {
+        const int lv = s_len[v];
+        pos += (lv > len) || (lv == len && v < u);
+      }
+      units[pos] = s_units[u];
+    }
   }
   if (threadIdx.x == 0) {
     plan[0] = base;
@@ -400,7 +432,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   uint64_t *pv_done = bar + 13;    // [2] O += P_j V_j has landed
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 15);
   volatile int *fail = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  __shared__ int s_unit[6];        // b, g, tile, first block, end block, split (-1: none)
+  __shared__ int s_unit[7];        // b, g, tile, first block, end block, split (-1: none), slot
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   grid_dep_wait();      // q, the cache and q_pos come from earlier kernels
@@ -408,6 +440,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   if (threadIdx.x == 0) {
     // this CTA's unit: a tile and a range of its key blocks
     int tile, jb, jcap, split;
+    int pslot = blockIdx.x;        // partial slot of a split tile's unit
     if (P.plan) {
       if ((int)blockIdx.x >= P.plan[0]) {
         tile = -1;
@@ -418,6 +451,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
         tile = u.x;
         jb = u.y;
         jcap = u.z;
+        pslot = u.w;
         split = P.plan[5 + 2 * tile] > 1;
       }
     } else {
@@ -427,6 +461,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
       split = P.n_chunks > 1;
     }
     s_unit[5] = tile < 0 ? -1 : split;
+    s_unit[6] = pslot;
     if (tile >= 0) {
       const TileId id = decode_tile(P, tile);
       const AttnReq &R = P.r[id.b];
@@ -456,6 +491,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   if (s_unit[5] < 0) return;                      // no unit for this CTA
   const bool split = s_unit[5] != 0;              // partial of a split tile
   const int b = s_unit[0], g = s_unit[1], t = s_unit[2], jb = s_unit[3], je = s_unit[4];
+  const int64_t pslot = s_unit[6];
   const int nb = je - jb;                         // key blocks of this unit
   const AttnReq &R = P.r[b];
   const int row0 = R.q_begin + t * P.QT;          // first q row of the tile
@@ -463,7 +499,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   if (nb == 0) {
     // a key chunk past the tile's last query: an empty partial, nothing else
     if (split && threadIdx.x < 128 && (int)threadIdx.x % P.QT < n_valid)
-      part_ml[(int64_t)blockIdx.x * 128 + threadIdx.x] = make_float2(-INFINITY, 0.f);
+      part_ml[pslot * 128 + threadIdx.x] = make_float2(-INFINITY, 0.f);
     return;
   }
   if (warp == 1) {
@@ -670,7 +706,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
       // O chunks straight from TMEM to the output (warp-wide loads)
       const int q_row = row0 + qi, head = g * P.G + h;
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const int64_t slot = (int64_t)blockIdx.x * 128 + row;
+      const int64_t slot = pslot * 128 + row;
 #pragma unroll 1
       for (int c = 0; c < HD; c += 32) {
         float o[32];
