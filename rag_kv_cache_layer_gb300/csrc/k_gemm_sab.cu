@@ -479,7 +479,9 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
             }
           }
         } else if (EPI == EPI_SWIGLU) {
-          // tile rows 0..63 gate, 64..127 up: 32 tokens x 8 vectors of 8
+          // tile rows 0..63 gate, 64..127 up: 32 tokens x 8 vectors of 8.  The
+          // fast divide (2 ulp; 0 once the denominator passes 2^126, where SiLU
+          // is 0 to fp32 precision) is well inside the bf16 output's rounding.
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             const int v = t + 128 * q, i = v >> 3, j = v & 7;
@@ -489,7 +491,7 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
               const float *u = g + 64;
               float y[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) y[e] = g[e] / (1.f + __expf(-g[e])) * u[e];
+              for (int e = 0; e < 8; ++e) y[e] = __fdividef(g[e], 1.f + __expf(-g[e])) * u[e];
               store_bf16x8(reinterpret_cast<bf16 *>(p.out) + (int64_t)tok * p.ldo + f, y);
             }
           }

@@ -373,7 +373,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
           if (row_ok && n0 + c < N) {
             float y[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) y[i] = g[i] / (1.f + __expf(-g[i])) * v[i];
+            for (int i = 0; i < 32; ++i) y[i] = __fdividef(g[i], 1.f + __expf(-g[i])) * v[i];
             store_bf16_chunk(o + c, y, N - (n0 + c));
           }
         }
