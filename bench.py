@@ -424,21 +424,33 @@ def run_ours(args):
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n_layers = wl.model.n_layers
+    # the user's own stream: the library records a repeated call into a CUDA
+    # graph on its second use and replays it after that (the legacy default
+    # stream cannot be recorded)
+    es = torch.cuda.Stream()
+    with torch.cuda.stream(es):
+        for _ in range(2):
+            step()
+    torch.cuda.synchronize()
 
     def e2e_loop():
-        e0.record(st)
-        for _ in range(args.steps):
-            tok_dev.copy_(tok_host, non_blocking=True)
-            step()
-            sel_host.copy_(outs["selected"][: int(plan.K_total)], non_blocking=True)
-            tok_out.copy_(outs["first_token"], non_blocking=True)
-        e1.record(st)
+        with torch.cuda.stream(es):
+            e0.record(es)
+            for _ in range(args.steps):
+                tok_dev.copy_(tok_host, non_blocking=True)
+                step()
+                sel_host.copy_(outs["selected"][: int(plan.K_total)], non_blocking=True)
+                tok_out.copy_(outs["first_token"], non_blocking=True)
+            e1.record(es)
         torch.cuda.synchronize()
-    # the dominant kernel's launches are bracketed by events on their own
-    # stream inside this timed region
-    n_dom, ms_dom = probe_steps(L, L.CB_PROBE_SWIGLU, n_layers * args.steps, e2e_loop)
+    # end to end as a user calls it (no probe events in the stream)
+    e2e_loop()
     e2e_ms, e2e_tokens = combine_ranks(e0.elapsed_time(e1), B * T * args.steps, device)
     e2e_value = e2e_tokens / (e2e_ms / 1e3)
+    # the same loop again with the dominant kernel's launches bracketed by
+    # events on their own stream (the events cut the overlap of neighbouring
+    # launches, so this loop is timed for the kernels only)
+    n_dom, ms_dom = probe_steps(L, L.CB_PROBE_SWIGLU, n_layers * args.steps, e2e_loop)
     if R.device_status() != 0:
         raise RuntimeError("device status set during the timed region")
 
@@ -489,7 +501,8 @@ def run_ours(args):
                 "ttft_ms_median": statistics.median(per),
                 "ttft_ms_p95": float(np.percentile(per, 95)),
                 "execution": "step captured once in a CUDA graph and replayed; "
-                             "e2e calls cb_blend_prefill directly every step",
+                             "e2e calls cb_blend_prefill every step on its own stream "
+                             "(the library replays its recording of the repeated call)",
                 "host_enqueue_ms_per_call": statistics.median(host_ms),
                 "l2": "inputs larger than L2 (14.5 GB of weights and 0.8 GB of "
                       "chunk caches read per step)"},
@@ -499,8 +512,8 @@ def run_ours(args):
                          "unit": "TFLOP/s", "frac": achieved / peak,
                          "traffic": captured_traffic(),
                          "kernel": (f"gate/up SwiGLU projection (N=2x{s_.d_ffn}, "
-                                    f"K={s_.d_model}), {n_dom} launches inside the e2e "
-                                    f"timed region: 1 per step at M={rows[0]}, "
+                                    f"K={s_.d_model}), {n_dom} launches in a timed repeat "
+                                    f"of the e2e loop: 1 per step at M={rows[0]}, "
                                     f"{n_layers - 1} at M={rows[-1]}; "
                                     f"{kms * 1e3:.1f} us/launch on average"),
                          "traffic_note": "ncu dram bytes of one M=524 launch",

@@ -557,6 +557,13 @@ cb_status cb_blend_plan(const cb_model *m, const cb_request *reqs, int B,
  *   5. final norm + LM head + argmax of each request's last row.
  * Every step runs in this library's kernels on `stream`; nothing is
  * synchronised.  ws: device workspace of >= cb_plan.workspace_bytes.
+ * Recorded calls: on a stream other than the legacy default stream (and one
+ * the caller is not capturing), the second call with the same host
+ * arguments (every field above, host arrays by content, device buffers by
+ * address) records its launches into a CUDA graph held by the model, and
+ * later such calls replay it; the device data behind the pointers is read
+ * when the replay runs.  The model keeps the 4 most recently used
+ * recordings; cb_model_destroy releases them.
  * Errors: CB_ERR_INVALID_ARG (B > CB_MAX_BATCH, a request whose cached
  *   segments do not all precede its uncached ones, a request that ends in
  *   a cached segment, positions >= max_positions), CB_ERR_WORKSPACE. */

@@ -392,6 +392,14 @@ extern "C" cb_status cb_sparse_query_attention(const void *q, int64_t ld_q,
 }
 
 // ------------------------------------------------------------------ model --
+// A recorded blended call: the key is its host arguments, serialised.
+struct CallGraph {
+  std::vector<uint8_t> key;
+  cudaGraphExec_t exec = nullptr;
+  unsigned long long launches = 0;   // kernels the call launches
+  unsigned long long used = 0;       // last use, for eviction
+};
+
 struct cb_model {
   cb_model_config cfg;
   cb_weights w;
@@ -402,9 +410,16 @@ struct cb_model {
   // stream): fork, per staging buffer "copied" and "consumed"
   cudaEvent_t ev_fork = nullptr, ev_copied[2] = {nullptr, nullptr},
               ev_free[2] = {nullptr, nullptr};
+  // recorded blended calls (the most recently used few)
+  std::mutex graph_mu;
+  std::vector<CallGraph> graphs;
+  std::vector<std::vector<uint8_t>> graph_seen;   // keys called once, not yet recorded
+  unsigned long long graph_clock = 0;
   ~cb_model() {
     for (cudaEvent_t e : {ev_fork, ev_copied[0], ev_copied[1], ev_free[0], ev_free[1]})
       if (e) cudaEventDestroy(e);
+    for (CallGraph &g : graphs)
+      if (g.exec) cudaGraphExecDestroy(g.exec);
   }
 };
 
@@ -1408,10 +1423,150 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
   return CB_OK;
 }
 
+// ----------------------------------------------------------- call graphs --
+// The kernels of a blended call and every argument they receive follow from
+// its host arguments alone: device data is read through pointers, and the
+// call neither synchronises nor reads anything back.  The first call with a
+// given argument set therefore records its launches into a CUDA graph, and
+// later calls with the same set replay it, which removes the host's launch
+// cost and most of the gaps between the launches.  A set is recorded on its
+// second call (the first runs directly and also does the one-time host
+// set-up of the kernels).  The call runs its launches directly on the legacy
+// default stream (which cannot be captured), on a stream that the caller is
+// capturing, and while the launch probe is on.
+namespace {
+constexpr size_t kCallGraphs = 4;
+
+struct KeyWriter {
+  std::vector<uint8_t> v;
+  template <class T>
+  void put(const T &x) {
+    const uint8_t *b = reinterpret_cast<const uint8_t *>(&x);
+    v.insert(v.end(), b, b + sizeof(T));
+  }
+};
+
+// Every host argument of cb_blend_prefill, field by field (no padding bytes).
+std::vector<uint8_t> call_key(const cb_model *m, const cb_request *reqs, int B,
+                              const cb_blend_params *p, const cb_blend_out *out, void *ws,
+                              size_t ws_bytes, cudaStream_t stream) {
+  KeyWriter k;
+  int dev = -1;
+  cudaGetDevice(&dev);
+  k.put(dev);
+  k.put(m);
+  k.put(g_gemm_path.load(std::memory_order_relaxed));
+  k.put(B);
+  int n_cached = 0;
+  for (int b = 0; b < B; ++b) {
+    k.put(reqs[b].tokens);
+    k.put(reqs[b].n_segments);
+    for (int i = 0; i < reqs[b].n_segments; ++i) {
+      const cb_segment &g = reqs[b].segments[i];
+      k.put(g.len);
+      k.put(g.k_pic);
+      k.put(g.v_pic);
+      k.put(g.pic_layer_stride);
+      k.put(g.pic_pos0);
+      n_cached += g.k_pic != nullptr;
+    }
+  }
+  k.put(p->ratio_bp);
+  k.put(p->policy);
+  k.put(p->sel_layer);
+  k.put(p->n_schedule);
+  for (int i = 0; i < p->n_schedule; ++i) {
+    k.put(p->schedule[i].layer);
+    k.put(p->schedule[i].keep);
+  }
+  k.put(p->span_len);
+  k.put(p->span_offset);
+  k.put(p->span_order != nullptr);
+  if (p->span_order)
+    for (int i = 0; i < n_cached; ++i) k.put(p->span_order[i]);
+  k.put(p->forced_selected);
+  k.put(p->anchor_rule);
+  k.put(p->anchor_bp);
+  k.put(p->n_crit);
+  for (int i = 0; i < p->n_crit && p->crit_layers; ++i) k.put(p->crit_layers[i]);
+  k.put(out->k_cache);
+  k.put(out->v_cache);
+  k.put(out->cache_layer_stride);
+  k.put(out->deviation);
+  k.put(out->selected);
+  k.put(out->hidden);
+  k.put(out->rows);
+  k.put(out->first_token);
+  k.put(ws);
+  k.put(ws_bytes);
+  k.put(stream);
+  return std::move(k.v);
+}
+}  // namespace
+
 extern "C" cb_status cb_blend_prefill(cb_model *m, const cb_request *reqs, int B,
                                       const cb_blend_params *p, const cb_blend_out *out,
                                       void *ws, size_t ws_bytes, cb_stream stream) {
-  return blend_impl(m, reqs, B, p, out, ws, ws_bytes, stream, false, nullptr);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  const bool direct = !m || !reqs || B <= 0 || B > CB_MAX_BATCH || !p || !out ||
+                      stream == nullptr || stream == cudaStreamLegacy ||
+                      stream == cudaStreamPerThread ||
+                      g_probe_kind.load(std::memory_order_relaxed) != 0 ||
+                      cudaStreamIsCapturing(stream, &cap) != cudaSuccess ||
+                      cap != cudaStreamCaptureStatusNone;
+  if (direct) return blend_impl(m, reqs, B, p, out, ws, ws_bytes, stream, false, nullptr);
+  for (int b = 0; b < B; ++b)
+    if (!reqs[b].segments || reqs[b].n_segments <= 0)
+      return blend_impl(m, reqs, B, p, out, ws, ws_bytes, stream, false, nullptr);
+  std::vector<uint8_t> key = call_key(m, reqs, B, p, out, ws, ws_bytes, stream);
+  std::lock_guard<std::mutex> lk(m->graph_mu);
+  for (CallGraph &g : m->graphs)
+    if (g.key == key) {
+      g.used = ++m->graph_clock;
+      CB_CUDA(cudaGraphLaunch(g.exec, stream));
+      g_launches.fetch_add(g.launches);
+      return CB_OK;
+    }
+  auto seen = std::find(m->graph_seen.begin(), m->graph_seen.end(), key);
+  if (seen == m->graph_seen.end()) {
+    const cb_status rc = blend_impl(m, reqs, B, p, out, ws, ws_bytes, stream, false, nullptr);
+    if (rc == CB_OK) {
+      if (m->graph_seen.size() >= 2 * kCallGraphs) m->graph_seen.erase(m->graph_seen.begin());
+      m->graph_seen.push_back(std::move(key));
+    }
+    return rc;
+  }
+  m->graph_seen.erase(seen);
+  // record the call (nothing runs while the stream captures), then run it
+  const unsigned long long n0 = g_launches.load();
+  CB_CUDA(cudaStreamBeginCapture(stream, cudaStreamCaptureModeThreadLocal));
+  const cb_status rc = blend_impl(m, reqs, B, p, out, ws, ws_bytes, stream, false, nullptr);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ce = cudaStreamEndCapture(stream, &graph);
+  if (rc != CB_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+  }
+  if (ce != cudaSuccess) return fail(CB_ERR_CUDA, "recording the call: %s", cudaGetErrorString(ce));
+  cudaGraphExec_t exec = nullptr;
+  const cudaError_t ie = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (ie != cudaSuccess) return fail(CB_ERR_CUDA, "instantiating the call: %s", cudaGetErrorString(ie));
+  CallGraph g;
+  g.key = std::move(key);
+  g.exec = exec;
+  g.launches = g_launches.load() - n0;
+  g.used = ++m->graph_clock;
+  if (m->graphs.size() >= kCallGraphs) {
+    auto lru = std::min_element(m->graphs.begin(), m->graphs.end(),
+                                [](const CallGraph &a, const CallGraph &b) { return a.used < b.used; });
+    cudaGraphExecDestroy(lru->exec);
+    *lru = std::move(g);
+  } else {
+    m->graphs.push_back(std::move(g));
+  }
+  CB_CUDA(cudaGraphLaunch(exec, stream));
+  return CB_OK;
 }
 
 extern "C" cb_status cb_blend_plan_host_kv(const cb_model *m, const cb_request *reqs, int B,
