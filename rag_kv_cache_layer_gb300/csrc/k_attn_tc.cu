@@ -874,7 +874,11 @@ static int num_sms() {
 
 // Tiles of a call and the key-range split: tiles that alone fill fewer than
 // all SMs get their key blocks split into chunks so that about two waves of
-// CTAs run; chunks past a tile's last query position exit at once.
+// CTAs run; chunks past a tile's last query position exit at once.  A chunk
+// holds at least kMinChunkBlocks blocks: a CTA's fixed cost (set-up, first
+// loads, writing O) is worth about six blocks of its loop, and a split also
+// needs the combine, so shorter ranges run unsplit.
+constexpr int kMinChunkBlocks = 8;
 static void plan_split(Params &P, const AttnReq *reqs, int n_req, int Hq, int Hkv) {
   P.n_req = n_req;
   P.plan = nullptr;
@@ -895,10 +899,10 @@ static void plan_split(Params &P, const AttnReq *reqs, int n_req, int Hq, int Hk
   P.chunk_blocks = max_nb > 0 ? max_nb : 1;
   const int sms = num_sms();
   const int slots = kCtasPerSm * sms;            // CTAs resident at once
-  if (tiles > 0 && tiles < slots && max_nb > 1) {
+  if (tiles > 0 && tiles < slots && max_nb > kMinChunkBlocks) {
     int want = (2 * slots + tiles - 1) / tiles;
     if (want > max_nb) want = max_nb;
-    P.chunk_blocks = (max_nb + want - 1) / want;
+    P.chunk_blocks = max((max_nb + want - 1) / want, kMinChunkBlocks);
     P.n_chunks = (max_nb + P.chunk_blocks - 1) / P.chunk_blocks;
   }
 }

@@ -37,10 +37,14 @@ constexpr int kTokTab = 256 * 12;            // Q/K/V epilogue: a tile's positio
 constexpr int kSmemMax = 232448;
 constexpr int kPartFloats = 8 * FM * 32;     // one CTA's partial: 8 chunks x 128 features x 32 tokens
 constexpr int kSplitFlagBytes = 4096;       // arrival counters: one per tail tile and CTA (<= SMs)
-// Epilogues that take the tail split.  The residual one uses stream-K; the
-// Q/K/V one is at its register limit and keeps whole tiles.
+// Epilogues that take the tail split (the residual one uses stream-K), and
+// the kernel compiled with it.  The Q/K/V epilogue is at its register limit
+// (168 for 320 threads): it has a second instantiation with the split, used
+// only by launches that do split, so that the others keep their registers.
 template <int EPI>
-constexpr bool can_split() { return EPI == EPI_SWIGLU || EPI == EPI_STORE || EPI == EPI_STORE_F32; }
+constexpr bool can_split() { return EPI != EPI_RESID; }
+template <int EPI>
+constexpr bool split_by_default() { return can_split<EPI>() && EPI != EPI_QKV; }
 
 struct Params {
   int M, N, K;           // tokens, output features, reduction
@@ -172,7 +176,7 @@ __device__ __forceinline__ void store_bf16x8(bf16 *dst, const float *v) {
   *reinterpret_cast<uint4 *>(dst) = pk;
 }
 
-template <int EPI, int CG>
+template <int EPI, int CG, bool TS>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW,
                 const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ Params p,
@@ -368,8 +372,8 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
       }
       // tail split: segment 0 finishes the tile once the other segments'
       // partials have arrived; the later segments only leave partials
-      const bool helper = can_split<EPI>() && wk.seg > 0;
-      const bool finisher = can_split<EPI>() && wk.seg == 0 && wk.split > 1;
+      const bool helper = TS && wk.seg > 0;
+      const bool finisher = TS && wk.seg == 0 && wk.split > 1;
       int *flag = wk.split > 1 ? p.flag + (int64_t)wk.tj * CG + rank : nullptr;
       bool bad_l = !mbar_wait_bounded(smem_u32(&tfull[buf]), bphase, kWaitLimitNs, status) || *fail;
       if (finisher && warp == 2 && lane == 0 && !bad_l) {
@@ -573,10 +577,54 @@ static int max_pairs(int smem) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_sab_kernel<EPI, 2>, &cfg) != cudaSuccess || n <= 0)
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_sab_kernel<EPI, 2, split_by_default<EPI>()>, &cfg) !=
+          cudaSuccess ||
+      n <= 0)
     n = num_sms() / 2;
   cached = n;
   return n;
+}
+
+// Function attributes of one instantiation, set once.
+template <int EPI, int CG, bool TS>
+static cudaError_t prepare() {
+  static bool done = false;
+  if (done) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(gemm_sab_kernel<EPI, CG, TS>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+  if (e != cudaSuccess) return e;
+  if (CG == 2) {
+    e = cudaFuncSetAttribute(gemm_sab_kernel<EPI, CG, TS>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    if (e != cudaSuccess) return e;
+  }
+  done = true;
+  return cudaSuccess;
+}
+
+template <int EPI, int CG, bool TS>
+static cudaError_t launch(int units, int smem, const CUtensorMap &mx, const CUtensorMap &mw,
+                          const CUtensorMap &mw2, const Params &p, int *status, cudaStream_t s) {
+  cudaError_t e = prepare<EPI, CG, TS>();
+  if (e != cudaSuccess) return e;
+  if (CG == 1)
+    return launch_pdl(gemm_sab_kernel<EPI, 1, TS>, dim3(units), dim3(kThreads), smem, s, mx, mw,
+                      mw2, p, status);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * units, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemm_sab_kernel<EPI, 2, TS>, mx, mw, mw2, p, status);
 }
 
 template <int EPI, int CG>
@@ -588,18 +636,8 @@ static cudaError_t run(const CUtensorMap &mx, const CUtensorMap &mw, const CUten
   if (p.stages > 8) p.stages = 8;
   if (p.stages < 2) return cudaErrorInvalidValue;
   const int smem = p.stages * p.stage_bytes + fixed;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_sab_kernel<EPI, CG>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-    if (e != cudaSuccess) return e;
-    if (CG == 2) {
-      e = cudaFuncSetAttribute(gemm_sab_kernel<EPI, CG>,
-                               cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-      if (e != cudaSuccess) return e;
-    }
-    attr = true;
-  }
+  cudaError_t e = prepare<EPI, CG, split_by_default<EPI>()>();
+  if (e != cudaSuccess) return e;
   // units: CTAs, or CTA pairs
   const int max_units = CG == 2 ? max_pairs<EPI>(kSmemMax) : num_sms();
   const int n_ft = (p.n_ft + CG - 1) / CG;
@@ -630,28 +668,11 @@ static cudaError_t run(const CUtensorMap &mx, const CUtensorMap &mw, const CUten
       }
     }
   }
-  if (CG == 1) {
-    cudaError_t e = launch_pdl(gemm_sab_kernel<EPI, 1>, dim3(units), dim3(kThreads), smem, s, mx,
-                               mw, mw2, p, status);
-    if (e != cudaSuccess) return e;
-  } else {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * units, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute at[2];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = 2;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_sab_kernel<EPI, 2>, mx, mw, mw2, p, status);
-    if (e != cudaSuccess) return e;
-  }
+  if (p.split > 1 && !split_by_default<EPI>())
+    e = launch<EPI, CG, can_split<EPI>()>(units, smem, mx, mw, mw2, p, status, s);
+  else
+    e = launch<EPI, CG, split_by_default<EPI>()>(units, smem, mx, mw, mw2, p, status, s);
+  if (e != cudaSuccess) return e;
   return launched(1);
 }
 

@@ -304,13 +304,14 @@ def test_bounded_wait_expires_with_status():
 @pytest.mark.parametrize("Hq,Hkv,hd", [(4, 2, 64), (32, 8, 128)])
 def test_attention_matches_oracle(dt, Hq, Hkv, hd):
     rng = np.random.default_rng(8)
-    Ts = [300, 129, 1]
-    kv0 = [0, 300, 429]
+    # the last request's 18 key blocks are split into chunks (and combined)
+    Ts = [300, 129, 1, 1100]
+    kv0 = [0, 300, 429, 430]
     Ttot = sum(Ts)
     K = _vals(rng, (Ttot, Hkv * hd), dt)
     V = _vals(rng, (Ttot, Hkv * hd), dt)
     pos, reqs, q0 = [], [], 0
-    for T, k0, nq in zip(Ts, kv0, [40, 129, 1]):
+    for T, k0, nq in zip(Ts, kv0, [40, 129, 1, 24]):
         p = np.sort(rng.choice(T, nq, replace=False))
         pos.append(p)
         reqs.append((q0, q0 + nq, k0, T))
