@@ -168,8 +168,8 @@ def setup_replica(rank, device, n_layers=None):
 # compact layer: the CTA-pair swapped GEMM), valid only for the kernel source
 # it was taken on.
 TRAFFIC_CAPTURE = {"source": "rag_kv_cache_layer_gb300/csrc/k_gemm_sab.cu",
-                   "sha256": "bf1bbc2df74787db250974abb270ae7e1874a8dd38ed2141153ab9f8ef8a61c5",
-                   "bytes_per_launch": 241394176 + 18594304,
+                   "sha256": "d80816d0c586d27f847ae7e0b733c2a7bb2fac60fc8abf1ca7aaf9230850afaa",
+                   "bytes_per_launch": 241400320 + 18620672,
                    "profile": "profiles/gemm_swiglu_M524_llama8b.md"}
 
 
