@@ -136,9 +136,9 @@ __global__ void probe_rows_kernel(const __grid_constant__ ProbeParams p,
 // rows are ordered r = h * n_u + u, so a kv head's rows are contiguous.
 constexpr int HD = 128;
 constexpr int KC = 64;                  // keys per score tile
-constexpr int RC = 64;                  // rows per score tile
-constexpr int kTileThreads = 256;       // 16 x 16 threads, 4 rows x 4 keys each
-constexpr int kScoreSmem = 2 * HD * 64 * 4;
+constexpr int RC = 128;                 // rows per score tile
+constexpr int kTileThreads = 256;       // 16 x 16 threads, 8 rows x 4 keys each
+constexpr int kScoreSmem = HD * (RC + KC) * 4;
 
 // Scores s[t][r] = log2(e) q_r.k_t / sqrt(hd) of a 64-row x 64-key tile
 // (all rows of one kv head's group), and each row's (max, sum of
@@ -165,7 +165,7 @@ mass_score_kernel(const bf16 *__restrict__ q, int64_t ld_q, int u_off, int n_u,
   const int t0 = blockIdx.x * KC;
   const int nk = min(KC, n_ctx - t0);
   const int n_rows = Hq * n_u;
-  // stage: entry i is row (and key) i % 64, dims 8 * (i / 64) .. + 7
+  // stage: entry i is row i % RC (key i % KC), dims 8 * (i / RC) .. + 7
   for (int i = threadIdx.x; i < RC * (HD / 8); i += kTileThreads) {
     const int row = i % RC, e = 8 * (i / RC);
     float qv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -179,6 +179,9 @@ mass_score_kernel(const bf16 *__restrict__ q, int64_t ld_q, int u_off, int n_u,
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) qs[(e + j) * RC + row] = qv[j];
+  }
+  for (int i = threadIdx.x; i < KC * (HD / 8); i += kTileThreads) {
+    const int row = i % KC, e = 8 * (i / KC);
     float kv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (row < nk) {
       const uint4 raw = *reinterpret_cast<const uint4 *>(
@@ -191,38 +194,42 @@ mass_score_kernel(const bf16 *__restrict__ q, int64_t ld_q, int u_off, int n_u,
     for (int j = 0; j < 8; ++j) ks[(e + j) * KC + row] = kv[j];
   }
   __syncthreads();
+  // thread (ty, tx): rows 8 ty .. 8 ty + 7, keys 4 tx .. 4 tx + 3
   const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
-  float acc[4][4];
+  float acc[8][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-#pragma unroll 8
+#pragma unroll 4
   for (int e = 0; e < HD; ++e) {
-    const float4 a = *reinterpret_cast<const float4 *>(qs + e * RC + 4 * ty);
+    const float4 a0 = *reinterpret_cast<const float4 *>(qs + e * RC + 8 * ty);
+    const float4 a1 = *reinterpret_cast<const float4 *>(qs + e * RC + 8 * ty + 4);
     const float4 b = *reinterpret_cast<const float4 *>(ks + e * KC + 4 * tx);
-    const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+    const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const float bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
   }
-  // scores out (4 consecutive rows per key), then each row's statistics over
+  // scores out (8 consecutive rows per key), then each row's statistics over
   // the tile's keys: the 16 threads of a row group are 16 consecutive lanes
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int t = 4 * tx + j;
-    if (t < nk && 4 * ty < nr) {
-      float *dst = s + (int64_t)(t0 + t) * n_rows + r0 + 4 * ty;
-      if (4 * ty + 4 <= nr && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-        *reinterpret_cast<float4 *>(dst) = make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
+    if (t < nk && 8 * ty < nr) {
+      float *dst = s + (int64_t)(t0 + t) * n_rows + r0 + 8 * ty;
+      if (8 * ty + 8 <= nr && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+        reinterpret_cast<float4 *>(dst)[0] = make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
+        reinterpret_cast<float4 *>(dst)[1] = make_float4(acc[4][j], acc[5][j], acc[6][j], acc[7][j]);
       } else {
-        for (int i = 0; i < 4 && 4 * ty + i < nr; ++i) dst[i] = acc[i][j];
+        for (int i = 0; i < 8 && 8 * ty + i < nr; ++i) dst[i] = acc[i][j];
       }
     }
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < 8; ++i) {
     float mx = -INFINITY;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
@@ -233,12 +240,13 @@ mass_score_kernel(const bf16 *__restrict__ q, int64_t ld_q, int u_off, int n_u,
     for (int j = 0; j < 4; ++j)
       if (4 * tx + j < nk) sum += exp2f(acc[i][j] - mx);
     for (int o = 8; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (tx == 0 && 4 * ty + i < nr)
-      part[(int64_t)blockIdx.x * n_rows + r0 + 4 * ty + i] = make_float2(mx, sum);
+    if (tx == 0 && 8 * ty + i < nr)
+      part[(int64_t)blockIdx.x * n_rows + r0 + 8 * ty + i] = make_float2(mx, sum);
   }
 }
 
-// Each row's softmax statistics over all of the request's keys.
+// Each row's softmax statistics over all of the request's keys: the maximum
+// and the reciprocal of the sum (the sum pass multiplies).
 __global__ void mass_stats_kernel(const float2 *__restrict__ part, int n_chunks, int n_rows,
                                   float2 *__restrict__ ml) {
   grid_dep_wait();
@@ -252,11 +260,11 @@ __global__ void mass_stats_kernel(const float2 *__restrict__ part, int n_chunks,
     const float2 v = part[(int64_t)c * n_rows + r];
     L += v.y * exp2f(v.x - M);
   }
-  ml[r] = make_float2(M, L);
+  ml[r] = make_float2(M, 1.f / L);
 }
 
-// One warp per key: I[t] += sum over every row of 2^(s - m_r) / l_r, lanes
-// striding the rows, then a fixed-order butterfly.
+// One warp per key: I[t] += sum over every row of 2^(s - m_r) / l_r (ml holds
+// m_r and 1 / l_r), lanes striding the rows, then a fixed-order butterfly.
 __global__ void mass_sum_kernel(const float *__restrict__ s, const float2 *__restrict__ ml,
                                 int n_rows, int n_ctx, float *__restrict__ mass) {
   grid_dep_wait();
@@ -268,7 +276,7 @@ __global__ void mass_sum_kernel(const float *__restrict__ s, const float2 *__res
   float acc = 0.f;
   for (int r = lane; r < n_rows; r += 32) {
     const float2 v = ml[r];
-    acc += exp2f(row[r] - v.x) / v.y;
+    acc += exp2f(row[r] - v.x) * v.y;
   }
   for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (lane == 0) mass[t] += acc;
