@@ -815,6 +815,21 @@ def run_qcf(args):
     st = torch.cuda.current_stream()
     mid = n_layers // 2
     crit = sorted({min(max(l, 0), n_layers - 1) for l in (mid - 1, mid, mid + 1)})
+    if args.profile:
+        # one anchor-probe call between cudaProfilerStart and cudaProfilerStop
+        kw = dict(policy=L.CB_POLICY_QUERY_PROBE, sel_layer=0,
+                  query={"anchor_rule": L.CB_ANCHOR_KNORM, "anchor_bp": 1000, "crit_layers": crit})
+        o = model.alloc_outputs(model.plan(reqs, 1500, **kw), 1)
+        for _ in range(max(args.warmup, 1)):
+            model.cb_blend_prefill(reqs, 1500, outputs=o, **kw)
+        torch.cuda.synchronize()
+        torch.cuda.cudart().cudaProfilerStart()
+        model.cb_blend_prefill(reqs, 1500, outputs=o, **kw)
+        torch.cuda.synchronize()
+        torch.cuda.cudart().cudaProfilerStop()
+        if R.device_status() != 0:
+            raise RuntimeError("device status set during the profiled call")
+        return
     full_outs = model.alloc_outputs(model.plan(reqs), 1, blend=False)
     full_ms, _ = _graph_ms(lambda: model.cb_full_prefill(reqs, outputs=full_outs), args.steps, st)
     del full_outs
