@@ -264,11 +264,11 @@ typedef struct {
  * The selected context indices are written ascending to
  * idx_out[idx_offset .. idx_offset + k).
  * k_fresh, k_reused: device [rows][ld] of dtype.  dev_out: device float.
- * idx_out: device int32.  ws: device workspace of at least
- * cb_select_workspace_size(n_req) bytes.
+ * idx_out: device int32.  ws, ws_bytes: reserved; the selection needs no
+ * scratch beyond dev_out, so ws may be NULL with ws_bytes 0 (a non-NULL ws
+ * is not touched), and cb_select_workspace_size returns 0.
  * Errors: CB_ERR_INVALID_ARG (n_req > CB_MAX_BATCH, k > n_ctx, spans not
- *   covering [0, n_ctx] ascending, total spans > CB_MAX_SPANS),
- *   CB_ERR_WORKSPACE. */
+ *   covering [0, n_ctx] ascending, total spans > CB_MAX_SPANS). */
 size_t cb_select_workspace_size(int n_req);
 cb_status cb_kv_deviation_topk(const void *k_fresh, int64_t ld_fresh,
                                const void *k_reused, int64_t ld_reused,
@@ -284,9 +284,9 @@ cb_status cb_kv_deviation_topk(const void *k_fresh, int64_t ld_fresh,
  * synchronisation is not acceptable).  The pages have no counterpart: this
  * is an integration variant.  The per-token deviations live in a fixed 4 MiB
  * device array inside the library instead of caller memory, so a call takes
- * no dev_out and no workspace; req.dev_offset is ignored (the library packs
- * the deviations request after request) and the selected indices go to
- * idx_out exactly as in cb_kv_deviation_topk.
+ * no dev_out and no workspace; req.dev_offset is ignored, whatever its
+ * value (the library packs the deviations request after request), and the
+ * selected indices go to idx_out exactly as in cb_kv_deviation_topk.
  * Limit: at most 1048576 context tokens (sum of n_ctx) per call; larger calls
  * return CB_ERR_INVALID_ARG and enqueue nothing.
  * The first call on each device resolves the array's device address, so make

@@ -83,16 +83,14 @@ def cb_rope_reposition(descs, layer_begin, layer_end, k_cache, v_cache,
 def cb_kv_deviation_topk(k_fresh, k_reused, reqs, policy, dev_out, idx_out,
                          ws=None, stream=None):
     """reqs: list of dicts with n_ctx, k, fresh_row0, reused_row0,
-    dev_offset, idx_offset and (doc-aligned) span_offsets."""
+    dev_offset, idx_offset and (doc-aligned) span_offsets.  ws is reserved
+    by the library (the selection needs no scratch) and may stay None."""
     n = len(reqs)
     arr, keep = _select_reqs(reqs)
-    need = lib.cb_select_workspace_size(n)
-    if ws is None:
-        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=k_fresh.device)
     check(lib.cb_kv_deviation_topk(
         _p(k_fresh), k_fresh.stride(0), _p(k_reused), k_reused.stride(0),
         k_fresh.shape[1], dtype_code(k_fresh.dtype), arr, n, policy,
-        _p(dev_out), _p(idx_out), _p(ws), ws.numel(), _s(stream)))
+        _p(dev_out), _p(idx_out), _p(ws), 0 if ws is None else ws.numel(), _s(stream)))
 
 
 def _select_reqs(reqs, dev_offsets=True):

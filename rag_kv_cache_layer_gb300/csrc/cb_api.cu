@@ -148,9 +148,9 @@ static __device__ int g_status_word;
 namespace cb {
 int *device_status_ptr() {
   static std::mutex mu;
-  static int *ptrs[64] = {nullptr};
+  static int *ptrs[kMaxDevices] = {nullptr};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lk(mu);
   if (!ptrs[dev]) {
     void *p = nullptr;
@@ -158,6 +158,21 @@ int *device_status_ptr() {
     ptrs[dev] = (int *)p;
   }
   return ptrs[dev];
+}
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int n[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!n[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      return 148;
+    n[dev] = v;
+  }
+  return n[dev];
 }
 }  // namespace cb
 
@@ -271,7 +286,8 @@ extern "C" cb_status cb_kv_deviation_topk(const void *k_fresh, int64_t ld_fresh,
   if (row_elems <= 0 || (row_elems * eb) % 16 || ld_fresh < row_elems || ld_reused < row_elems ||
       (ld_fresh * eb) % 16 || (ld_reused * eb) % 16 || !aligned16(k_fresh) || !aligned16(k_reused))
     return fail(CB_ERR_INVALID_ARG, "rows must be 16-byte aligned and ld >= row_elems");
-  if (!ws || ws_bytes < cb_select_workspace_size(n_req)) return fail(CB_ERR_WORKSPACE, "workspace too small");
+  (void)ws;        // reserved: the selection needs no scratch beyond dev_out
+  (void)ws_bytes;
   SelPlan plan;
   const char *err = "";
   if (make_sel_plan(reqs, n_req, policy, plan, &err) != CB_OK) return fail(CB_ERR_INVALID_ARG, "%s", err);

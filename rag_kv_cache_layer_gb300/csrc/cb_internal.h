@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <utility>
 #include <vector>
 
@@ -28,6 +29,37 @@ struct BatchMeta {
 
 // Device address of this library's status word on the current device.
 int *device_status_ptr();
+
+// Number of devices the per-device caches below cover.
+constexpr int kMaxDevices = 64;
+
+// One-time host set-up per device (a kernel's function attributes, an
+// occupancy query): such state belongs to each device's context, so it is
+// done once for every device the library runs on.  run(f) calls f() with the
+// current device's index until it first returns cudaSuccess; concurrent
+// first calls from several threads are serialised.
+class PerDeviceOnce {
+ public:
+  template <typename F>
+  cudaError_t run(F &&f) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu_);
+    if (done_[dev]) return cudaSuccess;
+    e = f(dev);
+    if (e == cudaSuccess) done_[dev] = true;
+    return e;
+  }
+
+ private:
+  std::mutex mu_;
+  bool done_[kMaxDevices] = {};
+};
+
+// Streaming multiprocessors of the current device (queried once per device).
+int device_sm_count();
 
 // Sets the thread's cb_last_error_message and returns s.
 cb_status record_error(cb_status s, const char *msg);

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "cb_common.cuh"
+#include "cb_internal.h"
 
 namespace cb {
 namespace tcx {
@@ -213,16 +214,7 @@ inline bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t c
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-inline int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
+inline int num_sms() { return device_sm_count(); }
 
 }  // namespace tcx
 }  // namespace cb

@@ -861,16 +861,7 @@ static bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t c
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
+static int num_sms() { return device_sm_count(); }
 
 // Tiles of a call and the key-range split: tiles that alone fill fewer than
 // all SMs get their key blocks split into chunks so that about two waves of
@@ -986,14 +977,12 @@ cudaError_t launch_attention_tc(const void *q, int64_t ld_q, const int32_t *q_po
       !make_map(&mk, k_cache, kv_rows, (int64_t)Hkv * HD, ld_kv, BN) ||
       !make_map(&mv, v_cache, kv_rows, (int64_t)Hkv * HD, ld_kv, BN))
     return cudaErrorInvalidValue;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  cudaError_t e = launch_pdl(attn_tc_kernel, dim3(grid), dim3(kThreads), kSmem, s,
+  static PerDeviceOnce attr;
+  cudaError_t e = attr.run([](int) {
+    return cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  });
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(attn_tc_kernel, dim3(grid), dim3(kThreads), kSmem, s,
                              mq, mk, mv, P, q_pos, reinterpret_cast<bf16 *>(out), ld_out, part_o,
                              part_ml, status);
   if (e != cudaSuccess) return e;

@@ -563,8 +563,12 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
 // (a pair needs two SMs of one GPC).
 template <int EPI>
 static int max_pairs(int smem) {
-  static int cached = 0;
-  if (cached) return cached;
+  static std::mutex mu;
+  static int cached[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return num_sms() / 2;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cached[dev]) return cached[dev];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * num_sms(), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -581,25 +585,22 @@ static int max_pairs(int smem) {
           cudaSuccess ||
       n <= 0)
     n = num_sms() / 2;
-  cached = n;
+  cached[dev] = n;
   return n;
 }
 
 // Function attributes of one instantiation, set once.
 template <int EPI, int CG, bool TS>
 static cudaError_t prepare() {
-  static bool done = false;
-  if (done) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(gemm_sab_kernel<EPI, CG, TS>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-  if (e != cudaSuccess) return e;
-  if (CG == 2) {
-    e = cudaFuncSetAttribute(gemm_sab_kernel<EPI, CG, TS>,
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-    if (e != cudaSuccess) return e;
-  }
-  done = true;
-  return cudaSuccess;
+  static PerDeviceOnce once;
+  return once.run([](int) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_sab_kernel<EPI, CG, TS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (e == cudaSuccess && CG == 2)
+      e = cudaFuncSetAttribute(gemm_sab_kernel<EPI, CG, TS>,
+                               cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    return e;
+  });
 }
 
 template <int EPI, int CG, bool TS>

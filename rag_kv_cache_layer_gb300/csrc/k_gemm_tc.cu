@@ -514,29 +514,19 @@ static bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t c
   return r == CUDA_SUCCESS;
 }
 
-static int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
+static int num_sms() { return device_sm_count(); }
 
 template <int BN, int EPI>
 static cudaError_t run(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mb2,
                        int M, int N, int K, bool stream_k, const EpiParams &ep, int *status,
                        cudaStream_t s) {
   using C = Cfg<BN, EPI>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static PerDeviceOnce attr;
+  cudaError_t ea = attr.run([](int) {
+    return cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::kSmem);
+  });
+  if (ea != cudaSuccess) return ea;
   const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + C::kOutN - 1) / C::kOutN);
   const int64_t work = stream_k ? tiles * ((K + BK - 1) / BK) : tiles;
   const int grid = work < num_sms() ? (int)work : num_sms();

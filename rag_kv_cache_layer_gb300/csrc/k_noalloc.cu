@@ -65,9 +65,15 @@ extern "C" cb_status cb_kv_deviation_topk_noalloc(const void *k_fresh, int64_t l
       (ld_fresh * eb) % 16 || (ld_reused * eb) % 16 || ((uintptr_t)k_fresh & 15) ||
       ((uintptr_t)k_reused & 15))
     return record_error(CB_ERR_INVALID_ARG, "rows must be 16-byte aligned and ld >= row_elems");
+  if (n_req < 0 || n_req > CB_MAX_BATCH) return record_error(CB_ERR_INVALID_ARG, "n_req must be in [0, CB_MAX_BATCH]");
+  if (n_req > 0 && !reqs) return record_error(CB_ERR_INVALID_ARG, "reqs is NULL");
+  // dev_offset is not an input of this entry point (the deviations are
+  // packed below), so whatever the caller left in it is not validated
+  std::vector<cb_select_req> rq(reqs, reqs + n_req);
+  for (cb_select_req &r : rq) r.dev_offset = 0;
   SelPlan plan;
   const char *err = "";
-  if (make_sel_plan(reqs, n_req, policy, plan, &err) != CB_OK)
+  if (make_sel_plan(rq.data(), n_req, policy, plan, &err) != CB_OK)
     return record_error(CB_ERR_INVALID_ARG, err);
   // deviations are packed request after request into the static array
   int64_t total = 0;

@@ -366,13 +366,12 @@ cudaError_t launch_attention_mass(const void *q, int64_t ld_q, int u_off, int n_
   w += ((size_t)n_chunks * n_rows * 8 + 255) / 256 * 256;
   float2 *ml = reinterpret_cast<float2 *>(w);
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(mass_score_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static PerDeviceOnce attr;
+  cudaError_t ea = attr.run([](int) {
+    return cudaFuncSetAttribute(mass_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kScoreSmem);
+  });
+  if (ea != cudaSuccess) return ea;
   const int tiles_per_group = ((Hq / Hkv) * n_u + RC - 1) / RC;
   cudaError_t e = launch_pdl(mass_score_kernel, dim3(n_chunks, Hkv * tiles_per_group),
                              dim3(kTileThreads), kScoreSmem, s,

@@ -358,16 +358,7 @@ lm_head_kernel(const float *__restrict__ x, int B, const T *__restrict__ E,
 }
 
 // SMs of the current device (one persistent CTA each for the GEMV).
-static int num_sms_rows() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
+static int num_sms_rows() { return device_sm_count(); }
 
 // One request, d = 4096, bf16 embedding: each lane holds its 128 entries of
 // the normed hidden state in registers (dims 8 * lane + 256 k) and issues the

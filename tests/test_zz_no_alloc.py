@@ -45,9 +45,36 @@ def test_noalloc_matches_scratch_version_on_two_calls(policy):
         assert torch.equal(got, ref)
 
 
+def test_noalloc_ignores_the_callers_dev_offset():
+    """dev_offset is not an input here: a C caller that leaves it at any
+    value (here -1, which cb_kv_deviation_topk would reject) gets the same
+    selection."""
+    import ctypes as C
+    kf, kr, reqs, k_total, n_total = _inputs(3)
+    ref = torch.full((k_total,), -1, dtype=torch.int32, device="cuda")
+    d = torch.empty(n_total, dtype=torch.float32, device="cuda")
+    R.cb_kv_deviation_topk(kf, kr, reqs, L.CB_POLICY_TOKEN_TOPK, d, ref)
+    arr = (L.SelectReq * len(reqs))()
+    for i, r in enumerate(reqs):
+        arr[i] = L.SelectReq(r["n_ctx"], r["k"], r["fresh_row0"], r["reused_row0"], -1,
+                             r["idx_offset"], 0, None, None, 0, 0)
+    got = torch.full((k_total,), -2, dtype=torch.int32, device="cuda")
+    L.check(L.lib.cb_kv_deviation_topk_noalloc(
+        C.c_void_p(kf.data_ptr()), kf.stride(0), C.c_void_p(kr.data_ptr()), kr.stride(0),
+        kf.shape[1], L.CB_BF16, arr, len(reqs), L.CB_POLICY_TOKEN_TOPK,
+        C.c_void_p(got.data_ptr()), C.c_void_p(torch.cuda.current_stream().cuda_stream)))
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    assert torch.equal(got, ref)
+
+
 def test_noalloc_rejects_more_than_its_limit():
-    kf = torch.zeros(16, 64, device="cuda")
-    reqs = [dict(n_ctx=(1 << 20) + 1, k=1)]
+    # inputs that hold every row the request names (8 bf16 = 16 bytes per
+    # row), so a limit check that let the call through would read in bounds
+    # and show up only as the missing error below
+    n = (1 << 20) + 1
+    kf = torch.zeros(n, 8, dtype=torch.bfloat16, device="cuda")
+    reqs = [dict(n_ctx=n, k=1)]
     with pytest.raises(L.CBError) as e:
         R.cb_kv_deviation_topk_noalloc(kf, kf, reqs, L.CB_POLICY_TOKEN_TOPK,
                                        torch.empty(1, dtype=torch.int32, device="cuda"))
