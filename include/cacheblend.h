@@ -166,7 +166,10 @@ cb_status cb_debug_gemm_path(int path);
 #define CB_PROBE_SWIGLU 3    /* gate/up projection with SiLU gating */
 #define CB_PROBE_DOWN 4      /* down projection + residual */
 #define CB_PROBE_ATTENTION 5 /* selected-query attention */
-#define CB_PROBE_STITCH 6    /* re-position + stitch of the cached segments */
+#define CB_PROBE_STITCH 6    /* re-position + stitch of the cached segments;
+                                in cb_blend_prefill_host_kv, each layer's load
+                                on copy_stream (copies, or the zero-copy
+                                re-position) */
 #define CB_PROBE_SELECT 7    /* deviation + ranking at the selection layer */
 #define CB_PROBE_GATHER 8    /* computed-row list + hidden-state gather */
 #define CB_PROBE_LM_HEAD 9   /* final norm + tied LM head + arg-max */
@@ -487,6 +490,24 @@ typedef struct {
                           chunk                                             */
   int n_crit;          /* the critical-layer set L*: n_crit >= 1 distinct  */
   const int32_t *crit_layers; /* host [n_crit] layers in [0, n_layers)     */
+  const int32_t *forced_kept; /* device or NULL, used with a schedule: the
+                          context positions each gradual step keeps, step
+                          after step, each step's requests in order (k'_b
+                          ascending request-local positions per request, a
+                          subset of the rows selected before the step),
+                          taken instead of ranking the step's deviations --
+                          the per-step counterpart of forced_selected.  A
+                          position that is not in the current selection, or
+                          out of order, records CB_ERR_DEVICE_INDEX.       */
+  int host_load_ctas;  /* cb_blend_prefill_host_kv only.  0: the copy
+                          engines copy each layer's chunk caches into a
+                          staging area, then they are re-positioned.  > 0:
+                          the re-position kernel itself reads the pinned
+                          chunk caches (zero-copy) on copy_stream with at
+                          most this many CTAs per layer, which bounds the
+                          load bandwidth (a slower storage tier is emulated
+                          by a small count) and needs no staging area.
+                          0 .. 4096.                                       */
 } cb_blend_params;
 
 /* Per-chunk anchors of [QCF] Eq. 14, as the offline cache preparation of
@@ -591,6 +612,44 @@ cb_status cb_blend_prefill_host_kv(cb_model *m, const cb_request *reqs, int B,
                                    const cb_blend_params *p, const cb_blend_out *out,
                                    void *ws, size_t ws_bytes, cb_stream stream,
                                    cb_stream copy_stream);
+
+/* Loading controller of [CB] "Hiding Recompute Behind I/O": with the chunk
+ * caches loaded layer by layer, recomputing a fraction r of the tokens is
+ * free while its per-layer compute time stays within the per-layer K/V load
+ * time, so r = max(r_load, r_min), r_load the largest of the n measured
+ * ratios ratio_bp[i] whose recompute_ms_per_layer[i] <= load_ms_per_layer
+ * (r_min = min_ratio_bp, the page's 15% quality floor, 1500).
+ * ratio_bp, recompute_ms_per_layer: host [n].  *ratio_out: the chosen ratio
+ * in basis points.  Host only (no device work).  Errors:
+ * CB_ERR_INVALID_ARG for n < 0, NULL arrays with n > 0, ratios outside
+ * [0, 10000], a negative or NaN time. */
+cb_status cb_loading_ratio(double load_ms_per_layer, const int32_t *ratio_bp,
+                           const double *recompute_ms_per_layer, int n,
+                           int32_t min_ratio_bp, int32_t *ratio_out);
+
+/* Diagnostics of selections ([ROM] §4.4, Table 2): for request b of a
+ * selection (reqs[b].n_ctx, .k, .dev_offset, .idx_offset as for
+ * cb_kv_deviation_topk; the other fields are ignored), the number of
+ * separate contiguous regions its selected positions occupy (maximal runs
+ * of consecutive positions) and the share of the request's total deviation
+ * the selected tokens carry (sum of d over the selection / sum over all
+ * n_ctx, 0 when the total is 0; sums in double).
+ * dev: device float deviations; idx: device int32 selections, ascending per
+ * request.  segments_out: device int32 [n_req]; captured_out: device double
+ * [n_req].  An index outside [0, n_ctx) records CB_ERR_DEVICE_INDEX and is
+ * skipped.  Errors: CB_ERR_INVALID_ARG (NULL pointers, n_req outside
+ * [0, CB_MAX_BATCH], k > n_ctx, negative offsets). */
+cb_status cb_selection_stats(const float *dev, const int32_t *idx,
+                             const cb_select_req *reqs, int n_req,
+                             int32_t *segments_out, double *captured_out,
+                             cb_stream stream);
+
+/* Number of anchors cb_anchor_select writes for these chunks: the sum over
+ * chunks of ceil(ratio_bp |c_i| / 10000) ([QCF] Eq. 14).  Errors:
+ * CB_ERR_INVALID_ARG (NULL pointers, n_chunks < 0, a negative length,
+ * ratio_bp outside [0, 10000]). */
+cb_status cb_anchor_count(const cb_segment *chunks, int n_chunks, int ratio_bp,
+                          int64_t *n_anchors);
 
 /* Full prefill ([QCF] Eq. 2): every row of every layer is computed under
  * the whole request (segments' caches are ignored).  Fills k_cache,

@@ -43,7 +43,8 @@ import numpy as np
 __all__ = [
     "Model", "model_from_weights", "rope_inv_freq", "rope_rotate",
     "reposition_keys", "stitch", "rms_norm", "silu", "causal_attention",
-    "qkv_rows", "kv_rows", "decoder_layer", "full_prefill", "chunk_prefill", "kv_deviation",
+    "qkv_rows", "kv_rows", "decoder_layer", "full_prefill", "chunk_prefill",
+    "chunk_prefill_all", "kv_deviation",
     "select_count", "token_topk", "doc_aligned_select", "blend_prefill",
     "first_token", "first_token_logits", "embed_rows", "kv_bytes_per_layer",
     "selection_segments", "captured_deviation", "single_window_select",
@@ -297,6 +298,24 @@ def chunk_prefill(m: Model, chunk_tokens):
     return r.K, r.V
 
 
+def chunk_prefill_all(m: Model, chunks):
+    """chunk_prefill of every chunk in ``chunks`` (token lists), with the
+    layer loop outside the chunk loop: each chunk still runs alone at its
+    local positions, through the same decoder_layer calls in the same order
+    per chunk, so the result is the per-chunk one bit for bit.  A model
+    whose layers are fetched on demand then reads each layer once."""
+    kvw = m.n_kv_heads * m.head_dim
+    toks = [np.asarray(c) for c in chunks]
+    K = [np.zeros((m.n_layers, len(t), kvw)) for t in toks]
+    V = [np.zeros((m.n_layers, len(t), kvw)) for t in toks]
+    h = [embed_rows(m, t) for t in toks]
+    for l in range(m.n_layers):
+        for i, t in enumerate(toks):
+            rows = np.arange(len(t))
+            h[i], _, _ = decoder_layer(m, l, h[i], rows, K[i][l], V[i][l], rows)
+    return list(zip(K, V))
+
+
 # --------------------------------------------------------------------------
 # deviation and selection
 # --------------------------------------------------------------------------
@@ -443,7 +462,7 @@ class BlendResult:
 def blend_prefill(m: Model, segments, store, ratio_bp: int,
                   policy: str = "token_topk", sel_layer: int = 1,
                   span_len: int = 0, span_offset: int = 0, span_order=None,
-                  forced=None, schedule=None) -> BlendResult:
+                  forced=None, schedule=None, forced_steps=None) -> BlendResult:
     """Selective KV recomputation over a partially reused cache (QCFuse
     §2.1.3 Eqs. 6-7; CacheBlend blog ``blend_layer``; LMCache flow of
     "Request Order Matters" §2.2).
@@ -466,6 +485,11 @@ def blend_prefill(m: Model, segments, store, ratio_bp: int,
       list of (layer, keep_count) with layer > sel_layer; at that layer the
       current P is re-ranked by the deviation of its fresh keys and only
       keep_count rows are kept from then on.
+    forced_steps: optional {layer: positions} for schedule layers: the
+      context positions kept at that step (a subset of the current P, of
+      min(keep_count, |P|) entries) are taken from it instead of the
+      re-ranking -- the per-step counterpart of ``forced``; the step's
+      deviations are still computed.
 
     Steps:
       1. positions 0..T-1; context positions of cached segments are the
@@ -569,8 +593,14 @@ def blend_prefill(m: Model, segments, store, ratio_bp: int,
                 kp = rope_rotate(kp, rows_p, m.rope_base).reshape(-1, kvw)
                 dp = kv_deviation(kp, K[l][rows_p])
                 dev_steps[l] = dict(zip(P.tolist(), dp.tolist()))
-                keep = token_topk(dp, min(sched[l], len(P)))
-                P = P[keep]
+                if forced_steps is not None and l in forced_steps:
+                    kept = np.asarray(forced_steps[l], dtype=np.int64)
+                    assert len(kept) == min(sched[l], len(P)), "forced step has the wrong size"
+                    assert np.all(np.isin(kept, P)), "forced step keeps a row not in P"
+                    P = np.sort(kept)
+                else:
+                    keep = token_topk(dp, min(sched[l], len(P)))
+                    P = P[keep]
             new_active = np.union1d(ctx_rows[P], always).astype(np.int64)
             if active is None:
                 h_act = h[new_active]

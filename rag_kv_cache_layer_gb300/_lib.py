@@ -99,7 +99,8 @@ class BlendParams(C.Structure):
                 ("span_len", i32), ("span_offset", i32),
                 ("span_order", C.POINTER(C.c_int32)), ("forced_selected", vp),
                 ("anchor_rule", i32), ("anchor_bp", i32), ("n_crit", i32),
-                ("crit_layers", C.POINTER(C.c_int32))]
+                ("crit_layers", C.POINTER(C.c_int32)), ("forced_kept", vp),
+                ("host_load_ctas", i32)]
 
 
 class BlendOut(C.Structure):
@@ -173,6 +174,10 @@ def _load():
         "cb_anchor_workspace_size": (C.c_size_t, [vp, C.POINTER(Segment), i32]),
         "cb_anchor_select": (S, [vp, C.POINTER(Segment), i32, i32, i32, vp, vp, vp,
                                  C.c_size_t, vp]),
+        "cb_anchor_count": (S, [C.POINTER(Segment), i32, i32, C.POINTER(i64)]),
+        "cb_loading_ratio": (S, [C.c_double, C.POINTER(C.c_int32), C.POINTER(C.c_double), i32,
+                                 C.c_int32, C.POINTER(C.c_int32)]),
+        "cb_selection_stats": (S, [vp, vp, C.POINTER(SelectReq), i32, vp, vp, vp]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(lib, name)
@@ -199,7 +204,8 @@ EXPORTED = [
     "cb_blend_prefill", "cb_blend_plan_host_kv", "cb_blend_prefill_host_kv",
     "cb_full_plan", "cb_full_prefill",
     "cb_layer_workspace_size", "cb_blend_layer",
-    "cb_anchor_workspace_size", "cb_anchor_select",
+    "cb_anchor_workspace_size", "cb_anchor_select", "cb_anchor_count",
+    "cb_loading_ratio", "cb_selection_stats",
 ]
 
 

@@ -20,7 +20,7 @@ __all__ = [
     "cb_scatter_kv",
     "cb_sparse_query_attention", "cb_debug_expire_wait", "cb_debug_gemm_path", "Seg", "Req",
     "BlendModel", "ChunkStore", "HostChunkStore", "RollingWindow", "selection_stats",
-    "loading_controller", "select_count",
+    "loading_controller",
     "device_status",
 ]
 
@@ -46,13 +46,6 @@ def _p(t):
 def _s(stream=None):
     st = stream if stream is not None else torch.cuda.current_stream()
     return C.c_void_p(st.cuda_stream)
-
-
-def select_count(n_ctx: int, ratio_bp: int) -> int:
-    """k = max(1, floor(N r)) for r > 0, 0 for r = 0 (integer basis points)."""
-    if ratio_bp <= 0 or n_ctx <= 0:
-        return 0
-    return max(1, (n_ctx * ratio_bp) // 10000)
 
 
 # ------------------------------------------------------------ primitives --
@@ -303,7 +296,8 @@ class BlendModel:
                                  _s(stream)))
 
     def _params(self, ratio_bp, policy, sel_layer, schedule, forced=None, span_len=0,
-                span_offset=0, span_order=None, query=None):
+                span_offset=0, span_order=None, query=None, forced_kept=None,
+                host_load_ctas=0):
         """query: for the query-aware policies, a dict with anchor_rule,
         anchor_bp and crit_layers (QCFuse Eqs. 14, 20)."""
         n = len(schedule or [])
@@ -322,7 +316,9 @@ class BlendModel:
                              None if forced is None else forced.data_ptr(),
                              int(q.get("anchor_rule", L.CB_ANCHOR_SINK)),
                              int(q.get("anchor_bp", 0)), len(crit),
-                             C.cast(crit_arr, C.POINTER(C.c_int32))), (sch, order, crit_arr)
+                             C.cast(crit_arr, C.POINTER(C.c_int32)),
+                             None if forced_kept is None else forced_kept.data_ptr(),
+                             int(host_load_ctas)), (sch, order, crit_arr)
 
     def plan(self, reqs, ratio_bp=None, policy=0, sel_layer=1, schedule=None, span_len=0,
              span_offset=0, span_order=None, query=None):
@@ -364,16 +360,19 @@ class BlendModel:
     def cb_blend_prefill(self, reqs, ratio_bp, policy=0, sel_layer=1,
                          schedule=None, outputs=None, forced=None,
                          stream=None, span_len=0, span_offset=0, span_order=None,
-                         query=None):
+                         query=None, forced_kept=None):
         """forced: optional device int32 tensor of selected context
         positions (ascending per request) used instead of the ranking.
+        forced_kept: with a schedule, the positions each gradual step keeps
+        (device int32, step after step, requests in order) instead of its
+        ranking.
         span_len / span_offset (fixed-chunk) and span_order (random-document,
         all requests' segment orders concatenated) as in cb_blend_params.
         query: anchor_rule / anchor_bp / crit_layers of the query-aware
         policies (sel_layer must then be 0)."""
         arr, keep = _requests(reqs)
         p, sch = self._params(ratio_bp, policy, sel_layer, schedule, forced, span_len,
-                              span_offset, span_order, query)
+                              span_offset, span_order, query, forced_kept)
         if outputs is None:
             plan = L.Plan()
             check(lib.cb_blend_plan(self.handle, arr, len(reqs), C.byref(p),
@@ -387,13 +386,17 @@ class BlendModel:
 
     def cb_blend_prefill_host_kv(self, reqs, ratio_bp, copy_stream, policy=0, sel_layer=1,
                                  outputs=None, stream=None, span_len=0, span_offset=0,
-                                 span_order=None, schedule=None):
+                                 span_order=None, schedule=None, host_load_ctas=0,
+                                 forced=None):
         """cb_blend_prefill with the requests' chunk caches in pinned host
         memory (HostChunkStore segments), loaded layer by layer on
-        copy_stream while earlier layers compute."""
+        copy_stream while earlier layers compute.  host_load_ctas > 0: the
+        re-position kernel reads the host caches directly with that many
+        CTAs per layer (a bandwidth-bounded load) instead of the copy
+        engines."""
         arr, keep = _requests(reqs)
-        p, sch = self._params(ratio_bp, policy, sel_layer, schedule, None, span_len,
-                              span_offset, span_order)
+        p, sch = self._params(ratio_bp, policy, sel_layer, schedule, forced, span_len,
+                              span_offset, span_order, host_load_ctas=host_load_ctas)
         if outputs is None:
             plan = L.Plan()
             check(lib.cb_blend_plan_host_kv(self.handle, arr, len(reqs), C.byref(p),
@@ -415,7 +418,9 @@ class BlendModel:
             sa[j] = L.Segment(sg.len, None if sg.k_pic is None else sg.k_pic.data_ptr(),
                               None if sg.v_pic is None else sg.v_pic.data_ptr(),
                               sg.pic_layer_stride, sg.pic_pos0)
-        n_a = sum((sg.len * ratio_bp + 9999) // 10000 for sg in segs)
+        n_anchor = C.c_int64(0)
+        check(lib.cb_anchor_count(sa, len(segs), ratio_bp, C.byref(n_anchor)))
+        n_a = n_anchor.value
         n = sum(sg.len for sg in segs)
         anchors = torch.empty(max(n_a, 1), dtype=torch.int32, device=self.device)
         scores = torch.empty(max(n, 1), dtype=torch.float32, device=self.device) if with_scores else None
@@ -426,9 +431,9 @@ class BlendModel:
                                    anchors.data_ptr(), _p(ws), ws.numel(), _s(stream)))
         return anchors[:n_a], (None if scores is None else scores[:n])
 
-    def plan_host_kv(self, reqs, ratio_bp, policy=0, sel_layer=1):
+    def plan_host_kv(self, reqs, ratio_bp, policy=0, sel_layer=1, host_load_ctas=0):
         arr, keep = _requests(reqs)
-        p, sch = self._params(ratio_bp, policy, sel_layer, None)
+        p, sch = self._params(ratio_bp, policy, sel_layer, None, host_load_ctas=host_load_ctas)
         out = L.Plan()
         check(lib.cb_blend_plan_host_kv(self.handle, arr, len(reqs), C.byref(p), C.byref(out)))
         return out
@@ -580,12 +585,17 @@ class HostChunkStore:
 
 def loading_controller(load_ms_per_layer: float, compute_ms_per_layer: dict,
                        min_ratio_bp: int = 1500) -> int:
-    """Recompute ratio that the layer-wise load hides ([CB] "Hiding
-    Recompute Behind I/O": r = max(r_load, 15%)): the largest measured ratio
-    whose per-layer recompute time does not exceed the per-layer KV load
-    time, and at least min_ratio_bp.  compute_ms_per_layer: {ratio_bp: ms}."""
-    fits = [r for r, ms in compute_ms_per_layer.items() if ms <= load_ms_per_layer]
-    return max([min_ratio_bp] + fits)
+    """cb_loading_ratio ([CB] "Hiding Recompute Behind I/O": r = max(r_load,
+    15%)): compute_ms_per_layer is {ratio_bp: measured recompute ms per
+    layer}; returns the ratio in basis points."""
+    items = sorted(compute_ms_per_layer.items())
+    n = len(items)
+    ratios = (C.c_int32 * max(1, n))(*[int(r) for r, _ in items])
+    times = (C.c_double * max(1, n))(*[float(t) for _, t in items])
+    out = C.c_int32(0)
+    check(lib.cb_loading_ratio(float(load_ms_per_layer), ratios, times, n, int(min_ratio_bp),
+                               C.byref(out)))
+    return out.value
 
 
 class RollingWindow:
@@ -649,14 +659,15 @@ class RollingWindow:
             del self.tokens[old]
 
 
-def selection_stats(selected: torch.Tensor, deviation: torch.Tensor):
+def selection_stats(selected: torch.Tensor, deviation: torch.Tensor, stream=None):
     """Diagnostics of one request's selection ("Request Order Matters" §4.4,
-    Table 2): the number of contiguous regions it occupies and the share of
-    the total deviation it carries.  selected: ascending positions; deviation:
-    d over the request's reusable tokens (host-side reporting only)."""
-    sel = selected.detach().to("cpu", torch.int64)
-    d = deviation.detach().to("cpu", torch.float64)
-    segments = 0 if sel.numel() == 0 else 1 + int((sel[1:] - sel[:-1] != 1).sum())
-    total = float(d.sum())
-    captured = float(d[sel].sum()) / total if total > 0 else 0.0
-    return segments, captured
+    Table 2), computed by cb_selection_stats: the number of contiguous
+    regions it occupies and the share of the total deviation it carries.
+    selected: ascending positions (device int32); deviation: d over the
+    request's reusable tokens (device float).  Returns host values."""
+    seg = torch.empty(1, dtype=torch.int32, device=deviation.device)
+    cap = torch.empty(1, dtype=torch.float64, device=deviation.device)
+    arr, keep = _select_reqs([dict(n_ctx=int(deviation.numel()), k=int(selected.numel()))])
+    check(lib.cb_selection_stats(_p(deviation), _p(selected), arr, 1, _p(seg), _p(cap),
+                                 _s(stream)))
+    return int(seg.item()), float(cap.item())

@@ -12,10 +12,29 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "cb_common.cuh"
 #include "cb_internal.h"
 
 using namespace cb;
+
+// NVTX range over a host scope: a profiler's timeline shows each call, and
+// each decoder layer inside it, as a named range of the enqueueing thread
+// (NVTX is inert unless a tool is attached).
+namespace {
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  NvtxRange(const char *fmt, int i) {
+    char buf[48];
+    snprintf(buf, sizeof buf, fmt, i);
+    nvtxRangePushA(buf);
+  }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange &) = delete;
+  NvtxRange &operator=(const NvtxRange &) = delete;
+};
+}  // namespace
 
 // ------------------------------------------------------------------ errors --
 static thread_local std::string g_msg;
@@ -295,6 +314,45 @@ extern "C" cb_status cb_kv_deviation_topk(const void *k_fresh, int64_t ld_fresh,
   CB_TRY(status_ptr(&st));
   return run_selection(k_fresh, ld_fresh, k_reused, ld_reused, row_elems, dtype, plan, dev_out,
                        idx_out, st, stream);
+}
+
+extern "C" cb_status cb_selection_stats(const float *dev, const int32_t *idx,
+                                        const cb_select_req *reqs, int n_req,
+                                        int32_t *segments_out, double *captured_out,
+                                        cb_stream stream) {
+  if (n_req < 0 || n_req > CB_MAX_BATCH) return fail(CB_ERR_INVALID_ARG, "n_req must be in [0, %d]", CB_MAX_BATCH);
+  if (n_req == 0) return CB_OK;
+  if (!dev || !idx || !reqs || !segments_out || !captured_out) return fail(CB_ERR_INVALID_ARG, "NULL pointer");
+  std::vector<SelReq> sr(n_req);
+  for (int i = 0; i < n_req; ++i) {
+    const cb_select_req &r = reqs[i];
+    if (r.n_ctx < 0 || r.k < 0 || r.k > r.n_ctx) return fail(CB_ERR_INVALID_ARG, "request %d: need 0 <= k <= n_ctx", i);
+    if (r.dev_offset < 0 || r.idx_offset < 0) return fail(CB_ERR_INVALID_ARG, "request %d: negative offset", i);
+    sr[i] = SelReq{r.n_ctx, r.k, 0, 0, r.dev_offset, r.idx_offset, 0, 0};
+  }
+  int *st;
+  CB_TRY(status_ptr(&st));
+  CB_CUDA(launch_selection_stats(dev, idx, sr.data(), n_req, segments_out, captured_out, st, stream));
+  return CB_OK;
+}
+
+extern "C" cb_status cb_loading_ratio(double load_ms_per_layer, const int32_t *ratio_bp,
+                                      const double *recompute_ms_per_layer, int n,
+                                      int32_t min_ratio_bp, int32_t *ratio_out) {
+  if (!ratio_out) return fail(CB_ERR_INVALID_ARG, "ratio_out is NULL");
+  if (n < 0 || (n > 0 && (!ratio_bp || !recompute_ms_per_layer)))
+    return fail(CB_ERR_INVALID_ARG, "need n >= 0 and both arrays");
+  if (min_ratio_bp < 0 || min_ratio_bp > 10000) return fail(CB_ERR_INVALID_ARG, "min_ratio_bp must be in [0, 10000]");
+  if (!(load_ms_per_layer >= 0.0)) return fail(CB_ERR_INVALID_ARG, "load time must be >= 0");
+  int32_t r = min_ratio_bp;
+  for (int i = 0; i < n; ++i) {
+    if (ratio_bp[i] < 0 || ratio_bp[i] > 10000) return fail(CB_ERR_INVALID_ARG, "ratio %d outside [0, 10000]", i);
+    if (!(recompute_ms_per_layer[i] >= 0.0)) return fail(CB_ERR_INVALID_ARG, "time %d must be >= 0", i);
+    // recompute at this ratio hides behind the load of the next layer
+    if (recompute_ms_per_layer[i] <= load_ms_per_layer && ratio_bp[i] > r) r = ratio_bp[i];
+  }
+  *ratio_out = r;
+  return CB_OK;
 }
 
 // -------------------------------------------------------- gather/scatter --
@@ -734,6 +792,8 @@ static cb_status make_plan(const cb_model *m, const cb_request *reqs, int B,
         }
       }
     }
+    if (p->host_load_ctas < 0 || p->host_load_ctas > 4096)
+      return fail(CB_ERR_INVALID_ARG, "host_load_ctas must be in [0, 4096]");
     if (p->policy == CB_POLICY_RANDOM_DOC && !p->span_order)
       return fail(CB_ERR_INVALID_ARG, "random-document needs span_order");
     if (p->policy == CB_POLICY_FIXED_CHUNK &&
@@ -877,7 +937,7 @@ static cb_status make_plan(const cb_model *m, const cb_request *reqs, int B,
     P.qp_mass_bytes = mass;
     P.qp_mass = cv.take(mass);
   }
-  if (host_kv) {
+  if (host_kv && p->host_load_ctas == 0) {
     P.stage_bytes = (size_t)(P.N_total + 1) * m->kvw * m->eb;
     P.stage_bytes = (P.stage_bytes + 255) / 256 * 256;
     P.stage = cv.take(4 * P.stage_bytes);         // [buffer][K, V]
@@ -925,6 +985,7 @@ static cb_status layer_forward(cb_model *m, int l, float *h, int n, const int32_
                                void *kc, void *vc, const LayerScratch &S, int *st,
                                cudaStream_t s, const int *attn_plan = nullptr,
                                const int32_t *attn_pos = nullptr) {
+  const NvtxRange range("layer %d", l);
   const cb_model_config &c = m->cfg;
   const cb_layer_weights &L = m->layers[l];
   const int d = c.d_model, F = c.d_ffn, hd = c.head_dim;
@@ -1045,7 +1106,7 @@ static cb_status filter_rows(cb_model *m, int l, const BatchMeta &cur, const Bat
                              int32_t *pos_n, int32_t *glob_n, int32_t *sel_n, int R_cur,
                              char *ws, const Plan &P, const LayerScratch &S,
                              const cb_blend_out *out, int64_t lstride, int *st,
-                             cudaStream_t s) {
+                             cudaStream_t s, const int32_t *forced = nullptr) {
   const cb_model_config &c = m->cfg;
   const cb_layer_weights &Lw = m->layers[l];
   const int d = c.d_model, B = cur.B;
@@ -1053,6 +1114,13 @@ static cb_status filter_rows(cb_model *m, int l, const BatchMeta &cur, const Bat
   float *dp = (float *)(ws + P.g_dev);
   int32_t *keep = (int32_t *)(ws + P.g_keep);
   int32_t *src = (int32_t *)(ws + P.g_src);
+  if (forced) {
+    // the caller gives the kept positions: no ranking at this step
+    CB_CUDA(launch_keep_from_positions(cur, nxt, forced, sel, keep, nxt.k_off[B], st, s));
+    CB_CUDA(launch_filter_rows(cur, nxt, keep, sel, sel_n, pos_n, glob_n, src, R_nxt, st, s));
+    CB_CUDA(launch_gather(h, d, R_cur, src, R_nxt, d, h_n, d, sizeof(float), st, s));
+    return CB_OK;
+  }
   CB_CUDA(launch_rmsnorm(h, d, nullptr, R_cur, d, Lw.norm1, c.norm_eps, S.x, d, c.dtype, s));
   const char *wk = (const char *)Lw.w_qkv + (int64_t)m->qw * d * m->eb;
   CB_TRY(run_linear(m, S.x, d, wk, nullptr, d, R_cur, m->kvw, d, EPI_STORE_F32, S.qkv32,
@@ -1160,6 +1228,20 @@ static cb_status query_probe(cb_model *m, const cb_request *reqs, int B,
   return CB_OK;
 }
 
+extern "C" cb_status cb_anchor_count(const cb_segment *chunks, int n_chunks, int ratio_bp,
+                                     int64_t *n_anchors) {
+  if (!n_anchors || (n_chunks > 0 && !chunks) || n_chunks < 0)
+    return fail(CB_ERR_INVALID_ARG, "NULL pointer or n_chunks < 0");
+  if (ratio_bp < 0 || ratio_bp > 10000) return fail(CB_ERR_INVALID_ARG, "ratio_bp must be in [0, 10000]");
+  int64_t total = 0;
+  for (int i = 0; i < n_chunks; ++i) {
+    if (chunks[i].len < 0) return fail(CB_ERR_INVALID_ARG, "chunk %d: len < 0", i);
+    total += ((int64_t)chunks[i].len * ratio_bp + 9999) / 10000;
+  }
+  *n_anchors = total;
+  return CB_OK;
+}
+
 extern "C" size_t cb_anchor_workspace_size(const cb_model *m, const cb_segment *chunks,
                                            int n_chunks) {
   if (!m || !chunks || n_chunks <= 0) return 256;
@@ -1205,6 +1287,7 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
                             const cb_blend_params *p, const cb_blend_out *out, void *ws_v,
                             size_t ws_bytes, cudaStream_t stream, bool host_kv,
                             cudaStream_t copy_stream) {
+  const NvtxRange range(host_kv ? "cb_blend_prefill_host_kv" : "cb_blend_prefill");
   Plan P;
   CB_TRY(make_plan(m, reqs, B, p, true, P, host_kv));
   CB_TRY(check_out(m, out));
@@ -1241,8 +1324,21 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
   const size_t sb = P.stage_bytes;
   auto stage_k = [&](int l) { return ws + P.stage + (size_t)(l & 1) * 2 * sb; };
   auto stage_v = [&](int l) { return ws + P.stage + (size_t)(l & 1) * 2 * sb + sb; };
+  const int zc_ctas = host_kv ? p->host_load_ctas : 0;
   auto issue_copies = [&](int l) -> cb_status {
+    if (zc_ctas > 0) {
+      // zero-copy: the re-position kernel reads layer l of the pinned chunk
+      // caches itself, with a capped grid, straight into the fused cache
+      probe_mark(CB_PROBE_STITCH, true, copy_stream);
+      CB_CUDA(launch_reposition(descs.data(), (int)descs.size(), l, l + 1, out->k_cache,
+                                out->v_cache, lstride, m->kvw, c.head_dim, m->w.rope_table,
+                                c.dtype, st, copy_stream, zc_ctas));
+      probe_mark(CB_PROBE_STITCH, false, copy_stream);
+      CB_CUDA(cudaEventRecord(m->ev_copied[l & 1], copy_stream));
+      return CB_OK;
+    }
     CB_CUDA(cudaStreamWaitEvent(copy_stream, m->ev_free[l & 1], 0));
+    probe_mark(CB_PROBE_STITCH, true, copy_stream);
     for (int b = 0; b < B; ++b)
       for (int i = 0; i < reqs[b].n_segments; ++i) {
         const cb_segment &sg = reqs[b].segments[i];
@@ -1255,10 +1351,15 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
         CB_CUDA(cudaMemcpyAsync(stage_v(l) + off, (const char *)sg.v_pic + src, bytes,
                                 cudaMemcpyHostToDevice, copy_stream));
       }
+    probe_mark(CB_PROBE_STITCH, false, copy_stream);
     CB_CUDA(cudaEventRecord(m->ev_copied[l & 1], copy_stream));
     return CB_OK;
   };
   auto stitch_layer = [&](int l) -> cb_status {
+    if (zc_ctas > 0) {
+      CB_CUDA(cudaStreamWaitEvent(s, m->ev_copied[l & 1], 0));
+      return CB_OK;
+    }
     std::vector<cb_stitch_desc> ld;
     for (int b = 0; b < B; ++b)
       for (int i = 0; i < reqs[b].n_segments; ++i) {
@@ -1392,6 +1493,7 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
   BatchMeta bm = P.bm;
   int R_cur = (int)P.R_total;
   size_t next_step = 0;
+  int64_t forced_at = 0;    // this step's part of p->forced_kept
   std::vector<AttnReq> ar_c(B);
   // the compact layers' attention units, planned from the rows' positions
   // whenever the set changes (its first layer, each filtering step)
@@ -1406,7 +1508,9 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
       const Plan::Step &stp = P.sched[next_step++];
       CB_TRY(filter_rows(m, l, bm, stp.bm, (int)stp.R_total, h_b[cur], pos_b[cur], glob_b[cur],
                          sel_b[cur], h_b[cur ^ 1], pos_b[cur ^ 1], glob_b[cur ^ 1],
-                         sel_b[cur ^ 1], R_cur, ws, P, S, out, lstride, st, s));
+                         sel_b[cur ^ 1], R_cur, ws, P, S, out, lstride, st, s,
+                         p->forced_kept ? p->forced_kept + forced_at : nullptr));
+      forced_at += stp.K_total;
       cur ^= 1;
       bm = stp.bm;
       R_cur = (int)stp.R_total;
@@ -1501,6 +1605,8 @@ std::vector<uint8_t> call_key(const cb_model *m, const cb_request *reqs, int B,
   if (p->span_order)
     for (int i = 0; i < n_cached; ++i) k.put(p->span_order[i]);
   k.put(p->forced_selected);
+  k.put(p->forced_kept);
+  k.put(p->host_load_ctas);
   k.put(p->anchor_rule);
   k.put(p->anchor_bp);
   k.put(p->n_crit);
@@ -1538,6 +1644,7 @@ extern "C" cb_status cb_blend_prefill(cb_model *m, const cb_request *reqs, int B
   std::lock_guard<std::mutex> lk(m->graph_mu);
   for (CallGraph &g : m->graphs)
     if (g.key == key) {
+      const NvtxRange range("cb_blend_prefill (recorded call)");
       g.used = ++m->graph_clock;
       CB_CUDA(cudaGraphLaunch(g.exec, stream));
       g_launches.fetch_add(g.launches);
@@ -1610,6 +1717,10 @@ extern "C" cb_status cb_blend_prefill_host_kv(cb_model *m, const cb_request *req
         cudaPointerAttributes a;
         if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess || a.type != cudaMemoryTypeHost)
           return fail(CB_ERR_INVALID_ARG, "request %d segment %d: chunk caches must be pinned host memory", b, i);
+        // the zero-copy load dereferences the host pointer in a kernel: it
+        // must be the allocation's device address as well (unified addressing)
+        if (p && p->host_load_ctas > 0 && a.devicePointer != ptr)
+          return fail(CB_ERR_INVALID_ARG, "request %d segment %d: chunk cache is not mapped at the same device address (zero-copy load)", b, i);
       }
     }
   return blend_impl(m, reqs, B, p, out, ws, ws_bytes, stream, true, copy_stream);
@@ -1618,6 +1729,7 @@ extern "C" cb_status cb_blend_prefill_host_kv(cb_model *m, const cb_request *req
 extern "C" cb_status cb_full_prefill(cb_model *m, const cb_request *reqs, int B,
                                      const cb_blend_out *out, void *ws_v, size_t ws_bytes,
                                      cb_stream stream) {
+  const NvtxRange range("cb_full_prefill");
   Plan P;
   CB_TRY(make_plan(m, reqs, B, nullptr, false, P));
   CB_TRY(check_out(m, out));

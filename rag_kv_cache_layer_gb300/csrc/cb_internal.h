@@ -94,11 +94,14 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
 // ----------------------------------------------------------------- RoPE --
 cudaError_t launch_rope_table(float *table, int max_pos, int head_dim,
                               float base, cudaStream_t s);
+// max_blocks > 0 caps the grid's x extent (a bandwidth-bounded zero-copy
+// load when the sources are pinned host memory).
 cudaError_t launch_reposition(const cb_stitch_desc *descs, int n_desc,
                               int layer_begin, int layer_end, void *k_cache,
                               void *v_cache, int64_t cache_layer_stride,
                               int row_elems, int head_dim, const float *table,
-                              cb_dtype dt, int *status, cudaStream_t s);
+                              cb_dtype dt, int *status, cudaStream_t s,
+                              int max_blocks = 0);
 
 // ------------------------------------------------------------ selection --
 struct SelReq {
@@ -140,8 +143,19 @@ cudaError_t launch_filter_rows(const BatchMeta &cur, const BatchMeta &nxt,
                                const int32_t *keep, const int32_t *sel_cur,
                                int32_t *sel_nxt, int32_t *pos, int32_t *glob,
                                int32_t *src, int n_rows, int *status, cudaStream_t s);
+// The keep indices of a gradual step whose kept positions are given:
+// forced holds each request's k'_b positions at nxt.k_off[b], a subset of
+// its current selection sel_cur (cur.k_off[b] ..).
+cudaError_t launch_keep_from_positions(const BatchMeta &cur, const BatchMeta &nxt,
+                                       const int32_t *forced, const int32_t *sel_cur,
+                                       int32_t *keep, int n_keep, int *status, cudaStream_t s);
 cudaError_t launch_iota_rows(const BatchMeta &bm, int32_t *pos, int32_t *glob,
                              int n_rows, cudaStream_t s);
+// Per request: contiguous regions of its selection and the share of its
+// deviation the selection carries (Table 2 diagnostics).
+cudaError_t launch_selection_stats(const float *dev, const int32_t *idx, const SelReq *reqs,
+                                   int n_req, int32_t *segments, double *captured, int *status,
+                                   cudaStream_t s);
 
 // ----------------------------------------------------------------- rows --
 cudaError_t launch_embed(const int32_t *const *tokens, const BatchMeta &bm,

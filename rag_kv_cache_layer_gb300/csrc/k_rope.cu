@@ -126,7 +126,7 @@ cudaError_t launch_reposition(const cb_stitch_desc *descs, int n_desc,
                               int layer_begin, int layer_end, void *k_cache,
                               void *v_cache, int64_t cache_layer_stride,
                               int row_elems, int head_dim, const float *table,
-                              cb_dtype dt, int *status, cudaStream_t s) {
+                              cb_dtype dt, int *status, cudaStream_t s, int max_blocks) {
   if (layer_end <= layer_begin) return cudaSuccess;
   for (int base = 0; base < n_desc; base += kMaxStitch) {
     StitchParams p;
@@ -142,6 +142,7 @@ cudaError_t launch_reposition(const cb_stitch_desc *descs, int n_desc,
     const int64_t units = (int64_t)rows * (row_elems / (2 * vec) + row_elems / vec);
     int64_t blocks = (units + 255) / 256;
     if (blocks > 65535) blocks = 65535;
+    if (max_blocks > 0 && blocks > max_blocks) blocks = max_blocks;
     dim3 grid((unsigned)blocks, (unsigned)(layer_end - layer_begin));
     const float2 *tab = reinterpret_cast<const float2 *>(table);
     if (dt == CB_BF16)

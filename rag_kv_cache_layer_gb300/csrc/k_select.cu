@@ -575,6 +575,99 @@ cudaError_t launch_filter_rows(const BatchMeta &cur, const BatchMeta &nxt,
   return launched(1);
 }
 
+// A gradual step whose kept rows are given (cb_blend_params.forced_kept):
+// request b's k'_b positions forced[nxt.k_off[b] ..] become indices into its
+// current selection sel_cur (ascending, so a binary search finds them),
+// which is the form filter_rows_kernel takes.  A position that is not
+// selected, or not above the previous one, records CB_ERR_DEVICE_INDEX.
+__global__ void keep_from_positions_kernel(const __grid_constant__ BatchMeta cur,
+                                           const __grid_constant__ BatchMeta nxt,
+                                           const int32_t *__restrict__ forced,
+                                           const int32_t *__restrict__ sel_cur,
+                                           int32_t *__restrict__ keep, int n_keep,
+                                           int *status) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= n_keep) return;
+  int b = 0;
+  while (nxt.k_off[b + 1] <= r) ++b;
+  const int p = forced[r];
+  const int32_t *sel = sel_cur + cur.k_off[b];
+  int lo = 0, hi = cur.k_off[b + 1] - cur.k_off[b];
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (sel[mid] < p) lo = mid + 1; else hi = mid;
+  }
+  const bool found = lo < cur.k_off[b + 1] - cur.k_off[b] && sel[lo] == p;
+  const bool ordered = r == nxt.k_off[b] || forced[r - 1] < p;
+  if (!found || !ordered) {
+    report(status, CB_ERR_DEVICE_INDEX);
+    lo = 0;
+  }
+  keep[r] = lo;
+}
+
+cudaError_t launch_keep_from_positions(const BatchMeta &cur, const BatchMeta &nxt,
+                                       const int32_t *forced, const int32_t *sel_cur,
+                                       int32_t *keep, int n_keep, int *status, cudaStream_t s) {
+  if (n_keep == 0) return cudaSuccess;
+  keep_from_positions_kernel<<<(n_keep + 255) / 256, 256, 0, s>>>(cur, nxt, forced, sel_cur, keep,
+                                                                  n_keep, status);
+  return launched(1);
+}
+
+// Table 2 diagnostics of "Request Order Matters" §4.4, one CTA per request:
+// segments = maximal runs of consecutive selected positions (the number of
+// j with j == 0 or idx[j] != idx[j-1] + 1), captured = sum of d over the
+// selection / sum of d over the request, both sums in double in a fixed
+// order (per-thread strides, then a fixed tree), so results are
+// deterministic.
+__global__ void __launch_bounds__(256)
+selection_stats_kernel(const __grid_constant__ SelParams p, const float *__restrict__ dev,
+                       const int32_t *__restrict__ idx, int32_t *__restrict__ segments,
+                       double *__restrict__ captured, int *status) {
+  __shared__ double s_tot[8], s_sel[8];
+  __shared__ int s_seg[8];
+  const SelReq &q = p.r[blockIdx.x];
+  const float *d = dev + q.dev_offset;
+  const int32_t *sel = idx + q.idx_offset;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  double tot = 0.0, got = 0.0;
+  int seg = 0;
+  for (int i = tid; i < q.n_ctx; i += blockDim.x) tot += (double)__ldg(d + i);
+  for (int j = tid; j < q.k; j += blockDim.x) {
+    const int t = sel[j];
+    if (t < 0 || t >= q.n_ctx) {
+      report(status, CB_ERR_DEVICE_INDEX);
+      continue;
+    }
+    got += (double)__ldg(d + t);
+    seg += (j == 0 || sel[j - 1] + 1 != t) ? 1 : 0;
+  }
+  tot = warp_sum_d(tot);
+  got = warp_sum_d(got);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) seg += __shfl_xor_sync(0xffffffffu, seg, o);
+  if (lane == 0) { s_tot[w] = tot; s_sel[w] = got; s_seg[w] = seg; }
+  __syncthreads();
+  if (tid == 0) {
+    double a = 0.0, b = 0.0;
+    int c = 0;
+    for (int i = 0; i < 8; ++i) { a += s_tot[i]; b += s_sel[i]; c += s_seg[i]; }
+    segments[blockIdx.x] = c;
+    captured[blockIdx.x] = a > 0.0 ? b / a : 0.0;
+  }
+}
+
+cudaError_t launch_selection_stats(const float *dev, const int32_t *idx, const SelReq *reqs,
+                                   int n_req, int32_t *segments, double *captured, int *status,
+                                   cudaStream_t s) {
+  if (n_req == 0) return cudaSuccess;
+  SelParams p;
+  fill_params(p, reqs, n_req);
+  selection_stats_kernel<<<n_req, 256, 0, s>>>(p, dev, idx, segments, captured, status);
+  return launched(1);
+}
+
 __global__ void iota_rows_kernel(const __grid_constant__ BatchMeta bm,
                                  int32_t *__restrict__ pos,
                                  int32_t *__restrict__ glob, int n_rows) {

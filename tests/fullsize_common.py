@@ -90,3 +90,96 @@ def check_request(ref, k_cache, v_cache, deviation, selected, extra_rows=()):
     assert rms_rel(f64(k_cache[1][ix]), k_ref) <= TOL
     assert rms_rel(f64(v_cache[1][ix]), v_ref) <= TOL
     return d_gpu, chosen
+
+
+class DeviceLayers:
+    """The oracle's per-layer weights, read as float64 from the device tensors
+    the GPU runs on (the seeded generator's values), one layer at a time: the
+    oracle walks the layers in order, so holding the last layer read keeps
+    host memory to one layer (1.75 GB in float64 for the Llama shape)."""
+
+    KEYS = ("w_qkv", "w_o", "w_gate", "w_up", "w_down", "norm1", "norm2")
+
+    def __init__(self, dev_layers):
+        self.dev = dev_layers
+        self.at, self.cur = None, None
+        self.reads = 0
+
+    def __len__(self):
+        return len(self.dev)
+
+    def __getitem__(self, l):
+        if l != self.at:
+            self.cur = {k: self.dev[l][k].double().cpu().numpy() for k in self.KEYS}
+            self.at = l
+            self.reads += 1
+        return self.cur
+
+
+class DeviceEmbedding:
+    """The embedding table as float64 rows fetched on demand (a token list or
+    a block of rows); the oracle widens rows where it uses them."""
+
+    def __init__(self, t):
+        self.t = t
+        self.shape = tuple(t.shape)
+
+    def __getitem__(self, idx):
+        if isinstance(idx, slice):
+            return self.t[idx].double().cpu().numpy()
+        ix = np.asarray(idx)
+        rows = torch.from_numpy(ix.reshape(-1).astype(np.int64)).to(self.t.device)
+        return self.t.index_select(0, rows).double().cpu().numpy().reshape(*ix.shape, -1)
+
+
+def oracle_model_full(shape, dev_weights):
+    """The whole float64 oracle model over the device weights, layers and
+    embedding read on demand."""
+    return O.Model(shape.n_layers, shape.d_model, shape.n_q_heads, shape.n_kv_heads,
+                   shape.head_dim, shape.d_ffn, shape.vocab, shape.rope_base, shape.norm_eps,
+                   DeviceEmbedding(dev_weights["embed"]),
+                   dev_weights["final_norm"].double().cpu().numpy(),
+                   DeviceLayers(dev_weights["layers"]))
+
+
+def plain_bf16_prefill(shape, dev_weights, tokens):
+    """A plain PyTorch bf16 prefill of one standalone token run (positions
+    0..n-1): F.linear on bf16 operands, scaled_dot_product_attention in bf16,
+    the residual stream in fp32.  It is not the oracle: it measures the
+    accumulated rounding of an ordinary bf16 datapath on this model, the
+    floor any bf16 implementation is held against at depth.  Returns the
+    per-layer K and V rows as float64 numpy [n_layers][n][Hkv*hd]."""
+    import torch.nn.functional as F
+    dev = dev_weights["embed"].device
+    toks = torch.from_numpy(np.asarray(tokens, np.int64)).to(dev)
+    n, hd = len(tokens), shape.head_dim
+    Hq, Hkv = shape.n_q_heads, shape.n_kv_heads
+    inv = shape.rope_base ** (-torch.arange(hd // 2, dtype=torch.float64, device=dev) * 2 / hd)
+    ang = torch.arange(n, dtype=torch.float64, device=dev)[:, None] * inv[None]
+    cos, sin = torch.cos(ang).float()[:, None], torch.sin(ang).float()[:, None]
+
+    def rope(x):
+        a, b = x[..., :hd // 2], x[..., hd // 2:]
+        return torch.cat([a * cos - b * sin, b * cos + a * sin], -1)
+
+    def norm(h, g):
+        return (h / torch.sqrt((h * h).mean(-1, keepdim=True) + shape.norm_eps) * g).to(torch.bfloat16)
+
+    Ks, Vs = [], []
+    with torch.no_grad():
+        h = dev_weights["embed"][toks].float()
+        for L in dev_weights["layers"]:
+            qkv = F.linear(norm(h, L["norm1"]), L["w_qkv"]).float()
+            q = rope(qkv[:, :Hq * hd].reshape(n, Hq, hd)).to(torch.bfloat16)
+            k = rope(qkv[:, Hq * hd:(Hq + Hkv) * hd].reshape(n, Hkv, hd)).to(torch.bfloat16)
+            v = qkv[:, (Hq + Hkv) * hd:].reshape(n, Hkv, hd).to(torch.bfloat16)
+            Ks.append(k.reshape(n, -1).double().cpu().numpy())
+            Vs.append(v.reshape(n, -1).double().cpu().numpy())
+            o = F.scaled_dot_product_attention(q.transpose(0, 1)[None], k.transpose(0, 1)[None],
+                                               v.transpose(0, 1)[None], is_causal=True,
+                                               enable_gqa=True)[0].transpose(0, 1)
+            h = h + F.linear(o.reshape(n, -1), L["w_o"]).float()
+            x = norm(h, L["norm2"])
+            g = F.silu(F.linear(x, L["w_gate"]).float()) * F.linear(x, L["w_up"]).float()
+            h = h + F.linear(g.to(torch.bfloat16), L["w_down"]).float()
+    return np.stack(Ks), np.stack(Vs)

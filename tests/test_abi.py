@@ -49,7 +49,8 @@ STRUCTS = {
     "cb_blend_params": (L.BlendParams, ["ratio_bp", "policy", "sel_layer", "n_schedule",
                                         "schedule", "span_len", "span_offset", "span_order",
                                         "forced_selected", "anchor_rule", "anchor_bp",
-                                        "n_crit", "crit_layers"]),
+                                        "n_crit", "crit_layers", "forced_kept",
+                                        "host_load_ctas"]),
     "cb_blend_out": (L.BlendOut, ["k_cache", "v_cache", "cache_layer_stride", "deviation",
                                   "selected", "hidden", "rows", "first_token"]),
     "cb_plan": (L.Plan, ["T_total", "N_total", "K_total", "R_total", "workspace_bytes",
@@ -141,7 +142,32 @@ def test_span_policy_requests_are_validated_on_the_host():
         assert lib.cb_last_error_message()
 
 
-def test_select_count_matches_page_rule():
-    assert R.select_count(3072, 1500) == 460
-    assert R.select_count(100, 0) == 0
-    assert R.select_count(10, 1) == 1
+def test_loading_controller_rule():
+    """[CB] "Hiding Recompute Behind I/O": r = max(r_load, 15%), r_load the
+    largest measured ratio whose per-layer recompute fits in the per-layer
+    load (host-only call)."""
+    table = {500: 0.2, 1500: 0.25, 3000: 0.4, 5000: 0.6, 10000: 1.1}
+    assert R.loading_controller(0.07, table) == 1500        # every load hides: the floor
+    assert R.loading_controller(0.45, table) == 3000
+    assert R.loading_controller(0.6, table) == 5000          # equal time still hides
+    assert R.loading_controller(2.6, table) == 10000         # slow storage: recompute all
+    assert R.loading_controller(0.45, table, min_ratio_bp=5000) == 5000
+    import ctypes as C
+    out = C.c_int32(0)
+    bad = (C.c_int32 * 1)(10001)
+    t = (C.c_double * 1)(0.1)
+    assert L.lib.cb_loading_ratio(1.0, bad, t, 1, 1500, C.byref(out)) == L.CB_ERR_INVALID_ARG
+    assert L.lib.cb_loading_ratio(float("nan"), None, None, 0, 1500, C.byref(out)) == L.CB_ERR_INVALID_ARG
+
+
+def test_anchor_count_is_the_ceiling_per_chunk():
+    """QCFuse Eq. 14: ceil(r_a |c_i|) anchors per chunk (host-only call)."""
+    import ctypes as C
+    segs = (L.Segment * 3)(L.Segment(512, None, None, 0, 0), L.Segment(7, None, None, 0, 0),
+                           L.Segment(0, None, None, 0, 0))
+    n = C.c_int64(0)
+    L.check(L.lib.cb_anchor_count(segs, 3, 1000, C.byref(n)))
+    assert n.value == 52 + 1 + 0
+    L.check(L.lib.cb_anchor_count(segs, 3, 10000, C.byref(n)))
+    assert n.value == 519
+    assert L.lib.cb_anchor_count(segs, 3, 10001, C.byref(n)) == L.CB_ERR_INVALID_ARG

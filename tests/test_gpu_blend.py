@@ -7,7 +7,10 @@ CUDA path against the CPU oracle, on the seeded workloads:
 * a Llama-3-8B-shaped bf16 stack truncated to 2 layers: the oracle's
   selection is imposed on the GPU (forced P) and blended K/V and hidden
   states are compared at 2e-2 RMS-relative; the GPU's own ranking is checked
-  bit-exactly against a sort of its own deviations.
+  bit-exactly against a sort of its own deviations;
+* the same stack at 4 layers with a gradual schedule: the oracle's layer-1
+  selection and per-step kept rows imposed on the GPU, every layer's K/V
+  and the final hidden states at 2e-2.
 """
 import numpy as np
 import pytest
@@ -124,7 +127,8 @@ def test_blend_endpoints(tiny):
 def test_unselected_rows_keep_reused_cache_exactly(tiny):
     rq = tiny.wl.requests[0]
     out = tiny.model.cb_blend_prefill(tiny.gpu_reqs(), 1500)
-    k = R.select_count(rq.n_ctx, 1500)
+    k = int(tiny.model.plan(tiny.gpu_reqs(), 1500).K_total)
+    assert k == O.select_count(rq.n_ctx, 1500)
     sel = out["selected"][:k].cpu().numpy()
     # the stitched cache through the primitive, on its own
     kvw = tiny.model.kvw
@@ -154,7 +158,7 @@ def test_forced_selection_and_doc_aligned(tiny):
     assert_close(host(out["k_cache"]), ref.K, torch.float32)
     assert_close(host(out["hidden"][:len(ref.rows)]), ref.hidden, torch.float32)
     # document-aligned spans (each cached chunk is a document)
-    k = R.select_count(rq.n_ctx, 1500)
+    k = int(tiny.model.plan(tiny.gpu_reqs(), 1500).K_total)
     out = tiny.model.cb_blend_prefill(tiny.gpu_reqs(), 1500, policy=L.CB_POLICY_DOC_ALIGNED)
     d = out["deviation"][:rq.n_ctx].cpu().numpy().astype(np.float64)
     sel = out["selected"][:k].cpu().numpy()
@@ -173,7 +177,7 @@ def test_batch_of_requests_is_independent(tiny):
     out = tiny.model.cb_blend_prefill(tiny.gpu_reqs([rq, alt]), 1500)
     single = tiny.model.cb_blend_prefill(tiny.gpu_reqs([alt]), 1500)
     T = rq.n_tokens
-    k = R.select_count(rq.n_ctx, 1500)
+    k = int(tiny.model.plan(tiny.gpu_reqs([alt]), 1500).K_total)
     assert torch.equal(out["selected"][k:2 * k], single["selected"][:k])
     assert_close(host(out["k_cache"][:, T:2 * T]), host(single["k_cache"][:, :T]), torch.float32)
     ref = tiny.oracle_blend(alt, 1500)
@@ -230,6 +234,52 @@ def test_bf16_llama_truncated_free_selection(llama2, llama2_ref):
     jac = len(set(sel) & set(ref.selected)) / len(set(sel) | set(ref.selected))
     print(f"bf16 free-selection Jaccard vs oracle: {jac:.3f}")
     assert jac > 0.5
+
+
+@pytest.fixture(scope="module")
+def llama4():
+    wl = W.llama_rag(n_layers=4, n_chunks=2, chunk_len=256, n_query=64)
+    return Setup(wl, max_pos=4096)
+
+
+def test_bf16_gradual_schedule_forced_matches_oracle(llama4):
+    """Gradual filtering (CacheBlend blog, select_hkvd) in bf16: the oracle
+    ranks every step itself (float64); its layer-1 selection and the rows
+    each step keeps are imposed on the GPU (forced, forced_kept), which then
+    recomputes the same rows at every layer."""
+    rq = llama4.wl.requests[0]
+    sch = [(2, 100), (3, 60)]
+    ref = llama4.oracle_blend(rq, 3000, schedule=sch)
+    P1, P2, P3 = (ref.selected_per_layer[l] for l in (1, 2, 3))
+    assert len(P1) == O.select_count(rq.n_ctx, 3000) > 100 and len(P2) == 100 and len(P3) == 60
+    as_dev = lambda a: torch.from_numpy(np.asarray(a, np.int32)).cuda()
+    out = llama4.model.cb_blend_prefill(llama4.gpu_reqs(), 3000, schedule=sch,
+                                        forced=as_dev(P1),
+                                        forced_kept=as_dev(np.concatenate([P2, P3])))
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    for l in range(4):
+        assert rms_rel(host(out["k_cache"][l]), ref.K[l]) <= 2e-2, l
+        assert rms_rel(host(out["v_cache"][l]), ref.V[l]) <= 2e-2, l
+    Rn = len(ref.rows)
+    assert np.array_equal(out["rows"][:Rn].cpu().numpy(), ref.rows)
+    assert np.array_equal(out["selected"][:len(P3)].cpu().numpy(), P3)
+    assert rms_rel(host(out["hidden"][:Rn]), ref.hidden) <= 2e-2
+
+
+def test_forced_kept_position_outside_the_selection_is_recorded(llama4):
+    # the kernel's own check turns a kept position that was not selected
+    # into CB_ERR_DEVICE_INDEX (and reads index 0 instead)
+    rq = llama4.wl.requests[0]
+    sch = [(2, 4)]
+    P1 = np.arange(0, 2 * O.select_count(rq.n_ctx, 1000), 2, dtype=np.int32)
+    kept = np.array([P1[0], P1[1], P1[2] + 1, P1[3]], dtype=np.int32)   # one odd position
+    llama4.model.cb_blend_prefill(llama4.gpu_reqs(), 1000, schedule=sch,
+                                  forced=torch.from_numpy(P1).cuda(),
+                                  forced_kept=torch.from_numpy(kept).cuda())
+    torch.cuda.synchronize()
+    assert R.device_status() == L.CB_ERR_DEVICE_INDEX
+    assert R.device_status() == 0
 
 
 def test_blend_replays_from_a_cuda_graph(tiny, llama2):
@@ -383,37 +433,76 @@ def test_span_policies_in_blend_match_oracle(tiny, name, policy, kw):
 
 
 # ------------------------------------------- host-resident chunk caches --
-def test_host_resident_chunks_match_device_store(tiny):
-    """[CB] "Hiding Recompute Behind I/O": the chunk caches stay in pinned
-    host memory and are loaded layer by layer on a second stream; the fused
-    cache, selection and hidden states equal the device-resident blend bit
-    for bit (the fp32 path is deterministic), also when replayed from a CUDA
-    graph."""
-    rq = tiny.wl.requests[0]
-    hs = R.HostChunkStore(tiny.model, sum(len(sg.tokens) for sg in rq.segments if sg.cached))
+def _host_store(setup):
+    rq = setup.wl.requests[0]
+    hs = R.HostChunkStore(setup.model, sum(len(sg.tokens) for sg in rq.segments if sg.cached))
     hs.prefill({sg.chunk_id: torch.from_numpy(sg.tokens).cuda() for sg in rq.segments if sg.cached})
     toks = torch.from_numpy(rq.tokens).cuda()
     hreq = [R.Req(toks, [hs.seg(sg.chunk_id) if sg.cached else R.Seg(len(sg.tokens))
                          for sg in rq.segments])]
-    ref = tiny.model.cb_blend_prefill(tiny.gpu_reqs(), 1500)
+    return hs, hreq
+
+
+@pytest.mark.parametrize("ctas", [0, 2], ids=["copy_engines", "zero_copy_2_ctas"])
+def test_host_resident_chunks_match_oracle(tiny, ctas):
+    """[CB] "Hiding Recompute Behind I/O": the chunk caches stay in pinned
+    host memory and are loaded layer by layer on a second stream -- by the
+    copy engines into a staging area, or (ctas > 0) read directly by a
+    re-position kernel of that many CTAs.  Against the oracle: K/V of every
+    layer and hidden states within 1e-4, selection up to deviation ties; and
+    equal bit for bit to the device-resident blend (the fp32 path is
+    deterministic), also when replayed from a CUDA graph."""
+    rq = tiny.wl.requests[0]
+    hs, hreq = _host_store(tiny)
     cs = torch.cuda.Stream()
-    out = tiny.model.cb_blend_prefill_host_kv(hreq, 1500, cs)
+    out = tiny.model.cb_blend_prefill_host_kv(hreq, 1500, cs, host_load_ctas=ctas)
     torch.cuda.synchronize()
     assert R.device_status() == 0
+    oref = tiny.oracle_blend(rq, 1500)
+    k = len(oref.selected)
+    sel = out["selected"][:k].cpu().numpy()
+    assert ties_ok(sel, oref.selected, oref.deviation, k)
+    if set(sel) == set(oref.selected):
+        assert_close(host(out["k_cache"]), oref.K, torch.float32)
+        assert_close(host(out["v_cache"]), oref.V, torch.float32)
+        assert_close(host(out["hidden"][:len(oref.rows)]), oref.hidden, torch.float32)
+    assert_close(host(out["deviation"][:rq.n_ctx]), oref.deviation, torch.float32)
+    ref = tiny.model.cb_blend_prefill(tiny.gpu_reqs(), 1500)
+    torch.cuda.synchronize()
     for key in ("k_cache", "v_cache", "selected", "deviation", "rows", "first_token"):
         assert torch.equal(out[key], ref[key]), key
-    Rn = int((ref["rows"] >= 0).sum())
+    Rn = len(oref.rows)
     assert torch.equal(out["hidden"][:Rn], ref["hidden"][:Rn])
     # CUDA graph: both streams are captured through the fork / join events
     outs = {k: torch.empty_like(v) for k, v in out.items()}
-    tiny.model.cb_blend_prefill_host_kv(hreq, 1500, cs, outputs=outs)
+    tiny.model.cb_blend_prefill_host_kv(hreq, 1500, cs, outputs=outs, host_load_ctas=ctas)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        tiny.model.cb_blend_prefill_host_kv(hreq, 1500, cs, outputs=outs)
+        tiny.model.cb_blend_prefill_host_kv(hreq, 1500, cs, outputs=outs, host_load_ctas=ctas)
     outs["k_cache"].zero_()
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(outs["k_cache"], ref["k_cache"])
+
+
+@pytest.mark.parametrize("ctas", [0, 4], ids=["copy_engines", "zero_copy_4_ctas"])
+def test_host_resident_bf16_forced_matches_oracle(llama2, llama2_ref, ctas):
+    """The host-resident path on the bf16 Llama-shaped stack with the
+    oracle's selection imposed: every layer's K/V and the hidden states
+    within 2e-2 of the oracle."""
+    ref = llama2_ref
+    hs, hreq = _host_store(llama2)
+    forced = torch.from_numpy(ref.selected.astype(np.int32)).cuda()
+    cs = torch.cuda.Stream()
+    outs = llama2.model.cb_blend_prefill_host_kv(hreq, 1500, cs, forced=forced,
+                                                 host_load_ctas=ctas)
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    for l in range(2):
+        assert rms_rel(host(outs["k_cache"][l]), ref.K[l]) <= 2e-2
+        assert rms_rel(host(outs["v_cache"][l]), ref.V[l]) <= 2e-2
+    Rn = len(ref.rows)
+    assert rms_rel(host(outs["hidden"][:Rn]), ref.hidden) <= 2e-2
 
 
 def test_host_resident_path_rejects_device_memory_and_one_stream(tiny):

@@ -3,8 +3,11 @@ stack, one request of 6 x 512 cached tokens + 64 query tokens, 15% token
 top-k at layer 1, run exactly as bench.py times it (one cb_blend_prefill
 call captured in a CUDA graph and replayed).
 
-The oracle cannot run the whole request (about 9 TFLOP in float64), so it
-computes sampled outputs one by one from the weights and tokens alone:
+Here the GPU ranks the deviations itself, so its selection (decided near
+the k-th deviation by bf16 rounding) need not be the oracle's; the whole
+request under the oracle's own selection is tests/test_gpu_fulldepth.py.
+For the free selection the oracle computes sampled outputs one by one from
+the weights and tokens alone:
 
 * the layer-0 K/V rows of sampled positions (layer 0 sees only each row's
   own embedding, so every row is fresh there);

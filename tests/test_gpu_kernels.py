@@ -475,3 +475,39 @@ def test_linear_workspace_is_validated(llama_proj):
     with pytest.raises(L.CBError) as e:
         model.cb_linear_ws(A, dw["w_qkv"], out, L.CB_EPI_STORE, ws=small)
     assert e.value.status == L.CB_ERR_WORKSPACE
+
+
+def test_selection_stats_match_the_definitions():
+    """cb_selection_stats against the oracle's Table 2 definitions ("Request
+    Order Matters" §4.4): contiguous regions of a selection and the share of
+    the deviation it carries, on random requests, several per call."""
+    import ctypes as C
+    rng = np.random.default_rng(0)
+    for trial in range(10):
+        reqs, ds, Ps, d_off, i_off = [], [], [], 0, 0
+        for b in range(int(rng.integers(1, 5))):
+            n = int(rng.integers(1, 3000))
+            d = rng.random(n).astype(np.float32)
+            k = int(rng.integers(0, n + 1))
+            P = np.sort(rng.choice(n, size=k, replace=False)).astype(np.int32)
+            reqs.append(dict(n_ctx=n, k=k, dev_offset=d_off, idx_offset=i_off))
+            ds.append(d); Ps.append(P)
+            d_off += n; i_off += k
+        dev = torch.from_numpy(np.concatenate(ds)).cuda()
+        idx = torch.from_numpy(np.concatenate(Ps + [np.zeros(1, np.int32)])).cuda()
+        seg = torch.full((len(reqs),), -1, dtype=torch.int32, device="cuda")
+        cap = torch.full((len(reqs),), -1.0, dtype=torch.float64, device="cuda")
+        arr, keep = R.api._select_reqs(reqs)
+        L.check(L.lib.cb_selection_stats(C.c_void_p(dev.data_ptr()), C.c_void_p(idx.data_ptr()),
+                                         arr, len(reqs), C.c_void_p(seg.data_ptr()),
+                                         C.c_void_p(cap.data_ptr()),
+                                         C.c_void_p(torch.cuda.current_stream().cuda_stream)))
+        torch.cuda.synchronize()
+        assert R.device_status() == 0
+        for b, (d, P) in enumerate(zip(ds, Ps)):
+            assert int(seg[b]) == O.selection_segments(P)
+            assert abs(float(cap[b]) - O.captured_deviation(P, d.astype(np.float64))) < 1e-9
+    # the single-request binding
+    s_, c_ = R.selection_stats(torch.tensor([3, 4, 5, 9], dtype=torch.int32, device="cuda"),
+                               torch.ones(12, dtype=torch.float32, device="cuda"))
+    assert (s_, c_) == (2, 4 / 12)

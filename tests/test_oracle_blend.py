@@ -204,6 +204,48 @@ def test_gradual_step_reranks_the_current_set_by_its_fresh_keys():
     assert list(r.selected) == sorted(P[order].tolist())
 
 
+def test_chunk_prefill_all_equals_each_chunk_alone():
+    # the layer-outer order of the batched chunk prefill changes nothing
+    m = _model()
+    chunks, query, segs, store = _request(m)
+    for (k, v), (k1, v1) in zip(O.chunk_prefill_all(m, chunks), store):
+        assert np.array_equal(k, k1) and np.array_equal(v, v1)
+
+
+def test_forced_steps_reproduce_the_free_steps():
+    m = _model(n_layers=4)
+    chunks, query, segs, store = _request(m)
+    sch = [(2, 3), (3, 2)]
+    a = O.blend_prefill(m, segs, store, ratio_bp=2000, schedule=sch)
+    b = O.blend_prefill(m, segs, store, ratio_bp=2000, schedule=sch, forced=a.selected_per_layer[1],
+                        forced_steps={l: a.selected_per_layer[l] for l, _ in sch})
+    assert np.array_equal(a.K, b.K) and np.array_equal(a.hidden, b.hidden)
+    assert all(np.array_equal(a.selected_per_layer[l], b.selected_per_layer[l]) for l in (1, 2, 3))
+
+
+def test_forced_step_computes_the_given_rows_from_its_layer_on():
+    """A forced step keeps exactly the given rows: from that layer on the
+    dropped rows keep the stitched cache (Eq. 7) and the kept ones are
+    recomputed, whatever their deviation rank."""
+    m = _model(n_layers=4)
+    chunks, query, segs, store = _request(m)
+    a = O.blend_prefill(m, segs, store, ratio_bp=2000, schedule=[(2, 3)])
+    P1 = a.selected_per_layer[1]
+    d = a.deviation_per_layer[2]
+    low = np.sort(sorted(P1.tolist(), key=lambda i: (d[i], i))[:3])   # the smallest deviations
+    assert not np.array_equal(low, a.selected_per_layer[2])
+    b = O.blend_prefill(m, segs, store, ratio_bp=2000, schedule=[(2, 3)], forced_steps={2: low})
+    assert np.array_equal(b.selected_per_layer[2], low) and np.array_equal(b.selected, low)
+    K, V = O.stitch(store, [len(c) for c in chunks], m.n_kv_heads, m.head_dim, m.rope_base)
+    dropped = np.setdiff1d(P1, low)
+    for l in (2, 3):
+        assert np.array_equal(b.K[l, dropped], K[l, dropped])
+        assert np.array_equal(b.V[l, dropped], V[l, dropped])
+        assert np.all(np.abs(b.K[l, low] - K[l, low]).max(1) > 0)
+    N = sum(len(c) for c in chunks)
+    assert list(b.rows) == list(low) + list(range(N, N + len(query)))
+
+
 def test_selection_past_last_layer_is_full_prefill():
     m = _model()
     chunks, query, segs, store = _request(m)

@@ -1,12 +1,10 @@
 """Host logic without a GPU: the chunk store's row allocator (first-fit
-runs, eviction with merging) and the selection diagnostics against the
-oracle's definitions ("Request Order Matters" §4.4, Table 2)."""
+runs, eviction with merging) and the loading controller (a host-only
+library call)."""
 import types
 
-import numpy as np
 import torch
 
-import oracle as O
 from rag_kv_cache_layer_gb300 import api
 
 
@@ -42,18 +40,6 @@ def test_store_full_is_an_error():
     except RuntimeError:
         return
     raise AssertionError("allocation past capacity must fail")
-
-
-def test_selection_stats_match_the_definitions():
-    rng = np.random.default_rng(0)
-    for _ in range(20):
-        n = int(rng.integers(1, 60))
-        d = rng.random(n)
-        k = int(rng.integers(0, n + 1))
-        P = np.sort(rng.choice(n, size=k, replace=False))
-        seg, cap = api.selection_stats(torch.from_numpy(P), torch.from_numpy(d))
-        assert seg == O.selection_segments(P)
-        assert abs(cap - O.captured_deviation(P, d)) < 1e-12
 
 
 def test_loading_controller_picks_the_largest_hidden_ratio():
