@@ -224,7 +224,8 @@ def kernel_table(L, run_step, shape, peaks, work, stitch_layers, n_ctx, n_rows, 
 
     work: the contraction classes' FLOP per call (blend_work).  Byte counts:
     stitch reads and writes K and V of every context row of every stitched
-    layer; selection reads fresh and reused keys of every context row and
+    layer; selection reads the per-head deviation partials that the key
+    projection's epilogue leaves (one float per kv head and context row) and
     writes d; gather moves the computed rows' hidden states; the LM head
     reads the embedding once per 8 requests."""
     d, hd = shape.d_model, shape.head_dim
@@ -238,7 +239,9 @@ def kernel_table(L, run_step, shape, peaks, work, stitch_layers, n_ctx, n_rows, 
         ("swiglu", L.CB_PROBE_SWIGLU, "tensor", work["swiglu"]),
         ("down_proj", L.CB_PROBE_DOWN, "tensor", work["down_proj"]),
         ("stitch", L.CB_PROBE_STITCH, "hbm", stitch_layers * n_ctx * kvw * 2.0 * 4),
-        ("select", L.CB_PROBE_SELECT, "hbm", 2.0 * n_ctx * kvw * 2 + 4.0 * n_ctx),
+        # the fused path's select class sums the key projection's per-head
+        # partials and ranks them (the keys themselves are read there)
+        ("select", L.CB_PROBE_SELECT, "hbm", (shape.n_kv_heads + 1) * 4.0 * n_ctx),
         ("gather", L.CB_PROBE_GATHER, "hbm", 2.0 * n_rows * d * 4),
         ("lm_head", L.CB_PROBE_LM_HEAD, "hbm", math.ceil(n_req / 8) * 2.0 * shape.vocab * d),
     ]

@@ -560,10 +560,11 @@ static cb_status run_linear(const cb_model *m, const void *A, int64_t lda, const
     int *st;
     CB_TRY(status_ptr(&st));
     const int path = g_gemm_path.load(std::memory_order_relaxed);
-    const int form = path == CB_GEMM_AUTO        ? gemm_auto_form(M, K, epi)
-                     : path == CB_GEMM_SWAP_AB      ? 1
-                     : path == CB_GEMM_SWAP_AB_PAIR ? 2
-                                                    : 0;
+    int form = path == CB_GEMM_AUTO        ? gemm_auto_form(M, K, epi)
+               : path == CB_GEMM_SWAP_AB      ? 1
+               : path == CB_GEMM_SWAP_AB_PAIR ? 2
+                                              : 0;
+    if (epi == EPI_KDEV && form == 0) form = 1;   // the key-deviation epilogue is swapped-only
     if (form)
       CB_CUDA(launch_gemm_sab(A, lda, W, W2, ldw, M, N, K, epi, out, ldo, qkv, st, s, form,
                               split_ws));
@@ -692,6 +693,7 @@ struct Plan {
   // workspace
   LayerOffsets lay;
   size_t h_all, kf, dev, sel, pos_all, glob_all, pos_c, glob_c, h_c, lm_x, lm_best, total;
+  size_t kdev = 0, dev_idx = 0;   // fused key deviation: per-head partials, row -> d index
   size_t attn_plan = 0, attn_plan_bytes = 0;   // unit table of the compact layers' attention
   // query-aware selection ([QCF] §3.3-3.4)
   ProbeLayout probe;
@@ -872,6 +874,10 @@ static cb_status make_plan(const cb_model *m, const cb_request *reqs, int B,
   P.h_c = cv.take((P.R_total + 1) * c.d_model * sizeof(float));
   P.lm_x = cv.take((size_t)B * c.d_model * sizeof(float));
   P.lm_best = cv.take((size_t)B * sizeof(unsigned long long));
+  if (blend) {
+    P.kdev = cv.take((size_t)c.n_kv_heads * (P.N_total + 1) * sizeof(float));
+    P.dev_idx = cv.take((P.T_total + 1) * sizeof(int32_t));
+  }
   if (c.dtype == CB_BF16 && attention_tc_supported(c.n_q_heads, c.n_kv_heads, c.head_dim)) {
     // the compact rows of each request (the largest set; filtering only shrinks it)
     std::vector<AttnReq> ar(B);
@@ -1395,7 +1401,8 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
   const int32_t *toks[CB_MAX_BATCH];
   for (int b = 0; b < B; ++b) toks[b] = reqs[b].tokens;
   CB_CUDA(launch_embed(toks, P.bm, m->w.embed, c.vocab, d, c.dtype, h_all, st, s));
-  CB_CUDA(launch_iota_rows(P.bm, pos_all, glob_all, (int)P.T_total, s));
+  int32_t *dev_idx = (int32_t *)(ws + P.dev_idx);
+  CB_CUDA(launch_iota_rows(P.bm, pos_all, glob_all, (int)P.T_total, s, dev_idx));
   std::vector<AttnReq> ar_full;
   full_attn_reqs(P, ar_full);
   for (int l = 0; l < s_layer; ++l)
@@ -1406,6 +1413,12 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
   // query-aware policies score the context with the query probe instead
   if (host_kv) CB_TRY(stitch_layer(s_layer));
   const bool query = is_query_policy(p->policy);
+  // bf16 with 128-wide heads: the key projection's epilogue compares the
+  // fresh keys with the stitched ones and leaves per-head squared
+  // differences; the fresh keys are never stored
+  const bool fused_dev = !query && c.dtype == CB_BF16 && c.head_dim == 128;
+  float *kparts = (float *)(ws + P.kdev);
+  const int64_t kstride = P.N_total + 1;
   {
     const cb_layer_weights &Ls = m->layers[s_layer];
     void *kf = ws + P.kf;
@@ -1413,11 +1426,18 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
       CB_CUDA(launch_rmsnorm(h_all, d, nullptr, (int)P.T_total, d, Ls.norm1, c.norm_eps, S.x, d,
                              c.dtype, s));
       const char *wk = (const char *)Ls.w_qkv + (int64_t)m->qw * d * m->eb;
-      CB_TRY(run_linear(m, S.x, d, wk, nullptr, d, (int)P.T_total, m->kvw, d, EPI_STORE_F32,
-                        S.qkv32, m->kvw, s));
-      CB_CUDA(launch_qkv_finish(S.qkv32, m->kvw, (int)P.T_total, pos_all, nullptr, c.n_q_heads,
-                                c.n_kv_heads, c.head_dim, m->w.rope_table, nullptr, 0, kf,
-                                nullptr, m->kvw, c.dtype, 0, s));
+      if (fused_dev) {
+        QkvEpi q{pos_all, glob_all, layer_ptr(out->k_cache, s_layer, lstride, m->eb), nullptr,
+                 m->kvw, m->w.rope_table, c.n_q_heads, c.n_kv_heads, dev_idx};
+        CB_TRY(run_linear(m, S.x, d, wk, nullptr, d, (int)P.T_total, m->kvw, d, EPI_KDEV, kparts,
+                          kstride, s, &q));
+      } else {
+        CB_TRY(run_linear(m, S.x, d, wk, nullptr, d, (int)P.T_total, m->kvw, d, EPI_STORE_F32,
+                          S.qkv32, m->kvw, s));
+        CB_CUDA(launch_qkv_finish(S.qkv32, m->kvw, (int)P.T_total, pos_all, nullptr, c.n_q_heads,
+                                  c.n_kv_heads, c.head_dim, m->w.rope_table, nullptr, 0, kf,
+                                  nullptr, m->kvw, c.dtype, 0, s));
+      }
     }
     // selection requests: every request's cached segments are its spans
     std::vector<cb_select_req> cr(B);
@@ -1466,11 +1486,19 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
       }
     } else if (p->forced_selected) {
       // the caller fixes P; d is still produced for inspection
-      CB_CUDA(launch_deviation(kf, m->kvw, layer_ptr(out->k_cache, s_layer, lstride, m->eb),
-                               m->kvw, m->kvw, c.dtype, sr.data(), B, dev, s));
+      if (fused_dev)
+        CB_CUDA(launch_reduce_parts(kparts, c.n_kv_heads, kstride, sr.data(), B, dev, s));
+      else
+        CB_CUDA(launch_deviation(kf, m->kvw, layer_ptr(out->k_cache, s_layer, lstride, m->eb),
+                                 m->kvw, m->kvw, c.dtype, sr.data(), B, dev, s));
       if (sel != p->forced_selected && P.K_total > 0)
         CB_CUDA(cudaMemcpyAsync(sel, p->forced_selected, P.K_total * sizeof(int32_t),
                                 cudaMemcpyDeviceToDevice, s));
+    } else if (fused_dev && p->policy == CB_POLICY_TOKEN_TOPK) {
+      CB_CUDA(launch_topk_parts(kparts, c.n_kv_heads, kstride, sr.data(), B, dev, sel, s));
+    } else if (fused_dev) {
+      CB_CUDA(launch_reduce_parts(kparts, c.n_kv_heads, kstride, sr.data(), B, dev, s));
+      CB_CUDA(launch_selection(dev, plan, sel, st, s));
     } else {
       CB_TRY(run_selection(kf, m->kvw, layer_ptr(out->k_cache, s_layer, lstride, m->eb),
                            m->kvw, m->kvw, c.dtype, plan, dev, sel, st, s));

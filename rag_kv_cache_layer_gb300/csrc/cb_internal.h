@@ -120,6 +120,15 @@ cudaError_t launch_deviation(const void *k_fresh, int64_t ld_fresh,
 // reused_row0 + reused_rows[f] instead of reused_row0 + i.
 cudaError_t launch_topk(const float *dev, const SelReq *reqs, int n_req,
                         int32_t *idx_out, cudaStream_t s);
+// Deviations from per-head partials (EPI_KDEV): d[dev_offset + i] =
+// sum over h < n_parts of parts[h * part_stride + dev_offset + i], summed in
+// head order (deterministic).  launch_topk_parts also ranks them (token
+// top-k, as launch_topk) in the same kernel.
+cudaError_t launch_reduce_parts(const float *parts, int n_parts, int64_t part_stride,
+                                const SelReq *reqs, int n_req, float *dev_out, cudaStream_t s);
+cudaError_t launch_topk_parts(const float *parts, int n_parts, int64_t part_stride,
+                              const SelReq *reqs, int n_req, float *dev_out, int32_t *idx_out,
+                              cudaStream_t s);
 // A selection call after validation: the requests, their packed spans and,
 // per span, the visiting order (random document) or the token counts
 // (first tokens).  make_sel_plan builds the spans every policy uses.
@@ -149,8 +158,11 @@ cudaError_t launch_filter_rows(const BatchMeta &cur, const BatchMeta &nxt,
 cudaError_t launch_keep_from_positions(const BatchMeta &cur, const BatchMeta &nxt,
                                        const int32_t *forced, const int32_t *sel_cur,
                                        int32_t *keep, int n_keep, int *status, cudaStream_t s);
+// dev_idx (may be NULL): for row r of request b at position p, the index
+// n_off[b] + p of its deviation when p < n_ctx[b] (reusable context), else
+// -1; n_off: prefix sums of n_ctx.
 cudaError_t launch_iota_rows(const BatchMeta &bm, int32_t *pos, int32_t *glob,
-                             int n_rows, cudaStream_t s);
+                             int n_rows, cudaStream_t s, int32_t *dev_idx = nullptr);
 // Per request: contiguous regions of its selection and the share of its
 // deviation the selection carries (Table 2 diagnostics).
 cudaError_t launch_selection_stats(const float *dev, const int32_t *idx, const SelReq *reqs,
@@ -201,7 +213,8 @@ enum GemmEpi {
   EPI_STORE = 1,
   EPI_RESID = 2,
   EPI_SWIGLU = 3,
-  EPI_QKV = 4
+  EPI_QKV = 4,
+  EPI_KDEV = 5   // keys -> per-head deviation partials (bf16 swapped GEMM only)
 };
 // out = epi(A[M][K] W[N][K]^T); A and W of dtype dt; STORE_F32 and RESID
 // write float, STORE and SWIGLU write dt.
@@ -213,6 +226,15 @@ cudaError_t launch_gemm_simt(const void *A, int64_t lda, const void *W,
 // Arguments of the fused Q/K/V epilogue: q heads (rotated at pos[m]) go to
 // out[m], k heads (rotated) and v heads to cache row dst_row[m] of k_cache /
 // v_cache (this layer's cache, row stride ld_kv).  head_dim must be 128.
+//
+// EPI_KDEV ("Request Order Matters" §2.2 Eq. 1 at the selection layer): the
+// GEMM's weights are the key rows W_k only, so tile h is kv head h.  Each
+// token's fresh key head is rotated at pos[m] and compared with the reused
+// key in k_cache at row dst_row[m] (this layer's fused cache, holding the
+// stitched chunk caches); the squared difference summed over the head's
+// 128 features goes to out[h * ldo + dev_idx[m]] (fp32).  Tokens with
+// dev_idx[m] < 0 (not reusable context) are skipped.  The fresh keys are
+// never stored.
 struct QkvEpi {
   const int32_t *pos;
   const int32_t *dst_row;
@@ -220,6 +242,7 @@ struct QkvEpi {
   int64_t ld_kv;
   const float *rope;  // cb_rope_table_init layout
   int n_q_heads, n_kv_heads;
+  const int32_t *dev_idx = nullptr;   // EPI_KDEV only
 };
 // bf16 tcgen05 GEMM (sm_103a); qkv is read for EPI_QKV only.
 cudaError_t launch_gemm_tc(const void *A, int64_t lda, const void *W,

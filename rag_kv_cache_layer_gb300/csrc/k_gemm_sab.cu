@@ -14,7 +14,10 @@
 // a warp write 32 consecutive features.  Two epilogues pair feature r with r + 64
 // through a shared-memory exchange: SwiGLU (tile rows 0..63 are W_gate rows,
 // 64..127 the matching W_up rows) and the QKV RoPE (rotate-half pairs
-// (e, e + 64) of a 128-wide head).  Residual outputs may use stream-K.
+// (e, e + 64) of a 128-wide head).  The key-deviation epilogue rotates the
+// same way and, instead of storing the keys, compares each token's head with
+// the reused key in the fused cache and leaves the head's squared
+// difference.  Residual outputs may use stream-K.
 // Other outputs may split the tiles of a partial last wave along K: the
 // units that run the later k-segments leave fp32 partials in a workspace
 // and the unit that runs segment 0 adds them, in segment order, before its
@@ -33,7 +36,7 @@ constexpr int kThreads = 320;
 constexpr int kTileW = FM * BK * 2;          // 16 KB
 constexpr int kTrStride = 132;               // floats per transposed token row
 constexpr int kTr = 32 * kTrStride * 4;      // 32 tokens x 128 features, fp32
-constexpr int kTokTab = 256 * 12;            // Q/K/V epilogue: a tile's positions, cache rows
+constexpr int kTokTab = 256 * 16;            // Q/K/V, K-deviation: positions, cache rows, d index
 constexpr int kSmemMax = 232448;
 constexpr int kPartFloats = 8 * FM * 32;     // one CTA's partial: 8 chunks x 128 features x 32 tokens
 constexpr int kSplitFlagBytes = 4096;       // arrival counters: one per tail tile and CTA (<= SMs)
@@ -42,7 +45,7 @@ constexpr int kSplitFlagBytes = 4096;       // arrival counters: one per tail ti
 // (168 for 320 threads): it has a second instantiation with the split, used
 // only by launches that do split, so that the others keep their registers.
 template <int EPI>
-constexpr bool can_split() { return EPI != EPI_RESID; }
+constexpr bool can_split() { return EPI != EPI_RESID && EPI != EPI_KDEV; }
 template <int EPI>
 constexpr bool split_by_default() { return can_split<EPI>() && EPI != EPI_QKV; }
 
@@ -60,7 +63,7 @@ struct Params {
   // epilogue
   void *out;
   int64_t ldo;
-  const int32_t *pos, *dst_row;
+  const int32_t *pos, *dst_row, *dev_idx;
   void *k_cache, *v_cache;
   int64_t ld_kv;
   const float2 *rope;
@@ -186,6 +189,7 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.stages * p.stage_bytes + 2 * kTr);
   int64_t *s_dst = reinterpret_cast<int64_t *>(smem + p.stages * p.stage_bytes + 2 * kTr + 256);
   int32_t *s_pos = reinterpret_cast<int32_t *>(s_dst + 256);
+  int32_t *s_dev = s_pos + 256;                  // EPI_KDEV: deviation index (-1: none)
   uint64_t *full = bars;                 // [stages]
   uint64_t *empty = bars + 8;            // [stages]
   uint64_t *tfull = bars + 16;           // [2]
@@ -360,7 +364,7 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
     int tt, ft, kb0, kb1;
     while (wk.next(tt, ft, kb0, kb1)) {
       const bool whole = kb0 == 0 && kb1 == num_kb;
-      if (EPI == EPI_QKV) {
+      if (EPI == EPI_QKV || EPI == EPI_KDEV) {
         // the tile's positions and fused-cache rows, read while the MMAs run,
         // once every warp is done with the previous tile's table
         epi_all_bar();
@@ -368,6 +372,7 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
           const int tok = tt * p.BT + i;
           s_pos[i] = tok < p.M ? p.pos[tok] : 0;
           s_dst[i] = tok < p.M ? (int64_t)p.dst_row[tok] : 0;
+          if (EPI == EPI_KDEV) s_dev[i] = tok < p.M ? p.dev_idx[tok] : -1;
         }
       }
       // tail split: segment 0 finishes the tile once the other segments'
@@ -400,6 +405,9 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
       if (EPI == EPI_QKV) {
         head = ft;
         rotate = head < p.Hq + p.Hkv;
+      } else if (EPI == EPI_KDEV) {
+        head = ft;                                   // tile h = kv head h of W_k
+        rotate = true;
       }
       // this tile's partial slots: [segment][CG][kPartFloats]
       float *part = wk.split > 1 ? p.part + ((int64_t)wk.tj * wk.split * CG + rank) * kPartFloats
@@ -435,8 +443,9 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
         }
         // Q/K heads: this thread's rotation factors for the chunk, loaded
         // before the transpose so that their latency overlaps it
-        float4 rf[EPI == EPI_QKV ? 4 : 1][EPI == EPI_QKV ? 4 : 1];
-        if (EPI == EPI_QKV && rotate) {
+        constexpr bool kRope = EPI == EPI_QKV || EPI == EPI_KDEV;
+        float4 rf[kRope ? 4 : 1][kRope ? 4 : 1];
+        if (kRope && rotate) {
           const int e0 = 8 * ((t & 15) & 7);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -498,6 +507,35 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
               for (int e = 0; e < 8; ++e) y[e] = __fdividef(g[e], 1.f + __expf(-g[e])) * u[e];
               store_bf16x8(reinterpret_cast<bf16 *>(p.out) + (int64_t)tok * p.ldo + f, y);
             }
+          }
+        } else if (EPI == EPI_KDEV) {
+          // 32 tokens x 16 groups of 8 features; the 16 threads of a token
+          // are one half-warp, which sums the head's squared differences
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int v = t + 128 * q, i = v >> 4, j = v & 15;
+            const int tok = tok0 + c + i;
+            const int di = (c + i < p.BT && tok < p.M) ? s_dev[c + i] : -1;
+            float acc = 0.f;
+            if (di >= 0) {
+              const float *row = tr + i * kTrStride;
+              const int e0 = 8 * (j & 7);
+              const float *w = reinterpret_cast<const float *>(rf[q]);   // (cos, sin) x 8
+              float kr[8];
+              load16<bf16>(reinterpret_cast<const bf16 *>(p.k_cache) + s_dst[c + i] * p.ld_kv +
+                               head * 128 + 8 * j, kr);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float x1 = row[e0 + e], x2 = row[64 + e0 + e];
+                const float co = w[2 * e], si = w[2 * e + 1];
+                const float y = j < 8 ? x1 * co - x2 * si : x2 * co + x1 * si;
+                const float dlt = y - kr[e];
+                acc = fmaf(dlt, dlt, acc);
+              }
+            }
+#pragma unroll
+            for (int o = 8; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (j == 0 && di >= 0) reinterpret_cast<float *>(p.out)[head * p.ldo + di] = acc;
           }
         } else {  // EPI_QKV: one head per tile
 #pragma unroll
@@ -631,7 +669,7 @@ static cudaError_t launch(int units, int smem, const CUtensorMap &mx, const CUte
 template <int EPI, int CG>
 static cudaError_t run(const CUtensorMap &mx, const CUtensorMap &mw, const CUtensorMap &mw2,
                        Params &p, int *status, cudaStream_t s) {
-  const int fixed = 2 * kTr + 256 + (EPI == EPI_QKV ? kTokTab : 0) + 1024;
+  const int fixed = 2 * kTr + 256 + (EPI == EPI_QKV || EPI == EPI_KDEV ? kTokTab : 0) + 1024;
   p.stage_bytes = kTileW + (p.BT / CG) * BK * 2;
   p.stages = (kSmemMax - fixed) / p.stage_bytes;
   if (p.stages > 8) p.stages = 8;
@@ -715,7 +753,7 @@ cudaError_t launch_gemm_sab(const void *A, int64_t lda, const void *W, const voi
   p.K = K;
   p.n_tt = (M + 255) / 256;
   p.BT = ((M + p.n_tt - 1) / p.n_tt + 15) / 16 * 16;
-  if (epi == EPI_QKV && (N / 128) % 2) cta_group = 1;   // pairs take two heads
+  if ((epi == EPI_QKV || epi == EPI_KDEV) && (N / 128) % 2) cta_group = 1;   // pairs take two heads
   if (p.BT < 32) cta_group = 1;                           // keep each CTA's half >= 16 rows
   const int cg = cta_group;
   p.idesc = idesc_bf16(FM * cg, p.BT);
@@ -747,6 +785,19 @@ cudaError_t launch_gemm_sab(const void *A, int64_t lda, const void *W, const voi
       p.Hkv = qkv->n_kv_heads;
       if (!make_map(&mw, W, N, K, ldw, FM)) return cudaErrorInvalidValue;
       return run_cg<EPI_QKV>(mx, mw, mw, p, cg, status, s);
+    case EPI_KDEV:
+      if (!qkv || !qkv->dev_idx || N % 128) return cudaErrorInvalidValue;
+      p.n_ft = N / 128;
+      p.pos = qkv->pos;
+      p.dst_row = qkv->dst_row;
+      p.dev_idx = qkv->dev_idx;
+      p.k_cache = qkv->k_cache;
+      p.ld_kv = qkv->ld_kv;
+      p.rope = reinterpret_cast<const float2 *>(qkv->rope);
+      p.Hq = qkv->n_q_heads;
+      p.Hkv = qkv->n_kv_heads;
+      if (!make_map(&mw, W, N, K, ldw, FM)) return cudaErrorInvalidValue;
+      return run_cg<EPI_KDEV>(mx, mw, mw, p, cg, status, s);
     case EPI_RESID:
       p.n_ft = (N + FM - 1) / FM;
       p.stream_k = 1;

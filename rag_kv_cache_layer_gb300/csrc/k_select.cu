@@ -131,19 +131,14 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_buf,
   return before;
 }
 
-__global__ void __launch_bounds__(kSelThreads)
-topk_kernel(const __grid_constant__ SelParams p, const float *__restrict__ dev,
-            int32_t *__restrict__ idx_out) {
+// The k largest of d[0 .. n) (ties to the lower index), their indices
+// written ascending to out: the body of the top-k kernels, one CTA.  d is a
+// generic pointer (global or shared memory) that the whole CTA reads.
+__device__ void topk_block(const float *d, int n, int k, int32_t *__restrict__ out) {
   __shared__ uint32_t hist[256];
   __shared__ int warp_buf[32];
   __shared__ uint32_t s_prefix, s_mask;
   __shared__ int s_remaining;
-  const SelReq &q = p.r[blockIdx.x];
-  const int n = q.n_ctx;
-  const int k = q.k;
-  if (k <= 0) return;
-  const float *d = dev + q.dev_offset;
-  int32_t *out = idx_out + q.idx_offset;
   const int tid = threadIdx.x;
 
   if (tid == 0) { s_prefix = 0; s_mask = 0; s_remaining = k; }
@@ -158,7 +153,7 @@ topk_kernel(const __grid_constant__ SelParams p, const float *__restrict__ dev,
       bool active = false;
       uint32_t digit = 0;
       if (i < n) {
-        const uint32_t key = float_key(__ldg(d + i));
+        const uint32_t key = float_key(d[i]);
         if ((key & mask) == prefix) { active = true; digit = (key >> shift) & 255u; }
       }
       // warp-aggregated histogram update: one atomic per distinct digit
@@ -213,7 +208,7 @@ topk_kernel(const __grid_constant__ SelParams p, const float *__restrict__ dev,
   for (int base = 0; base < n; base += kSelThreads) {
     const int i = base + tid;
     uint32_t key = 0;
-    if (i < n) key = float_key(__ldg(d + i));
+    if (i < n) key = float_key(d[i]);
     const int gt = (i < n && key > thr) ? 1 : 0;
     const int eq = (i < n && key == thr) ? 1 : 0;
     int eq_total;
@@ -226,6 +221,72 @@ topk_kernel(const __grid_constant__ SelParams p, const float *__restrict__ dev,
     taken_eq += eq_total;
     if (written >= k) break;
   }
+}
+
+__global__ void __launch_bounds__(kSelThreads)
+topk_kernel(const __grid_constant__ SelParams p, const float *__restrict__ dev,
+            int32_t *__restrict__ idx_out) {
+  const SelReq &q = p.r[blockIdx.x];
+  if (q.k <= 0) return;
+  topk_block(dev + q.dev_offset, q.n_ctx, q.k, idx_out + q.idx_offset);
+}
+
+// Deviations of the selection layer from the per-head partials that the key
+// projection's epilogue leaves (EPI_KDEV), summed in head order, then (with
+// rank) the request's token top-k over them.  One CTA per request; with
+// rank the deviations stay in shared memory (kSmemCtx floats at most; a
+// longer request reads them back from dev_out) for the select's passes.
+constexpr int kSmemCtx = 40960;
+template <bool RANK>
+__global__ void __launch_bounds__(kSelThreads)
+parts_kernel(const __grid_constant__ SelParams p, const float *__restrict__ parts, int n_parts,
+             int64_t part_stride, float *__restrict__ dev_out, int32_t *__restrict__ idx_out) {
+  extern __shared__ float s_d[];
+  grid_dep_wait();      // the partials come from the previous kernel
+  grid_dep_launch();
+  const SelReq &q = p.r[blockIdx.x];
+  const int n = q.n_ctx;
+  const bool in_smem = RANK && n <= kSmemCtx;
+  for (int i = threadIdx.x; i < n; i += kSelThreads) {
+    const float *src = parts + q.dev_offset + i;
+    float v = 0.f;
+    for (int h = 0; h < n_parts; ++h) v += __ldg(src + h * part_stride);
+    dev_out[q.dev_offset + i] = v;
+    if (in_smem) s_d[i] = v;
+  }
+  if (!RANK || q.k <= 0) return;
+  __syncthreads();
+  topk_block(in_smem ? s_d : dev_out + q.dev_offset, n, q.k, idx_out + q.idx_offset);
+}
+
+cudaError_t launch_reduce_parts(const float *parts, int n_parts, int64_t part_stride,
+                                const SelReq *reqs, int n_req, float *dev_out, cudaStream_t s) {
+  if (n_req == 0) return cudaSuccess;
+  SelParams p;
+  fill_params(p, reqs, n_req);
+  cudaError_t e = launch_pdl(parts_kernel<false>, dim3(n_req), dim3(kSelThreads), 0, s, p, parts,
+                             n_parts, part_stride, dev_out, (int32_t *)nullptr);
+  return e != cudaSuccess ? e : launched(1);
+}
+
+cudaError_t launch_topk_parts(const float *parts, int n_parts, int64_t part_stride,
+                              const SelReq *reqs, int n_req, float *dev_out, int32_t *idx_out,
+                              cudaStream_t s) {
+  if (n_req == 0) return cudaSuccess;
+  SelParams p;
+  fill_params(p, reqs, n_req);
+  int n_max = 0;
+  for (int i = 0; i < n_req; ++i) n_max = reqs[i].n_ctx > n_max ? reqs[i].n_ctx : n_max;
+  const size_t smem = (size_t)(n_max < kSmemCtx ? n_max : kSmemCtx) * sizeof(float);
+  static PerDeviceOnce attr;
+  cudaError_t e = attr.run([](int) {
+    return cudaFuncSetAttribute(parts_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemCtx * (int)sizeof(float));
+  });
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(parts_kernel<true>, dim3(n_req), dim3(kSelThreads), smem, s, p, parts, n_parts,
+                 part_stride, dev_out, idx_out);
+  return e != cudaSuccess ? e : launched(1);
 }
 
 cudaError_t launch_topk(const float *dev, const SelReq *reqs, int n_req,
@@ -670,19 +731,22 @@ cudaError_t launch_selection_stats(const float *dev, const int32_t *idx, const S
 
 __global__ void iota_rows_kernel(const __grid_constant__ BatchMeta bm,
                                  int32_t *__restrict__ pos,
-                                 int32_t *__restrict__ glob, int n_rows) {
+                                 int32_t *__restrict__ glob, int n_rows,
+                                 int32_t *__restrict__ dev_idx) {
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= n_rows) return;
-  int b = 0;
-  while (bm.t_off[b + 1] <= r) ++b;
-  pos[r] = r - bm.t_off[b];
+  int b = 0, n_off = 0;
+  while (bm.t_off[b + 1] <= r) n_off += bm.n_ctx[b++];
+  const int p = r - bm.t_off[b];
+  pos[r] = p;
   glob[r] = r;
+  if (dev_idx) dev_idx[r] = p < bm.n_ctx[b] ? n_off + p : -1;
 }
 
 cudaError_t launch_iota_rows(const BatchMeta &bm, int32_t *pos, int32_t *glob,
-                             int n_rows, cudaStream_t s) {
+                             int n_rows, cudaStream_t s, int32_t *dev_idx) {
   if (n_rows == 0) return cudaSuccess;
-  iota_rows_kernel<<<(n_rows + 255) / 256, 256, 0, s>>>(bm, pos, glob, n_rows);
+  iota_rows_kernel<<<(n_rows + 255) / 256, 256, 0, s>>>(bm, pos, glob, n_rows, dev_idx);
   return launched(1);
 }
 

@@ -282,6 +282,23 @@ def test_forced_kept_position_outside_the_selection_is_recorded(llama4):
     assert R.device_status() == 0
 
 
+def test_bf16_llama_truncated_doc_aligned_on_own_deviation(llama2, llama2_ref):
+    """bf16: the key projection's epilogue leaves per-head deviation partials;
+    a non-top-k policy sums them into d and ranks d with the span kernel.  The
+    spans chosen are exactly the oracle's rule on the GPU's own d, and d is
+    within 2e-2 of the oracle's."""
+    rq = llama2.wl.requests[0]
+    out = llama2.model.cb_blend_prefill(llama2.gpu_reqs(), 1500, policy=L.CB_POLICY_DOC_ALIGNED)
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    N = rq.n_ctx
+    k = len(llama2_ref.selected)
+    d = out["deviation"][:N].cpu().numpy().astype(np.float64)
+    assert rms_rel(d, llama2_ref.deviation) <= 2e-2
+    offs = np.concatenate([[0], np.cumsum([len(sg.tokens) for sg in rq.segments if sg.cached])])
+    assert list(out["selected"][:k].cpu().numpy()) == list(O.doc_aligned_select(d, offs, k))
+
+
 def test_blend_replays_from_a_cuda_graph(tiny, llama2):
     """cb_blend_prefill allocates nothing and never synchronises, so one call
     captured into a CUDA graph replays the same computation.  The fp32 path
