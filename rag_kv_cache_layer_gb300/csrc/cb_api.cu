@@ -925,7 +925,7 @@ static cb_status make_plan(const cb_model *m, const cb_request *reqs, int B,
       Q.reqs[b] = r;
       probe_off += r.n_anchor + r.n_u;
       u_off += r.n_u;
-      const size_t mb = mass_ws_bytes(r.n_u, c.n_q_heads, r.n_ctx);
+      const size_t mb = mass_ws_bytes(r.n_u, c.n_q_heads, c.n_kv_heads, r.n_ctx);
       if (mb > mass) mass = mb;
     }
     if ((int)Q.segs.size() > CB_MAX_SPANS)
@@ -1228,7 +1228,7 @@ static cb_status query_probe(cb_model *m, const cb_request *reqs, int B,
       const ProbeLayout::Req &r = Q.reqs[b];
       CB_CUDA(launch_attention_mass(S.q, m->qw, r.u_off, r.n_u, kl, m->kvw, r.t_off, r.n_ctx,
                                     c.n_q_heads, c.n_kv_heads, c.head_dim, ws + P.qp_mass,
-                                    P.qp_mass_bytes, I + P.n_off[b], s));
+                                    P.qp_mass_bytes, I + P.n_off[b], st, s));
     }
   }
   return CB_OK;

@@ -336,11 +336,11 @@ cudaError_t launch_probe_rows(const ProbeLayout &L, const int32_t *anchors, int3
                               int *status, cudaStream_t s);
 // mass[t] += sum over the request's query rows u and q heads h of the
 // softmax over its n_ctx context keys of q.k / sqrt(hd) (head_dim 128, bf16).
-size_t mass_ws_bytes(int n_u, int Hq, int n_ctx);
+size_t mass_ws_bytes(int n_u, int Hq, int Hkv, int n_ctx);
 cudaError_t launch_attention_mass(const void *q, int64_t ld_q, int u_off, int n_u,
                                   const void *k_cache, int64_t ld_k, int t_off, int n_ctx,
                                   int Hq, int Hkv, int hd, void *ws, size_t ws_bytes,
-                                  float *mass, cudaStream_t s);
+                                  float *mass, int *status, cudaStream_t s);
 
 // ---------------------------------------------------------------- debug --
 cudaError_t launch_expire_wait(int limit_us, int *status, cudaStream_t s);

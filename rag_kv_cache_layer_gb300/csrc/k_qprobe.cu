@@ -12,6 +12,7 @@
 // scheduling.
 #include "cb_common.cuh"
 #include "cb_internal.h"
+#include "cb_tc.cuh"
 
 namespace cb {
 namespace qp {
@@ -133,120 +134,199 @@ __global__ void probe_rows_kernel(const __grid_constant__ ProbeParams p,
 // ---------------------------------------------------------- attention mass
 // One request: query rows q[u_off + u] (n_u of them, q head h at column
 // h * 128), context keys in the fused cache rows t_off + t, t < N.  Score
-// rows are ordered r = h * n_u + u, so a kv head's rows are contiguous.
+// rows are ordered r = h * n_u + u, so kv head g's rows are the contiguous
+// range [g * R_g, (g + 1) * R_g), R_g = G * n_u.
+//
+// Both contractions run on the tensor cores (tcgen05, fp32 accumulators in
+// TMEM), with the scores never stored:
+//   1. gather: each group's query rows, contiguous and zero-padded to a
+//      multiple of 256 rows (qg[g][i], i = h_local * n_u + u);
+//   2. statistics: tiles S = Q_g K^T of 128 rows x 256 keys; epilogue thread
+//      i holds row i's 256 scores, so the tile's (max, sum of 2^(s - max))
+//      per row needs no exchange;
+//   3. combine: every row's max M_r and 1 / L_r over all key tiles;
+//   4. mass: the swapped tiles S^T = K Q_g^T of 128 keys x 256 rows; thread
+//      t holds key t's 256 scores, so sum_r 2^(s - M_r) / L_r is again a
+//      per-thread sum, left per (row tile, key);
+//   5. the row tiles' sums are added to I in a fixed order.
+// One CTA per tile, four warps: warp 0 issues the copies and the eight
+// MMAs (K = 16 each over the head dimension), all four drain TMEM.  Every
+// wait is bounded.
 constexpr int HD = 128;
-constexpr int KC = 64;                  // keys per score tile
-constexpr int RC = 128;                 // rows per score tile
-constexpr int kTileThreads = 256;       // 16 x 16 threads, 8 rows x 4 keys each
-constexpr int kScoreSmem = HD * (RC + KC) * 4;
+constexpr int kMassThreads = 128;
+constexpr int kRowsA = 128;                 // MMA M
+constexpr int kRowsB = 256;                 // MMA N
+constexpr int kAtomA = kRowsA * 128;        // one 64-wide swizzle atom of A (bytes)
+constexpr int kAtomB = kRowsB * 128;
+constexpr int kMassSmem = 2 * kAtomA + 2 * kAtomB + 1024 + 64;
+constexpr int kMassCols = 256;              // TMEM columns: the 128 x 256 accumulator
 
-// Scores s[t][r] = log2(e) q_r.k_t / sqrt(hd) of a 64-row x 64-key tile
-// (all rows of one kv head's group), and each row's (max, sum of
-// 2^(s - max)) over the tile's keys.  Q and K are staged transposed in shared
-// memory ([dim][row], [dim][key]), so each step of the dot products reads
-// one float4 of rows and one of keys for 16 FMAs.
-__global__ void __launch_bounds__(kTileThreads)
-mass_score_kernel(const bf16 *__restrict__ q, int64_t ld_q, int u_off, int n_u,
-                  const bf16 *__restrict__ kc, int64_t ld_k, int t_off, int n_ctx, int Hq,
-                  int Hkv, float scale_log2, float *__restrict__ s,
-                  float2 *__restrict__ part) {
+__host__ __device__ inline int group_pad(int group_rows) { return (group_rows + 255) / 256 * 256; }
+
+// qg[g * pad + i] = q row (u_off + u), columns (g * G + h) * 128 .. + 127,
+// for i = h * n_u + u < G * n_u; zero above.  One thread per 16 bytes.
+__global__ void mass_gather_kernel(const bf16 *__restrict__ q, int64_t ld_q, int u_off, int n_u,
+                                   int G, int Hkv, bf16 *__restrict__ qg) {
   grid_dep_wait();
   grid_dep_launch();
-  extern __shared__ __align__(16) float sm[];
-  float *qs = sm;                        // [HD][RC]
-  float *ks = sm + HD * RC;              // [HD][KC]
-  const int G = Hq / Hkv;
-  const int group_rows = G * n_u;
-  const int tiles_per_group = (group_rows + RC - 1) / RC;
-  const int g = blockIdx.y / tiles_per_group;
-  const int rt = blockIdx.y % tiles_per_group;
-  const int r0 = g * group_rows + rt * RC;           // first row of the tile
-  const int nr = min(RC, group_rows - rt * RC);
-  const int t0 = blockIdx.x * KC;
-  const int nk = min(KC, n_ctx - t0);
-  const int n_rows = Hq * n_u;
-  // stage: entry i is row i % RC (key i % KC), dims 8 * (i / RC) .. + 7
-  for (int i = threadIdx.x; i < RC * (HD / 8); i += kTileThreads) {
-    const int row = i % RC, e = 8 * (i / RC);
-    float qv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (row < nr) {
-      const int r = r0 + row, h = r / n_u, u = r % n_u;
-      const uint4 raw =
-          *reinterpret_cast<const uint4 *>(q + (int64_t)(u_off + u) * ld_q + h * HD + e);
-      const bf16 *v = reinterpret_cast<const bf16 *>(&raw);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) qv[j] = __bfloat162float(v[j]) * scale_log2;
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) qs[(e + j) * RC + row] = qv[j];
+  const int rows = G * n_u, pad = group_pad(rows);
+  const int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // 16-byte unit
+  if (v >= (int64_t)Hkv * pad * 16) return;
+  const int e = (int)(v % 16) * 8;
+  const int64_t gi = v / 16;
+  const int g = (int)(gi / pad), i = (int)(gi % pad);
+  uint4 val = make_uint4(0u, 0u, 0u, 0u);
+  if (i < rows) {
+    const int h = g * G + i / n_u, u = i % n_u;
+    val = *reinterpret_cast<const uint4 *>(q + (int64_t)(u_off + u) * ld_q + h * HD + e);
   }
-  for (int i = threadIdx.x; i < KC * (HD / 8); i += kTileThreads) {
-    const int row = i % KC, e = 8 * (i / KC);
-    float kv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (row < nk) {
-      const uint4 raw = *reinterpret_cast<const uint4 *>(
-          kc + (int64_t)(t_off + t0 + row) * ld_k + g * HD + e);
-      const bf16 *v = reinterpret_cast<const bf16 *>(&raw);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) kv[j] = __bfloat162float(v[j]);
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) ks[(e + j) * KC + row] = kv[j];
+  *reinterpret_cast<uint4 *>(qg + gi * HD + e) = val;
+}
+
+struct MassParams {
+  int n_ctx, n_u, G, Hkv, pad;
+  int rt_per_g;          // row tiles per group (128 rows in STATS, 256 in MASS)
+  int n_kt;              // key tiles (256 keys in STATS, 128 in MASS)
+  float scale_log2;      // log2(e) / sqrt(hd)
+  int key_row0;          // fused-cache row of context key 0
+};
+
+// MASS == false: statistics tiles (A = 128 query rows, B = 256 keys); part0
+// gets (max, sum) per (key tile, row).  MASS == true: mass tiles (A = 128
+// keys, B = 256 query rows); partI gets sum_r 2^(s - M_r) / L_r per (row
+// tile, key), with ml = (M_r, 1 / L_r).
+template <bool MASS>
+__global__ void __launch_bounds__(kMassThreads)
+mass_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+               const __grid_constant__ MassParams p, float2 *__restrict__ part0,
+               const float2 *__restrict__ ml, float *__restrict__ partI, int *status) {
+  using namespace tcx;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *sa = smem, *sb = smem + 2 * kAtomA;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + 2 * kAtomA + 2 * kAtomB);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 2);
+  __shared__ float2 s_ml[kRowsB];
+  __shared__ int s_ok;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // tile: blockIdx.x = key tile, blockIdx.y = g * rt_per_g + row tile
+  const int kt = blockIdx.x, g = blockIdx.y / p.rt_per_g, rt = blockIdx.y % p.rt_per_g;
+  const int group_rows = p.G * p.n_u;
+  const int q_row0 = g * p.pad + rt * (MASS ? kRowsB : kRowsA);   // first qg row of the tile
+  const int key0 = kt * (MASS ? kRowsA : kRowsB);                 // first key of the tile
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar[0]), 1);
+    mbar_init(smem_u32(&bar[1]), 1);
+    s_ok = 1;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), kMassCols);
+  fence_before();
   __syncthreads();
-  // thread (ty, tx): rows 8 ty .. 8 ty + 7, keys 4 tx .. 4 tx + 3
-  const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
-  float acc[8][4];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-#pragma unroll 4
-  for (int e = 0; e < HD; ++e) {
-    const float4 a0 = *reinterpret_cast<const float4 *>(qs + e * RC + 8 * ty);
-    const float4 a1 = *reinterpret_cast<const float4 *>(qs + e * RC + 8 * ty + 4);
-    const float4 b = *reinterpret_cast<const float4 *>(ks + e * KC + 4 * tx);
-    const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-    const float bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();      // q (gathered) and the statistics come from earlier kernels
+  grid_dep_launch();
+  if (MASS) {
+    // the tile's 256 rows: (M_r, 1 / L_r); rows past the group weigh 0
+    for (int c = threadIdx.x; c < kRowsB; c += kMassThreads) {
+      const int i = rt * kRowsB + c;
+      s_ml[c] = i < group_rows ? ml[g * group_rows + i] : make_float2(0.f, 0.f);
+    }
   }
-  // scores out (8 consecutive rows per key), then each row's statistics over
-  // the tile's keys: the 16 threads of a row group are 16 consecutive lanes
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int t = 4 * tx + j;
-    if (t < nk && 8 * ty < nr) {
-      float *dst = s + (int64_t)(t0 + t) * n_rows + r0 + 8 * ty;
-      if (8 * ty + 8 <= nr && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-        reinterpret_cast<float4 *>(dst)[0] = make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
-        reinterpret_cast<float4 *>(dst)[1] = make_float4(acc[4][j], acc[5][j], acc[6][j], acc[7][j]);
-      } else {
-        for (int i = 0; i < 8 && 8 * ty + i < nr; ++i) dst[i] = acc[i][j];
+  if (warp == 0) {
+    if (elect_one()) {
+      const uint32_t b = smem_u32(&bar[0]);
+      expect_tx(b, 2 * kAtomA + 2 * kAtomB);
+      for (int half = 0; half < 2; ++half) {
+        // MASS: A = keys, B = query rows; statistics: the other way round
+        if (MASS) {
+          tma_load_2d(smem_u32(sa + half * kAtomA), &mapK, b, g * HD + half * 64, p.key_row0 + key0);
+          tma_load_2d(smem_u32(sb + half * kAtomB), &mapQ, b, half * 64, q_row0);
+        } else {
+          tma_load_2d(smem_u32(sa + half * kAtomA), &mapQ, b, half * 64, q_row0);
+          tma_load_2d(smem_u32(sb + half * kAtomB), &mapK, b, g * HD + half * 64, p.key_row0 + key0);
+        }
       }
     }
+    __syncwarp();
+    const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&bar[0]), 0, kWaitLimitNs, status));
+    if (got) {
+      fence_after();
+      if (elect_one()) {
+        const uint32_t a = smem_u32(sa), bb = smem_u32(sb);
+        constexpr uint32_t id = idesc_bf16(kRowsA, kRowsB);
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint32_t o = (k & 3) * 32;
+          mma(tmem, desc_kmajor(a + (k >> 2) * kAtomA + o), desc_kmajor(bb + (k >> 2) * kAtomB + o),
+              id, k > 0);
+        }
+        commit(smem_u32(&bar[1]));
+      }
+      __syncwarp();
+    } else if (lane == 0) {
+      s_ok = 0;
+      // let the copies land before this CTA's shared memory goes away
+      mbar_wait_bounded(smem_u32(&bar[0]), 0, 10000000ull, nullptr);
+    }
   }
+  __syncthreads();
+  bool ok = s_ok != 0;
+  if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&bar[1]), 0, kWaitLimitNs, status));
+  if (ok) {
+    fence_after();
+    const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
+    const int me = warp * 32 + lane;               // this thread's A row
+    const float sl2 = p.scale_log2;
+    if (!MASS) {
+      // row me of the tile over its 256 keys: running (max, sum)
+      const int i = rt * kRowsA + me;
+      float m = -INFINITY, l = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < kRowsB; c += 32) {
+        float x[32];
+        tmem_ld32(tbase + c, x);
+        const int n_vis = min(32, p.n_ctx - (key0 + c));
+        float mc = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float mx = -INFINITY;
+        for (int j = 0; j < 32; ++j) if (j < n_vis) mc = fmaxf(mc, x[j] * sl2);
+        if (mc == -INFINITY) continue;
+        const float mn = fmaxf(m, mc);
+        float sum = 0.f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (4 * tx + j < nk) mx = fmaxf(mx, acc[i][j]);
-    for (int o = 8; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float sum = 0.f;
+        for (int j = 0; j < 32; ++j) if (j < n_vis) sum += exp2f(x[j] * sl2 - mn);
+        l = l * exp2f(m - mn) + sum;
+        m = mn;
+      }
+      if (i < group_rows) part0[(int64_t)kt * (p.Hkv * group_rows) + g * group_rows + i] = make_float2(m, l);
+    } else {
+      // key me of the tile over its 256 query rows
+      const int t = key0 + me;
+      float acc = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < kRowsB; c += 32) {
+        float x[32];
+        tmem_ld32(tbase + c, x);
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (4 * tx + j < nk) sum += exp2f(acc[i][j] - mx);
-    for (int o = 8; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (tx == 0 && 8 * ty + i < nr)
-      part[(int64_t)blockIdx.x * n_rows + r0 + 8 * ty + i] = make_float2(mx, sum);
+        for (int j = 0; j < 32; ++j) {
+          const float2 w = s_ml[c + j];
+          acc += exp2f(x[j] * sl2 - w.x) * w.y;
+        }
+      }
+      if (t < p.n_ctx) partI[(int64_t)blockIdx.y * p.n_ctx + t] = acc;
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after();
+    tmem_dealloc(tmem, kMassCols);
   }
 }
 
 // Each row's softmax statistics over all of the request's keys: the maximum
-// and the reciprocal of the sum (the sum pass multiplies).
+// and the reciprocal of the sum.
 __global__ void mass_stats_kernel(const float2 *__restrict__ part, int n_chunks, int n_rows,
                                   float2 *__restrict__ ml) {
   grid_dep_wait();
@@ -258,28 +338,21 @@ __global__ void mass_stats_kernel(const float2 *__restrict__ part, int n_chunks,
   float L = 0.f;
   for (int c = 0; c < n_chunks; ++c) {
     const float2 v = part[(int64_t)c * n_rows + r];
-    L += v.y * exp2f(v.x - M);
+    if (v.x != -INFINITY) L += v.y * exp2f(v.x - M);
   }
-  ml[r] = make_float2(M, 1.f / L);
+  ml[r] = make_float2(M, L > 0.f ? 1.f / L : 0.f);
 }
 
-// One warp per key: I[t] += sum over every row of 2^(s - m_r) / l_r (ml holds
-// m_r and 1 / l_r), lanes striding the rows, then a fixed-order butterfly.
-__global__ void mass_sum_kernel(const float *__restrict__ s, const float2 *__restrict__ ml,
-                                int n_rows, int n_ctx, float *__restrict__ mass) {
+// I[t] += the row tiles' sums for key t, in row-tile order.
+__global__ void mass_final_kernel(const float *__restrict__ partI, int n_parts, int n_ctx,
+                                  float *__restrict__ mass) {
   grid_dep_wait();
   grid_dep_launch();
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= n_ctx) return;
-  const float *row = s + (int64_t)t * n_rows;
   float acc = 0.f;
-  for (int r = lane; r < n_rows; r += 32) {
-    const float2 v = ml[r];
-    acc += exp2f(row[r] - v.x) * v.y;
-  }
-  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) mass[t] += acc;
+  for (int j = 0; j < n_parts; ++j) acc += partI[(int64_t)j * n_ctx + t];
+  mass[t] += acc;
 }
 
 }  // namespace qp
@@ -343,49 +416,95 @@ cudaError_t launch_probe_rows(const ProbeLayout &L, const int32_t *anchors, int3
   return launched(1);
 }
 
-size_t mass_ws_bytes(int n_u, int Hq, int n_ctx) {
-  const int64_t rows = (int64_t)Hq * n_u;
-  const int64_t chunks = (n_ctx + qp::KC - 1) / qp::KC;
-  return (size_t)(rows * n_ctx * 4 + chunks * rows * 8 + rows * 8) + 3 * 256;
+// Scratch of one request's mass: the gathered query rows, the statistics
+// tiles' (max, sum), the rows' (max, 1 / sum), the mass tiles' key sums.
+struct MassLayout {
+  size_t qg, part0, ml, partI, total;
+  int pad, n_kt0, n_kt1, rt0, rt1;
+};
+static MassLayout mass_layout(int n_u, int Hq, int Hkv, int n_ctx) {
+  MassLayout L;
+  const int G = Hq / Hkv, rows = G * n_u;
+  L.pad = qp::group_pad(rows);
+  L.rt0 = (rows + qp::kRowsA - 1) / qp::kRowsA;
+  L.rt1 = L.pad / qp::kRowsB;
+  L.n_kt0 = (n_ctx + qp::kRowsB - 1) / qp::kRowsB;
+  L.n_kt1 = (n_ctx + qp::kRowsA - 1) / qp::kRowsA;
+  auto up = [](size_t b) { return (b + 255) / 256 * 256; };
+  size_t off = 0;
+  L.qg = off;
+  off += up((size_t)Hkv * L.pad * qp::HD * sizeof(bf16));
+  L.part0 = off;
+  off += up((size_t)L.n_kt0 * Hq * n_u * sizeof(float2));
+  L.ml = off;
+  off += up((size_t)Hq * n_u * sizeof(float2));
+  L.partI = off;
+  off += up((size_t)Hkv * L.rt1 * n_ctx * sizeof(float));
+  L.total = off;
+  return L;
+}
+
+size_t mass_ws_bytes(int n_u, int Hq, int Hkv, int n_ctx) {
+  if (n_u <= 0 || n_ctx <= 0 || Hkv <= 0) return 256;
+  return mass_layout(n_u, Hq, Hkv, n_ctx).total;
 }
 
 cudaError_t launch_attention_mass(const void *q, int64_t ld_q, int u_off, int n_u,
                                   const void *k_cache, int64_t ld_k, int t_off, int n_ctx,
                                   int Hq, int Hkv, int hd, void *ws, size_t ws_bytes,
-                                  float *mass, cudaStream_t s) {
+                                  float *mass, int *status, cudaStream_t s) {
   using namespace qp;
   if (n_u <= 0 || n_ctx <= 0) return cudaSuccess;
   if (hd != HD || Hq % Hkv) return cudaErrorInvalidValue;
-  if (!ws || ws_bytes < mass_ws_bytes(n_u, Hq, n_ctx)) return cudaErrorInvalidValue;
-  const int n_rows = Hq * n_u;
-  const int n_chunks = (n_ctx + KC - 1) / KC;
+  const MassLayout Lo = mass_layout(n_u, Hq, Hkv, n_ctx);
+  if (!ws || ws_bytes < Lo.total) return cudaErrorInvalidValue;
   char *w = reinterpret_cast<char *>(ws);
-  float *sc = reinterpret_cast<float *>(w);
-  w += ((size_t)n_rows * n_ctx * 4 + 255) / 256 * 256;
-  float2 *part = reinterpret_cast<float2 *>(w);
-  w += ((size_t)n_chunks * n_rows * 8 + 255) / 256 * 256;
-  float2 *ml = reinterpret_cast<float2 *>(w);
-  const float scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
+  bf16 *qg = reinterpret_cast<bf16 *>(w + Lo.qg);
+  float2 *part0 = reinterpret_cast<float2 *>(w + Lo.part0);
+  float2 *ml = reinterpret_cast<float2 *>(w + Lo.ml);
+  float *partI = reinterpret_cast<float *>(w + Lo.partI);
+  const int G = Hq / Hkv, n_rows = Hq * n_u;
+  MassParams p{n_ctx, n_u, G, Hkv, Lo.pad, Lo.rt0, Lo.n_kt0,
+               1.4426950408889634f / sqrtf((float)hd), t_off};
+  // keys: the context rows only (rows past them read as zeros and are masked)
+  CUtensorMap mq0, mq1, mk0, mk1;
+  if (!tcx::make_map(&mq0, qg, (int64_t)Hkv * Lo.pad, HD, HD, kRowsA) ||
+      !tcx::make_map(&mq1, qg, (int64_t)Hkv * Lo.pad, HD, HD, kRowsB) ||
+      !tcx::make_map(&mk0, k_cache, (int64_t)t_off + n_ctx, (int64_t)Hkv * HD, ld_k, kRowsB) ||
+      !tcx::make_map(&mk1, k_cache, (int64_t)t_off + n_ctx, (int64_t)Hkv * HD, ld_k, kRowsA))
+    return cudaErrorInvalidValue;
   static PerDeviceOnce attr;
-  cudaError_t ea = attr.run([](int) {
-    return cudaFuncSetAttribute(mass_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kScoreSmem);
+  cudaError_t e = attr.run([](int) {
+    cudaError_t r = cudaFuncSetAttribute(mass_tc_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kMassSmem);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(mass_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kMassSmem);
+    return r;
   });
-  if (ea != cudaSuccess) return ea;
-  const int tiles_per_group = ((Hq / Hkv) * n_u + RC - 1) / RC;
-  cudaError_t e = launch_pdl(mass_score_kernel, dim3(n_chunks, Hkv * tiles_per_group),
-                             dim3(kTileThreads), kScoreSmem, s,
-                             reinterpret_cast<const bf16 *>(q), ld_q, u_off, n_u,
-                             reinterpret_cast<const bf16 *>(k_cache), ld_k, t_off, n_ctx, Hq, Hkv,
-                             scale_log2, sc, part);
+  if (e != cudaSuccess) return e;
+  const int64_t units = (int64_t)Hkv * Lo.pad * 16;
+  e = launch_pdl(mass_gather_kernel, dim3((unsigned)((units + 255) / 256)), dim3(256), 0, s,
+                 reinterpret_cast<const bf16 *>(q), ld_q, u_off, n_u, G, Hkv, qg);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(mass_tc_kernel<false>, dim3(Lo.n_kt0, Hkv * Lo.rt0), dim3(kMassThreads),
+                 kMassSmem, s, mq0, mk0, p, part0, (const float2 *)nullptr, (float *)nullptr,
+                 status);
   if (e != cudaSuccess) return e;
   e = launch_pdl(mass_stats_kernel, dim3((n_rows + 255) / 256), dim3(256), 0, s,
-                 (const float2 *)part, n_chunks, n_rows, ml);
+                 (const float2 *)part0, Lo.n_kt0, n_rows, ml);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(mass_sum_kernel, dim3((n_ctx * 32 + 255) / 256), dim3(256), 0, s,
-                 (const float *)sc, (const float2 *)ml, n_rows, n_ctx, mass);
+  MassParams p1 = p;
+  p1.rt_per_g = Lo.rt1;
+  p1.n_kt = Lo.n_kt1;
+  e = launch_pdl(mass_tc_kernel<true>, dim3(Lo.n_kt1, Hkv * Lo.rt1), dim3(kMassThreads),
+                 kMassSmem, s, mq1, mk1, p1, (float2 *)nullptr, (const float2 *)ml, partI,
+                 status);
   if (e != cudaSuccess) return e;
-  return launched(3);
+  e = launch_pdl(mass_final_kernel, dim3((n_ctx + 255) / 256), dim3(256), 0, s,
+                 (const float *)partI, Hkv * Lo.rt1, n_ctx, mass);
+  if (e != cudaSuccess) return e;
+  return launched(5);
 }
 
 }  // namespace cb
