@@ -1507,9 +1507,7 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
   }
   // 4. computed rows: selected context rows + uncached rows, gathered once
   probe_mark(CB_PROBE_GATHER, true, s);
-  CB_CUDA(launch_build_rows(P.bm, sel, pos_c, glob_c, (int)P.R_total, st, s));
-  CB_CUDA(launch_gather(h_all, d, P.T_total, glob_c, (int)P.R_total, d, h_c, d, sizeof(float),
-                        st, s));
+  CB_CUDA(launch_rows_gather(P.bm, sel, pos_c, glob_c, (int)P.R_total, h_all, d, h_c, st, s));
   probe_mark(CB_PROBE_GATHER, false, s);
   // 5. layers >= s on the computed rows; gradual filtering steps shrink the
   // set between layers (the rows alternate between two buffer sets)

@@ -145,6 +145,11 @@ cudaError_t launch_selection(const float *dev, const SelPlan &plan, int32_t *idx
 cudaError_t launch_build_rows(const BatchMeta &bm, const int32_t *sel,
                               int32_t *pos, int32_t *glob, int n_rows,
                               int *status, cudaStream_t s);
+// launch_build_rows followed by the gather of the rows' hidden states
+// (h_dst[r] = h_src[glob[r]], d floats, d % 4 == 0), in one kernel.
+cudaError_t launch_rows_gather(const BatchMeta &bm, const int32_t *sel, int32_t *pos,
+                               int32_t *glob, int n_rows, const float *h_src, int d,
+                               float *h_dst, int *status, cudaStream_t s);
 // One gradual-filtering step: from the current rows (cur) to the rows kept
 // (nxt, same requests, k'_b <= k_b); keep holds k'_b ascending local
 // indices per request at nxt.k_off[b].

@@ -157,6 +157,8 @@ __device__ void topk_block(const float *d, int n, int k, int32_t *__restrict__ o
         if ((key & mask) == prefix) { active = true; digit = (key >> shift) & 255u; }
       }
       // warp-aggregated histogram update: one atomic per distinct digit
+      // (deviations share their leading bits, so plain atomics would pile
+      // onto a few bins)
       const unsigned act = __ballot_sync(0xffffffffu, active);
       if (active) {
         const unsigned peers = __match_any_sync(act, digit);
@@ -182,9 +184,7 @@ __device__ void topk_block(const float *d, int n, int k, int32_t *__restrict__ o
       }
       const uint32_t excl = incl - mysum;
       const uint32_t rem = (uint32_t)s_remaining;
-      const bool mine = excl < rem && incl >= rem;
-      const unsigned who = __ballot_sync(0xffffffffu, mine);
-      if (mine) {
+      if (excl < rem && incl >= rem) {
         uint32_t acc = excl;
         int j = 0;
         for (; j < 8; ++j) {
@@ -196,14 +196,40 @@ __device__ void topk_block(const float *d, int n, int k, int32_t *__restrict__ o
         s_mask = mask | (255u << shift);
         s_remaining = (int)(rem - acc);
       }
-      (void)who;
     }
     __syncthreads();
   }
   const uint32_t thr = s_prefix;     // key of the k-th largest value
   const int need_eq = s_remaining;   // how many keys equal to thr to take
   // ---- ordered compaction: keep key > thr, and the first need_eq keys
-  // equal to thr in index order.
+  // equal to thr in index order.  Thread t owns the contiguous range
+  // [t * per, (t + 1) * per); one block scan of its packed (greater, equal)
+  // counts gives every output position (a key's position is the number of
+  // greater keys before it plus the taken equal keys before it).
+  if (n < 32768) {     // both packed counts stay below 2^15
+    const int per = (n + kSelThreads - 1) / kSelThreads;
+    const int i0 = tid * per, i1 = min(n, i0 + per);
+    int gt = 0, eq = 0;
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t key = float_key(d[i]);
+      gt += key > thr;
+      eq += key == thr;
+    }
+    int total;
+    const int before = block_exclusive_scan((gt << 16) | eq, warp_buf, &total);
+    int g = before >> 16, e = before & 0xFFFF;
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t key = float_key(d[i]);
+      if (key > thr) {
+        out[g + min(e, need_eq)] = i;
+        ++g;
+      } else if (key == thr) {
+        if (e < need_eq) out[g + e] = i;
+        ++e;
+      }
+    }
+    return;
+  }
   int taken_eq = 0, written = 0;
   for (int base = 0; base < n; base += kSelThreads) {
     const int i = base + tid;
@@ -577,6 +603,47 @@ __global__ void build_rows_kernel(const __grid_constant__ BatchMeta bm,
   }
   pos[r] = p;
   glob[r] = bm.t_off[b] + p;
+}
+
+// build_rows_kernel and the gather of the rows' hidden states in one
+// launch: block r computes row r's position and cache row, then copies its
+// d floats of h (16-byte vectors).
+__global__ void __launch_bounds__(256)
+rows_gather_kernel(const __grid_constant__ BatchMeta bm, const int32_t *__restrict__ sel,
+                   int32_t *__restrict__ pos, int32_t *__restrict__ glob,
+                   const float *__restrict__ h_src, int d, float *__restrict__ h_dst,
+                   int *status) {
+  grid_dep_wait();      // the selection comes from the previous kernel
+  grid_dep_launch();
+  __shared__ int64_t s_src;
+  const int r = blockIdx.x;
+  if (threadIdx.x == 0) {
+    int b = 0;
+    while (bm.r_off[b + 1] <= r) ++b;
+    const int j = r - bm.r_off[b];
+    const int kb = bm.k_off[b + 1] - bm.k_off[b];
+    int p = j < kb ? sel[bm.k_off[b] + j] : bm.n_ctx[b] + (j - kb);
+    if (p < 0 || p >= (j < kb ? bm.n_ctx[b] : bm.t_off[b + 1] - bm.t_off[b])) {
+      report(status, CB_ERR_DEVICE_INDEX);
+      p = 0;
+    }
+    pos[r] = p;
+    glob[r] = bm.t_off[b] + p;
+    s_src = (int64_t)(bm.t_off[b] + p) * d;
+  }
+  __syncthreads();
+  const float4 *src = reinterpret_cast<const float4 *>(h_src + s_src);
+  float4 *dst = reinterpret_cast<float4 *>(h_dst + (int64_t)r * d);
+  for (int i = threadIdx.x; i < d / 4; i += 256) dst[i] = __ldg(src + i);
+}
+
+cudaError_t launch_rows_gather(const BatchMeta &bm, const int32_t *sel, int32_t *pos,
+                               int32_t *glob, int n_rows, const float *h_src, int d,
+                               float *h_dst, int *status, cudaStream_t s) {
+  if (n_rows == 0) return cudaSuccess;
+  cudaError_t e = launch_pdl(rows_gather_kernel, dim3(n_rows), dim3(256), 0, s, bm, sel, pos, glob,
+                             h_src, d, h_dst, status);
+  return e != cudaSuccess ? e : launched(1);
 }
 
 cudaError_t launch_build_rows(const BatchMeta &bm, const int32_t *sel,
