@@ -168,8 +168,8 @@ def setup_replica(rank, device, n_layers=None):
 # compact layer: the CTA-pair swapped GEMM), valid only for the kernel source
 # it was taken on.
 TRAFFIC_CAPTURE = {"source": "rag_kv_cache_layer_gb300/csrc/k_gemm_sab.cu",
-                   "sha256": "d80816d0c586d27f847ae7e0b733c2a7bb2fac60fc8abf1ca7aaf9230850afaa",
-                   "bytes_per_launch": 241400320 + 18620672,
+                   "sha256": "0cd1506b54829ca7a9f43e31eaa122b1c89fa33e35e2f1137e0db1107f48be8c",
+                   "bytes_per_launch": 241362944 + 17981440,
                    "profile": "profiles/gemm_swiglu_M524_llama8b.md"}
 
 

@@ -456,6 +456,20 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
             for (int u = 0; u < 4; ++u) rf[q][u] = __ldg(src + u);
           }
         }
+        // K-deviation: the reused keys this thread compares, also loaded
+        // before the transpose
+        uint4 kraw[EPI == EPI_KDEV ? 4 : 1];
+        if (EPI == EPI_KDEV) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int i = (t >> 4) + 8 * q;
+            const bool use = c + i < p.BT && tok0 + c + i < p.M && s_dev[c + i] >= 0;
+            kraw[q] = use ? __ldg(reinterpret_cast<const uint4 *>(
+                                reinterpret_cast<const bf16 *>(p.k_cache) + s_dst[c + i] * p.ld_kv +
+                                head * 128 + 8 * (t & 15)))
+                          : make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
         // transpose: feature column r of 32 tokens -> rows of the chunk
 #pragma unroll
         for (int i = 0; i < 32; ++i) tr[i * kTrStride + r] = x[i];
@@ -521,15 +535,13 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
               const float *row = tr + i * kTrStride;
               const int e0 = 8 * (j & 7);
               const float *w = reinterpret_cast<const float *>(rf[q]);   // (cos, sin) x 8
-              float kr[8];
-              load16<bf16>(reinterpret_cast<const bf16 *>(p.k_cache) + s_dst[c + i] * p.ld_kv +
-                               head * 128 + 8 * j, kr);
+              const bf16 *kb = reinterpret_cast<const bf16 *>(&kraw[q]);
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
                 const float x1 = row[e0 + e], x2 = row[64 + e0 + e];
                 const float co = w[2 * e], si = w[2 * e + 1];
                 const float y = j < 8 ? x1 * co - x2 * si : x2 * co + x1 * si;
-                const float dlt = y - kr[e];
+                const float dlt = y - __bfloat162float(kb[e]);
                 acc = fmaf(dlt, dlt, acc);
               }
             }
