@@ -293,31 +293,43 @@ def test_doc_aligned_golden():
         assert list(got) == c["expect"], c
 
 
-def _brute_doc_aligned(d, offs, k):
-    """Same policy stated as a search: try spans in rank order, the first
-    span that cannot be taken whole gets the best window found by checking
-    every start; exactly k tokens."""
+def _doc_aligned_properties_hold(d, offs, k, got):
+    """Checks a selection against the statements of "Request Order Matters"
+    §2.3 (Eq. 3 and the policy text) one by one, without re-running the
+    policy: the result splits into whole spans W and at most one contiguous
+    window inside one further span p; W is a prefix of the spans ranked by
+    mean deviation (ties: lower span), skipping none that would fit; p is the
+    first ranked span after W (the first that does not fit), and the window
+    has the largest total deviation among all windows of its length inside p,
+    leftmost on ties; exactly k tokens."""
     spans = [(a, b) for a, b in zip(offs[:-1], offs[1:]) if b > a]
-    ranked = sorted(range(len(spans)), key=lambda j: (
-        -sum(d[spans[j][0]:spans[j][1]]) / (spans[j][1] - spans[j][0]), j))
-    out, rem = set(), k
-    for j in ranked:
-        a, b = spans[j]
-        if rem == 0:
-            break
-        if b - a <= rem:
-            out |= set(range(a, b))
-            rem -= b - a
-        else:
-            starts = list(range(a, b - rem + 1))
-            sums = [sum(d[s:s + rem]) for s in starts]
-            s = starts[sums.index(max(sums))]
-            out |= set(range(s, s + rem))
-            rem = 0
-    return sorted(out)
+    got = set(int(i) for i in got)
+    if len(got) != k:
+        return False
+    whole = [j for j, (a, b) in enumerate(spans) if set(range(a, b)) <= got]
+    rest = got - set().union(*[set(range(*spans[j])) for j in whole]) if whole else set(got)
+    mean = lambda j: sum(d[spans[j][0]:spans[j][1]]) / (spans[j][1] - spans[j][0])
+    ranked = sorted(range(len(spans)), key=lambda j: (-mean(j), j))
+    # W is exactly the first len(W) ranked spans
+    if sorted(whole) != sorted(ranked[:len(whole)]):
+        return False
+    if not rest:
+        # no window: the budget is used up by whole spans (or k covers everything)
+        return sum(spans[j][1] - spans[j][0] for j in whole) == k
+    # the window: contiguous, inside the next ranked span, which does not fit whole
+    p = ranked[len(whole)]
+    a, b = spans[p]
+    lo, hi = min(rest), max(rest)
+    if not (a <= lo and hi < b and hi - lo + 1 == len(rest)):
+        return False
+    if b - a <= k - sum(spans[j][1] - spans[j][0] for j in whole):
+        return False          # p would have fitted whole
+    w = len(rest)
+    sums = [sum(d[s:s + w]) for s in range(a, b - w + 1)]
+    return sums[lo - a] == max(sums) and sums.index(max(sums)) == lo - a
 
 
-def test_doc_aligned_random_vs_search():
+def test_doc_aligned_random_against_the_policy_statements():
     rng = np.random.default_rng(11)
     for _ in range(200):
         m = rng.integers(1, 6)
@@ -329,8 +341,21 @@ def test_doc_aligned_random_vs_search():
         d = rng.integers(0, 5, size=N).astype(float)
         for k in range(0, N + 1):
             got = list(O.doc_aligned_select(d, offs, k))
-            assert len(got) == k
-            assert got == _brute_doc_aligned(d, offs, k)
+            assert _doc_aligned_properties_hold(d, offs, k, got), (d, offs, k, got)
+
+
+def test_doc_aligned_property_check_rejects_wrong_selections():
+    # the property check itself: a selection that breaks each statement fails
+    d = np.array([5.0, 5, 1, 1, 9, 9, 9, 0], dtype=float)
+    offs = [0, 2, 4, 8]        # means 5, 1, 6.75
+    assert _doc_aligned_properties_hold(d, offs, 6, [0, 1, 4, 5, 6, 7])
+    assert not _doc_aligned_properties_hold(d, offs, 6, [0, 1, 2, 3, 4, 5])   # skips rank 2
+    assert _doc_aligned_properties_hold(d, offs, 5, [0, 4, 5, 6, 7])          # tie in span 0: leftmost
+    assert not _doc_aligned_properties_hold(d, offs, 5, [1, 4, 5, 6, 7])      # not the leftmost
+    assert not _doc_aligned_properties_hold(d, offs, 5, [3, 4, 5, 6, 7])      # window not in the next span
+    assert _doc_aligned_properties_hold(d, offs, 3, [4, 5, 6])                # best window of span 2
+    assert not _doc_aligned_properties_hold(d, offs, 3, [5, 6, 7])            # not the best window
+    assert not _doc_aligned_properties_hold(d, offs, 2, [4])                  # wrong size
 
 
 def test_doc_aligned_whole_document_budget():
