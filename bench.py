@@ -168,8 +168,8 @@ def setup_replica(rank, device, n_layers=None):
 # compact layer: the CTA-pair swapped GEMM), valid only for the kernel source
 # it was taken on.
 TRAFFIC_CAPTURE = {"source": "rag_kv_cache_layer_gb300/csrc/k_gemm_sab.cu",
-                   "sha256": "0cd1506b54829ca7a9f43e31eaa122b1c89fa33e35e2f1137e0db1107f48be8c",
-                   "bytes_per_launch": 241362944 + 17981440,
+                   "sha256": "60654291e3b221627eb7645f7a5550b0de02fe653f88bda79b81721245f958c0",
+                   "bytes_per_launch": 241381888 + 18391808,
                    "profile": "profiles/gemm_swiglu_M524_llama8b.md"}
 
 

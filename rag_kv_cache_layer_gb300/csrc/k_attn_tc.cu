@@ -435,11 +435,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   __shared__ int s_unit[7];        // b, g, tile, first block, end block, split (-1: none), slot
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Before the grid dependency wait: the unit table and q_pos come from
-  // kernels two or more launches back (complete once the previous kernel
-  // could start this one), so the unit decode, the barriers and the TMEM
-  // allocation overlap the previous kernel's tail; only Q and the cache are
-  // read after the wait.
+  grid_dep_wait();      // q, the cache and q_pos come from earlier kernels
+  grid_dep_launch();
   if (threadIdx.x == 0) {
     // this CTA's unit: a tile and a range of its key blocks
     int tile, jb, jcap, split;
@@ -501,8 +498,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   const int n_valid = min(P.QT, R.q_end - row0);  // q rows of the request in the tile
   if (nb == 0) {
     // a key chunk past the tile's last query: an empty partial, nothing else
-    grid_dep_wait();
-    grid_dep_launch();
     if (split && threadIdx.x < 128 && (int)threadIdx.x % P.QT < n_valid)
       part_ml[pslot * 128 + threadIdx.x] = make_float2(-INFINITY, 0.f);
     return;
@@ -518,8 +513,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_slot;
-  grid_dep_wait();      // q and the cache come from the previous kernels
-  grid_dep_launch();
 
   if (warp == 0 && lane < 2) {
     // ----------------------------------------------- producers (K: lane 0, V: lane 1)
@@ -779,8 +772,7 @@ attn_combine_kernel(const __grid_constant__ Params P, const bf16 *__restrict__ p
   const int row0 = R.q_begin + id.t * P.QT;
   const int n_valid = min(P.QT, R.q_end - row0);
   // lane c holds partial c's (m, l) of each row: the weights come from warp
-  // reductions; then the rows of up to four partials are loaded together
-  // (one round of L2 latency per four partials) and summed
+  // reductions, then the partial rows are read back to back
   float M[kCombineRows], l[kCombineRows];
   float4 o[kCombineRows];
 #pragma unroll
@@ -789,53 +781,39 @@ attn_combine_kernel(const __grid_constant__ Params P, const bf16 *__restrict__ p
     l[r] = 0.f;
     o[r] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  for (int c0 = 0; c0 < count; c0 += 32) {
-    float2 ml[kCombineRows];
+  for (int c = lane; c < count; c += 32) {
 #pragma unroll
-    for (int r = 0; r < kCombineRows; ++r) {
-      ml[r] = c0 + lane < count ? part_ml[((int64_t)first + c0 + lane) * 128 + row_base + 8 * r]
-                                : make_float2(-INFINITY, 0.f);
-      float mx = ml[r].x;
-      for (int s = 16; s; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
-      // a later chunk of 32 partials can raise the maximum: rescale
-      const float Mn = fmaxf(M[r], mx);
-      if (Mn != -INFINITY && M[r] != Mn && M[r] != -INFINITY) {
-        const float f = exp2f(M[r] - Mn);
-        l[r] *= f;
-        o[r].x *= f; o[r].y *= f; o[r].z *= f; o[r].w *= f;
-      }
-      M[r] = Mn;
-    }
+    for (int r = 0; r < kCombineRows; ++r)
+      M[r] = fmaxf(M[r], part_ml[((int64_t)first + c) * 128 + row_base + 8 * r].x);
+  }
+#pragma unroll
+  for (int r = 0; r < kCombineRows; ++r)
+    for (int s = 16; s; s >>= 1) M[r] = fmaxf(M[r], __shfl_xor_sync(0xffffffffu, M[r], s));
+  for (int c0 = 0; c0 < count; c0 += 32) {
     float w[kCombineRows];
 #pragma unroll
     for (int r = 0; r < kCombineRows; ++r) {
+      const float2 ml = c0 + lane < count
+                            ? part_ml[((int64_t)first + c0 + lane) * 128 + row_base + 8 * r]
+                            : make_float2(-INFINITY, 0.f);
       // a chunk's weight is its sum l rescaled to the common maximum (its
       // partial is already divided by l); an empty chunk has none
-      w[r] = ml[r].x == -INFINITY ? 0.f : exp2f(ml[r].x - M[r]) * ml[r].y;
+      w[r] = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M[r]) * ml.y;
       l[r] += w[r];
     }
     const int n = min(32, count - c0);
-    for (int i0 = 0; i0 < n; i0 += 4) {
-      uint2 raw[4][kCombineRows];
+    for (int i = 0; i < n; ++i) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int r = 0; r < kCombineRows; ++r)
-          raw[i][r] = i0 + i < n ? reinterpret_cast<const uint2 *>(
-                                       part_o + (((int64_t)first + c0 + i0 + i) * 128 + row_base +
-                                                 8 * r) * HD)[lane]
-                                 : make_uint2(0u, 0u);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int r = 0; r < kCombineRows; ++r) {
-          const float wi = __shfl_sync(0xffffffffu, w[r], (i0 + i) & 31);
-          if (i0 + i < n && wi != 0.f) {
-            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw[i][r].x));
-            const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw[i][r].y));
-            o[r].x += wi * a.x; o[r].y += wi * a.y; o[r].z += wi * b.x; o[r].w += wi * b.y;
-          }
+      for (int r = 0; r < kCombineRows; ++r) {
+        const float wi = __shfl_sync(0xffffffffu, w[r], i);
+        if (wi != 0.f) {
+          const uint2 raw = reinterpret_cast<const uint2 *>(
+              part_o + (((int64_t)first + c0 + i) * 128 + row_base + 8 * r) * HD)[lane];
+          const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
+          const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
+          o[r].x += wi * a.x; o[r].y += wi * a.y; o[r].z += wi * b.x; o[r].w += wi * b.y;
         }
+      }
     }
   }
 #pragma unroll

@@ -40,9 +40,15 @@ def bf16_values(a):
 
 def ties_ok(sel_gpu, sel_ref, d_ref, k, rel=1e-3):
     """Selected sets agree except for positions whose reference deviation
-    ties the k-th largest within ``rel`` (relative)."""
+    ties the k-th largest within ``rel`` (relative).  Deviations below 1e-12
+    of the largest are zero up to float64 rounding -- the first chunk's are
+    exactly zero in exact arithmetic ("Request Order Matters" §2.2: its
+    prefix is unchanged) -- so they tie with each other and with a zero k-th
+    value."""
     if k == 0:
         return len(sel_gpu) == 0
+    d_ref = np.asarray(d_ref, np.float64)
+    zero = 1e-12 * float(np.max(np.abs(d_ref))) if d_ref.size else 0.0
     kth = np.sort(d_ref)[::-1][k - 1]
     diff = set(map(int, sel_gpu)) ^ set(map(int, sel_ref))
-    return all(abs(d_ref[i] - kth) <= rel * max(abs(kth), 1e-30) for i in diff)
+    return all(abs(d_ref[i] - kth) <= max(rel * abs(kth), zero, 1e-300) for i in diff)

@@ -1,0 +1,145 @@
+"""Edge shapes through the whole blended prefill against the oracle:
+
+* ragged chunks (1, 37, 200 and 63 tokens) and a 5-token query on the fp32
+  model, so no length is a multiple of a tile, a block or a warp;
+* the largest batch one call takes (CB_MAX_BATCH = 64 requests of two short
+  chunks and a 1-4-token query each, drawn from a shared pool), each
+  request checked alone against the oracle;
+* the degenerate budgets: one cached token with the smallest nonzero ratio
+  (k = max(1, floor(N r)) = 1, the only token) and r = 0 (pure reuse), with
+  a one-token query;
+* the bf16 tensor-core path on ragged chunks (100, 333 and 7 tokens + 13
+  query tokens) with the oracle's selection imposed: row counts that leave
+  partial GEMM tiles and attention tiles everywhere.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workload as W
+import rag_kv_cache_layer_gb300 as R
+from rag_kv_cache_layer_gb300 import _lib as L
+from gpu_common import assert_close, host, rms_rel, ties_ok
+
+pytestmark = pytest.mark.gpu
+
+
+class Stack:
+    """A model on the device and in the oracle, with a chunk pool in both."""
+
+    def __init__(self, shape, seed, chunks, max_pos=4096):
+        self.shape = shape
+        self.weights = W.make_weights(shape, seed)
+        self.model = R.BlendModel.from_host(shape, self.weights, max_pos)
+        self.om = O.model_from_weights(shape, self.weights)
+        self.chunks = chunks
+        self.store = R.ChunkStore(self.model, sum(len(c) for c in chunks))
+        self.store.prefill({i: torch.from_numpy(c).cuda() for i, c in enumerate(chunks)})
+        self.ostore = O.chunk_prefill_all(self.om, chunks)
+        torch.cuda.synchronize()
+
+    def gpu_req(self, chunk_ids, query):
+        toks = np.concatenate([self.chunks[i] for i in chunk_ids] + [query]).astype(np.int32)
+        segs = [self.store.seg(i) for i in chunk_ids] + [R.Seg(len(query))]
+        return R.Req(torch.from_numpy(toks).cuda(), segs)
+
+    def oracle(self, chunk_ids, query, ratio_bp, **kw):
+        segs = [(self.chunks[i], True) for i in chunk_ids] + [(query, False)]
+        return O.blend_prefill(self.om, segs, [self.ostore[i] for i in chunk_ids], ratio_bp, **kw)
+
+
+def _check_fp32(out, ref, t0, T, r0, k0, k):
+    """Request at fused-cache rows [t0, t0 + T), computed rows from r0,
+    selection from k0."""
+    sel = out["selected"][k0:k0 + k].cpu().numpy()
+    assert ties_ok(sel, ref.selected, ref.deviation, k)
+    if set(sel.tolist()) == set(ref.selected.tolist()):
+        assert_close(host(out["k_cache"][:, t0:t0 + T]), ref.K, torch.float32)
+        assert_close(host(out["v_cache"][:, t0:t0 + T]), ref.V, torch.float32)
+        Rn = len(ref.rows)
+        assert np.array_equal(out["rows"][r0:r0 + Rn].cpu().numpy(), ref.rows)
+        assert_close(host(out["hidden"][r0:r0 + Rn]), ref.hidden, torch.float32)
+
+
+def test_ragged_chunks_fp32():
+    rng = np.random.default_rng(5)
+    shape = W.TINY_F32
+    chunks = [W.make_tokens(rng, n, shape.vocab) for n in (1, 37, 200, 63)]
+    st = Stack(shape, 3, chunks)
+    query = W.make_tokens(rng, 5, shape.vocab)
+    ids = [0, 1, 2, 3]
+    out = st.model.cb_blend_prefill([st.gpu_req(ids, query)], 1500)
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    ref = st.oracle(ids, query, 1500)
+    assert len(ref.selected) == O.select_count(301, 1500) == 45
+    _check_fp32(out, ref, 0, 306, 0, 0, 45)
+
+
+def test_largest_batch_fp32():
+    rng = np.random.default_rng(6)
+    shape = W.TINY_F32
+    pool = [W.make_tokens(rng, int(rng.integers(1, 25)), shape.vocab) for _ in range(40)]
+    st = Stack(shape, 4, pool)
+    B = L.CB_MAX_BATCH
+    picks = [rng.choice(len(pool), size=2, replace=False).tolist() for _ in range(B)]
+    queries = [W.make_tokens(rng, int(rng.integers(1, 5)), shape.vocab) for _ in range(B)]
+    reqs = [st.gpu_req(p, q) for p, q in zip(picks, queries)]
+    out = st.model.cb_blend_prefill(reqs, 3000)
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    t0 = r0 = k0 = 0
+    for p, q in zip(picks, queries):
+        ref = st.oracle(p, q, 3000)
+        T = sum(len(pool[i]) for i in p) + len(q)
+        k = len(ref.selected)
+        _check_fp32(out, ref, t0, T, r0, k0, k)
+        t0, r0, k0 = t0 + T, r0 + len(ref.rows), k0 + k
+    with pytest.raises(L.CBError):          # one more request than a call takes
+        st.model.cb_blend_prefill(reqs + reqs[:1], 3000)
+
+
+@pytest.mark.parametrize("ratio_bp", [1, 0])
+def test_one_cached_token_budgets(ratio_bp):
+    rng = np.random.default_rng(7)
+    shape = W.TINY_F32
+    chunks = [W.make_tokens(rng, 1, shape.vocab)]
+    st = Stack(shape, 5, chunks)
+    query = W.make_tokens(rng, 1, shape.vocab)
+    out = st.model.cb_blend_prefill([st.gpu_req([0], query)], ratio_bp)
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    ref = st.oracle([0], query, ratio_bp)
+    k = O.select_count(1, ratio_bp)
+    assert len(ref.selected) == k == (1 if ratio_bp else 0)
+    _check_fp32(out, ref, 0, 2, 0, 0, k)
+    assert int(out["first_token"][0]) == ref.token or \
+        O.first_token_logits(st.om, ref.hidden[-1])[int(out["first_token"][0])] >= \
+        O.first_token_logits(st.om, ref.hidden[-1]).max() - 1e-4
+
+
+def test_ragged_chunks_bf16_forced():
+    rng = np.random.default_rng(8)
+    shape = W.LLAMA3_8B.truncated(2)
+    chunks = [W.make_tokens(rng, n, shape.vocab) for n in (100, 333, 7)]
+    st = Stack(shape, 9, chunks)
+    query = W.make_tokens(rng, 13, shape.vocab)
+    ids = [0, 1, 2]
+    ref = st.oracle(ids, query, 1500)
+    forced = torch.from_numpy(ref.selected.astype(np.int32)).cuda()
+    out = st.model.cb_blend_prefill([st.gpu_req(ids, query)], 1500, forced=forced)
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    for l in range(2):
+        assert rms_rel(host(out["k_cache"][l]), ref.K[l]) <= 2e-2
+        assert rms_rel(host(out["v_cache"][l]), ref.V[l]) <= 2e-2
+    Rn = len(ref.rows)
+    assert np.array_equal(out["rows"][:Rn].cpu().numpy(), ref.rows)
+    assert rms_rel(host(out["hidden"][:Rn]), ref.hidden) <= 2e-2
+    # the GPU's own ranking on the same request: exact top-k of its own d
+    free = st.model.cb_blend_prefill([st.gpu_req(ids, query)], 1500)
+    N, k = 440, len(ref.selected)
+    d = free["deviation"][:N].cpu().numpy().astype(np.float64)
+    assert list(free["selected"][:k].cpu().numpy()) == list(O.token_topk(d, k))
+    assert rms_rel(d, ref.deviation) <= 2e-2
