@@ -152,6 +152,18 @@ unsigned long long cb_debug_launch_count(void);
 #define CB_GEMM_SWAP_AB_PAIR 3
 cb_status cb_debug_gemm_path(int path);
 
+/* Debug index checks (process-wide, off by default).  While on, every call
+ * also validates the device-side index arrays it consumes before using them:
+ * a blended prefill's selected positions (forced or ranked) and each gradual
+ * step's kept positions must be strictly ascending per request and inside
+ * [0, N_b); an attention call's query positions must ascend per request and
+ * lie in [0, kv_len); a selection call's outputs must be strictly ascending
+ * inside [0, n_ctx).  A violation records CB_ERR_DEVICE_INDEX in the device
+ * status word (read with cb_get_device_status); nothing traps.  The checks
+ * are extra launches, so they stay off on the fast path; they never change a
+ * result.  Returns CB_ERR_INVALID_ARG for on not 0 or 1. */
+cb_status cb_debug_index_checks(int on);
+
 /* Launch probe: times the launches of one kernel class of the decoder layer
  * inside real calls.  After cb_debug_probe_start(kind, max_launches) every
  * launch of that class (up to max_launches, on any call's stream, outside

@@ -80,6 +80,25 @@ void cb::note_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
 extern "C" unsigned long long cb_debug_launch_count(void) { return g_launches.load(); }
 
 static std::atomic<int> g_gemm_path{CB_GEMM_AUTO};
+static std::atomic<int> g_index_checks{0};
+bool cb::index_checks_on() { return g_index_checks.load(std::memory_order_relaxed) != 0; }
+extern "C" cb_status cb_debug_index_checks(int on) {
+  if (on != 0 && on != 1) return fail(CB_ERR_INVALID_ARG, "on must be 0 or 1");
+  g_index_checks.store(on);
+  return CB_OK;
+}
+
+// The selections of a call: per request, k entries ascending in [0, n).
+static cudaError_t check_selection(const int32_t *idx, const int *k_off, const int *n, int B,
+                                   int *st, cudaStream_t s) {
+  if (!index_checks_on()) return cudaSuccess;
+  IndexCheck c;
+  c.n_seg = B;
+  c.strict = 1;
+  for (int b = 0; b <= B; ++b) c.off[b] = k_off[b];
+  for (int b = 0; b < B; ++b) c.hi[b] = n[b];
+  return launch_index_check(idx, c, st, s);
+}
 extern "C" cb_status cb_debug_gemm_path(int path) {
   if (path < CB_GEMM_AUTO || path > CB_GEMM_SWAP_AB_PAIR)
     return fail(CB_ERR_INVALID_ARG, "path must be CB_GEMM_AUTO, _TOKEN_M, _SWAP_AB or _SWAP_AB_PAIR");
@@ -312,8 +331,16 @@ extern "C" cb_status cb_kv_deviation_topk(const void *k_fresh, int64_t ld_fresh,
   if (make_sel_plan(reqs, n_req, policy, plan, &err) != CB_OK) return fail(CB_ERR_INVALID_ARG, "%s", err);
   int *st;
   CB_TRY(status_ptr(&st));
-  return run_selection(k_fresh, ld_fresh, k_reused, ld_reused, row_elems, dtype, plan, dev_out,
-                       idx_out, st, stream);
+  CB_TRY(run_selection(k_fresh, ld_fresh, k_reused, ld_reused, row_elems, dtype, plan, dev_out,
+                       idx_out, st, stream));
+  if (index_checks_on()) {
+    // outputs are packed per request at idx_offset; check each run alone
+    for (const SelReq &r : plan.reqs) {
+      const int off[2] = {0, r.k}, n[1] = {r.n_ctx};
+      CB_CUDA(check_selection(idx_out + r.idx_offset, off, n, 1, st, stream));
+    }
+  }
+  return CB_OK;
 }
 
 extern "C" cb_status cb_selection_stats(const float *dev, const int32_t *idx,
@@ -407,6 +434,20 @@ static cb_status run_attention(const void *q, int64_t ld_q, const int32_t *q_pos
                                float scale, void *out, int64_t ld_out, cb_dtype dt,
                                void *ws, size_t ws_bytes, int *st, cudaStream_t s,
                                const int *plan = nullptr) {
+  if (index_checks_on()) {
+    // query positions ascend per request and lie inside its cache
+    IndexCheck c;
+    c.n_seg = (int)reqs.size();
+    c.strict = 0;
+    for (int b = 0; b < c.n_seg; ++b) {
+      c.off[b] = reqs[b].q_begin;
+      c.hi[b] = reqs[b].kv_len;
+    }
+    c.off[c.n_seg] = c.n_seg ? reqs[c.n_seg - 1].q_end : 0;
+    bool contiguous = true;
+    for (int b = 0; b + 1 < c.n_seg; ++b) contiguous &= reqs[b].q_end == reqs[b + 1].q_begin;
+    if (contiguous && (c.n_seg == 0 || reqs[0].q_begin >= 0)) CB_CUDA(launch_index_check(q_pos, c, st, s));
+  }
   if (dt == CB_BF16 && attention_tc_supported(Hq, Hkv, hd)) {
     const size_t need = plan ? 0 : attention_tc_ws_bytes(reqs.data(), (int)reqs.size(), Hq, Hkv);
     if (need > 0 && (!ws || ws_bytes < need))
@@ -1122,6 +1163,7 @@ static cb_status filter_rows(cb_model *m, int l, const BatchMeta &cur, const Bat
   int32_t *src = (int32_t *)(ws + P.g_src);
   if (forced) {
     // the caller gives the kept positions: no ranking at this step
+    CB_CUDA(check_selection(forced, nxt.k_off, nxt.n_ctx, B, st, s));
     CB_CUDA(launch_keep_from_positions(cur, nxt, forced, sel, keep, nxt.k_off[B], st, s));
     CB_CUDA(launch_filter_rows(cur, nxt, keep, sel, sel_n, pos_n, glob_n, src, R_nxt, st, s));
     CB_CUDA(launch_gather(h, d, R_cur, src, R_nxt, d, h_n, d, sizeof(float), st, s));
@@ -1505,6 +1547,7 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
     }
     probe_mark(CB_PROBE_SELECT, false, s);
   }
+  CB_CUDA(check_selection(sel, P.bm.k_off, P.bm.n_ctx, B, st, s));
   // 4. computed rows: selected context rows + uncached rows, gathered once
   probe_mark(CB_PROBE_GATHER, true, s);
   CB_CUDA(launch_rows_gather(P.bm, sel, pos_c, glob_c, (int)P.R_total, h_all, d, h_c, st, s));

@@ -166,6 +166,18 @@ cudaError_t launch_keep_from_positions(const BatchMeta &cur, const BatchMeta &nx
 // dev_idx (may be NULL): for row r of request b at position p, the index
 // n_off[b] + p of its deviation when p < n_ctx[b] (reusable context), else
 // -1; n_off: prefix sums of n_ctx.
+// Debug index check: for each of n_seg segments s, the entries
+// idx[off[s] .. off[s + 1]) must lie in [0, hi[s]) and ascend (strictly
+// when `strict`); a violation records CB_ERR_DEVICE_INDEX.
+struct IndexCheck {
+  int n_seg, strict;
+  int off[CB_MAX_BATCH + 1];
+  int hi[CB_MAX_BATCH];
+};
+cudaError_t launch_index_check(const int32_t *idx, const IndexCheck &c, int *status,
+                               cudaStream_t s);
+// Whether the debug index checks are on (cb_debug_index_checks).
+bool index_checks_on();
 cudaError_t launch_iota_rows(const BatchMeta &bm, int32_t *pos, int32_t *glob,
                              int n_rows, cudaStream_t s, int32_t *dev_idx = nullptr);
 // Per request: contiguous regions of its selection and the share of its

@@ -796,6 +796,32 @@ cudaError_t launch_selection_stats(const float *dev, const int32_t *idx, const S
   return launched(1);
 }
 
+__global__ void index_check_kernel(const int32_t *__restrict__ idx,
+                                   const __grid_constant__ IndexCheck c, int *status) {
+  const int total = c.off[c.n_seg];
+  for (int i = c.off[0] + blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += gridDim.x * blockDim.x) {
+    int sg = 0;
+    while (c.off[sg + 1] <= i) ++sg;
+    const int v = idx[i];
+    bool bad = v < 0 || v >= c.hi[sg];
+    if (i > c.off[sg]) {
+      const int prev = idx[i - 1];
+      bad |= c.strict ? !(prev < v) : !(prev <= v);
+    }
+    if (bad) report(status, CB_ERR_DEVICE_INDEX);
+  }
+}
+
+cudaError_t launch_index_check(const int32_t *idx, const IndexCheck &c, int *status,
+                               cudaStream_t s) {
+  const int total = c.off[c.n_seg] - c.off[0];
+  if (total <= 0) return cudaSuccess;
+  const int blocks = (total + 255) / 256 < 1024 ? (total + 255) / 256 : 1024;
+  index_check_kernel<<<blocks, 256, 0, s>>>(idx, c, status);
+  return launched(1);
+}
+
 __global__ void iota_rows_kernel(const __grid_constant__ BatchMeta bm,
                                  int32_t *__restrict__ pos,
                                  int32_t *__restrict__ glob, int n_rows,

@@ -171,3 +171,9 @@ def test_anchor_count_is_the_ceiling_per_chunk():
     L.check(L.lib.cb_anchor_count(segs, 3, 10000, C.byref(n)))
     assert n.value == 519
     assert L.lib.cb_anchor_count(segs, 3, 10001, C.byref(n)) == L.CB_ERR_INVALID_ARG
+
+
+def test_debug_index_checks_switch_is_validated():
+    assert L.lib.cb_debug_index_checks(2) == L.CB_ERR_INVALID_ARG
+    L.check(L.lib.cb_debug_index_checks(1))
+    L.check(L.lib.cb_debug_index_checks(0))

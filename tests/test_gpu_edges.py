@@ -143,3 +143,58 @@ def test_ragged_chunks_bf16_forced():
     d = free["deviation"][:N].cpu().numpy().astype(np.float64)
     assert list(free["selected"][:k].cpu().numpy()) == list(O.token_topk(d, k))
     assert rms_rel(d, ref.deviation) <= 2e-2
+
+
+@pytest.fixture
+def index_checks():
+    L.check(L.lib.cb_debug_index_checks(1))
+    yield
+    L.check(L.lib.cb_debug_index_checks(0))
+
+
+def test_index_checks_pass_correct_calls_and_change_nothing(index_checks):
+    rng = np.random.default_rng(9)
+    shape = W.TINY_F32
+    chunks = [W.make_tokens(rng, n, shape.vocab) for n in (50, 70)]
+    st = Stack(shape, 6, chunks)
+    query = W.make_tokens(rng, 9, shape.vocab)
+    on = st.model.cb_blend_prefill([st.gpu_req([0, 1], query)], 2000,
+                                   schedule=[(1, 5)] if shape.n_layers > 2 else None)
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    L.check(L.lib.cb_debug_index_checks(0))
+    off = st.model.cb_blend_prefill([st.gpu_req([0, 1], query)], 2000)
+    torch.cuda.synchronize()
+    for key in ("k_cache", "v_cache", "selected", "rows", "first_token"):
+        assert torch.equal(on[key], off[key]), key
+
+
+def test_index_checks_report_an_unsorted_forced_selection(index_checks):
+    """A forced selection in range but out of order: without the checks the
+    call runs (on wrong rows); with them the status word says so."""
+    rng = np.random.default_rng(10)
+    shape = W.TINY_F32
+    chunks = [W.make_tokens(rng, 40, shape.vocab)]
+    st = Stack(shape, 7, chunks)
+    query = W.make_tokens(rng, 4, shape.vocab)
+    k = O.select_count(40, 1000)
+    bad = torch.arange(k, 0, -1, dtype=torch.int32, device="cuda")      # descending
+    st.model.cb_blend_prefill([st.gpu_req([0], query)], 1000, forced=bad)
+    torch.cuda.synchronize()
+    assert R.device_status() == L.CB_ERR_DEVICE_INDEX
+    assert R.device_status() == 0
+
+
+def test_index_checks_report_unsorted_attention_positions(index_checks):
+    n_q, T = 8, 64
+    q = torch.randn(n_q, 4 * 64, device="cuda")
+    kc = torch.randn(T, 2 * 64, device="cuda")
+    vc = torch.randn(T, 2 * 64, device="cuda")
+    out = torch.empty_like(q)
+    good = torch.arange(10, 10 + n_q, dtype=torch.int32, device="cuda")
+    R.cb_sparse_query_attention(q, good, [(0, n_q, 0, T)], kc, vc, 4, 2, 64, out)
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    R.cb_sparse_query_attention(q, good.flip(0), [(0, n_q, 0, T)], kc, vc, 4, 2, 64, out)
+    torch.cuda.synchronize()
+    assert R.device_status() == L.CB_ERR_DEVICE_INDEX
