@@ -978,8 +978,15 @@ static cb_status make_plan(const cb_model *m, const cb_request *reqs, int B,
     P.qp_anchors = cv.take((size_t)(anchor_off + 1) * sizeof(int32_t));
     P.qp_rows = cv.take((size_t)(probe_off + 1) * sizeof(int32_t));
     P.qp_u = cv.take((size_t)4 * (u_off + 1) * sizeof(int32_t));
-    P.qp_k = cv.take((size_t)(probe_off + 1) * m->kvw * m->eb);
-    P.qp_v = cv.take((size_t)(probe_off + 1) * m->kvw * m->eb);
+    // the anchor probe's cache for layers 0 .. max(L*) (the full view works
+    // in the fused cache)
+    int probe_layers = 0;
+    if (!all)
+      for (int i = 0; i < p->n_crit; ++i)
+        probe_layers = std::max(probe_layers, p->crit_layers[i] + 1);
+    const size_t pcache = (size_t)probe_layers * probe_off * m->kvw * m->eb + 256;
+    P.qp_k = cv.take(pcache);
+    P.qp_v = cv.take(pcache);
     P.qp_h = cv.take((size_t)(u_off + 1) * c.d_model * sizeof(float));
     P.qp_mass_bytes = mass;
     P.qp_mass = cv.take(mass);
@@ -1258,12 +1265,22 @@ static cb_status query_probe(cb_model *m, const cb_request *reqs, int B,
     const ProbeLayout::Req &r = Q.reqs[b];
     ar[b] = AttnReq{r.u_off, r.u_off + r.n_u, (int64_t)r.probe_off, r.n_anchor + r.n_u};
   }
-  void *pk = ws + P.qp_k, *pv = ws + P.qp_v;
+  // The probe cache of every probe layer.  Full view: every context
+  // position is an anchor, so the probe cache is the fused cache itself, row
+  // for row (the query rows' K/V written there are recomputed by the blend
+  // before it reads them).  Anchor probe: the anchors' stitched rows of all
+  // probe layers, gathered at once.
+  const int64_t pstride = (int64_t)Q.n_probe * m->kvw;    // elements per probe layer
+  if (!Q.all) {
+    CB_CUDA(launch_gather_layers(out->k_cache, lstride, m->kvw, P.T_total, rows, Q.n_probe,
+                                 m->kvw, ws + P.qp_k, pstride, m->kvw, m->eb, last + 1, st, s));
+    CB_CUDA(launch_gather_layers(out->v_cache, lstride, m->kvw, P.T_total, rows, Q.n_probe,
+                                 m->kvw, ws + P.qp_v, pstride, m->kvw, m->eb, last + 1, st, s));
+  }
   for (int l = 0; l <= last; ++l) {
     const char *kl = layer_ptr(out->k_cache, l, lstride, m->eb);
-    const char *vl = layer_ptr(out->v_cache, l, lstride, m->eb);
-    CB_CUDA(launch_gather(kl, m->kvw, P.T_total, rows, Q.n_probe, m->kvw, pk, m->kvw, m->eb, st, s));
-    CB_CUDA(launch_gather(vl, m->kvw, P.T_total, rows, Q.n_probe, m->kvw, pv, m->kvw, m->eb, st, s));
+    void *pk = Q.all ? layer_ptr(out->k_cache, l, lstride, m->eb) : layer_ptr(ws + P.qp_k, l, pstride, m->eb);
+    void *pv = Q.all ? layer_ptr(out->v_cache, l, lstride, m->eb) : layer_ptr(ws + P.qp_v, l, pstride, m->eb);
     CB_TRY(layer_forward(m, l, h_u, nu, u_pos, u_cache, ar, pk, pv, S, st, s, nullptr, u_mask));
     if (!crit[l]) continue;
     for (int b = 0; b < B; ++b) {

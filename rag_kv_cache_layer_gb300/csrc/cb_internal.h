@@ -198,6 +198,12 @@ cudaError_t launch_gather(const void *src, int64_t ld_src, int64_t src_rows,
                           const int32_t *idx, int n, int row_elems, void *dst,
                           int64_t ld_dst, size_t elem_bytes, int *status,
                           cudaStream_t s);
+// launch_gather for layers [0, n_layers) in one launch: layer l from
+// src + l * src_lstride to dst + l * dst_lstride (elements).
+cudaError_t launch_gather_layers(const void *src, int64_t src_lstride, int64_t ld_src,
+                                 int64_t src_rows, const int32_t *idx, int n, int row_elems,
+                                 void *dst, int64_t dst_lstride, int64_t ld_dst, size_t eb,
+                                 int n_layers, int *status, cudaStream_t s);
 cudaError_t launch_scatter_kv(const void *k_new, const void *v_new,
                               int64_t ld_new, const int32_t *rows, int n,
                               void *k_cache, void *v_cache, int64_t ld_cache,

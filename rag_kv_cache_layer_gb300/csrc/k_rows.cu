@@ -186,6 +186,39 @@ cudaError_t launch_gather(const void *src, int64_t ld_src, int64_t src_rows,
   return launched(1);
 }
 
+// The same row gather for layers [0, n_layers) at once: layer l reads
+// src + l * src_lstride and writes dst + l * dst_lstride (elements).
+__global__ void __launch_bounds__(256)
+gather_layers_kernel(const char *__restrict__ src, int64_t src_lstride_b, int64_t ld_src_b,
+                     int64_t src_rows, const int32_t *__restrict__ idx, int n, int row_units,
+                     char *__restrict__ dst, int64_t dst_lstride_b, int64_t ld_dst_b,
+                     int *status) {
+  const char *sl = src + (int64_t)blockIdx.y * src_lstride_b;
+  char *dl = dst + (int64_t)blockIdx.y * dst_lstride_b;
+  const int64_t total = (int64_t)n * row_units;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int i = (int)(t / row_units), u = (int)(t % row_units);
+    const int r = idx[i];
+    if (r < 0 || r >= src_rows) { report(status, CB_ERR_DEVICE_INDEX); continue; }
+    stg16(dl + i * ld_dst_b + (int64_t)u * 16, ldg16(sl + r * ld_src_b + (int64_t)u * 16));
+  }
+}
+
+cudaError_t launch_gather_layers(const void *src, int64_t src_lstride, int64_t ld_src,
+                                 int64_t src_rows, const int32_t *idx, int n, int row_elems,
+                                 void *dst, int64_t dst_lstride, int64_t ld_dst, size_t eb,
+                                 int n_layers, int *status, cudaStream_t s) {
+  if (n == 0 || n_layers <= 0) return cudaSuccess;
+  const int units = (int)(row_elems * eb / 16);
+  int bx = grid_for((int64_t)n * units, 256) / n_layers;
+  if (bx < 1) bx = 1;
+  gather_layers_kernel<<<dim3(bx, n_layers), 256, 0, s>>>(
+      (const char *)src, src_lstride * (int64_t)eb, ld_src * (int64_t)eb, src_rows, idx, n, units,
+      (char *)dst, dst_lstride * (int64_t)eb, ld_dst * (int64_t)eb, status);
+  return launched(1);
+}
+
 __global__ void __launch_bounds__(256)
 scatter_kv_kernel(const char *__restrict__ kn, const char *__restrict__ vn,
                   int64_t ld_new_b, const int32_t *__restrict__ rows, int n,
