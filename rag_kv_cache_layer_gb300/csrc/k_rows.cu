@@ -211,8 +211,7 @@ cudaError_t launch_gather_layers(const void *src, int64_t src_lstride, int64_t l
                                  int n_layers, int *status, cudaStream_t s) {
   if (n == 0 || n_layers <= 0) return cudaSuccess;
   const int units = (int)(row_elems * eb / 16);
-  int bx = grid_for((int64_t)n * units, 256) / n_layers;
-  if (bx < 1) bx = 1;
+  const int bx = grid_for((int64_t)n * units, 256);   // a full grid's worth per layer
   gather_layers_kernel<<<dim3(bx, n_layers), 256, 0, s>>>(
       (const char *)src, src_lstride * (int64_t)eb, ld_src * (int64_t)eb, src_rows, idx, n, units,
       (char *)dst, dst_lstride * (int64_t)eb, ld_dst * (int64_t)eb, status);
