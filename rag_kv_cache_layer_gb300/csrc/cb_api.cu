@@ -1033,12 +1033,14 @@ static inline char *layer_ptr(void *base, int l, int64_t stride, size_t eb) {
   return (char *)base + (int64_t)l * stride * (int64_t)eb;
 }
 
-// One decoder layer over n rows of h (see cb_blend_layer).
+// One decoder layer over n rows of h (see cb_blend_layer).  q_only: stop
+// once the rows' rotated queries are in S.q (bf16: only the W_q rows of the
+// projection run; h, kc and vc are left as they are).
 static cb_status layer_forward(cb_model *m, int l, float *h, int n, const int32_t *pos,
                                const int32_t *cache_row, const std::vector<AttnReq> &ar,
                                void *kc, void *vc, const LayerScratch &S, int *st,
                                cudaStream_t s, const int *attn_plan = nullptr,
-                               const int32_t *attn_pos = nullptr) {
+                               const int32_t *attn_pos = nullptr, bool q_only = false) {
   const NvtxRange range("layer %d", l);
   const cb_model_config &c = m->cfg;
   const cb_layer_weights &L = m->layers[l];
@@ -1049,8 +1051,8 @@ static cb_status layer_forward(cb_model *m, int l, float *h, int n, const int32_
   if (dt == CB_BF16 && hd == 128) {
     // projection, RoPE and the Eq. 7 scatter in one kernel
     const QkvEpi q{pos, cache_row, kc, vc, m->kvw, m->w.rope_table, c.n_q_heads, c.n_kv_heads};
-    CB_TRY(run_linear(m, S.x, d, L.w_qkv, nullptr, d, n, m->qkv_rows, d, EPI_QKV, S.q, m->qw,
-                      s, &q, S.split));
+    CB_TRY(run_linear(m, S.x, d, L.w_qkv, nullptr, d, n, q_only ? m->qw : m->qkv_rows, d,
+                      EPI_QKV, S.q, m->qw, s, &q, S.split));
   } else {
     CB_TRY(run_linear(m, S.x, d, L.w_qkv, nullptr, d, n, m->qkv_rows, d, EPI_STORE_F32,
                       S.qkv32, m->qkv_rows, s));
@@ -1059,6 +1061,7 @@ static cb_status layer_forward(cb_model *m, int l, float *h, int n, const int32_
                               dt, 0, s));
   }
   probe_mark(CB_PROBE_QKV, false, s);
+  if (q_only) return CB_OK;
   probe_mark(CB_PROBE_ATTENTION, true, s);
   // attn_pos: the rows' causal-mask positions in kc / vc when these are not
   // their request positions (the query probe's compact cache)
@@ -1281,7 +1284,10 @@ static cb_status query_probe(cb_model *m, const cb_request *reqs, int B,
     const char *kl = layer_ptr(out->k_cache, l, lstride, m->eb);
     void *pk = Q.all ? layer_ptr(out->k_cache, l, lstride, m->eb) : layer_ptr(ws + P.qp_k, l, pstride, m->eb);
     void *pv = Q.all ? layer_ptr(out->v_cache, l, lstride, m->eb) : layer_ptr(ws + P.qp_v, l, pstride, m->eb);
-    CB_TRY(layer_forward(m, l, h_u, nu, u_pos, u_cache, ar, pk, pv, S, st, s, nullptr, u_mask));
+    // the last probe layer only feeds its queries to the mass: nothing after
+    // its Q projection is read
+    CB_TRY(layer_forward(m, l, h_u, nu, u_pos, u_cache, ar, pk, pv, S, st, s, nullptr, u_mask,
+                         l == last));
     if (!crit[l]) continue;
     for (int b = 0; b < B; ++b) {
       const ProbeLayout::Req &r = Q.reqs[b];
