@@ -263,6 +263,8 @@ topk_kernel(const __grid_constant__ SelParams p, const float *__restrict__ dev,
 // rank the deviations stay in shared memory (kSmemCtx floats at most; a
 // longer request reads them back from dev_out) for the select's passes.
 constexpr int kSmemCtx = 40960;
+constexpr int kPartsUnroll = 8;            // head partials loaded at once (more: one by one)
+constexpr int kPartsTok = 3;               // tokens per thread per round
 template <bool RANK>
 __global__ void __launch_bounds__(kSelThreads)
 parts_kernel(const __grid_constant__ SelParams p, const float *__restrict__ parts, int n_parts,
@@ -273,12 +275,39 @@ parts_kernel(const __grid_constant__ SelParams p, const float *__restrict__ part
   const SelReq &q = p.r[blockIdx.x];
   const int n = q.n_ctx;
   const bool in_smem = RANK && n <= kSmemCtx;
-  for (int i = threadIdx.x; i < n; i += kSelThreads) {
-    const float *src = parts + q.dev_offset + i;
-    float v = 0.f;
-    for (int h = 0; h < n_parts; ++h) v += __ldg(src + h * part_stride);
-    dev_out[q.dev_offset + i] = v;
-    if (in_smem) s_d[i] = v;
+  if (n_parts <= kPartsUnroll) {
+    // every load of a thread's kPartsTok tokens is issued before the first
+    // add (one memory round trip); the adds keep the head order
+    for (int i0 = threadIdx.x; i0 < n; i0 += kSelThreads * kPartsTok) {
+      float x[kPartsTok][kPartsUnroll];
+#pragma unroll
+      for (int u = 0; u < kPartsTok; ++u) {
+        const int i = i0 + u * kSelThreads;
+        const float *src = parts + q.dev_offset + i;
+#pragma unroll
+        for (int h = 0; h < kPartsUnroll; ++h)
+          x[u][h] = (i < n && h < n_parts) ? __ldg(src + h * part_stride) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kPartsTok; ++u) {
+        const int i = i0 + u * kSelThreads;
+        if (i >= n) break;
+        float v = 0.f;
+#pragma unroll
+        for (int h = 0; h < kPartsUnroll; ++h)
+          if (h < n_parts) v += x[u][h];
+        dev_out[q.dev_offset + i] = v;
+        if (in_smem) s_d[i] = v;
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < n; i += kSelThreads) {
+      const float *src = parts + q.dev_offset + i;
+      float v = 0.f;
+      for (int h = 0; h < n_parts; ++h) v += __ldg(src + h * part_stride);
+      dev_out[q.dev_offset + i] = v;
+      if (in_smem) s_d[i] = v;
+    }
   }
   if (!RANK || q.k <= 0) return;
   __syncthreads();
