@@ -43,7 +43,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -551,6 +551,7 @@ def run_ours(args):
                 "global_batch": world * B, "seq_len": T,
                 "parallelism": "replicas" if world > 1 else "none",
                 "k_selected": int(plan.K_total), "rows_computed": int(plan.R_total),
+                "recomputed_rows_per_s": world * int(plan.R_total) / (ms_per_step / 1e3),
                 "ttft_ms_median": statistics.median(per),
                 "ttft_ms_p95": float(np.percentile(per, 95)),
                 "execution": "step captured once in a CUDA graph and replayed; "
