@@ -868,6 +868,23 @@ def run_host_kv(args):
                        "controller_ratio": f"{chosen / 100:g}%",
                        "ttft_ms_at_15pct": t15, "ttft_ms_at_controller_ratio": tr}
         del houts
+    # the anchor probe (QCFuse §3.3-3.4) with the chunk caches in host
+    # memory: its probe layers are loaded first, the later layers' loads
+    # overlap the probe and the blend
+    mid = n_layers // 2
+    crit = sorted({min(max(l, 0), n_layers - 1) for l in (mid - 1, mid, mid + 1)})
+    q = {"anchor_rule": L.CB_ANCHOR_KNORM, "anchor_bp": 1000, "crit_layers": crit}
+    qd = model.alloc_outputs(model.plan(reqs, RATIO_BP, policy=L.CB_POLICY_QUERY_PROBE,
+                                        sel_layer=0, query=q), 1)
+    qh = model.alloc_outputs(model.plan_host_kv(hreq, RATIO_BP, policy=L.CB_POLICY_QUERY_PROBE,
+                                                sel_layer=0, query=q), 1)
+    probe_dev, _ = _graph_ms(lambda: model.cb_blend_prefill(
+        reqs, RATIO_BP, policy=L.CB_POLICY_QUERY_PROBE, sel_layer=0, query=q, outputs=qd),
+        args.steps, st)
+    probe_host, _ = _graph_ms(lambda: model.cb_blend_prefill_host_kv(
+        hreq, RATIO_BP, cs, policy=L.CB_POLICY_QUERY_PROBE, sel_layer=0, query=q, outputs=qh),
+        args.steps, st)
+    del qd, qh
     clk = clocks.stop()
     if R.device_status() != 0:
         raise RuntimeError("device status set during the host-resident workload")
@@ -880,7 +897,10 @@ def run_host_kv(args):
                        "layer_kv_bytes": layer_bytes},
             "ttft_ms_device_store": dev_ms,
             "recompute_ms_per_layer": {f"r={r / 100:g}%": v for r, v in table.items()},
-            "load_modes": modes, "clocks": clk,
+            "load_modes": modes,
+            "anchor_probe_ttft_ms": {"device store": probe_dev, "copy engines": probe_host,
+                                     "critical_layers": crit},
+            "clocks": clk,
             "context": "CacheBlend blog: 4.8 GB/s NVMe, Llama-7B 4K context, 16 ms load vs 3 ms "
                        "recompute at 15% per layer; QCFuse §4.4: NVMe throttled to about 3 GB/s"}
     print(json.dumps(line), flush=True)

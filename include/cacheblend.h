@@ -616,8 +616,15 @@ cb_status cb_blend_prefill(cb_model *m, const cb_request *reqs, int B,
  * share a model must be issued one at a time.  Results are those of
  * cb_blend_prefill.  Workspace: cb_blend_plan_host_kv (cb_blend_plan plus
  * the staging area, 4 * N_total * row_elems * dtype bytes).
+ * The query-aware policies load the layers their probe reads first: the
+ * anchor probe layers 0 .. max(L*) before its cache gather, the full view
+ * each layer just before its probe layer; the later layers' loads overlap
+ * the probe and the blend.  With CB_ANCHOR_KNORM the anchor scores read
+ * every layer's chunk keys from the host memory in a kernel.
  * Errors: as cb_blend_prefill; CB_ERR_INVALID_ARG when a chunk cache is not
- * pinned host memory or copy_stream is NULL or equal to stream. */
+ * pinned host memory, when a kernel reads it (host_load_ctas > 0, or the
+ * key-norm anchor rule) and the host pointer is not also its device
+ * address, or when copy_stream is NULL or equal to stream. */
 cb_status cb_blend_plan_host_kv(const cb_model *m, const cb_request *reqs, int B,
                                 const cb_blend_params *p, cb_plan *out);
 cb_status cb_blend_prefill_host_kv(cb_model *m, const cb_request *reqs, int B,

@@ -387,7 +387,7 @@ class BlendModel:
     def cb_blend_prefill_host_kv(self, reqs, ratio_bp, copy_stream, policy=0, sel_layer=1,
                                  outputs=None, stream=None, span_len=0, span_offset=0,
                                  span_order=None, schedule=None, host_load_ctas=0,
-                                 forced=None):
+                                 forced=None, query=None):
         """cb_blend_prefill with the requests' chunk caches in pinned host
         memory (HostChunkStore segments), loaded layer by layer on
         copy_stream while earlier layers compute.  host_load_ctas > 0: the
@@ -396,7 +396,8 @@ class BlendModel:
         engines."""
         arr, keep = _requests(reqs)
         p, sch = self._params(ratio_bp, policy, sel_layer, schedule, forced, span_len,
-                              span_offset, span_order, host_load_ctas=host_load_ctas)
+                              span_offset, span_order, query=query,
+                              host_load_ctas=host_load_ctas)
         if outputs is None:
             plan = L.Plan()
             check(lib.cb_blend_plan_host_kv(self.handle, arr, len(reqs), C.byref(p),
@@ -431,9 +432,10 @@ class BlendModel:
                                    anchors.data_ptr(), _p(ws), ws.numel(), _s(stream)))
         return anchors[:n_a], (None if scores is None else scores[:n])
 
-    def plan_host_kv(self, reqs, ratio_bp, policy=0, sel_layer=1, host_load_ctas=0):
+    def plan_host_kv(self, reqs, ratio_bp, policy=0, sel_layer=1, host_load_ctas=0, query=None):
         arr, keep = _requests(reqs)
-        p, sch = self._params(ratio_bp, policy, sel_layer, None, host_load_ctas=host_load_ctas)
+        p, sch = self._params(ratio_bp, policy, sel_layer, None, query=query,
+                              host_load_ctas=host_load_ctas)
         out = L.Plan()
         check(lib.cb_blend_plan_host_kv(self.handle, arr, len(reqs), C.byref(p), C.byref(out)))
         return out

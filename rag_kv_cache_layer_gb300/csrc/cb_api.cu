@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <functional>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -815,8 +816,6 @@ static cb_status make_plan(const cb_model *m, const cb_request *reqs, int B,
       // [QCF] §3.5: P exists before layer 0, every layer recomputes it
       if (p->sel_layer != 0 || p->n_schedule != 0)
         return fail(CB_ERR_INVALID_ARG, "query-aware policies select before layer 0: sel_layer and n_schedule must be 0");
-      if (host_kv)
-        return fail(CB_ERR_UNSUPPORTED, "query-aware policies need the chunk caches on the device");
       if (m->cfg.dtype != CB_BF16 || m->cfg.head_dim != 128)
         return fail(CB_ERR_UNSUPPORTED, "query-aware policies run on bf16 models with head_dim 128");
       if (p->policy == CB_POLICY_QUERY_PROBE) {
@@ -1227,10 +1226,13 @@ static cb_status rank_anchors(const cb_model *m, const std::vector<AnchorChunk> 
 // after each critical layer their attention mass on the request's context
 // keys is added into I (Eq. 20).  QUERY_FULL: every position is an anchor
 // and every layer critical (Eqs. 9-10).
+// ready(l): layers 0 .. l of the fused cache hold the stitched chunk caches
+// (host-resident chunks arrive layer by layer).
 static cb_status query_probe(cb_model *m, const cb_request *reqs, int B,
                              const cb_blend_params *p, const Plan &P, char *ws,
                              const cb_blend_out *out, int64_t lstride, const LayerScratch &S,
-                             const float *h_all, float *I, int *st, cudaStream_t s) {
+                             const float *h_all, float *I, int *st, cudaStream_t s,
+                             const std::function<cb_status(int)> &ready) {
   const cb_model_config &c = m->cfg;
   const ProbeLayout &Q = P.probe;
   const int d = c.d_model;
@@ -1275,12 +1277,14 @@ static cb_status query_probe(cb_model *m, const cb_request *reqs, int B,
   // probe layers, gathered at once.
   const int64_t pstride = (int64_t)Q.n_probe * m->kvw;    // elements per probe layer
   if (!Q.all) {
+    CB_TRY(ready(last));
     CB_CUDA(launch_gather_layers(out->k_cache, lstride, m->kvw, P.T_total, rows, Q.n_probe,
                                  m->kvw, ws + P.qp_k, pstride, m->kvw, m->eb, last + 1, st, s));
     CB_CUDA(launch_gather_layers(out->v_cache, lstride, m->kvw, P.T_total, rows, Q.n_probe,
                                  m->kvw, ws + P.qp_v, pstride, m->kvw, m->eb, last + 1, st, s));
   }
   for (int l = 0; l <= last; ++l) {
+    if (Q.all) CB_TRY(ready(l));
     const char *kl = layer_ptr(out->k_cache, l, lstride, m->eb);
     void *pk = Q.all ? layer_ptr(out->k_cache, l, lstride, m->eb) : layer_ptr(ws + P.qp_k, l, pstride, m->eb);
     void *pv = Q.all ? layer_ptr(out->v_cache, l, lstride, m->eb) : layer_ptr(ws + P.qp_v, l, pstride, m->eb);
@@ -1447,6 +1451,23 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
     CB_CUDA(cudaEventRecord(m->ev_free[l & 1], s));
     return CB_OK;
   };
+  // Host-resident chunks: layer l is loaded (issue_copies) at most two
+  // layers ahead of the last one stitched, since its staging buffer (or its
+  // copy-done event) is that of layer l - 2; stitch_through(l) stitches every
+  // layer up to l, keeping the loads two layers ahead.
+  int next_issue = s_layer, next_stitch = s_layer;
+  auto prefetch = [&]() -> cb_status {
+    while (next_issue < L && next_issue < next_stitch + 2) CB_TRY(issue_copies(next_issue++));
+    return CB_OK;
+  };
+  auto stitch_through = [&](int upto) -> cb_status {
+    if (!host_kv) return CB_OK;
+    while (next_stitch <= upto && next_stitch < L) {
+      CB_TRY(prefetch());
+      CB_TRY(stitch_layer(next_stitch++));
+    }
+    return prefetch();
+  };
   if (host_kv) {
     // fork the copy stream from the compute stream (a graph capture then
     // covers both); both staging buffers start free
@@ -1454,7 +1475,7 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
     CB_CUDA(cudaStreamWaitEvent(copy_stream, m->ev_fork, 0));
     CB_CUDA(cudaEventRecord(m->ev_free[0], s));
     CB_CUDA(cudaEventRecord(m->ev_free[1], s));
-    for (int l = s_layer; l < L && l < s_layer + 2; ++l) CB_TRY(issue_copies(l));
+    CB_TRY(prefetch());
   } else {
     probe_mark(CB_PROBE_STITCH, true, s);
     CB_CUDA(launch_reposition(descs.data(), (int)descs.size(), s_layer, L, out->k_cache,
@@ -1476,8 +1497,10 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
                          layer_ptr(out->v_cache, l, lstride, m->eb), S, st, s));
   // 3. selection layer: fresh keys of every row, deviation, ranking; the
   // query-aware policies score the context with the query probe instead
-  if (host_kv) CB_TRY(stitch_layer(s_layer));
   const bool query = is_query_policy(p->policy);
+  // the key projection compares with the stitched layer s; the query probe
+  // asks for its layers itself
+  if (!query) CB_TRY(stitch_through(s_layer));
   // bf16 with 128-wide heads: the key projection's epilogue compares the
   // fresh keys with the stitched ones and leaves per-head squared
   // differences; the fresh keys are never stored
@@ -1541,7 +1564,8 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
     probe_mark(CB_PROBE_SELECT, true, s);
     if (query) {
       // I(t) in the deviation buffer, then P = TopK(I, k) ([QCF] Eq. 11)
-      CB_TRY(query_probe(m, reqs, B, p, P, ws, out, lstride, S, h_all, dev, st, s));
+      CB_TRY(query_probe(m, reqs, B, p, P, ws, out, lstride, S, h_all, dev, st, s,
+                         stitch_through));
       if (p->forced_selected) {
         if (sel != p->forced_selected && P.K_total > 0)
           CB_CUDA(cudaMemcpyAsync(sel, p->forced_selected, P.K_total * sizeof(int32_t),
@@ -1592,10 +1616,7 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
   int *attn_plan = P.attn_plan_bytes ? (int *)(ws + P.attn_plan) : nullptr;
   bool plan_stale = true;
   for (int l = s_layer; l < L; ++l) {
-    if (host_kv) {
-      if (l > s_layer) CB_TRY(stitch_layer(l));
-      if (l + 2 < L) CB_TRY(issue_copies(l + 2));
-    }
+    CB_TRY(stitch_through(l));
     if (next_step < P.sched.size() && P.sched[next_step].layer == l) {
       const Plan::Step &stp = P.sched[next_step++];
       CB_TRY(filter_rows(m, l, bm, stp.bm, (int)stp.R_total, h_b[cur], pos_b[cur], glob_b[cur],
@@ -1809,10 +1830,14 @@ extern "C" cb_status cb_blend_prefill_host_kv(cb_model *m, const cb_request *req
         cudaPointerAttributes a;
         if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess || a.type != cudaMemoryTypeHost)
           return fail(CB_ERR_INVALID_ARG, "request %d segment %d: chunk caches must be pinned host memory", b, i);
-        // the zero-copy load dereferences the host pointer in a kernel: it
-        // must be the allocation's device address as well (unified addressing)
-        if (p && p->host_load_ctas > 0 && a.devicePointer != ptr)
-          return fail(CB_ERR_INVALID_ARG, "request %d segment %d: chunk cache is not mapped at the same device address (zero-copy load)", b, i);
+        // the zero-copy load, and the key-norm anchor scores of the query
+        // probe, dereference the host pointer in a kernel: it must be the
+        // allocation's device address as well (unified addressing)
+        const bool kernel_reads =
+            p && (p->host_load_ctas > 0 ||
+                  (p->policy == CB_POLICY_QUERY_PROBE && p->anchor_rule == CB_ANCHOR_KNORM));
+        if (kernel_reads && a.devicePointer != ptr)
+          return fail(CB_ERR_INVALID_ARG, "request %d segment %d: chunk cache is not mapped at the same device address (read by a kernel)", b, i);
       }
     }
   return blend_impl(m, reqs, B, p, out, ws, ws_bytes, stream, true, copy_stream);

@@ -22,7 +22,7 @@ import workload as W
 import rag_kv_cache_layer_gb300 as R
 from rag_kv_cache_layer_gb300 import _lib as L
 from gpu_common import host, rms_rel
-from test_gpu_blend import Setup
+from test_gpu_blend import Setup, _host_store
 
 pytestmark = pytest.mark.gpu
 
@@ -106,6 +106,64 @@ def test_query_probe_blend(q3, policy, query, rule, bp, crit):
         assert rms_rel(host(out["v_cache"][l]), ref.V[l]) <= TOL
     Rn = len(ref.rows)
     assert rms_rel(host(out["hidden"][:Rn]), ref.hidden) <= TOL
+
+
+@pytest.mark.parametrize("ctas", [0, 2], ids=["copy_engines", "zero_copy_2_ctas"])
+@pytest.mark.parametrize("policy,query,rule,bp,crit", [
+    (L.CB_POLICY_QUERY_PROBE, {"anchor_rule": L.CB_ANCHOR_SINK, "anchor_bp": 1000,
+                               "crit_layers": [1, 2]}, "sink", 1000, [1, 2]),
+    (L.CB_POLICY_QUERY_PROBE, {"anchor_rule": L.CB_ANCHOR_KNORM, "anchor_bp": 1000,
+                               "crit_layers": [0, 1]}, None, 1000, [0, 1]),
+    (L.CB_POLICY_QUERY_FULL, None, "all", 0, None),
+], ids=["probe_sink", "probe_knorm", "full_view"])
+def test_query_policies_on_host_resident_chunks(q3, policy, query, rule, bp, crit, ctas):
+    """[CB] "Hiding Recompute Behind I/O" with QCFuse's selectors: the chunk
+    caches stay in pinned host memory and arrive layer by layer (the layers
+    the probe reads first; Knorm scores read the host keys in a kernel).
+    Against the device-resident call on a device copy of the same store:
+    I(t) within 1e-3 (the residual projections add their split tiles with
+    fp32 atomics, so the last bits vary from run to run), P the exact top-k
+    of its own I, and every row that both calls left unselected identical
+    in every layer (the stitch).
+    Against the oracle (Sink probe, full view): I(t) at 5e-2, the blend
+    with this call's P at 2e-2."""
+    hs, hreq = _host_store(q3)
+    cs = torch.cuda.Stream()
+    out = q3.model.cb_blend_prefill_host_kv(hreq, 1500, cs, policy=policy, sel_layer=0,
+                                            query=query, host_load_ctas=ctas)
+    # the device-resident call on a device copy of the same host store (a
+    # second chunk prefill would differ in the last bits)
+    dK, dV = hs.K.cuda(), hs.V.cuda()
+    dsegs = [R.Seg(sg.len, dK[0, hs.where[c.chunk_id][0]], dV[0, hs.where[c.chunk_id][0]],
+                   sg.pic_layer_stride, 0) if sg.k_pic is not None else sg
+             for sg, c in zip(hreq[0].segs, q3.wl.requests[0].segments)]
+    ref = q3.model.cb_blend_prefill([R.Req(hreq[0].tokens, dsegs)], 1500, policy=policy,
+                                    sel_layer=0, query=query)
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    segs, store = _oracle_inputs(q3)
+    N = sum(len(s) for s, c in segs if c)
+    k = O.select_count(N, 1500)
+    I_h = out["deviation"][:N].cpu().numpy().astype(np.float64)
+    I_d = ref["deviation"][:N].cpu().numpy().astype(np.float64)
+    assert rms_rel(I_h, I_d) <= 1e-3
+    P_h = out["selected"][:k].cpu().numpy()
+    assert list(P_h) == list(O.token_topk(I_h, k))
+    both = np.setdiff1d(np.arange(N), np.union1d(P_h, ref["selected"][:k].cpu().numpy()))
+    rows = torch.from_numpy(both).cuda()
+    for l in range(q3.shape.n_layers):
+        assert torch.equal(out["k_cache"][l][rows], ref["k_cache"][l][rows]), l
+        assert torch.equal(out["v_cache"][l][rows], ref["v_cache"][l][rows]), l
+    if rule is None:
+        return
+    _, I_ref, _ = O.query_probe_select(q3.om, segs, store, 1500, rule, bp, crit)
+    assert rms_rel(I_h, I_ref) <= TOL_I
+    oref = O.blend_prefill(q3.om, segs, store, 1500, sel_layer=0, forced=P_h)
+    for l in range(q3.shape.n_layers):
+        assert rms_rel(host(out["k_cache"][l]), oref.K[l]) <= TOL
+        assert rms_rel(host(out["v_cache"][l]), oref.V[l]) <= TOL
+    Rn = len(oref.rows)
+    assert rms_rel(host(out["hidden"][:Rn]), oref.hidden) <= TOL
 
 
 def test_query_probe_knorm_with_the_gpu_anchors(q3):
