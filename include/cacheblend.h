@@ -520,6 +520,16 @@ typedef struct {
                           load bandwidth (a slower storage tier is emulated
                           by a small count) and needs no staging area.
                           0 .. 4096.                                       */
+  const int32_t *anchors; /* CB_POLICY_QUERY_PROBE only.  NULL: the library
+                          ranks every chunk's anchors by anchor_rule
+                          ([QCF] Eq. 14).  Else device int32: the anchors of
+                          every cached segment -- request by request,
+                          segments in order, each chunk's ceil(anchor_bp
+                          |c| / 10^4) chunk-local positions ascending, the
+                          layout cb_anchor_select writes.  A store can keep
+                          them with its chunks: the Knorm scores depend only
+                          on a chunk's own keys.  A position outside its
+                          chunk records CB_ERR_DEVICE_INDEX.               */
 } cb_blend_params;
 
 /* Per-chunk anchors of [QCF] Eq. 14, as the offline cache preparation of

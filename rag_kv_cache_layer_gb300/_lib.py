@@ -100,7 +100,7 @@ class BlendParams(C.Structure):
                 ("span_order", C.POINTER(C.c_int32)), ("forced_selected", vp),
                 ("anchor_rule", i32), ("anchor_bp", i32), ("n_crit", i32),
                 ("crit_layers", C.POINTER(C.c_int32)), ("forced_kept", vp),
-                ("host_load_ctas", i32)]
+                ("host_load_ctas", i32), ("anchors", vp)]
 
 
 class BlendOut(C.Structure):

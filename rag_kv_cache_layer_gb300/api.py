@@ -299,7 +299,9 @@ class BlendModel:
                 span_offset=0, span_order=None, query=None, forced_kept=None,
                 host_load_ctas=0):
         """query: for the query-aware policies, a dict with anchor_rule,
-        anchor_bp and crit_layers (QCFuse Eqs. 14, 20)."""
+        anchor_bp and crit_layers (QCFuse Eqs. 14, 20), and optionally
+        anchors (a device int32 tensor in cb_anchor_select's layout: the
+        chunks' precomputed anchors)."""
         n = len(schedule or [])
         sch = (L.ScheduleStep * max(1, n))()
         for i, (l, k) in enumerate(schedule or []):
@@ -318,7 +320,9 @@ class BlendModel:
                              int(q.get("anchor_bp", 0)), len(crit),
                              C.cast(crit_arr, C.POINTER(C.c_int32)),
                              None if forced_kept is None else forced_kept.data_ptr(),
-                             int(host_load_ctas)), (sch, order, crit_arr)
+                             int(host_load_ctas),
+                             None if q.get("anchors") is None else q["anchors"].data_ptr()), \
+            (sch, order, crit_arr)
 
     def plan(self, reqs, ratio_bp=None, policy=0, sel_layer=1, schedule=None, span_len=0,
              span_offset=0, span_order=None, query=None):

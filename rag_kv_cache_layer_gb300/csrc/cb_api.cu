@@ -1226,18 +1226,20 @@ static cb_status rank_anchors(const cb_model *m, const std::vector<AnchorChunk> 
 // after each critical layer their attention mass on the request's context
 // keys is added into I (Eq. 20).  QUERY_FULL: every position is an anchor
 // and every layer critical (Eqs. 9-10).
-// ready(l): layers 0 .. l of the fused cache hold the stitched chunk caches
-// (host-resident chunks arrive layer by layer).
+// ready(l): layers 0 .. l of the fused cache hold the stitched chunk caches.
+// layerwise (host-resident chunks, which arrive layer by layer): the anchor
+// probe gathers each layer's probe cache just before its probe layer, so
+// the probe overlaps the loads of its later layers.
 static cb_status query_probe(cb_model *m, const cb_request *reqs, int B,
                              const cb_blend_params *p, const Plan &P, char *ws,
                              const cb_blend_out *out, int64_t lstride, const LayerScratch &S,
                              const float *h_all, float *I, int *st, cudaStream_t s,
-                             const std::function<cb_status(int)> &ready) {
+                             const std::function<cb_status(int)> &ready, bool layerwise) {
   const cb_model_config &c = m->cfg;
   const ProbeLayout &Q = P.probe;
   const int d = c.d_model;
-  int32_t *anchors = (int32_t *)(ws + P.qp_anchors);
-  if (!Q.all) {
+  const int32_t *anchors = p->anchors ? p->anchors : (const int32_t *)(ws + P.qp_anchors);
+  if (!Q.all && !p->anchors) {
     std::vector<AnchorChunk> ch;
     for (int b = 0; b < B; ++b)
       for (int i = 0; i < reqs[b].n_segments; ++i) {
@@ -1246,7 +1248,8 @@ static cb_status query_probe(cb_model *m, const cb_request *reqs, int B,
         ch.push_back(AnchorChunk{sg.k_pic, sg.pic_layer_stride, sg.len,
                                  P.n_off[b] + P.seg_start[b][i]});
       }
-    CB_TRY(rank_anchors(m, ch, Q.segs, p->anchor_rule, (float *)(ws + P.qp_scores), anchors, s));
+    CB_TRY(rank_anchors(m, ch, Q.segs, p->anchor_rule, (float *)(ws + P.qp_scores),
+                        (int32_t *)(ws + P.qp_anchors), s));
   }
   const int nu = Q.n_u;
   int32_t *u = (int32_t *)(ws + P.qp_u);
@@ -1276,7 +1279,7 @@ static cb_status query_probe(cb_model *m, const cb_request *reqs, int B,
   // before it reads them).  Anchor probe: the anchors' stitched rows of all
   // probe layers, gathered at once.
   const int64_t pstride = (int64_t)Q.n_probe * m->kvw;    // elements per probe layer
-  if (!Q.all) {
+  if (!Q.all && !layerwise) {
     CB_TRY(ready(last));
     CB_CUDA(launch_gather_layers(out->k_cache, lstride, m->kvw, P.T_total, rows, Q.n_probe,
                                  m->kvw, ws + P.qp_k, pstride, m->kvw, m->eb, last + 1, st, s));
@@ -1285,6 +1288,17 @@ static cb_status query_probe(cb_model *m, const cb_request *reqs, int B,
   }
   for (int l = 0; l <= last; ++l) {
     if (Q.all) CB_TRY(ready(l));
+    if (!Q.all && layerwise) {
+      CB_TRY(ready(l));
+      CB_CUDA(launch_gather_layers(layer_ptr(out->k_cache, l, lstride, m->eb), lstride, m->kvw,
+                                   P.T_total, rows, Q.n_probe, m->kvw,
+                                   layer_ptr(ws + P.qp_k, l, pstride, m->eb), pstride, m->kvw,
+                                   m->eb, 1, st, s));
+      CB_CUDA(launch_gather_layers(layer_ptr(out->v_cache, l, lstride, m->eb), lstride, m->kvw,
+                                   P.T_total, rows, Q.n_probe, m->kvw,
+                                   layer_ptr(ws + P.qp_v, l, pstride, m->eb), pstride, m->kvw,
+                                   m->eb, 1, st, s));
+    }
     const char *kl = layer_ptr(out->k_cache, l, lstride, m->eb);
     void *pk = Q.all ? layer_ptr(out->k_cache, l, lstride, m->eb) : layer_ptr(ws + P.qp_k, l, pstride, m->eb);
     void *pv = Q.all ? layer_ptr(out->v_cache, l, lstride, m->eb) : layer_ptr(ws + P.qp_v, l, pstride, m->eb);
@@ -1565,7 +1579,7 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
     if (query) {
       // I(t) in the deviation buffer, then P = TopK(I, k) ([QCF] Eq. 11)
       CB_TRY(query_probe(m, reqs, B, p, P, ws, out, lstride, S, h_all, dev, st, s,
-                         stitch_through));
+                         stitch_through, host_kv));
       if (p->forced_selected) {
         if (sel != p->forced_selected && P.K_total > 0)
           CB_CUDA(cudaMemcpyAsync(sel, p->forced_selected, P.K_total * sizeof(int32_t),
@@ -1720,6 +1734,7 @@ std::vector<uint8_t> call_key(const cb_model *m, const cb_request *reqs, int B,
   k.put(p->forced_selected);
   k.put(p->forced_kept);
   k.put(p->host_load_ctas);
+  k.put(p->anchors);
   k.put(p->anchor_rule);
   k.put(p->anchor_bp);
   k.put(p->n_crit);
@@ -1835,7 +1850,8 @@ extern "C" cb_status cb_blend_prefill_host_kv(cb_model *m, const cb_request *req
         // allocation's device address as well (unified addressing)
         const bool kernel_reads =
             p && (p->host_load_ctas > 0 ||
-                  (p->policy == CB_POLICY_QUERY_PROBE && p->anchor_rule == CB_ANCHOR_KNORM));
+                  (p->policy == CB_POLICY_QUERY_PROBE && p->anchor_rule == CB_ANCHOR_KNORM &&
+                   !p->anchors));
         if (kernel_reads && a.devicePointer != ptr)
           return fail(CB_ERR_INVALID_ARG, "request %d segment %d: chunk cache is not mapped at the same device address (read by a kernel)", b, i);
       }

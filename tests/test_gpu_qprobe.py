@@ -114,8 +114,10 @@ def test_query_probe_blend(q3, policy, query, rule, bp, crit):
                                "crit_layers": [1, 2]}, "sink", 1000, [1, 2]),
     (L.CB_POLICY_QUERY_PROBE, {"anchor_rule": L.CB_ANCHOR_KNORM, "anchor_bp": 1000,
                                "crit_layers": [0, 1]}, None, 1000, [0, 1]),
+    (L.CB_POLICY_QUERY_PROBE, {"anchor_rule": L.CB_ANCHOR_KNORM, "anchor_bp": 1000,
+                               "crit_layers": [1, 2], "anchors": "given"}, None, 1000, [1, 2]),
     (L.CB_POLICY_QUERY_FULL, None, "all", 0, None),
-], ids=["probe_sink", "probe_knorm", "full_view"])
+], ids=["probe_sink", "probe_knorm", "probe_given_anchors", "full_view"])
 def test_query_policies_on_host_resident_chunks(q3, policy, query, rule, bp, crit, ctas):
     """[CB] "Hiding Recompute Behind I/O" with QCFuse's selectors: the chunk
     caches stay in pinned host memory and arrive layer by layer (the layers
@@ -129,14 +131,19 @@ def test_query_policies_on_host_resident_chunks(q3, policy, query, rule, bp, cri
     with this call's P at 2e-2."""
     hs, hreq = _host_store(q3)
     cs = torch.cuda.Stream()
-    out = q3.model.cb_blend_prefill_host_kv(hreq, 1500, cs, policy=policy, sel_layer=0,
-                                            query=query, host_load_ctas=ctas)
-    # the device-resident call on a device copy of the same host store (a
-    # second chunk prefill would differ in the last bits)
+    # the device-resident call runs on a device copy of the same host store
+    # (a second chunk prefill would differ in the last bits)
     dK, dV = hs.K.cuda(), hs.V.cuda()
     dsegs = [R.Seg(sg.len, dK[0, hs.where[c.chunk_id][0]], dV[0, hs.where[c.chunk_id][0]],
                    sg.pic_layer_stride, 0) if sg.k_pic is not None else sg
              for sg, c in zip(hreq[0].segs, q3.wl.requests[0].segments)]
+    if query is not None and query.get("anchors") == "given":
+        # the chunks' anchors kept with the store: no kernel reads the host keys
+        anchors, _ = q3.model.cb_anchor_select([sg for sg in dsegs if sg.k_pic is not None],
+                                              L.CB_ANCHOR_KNORM, 1000, with_scores=False)
+        query = dict(query, anchors=anchors)
+    out = q3.model.cb_blend_prefill_host_kv(hreq, 1500, cs, policy=policy, sel_layer=0,
+                                            query=query, host_load_ctas=ctas)
     ref = q3.model.cb_blend_prefill([R.Req(hreq[0].tokens, dsegs)], 1500, policy=policy,
                                     sel_layer=0, query=query)
     torch.cuda.synchronize()
@@ -164,6 +171,34 @@ def test_query_policies_on_host_resident_chunks(q3, policy, query, rule, bp, cri
         assert rms_rel(host(out["v_cache"][l]), oref.V[l]) <= TOL
     Rn = len(oref.rows)
     assert rms_rel(host(out["hidden"][:Rn]), oref.hidden) <= TOL
+
+
+def test_query_probe_with_given_anchors(q3):
+    """A store that keeps each chunk's anchors (cb_anchor_select, Knorm at
+    10%) passes them in: the probe then ranks nothing, and its I(t) agrees
+    with the call that ranks the same anchors itself (up to the residual
+    projections' run-to-run rounding), P the exact top-k of its own I.  An
+    anchor outside its chunk is reported as CB_ERR_DEVICE_INDEX."""
+    chunks = _chunks(q3)
+    segs_g = [q3.store.seg(s.chunk_id) for s in chunks]
+    anchors, _ = q3.model.cb_anchor_select(segs_g, L.CB_ANCHOR_KNORM, 1000, with_scores=False)
+    base = {"anchor_rule": L.CB_ANCHOR_KNORM, "anchor_bp": 1000, "crit_layers": [1, 2]}
+    kw = dict(policy=L.CB_POLICY_QUERY_PROBE, sel_layer=0)
+    own = q3.model.cb_blend_prefill(q3.gpu_reqs(), 1500, query=base, **kw)
+    given = q3.model.cb_blend_prefill(q3.gpu_reqs(), 1500, query=dict(base, anchors=anchors), **kw)
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    N = sum(s.len for s in segs_g)
+    k = O.select_count(N, 1500)
+    I_o = own["deviation"][:N].cpu().numpy().astype(np.float64)
+    I_g = given["deviation"][:N].cpu().numpy().astype(np.float64)
+    assert rms_rel(I_g, I_o) <= 1e-3
+    assert list(given["selected"][:k].cpu().numpy()) == list(O.token_topk(I_g, k))
+    bad = anchors.clone()
+    bad[0] = segs_g[0].len                       # one past the first chunk
+    q3.model.cb_blend_prefill(q3.gpu_reqs(), 1500, query=dict(base, anchors=bad), **kw)
+    torch.cuda.synchronize()
+    assert R.device_status() == L.CB_ERR_DEVICE_INDEX
 
 
 def test_query_probe_knorm_with_the_gpu_anchors(q3):
