@@ -75,8 +75,11 @@ def load_peaks():
 
 # ---------------------------------------------------------------- clocks --
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms.  mark(True)
+    and mark(False) bracket the timed region on the host clock; stop() then
+    keeps the samples taken inside it (all samples when none fell inside,
+    with samples_in_window 0)."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -84,6 +87,7 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.path = None
+        self.window = [None, None]
 
     def start(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -91,10 +95,23 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+
+    def mark(self, begin):
+        self.window[0 if begin else 1] = time.time()
+
+    @staticmethod
+    def _when(stamp):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(stamp, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
 
     def stop(self):
         if self.proc is None:
@@ -104,25 +121,30 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, mx, reasons = [], [], set()
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
+                    rows.append((self._when(parts[0]), float(parts[2]), float(parts[3]),
+                                 {n for n, v in zip(names, parts[6:10])
+                                  if v.lower().startswith("active")}))
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
         os.unlink(self.path)
+        t0, t1 = self.window
+        inside = [r for r in rows if t0 is not None and t1 is not None and r[0] is not None
+                  and t0 <= r[0] <= t1]
+        use = inside or rows
+        sm = [r[1] for r in use]
+        reasons = set().union(*[r[3] for r in use]) if use else set()
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "sm_max_mhz": max(r[2] for r in use) if use else None,
+                "samples": len(sm), "samples_in_window": len(inside),
+                "reasons": sorted(reasons)}
 
 
 # --------------------------------------------------------------- ranks --
@@ -269,7 +291,9 @@ def timed_with_clocks(index, fn):
     clocks.start()
     time.sleep(0.3)
     try:
+        clocks.mark(True)
         r = fn()
+        clocks.mark(False)
     finally:
         clk = clocks.stop()
     return r, clk
@@ -452,11 +476,13 @@ def run_ours(args):
     clocks.start()
     time.sleep(0.3)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    clocks.mark(True)
     ev[0].record(st)
     for i in range(args.steps):
         graph.replay()
         ev[i + 1].record(st)
     torch.cuda.synchronize()
+    clocks.mark(False)
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
@@ -618,6 +644,7 @@ def run_rolling(args):
     clocks = ClockSampler(device.index)
     clocks.start()
     time.sleep(0.3)
+    clocks.mark(True)
     for name, policy in (("token_topk", L.CB_POLICY_TOKEN_TOPK),
                          ("single_window", L.CB_POLICY_SINGLE_WINDOW),
                          ("fixed_chunk", L.CB_POLICY_FIXED_CHUNK),
@@ -673,6 +700,7 @@ def run_rolling(args):
                         "captured_deviation_median": statistics.median(caps)}
         if fulls:
             result["full_prefill_ttft_ms_median"] = statistics.median(fulls)
+    clocks.mark(False)
     clk = clocks.stop()
     T = len(wl.requests[0].tokens)
     full = result.get("full_prefill_ttft_ms_median")
@@ -771,6 +799,7 @@ def run_batch(args):
     clocks = ClockSampler(device.index)
     clocks.start()
     time.sleep(0.3)
+    clocks.mark(True)
     for r in ratios:
         plan = model.plan(reqs, r)
         outs = model.alloc_outputs(plan, len(reqs))
@@ -788,6 +817,7 @@ def run_batch(args):
                                    "kernels": kern}
         del outs
         torch.cuda.empty_cache()
+    clocks.mark(False)
     clk = clocks.stop()
     if R.device_status() != 0:
         raise RuntimeError("device status set during the batched workload")
@@ -840,6 +870,7 @@ def run_host_kv(args):
     clocks = ClockSampler(device.index)
     clocks.start()
     time.sleep(0.3)
+    clocks.mark(True)
     dev_ms, _ = _graph_ms(lambda: model.cb_blend_prefill(reqs, RATIO_BP, outputs=outs),
                           args.steps, st)
     # per-layer recompute time of the blend at each ratio (device store)
@@ -897,6 +928,7 @@ def run_host_kv(args):
         reqs, RATIO_BP, policy=L.CB_POLICY_QUERY_PROBE, sel_layer=0, query=qa, outputs=qd),
         args.steps, st)
     del qd, qh
+    clocks.mark(False)
     clk = clocks.stop()
     if R.device_status() != 0:
         raise RuntimeError("device status set during the host-resident workload")
@@ -976,6 +1008,7 @@ def run_qcf(args):
     clocks = ClockSampler(device.index)
     clocks.start()
     time.sleep(0.3)
+    clocks.mark(True)
     for r in (1500, 3000):
         for name, kw in pols.items():
             plan_r = model.plan(reqs, r, **kw)
@@ -1009,6 +1042,7 @@ def run_qcf(args):
             rows[f"{name} r={r / 100:g}%"] = entry
             del o
             torch.cuda.empty_cache()
+    clocks.mark(False)
     clk = clocks.stop()
     if R.device_status() != 0:
         raise RuntimeError("device status set during the query-aware workload")
