@@ -7,7 +7,7 @@
   request checked alone against the oracle;
 * the degenerate budgets: one cached token with the smallest nonzero ratio
   (k = max(1, floor(N r)) = 1, the only token) and r = 0 (pure reuse), with
-  a one-token query;
+  a one-token query; a request with no cached chunk (N = 0) in a batch;
 * the bf16 tensor-core path on ragged chunks (100, 333 and 7 tokens + 13
   query tokens) with the oracle's selection imposed: row counts that leave
   partial GEMM tiles and attention tiles everywhere.
@@ -117,6 +117,35 @@ def test_one_cached_token_budgets(ratio_bp):
     assert int(out["first_token"][0]) == ref.token or \
         O.first_token_logits(st.om, ref.hidden[-1])[int(out["first_token"][0])] >= \
         O.first_token_logits(st.om, ref.hidden[-1]).max() - 1e-4
+
+
+def test_request_without_cached_chunks_in_a_batch_fp32():
+    """A request whose context has no cached chunk (N = 0, so k = 0: every
+    row is computed at every layer) batched after a normal one.  Each
+    request against the oracle; the chunk-less one also equals a full
+    prefill of its tokens alone (the same sums in the same order)."""
+    rng = np.random.default_rng(11)
+    shape = W.TINY_F32
+    chunks = [W.make_tokens(rng, n, shape.vocab) for n in (64, 96)]
+    st = Stack(shape, 13, chunks)
+    q0 = W.make_tokens(rng, 9, shape.vocab)
+    q1 = W.make_tokens(rng, 41, shape.vocab)
+    bare = R.Req(torch.from_numpy(q1.astype(np.int32)).cuda(), [R.Seg(len(q1))])
+    out = st.model.cb_blend_prefill([st.gpu_req([0, 1], q0), bare], 1500)
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    k0 = O.select_count(160, 1500)
+    ref0 = st.oracle([0, 1], q0, 1500)
+    _check_fp32(out, ref0, 0, 169, 0, 0, k0)
+    ref1 = O.blend_prefill(st.om, [(q1, False)], [], 1500)
+    assert len(ref1.selected) == 0 and len(ref1.rows) == 41
+    R0 = len(ref0.rows)
+    _check_fp32(out, ref1, 169, 41, R0, k0, 0)
+    full = st.model.cb_full_prefill([bare])
+    torch.cuda.synchronize()
+    assert torch.equal(out["k_cache"][:, 169:210], full["k_cache"][:, :41])
+    assert torch.equal(out["v_cache"][:, 169:210], full["v_cache"][:, :41])
+    assert int(out["first_token"][1]) == int(full["first_token"][0])
 
 
 def test_ragged_chunks_bf16_forced():
