@@ -264,7 +264,7 @@ topk_kernel(const __grid_constant__ SelParams p, const float *__restrict__ dev,
 // longer request reads them back from dev_out) for the select's passes.
 constexpr int kSmemCtx = 40960;
 constexpr int kPartsUnroll = 8;            // head partials loaded at once (more: one by one)
-constexpr int kPartsTok = 3;               // tokens per thread per round
+constexpr int kPartsTok = 3;               // tokens per thread per pass
 template <bool RANK>
 __global__ void __launch_bounds__(kSelThreads)
 parts_kernel(const __grid_constant__ SelParams p, const float *__restrict__ parts, int n_parts,

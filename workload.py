@@ -225,7 +225,7 @@ def llama_rag(seed: int = 1, n_layers: int | None = None, n_chunks: int = 6,
     chunks = [make_tokens(rng, chunk_len, m.vocab) for _ in range(n_chunks)]
     segs = [Segment(c, i) for i, c in enumerate(chunks)]
     segs.append(Segment(make_tokens(rng, n_query, m.vocab)))
-    return Workload("llama8b_rag_6x512_r15", m, seed, ratio_bp, "token_topk",
+    return Workload("llama8b_rag_6x512_ratio15pct", m, seed, ratio_bp, "token_topk",
                     chunks, [Request(segs)])
 
 
@@ -243,7 +243,7 @@ def qwen_pool(seed: int = 2, n_layers: int | None = None, pool: int = 40,
         segs = [Segment(chunks[i], int(i)) for i in order]
         segs.append(Segment(make_tokens(rng, n_query, m.vocab)))
         reqs.append(Request(segs))
-    return Workload("qwen8b_pool40_10x1024_b4_r30", m, seed, ratio_bp,
+    return Workload("qwen8b_pool40_10x1024_b4_ratio30pct", m, seed, ratio_bp,
                     "token_topk", chunks, reqs)
 
 
