@@ -47,3 +47,26 @@ def test_no_sample_in_the_window_falls_back_to_all():
     r = _sampler(rows, (t0, t0 + 0.1)).stop()
     assert r["samples_in_window"] == 0 and r["samples"] == 2
     assert r["sm_mhz"] == 2035.0
+
+
+def test_reference_arm_prints_its_line():
+    """bench.py --impl reference (the oracle on the host cores): one JSON
+    line with the base contract's keys, the oracle's cpu_baseline and an
+    e2e object of its own value."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    run = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "1"],
+                         capture_output=True, text=True, timeout=600, cwd=root)
+    assert run.returncode == 0, run.stderr[-2000:]
+    lines = [l for l in run.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 1
+    for key in ("metric", "unit", "n_gpus", "ms_per_step", "higher_is_better", "dtype",
+                "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
