@@ -173,6 +173,49 @@ def test_query_policies_on_host_resident_chunks(q3, policy, query, rule, bp, cri
     assert rms_rel(host(out["hidden"][:Rn]), oref.hidden) <= TOL
 
 
+@pytest.mark.parametrize("policy,query", [
+    (L.CB_POLICY_QUERY_PROBE, {"anchor_rule": L.CB_ANCHOR_KNORM, "anchor_bp": 1000,
+                               "crit_layers": [1, 2]}),
+    (L.CB_POLICY_QUERY_FULL, None),
+], ids=["probe_knorm", "full_view"])
+def test_query_policies_batch_of_two(q3, policy, query):
+    """Two requests in one call (the test request, and its chunks in the
+    other order with another query) against each request alone: I(t)
+    within 1e-3 (run-to-run rounding of the residual projections), P the
+    exact top-k of its own I, and every row left unselected in both calls
+    identical in every layer."""
+    rng = np.random.default_rng(31)
+    rq = q3.wl.requests[0]
+    cached = [s for s in rq.segments if s.cached]
+    q2 = W.make_tokens(rng, 48, q3.shape.vocab)
+    reqs_np = [(list(cached), rq.segments[-1].tokens), (list(reversed(cached)), q2)]
+    def gpu_req(chunks, q):
+        toks = np.concatenate([s.tokens for s in chunks] + [q]).astype(np.int32)
+        return R.Req(torch.from_numpy(toks).cuda(),
+                     [q3.store.seg(s.chunk_id) for s in chunks] + [R.Seg(len(q))])
+    kw = dict(policy=policy, sel_layer=0, query=query)
+    both = q3.model.cb_blend_prefill([gpu_req(*r) for r in reqs_np], 1500, **kw)
+    alone = [q3.model.cb_blend_prefill([gpu_req(*r)], 1500, **kw) for r in reqs_np]
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    t_off = n_off = k_off = 0
+    for (chunks, q), one in zip(reqs_np, alone):
+        N = sum(len(s.tokens) for s in chunks)
+        T, k = N + len(q), O.select_count(N, 1500)
+        I_b = both["deviation"][n_off:n_off + N].cpu().numpy().astype(np.float64)
+        I_a = one["deviation"][:N].cpu().numpy().astype(np.float64)
+        assert rms_rel(I_b, I_a) <= 1e-3
+        P_b = both["selected"][k_off:k_off + k].cpu().numpy()
+        assert list(P_b) == list(O.token_topk(I_b, k))
+        keep = np.setdiff1d(np.arange(N), np.union1d(P_b, one["selected"][:k].cpu().numpy()))
+        rows_b = torch.from_numpy(keep + t_off).cuda()
+        rows_a = torch.from_numpy(keep).cuda()
+        for l in range(q3.shape.n_layers):
+            assert torch.equal(both["k_cache"][l][rows_b], one["k_cache"][l][rows_a]), l
+            assert torch.equal(both["v_cache"][l][rows_b], one["v_cache"][l][rows_a]), l
+        t_off, n_off, k_off = t_off + T, n_off + N, k_off + k
+
+
 def test_query_probe_with_given_anchors(q3):
     """A store that keeps each chunk's anchors (cb_anchor_select, Knorm at
     10%) passes them in: the probe then ranks nothing, and its I(t) agrees
