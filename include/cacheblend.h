@@ -152,6 +152,20 @@ unsigned long long cb_debug_launch_count(void);
 #define CB_GEMM_SWAP_AB_PAIR 3
 cb_status cb_debug_gemm_path(int path);
 
+/* Whether a bf16 decoder layer runs its MLP (gate/up projection with SiLU
+ * gating, then the down projection + residual) as one launch (on = 1, the
+ * default) or as two (on = 0), for every call issued after this one
+ * (process-wide).  In the one-launch form each down-projection k-block waits
+ * only for the gate/up tile that wrote its 64 features (a flag in the
+ * workspace), so the down projection starts while the last gate/up tiles
+ * finish.  Both forms compute the same function; they differ in the order of
+ * fp32 additions (partial sums of split tiles, residual accumulation).  The
+ * one-launch form applies where both projections take the same swapped
+ * GEMM form (cb_debug_gemm_path) and the flags fit (rows <= 16384 / (d_ffn
+ * / 64) * 256); otherwise the two launches run.  Returns CB_ERR_INVALID_ARG
+ * for on not 0 or 1. */
+cb_status cb_debug_mlp_fusion(int on);
+
 /* Debug index checks (process-wide, off by default).  While on, every call
  * also validates the device-side index arrays it consumes before using them:
  * a blended prefill's selected positions (forced or ranked) and each gradual
@@ -185,6 +199,10 @@ cb_status cb_debug_index_checks(int on);
 #define CB_PROBE_SELECT 7    /* deviation + ranking at the selection layer */
 #define CB_PROBE_GATHER 8    /* computed-row list + hidden-state gather */
 #define CB_PROBE_LM_HEAD 9   /* final norm + tied LM head + arg-max */
+#define CB_PROBE_MLP 10      /* gate/up with SiLU gating, then down projection +
+                                residual, as one launch (the bf16 default; see
+                                cb_debug_mlp_fusion): classes 3 and 4 then
+                                record nothing */
 cb_status cb_debug_probe_start(int kind, int max_launches);
 cb_status cb_debug_probe_stop(int *n_launches, float *total_ms);
 

@@ -28,6 +28,7 @@ CB_EPI_STORE, CB_EPI_RESID, CB_EPI_SWIGLU = 0, 1, 2
 CB_GEMM_AUTO, CB_GEMM_TOKEN_M, CB_GEMM_SWAP_AB, CB_GEMM_SWAP_AB_PAIR = 0, 1, 2, 3
 CB_PROBE_QKV, CB_PROBE_O, CB_PROBE_SWIGLU, CB_PROBE_DOWN, CB_PROBE_ATTENTION = 1, 2, 3, 4, 5
 CB_PROBE_STITCH, CB_PROBE_SELECT, CB_PROBE_GATHER, CB_PROBE_LM_HEAD = 6, 7, 8, 9
+CB_PROBE_MLP = 10
 CB_MAX_BATCH = 64
 CB_MAX_SPANS = 1024
 
@@ -130,6 +131,7 @@ def _load():
         "cb_debug_launch_count": (C.c_ulonglong, []),
         "cb_debug_gemm_path": (S, [i32]),
         "cb_debug_index_checks": (S, [i32]),
+        "cb_debug_mlp_fusion": (S, [i32]),
         "cb_debug_probe_start": (S, [i32, i32]),
         "cb_debug_probe_stop": (S, [C.POINTER(i32), C.POINTER(C.c_float)]),
         "cb_rope_table_elems": (C.c_size_t, [i32, i32]),
@@ -193,7 +195,7 @@ lib = _load()
 EXPORTED = [
     "cb_last_error_message", "cb_version", "cb_get_device_status",
     "cb_debug_expire_wait", "cb_debug_launch_count", "cb_debug_gemm_path",
-    "cb_debug_index_checks",
+    "cb_debug_index_checks", "cb_debug_mlp_fusion",
     "cb_debug_probe_start", "cb_debug_probe_stop",
     "cb_rope_table_elems",
     "cb_rope_table_init",

@@ -81,6 +81,12 @@ void cb::note_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
 extern "C" unsigned long long cb_debug_launch_count(void) { return g_launches.load(); }
 
 static std::atomic<int> g_gemm_path{CB_GEMM_AUTO};
+static std::atomic<int> g_mlp_fusion{1};
+extern "C" cb_status cb_debug_mlp_fusion(int on) {
+  if (on != 0 && on != 1) return fail(CB_ERR_INVALID_ARG, "on must be 0 or 1");
+  g_mlp_fusion.store(on);
+  return CB_OK;
+}
 static std::atomic<int> g_index_checks{0};
 bool cb::index_checks_on() { return g_index_checks.load(std::memory_order_relaxed) != 0; }
 extern "C" cb_status cb_debug_index_checks(int on) {
@@ -140,7 +146,7 @@ static void probe_release() {
 }
 
 extern "C" cb_status cb_debug_probe_start(int kind, int max_launches) {
-  if (kind < CB_PROBE_QKV || kind > CB_PROBE_LM_HEAD || max_launches <= 0 ||
+  if (kind < CB_PROBE_QKV || kind > CB_PROBE_MLP || max_launches <= 0 ||
       max_launches > 65536)
     return fail(CB_ERR_INVALID_ARG, "bad probe kind or max_launches");
   std::lock_guard<std::mutex> lk(g_probe_mu);
@@ -681,6 +687,7 @@ struct LayerScratch {
   void *attn;          // attention partials (split key ranges)
   size_t attn_bytes;
   void *split;         // the swapped GEMM's tail-split partials and counters (bf16)
+  int *mlp_epoch;      // the call's last fused-MLP epoch (host counter; NULL: no fusion)
 };
 
 struct LayerOffsets {
@@ -707,10 +714,13 @@ LayerOffsets carve_layer(Carver &c, const cb_model *m, int64_t n) {
 
 LayerScratch bind_layer(char *ws, const LayerOffsets &L) {
   return LayerScratch{ws + L.x, ws + L.q, ws + L.o, ws + L.g, (float *)(ws + L.qkv32),
-                      ws + L.attn, L.attn_bytes, L.split_bytes ? ws + L.split : nullptr};
+                      ws + L.attn, L.attn_bytes, L.split_bytes ? ws + L.split : nullptr,
+                      nullptr};
 }
 
-// The tail-split counters start at zero in every call (each GEMM leaves them zero).
+// The tail-split counters start at zero in every call (each GEMM leaves them
+// zero), and so do the fused MLP's flags (each launch of the call takes the
+// next epoch, counted from 1 in *S.mlp_epoch).
 cudaError_t reset_split(const LayerScratch &S, cudaStream_t s) {
   if (!S.split) return cudaSuccess;
   return cudaMemsetAsync((char *)S.split + gemm_split_flags_offset(), 0,
@@ -1073,6 +1083,24 @@ static cb_status layer_forward(cb_model *m, int l, float *h, int n, const int32_
   CB_TRY(run_linear(m, S.o, m->qw, L.w_o, nullptr, m->qw, n, d, m->qw, EPI_RESID, h, d, s));
   probe_mark(CB_PROBE_O, false, s);
   CB_CUDA(launch_rmsnorm(h, d, nullptr, n, d, L.norm2, c.norm_eps, S.x, d, dt, s));
+  if (dt == CB_BF16 && S.split && S.mlp_epoch && g_mlp_fusion.load(std::memory_order_relaxed)) {
+    // gate/up and down in one launch (the swapped pair form both take)
+    const int path = g_gemm_path.load(std::memory_order_relaxed);
+    const int form = path == CB_GEMM_AUTO        ? gemm_auto_form(n, d, EPI_SWIGLU)
+                     : path == CB_GEMM_SWAP_AB      ? 1
+                     : path == CB_GEMM_SWAP_AB_PAIR ? 2
+                                                    : 0;
+    const int form_down = path == CB_GEMM_AUTO ? gemm_auto_form(n, F, EPI_RESID) : form;
+    if (form && form == form_down && gemm_mlp_fits(n, F, form)) {
+      probe_mark(CB_PROBE_MLP, true, s);
+      const cudaError_t e = launch_gemm_mlp(S.x, d, L.w_gate, L.w_up, d, L.w_down, F, n, F, d,
+                                            S.g, F, h, d, st, s, form, S.split,
+                                            ++*S.mlp_epoch);
+      probe_mark(CB_PROBE_MLP, false, s);
+      CB_CUDA(e);
+      return CB_OK;
+    }
+  }
   probe_mark(CB_PROBE_SWIGLU, true, s);
   CB_TRY(run_linear(m, S.x, d, L.w_gate, L.w_up, d, n, F, d, EPI_SWIGLU, S.g, F, s, nullptr,
                     S.split));
@@ -1114,7 +1142,9 @@ extern "C" cb_status cb_blend_layer(cb_model *m, int layer, float *h, int n_rows
   }
   int *st;
   CB_TRY(status_ptr(&st));
-  const LayerScratch S = bind_layer((char *)ws, L);
+  LayerScratch S = bind_layer((char *)ws, L);
+  int mlp_epoch = 0;
+  S.mlp_epoch = &mlp_epoch;
   CB_CUDA(reset_split(S, stream));
   return layer_forward(m, layer, h, n_rows, pos, cache_row, ar, k_cache, v_cache, S, st, stream);
 }
@@ -1395,7 +1425,9 @@ static cb_status blend_impl(cb_model *m, const cb_request *reqs, int B,
   int32_t *pos_c = out->rows ? out->rows : (int32_t *)(ws + P.pos_c);
   int32_t *glob_c = (int32_t *)(ws + P.glob_c);
   float *h_c = out->hidden ? out->hidden : (float *)(ws + P.h_c);
-  const LayerScratch S = bind_layer(ws, P.lay);
+  LayerScratch S = bind_layer(ws, P.lay);
+  int mlp_epoch = 0;
+  S.mlp_epoch = &mlp_epoch;
   CB_CUDA(reset_split(S, stream));
 
   // 1. re-position + stitch of every cached segment, layers [s, L)
@@ -1875,7 +1907,9 @@ extern "C" cb_status cb_full_prefill(cb_model *m, const cb_request *reqs, int B,
   float *h = out->hidden ? out->hidden : (float *)(ws + P.h_all);
   int32_t *pos_all = out->rows ? out->rows : (int32_t *)(ws + P.pos_all);
   int32_t *glob_all = (int32_t *)(ws + P.glob_all);
-  const LayerScratch S = bind_layer(ws, P.lay);
+  LayerScratch S = bind_layer(ws, P.lay);
+  int mlp_epoch = 0;
+  S.mlp_epoch = &mlp_epoch;
   CB_CUDA(reset_split(S, stream));
   const int32_t *toks[CB_MAX_BATCH];
   for (int b = 0; b < B; ++b) toks[b] = reqs[b].tokens;

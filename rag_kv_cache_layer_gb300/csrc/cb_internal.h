@@ -237,7 +237,8 @@ enum GemmEpi {
   EPI_RESID = 2,
   EPI_SWIGLU = 3,
   EPI_QKV = 4,
-  EPI_KDEV = 5   // keys -> per-head deviation partials (bf16 swapped GEMM only)
+  EPI_KDEV = 5,  // keys -> per-head deviation partials (bf16 swapped GEMM only)
+  EPI_MLP = 6    // gate/up + SwiGLU, then down + residual, in one launch (launch_gemm_mlp)
 };
 // out = epi(A[M][K] W[N][K]^T); A and W of dtype dt; STORE_F32 and RESID
 // write float, STORE and SWIGLU write dt.
@@ -290,6 +291,23 @@ cudaError_t launch_gemm_sab(const void *A, int64_t lda, const void *W,
                             int cta_group = 1, void *split_ws = nullptr);
 size_t gemm_split_ws_bytes();
 size_t gemm_split_flags_offset();
+// The MLP of a decoder layer as one persistent launch of the swapped GEMM:
+// g = silu(x Wg^T) * (x Wu^T) (bf16 [M][F]), then h += g Wd^T (fp32,
+// stream-K).  Each down-projection k-block waits only for the gate/up tile
+// that wrote its 64 features of g for its token tile: that tile's epilogue
+// sets a flag to `epoch` after its stores, so the down projection runs
+// while the last gate/up tiles drain instead of after the whole launch.
+// The flags live in split_ws at gemm_mlp_flags_offset(); they must hold
+// values below `epoch` (zero them with the tail-split counters, then give
+// every launch on the workspace a larger epoch).  cudaErrorNotSupported:
+// the shapes do not fit one launch; run the two projections instead.
+cudaError_t launch_gemm_mlp(const void *x, int64_t ldx, const void *w_gate, const void *w_up,
+                            int64_t ldw, const void *w_down, int64_t ldwd, int M, int F, int d,
+                            void *g, int64_t ldg, float *h, int64_t ldh, int *status,
+                            cudaStream_t s, int cta_group, void *split_ws, int epoch);
+size_t gemm_mlp_flags_offset();
+// Whether launch_gemm_mlp takes M rows with F-wide gate/up features.
+bool gemm_mlp_fits(int M, int F, int cta_group);
 
 // ------------------------------------------------------------ attention --
 struct AttnReq {

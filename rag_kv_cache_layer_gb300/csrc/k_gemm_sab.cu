@@ -22,6 +22,8 @@
 // units that run the later k-segments leave fp32 partials in a workspace
 // and the unit that runs segment 0 adds them, in segment order, before its
 // epilogue.
+#include <type_traits>
+
 #include "cb_internal.h"
 #include "cb_tc.cuh"
 
@@ -40,6 +42,7 @@ constexpr int kTokTab = 256 * 16;            // Q/K/V, K-deviation: positions, c
 constexpr int kSmemMax = 232448;
 constexpr int kPartFloats = 8 * FM * 32;     // one CTA's partial: 8 chunks x 128 features x 32 tokens
 constexpr int kSplitFlagBytes = 4096;       // arrival counters: one per tail tile and CTA (<= SMs)
+constexpr int kMlpFlags = 16384;            // fused MLP: one flag per (gate/up CTA tile, token tile)
 // Epilogues that take the tail split (the residual one uses stream-K), and
 // the kernel compiled with it.  The Q/K/V epilogue is at its register limit
 // (168 for 320 threads): it has a second instantiation with the split, used
@@ -53,9 +56,15 @@ struct Params {
   int M, N, K;           // tokens, output features, reduction
   int BT, n_tt, n_ft;    // token tile width, token tiles, feature tiles
   int stream_k;
+  // stream-K with defer: a range that crosses a weight tile's end runs the
+  // part after the crossing first (the fused MLP's down projection, whose
+  // last k-blocks wait for the last gate/up tiles)
+  int defer;
   // tail split: tiles [0, n_whole) run whole; every later tile runs as
-  // `split` k-segments on as many units (split = 1: no split)
-  int n_whole, split;
+  // `split` k-segments on as many units (split = 1: no split).  tail_first:
+  // the split tiles are [0, n_tail) instead and the whole ones follow, so
+  // the last tiles to finish hold the highest features (the fused MLP)
+  int n_whole, split, tail_first;
   float *part;           // [tail tile][segment][CG][kPartFloats] partials
   int *flag;             // [tail tile][CG] arrivals of segments 1.., zero between launches
   int stages, stage_bytes;
@@ -68,6 +77,10 @@ struct Params {
   int64_t ld_kv;
   const float2 *rope;
   int Hq, Hkv;
+  // fused MLP: flag[fct * n_tt + tt] = epoch once gate/up CTA tile fct has
+  // written its 64 features of token tile tt
+  int *mlp_flag;
+  int epoch;
 };
 
 // Work decomposition.  Whole tiles: tile index with the token tile fastest,
@@ -84,36 +97,55 @@ struct Params {
 // count, so every unit still ends after the same number of whole tiles.
 // A "unit" is one CTA, or one CTA pair when the MMA spans two SMs (CG = 2);
 // both CTAs of a pair walk the same sequence, ft then counting pair tiles.
-template <int CG>
+// With tail_first the split tiles are the first n_tail tiles.  With defer
+// (stream-K) a range that starts inside a weight tile and runs past its end
+// takes the part after that end first and the first part last.
+template <int CG, bool EXT = false>   // EXT: tail_first and defer are read (the fused MLP)
 struct Work {
   int n_tt, num_kb, my_tt;
-  bool sk;
+  bool sk, tail_first;
   int n_whole, split;
   int seg, tj;           // tail split: k-segment of the current item (-1: whole) and tail tile
-  int64_t n_seg;         // items that are k-segments
+  int64_t n_seg, n_tail; // items that are k-segments; tiles that are split
   int64_t w, w_end, step;
+  int64_t dw0, dw1;      // stream-K: the deferred first part of the range
   __device__ Work(const Params &p, int num_kb_)
-      : n_tt(p.n_tt), num_kb(num_kb_), sk(p.stream_k != 0), n_whole(p.n_whole), split(p.split),
-        seg(-1), tj(0), n_seg(0) {
+      : n_tt(p.n_tt), num_kb(num_kb_), sk(p.stream_k != 0), tail_first(EXT && p.tail_first != 0),
+        n_whole(p.n_whole), split(p.split), seg(-1), tj(0), n_seg(0), n_tail(0), dw0(0), dw1(0) {
     const int unit = blockIdx.x / CG, n_units = gridDim.x / CG;
     const int n_ft = (p.n_ft + CG - 1) / CG;
     step = n_units;
     if (sk) {
       const int64_t total = (int64_t)n_ft * num_kb_;
-      const int groups = n_units / p.n_tt;
+      int64_t groups = n_units / p.n_tt;
+      if (groups > total) groups = total;
       const int g = unit / p.n_tt;
       my_tt = unit % p.n_tt;
       w = g < groups ? total * g / groups : 0;
       w_end = g < groups ? total * (g + 1) / groups : 0;
+      if (EXT && p.defer && w < w_end && w % num_kb_) {
+        const int64_t cross = (w / num_kb_ + 1) * num_kb_;
+        if (cross < w_end) {
+          dw0 = w;
+          dw1 = cross;
+          w = cross;
+        }
+      }
     } else {
       my_tt = 0;
       w = unit;
-      n_seg = split > 1 ? ((int64_t)p.n_tt * n_ft - n_whole) * split : 0;
+      n_tail = split > 1 ? (int64_t)p.n_tt * n_ft - n_whole : 0;
+      n_seg = n_tail * split;
       w_end = n_seg + n_whole;
     }
   }
   __device__ bool next(int &tt, int &ft, int &kb0, int &kb1) {
-    if (w >= w_end) return false;
+    if (w >= w_end) {
+      if (!EXT || dw0 >= dw1) return false;
+      w = dw0;
+      w_end = dw1;
+      dw0 = dw1;
+    }
     if (sk) {
       ft = (int)(w / num_kb);
       kb0 = (int)(w % num_kb);
@@ -122,14 +154,14 @@ struct Work {
       w += kb1 - kb0;
       tt = my_tt;
     } else {
-      int64_t tile = w - n_seg;
+      int64_t tile = w - n_seg + (tail_first ? n_tail : 0);
       kb0 = 0;
       kb1 = num_kb;
       seg = -1;
       if (w < n_seg) {
         tj = (int)(w / split);
         seg = (int)(w % split);
-        tile = n_whole + tj;
+        tile = tail_first ? tj : n_whole + tj;
         kb0 = num_kb * seg / split;
         kb1 = num_kb * (seg + 1) / split;
       }
@@ -171,6 +203,60 @@ __device__ __forceinline__ bool flag_wait_bounded(const int *flag, int want, uin
   }
 }
 
+__device__ __forceinline__ int load_relaxed(const int *flag) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+  return v;
+}
+// Fused MLP, down projection: waits until the k-block kb of its token tile
+// has been written by the gate/up tile (flag[kb * stride] >= epoch), looking
+// ahead over at most 256 k-blocks in one round of loads; returns the end of
+// the run of written k-blocks from kb (<= kb1), or -1 (after recording
+// CB_ERR_TIMEOUT) past the limit.  Called by a whole warp; the acquire and
+// proxy fences order the TMA loads that follow after the flags.
+__device__ int wait_written(const int *flag, int stride, int kb, int kb1, int epoch,
+                            int *status) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (it > 0) {
+      // until kb itself is written, one lane polls it alone (the whole
+      // warp's look-ahead loads would load L2 while gate/up tiles stream)
+      for (uint32_t w = 0;; ++w) {
+        int f = 0;
+        if (lane == 0) f = load_relaxed(flag + (int64_t)kb * stride);
+        if (__shfl_sync(0xffffffffu, f, 0) >= epoch) break;
+        if ((w & 15u) == 15u && globaltimer_ns() - t0 > kWaitLimitNs) {
+          if (lane == 0) report(status, CB_ERR_TIMEOUT);
+          return -1;
+        }
+        __nanosleep(256);
+      }
+    }
+    int v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = kb + 32 * j + lane;
+      v[j] = i < kb1 ? load_relaxed(flag + (int64_t)i * stride) : epoch;
+    }
+    int end = kb1 < kb + 256 ? kb1 : kb + 256;
+#pragma unroll
+    for (int j = 7; j >= 0; --j) {
+      const unsigned nw = __ballot_sync(0xffffffffu, v[j] < epoch);
+      if (nw) end = kb + 32 * j + __ffs(nw) - 1;
+    }
+    if (end > kb) {
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      return end;
+    }
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (lane == 0) report(status, CB_ERR_TIMEOUT);
+      return -1;
+    }
+  }
+}
+
 __device__ __forceinline__ void store_bf16x8(bf16 *dst, const float *v) {
   uint4 pk;
   __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&pk);
@@ -179,11 +265,32 @@ __device__ __forceinline__ void store_bf16x8(bf16 *dst, const float *v) {
   *reinterpret_cast<uint4 *>(dst) = pk;
 }
 
+// The phase's operand (p and the maps of phase 0, or p2 and those of phase
+// 1), chosen at compile time: each role's loop is instantiated per phase.
+template <int PH, typename T>
+__device__ __forceinline__ const T &pick(const T &a, const T &b) {
+  if constexpr (PH == 0) return a;
+  else return b;
+}
+template <int PH>
+__device__ __forceinline__ const CUtensorMap *pick(const CUtensorMap *a, const CUtensorMap *b) {
+  if constexpr (PH == 0) return a;
+  else return b;
+}
+
+// The kernel body.  EPI_MLP runs two GEMMs one after the other on the same
+// units, pipeline stages and accumulators: phase 0 the gate/up projection
+// (mapX, mapW, mapW2, p; SwiGLU epilogue), phase 1 the down projection
+// (mapX2 over phase 0's output, mapW3, p2; residual epilogue, stream-K).
+// The other epilogues run phase 0 only.
 template <int EPI, int CG, bool TS>
-__global__ void __launch_bounds__(kThreads, 1)
-gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW,
-                const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ Params p,
-                int *status) {
+__device__ __forceinline__ void gemm_body(const CUtensorMap *mapX, const CUtensorMap *mapW,
+                                          const CUtensorMap *mapW2, const CUtensorMap *mapX2,
+                                          const CUtensorMap *mapW3, const Params &p,
+                                          const Params &p2, int *status) {
+  constexpr bool MLP = EPI == EPI_MLP;
+  constexpr int kPhases = MLP ? 2 : 1;
+
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.stages * p.stage_bytes + 2 * kTr);
@@ -200,7 +307,6 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
   volatile int *vote = reinterpret_cast<volatile int *>(bars + 24);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_kb = (p.K + BK - 1) / BK;
   // CG = 2: this CTA's rank in its pair; the leader (rank 0) issues the MMAs
   const uint32_t rank = CG == 2 ? cluster_rank() : 0u;
   const bool leader = rank == 0;
@@ -236,48 +342,77 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
     uint32_t phase = 0;
     int issued[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     bool ok = true;
-    Work<CG> wk(p, num_kb);
-    int tt, ft, kb0, kb1;
-    const int bt = p.BT / CG;             // token rows of B held by this CTA
-    while (ok && wk.next(tt, ft, kb0, kb1)) {
-      const int fct = ft * CG + (int)rank;   // this CTA's 128-row weight tile
-      const int ty = tt * p.BT + (int)rank * bt;
-      for (int kb = kb0; kb < kb1; ++kb) {
-        const bool got =
-            mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, kWaitLimitNs, status) && !*fail;
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
-        }
-        if (elect_one()) {
+    auto produce = [&](auto phase_c) {
+      constexpr int ph = decltype(phase_c)::value;
+      const Params &pq = pick<ph>(p, p2);
+      const CUtensorMap *mx = pick<ph>(mapX, mapX2), *mw = pick<ph>(mapW, mapW3);
+      const bool swiglu = MLP ? ph == 0 : EPI == EPI_SWIGLU;
+      const bool gated = MLP && ph == 1;    // B rows come from phase 0 of this launch
+      const int num_kb = (pq.K + BK - 1) / BK;
+      Work<CG, MLP> wk(pq, num_kb);
+      int tt, ft, kb0, kb1;
+      const int bt = pq.BT / CG;             // token rows of B held by this CTA
+      while (ok && wk.next(tt, ft, kb0, kb1)) {
+        const int fct = ft * CG + (int)rank;   // this CTA's 128-row weight tile
+        const int ty = tt * pq.BT + (int)rank * bt;
+        int written = gated ? kb0 : kb1;       // B k-blocks known to be written
+        for (int kb = kb0; kb < kb1; ++kb) {
+          const bool got =
+              mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1, kWaitLimitNs, status) && !*fail;
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
           // the pair's operands all complete on the leader's barrier
           uint32_t fb = smem_u32(&full[stage]);
-          if (leader) expect_tx(fb, CG * p.stage_bytes);
           if (CG == 2) fb = map_to_rank(fb, 0);
           uint8_t *sw = smem + stage * p.stage_bytes;
           uint8_t *sx = sw + kTileW;
-          if (CG == 2) {
-            if (EPI == EPI_SWIGLU) {
-              tma_load_2d_pair(smem_u32(sw), &mapW, fb, kb * BK, fct * 64);
-              tma_load_2d_pair(smem_u32(sw + 64 * 128), &mapW2, fb, kb * BK, fct * 64);
+          // a gated k-block whose token rows are not yet known to be written
+          // issues its weights first and waits for the gate/up tile after
+          const bool wait_x = gated && kb >= written;
+          if (elect_one()) {
+            if (leader) expect_tx(smem_u32(&full[stage]), CG * p.stage_bytes);
+            if (CG == 2) {
+              if (swiglu) {
+                tma_load_2d_pair(smem_u32(sw), mw, fb, kb * BK, fct * 64);
+                tma_load_2d_pair(smem_u32(sw + 64 * 128), mapW2, fb, kb * BK, fct * 64);
+              } else {
+                tma_load_2d_pair(smem_u32(sw), mw, fb, kb * BK, fct * FM);
+              }
+              if (!wait_x) tma_load_2d_pair(smem_u32(sx), mx, fb, kb * BK, ty);
             } else {
-              tma_load_2d_pair(smem_u32(sw), &mapW, fb, kb * BK, fct * FM);
+              if (swiglu) {
+                tma_load_2d(smem_u32(sw), mw, fb, kb * BK, fct * 64);
+                tma_load_2d(smem_u32(sw + 64 * 128), mapW2, fb, kb * BK, fct * 64);
+              } else {
+                tma_load_2d(smem_u32(sw), mw, fb, kb * BK, fct * FM);
+              }
+              if (!wait_x) tma_load_2d(smem_u32(sx), mx, fb, kb * BK, ty);
             }
-            tma_load_2d_pair(smem_u32(sx), &mapX, fb, kb * BK, ty);
-          } else {
-            if (EPI == EPI_SWIGLU) {
-              tma_load_2d(smem_u32(sw), &mapW, fb, kb * BK, fct * 64);
-              tma_load_2d(smem_u32(sw + 64 * 128), &mapW2, fb, kb * BK, fct * 64);
-            } else {
-              tma_load_2d(smem_u32(sw), &mapW, fb, kb * BK, fct * FM);
-            }
-            tma_load_2d(smem_u32(sx), &mapX, fb, kb * BK, ty);
           }
+          __syncwarp();
+          if (wait_x) {
+            written = wait_written(pq.mlp_flag + tt, pq.n_tt, kb, kb1, pq.epoch, status);
+            if (!__all_sync(0xffffffffu, written > kb && !*fail)) {
+              ok = false;
+              ++issued[stage];     // the weight copy above completes on this stage's barrier
+              break;
+            }
+            if (elect_one()) {
+              if (CG == 2) tma_load_2d_pair(smem_u32(sx), mx, fb, kb * BK, ty);
+              else tma_load_2d(smem_u32(sx), mx, fb, kb * BK, ty);
+            }
+            __syncwarp();
+          }
+          ++issued[stage];
+          if (++stage == p.stages) { stage = 0; phase ^= 1; }
         }
-        __syncwarp();
-        ++issued[stage];
-        if (++stage == p.stages) { stage = 0; phase ^= 1; }
       }
+    };
+    produce(std::integral_constant<int, 0>());
+    if constexpr (kPhases > 1) {
+      if (ok) produce(std::integral_constant<int, 1>());
     }
     if (!ok && lane == 0) {
       *fail = 1;
@@ -304,47 +439,56 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
       int buf = 0;
       uint32_t bphase = 0;
       bool ok = true;
-      Work<CG> wk(p, num_kb);
-      int tt, ft, kb0, kb1;
-      while (ok && wk.next(tt, ft, kb0, kb1)) {
-        const bool got =
-            mbar_wait_bounded(smem_u32(&tempty[buf]), bphase ^ 1, kWaitLimitNs, status) && !*fail;
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
-        }
-        fence_after();
-        const uint32_t d = tmem + buf * 256;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[stage]), phase,
-                                                          kWaitLimitNs, status))) {
+      auto issue = [&](auto phase_c) {
+        constexpr int ph = decltype(phase_c)::value;
+        const Params &pq = pick<ph>(p, p2);
+        const int num_kb = (pq.K + BK - 1) / BK;
+        Work<CG, MLP> wk(pq, num_kb);
+        int tt, ft, kb0, kb1;
+        while (ok && wk.next(tt, ft, kb0, kb1)) {
+          const bool got =
+              mbar_wait_bounded(smem_u32(&tempty[buf]), bphase ^ 1, kWaitLimitNs, status) && !*fail;
+          if (!__all_sync(0xffffffffu, got)) {
             ok = false;
             break;
           }
           fence_after();
-          if (elect_one()) {
-            const uint32_t sw = smem_u32(smem + stage * p.stage_bytes);
-            const uint64_t dw = desc_kmajor(sw), dx = desc_kmajor(sw + kTileW);
-#pragma unroll
-            for (int k = 0; k < BK / 16; ++k) {
-              if (CG == 2)
-                mma_pair(d, dw + 2 * k, dx + 2 * k, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-              else
-                mma(d, dw + 2 * k, dx + 2 * k, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          const uint32_t d = tmem + buf * 256;
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full[stage]), phase,
+                                                            kWaitLimitNs, status))) {
+              ok = false;
+              break;
             }
-            if (CG == 2) commit_pair(smem_u32(&empty[stage]), 3);
-            else commit(smem_u32(&empty[stage]));
+            fence_after();
+            if (elect_one()) {
+              const uint32_t sw = smem_u32(smem + stage * p.stage_bytes);
+              const uint64_t dw = desc_kmajor(sw), dx = desc_kmajor(sw + kTileW);
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k) {
+                if (CG == 2)
+                  mma_pair(d, dw + 2 * k, dx + 2 * k, pq.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                else
+                  mma(d, dw + 2 * k, dx + 2 * k, pq.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+              }
+              if (CG == 2) commit_pair(smem_u32(&empty[stage]), 3);
+              else commit(smem_u32(&empty[stage]));
+            }
+            __syncwarp();
+            if (++stage == p.stages) { stage = 0; phase ^= 1; }
+          }
+          if (!ok) break;
+          if (elect_one()) {
+            if (CG == 2) commit_pair(smem_u32(&tfull[buf]), 3);
+            else commit(smem_u32(&tfull[buf]));
           }
           __syncwarp();
-          if (++stage == p.stages) { stage = 0; phase ^= 1; }
+          if (++buf == 2) { buf = 0; bphase ^= 1; }
         }
-        if (!ok) break;
-        if (elect_one()) {
-          if (CG == 2) commit_pair(smem_u32(&tfull[buf]), 3);
-          else commit(smem_u32(&tfull[buf]));
-        }
-        __syncwarp();
-        if (++buf == 2) { buf = 0; bphase ^= 1; }
+      };
+      issue(std::integral_constant<int, 0>());
+      if constexpr (kPhases > 1) {
+        if (ok) issue(std::integral_constant<int, 1>());
       }
       if (!ok && lane == 0) *fail = 1;
     }
@@ -360,243 +504,279 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
     int buf = 0;
     uint32_t bphase = 0;
     int n_tile = 0;
-    Work<CG> wk(p, num_kb);
-    int tt, ft, kb0, kb1;
-    while (wk.next(tt, ft, kb0, kb1)) {
-      const bool whole = kb0 == 0 && kb1 == num_kb;
-      if (EPI == EPI_QKV || EPI == EPI_KDEV) {
-        // the tile's positions and fused-cache rows, read while the MMAs run,
-        // once every warp is done with the previous tile's table
-        epi_all_bar();
-        for (int i = threadIdx.x - 64; i < p.BT; i += 256) {
-          const int tok = tt * p.BT + i;
-          s_pos[i] = tok < p.M ? p.pos[tok] : 0;
-          s_dst[i] = tok < p.M ? (int64_t)p.dst_row[tok] : 0;
-          if (EPI == EPI_KDEV) s_dev[i] = tok < p.M ? p.dev_idx[tok] : -1;
-        }
-      }
-      // tail split: segment 0 finishes the tile once the other segments'
-      // partials have arrived; the later segments only leave partials
-      const bool helper = TS && wk.seg > 0;
-      const bool finisher = TS && wk.seg == 0 && wk.split > 1;
-      int *flag = wk.split > 1 ? p.flag + (int64_t)wk.tj * CG + rank : nullptr;
-      bool bad_l = !mbar_wait_bounded(smem_u32(&tfull[buf]), bphase, kWaitLimitNs, status) || *fail;
-      if (finisher && warp == 2 && lane == 0 && !bad_l) {
-        bad_l = !flag_wait_bounded(flag, wk.split - 1, kWaitLimitNs, status);
-        if (!bad_l) *flag = 0;        // every segment has arrived: ready for the next launch
-      }
-      const bool bad_w = __any_sync(0xffffffffu, bad_l);
-      if (lane == 0) vote[(n_tile & 1) * 8 + warp - 2] = bad_w ? 1 : 0;
-      epi_all_bar();               // also publishes the table to both groups
-      bool bad = false;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) bad |= vote[(n_tile & 1) * 8 + w] != 0;
-      if (bad) {
-        if (lane == 0) *fail = 1;
-        break;
-      }
-      ++n_tile;
-      fence_after();
-      ft = ft * CG + (int)rank;                      // this CTA's 128 weight rows
-      const uint32_t tbase = tmem + buf * 256 + ((uint32_t)(quad * 32) << 16);
-      const int tok0 = tt * p.BT;
-      int head = 0;
-      bool rotate = false;
-      if (EPI == EPI_QKV) {
-        head = ft;
-        rotate = head < p.Hq + p.Hkv;
-      } else if (EPI == EPI_KDEV) {
-        head = ft;                                   // tile h = kv head h of W_k
-        rotate = true;
-      }
-      // this tile's partial slots: [segment][CG][kPartFloats]
-      float *part = wk.split > 1 ? p.part + ((int64_t)wk.tj * wk.split * CG + rank) * kPartFloats
-                                 : nullptr;
-#pragma unroll 1
-      for (int c = 32 * grp; c < p.BT; c += 64) {
-        float x[32];
-        tmem_ld32(tbase + c, x);
-        // partial layout: [chunk][token quad v][feature] float4s, so the 32
-        // lanes of a warp move 512 contiguous bytes per instruction
-        const int64_t po = (int64_t)(c >> 5) * (FM * 32) + r * 4;
-        if (helper) {
-          float4 *dst = reinterpret_cast<float4 *>(part + (int64_t)wk.seg * CG * kPartFloats + po);
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            __stcg(dst + v * FM, make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]));
-          continue;
-        }
-        if (finisher) {
-#pragma unroll 1
-          for (int g = 1; g < wk.split; ++g) {
-            const float4 *src =
-                reinterpret_cast<const float4 *>(part + (int64_t)g * CG * kPartFloats + po);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              const float4 a = __ldcg(src + v * FM);
-              x[4 * v] += a.x;
-              x[4 * v + 1] += a.y;
-              x[4 * v + 2] += a.z;
-              x[4 * v + 3] += a.w;
-            }
+    bool stop = false;
+    auto drain = [&](auto phase_c) {
+      constexpr int ph = decltype(phase_c)::value;
+      const Params &pq = pick<ph>(p, p2);
+      constexpr int epi = MLP ? (ph ? EPI_RESID : EPI_SWIGLU) : EPI;
+      constexpr bool kSplit = TS && !(MLP && ph == 1);   // the down projection never splits
+      const int num_kb = (pq.K + BK - 1) / BK;
+      Work<CG, MLP> wk(pq, num_kb);
+      int tt, ft, kb0, kb1;
+      while (wk.next(tt, ft, kb0, kb1)) {
+        const bool whole = kb0 == 0 && kb1 == num_kb;
+        if (EPI == EPI_QKV || EPI == EPI_KDEV) {
+          // the tile's positions and fused-cache rows, read while the MMAs run,
+          // once every warp is done with the previous tile's table
+          epi_all_bar();
+          for (int i = threadIdx.x - 64; i < pq.BT; i += 256) {
+            const int tok = tt * pq.BT + i;
+            s_pos[i] = tok < pq.M ? pq.pos[tok] : 0;
+            s_dst[i] = tok < pq.M ? (int64_t)pq.dst_row[tok] : 0;
+            if (EPI == EPI_KDEV) s_dev[i] = tok < pq.M ? pq.dev_idx[tok] : -1;
           }
         }
-        // Q/K heads: this thread's rotation factors for the chunk, loaded
-        // before the transpose so that their latency overlaps it
-        constexpr bool kRope = EPI == EPI_QKV || EPI == EPI_KDEV;
-        float4 rf[kRope ? 4 : 1][kRope ? 4 : 1];
-        if (kRope && rotate) {
-          const int e0 = 8 * ((t & 15) & 7);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int i = (t >> 4) + 8 * q;
-            const int ci = (c + i < p.BT && tok0 + c + i < p.M) ? c + i : 0;
-            const float4 *src = reinterpret_cast<const float4 *>(p.rope + (int64_t)s_pos[ci] * 64 + e0);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) rf[q][u] = __ldg(src + u);
-          }
+        // tail split: segment 0 finishes the tile once the other segments'
+        // partials have arrived; the later segments only leave partials
+        const bool helper = kSplit && wk.seg > 0;
+        const bool finisher = kSplit && wk.seg == 0 && wk.split > 1;
+        int *flag = wk.split > 1 ? pq.flag + (int64_t)wk.tj * CG + rank : nullptr;
+        bool bad_l = !mbar_wait_bounded(smem_u32(&tfull[buf]), bphase, kWaitLimitNs, status) || *fail;
+        if (finisher && warp == 2 && lane == 0 && !bad_l) {
+          bad_l = !flag_wait_bounded(flag, wk.split - 1, kWaitLimitNs, status);
+          if (!bad_l) *flag = 0;        // every segment has arrived: ready for the next launch
         }
-        // K-deviation: the reused keys this thread compares, also loaded
-        // before the transpose
-        uint4 kraw[EPI == EPI_KDEV ? 4 : 1];
-        if (EPI == EPI_KDEV) {
+        const bool bad_w = __any_sync(0xffffffffu, bad_l);
+        if (lane == 0) vote[(n_tile & 1) * 8 + warp - 2] = bad_w ? 1 : 0;
+        epi_all_bar();               // also publishes the table to both groups
+        bool bad = false;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int i = (t >> 4) + 8 * q;
-            const bool use = c + i < p.BT && tok0 + c + i < p.M && s_dev[c + i] >= 0;
-            kraw[q] = use ? __ldg(reinterpret_cast<const uint4 *>(
-                                reinterpret_cast<const bf16 *>(p.k_cache) + s_dst[c + i] * p.ld_kv +
-                                head * 128 + 8 * (t & 15)))
-                          : make_uint4(0u, 0u, 0u, 0u);
-          }
+        for (int w = 0; w < 8; ++w) bad |= vote[(n_tile & 1) * 8 + w] != 0;
+        if (bad) {
+          if (lane == 0) *fail = 1;
+          stop = true;
+          break;
         }
-        // transpose: feature column r of 32 tokens -> rows of the chunk
-#pragma unroll
-        for (int i = 0; i < 32; ++i) tr[i * kTrStride + r] = x[i];
-        epi_bar(grp);
-        if (EPI == EPI_STORE) {
-          // 32 tokens x 16 vectors of 8 bf16 features
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int v = t + 128 * q, i = v >> 4, j = v & 15;
-            const int tok = tok0 + c + i, f = ft * FM + 8 * j;
-            if (c + i < p.BT && tok < p.M && f < p.N)
-              store_bf16x8(reinterpret_cast<bf16 *>(p.out) + (int64_t)tok * p.ldo + f,
-                           tr + i * kTrStride + 8 * j);
-          }
-        } else if (EPI == EPI_STORE_F32 || EPI == EPI_RESID) {
-          // 32 tokens x 32 vectors of 4 fp32 features
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int v = t + 128 * q, i = v >> 5, j = v & 31;
-            const int tok = tok0 + c + i, f = ft * FM + 4 * j;
-            if (c + i < p.BT && tok < p.M && f < p.N) {
-              const float4 a = *reinterpret_cast<const float4 *>(tr + i * kTrStride + 4 * j);
-              float4 *o = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) +
-                                                     (int64_t)tok * p.ldo + f);
-              if (EPI == EPI_STORE_F32) {
-                *o = a;
-              } else if (whole) {
-                float4 h = *o;
-                h.x += a.x; h.y += a.y; h.z += a.z; h.w += a.w;
-                *o = h;
-              } else {
-                atomicAdd(o, a);
-              }
-            }
-          }
-        } else if (EPI == EPI_SWIGLU) {
-          // tile rows 0..63 gate, 64..127 up: 32 tokens x 8 vectors of 8.  The
-          // fast divide (2 ulp; 0 once the denominator passes 2^126, where SiLU
-          // is 0 to fp32 precision) is well inside the bf16 output's rounding.
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int v = t + 128 * q, i = v >> 3, j = v & 7;
-            const int tok = tok0 + c + i, f = ft * 64 + 8 * j;
-            if (c + i < p.BT && tok < p.M && f < p.N) {
-              const float *g = tr + i * kTrStride + 8 * j;
-              const float *u = g + 64;
-              float y[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) y[e] = __fdividef(g[e], 1.f + __expf(-g[e])) * u[e];
-              store_bf16x8(reinterpret_cast<bf16 *>(p.out) + (int64_t)tok * p.ldo + f, y);
-            }
-          }
+        ++n_tile;
+        fence_after();
+        ft = ft * CG + (int)rank;                      // this CTA's 128 weight rows
+        const uint32_t tbase = tmem + buf * 256 + ((uint32_t)(quad * 32) << 16);
+        const int tok0 = tt * pq.BT;
+        int head = 0;
+        bool rotate = false;
+        if (EPI == EPI_QKV) {
+          head = ft;
+          rotate = head < pq.Hq + pq.Hkv;
         } else if (EPI == EPI_KDEV) {
-          // 32 tokens x 16 groups of 8 features; the 16 threads of a token
-          // are one half-warp, which sums the head's squared differences
+          head = ft;                                   // tile h = kv head h of W_k
+          rotate = true;
+        }
+        // this tile's partial slots: [segment][CG][kPartFloats]
+        float *part = wk.split > 1 ? pq.part + ((int64_t)wk.tj * wk.split * CG + rank) * kPartFloats
+                                   : nullptr;
+#pragma unroll 1
+        for (int c = 32 * grp; c < pq.BT; c += 64) {
+          float x[32];
+          tmem_ld32(tbase + c, x);
+          // partial layout: [chunk][token quad v][feature] float4s, so the 32
+          // lanes of a warp move 512 contiguous bytes per instruction
+          const int64_t po = (int64_t)(c >> 5) * (FM * 32) + r * 4;
+          if (helper) {
+            float4 *dst = reinterpret_cast<float4 *>(part + (int64_t)wk.seg * CG * kPartFloats + po);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int v = t + 128 * q, i = v >> 4, j = v & 15;
-            const int tok = tok0 + c + i;
-            const int di = (c + i < p.BT && tok < p.M) ? s_dev[c + i] : -1;
-            float acc = 0.f;
-            if (di >= 0) {
-              const float *row = tr + i * kTrStride;
-              const int e0 = 8 * (j & 7);
-              const float *w = reinterpret_cast<const float *>(rf[q]);   // (cos, sin) x 8
-              const bf16 *kb = reinterpret_cast<const bf16 *>(&kraw[q]);
+            for (int v = 0; v < 8; ++v)
+              __stcg(dst + v * FM, make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]));
+            continue;
+          }
+          if (finisher) {
+#pragma unroll 1
+            for (int g = 1; g < wk.split; ++g) {
+              const float4 *src =
+                  reinterpret_cast<const float4 *>(part + (int64_t)g * CG * kPartFloats + po);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float x1 = row[e0 + e], x2 = row[64 + e0 + e];
-                const float co = w[2 * e], si = w[2 * e + 1];
-                const float y = j < 8 ? x1 * co - x2 * si : x2 * co + x1 * si;
-                const float dlt = y - __bfloat162float(kb[e]);
-                acc = fmaf(dlt, dlt, acc);
+              for (int v = 0; v < 8; ++v) {
+                const float4 a = __ldcg(src + v * FM);
+                x[4 * v] += a.x;
+                x[4 * v + 1] += a.y;
+                x[4 * v + 2] += a.z;
+                x[4 * v + 3] += a.w;
               }
             }
-#pragma unroll
-            for (int o = 8; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (j == 0 && di >= 0) reinterpret_cast<float *>(p.out)[head * p.ldo + di] = acc;
           }
-        } else {  // EPI_QKV: one head per tile
+          // Q/K heads: this thread's rotation factors for the chunk, loaded
+          // before the transpose so that their latency overlaps it
+          constexpr bool kRope = EPI == EPI_QKV || EPI == EPI_KDEV;
+          float4 rf[kRope ? 4 : 1][kRope ? 4 : 1];
+          if (kRope && rotate) {
+            const int e0 = 8 * ((t & 15) & 7);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int v = t + 128 * q, i = v >> 4, j = v & 15;
-            const int tok = tok0 + c + i;
-            if (c + i >= p.BT || tok >= p.M) continue;
-            const float *row = tr + i * kTrStride;
-            float y[8];
-            bf16 *dst;
-            if (rotate) {
-              // rotate-half pairs (e, e + 64) at the token's position
-              const int e0 = 8 * (j & 7);
-              const float *w = reinterpret_cast<const float *>(rf[q]);   // (cos, sin) x 8
+            for (int q = 0; q < 4; ++q) {
+              const int i = (t >> 4) + 8 * q;
+              const int ci = (c + i < pq.BT && tok0 + c + i < pq.M) ? c + i : 0;
+              const float4 *src = reinterpret_cast<const float4 *>(pq.rope + (int64_t)s_pos[ci] * 64 + e0);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float x1 = row[e0 + e], x2 = row[64 + e0 + e];
-                const float co = w[2 * e], si = w[2 * e + 1];
-                y[e] = j < 8 ? x1 * co - x2 * si : x2 * co + x1 * si;
+              for (int u = 0; u < 4; ++u) rf[q][u] = __ldg(src + u);
+            }
+          }
+          // K-deviation: the reused keys this thread compares, also loaded
+          // before the transpose
+          uint4 kraw[EPI == EPI_KDEV ? 4 : 1];
+          if (EPI == EPI_KDEV) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int i = (t >> 4) + 8 * q;
+              const bool use = c + i < pq.BT && tok0 + c + i < pq.M && s_dev[c + i] >= 0;
+              kraw[q] = use ? __ldg(reinterpret_cast<const uint4 *>(
+                                  reinterpret_cast<const bf16 *>(pq.k_cache) + s_dst[c + i] * pq.ld_kv +
+                                  head * 128 + 8 * (t & 15)))
+                            : make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+          // transpose: feature column r of 32 tokens -> rows of the chunk
+#pragma unroll
+          for (int i = 0; i < 32; ++i) tr[i * kTrStride + r] = x[i];
+          epi_bar(grp);
+          if (EPI == EPI_STORE) {
+            // 32 tokens x 16 vectors of 8 bf16 features
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int v = t + 128 * q, i = v >> 4, j = v & 15;
+              const int tok = tok0 + c + i, f = ft * FM + 8 * j;
+              if (c + i < pq.BT && tok < pq.M && f < pq.N)
+                store_bf16x8(reinterpret_cast<bf16 *>(pq.out) + (int64_t)tok * pq.ldo + f,
+                             tr + i * kTrStride + 8 * j);
+            }
+          } else if (epi == EPI_STORE_F32 || epi == EPI_RESID) {
+            // 32 tokens x 32 vectors of 4 fp32 features; one loop per kind of
+            // store (with the read-modify-write and the atomic add in one loop
+            // the two-phase kernel's residual epilogue took 13 us a tile
+            // instead of 3)
+            float *const o0 = reinterpret_cast<float *>(pq.out);
+            if (epi == EPI_STORE_F32 || whole) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const int v = t + 128 * q, i = v >> 5, j = v & 31;
+                const int tok = tok0 + c + i, f = ft * FM + 4 * j;
+                if (c + i < pq.BT && tok < pq.M && f < pq.N) {
+                  const float4 a = *reinterpret_cast<const float4 *>(tr + i * kTrStride + 4 * j);
+                  float4 *o = reinterpret_cast<float4 *>(o0 + (int64_t)tok * pq.ldo + f);
+                  if (epi == EPI_STORE_F32) {
+                    *o = a;
+                  } else {
+                    float4 h = *o;
+                    h.x += a.x; h.y += a.y; h.z += a.z; h.w += a.w;
+                    *o = h;
+                  }
+                }
               }
-              dst = head < p.Hq
-                        ? reinterpret_cast<bf16 *>(p.out) + (int64_t)tok * p.ldo + head * 128
-                        : reinterpret_cast<bf16 *>(p.k_cache) + s_dst[c + i] * p.ld_kv +
-                              (head - p.Hq) * 128;
             } else {
 #pragma unroll
-              for (int e = 0; e < 8; ++e) y[e] = row[8 * j + e];
-              dst = reinterpret_cast<bf16 *>(p.v_cache) + s_dst[c + i] * p.ld_kv +
-                    (head - p.Hq - p.Hkv) * 128;
+              for (int q = 0; q < 8; ++q) {
+                const int v = t + 128 * q, i = v >> 5, j = v & 31;
+                const int tok = tok0 + c + i, f = ft * FM + 4 * j;
+                if (c + i < pq.BT && tok < pq.M && f < pq.N)
+                  atomicAdd(reinterpret_cast<float4 *>(o0 + (int64_t)tok * pq.ldo + f),
+                            *reinterpret_cast<const float4 *>(tr + i * kTrStride + 4 * j));
+              }
             }
-            store_bf16x8(dst + 8 * j, y);
+          } else if (epi == EPI_SWIGLU) {
+            // tile rows 0..63 gate, 64..127 up: 32 tokens x 8 vectors of 8.  The
+            // fast divide (2 ulp; 0 once the denominator passes 2^126, where SiLU
+            // is 0 to fp32 precision) is well inside the bf16 output's rounding.
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              const int v = t + 128 * q, i = v >> 3, j = v & 7;
+              const int tok = tok0 + c + i, f = ft * 64 + 8 * j;
+              if (c + i < pq.BT && tok < pq.M && f < pq.N) {
+                const float *g = tr + i * kTrStride + 8 * j;
+                const float *u = g + 64;
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] = __fdividef(g[e], 1.f + __expf(-g[e])) * u[e];
+                store_bf16x8(reinterpret_cast<bf16 *>(pq.out) + (int64_t)tok * pq.ldo + f, y);
+              }
+            }
+          } else if (EPI == EPI_KDEV) {
+            // 32 tokens x 16 groups of 8 features; the 16 threads of a token
+            // are one half-warp, which sums the head's squared differences
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int v = t + 128 * q, i = v >> 4, j = v & 15;
+              const int tok = tok0 + c + i;
+              const int di = (c + i < pq.BT && tok < pq.M) ? s_dev[c + i] : -1;
+              float acc = 0.f;
+              if (di >= 0) {
+                const float *row = tr + i * kTrStride;
+                const int e0 = 8 * (j & 7);
+                const float *w = reinterpret_cast<const float *>(rf[q]);   // (cos, sin) x 8
+                const bf16 *kb = reinterpret_cast<const bf16 *>(&kraw[q]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const float x1 = row[e0 + e], x2 = row[64 + e0 + e];
+                  const float co = w[2 * e], si = w[2 * e + 1];
+                  const float y = j < 8 ? x1 * co - x2 * si : x2 * co + x1 * si;
+                  const float dlt = y - __bfloat162float(kb[e]);
+                  acc = fmaf(dlt, dlt, acc);
+                }
+              }
+#pragma unroll
+              for (int o = 8; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+              if (j == 0 && di >= 0) reinterpret_cast<float *>(pq.out)[head * pq.ldo + di] = acc;
+            }
+          } else if (EPI == EPI_QKV) {  // one head per tile
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int v = t + 128 * q, i = v >> 4, j = v & 15;
+              const int tok = tok0 + c + i;
+              if (c + i >= pq.BT || tok >= pq.M) continue;
+              const float *row = tr + i * kTrStride;
+              float y[8];
+              bf16 *dst;
+              if (rotate) {
+                // rotate-half pairs (e, e + 64) at the token's position
+                const int e0 = 8 * (j & 7);
+                const float *w = reinterpret_cast<const float *>(rf[q]);   // (cos, sin) x 8
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const float x1 = row[e0 + e], x2 = row[64 + e0 + e];
+                  const float co = w[2 * e], si = w[2 * e + 1];
+                  y[e] = j < 8 ? x1 * co - x2 * si : x2 * co + x1 * si;
+                }
+                dst = head < pq.Hq
+                          ? reinterpret_cast<bf16 *>(pq.out) + (int64_t)tok * pq.ldo + head * 128
+                          : reinterpret_cast<bf16 *>(pq.k_cache) + s_dst[c + i] * pq.ld_kv +
+                                (head - pq.Hq) * 128;
+              } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] = row[8 * j + e];
+                dst = reinterpret_cast<bf16 *>(pq.v_cache) + s_dst[c + i] * pq.ld_kv +
+                      (head - pq.Hq - pq.Hkv) * 128;
+              }
+              store_bf16x8(dst + 8 * j, y);
+            }
+          }
+          epi_bar(grp);
+        }
+        if (helper) {
+          // every epilogue thread's partial is written before the arrival
+          __threadfence();
+          epi_all_bar();
+          if (threadIdx.x == 64) signal_add(flag);
+        } else if (MLP && ph == 0) {
+          // this CTA's 64 features of g for the token tile are written: publish
+          // them to the down projection's copies (async proxy, other SMs)
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          epi_all_bar();
+          if (threadIdx.x == 64) {
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            int *const written = pq.mlp_flag + (int64_t)ft * pq.n_tt + tt;
+            asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(written), "r"(pq.epoch)
+                         : "memory");
           }
         }
-        epi_bar(grp);
+        fence_before();
+        if (CG == 2) {
+          __syncwarp();
+          if (lane == 0) arrive_remote(map_to_rank(smem_u32(&tempty[buf]), 0));
+        } else {
+          arrive(smem_u32(&tempty[buf]));
+        }
+        if (++buf == 2) { buf = 0; bphase ^= 1; }
       }
-      if (helper) {
-        // every epilogue thread's partial is written before the arrival
-        __threadfence();
-        epi_all_bar();
-        if (threadIdx.x == 64) signal_add(flag);
-      }
-      fence_before();
-      if (CG == 2) {
-        __syncwarp();
-        if (lane == 0) arrive_remote(map_to_rank(smem_u32(&tempty[buf]), 0));
-      } else {
-        arrive(smem_u32(&tempty[buf]));
-      }
-      if (++buf == 2) { buf = 0; bphase ^= 1; }
+    };
+    drain(std::integral_constant<int, 0>());
+    if constexpr (kPhases > 1) {
+      if (!stop) drain(std::integral_constant<int, 1>());
     }
   }
   fence_before();
@@ -607,6 +787,24 @@ gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant_
     if (CG == 2) tmem_dealloc_pair(tmem, 512);
     else tmem_dealloc(tmem, 512);
   }
+}
+
+template <int EPI, int CG, bool TS>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_sab_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW,
+                const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ Params p,
+                int *status) {
+  gemm_body<EPI, CG, TS>(&mapX, &mapW, &mapW2, &mapX, &mapW, p, p, status);
+}
+
+// The fused MLP: gate/up + SwiGLU into g, then h += g W_down^T.
+template <int CG>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_mlp_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapWg,
+                const __grid_constant__ CUtensorMap mapWu, const __grid_constant__ CUtensorMap mapG,
+                const __grid_constant__ CUtensorMap mapWd, const __grid_constant__ Params p,
+                const __grid_constant__ Params p2, int *status) {
+  gemm_body<EPI_MLP, CG, true>(&mapX, &mapWg, &mapWu, &mapG, &mapWd, p, p2, status);
 }
 
 // Largest number of CTA pairs of this kernel that fit on the device at once
@@ -733,10 +931,120 @@ static cudaError_t run_cg(const CUtensorMap &mx, const CUtensorMap &mw, const CU
   return cg == 2 ? run<EPI, 2>(mx, mw, mw2, p, status, s) : run<EPI, 1>(mx, mw, mw2, p, status, s);
 }
 
+// The fused MLP: one persistent unit per SM (pair), phase 0 with the tail
+// split (split tiles first), phase 1 stream-K with deferred crossings.
+template <int CG>
+static cudaError_t run_mlp(const CUtensorMap &mx, const CUtensorMap &mwg, const CUtensorMap &mwu,
+                           const CUtensorMap &mg, const CUtensorMap &mwd, Params &p, Params &p2,
+                           int *status, cudaStream_t s) {
+  const int fixed = 2 * kTr + 256 + 1024;
+  p.stage_bytes = p2.stage_bytes = kTileW + (p.BT / CG) * BK * 2;
+  p.stages = (kSmemMax - fixed) / p.stage_bytes;
+  if (p.stages > 8) p.stages = 8;
+  if (p.stages < 2) return cudaErrorInvalidValue;
+  p2.stages = p.stages;
+  const int smem = p.stages * p.stage_bytes + fixed;
+  static PerDeviceOnce once;
+  cudaError_t e = once.run([](int) {
+    cudaError_t r = cudaFuncSetAttribute(gemm_mlp_kernel<CG>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (r == cudaSuccess && CG == 2)
+      r = cudaFuncSetAttribute(gemm_mlp_kernel<CG>,
+                               cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    return r;
+  });
+  if (e != cudaSuccess) return e;
+  // same shared memory and threads as the SwiGLU kernel: the same residency
+  const int units = CG == 2 ? max_pairs<EPI_SWIGLU>(kSmemMax) : num_sms();
+  const int n_ft = (p.n_ft + CG - 1) / CG;
+  const int64_t tiles = (int64_t)p.n_tt * n_ft;
+  p.n_whole = (int)tiles;
+  p.split = 1;
+  p.tail_first = 1;
+  const int64_t rem = tiles % units;
+  const int num_kb = (p.K + BK - 1) / BK;
+  int split = rem ? (int)(units / rem) : 1;
+  if (split > num_kb / 8) split = num_kb / 8;       // segments of at least 8 k-blocks
+  if (split > 8) split = 8;
+  if (split >= 2) {
+    p.split = split;
+    p.n_whole = (int)(tiles - rem);
+  }
+  p2.stream_k = 1;
+  p2.defer = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CG * units, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[1].id = cudaLaunchAttributeClusterDimension;
+  at[1].val.clusterDim.x = CG;
+  at[1].val.clusterDim.y = 1;
+  at[1].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = CG == 2 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, gemm_mlp_kernel<CG>, mx, mwg, mwu, mg, mwd, p, p2, status);
+}
+
 }  // namespace sab
 
 size_t gemm_split_flags_offset() { return (size_t)tcx::num_sms() * sab::kPartFloats * sizeof(float); }
-size_t gemm_split_ws_bytes() { return gemm_split_flags_offset() + sab::kSplitFlagBytes; }
+size_t gemm_mlp_flags_offset() { return gemm_split_flags_offset() + sab::kSplitFlagBytes; }
+size_t gemm_split_ws_bytes() { return gemm_mlp_flags_offset() + sab::kMlpFlags * sizeof(int); }
+
+bool gemm_mlp_fits(int M, int F, int cta_group) {
+  if (M <= 0 || F <= 0 || F % 64 || (cta_group != 1 && cta_group != 2)) return false;
+  const int n_tt = (M + 255) / 256;
+  const int bt = ((M + n_tt - 1) / n_tt + 15) / 16 * 16;
+  const int cg = bt < 32 ? 1 : cta_group;
+  return (int64_t)((F / 64 + cg - 1) / cg * cg) * n_tt <= sab::kMlpFlags;
+}
+
+cudaError_t launch_gemm_mlp(const void *x, int64_t ldx, const void *w_gate, const void *w_up,
+                            int64_t ldw, const void *w_down, int64_t ldwd, int M, int F, int d,
+                            void *g, int64_t ldg, float *h, int64_t ldh, int *status,
+                            cudaStream_t s, int cta_group, void *split_ws, int epoch) {
+  using namespace sab;
+  if (M == 0) return cudaSuccess;
+  if (!split_ws || epoch <= 0 || !gemm_mlp_fits(M, F, cta_group)) return cudaErrorNotSupported;
+  Params p{};
+  p.M = M;
+  p.n_tt = (M + 255) / 256;
+  p.BT = ((M + p.n_tt - 1) / p.n_tt + 15) / 16 * 16;
+  if (p.BT < 32) cta_group = 1;                           // keep each CTA's half >= 16 rows
+  const int cg = cta_group;
+  p.idesc = idesc_bf16(FM * cg, p.BT);
+  Params p2 = p;
+  // phase 0: gate/up, 64 SwiGLU features per CTA tile
+  p.N = F;
+  p.K = d;
+  p.n_ft = F / 64;
+  p.out = g;
+  p.ldo = ldg;
+  p.part = reinterpret_cast<float *>(split_ws);
+  p.flag = reinterpret_cast<int *>(reinterpret_cast<char *>(split_ws) + gemm_split_flags_offset());
+  // phase 1: down + residual; its k-block kb is phase 0's CTA tile kb
+  p2.N = d;
+  p2.K = F;
+  p2.n_ft = (d + FM - 1) / FM;
+  p2.out = h;
+  p2.ldo = ldh;
+  p.mlp_flag = p2.mlp_flag =
+      reinterpret_cast<int *>(reinterpret_cast<char *>(split_ws) + gemm_mlp_flags_offset());
+  p.epoch = p2.epoch = epoch;
+  CUtensorMap mx, mwg, mwu, mg, mwd;
+  if (!make_map(&mx, x, M, d, ldx, p.BT / cg) || !make_map(&mwg, w_gate, F, d, ldw, 64) ||
+      !make_map(&mwu, w_up, F, d, ldw, 64) || !make_map(&mg, g, M, F, ldg, p.BT / cg) ||
+      !make_map(&mwd, w_down, d, F, ldwd, FM))
+    return cudaErrorInvalidValue;
+  const cudaError_t e = cg == 2 ? run_mlp<2>(mx, mwg, mwu, mg, mwd, p, p2, status, s)
+                                : run_mlp<1>(mx, mwg, mwu, mg, mwd, p, p2, status, s);
+  if (e != cudaSuccess) return e;
+  return launched(1);
+}
 
 // Automatic form, measured at the Llama-3-8B projection shapes for 512 to
 // 4096 token rows: the CTA-pair swapped form is fastest for the SwiGLU,

@@ -102,6 +102,7 @@ def test_host_validation_without_device():
     assert lib.cb_debug_gemm_path(L.CB_GEMM_AUTO) == L.CB_OK
     assert lib.cb_debug_probe_start(0, 4) == L.CB_ERR_INVALID_ARG
     assert lib.cb_debug_probe_start(L.CB_PROBE_SWIGLU, 0) == L.CB_ERR_INVALID_ARG
+    assert lib.cb_debug_probe_start(L.CB_PROBE_MLP + 1, 4) == L.CB_ERR_INVALID_ARG
     assert lib.cb_debug_probe_stop(None, None) == L.CB_ERR_INVALID_ARG
     # anchors: NULL model / chunks / output, bad rule or ratio
     assert lib.cb_anchor_select(None, None, 1, 0, 1000, None, None, None, 0, None) == \
@@ -177,3 +178,10 @@ def test_debug_index_checks_switch_is_validated():
     assert L.lib.cb_debug_index_checks(2) == L.CB_ERR_INVALID_ARG
     L.check(L.lib.cb_debug_index_checks(1))
     L.check(L.lib.cb_debug_index_checks(0))
+
+
+def test_debug_mlp_fusion_switch_is_validated():
+    assert L.lib.cb_debug_mlp_fusion(2) == L.CB_ERR_INVALID_ARG
+    assert L.lib.cb_debug_mlp_fusion(-1) == L.CB_ERR_INVALID_ARG
+    L.check(L.lib.cb_debug_mlp_fusion(0))
+    L.check(L.lib.cb_debug_mlp_fusion(1))

@@ -1,6 +1,7 @@
 """Kernel-level parity of the CUDA path (through the C ABI) against the CPU
 oracle, brute force and exact definitions, on seeded inputs.  Sizes span
 several tiles with ragged tails, plus the full sizes of the workloads."""
+import ctypes as C
 import math
 
 import numpy as np
@@ -464,6 +465,58 @@ def test_gemm_tail_split(M, gemm_path, llama_proj):
     model.cb_linear(Ad, dw["w_gate"], g1, L.CB_EPI_SWIGLU, W2=dw["w_up"])
     torch.cuda.synchronize()
     assert rms_rel(host(outs[0][1]), host(g1)) < 2e-3
+
+
+@pytest.fixture
+def mlp_fusion():
+    yield
+    L.check(L.lib.cb_debug_mlp_fusion(1))
+
+
+@pytest.mark.parametrize("gemm_path", [L.CB_GEMM_AUTO, L.CB_GEMM_SWAP_AB], indirect=True)
+@pytest.mark.parametrize("M", [524, 64, 300, 3136, 9])
+def test_fused_mlp_layer_matches_two_launches(M, gemm_path, llama_proj, mlp_fusion):
+    """One bf16 decoder layer (cb_blend_layer, M rows attending causally over
+    themselves) with the MLP as one launch (gate/up + SwiGLU, then the down
+    projection waiting per k-block on the gate/up tiles' flags) and as two.
+    The K/V the layer scatters precede the MLP and match bit for bit; the
+    layer's update of h matches up to fp32 summation order (split gate/up
+    tiles; the residual adds' order, which can move a bf16 rounding of the
+    normalised rows: about 2e-4 between repeats at 64 rows); the launch probe
+    sees one fused launch.  The workspace is filled with 0xFF bytes before
+    every call (NaN in the gate/up output, -1 in every flag), so a down
+    k-block read before its gate/up tile wrote it, or a flag not reset by
+    the call, shows as a non-finite h.  9 rows: the single-CTA form."""
+    w, model = llama_proj
+    rng = np.random.default_rng(300 + M)
+    h0 = dev(rng.standard_normal((M, 4096)).astype(np.float32))
+    pos = torch.arange(M, dtype=torch.int32, device="cuda")
+    reqs = [(0, M, 0, M)]
+    ws = torch.empty(max(L.lib.cb_layer_workspace_size(model.handle, M), 256), dtype=torch.uint8,
+                     device="cuda")
+    res = {}
+    for fused in (1, 0, 1):
+        L.check(L.lib.cb_debug_mlp_fusion(fused))
+        h = h0.clone()
+        kc = torch.zeros(M, 1024, dtype=torch.bfloat16, device="cuda")
+        vc = torch.zeros_like(kc)
+        ws.fill_(0xFF)
+        L.check(L.lib.cb_debug_probe_start(L.CB_PROBE_MLP, 4))
+        model.cb_blend_layer(0, h, pos, pos, reqs, kc, vc, ws=ws)
+        n = C.c_int()
+        ms = C.c_float()
+        L.check(L.lib.cb_debug_probe_stop(C.byref(n), C.byref(ms)))
+        assert n.value == fused
+        res.setdefault(fused, []).append((h, kc, vc))
+    torch.cuda.synchronize()
+    assert R.device_status() == 0
+    (hf, kf, vf), (hf2, _, _) = res[1]
+    hu, ku, vu = res[0][0]
+    assert torch.equal(kf, ku) and torch.equal(vf, vu)
+    d_f, d_u, d_f2 = host(hf) - host(h0), host(hu) - host(h0), host(hf2) - host(h0)
+    assert np.isfinite(d_f).all() and np.isfinite(d_f2).all() and np.isfinite(d_u).all()
+    assert rms_rel(d_f, d_u) < 2e-3
+    assert rms_rel(d_f2, d_f) < 2e-3
 
 
 def test_linear_workspace_is_validated(llama_proj):
