@@ -52,6 +52,10 @@ def parse_args():
                          "(for ncu --profile-from-start off); prints no JSON")
     ap.add_argument("--layers", type=int, default=None,
                     help="truncate the stack (profiling captures on a small footprint)")
+    ap.add_argument("--two-launch-mlp", action="store_true",
+                    help="run each layer's MLP as two launches (gate/up + SwiGLU, then "
+                         "down + residual) instead of the default single launch "
+                         "(cb_debug_mlp_fusion(0)); the same function")
     ap.add_argument("--workload", choices=["rag", "rolling", "qwen", "long", "host_kv", "qcf"],
                     default="rag",
                     help="rag: the headline request (default); rolling: the 50-request "
@@ -190,8 +194,8 @@ def setup_replica(rank, device, n_layers=None):
 # layer: gate/up + SwiGLU, then down + residual, on CTA pairs), valid only
 # for the kernel source it was taken on.
 TRAFFIC_CAPTURE = {"source": "rag_kv_cache_layer_gb300/csrc/k_gemm_sab.cu",
-                   "sha256": None,
-                   "bytes_per_launch": None,
+                   "sha256": "ef294dc58a3634c8491e09d5da67dfef872bc81bbd886983941abfcc4f533a90",
+                   "bytes_per_launch": 382264832 + 27298816,
                    "profile": "profiles/gemm_mlp_M524_llama8b.md"}
 
 
@@ -225,15 +229,37 @@ def blend_work(shape, T_list, pos_compact, sel_layer=1, probe=None):
     qw, kvw = shape.n_q_heads * hd, shape.n_kv_heads * hd
     T = sum(T_list)
     pos = np.asarray(pos_compact, dtype=np.float64)
-    rows = sel_layer * T + (n_layers - sel_layer) * len(pos)
+    # (rows, layers) of the layers that run the whole decoder layer
+    groups = [(T, sel_layer), (len(pos), n_layers - sel_layer)]
     keys = sel_layer * sum(t * (t + 1) / 2 for t in T_list) + (n_layers - sel_layer) * float((pos + 1).sum())
+    q_only_rows = 0
     if probe is not None:
+        # the last probe layer runs only its W_q projection
         p_layers, p_rows, p_keys = probe
-        rows += p_layers * p_rows
-        keys += p_layers * p_keys
-    return {"qkv": rows * 2.0 * d * (qw + 2 * kvw), "attention": 4.0 * hd * shape.n_q_heads * keys,
-            "o_proj": rows * 2.0 * qw * d, "swiglu": rows * 2.0 * d * 2 * F,
-            "down_proj": rows * 2.0 * F * d}
+        groups.append((p_rows, p_layers - 1))
+        q_only_rows = p_rows
+        keys += (p_layers - 1) * p_keys
+    rows = sum(r * n for r, n in groups)
+    mlp_rows = sum(r * n for r, n in groups if mlp_fuses(r, F))
+    two_rows = rows - mlp_rows
+    return {"qkv": rows * 2.0 * d * (qw + 2 * kvw) + q_only_rows * 2.0 * d * qw,
+            "attention": 4.0 * hd * shape.n_q_heads * keys,
+            "o_proj": rows * 2.0 * qw * d, "swiglu": two_rows * 2.0 * d * 2 * F,
+            "down_proj": two_rows * 2.0 * F * d, "mlp": mlp_rows * 2.0 * d * 3 * F}
+
+
+def mlp_fuses(M, F):
+    """Whether the library runs the MLP of a layer over M rows as one launch
+    (its rule for the bf16 path at these shapes): both projections take the
+    CTA-pair swapped GEMM (the down projection's reduction F is longer than
+    4096) and the flags, one per 64 gate/up features and 256-row token tile,
+    fit in 16384."""
+    if M <= 0 or F % 64 or F <= 4096:
+        return False
+    n_tt = -(-M // 256)
+    bt = (-(-M // n_tt) + 15) // 16 * 16
+    cg = 2 if bt >= 32 else 1
+    return -(-(F // 64) // cg) * cg * n_tt <= 16384
 
 
 def kernel_table(L, run_step, shape, peaks, work, stitch_layers, n_ctx, n_rows, n_req, reps=3,
@@ -261,7 +287,7 @@ def kernel_table(L, run_step, shape, peaks, work, stitch_layers, n_ctx, n_rows, 
         ("swiglu", L.CB_PROBE_SWIGLU, "tensor", work["swiglu"]),
         ("down_proj", L.CB_PROBE_DOWN, "tensor", work["down_proj"]),
         # gate/up + SwiGLU and down + residual as one launch (the bf16 default)
-        ("mlp", L.CB_PROBE_MLP, "tensor", work["swiglu"] + work["down_proj"]),
+        ("mlp", L.CB_PROBE_MLP, "tensor", work["mlp"]),
         ("stitch", L.CB_PROBE_STITCH, "hbm", stitch_layers * n_ctx * kvw * 2.0 * 4),
         # the fused path's select class sums the key projection's per-head
         # partials and ranks them (the keys themselves are read there)
@@ -566,8 +592,10 @@ def run_ours(args):
         peaks, src = load_peaks()
         s_ = wl.model
         rows = layer_rows(plan, n_layers)
-        # algorithmic FLOPs per row: gate/up 2 d (2F), down 2 F d
-        kflops = args.steps * sum(rows) * 2.0 * s_.d_model * (3 if dom_fused else 2) * s_.d_ffn
+        # algorithmic FLOPs per row: gate/up 2 d (2F), down 2 F d; the rows of
+        # the layers that run the timed kernel
+        dom_rows = sum(r for r in rows if mlp_fuses(r, s_.d_ffn) == dom_fused)
+        kflops = args.steps * dom_rows * 2.0 * s_.d_model * (3 if dom_fused else 2) * s_.d_ffn
         kms = ms_dom / max(n_dom, 1)
         achieved = kflops / (ms_dom / 1e3) / 1e12
         # each launch is bracketed by its own events inside a loop well
@@ -1072,6 +1100,9 @@ def run_qcf(args):
 
 def main():
     args = parse_args()
+    if args.two_launch_mlp and args.impl == "ours":
+        from rag_kv_cache_layer_gb300 import _lib as L
+        L.check(L.lib.cb_debug_mlp_fusion(0))
     if args.impl == "reference":
         run_reference(args)
     elif args.workload == "rolling":
