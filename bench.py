@@ -240,7 +240,7 @@ def blend_work(shape, T_list, pos_compact, sel_layer=1, probe=None):
         q_only_rows = p_rows
         keys += (p_layers - 1) * p_keys
     rows = sum(r * n for r, n in groups)
-    mlp_rows = sum(r * n for r, n in groups if mlp_fuses(r, F))
+    mlp_rows = sum(r * n for r, n in groups if n > 0 and mlp_fuses(r, shape))
     two_rows = rows - mlp_rows
     return {"qkv": rows * 2.0 * d * (qw + 2 * kvw) + q_only_rows * 2.0 * d * qw,
             "attention": 4.0 * hd * shape.n_q_heads * keys,
@@ -248,18 +248,11 @@ def blend_work(shape, T_list, pos_compact, sel_layer=1, probe=None):
             "down_proj": two_rows * 2.0 * F * d, "mlp": mlp_rows * 2.0 * d * 3 * F}
 
 
-def mlp_fuses(M, F):
-    """Whether the library runs the MLP of a layer over M rows as one launch
-    (its rule for the bf16 path at these shapes): both projections take the
-    CTA-pair swapped GEMM (the down projection's reduction F is longer than
-    4096) and the flags, one per 64 gate/up features and 256-row token tile,
-    fit in 16384."""
-    if M <= 0 or F % 64 or F <= 4096:
-        return False
-    n_tt = -(-M // 256)
-    bt = (-(-M // n_tt) + 15) // 16 * 16
-    cg = 2 if bt >= 32 else 1
-    return -(-(F // 64) // cg) * cg * n_tt <= 16384
+def mlp_fuses(M, shape):
+    """Whether the library runs the MLP of a layer over M rows as one launch,
+    under its current switches (its own rule, cb_debug_mlp_one_launch)."""
+    from rag_kv_cache_layer_gb300 import _lib as L
+    return bool(L.lib.cb_debug_mlp_one_launch(int(M), shape.d_model, shape.d_ffn))
 
 
 def kernel_table(L, run_step, shape, peaks, work, stitch_layers, n_ctx, n_rows, n_req, reps=3,
@@ -594,7 +587,7 @@ def run_ours(args):
         rows = layer_rows(plan, n_layers)
         # algorithmic FLOPs per row: gate/up 2 d (2F), down 2 F d; the rows of
         # the layers that run the timed kernel
-        dom_rows = sum(r for r in rows if mlp_fuses(r, s_.d_ffn) == dom_fused)
+        dom_rows = sum(r for r in rows if mlp_fuses(r, s_) == dom_fused)
         kflops = args.steps * dom_rows * 2.0 * s_.d_model * (3 if dom_fused else 2) * s_.d_ffn
         kms = ms_dom / max(n_dom, 1)
         achieved = kflops / (ms_dom / 1e3) / 1e12

@@ -161,10 +161,17 @@ cb_status cb_debug_gemm_path(int path);
  * finish.  Both forms compute the same function; they differ in the order of
  * fp32 additions (partial sums of split tiles, residual accumulation).  The
  * one-launch form applies where both projections take the same swapped
- * GEMM form (cb_debug_gemm_path) and the flags fit (rows <= 16384 / (d_ffn
- * / 64) * 256); otherwise the two launches run.  Returns CB_ERR_INVALID_ARG
+ * GEMM form (cb_debug_gemm_path) and the flags fit (ceil(rows / 256) * d_ffn /
+ * 64 <= 16384); otherwise the two launches run.  Returns CB_ERR_INVALID_ARG
  * for on not 0 or 1. */
 cb_status cb_debug_mlp_fusion(int on);
+
+/* 1 if a bf16 decoder layer over n_rows rows with these widths runs its MLP
+ * as one launch under the current switches (cb_debug_mlp_fusion,
+ * cb_debug_gemm_path), else 0 (two launches, or nonpositive arguments).
+ * Host arithmetic only; benchmarks use it to attribute each layer's work to
+ * the launch that does it. */
+int cb_debug_mlp_one_launch(int n_rows, int d_model, int d_ffn);
 
 /* Debug index checks (process-wide, off by default).  While on, every call
  * also validates the device-side index arrays it consumes before using them:

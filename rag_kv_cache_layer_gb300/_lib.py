@@ -132,6 +132,7 @@ def _load():
         "cb_debug_gemm_path": (S, [i32]),
         "cb_debug_index_checks": (S, [i32]),
         "cb_debug_mlp_fusion": (S, [i32]),
+        "cb_debug_mlp_one_launch": (i32, [i32, i32, i32]),
         "cb_debug_probe_start": (S, [i32, i32]),
         "cb_debug_probe_stop": (S, [C.POINTER(i32), C.POINTER(C.c_float)]),
         "cb_rope_table_elems": (C.c_size_t, [i32, i32]),
@@ -195,7 +196,7 @@ lib = _load()
 EXPORTED = [
     "cb_last_error_message", "cb_version", "cb_get_device_status",
     "cb_debug_expire_wait", "cb_debug_launch_count", "cb_debug_gemm_path",
-    "cb_debug_index_checks", "cb_debug_mlp_fusion",
+    "cb_debug_index_checks", "cb_debug_mlp_fusion", "cb_debug_mlp_one_launch",
     "cb_debug_probe_start", "cb_debug_probe_stop",
     "cb_rope_table_elems",
     "cb_rope_table_init",

@@ -1038,6 +1038,25 @@ extern "C" cb_status cb_full_plan(const cb_model *m, const cb_request *reqs, int
 }
 
 // ------------------------------------------------------------------ layer --
+// The swapped GEMM form (1 or 2 CTAs per MMA) in which a bf16 layer over n
+// rows runs its MLP as one launch, or 0 when it runs the two projections:
+// the one-launch form is switched on, both projections take the same swapped
+// form, and the flags fit.
+static int mlp_one_launch_form(int n, int d, int F) {
+  if (!g_mlp_fusion.load(std::memory_order_relaxed) || n <= 0 || d <= 0 || F <= 0) return 0;
+  const int path = g_gemm_path.load(std::memory_order_relaxed);
+  const int form = path == CB_GEMM_AUTO        ? gemm_auto_form(n, d, EPI_SWIGLU)
+                   : path == CB_GEMM_SWAP_AB      ? 1
+                   : path == CB_GEMM_SWAP_AB_PAIR ? 2
+                                                  : 0;
+  const int form_down = path == CB_GEMM_AUTO ? gemm_auto_form(n, F, EPI_RESID) : form;
+  return form && form == form_down && gemm_mlp_fits(n, F, form) ? form : 0;
+}
+
+extern "C" int cb_debug_mlp_one_launch(int n_rows, int d_model, int d_ffn) {
+  return mlp_one_launch_form(n_rows, d_model, d_ffn) != 0;
+}
+
 static inline char *layer_ptr(void *base, int l, int64_t stride, size_t eb) {
   return (char *)base + (int64_t)l * stride * (int64_t)eb;
 }
@@ -1083,15 +1102,10 @@ static cb_status layer_forward(cb_model *m, int l, float *h, int n, const int32_
   CB_TRY(run_linear(m, S.o, m->qw, L.w_o, nullptr, m->qw, n, d, m->qw, EPI_RESID, h, d, s));
   probe_mark(CB_PROBE_O, false, s);
   CB_CUDA(launch_rmsnorm(h, d, nullptr, n, d, L.norm2, c.norm_eps, S.x, d, dt, s));
-  if (dt == CB_BF16 && S.split && S.mlp_epoch && g_mlp_fusion.load(std::memory_order_relaxed)) {
-    // gate/up and down in one launch (the swapped pair form both take)
-    const int path = g_gemm_path.load(std::memory_order_relaxed);
-    const int form = path == CB_GEMM_AUTO        ? gemm_auto_form(n, d, EPI_SWIGLU)
-                     : path == CB_GEMM_SWAP_AB      ? 1
-                     : path == CB_GEMM_SWAP_AB_PAIR ? 2
-                                                    : 0;
-    const int form_down = path == CB_GEMM_AUTO ? gemm_auto_form(n, F, EPI_RESID) : form;
-    if (form && form == form_down && gemm_mlp_fits(n, F, form)) {
+  if (dt == CB_BF16 && S.split && S.mlp_epoch) {
+    // gate/up and down in one launch (the swapped form both take)
+    const int form = mlp_one_launch_form(n, d, F);
+    if (form) {
       probe_mark(CB_PROBE_MLP, true, s);
       const cudaError_t e = launch_gemm_mlp(S.x, d, L.w_gate, L.w_up, d, L.w_down, F, n, F, d,
                                             S.g, F, h, d, st, s, form, S.split,

@@ -121,3 +121,31 @@ def test_the_extensions_reorder_the_work(M):
         assert max(split_ft) < min(ft for u in range(units)
                                    for _, ft, _, _, seg in work_items(p0, 64, u, units, cg, True)
                                    if seg < 0) + 1
+
+
+def test_the_library_rule_for_one_launch():
+    """cb_debug_mlp_one_launch: one launch where both projections take the
+    same swapped form and the flags fit, as the replay above assumes; the
+    switches turn it off."""
+    from rag_kv_cache_layer_gb300 import _lib as L
+    one = lambda M, d=4096, F=14336: L.lib.cb_debug_mlp_one_launch(M, d, F)
+    L.check(L.lib.cb_debug_mlp_fusion(1))
+    L.check(L.lib.cb_debug_gemm_path(L.CB_GEMM_AUTO))
+    for M in (1, 9, 64, 524, 3136, 8192, 18688):
+        p0, _, cg, _ = launch_params(M, 14336, 4096, pairs=76)
+        assert one(M) == 1, M
+        assert (p0["n_ft"] + cg - 1) // cg * cg * p0["n_tt"] <= 16384
+    assert one(18689) == 0 and one(66048) == 0       # the flags no longer fit
+    assert one(12800, F=12288) == 1 and one(41472, F=12288) == 0
+    assert one(0) == 0 and one(-5) == 0
+    try:
+        L.check(L.lib.cb_debug_mlp_fusion(0))
+        assert one(524) == 0
+        L.check(L.lib.cb_debug_mlp_fusion(1))
+        L.check(L.lib.cb_debug_gemm_path(L.CB_GEMM_TOKEN_M))
+        assert one(524) == 0                         # token rows on M: two launches
+        L.check(L.lib.cb_debug_gemm_path(L.CB_GEMM_SWAP_AB))
+        assert one(524) == 1
+    finally:
+        L.check(L.lib.cb_debug_mlp_fusion(1))
+        L.check(L.lib.cb_debug_gemm_path(L.CB_GEMM_AUTO))
